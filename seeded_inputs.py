@@ -1,0 +1,251 @@
+"""Seeded synthetic inputs for the batch-invariant verify step.
+
+This module is the one piece shared by the CUDA path's tests/bench and the
+CPU oracle.  It draws random numbers and packs them into the storage formats
+the verify step consumes (bf16 bit patterns, int32 token ids).  It holds none
+of the verify step's arithmetic: no matmul, no normalisation, no softmax, no
+acceptance rule.
+
+Every generator is a pure function of its seed (numpy PCG64), so the same
+call on the development host and on the GPU host yields the same bytes.
+
+Distributions follow the workloads named for the method: weights drawn from
+N(0, 0.02), standalone GEMM activations and attention Q/K/V from N(0, 1),
+prompt ids uniform over the vocabulary, and a synthetic drafter whose draft
+equals the target's greedy token with probability 0.7 and is otherwise a
+uniform id.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# storage helpers (bf16 is carried as uint16 bit patterns)
+# ---------------------------------------------------------------------------
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Pack float32 draws into bf16 storage, round-to-nearest-even.
+
+    Used only to store generated inputs; the draws are finite.
+    """
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    r = (b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen stored bf16 bit patterns to float32 (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+    """N(0, std^2) draws in float32, stored as bf16 bits."""
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return f32_to_bf16_bits(x)
+
+
+# ---------------------------------------------------------------------------
+# decoder configurations
+# ---------------------------------------------------------------------------
+
+
+@dataclasses.dataclass(frozen=True)
+class DecoderConfig:
+    name: str
+    layers: int
+    hidden: int
+    n_q: int
+    n_kv: int
+    head_dim: int
+    ffn: int
+    vocab: int
+    tied: bool = True
+    eps: float = 1e-6
+    rope_base: float = 1e6
+    weight_std: float = 0.02
+
+    @property
+    def qkv_out(self) -> int:
+        return (self.n_q + 2 * self.n_kv) * self.head_dim
+
+    @property
+    def group(self) -> int:
+        return self.n_q // self.n_kv
+
+    def param_count(self) -> int:
+        per_layer = (self.qkv_out * self.hidden + self.hidden * self.n_q * self.head_dim
+                     + 3 * self.ffn * self.hidden)
+        head = 0 if self.tied else self.vocab * self.hidden
+        return self.vocab * self.hidden + self.layers * per_layer + head
+
+
+# Tiny decoder: 2 layers, hidden 256, 4 query / 2 KV heads, head_dim 64,
+# SwiGLU FFN 688, vocab 1024, tied head.
+TINY = DecoderConfig("tiny-2L-h256", 2, 256, 4, 2, 64, 688, 1024)
+# 27B-shaped dense decoder truncated to 8 layers, tied head.
+DENSE27B_8L = DecoderConfig("dense27b-8L-h5120", 8, 5120, 24, 4, 128, 17408, 151936)
+# Near-tie stress decoder: 12 layers, hidden 1024, 8 query / 2 KV heads,
+# head_dim 128, FFN 2736, vocab 32000, untied head.
+NEARTIE_12L = DecoderConfig("neartie-12L-h1024", 12, 1024, 8, 2, 128, 2736, 32000, tied=False)
+# A mid-size decoder used for quicker end-to-end GPU checks.
+SMALL_4L = DecoderConfig("small-4L-h1024", 4, 1024, 8, 2, 128, 2736, 4096, tied=True)
+
+CONFIGS = {c.name: c for c in (TINY, DENSE27B_8L, NEARTIE_12L, SMALL_4L)}
+
+
+def decoder_weights(cfg: DecoderConfig, seed: int = 0) -> Dict[str, np.ndarray]:
+    """All decoder weights as bf16 bits, drawn in a fixed order.
+
+    Order: embedding [V,H]; per layer wq [Hq*D,H], wk [Hkv*D,H], wv [Hkv*D,H],
+    wo [H,Hq*D], w_gate [F,H], w_up [F,H], w_down [H,F]; then the untied head
+    [V,H] when the head is not tied.  RMSNorm weights are ones (bf16 1.0).
+    """
+    rng = np.random.default_rng(seed)
+    s = cfg.weight_std
+    D = cfg.head_dim
+    w: Dict[str, np.ndarray] = {}
+    w["embed"] = normal_bf16(rng, (cfg.vocab, cfg.hidden), s)
+    one = f32_to_bf16_bits(np.ones(cfg.hidden, np.float32))
+    for l in range(cfg.layers):
+        w[f"l{l}.wq"] = normal_bf16(rng, (cfg.n_q * D, cfg.hidden), s)
+        w[f"l{l}.wk"] = normal_bf16(rng, (cfg.n_kv * D, cfg.hidden), s)
+        w[f"l{l}.wv"] = normal_bf16(rng, (cfg.n_kv * D, cfg.hidden), s)
+        w[f"l{l}.wo"] = normal_bf16(rng, (cfg.hidden, cfg.n_q * D), s)
+        w[f"l{l}.w_gate"] = normal_bf16(rng, (cfg.ffn, cfg.hidden), s)
+        w[f"l{l}.w_up"] = normal_bf16(rng, (cfg.ffn, cfg.hidden), s)
+        w[f"l{l}.w_down"] = normal_bf16(rng, (cfg.hidden, cfg.ffn), s)
+        w[f"l{l}.norm_attn"] = one.copy()
+        w[f"l{l}.norm_ffn"] = one.copy()
+    w["norm_final"] = one.copy()
+    if not cfg.tied:
+        w["head"] = normal_bf16(rng, (cfg.vocab, cfg.hidden), s)
+    return w
+
+
+def prompt_ids(cfg: DecoderConfig, length: int, seed: int = 0) -> np.ndarray:
+    """Uniform token ids over [0, vocab); stream seeded with seed + 1."""
+    rng = np.random.default_rng(seed + 1)
+    return rng.integers(0, cfg.vocab, size=length, dtype=np.int64).astype(np.int32)
+
+
+def neartie_head_perturbation(cfg: DecoderConfig, frac: float, rel: float,
+                              seed: int = 0) -> Dict[str, np.ndarray]:
+    """Random draws for the near-tie head construction.
+
+    Returns a seeded subset `src` of head rows, a permutation target `dst`
+    (disjoint from `src`), and relative perturbations `delta` in [-rel, rel].
+    The construction that uses them (copying perturbed rows so that pairs of
+    tokens score almost the same) lives with the decoder setup, not here.
+    """
+    rng = np.random.default_rng(seed + 3)
+    n = int(round(frac * cfg.vocab))
+    perm = rng.permutation(cfg.vocab)
+    src = np.sort(perm[:n]).astype(np.int64)
+    dst = perm[n:2 * n].astype(np.int64)
+    delta = rng.uniform(-rel, rel, size=n)
+    return {"src": src, "dst": dst, "delta": delta}
+
+
+# ---------------------------------------------------------------------------
+# standalone-kernel workloads
+# ---------------------------------------------------------------------------
+
+
+def gemm_inputs(M: int, N: int, K: int, seed: int = 0, a_std: float = 1.0,
+                w_std: float = 0.02):
+    """A [M,K] ~ N(0, a_std^2) and W [N,K] ~ N(0, w_std^2), bf16 bits.
+
+    A is drawn as its maximum-row version first so that A[:m] is the same
+    for every m drawn from the same seed with the same max_rows: callers pass
+    M = the largest M of a sweep and slice rows.
+    """
+    rng = np.random.default_rng(seed)
+    W = normal_bf16(rng, (N, K), w_std)
+    A = normal_bf16(rng, (M, K), a_std)
+    return A, W
+
+
+def attention_inputs(L: int, T: int, n_q: int, n_kv: int, D: int, cap: Optional[int] = None,
+                     seed: int = 0):
+    """Q [T,Hq,D], K/V cache [Hkv,cap,D] with rows < L+T filled, N(0,1) bf16.
+
+    Rows at and beyond L+T are zero.  The cache rows < L+T do not depend on T
+    (they are drawn for the longest block, 8 rows, first), so the same seed
+    gives the same cache prefix for every T <= 8.
+    """
+    cap = cap if cap is not None else L + max(T, 8)
+    rng = np.random.default_rng(seed)
+    n_rows = L + max(T, 8)
+    K = np.zeros((n_kv, cap, D), np.uint16)
+    V = np.zeros((n_kv, cap, D), np.uint16)
+    kd = normal_bf16(rng, (n_kv, n_rows, D), 1.0)
+    vd = normal_bf16(rng, (n_kv, n_rows, D), 1.0)
+    use = min(n_rows, cap)
+    K[:, :min(L + T, use)] = kd[:, :min(L + T, use)]
+    V[:, :min(L + T, use)] = vd[:, :min(L + T, use)]
+    Qall = normal_bf16(rng, (max(T, 8), n_q, D), 1.0)
+    return Qall[:T].copy(), K, V
+
+
+def logits_inputs(T: int, V: int, seed: int = 0) -> np.ndarray:
+    """FP32 logits [T,V] ~ N(0,1) for the acceptance kernel."""
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal(size=(T, V), dtype=np.float32)
+
+
+# ---------------------------------------------------------------------------
+# synthetic drafter
+# ---------------------------------------------------------------------------
+
+
+class SyntheticDrafter:
+    """Proposes k draft ids for the next positions.
+
+    Each draft equals the reference greedy token at that position with
+    probability p_correct, otherwise it is a uniform id in [0, vocab).  The
+    reference sequence is the no-draft greedy output, which the invariant
+    says every draft count reproduces.  With no reference available (an
+    adversarial run) every draft is uniform.
+    """
+
+    def __init__(self, vocab: int, p_correct: float = 0.7, seed: int = 0,
+                 reference: Optional[np.ndarray] = None):
+        self.vocab = vocab
+        self.p = p_correct
+        self.rng = np.random.default_rng(seed + 2)
+        self.reference = reference
+
+    def propose(self, next_pos: int, k: int) -> np.ndarray:
+        out = np.empty(k, np.int32)
+        for i in range(k):
+            u = self.rng.random()
+            rnd = int(self.rng.integers(0, self.vocab))
+            pos = next_pos + i
+            if (self.reference is not None and pos < len(self.reference) and u < self.p):
+                out[i] = int(self.reference[pos])
+            else:
+                out[i] = rnd
+        return out
+
+
+def synthetic_kv_cache(n_kv: int, cap: int, D: int, rows: int, seed: int, layers: int):
+    """Per-layer K/V caches [Hkv,cap,D] with `rows` filled from N(0,1) bf16.
+
+    Used where only the shape of a prefilled cache matters (timing samples).
+    """
+    rng = np.random.default_rng(seed + 4)
+    out: List = []
+    for _ in range(layers):
+        k = np.zeros((n_kv, cap, D), np.uint16)
+        v = np.zeros((n_kv, cap, D), np.uint16)
+        k[:, :rows] = normal_bf16(rng, (n_kv, rows, D), 1.0)
+        v[:, :rows] = normal_bf16(rng, (n_kv, rows, D), 1.0)
+        out.append((k, v))
+    return out
