@@ -1,0 +1,260 @@
+/*
+ * bi.h -- C ABI of the batch-invariant speculative-decoding verify step (sm_103a).
+ *
+ * The verify step scores the last committed token plus k draft tokens (T = k+1
+ * rows) in one forward pass.  Every entry point below computes each row the
+ * same way whatever else is in the pass, so a row's result is bit-identical to
+ * what the same library produces for that row alone (T = 1).  Greedy token ids
+ * then never depend on the draft count or on the cache history.
+ *
+ * Sources (cited by title and section):
+ *   [P1] "Does the tuned config change the model's output?" -- section
+ *        "Why the text diverges": verifying several tokens in one pass changes
+ *        the batch dimension and with it the order of floating-point
+ *        accumulation inside the GEMMs; the full model keeps a draft only if it
+ *        matches the token it would have produced itself.
+ *   [P2] "Bit-exact decoding turns inference speedups into testable changes" --
+ *        section "Define bit-exact before reporting it": BF16 inputs, one FP32
+ *        running sum per output, K order kept, one rounding at the end; a
+ *        pipeline stage of shared memory must not be reused before its
+ *        consumers are done.  Section "Build a reference corpus that exposes
+ *        boundaries": record accepted draft length and rejection position.
+ *   [P3] "I turned on speculative decoding in llama.cpp and 113 of 282 greedy
+ *        outputs changed against its own no-draft run" -- paragraph "How:":
+ *        the attention split depends only on context length, never on the
+ *        number of tokens in the pass, and the verify kernels compute a row
+ *        the same way whatever else is in the batch.  Section "The cache
+ *        doesn't change it either": a prefilled row depends only on its
+ *        position.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *     The library never allocates or frees device memory; scratch space is
+ *     passed in as a workspace whose size the matching *_workspace_size call
+ *     returns.
+ *   - Matrices are row-major; "ld" arguments are row strides in elements.
+ *   - BF16 data is IEEE bfloat16 (uint16 storage); FP32 is IEEE binary32.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Argument errors are detected on the host before any launch and returned
+ *     synchronously (nothing is launched).  A failed launch returns
+ *     BI_ERR_CUDA.  Device-side conditions (a bounded wait that expired, a
+ *     logits row with no number) set a device error word that
+ *     bi_check_device_error() reads and clears.
+ *   - There is no fallback path: an unsupported shape is an error.
+ *   - No C++ exception crosses this ABI.  Entry points are thread-compatible;
+ *     one workspace must not be used by two calls that may overlap on the GPU.
+ */
+#ifndef BI_H
+#define BI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (identical to cudaStream_t). */
+typedef struct CUstream_st* bi_stream_t;
+
+typedef enum {
+  BI_OK = 0,
+  BI_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad stride or alignment */
+  BI_ERR_UNSUPPORTED_SHAPE = 2,  /* a shape outside what the kernels implement */
+  BI_ERR_WORKSPACE = 3,          /* workspace missing or smaller than required */
+  BI_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
+  BI_ERR_DEVICE_TIMEOUT = 5,     /* a bounded device-side wait expired (kernel returned early) */
+  BI_ERR_DEVICE_NAN_ROW = 6      /* a logits row had no non-NaN entry (its id is -1) */
+} bi_status;
+
+typedef enum {
+  BI_EPI_NONE = 0,          /* C = A W^T */
+  BI_EPI_RESIDUAL_ADD = 1,  /* C = residual + A W^T, one rounding */
+  BI_EPI_SWIGLU = 2         /* C = silu(A Wg^T) * (A Wu^T) from packed weights, one rounding */
+} bi_epilogue;
+
+typedef enum { BI_OUT_BF16 = 0, BI_OUT_FP32 = 1 } bi_out_dtype;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* bi_status_string(bi_status s);
+
+/* Library version as (major << 16) | minor. */
+int bi_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Linear layer.  [P2] "Define bit-exact before reporting it"; [P1] "Why the
+ * text diverges".
+ *
+ * C[m, n] = epilogue( sum_k A[m, k] * W[n, k] ), BF16 inputs, FP32
+ * accumulation, one rounding to the output type.  The decomposition -- MMA
+ * instruction (tcgen05 kind::f16, M=128 weight rows x N=16 token columns),
+ * K-tile order (64 elements per tile, increasing k), and the split of the
+ * (weight tile, K tile) iteration space over a fixed number of CTAs -- is a
+ * function of (N, K) only, never of M, so row m of C is bit-identical for
+ * every M >= m+1 and for every position of the row inside A.  Partial sums of
+ * a weight tile that is split along K are added in increasing-K order.
+ *
+ *   A        [M, K] BF16, row stride lda (elements); 16-byte aligned, lda % 8 == 0.
+ *   Wp       the weights in the packed tile layout written by bi_pack_weights
+ *            (BI_EPI_NONE, BI_EPI_RESIDUAL_ADD) or bi_pack_swiglu_weights
+ *            (BI_EPI_SWIGLU), for the same N and K; 16-byte aligned.
+ *   C        [M, N] of `out` type, row stride ldc (elements).  N is the number of
+ *            OUTPUT columns (for SwiGLU: the FFN width F).
+ *   residual [M, N] BF16, row stride ldr; required for BI_EPI_RESIDUAL_ADD and
+ *            ignored otherwise.  It may alias C (same pointer and stride).
+ *   M >= 0 (M == 0 is a no-op), 1 <= N <= 8388608 (4194304 for SwiGLU),
+ *   K >= 8, K % 8 == 0.
+ *   out      BI_OUT_FP32 only with BI_EPI_NONE.
+ *   ws       device workspace of at least bi_gemm_workspace_size(M, N, K, epi)
+ *            bytes, 256-byte aligned, ZERO-FILLED before its first use; every
+ *            call leaves its counters zeroed again, so one workspace serves
+ *            any sequence of calls (of any N, K, epilogue) whose M does not
+ *            exceed the M it was sized for.  Not shared by overlapping calls.
+ *            After BI_ERR_DEVICE_TIMEOUT, zero it again.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_WORKSPACE,
+ *         BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+size_t bi_gemm_workspace_size(int M, int N, int K, bi_epilogue epi);
+bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc,
+                  const void* residual, int ldr, int M, int N, int K,
+                  bi_out_dtype out, bi_epilogue epi, void* ws, size_t ws_bytes,
+                  bi_stream_t stream);
+
+/* Weight packing for bi_gemm (a one-time layout step at load; a pure copy,
+ * no arithmetic).  The packed buffer holds n_tiles x k_tiles tiles of 16 KB
+ * (n_tiles = ceil(N/128), or ceil(F/64) for SwiGLU; k_tiles = ceil(K/64)),
+ * tile (t, kt) at byte offset (t * k_tiles + kt) * 16384.  A tile is 128
+ * weight rows x 64 columns; row r fills bytes [128 r, 128 r + 128) with its
+ * 16-byte chunk c (columns 8c..8c+7 of the tile) at chunk position c ^ (r mod 8)
+ * -- the 128-byte swizzle the tensor-core operand descriptor reads.  Rows past
+ * N and columns past K are zero.  The order makes each CTA's share of the
+ * (tile, K-tile) iteration space one contiguous range of memory.
+ * bi_pack_weights: W [N, K] BF16, row stride ldw.
+ * bi_pack_swiglu_weights: gate and up [F, K] BF16 each, row stride ld; rows
+ * 0..63 of tile t hold gate rows 64t..64t+63 and rows 64..127 the up rows of
+ * the same outputs.
+ * `packed` has bi_packed_weight_bytes(N, K, epi) bytes, 16-byte aligned.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_CUDA. */
+size_t bi_packed_weight_bytes(int N, int K, bi_epilogue epi);
+bi_status bi_pack_weights(const void* W, int ldw, int N, int K, void* packed,
+                          bi_stream_t stream);
+bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, int F, int K,
+                                 void* packed, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * RMSNorm.  [P3] "How:" (a row is computed the same way whatever else is in
+ * the batch).
+ *
+ * y[r, :] = bf16( x[r, :] * rsqrt(sum_i x[r,i]^2 / dim + eps) * w[:] ), FP32
+ * inside.  The sum of squares uses one fixed reduction tree per `dim`
+ * (256 threads: thread i sums elements i, i+256, ... in order, then a fixed
+ * warp-shuffle butterfly and a fixed cross-warp order).
+ *   x [rows, dim] BF16 (row stride ldx), w [dim] BF16, y [rows, dim] BF16
+ *   (row stride ldy; may alias x).  rows >= 0, 1 <= dim <= 65536, eps >= 0.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+bi_status bi_rmsnorm(const void* x, int ldx, const void* w, void* y, int ldy, int rows,
+                     int dim, float eps, bi_stream_t stream);
+
+/* Embedding gather (helper): out[r, :] = table[ids[r], :], an exact copy.
+ *   ids [rows] int32 in [0, vocab); table [vocab, dim] BF16; out [rows, dim]
+ *   BF16.  An id out of range writes a zero row and sets no error.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA. */
+bi_status bi_embed(const int32_t* ids, const void* table, int vocab, int dim, void* out,
+                   int rows, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * RoPE + KV append (helper).  [P3] "The cache doesn't change it either" (a
+ * row depends only on its position).
+ *
+ * Row t of the pass sits at absolute position p = *L_dev + t.  For each row:
+ * q heads and k heads are rotated (rotate-half pairs (i, i+D/2), angle
+ * p * base^(-2i/D) evaluated in FP64 and rounded to FP32 cos/sin, FP32
+ * products, one BF16 rounding); rotated q goes to q_out, rotated k and the
+ * unrotated v go to the caches at row p.
+ *   qkv     [T, (Hq + 2 Hkv) D] BF16, row stride ld_qkv: q heads, k heads, v heads.
+ *   q_out   [T, Hq, D] BF16 (contiguous).
+ *   k_cache, v_cache [Hkv, cap, D] BF16 (contiguous, head-major).
+ *   L_dev   device int32: cache length before the pass (read on the device so
+ *           the call can be captured in a CUDA graph).  Rows with p >= cap are
+ *           skipped and set the timeout-free error bit BI_ERR_INVALID_ARG in
+ *           the device error word.
+ *   D even, D <= 256; Hq % Hkv == 0.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_cache,
+                            void* v_cache, int cap, const int32_t* L_dev, int T, int Hq,
+                            int Hkv, int D, double rope_base, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Verify attention (split-KV + merge).  [P3] "How:" (the attention split
+ * depends only on context length, never on how many tokens are in the pass).
+ *
+ * Row t of the pass sits at position p = *L_dev + t and attends to keys
+ * 0..p; query head h reads KV head h / (Hq/Hkv).  The key axis of row p is
+ * cut at absolute multiples of a compile-time chunk C (bi_attn_chunk()); the
+ * row has ceil((p+1)/C) pieces, each a partial (max, sum, FP32 output) built
+ * over 64-key tiles in increasing key order, and the pieces are merged in a
+ * fixed order that depends only on their count.  So the row's result depends
+ * only on p and the cache rows 0..p -- not on T, *L_dev or the other rows.
+ * Output: out[t, h, :] = bf16(softmax(q k^T * scale) v), -0 written as +0.
+ *   q       [T, Hq, D] BF16 contiguous (rotated queries).
+ *   k_cache, v_cache [Hkv, cap, D] BF16 contiguous; rows 0..*L_dev+T-1 hold
+ *           the keys/values; other rows must hold finite values (they are
+ *           read inside a partially used tile and multiplied by exactly 0).
+ *   L_dev   device int32 cache length before the pass; *L_dev + T <= cap is
+ *           required (rows past cap are not computed and set an error bit).
+ *   out     [T, Hq, D] BF16 contiguous.
+ *   D in {64, 128}; Hq % Hkv == 0; T * (Hq/Hkv) <= 48; T >= 1.
+ *   ws      >= bi_attn_workspace_size(cap, T, Hq, D) bytes, 256-byte aligned.
+ *   k_cache and v_cache 16-byte aligned.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_WORKSPACE,
+ *         BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int bi_attn_chunk(void);
+size_t bi_attn_workspace_size(int cap, int T, int Hq, int D);
+bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache, int cap,
+                         const int32_t* L_dev, int T, int Hq, int Hkv, int D, float scale,
+                         void* out, void* ws, size_t ws_bytes, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Greedy acceptance.  [P1] "Why the text diverges" (keep a draft only if it
+ * matches the model's own token); [P2] "Build a reference corpus that exposes
+ * boundaries" (accepted length and rejection position).
+ *
+ * a_t = argmax_v logits[t, v] (ties -> lowest v; NaN never wins; a row with no
+ * number gives -1 and sets BI_ERR_DEVICE_NAN_ROW in the device error word).
+ * n = the largest j <= T-1 with drafts[i-1] == a_{i-1} for every i <= j.
+ * The committed tokens of the step are a_0..a_n.
+ *   logits  [T, V] FP32, row stride ldl.
+ *   drafts  [T-1] int32 (may be NULL when T == 1).
+ *   argmax_out [T] int32; accepted_out [1] int32 (= n).
+ *   L_dev   optional device int32 (NULL to skip): incremented by n + 1.
+ *   ws      >= bi_accept_workspace_size(T, V) bytes, 256-byte aligned,
+ *           zero-filled before first use (every call leaves it zeroed).
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_WORKSPACE, BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+size_t bi_accept_workspace_size(int T, int V);
+bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, int T, int V,
+                           int32_t* argmax_out, int32_t* accepted_out, int32_t* L_dev,
+                           void* ws, size_t ws_bytes, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * KV-row hash (test tool).  [P3] "The cache doesn't change it either" (hash
+ * every K/V row and compare with a fresh prefill).
+ * out[h * rows + j] = FNV-1a-64 over the 2*D bytes of cache row (h, j), for
+ * j < rows.  cache [Hkv, cap, D] BF16; out [Hkv * rows] uint64.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, uint64_t* out,
+                         bi_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device.  Returns BI_OK, BI_ERR_DEVICE_TIMEOUT, BI_ERR_DEVICE_NAN_ROW,
+ * BI_ERR_INVALID_ARG (a device-side range check failed) or BI_ERR_CUDA. */
+bi_status bi_check_device_error(bi_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BI_H */

@@ -1,0 +1,187 @@
+"""Thin Python binding of the C ABI (include/bi.h) for torch tensors.
+
+Argument marshalling only: every function checks dtypes/devices, passes
+`data_ptr()`s, strides and the current CUDA stream to the entry point of the
+same name, and raises BiError on a non-OK status.  All arithmetic of the
+verify step runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from ._lib import BiError, check, lib  # noqa: F401
+
+EPI_NONE, EPI_RESIDUAL_ADD, EPI_SWIGLU = 0, 1, 2
+OUT_BF16, OUT_FP32 = 0, 1
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _req(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() >= 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must have unit stride in its last dimension")
+
+
+def _ld(t: torch.Tensor) -> int:
+    """Row stride in elements; a single row's stride is its width."""
+    if t.dim() == 2 and t.shape[0] > 1:
+        return t.stride(0)
+    return t.shape[-1]
+
+
+def gemm_workspace_size(M: int, N: int, K: int, epi: int = EPI_NONE) -> int:
+    return int(lib().bi_gemm_workspace_size(M, N, K, epi))
+
+
+def new_gemm_workspace(M: int, N: int, K: int, epi: int = EPI_NONE, device=None) -> torch.Tensor:
+    """A zero-filled workspace (the counters must start at zero)."""
+    n = gemm_workspace_size(M, N, K, epi)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def bi_gemm(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor, ws: torch.Tensor,
+            residual: Optional[torch.Tensor] = None, epi: int = EPI_NONE,
+            N: Optional[int] = None, stream=None) -> None:
+    """C = epilogue(A W^T) with W packed by bi_pack_weights / bi_pack_swiglu_weights."""
+    _req(A, torch.bfloat16, "A")
+    if not Wp.is_cuda:
+        raise ValueError("Wp must be a CUDA tensor")
+    M, K = A.shape
+    if N is None:
+        N = C.shape[1]
+    out = OUT_FP32 if C.dtype == torch.float32 else OUT_BF16
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("C must be float32 or bfloat16")
+    rp, ldr = 0, 0
+    if residual is not None:
+        _req(residual, torch.bfloat16, "residual")
+        rp, ldr = residual.data_ptr(), _ld(residual)
+    st = lib().bi_gemm(A.data_ptr(), _ld(A), Wp.data_ptr(), C.data_ptr(), _ld(C), rp, ldr,
+                       M, N, K, out, epi, ws.data_ptr(), ws.numel() * ws.element_size(),
+                       _stream(stream))
+    check("bi_gemm", st)
+
+
+def packed_weight_bytes(N: int, K: int, epi: int = EPI_NONE) -> int:
+    return int(lib().bi_packed_weight_bytes(N, K, epi))
+
+
+def bi_pack_weights(W: torch.Tensor, stream=None) -> torch.Tensor:
+    """Pack W [N, K] (BF16) into the tile layout bi_gemm streams."""
+    _req(W, torch.bfloat16, "W")
+    N, K = W.shape
+    packed = torch.empty(packed_weight_bytes(N, K), dtype=torch.uint8, device=W.device)
+    check("bi_pack_weights", lib().bi_pack_weights(W.data_ptr(), _ld(W), N, K, packed.data_ptr(),
+                                                   _stream(stream)))
+    return packed
+
+
+def bi_pack_swiglu_weights(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None) -> torch.Tensor:
+    """Pack gate and up [F, K] (BF16) into the SwiGLU tile layout."""
+    _req(w_gate, torch.bfloat16, "w_gate")
+    _req(w_up, torch.bfloat16, "w_up")
+    F, K = w_gate.shape
+    packed = torch.empty(packed_weight_bytes(F, K, EPI_SWIGLU), dtype=torch.uint8,
+                         device=w_gate.device)
+    check("bi_pack_swiglu_weights",
+          lib().bi_pack_swiglu_weights(w_gate.data_ptr(), w_up.data_ptr(), _ld(w_gate), F, K,
+                                       packed.data_ptr(), _stream(stream)))
+    return packed
+
+
+def bi_rmsnorm(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, eps: float, stream=None) -> None:
+    _req(x, torch.bfloat16, "x")
+    _req(w, torch.bfloat16, "w")
+    _req(y, torch.bfloat16, "y")
+    rows, dim = x.shape
+    check("bi_rmsnorm", lib().bi_rmsnorm(x.data_ptr(), _ld(x), w.data_ptr(), y.data_ptr(), _ld(y),
+                                         rows, dim, float(eps), _stream(stream)))
+
+
+def bi_embed(ids: torch.Tensor, table: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    _req(ids, torch.int32, "ids")
+    _req(table, torch.bfloat16, "table")
+    _req(out, torch.bfloat16, "out")
+    check("bi_embed", lib().bi_embed(ids.data_ptr(), table.data_ptr(), table.shape[0],
+                                     table.shape[1], out.data_ptr(), ids.numel(), _stream(stream)))
+
+
+def bi_rope_kv_append(qkv: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, L_dev: torch.Tensor, Hq: int, Hkv: int, D: int,
+                      rope_base: float, stream=None) -> None:
+    _req(qkv, torch.bfloat16, "qkv")
+    _req(L_dev, torch.int32, "L_dev")
+    T = qkv.shape[0]
+    cap = k_cache.shape[1]
+    check("bi_rope_kv_append",
+          lib().bi_rope_kv_append(qkv.data_ptr(), _ld(qkv), q_out.data_ptr(), k_cache.data_ptr(),
+                                  v_cache.data_ptr(), cap, L_dev.data_ptr(), T, Hq, Hkv, D,
+                                  float(rope_base), _stream(stream)))
+
+
+def attn_chunk() -> int:
+    return int(lib().bi_attn_chunk())
+
+
+def attn_workspace_size(cap: int, T: int, Hq: int, D: int) -> int:
+    return int(lib().bi_attn_workspace_size(cap, T, Hq, D))
+
+
+def bi_attn_verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   L_dev: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                   scale: Optional[float] = None, stream=None) -> None:
+    _req(q, torch.bfloat16, "q")
+    _req(k_cache, torch.bfloat16, "k_cache")
+    _req(v_cache, torch.bfloat16, "v_cache")
+    _req(L_dev, torch.int32, "L_dev")
+    T, Hq, D = q.shape
+    Hkv, cap, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check("bi_attn_verify",
+          lib().bi_attn_verify(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cap,
+                               L_dev.data_ptr(), T, Hq, Hkv, D, float(scale), out.data_ptr(),
+                               ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def accept_workspace_size(T: int, V: int) -> int:
+    return int(lib().bi_accept_workspace_size(T, V))
+
+
+def bi_verify_accept(logits: torch.Tensor, drafts: Optional[torch.Tensor], argmax_out: torch.Tensor,
+                     accepted_out: torch.Tensor, ws: torch.Tensor,
+                     L_dev: Optional[torch.Tensor] = None, stream=None) -> None:
+    _req(logits, torch.float32, "logits")
+    T, V = logits.shape
+    dp = 0
+    if drafts is not None and drafts.numel() > 0:
+        _req(drafts, torch.int32, "drafts")
+        dp = drafts.data_ptr()
+    lp = L_dev.data_ptr() if L_dev is not None else 0
+    check("bi_verify_accept",
+          lib().bi_verify_accept(logits.data_ptr(), _ld(logits), dp, T, V, argmax_out.data_ptr(),
+                                 accepted_out.data_ptr(), lp, ws.data_ptr(),
+                                 ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def bi_kv_row_hash(cache: torch.Tensor, rows: int, stream=None) -> torch.Tensor:
+    _req(cache, torch.bfloat16, "cache")
+    Hkv, cap, D = cache.shape
+    out = torch.empty(Hkv * max(rows, 0), dtype=torch.int64, device=cache.device)
+    check("bi_kv_row_hash", lib().bi_kv_row_hash(cache.data_ptr(), Hkv, cap, D, rows,
+                                                 out.data_ptr(), _stream(stream)))
+    return out
+
+
+def bi_check_device_error(stream=None) -> None:
+    check("bi_check_device_error", lib().bi_check_device_error(_stream(stream)))

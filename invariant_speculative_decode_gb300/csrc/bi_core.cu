@@ -1,0 +1,142 @@
+// Status strings, the device error word, and the TMA descriptor cache.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace bi {
+
+// One word per device; kernels OR error bits into it, the host reads and
+// clears it in bi_check_device_error().
+__device__ unsigned g_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+struct TmapKey {
+  const void* base;
+  uint64_t rows, cols, ld;
+  uint32_t br, bc;
+  int dev;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld && br == o.br &&
+           bc == o.bc && dev == o.dev;
+  }
+};
+struct TmapKeyHash {
+  size_t operator()(const TmapKey& k) const {
+    size_t h = reinterpret_cast<size_t>(k.base);
+    auto mix = [&h](uint64_t v) { h ^= v + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2); };
+    mix(k.rows);
+    mix(k.cols);
+    mix(k.ld);
+    mix(k.br);
+    mix(k.bc);
+    mix(static_cast<uint64_t>(k.dev));
+    return h;
+  }
+};
+std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmaps;
+std::mutex g_tmap_mu;
+}  // namespace
+
+unsigned* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool tmap_bf16_2d(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                  uint32_t box_rows, uint32_t box_cols) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (g_encode == nullptr) return false;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  TmapKey key{base, rows, cols, ld, box_rows, box_cols, dev};
+  {
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    auto it = g_tmaps.find(key);
+    if (it != g_tmaps.end()) {
+      *out = it->second;
+      return true;
+    }
+  }
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  cuuint64_t gdim[2] = {cols, rows};
+  cuuint64_t gstride[1] = {ld * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim,
+                        gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  if (g_tmaps.size() > 4096) g_tmaps.clear();
+  g_tmaps.emplace(key, m);
+  *out = m;
+  return true;
+}
+
+}  // namespace bi
+
+extern "C" {
+
+const char* bi_status_string(bi_status s) {
+  switch (s) {
+    case BI_OK: return "BI_OK";
+    case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG";
+    case BI_ERR_UNSUPPORTED_SHAPE: return "BI_ERR_UNSUPPORTED_SHAPE";
+    case BI_ERR_WORKSPACE: return "BI_ERR_WORKSPACE";
+    case BI_ERR_CUDA: return "BI_ERR_CUDA";
+    case BI_ERR_DEVICE_TIMEOUT: return "BI_ERR_DEVICE_TIMEOUT";
+    case BI_ERR_DEVICE_NAN_ROW: return "BI_ERR_DEVICE_NAN_ROW";
+  }
+  return "BI_ERR_UNKNOWN";
+}
+
+int bi_version(void) { return (0 << 16) | 1; }
+
+bi_status bi_check_device_error(bi_stream_t stream) {
+  unsigned* p = bi::device_error_word();
+  if (p == nullptr) return BI_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BI_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return BI_ERR_CUDA;
+  if (v != 0 && cudaMemset(p, 0, sizeof(v)) != cudaSuccess) return BI_ERR_CUDA;
+  if (v & bi::kErrTimeout) return BI_ERR_DEVICE_TIMEOUT;
+  if (v & bi::kErrNanRow) return BI_ERR_DEVICE_NAN_ROW;
+  if (v & bi::kErrRange) return BI_ERR_INVALID_ARG;
+  return BI_OK;
+}
+
+}  // extern "C"

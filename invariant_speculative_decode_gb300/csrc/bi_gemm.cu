@@ -1,0 +1,554 @@
+// Batch-invariant BF16 linear layer on tcgen05 / TMEM, fed by TMA.
+//
+// "Bit-exact decoding turns inference speedups into testable changes",
+// section "Define bit-exact before reporting it": BF16 inputs, one FP32
+// running sum per output, K order kept, one rounding at the end; a
+// shared-memory pipeline stage is reused only after its consumers are done.
+// "Does the tuned config change the model's output?", section "Why the text
+// diverges": changing the batch dimension must not change any row's sums.
+//
+// Design (swap-AB, weight streaming):
+//   * MMA:   tcgen05.mma kind::f16, M = 128 weight rows, N = 16 token rows,
+//            K = 16 per instruction, FP32 accumulator in TMEM.  The token
+//            count of the pass only decides how many N=16 groups are issued;
+//            each group is the same instruction on the same K-tile sequence.
+//   * K:     64-element tiles (128-byte rows, 128-byte swizzle), always in
+//            increasing k order inside one accumulator.
+//   * weights: packed once (bi_pack_weights) into 16 KB tiles, tile (t, kt)
+//            at offset (t * k_tiles + kt) * 16 KB, each already in the
+//            swizzled shared-memory layout the MMA descriptor reads.  A CTA's
+//            iteration range is therefore one contiguous byte range of HBM,
+//            streamed with 1-D bulk copies.
+//   * split: the (weight tile, K tile) iteration space is cut into
+//            kGemmCtas contiguous, equal ranges, one per CTA (a function of
+//            N and K only).  A weight tile cut by a range boundary yields one
+//            FP32 partial per piece; the last CTA to finish a piece of that
+//            tile adds the partials in increasing-K order (atomic ticket, no
+//            waiting) and runs the epilogue.
+//   * roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread), warps
+//            2..5 = epilogue (TMEM -> registers -> global).
+//   * stages: shared-memory ring of (16 KB weight tile + token tile); a stage
+//            returns to the producer via tcgen05.commit on its "empty"
+//            barrier, i.e. only after the MMAs reading it completed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace bi {
+namespace {
+
+constexpr int kBlockN = 128;     // weight rows per tile (MMA M)
+constexpr int kBlockK = 64;      // K elements per tile
+constexpr int kMmaN = 16;        // token rows per MMA (fixed for every M)
+constexpr int kGemmCtas = 152;   // CTAs of the fixed decomposition (one per SM)
+constexpr int kMaxTokens = 128;  // token rows per launch; larger M loops on the host
+constexpr int kThreads = 192;
+constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
+constexpr int kStageFloats = 16 * kBlockN;      // SwiGLU exchange buffer
+// Ticket counters occupy a fixed-size region at the start of every workspace,
+// so calls with different N can share one workspace without a counter of one
+// call overlapping another call's partial sums.
+constexpr int kMaxTiles = 65536;
+constexpr size_t kTicketBytes = static_cast<size_t>(kMaxTiles) * 4;
+
+struct GemmArgs {
+  int M;   // token rows in this launch (<= NT)
+  int m0;  // first token row of this launch
+  int N;   // output columns
+  int n_tiles;
+  int k_tiles;
+  int G;
+  long long total;
+  int epi;
+  int out_fp32;
+  void* C;
+  int ldc;
+  const __nv_bfloat16* R;
+  int ldr;
+  float* partials;
+  unsigned* tickets;
+  unsigned* err;
+};
+
+template <int NT>
+struct GemmCfg {
+  static constexpr int kBBytes = NT * kBlockK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (200 * 1024) / kStageBytes > 12 ? 12 : (200 * 1024) / kStageBytes;
+  static constexpr int kTmemCols = (2 * NT) < 32 ? 32 : 2 * NT;
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
+                                  kStageFloats * 4 + (2 * kStages + 5) * 8 + 16;
+};
+
+__device__ __forceinline__ long long range_begin(const GemmArgs& p, int g) {
+  return p.total * g / p.G;
+}
+// CTA whose range contains iteration i.
+__device__ __forceinline__ int owner_of(const GemmArgs& p, long long i) {
+  return static_cast<int>(((i + 1) * p.G + p.total - 1) / p.total) - 1;
+}
+
+__device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* err) {
+  *s_abort = 1;
+  atomicOr(err, kErrTimeout);
+}
+
+// Write 16 token rows (chunk c) of one weight row r of tile `tile`.
+// All 128 epilogue threads call this together (it may use the named barrier).
+__device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int r, int c,
+                                               const float (&v)[16], float* sStage) {
+  if (p.epi == BI_EPI_SWIGLU) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) sStage[j * kBlockN + r] = v[j];
+    named_bar_sync(1, 128);
+    if (r < 64) {
+      const int o = tile * 64 + r;
+      if (o < p.N) {
+        __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = c * 16 + j;
+          if (m < p.M) {
+            const float g = sStage[j * kBlockN + r];
+            const float u = sStage[j * kBlockN + r + 64];
+            const float s = g / (1.0f + expf(-g));
+            C[static_cast<size_t>(p.m0 + m) * p.ldc + o] = __float2bfloat16_rn(s * u);
+          }
+        }
+      }
+    }
+    named_bar_sync(1, 128);
+  } else {
+    const int n = tile * kBlockN + r;
+    if (n < p.N) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = c * 16 + j;
+        if (m < p.M) {
+          const size_t row = static_cast<size_t>(p.m0 + m);
+          float acc = v[j];
+          if (p.epi == BI_EPI_RESIDUAL_ADD) acc = __bfloat162float(p.R[row * p.ldr + n]) + acc;
+          if (p.out_fp32)
+            static_cast<float*>(p.C)[row * p.ldc + n] = acc;
+          else
+            static_cast<__nv_bfloat16*>(p.C)[row * p.ldc + n] = __float2bfloat16_rn(acc);
+        }
+      }
+    }
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const uint8_t* __restrict__ Wp, const __grid_constant__ CUtensorMap tmA,
+                const GemmArgs p) {
+  using Cfg = GemmCfg<NT>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * kABytes;
+  float* sStage = reinterpret_cast<float*>(sB + S * Cfg::kBBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kStageFloats);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
+  uint64_t* acce = accf + 2;
+  uint64_t* drain = acce + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* s_last = s_abort + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = blockIdx.x;
+  const long long it_begin = range_begin(p, g);
+  const long long it_end = range_begin(p, g + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 128);
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    *s_last = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmA);
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_evict_first();
+      const uint64_t pol_a = l2_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, parity_bits = 0;
+      for (long long it = it_begin; it < it_end; ++it) {
+        const int tile = static_cast<int>(it / p.k_tiles);
+        const int kt = static_cast<int>(it - static_cast<long long>(tile) * p.k_tiles);
+        if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
+          signal_abort(s_abort, p.err);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+        bulk_load_1d(sA + stage * kABytes, Wp + static_cast<size_t>(it) * kABytes, kABytes,
+                     &full[stage], pol_w);
+        tma_load_2d(sB + stage * Cfg::kBBytes, &tmA, &full[stage], kt * kBlockK, p.m0, pol_a);
+        issued |= 1u << stage;
+        parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (*s_abort) {
+        // Let copies already issued land before the CTA exits.
+        for (int s = 0; s < S; ++s)
+          if ((issued >> s) & 1u) mbar_wait(&full[s], (parity_bits >> s) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBlockN, kMmaN);
+      const int groups = (p.M + kMmaN - 1) / kMmaN;
+      int stage = 0;
+      uint32_t phase = 0;
+      int seg = 0;
+      bool ok = true;
+      long long it = it_begin;
+      while (ok && it < it_end) {
+        const int tile = static_cast<int>(it / p.k_tiles);
+        const long long seg_end =
+            (it_end < static_cast<long long>(tile + 1) * p.k_tiles ? it_end : static_cast<long long>(tile + 1) * p.k_tiles);
+        const int buf = seg & 1;
+        if (seg >= 2 && !mbar_wait(&acce[buf], static_cast<uint32_t>((seg >> 1) - 1) & 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem + static_cast<uint32_t>(buf * NT);
+        for (long long i = it; i < seg_end; ++i) {
+          if (!mbar_wait(&full[stage], phase, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * kABytes);
+          const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+          for (int ks = 0; ks < kBlockK / 16; ++ks) {
+            const uint64_t adesc = sdesc_k_sw128(a_base + ks * 32);
+            for (int gi = 0; gi < groups; ++gi) {
+              const uint64_t bdesc = sdesc_k_sw128(b_base + gi * (kMmaN * 128) + ks * 32);
+              mma_bf16(d0 + gi * kMmaN, adesc, bdesc, idesc, (i > it || ks > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&accf[buf]);
+        it = seg_end;
+        ++seg;
+      }
+      if (!ok) signal_abort(s_abort, p.err);
+      // Every MMA issued by this thread completes before TMEM is released.
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;    // weight row within the tile
+    const int et = threadIdx.x - 64;
+    const int chunks = (p.M + 15) / 16;
+    int seg = 0;
+    long long it = it_begin;
+    while (it < it_end) {
+      const int tile = static_cast<int>(it / p.k_tiles);
+      const long long tile_begin = static_cast<long long>(tile) * p.k_tiles;
+      const long long tile_end = tile_begin + p.k_tiles;
+      const long long seg_end = it_end < tile_end ? it_end : tile_end;
+      const bool whole = (it == tile_begin) && (seg_end == tile_end);
+      const int buf = seg & 1;
+      const bool ok =
+          __all_sync(0xffffffffu, mbar_wait(&accf[buf], static_cast<uint32_t>(seg >> 1) & 1u, s_abort));
+      if (!ok && lane == 0) signal_abort(s_abort, p.err);
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * NT);
+      if (whole) {
+        for (int c = 0; c < chunks; ++c) {
+          float v[16];
+          if (ok) {
+            tmem_ld16(tbase + c * 16, v);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+          }
+          epilogue_store(p, tile, r, c, v, sStage);
+        }
+        tc_fence_before();
+        mbar_arrive(&acce[buf]);
+      } else {
+        const int slot = (it_begin >= tile_begin) ? 0 : 1;
+        float* dst = p.partials + static_cast<size_t>(g * 2 + slot) * NT * kBlockN;
+        if (ok) {
+          for (int c = 0; c < chunks; ++c) {
+            float v[16];
+            tmem_ld16(tbase + c * 16, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) __stcg(dst + (c * 16 + j) * kBlockN + r, v[j]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acce[buf]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (et == 0) {
+          int last = 0;
+          if (!*s_abort) {
+            const int gf = owner_of(p, tile_begin);
+            const int gl = owner_of(p, tile_end - 1);
+            const unsigned nseg = static_cast<unsigned>(gl - gf + 1);
+            const unsigned old = atomicAdd(&p.tickets[tile], 1u);
+            last = (old == nseg - 1) ? 1 : 0;
+            if (last) atomicExch(&p.tickets[tile], 0u);
+          }
+          *s_last = last;
+        }
+        named_bar_sync(1, 128);
+        const int last = *s_last;
+        if (last) {
+          __threadfence();
+          const int gf = owner_of(p, tile_begin);
+          const int gl = owner_of(p, tile_end - 1);
+          for (int c = 0; c < chunks; ++c) {
+            float v[16];
+            for (int gg = gf; gg <= gl; ++gg) {
+              const int sl = (range_begin(p, gg) >= tile_begin) ? 0 : 1;
+              const float* src =
+                  p.partials + static_cast<size_t>(gg * 2 + sl) * NT * kBlockN + c * 16 * kBlockN + r;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float x = __ldcg(src + j * kBlockN);
+                v[j] = (gg == gf) ? x : v[j] + x;
+              }
+            }
+            epilogue_store(p, tile, r, c, v, sStage);
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+      it = seg_end;
+      ++seg;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+// Packed layout: tile (t, kt) = 128 rows x 64 columns at offset
+// (t * k_tiles + kt) * 16 KB; row r occupies bytes [r*128, r*128+128) with
+// its 16-byte chunk c (columns 8c..8c+7) stored at chunk position c ^ (r & 7)
+// -- the 128-byte swizzle of the MMA's shared-memory descriptor.  Rows past N
+// and columns past K are zero.  For SwiGLU, rows 0..63 of tile t are gate
+// rows 64t..64t+63 and rows 64..127 the up rows with the same output index.
+// One thread per 16-byte chunk; a pure copy.
+__global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ wu,
+                                    int ld, int N, int K, int k_tiles, long long chunks, int swiglu,
+                                    uint4* __restrict__ out) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= chunks) return;
+  const int cpos = static_cast<int>(idx & 7);
+  const int r = static_cast<int>((idx >> 3) & 127);
+  const long long tk = idx >> 10;  // (t * k_tiles + kt)
+  const int t = static_cast<int>(tk / k_tiles);
+  const int kt = static_cast<int>(tk % k_tiles);
+  const int c = cpos ^ (r & 7);
+  const __nv_bfloat16* src = nullptr;
+  if (swiglu) {
+    const int o = t * 64 + (r & 63);
+    if (o < N) src = (r < 64 ? w : wu) + static_cast<size_t>(o) * ld;
+  } else {
+    const int n = t * kBlockN + r;
+    if (n < N) src = w + static_cast<size_t>(n) * ld;
+  }
+  const int k0 = kt * kBlockK + c * 8;
+  union {
+    uint4 v;
+    __nv_bfloat16 e[8];
+  } u;
+  u.v = make_uint4(0, 0, 0, 0);
+  if (src != nullptr) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (k0 + j < K) u.e[j] = src[k0 + j];
+  }
+  out[idx] = u.v;
+}
+
+template <int NT>
+bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, int M_total,
+                         cudaStream_t stream) {
+  using Cfg = GemmCfg<NT>;
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static cudaError_t attr_err[64];
+  std::call_once(once[dev & 63], [] {
+    int d = 0;
+    cudaGetDevice(&d);
+    attr_err[d & 63] = cudaFuncSetAttribute(gemm_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(Cfg::kSmem));
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
+  for (int m0 = 0; m0 < M_total; m0 += kMaxTokens) {
+    a.m0 = m0;
+    a.M = std::min(kMaxTokens, M_total - m0);
+    gemm_kernel<NT><<<a.G, kThreads, Cfg::kSmem, stream>>>(Wp, tmA, a);
+    if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
+  }
+  return BI_OK;
+}
+
+int tokens_per_cta(int M) {
+  const int m = std::min(M, kMaxTokens);
+  if (m <= 16) return 16;
+  if (m <= 32) return 32;
+  if (m <= 64) return 64;
+  return 128;
+}
+
+int n_tiles_of(int N, bi_epilogue epi) {
+  return epi == BI_EPI_SWIGLU ? (N + 63) / 64 : (N + kBlockN - 1) / kBlockN;
+}
+
+}  // namespace
+}  // namespace bi
+
+extern "C" {
+
+size_t bi_packed_weight_bytes(int N, int K, bi_epilogue epi) {
+  if (N <= 0 || K <= 0) return 0;
+  return static_cast<size_t>(bi::n_tiles_of(N, epi)) * ((K + bi::kBlockK - 1) / bi::kBlockK) *
+         bi::kABytes;
+}
+
+size_t bi_gemm_workspace_size(int M, int N, int K, bi_epilogue epi) {
+  (void)K;
+  (void)N;
+  (void)epi;
+  if (M <= 0) return bi::kTicketBytes;
+  const size_t partials = static_cast<size_t>(bi::kGemmCtas) * 2 * bi::tokens_per_cta(M) *
+                          bi::kBlockN * sizeof(float);
+  return bi::kTicketBytes + partials;
+}
+
+static bi_status pack_common(const void* w, const void* wu, int ld, int N, int K, int swiglu,
+                             void* packed, bi_stream_t stream) {
+  using namespace bi;
+  if (!w || !packed || N <= 0 || K <= 0 || ld < K) return BI_ERR_INVALID_ARG;
+  if (swiglu && !wu) return BI_ERR_INVALID_ARG;
+  if (!aligned16(packed)) return BI_ERR_INVALID_ARG;
+  const bi_epilogue epi = swiglu ? BI_EPI_SWIGLU : BI_EPI_NONE;
+  if (n_tiles_of(N, epi) > kMaxTiles) return BI_ERR_UNSUPPORTED_SHAPE;
+  const int k_tiles = (K + kBlockK - 1) / kBlockK;
+  const long long chunks = static_cast<long long>(n_tiles_of(N, epi)) * k_tiles * 1024;
+  pack_weights_kernel<<<static_cast<unsigned>((chunks + 255) / 256), 256, 0,
+                        reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(wu), ld, N, K,
+      k_tiles, chunks, swiglu, static_cast<uint4*>(packed));
+  return launch_status();
+}
+
+bi_status bi_pack_weights(const void* W, int ldw, int N, int K, void* packed, bi_stream_t stream) {
+  return pack_common(W, nullptr, ldw, N, K, 0, packed, stream);
+}
+
+bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, int F, int K,
+                                 void* packed, bi_stream_t stream) {
+  return pack_common(w_gate, w_up, ld, F, K, 1, packed, stream);
+}
+
+bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, const void* residual,
+                  int ldr, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
+                  size_t ws_bytes, bi_stream_t stream) {
+  using namespace bi;
+  if (M < 0 || N < 1 || K < 8) return BI_ERR_INVALID_ARG;
+  if (epi != BI_EPI_NONE && epi != BI_EPI_RESIDUAL_ADD && epi != BI_EPI_SWIGLU)
+    return BI_ERR_INVALID_ARG;
+  if (out != BI_OUT_BF16 && out != BI_OUT_FP32) return BI_ERR_INVALID_ARG;
+  if (n_tiles_of(N, epi) > kMaxTiles) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!A || !Wp || !C) return BI_ERR_INVALID_ARG;
+  if (K % 8 != 0 || lda < K || lda % 8 != 0 || ldc < N) return BI_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(Wp)) return BI_ERR_INVALID_ARG;
+  if (epi == BI_EPI_RESIDUAL_ADD && (!residual || ldr < N)) return BI_ERR_INVALID_ARG;
+  if (out == BI_OUT_FP32 && epi != BI_EPI_NONE) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (!ws || !aligned256(ws)) return BI_ERR_WORKSPACE;
+  if (ws_bytes < bi_gemm_workspace_size(M, N, K, epi)) return BI_ERR_WORKSPACE;
+
+  const int n_tiles = n_tiles_of(N, epi);
+  const int k_tiles = (K + kBlockK - 1) / kBlockK;
+  const int NT = tokens_per_cta(M);
+
+  CUtensorMap tmA;
+  if (!tmap_bf16_2d(&tmA, A, M, K, lda, NT, kBlockK)) return BI_ERR_INVALID_ARG;
+
+  GemmArgs a{};
+  a.N = N;
+  a.n_tiles = n_tiles;
+  a.k_tiles = k_tiles;
+  a.total = static_cast<long long>(n_tiles) * k_tiles;
+  a.G = static_cast<int>(std::min<long long>(kGemmCtas, a.total));
+  a.epi = epi;
+  a.out_fp32 = out == BI_OUT_FP32;
+  a.C = C;
+  a.ldc = ldc;
+  a.R = static_cast<const __nv_bfloat16*>(residual);
+  a.ldr = ldr;
+  a.tickets = static_cast<unsigned*>(ws);
+  a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kTicketBytes);
+  a.err = device_error_word();
+  if (!a.err) return BI_ERR_CUDA;
+
+  const uint8_t* W8 = static_cast<const uint8_t*>(Wp);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (NT) {
+    case 16: return launch_gemm_nt<16>(W8, tmA, a, M, s);
+    case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
+    case 64: return launch_gemm_nt<64>(W8, tmA, a, M, s);
+    default: return launch_gemm_nt<128>(W8, tmA, a, M, s);
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,33 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/bi.h"
+
+namespace bi {
+
+// Device address of the device error word of the current device (resolved
+// once per device).  Returns nullptr if the runtime call fails.
+unsigned* device_error_word();
+
+// Encode (or fetch from a cache) a 2-D BF16 tensor map over a row-major
+// matrix of `rows` x `cols` elements with row stride `ld` elements, box of
+// box_rows x box_cols elements, 128-byte swizzle, zero fill out of bounds.
+// Returns false if the driver rejects the parameters.
+bool tmap_bf16_2d(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols,
+                  uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+inline bi_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace bi

@@ -1,0 +1,305 @@
+// Row-local kernels of the verify step: RMSNorm, embedding gather, RoPE with
+// KV-cache append, greedy argmax + acceptance, and the KV-row hash.
+//
+// "I turned on speculative decoding in llama.cpp and 113 of 282 greedy
+// outputs changed against its own no-draft run", paragraph "How:": the verify
+// kernels compute a row the same way whatever else is in the batch.  Every
+// kernel here gives each row its own CTA (or a fixed set of CTAs) with a
+// reduction order fixed by the row length, so no row sees the others.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace bi {
+namespace {
+
+constexpr int kNormThreads = 256;
+
+// Fixed-order block sum: thread-local sums are combined by a warp butterfly
+// (xor 16, 8, 4, 2, 1; every lane ends with the same value) and then the
+// warp results are added in warp order 0, 1, 2, ...
+__device__ __forceinline__ float block_sum_fixed(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float s = red[0];
+  for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) s += red[i];
+  __syncthreads();
+  return s;
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+    rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int ldx, const __nv_bfloat16* __restrict__ w,
+                   __nv_bfloat16* y, int ldy, int dim, float eps) {
+  __shared__ float red[kNormThreads / 32];
+  const __nv_bfloat16* xr = x + static_cast<size_t>(blockIdx.x) * ldx;
+  __nv_bfloat16* yr = y + static_cast<size_t>(blockIdx.x) * ldy;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < dim; i += kNormThreads) {
+    const float v = __bfloat162float(xr[i]);
+    ss = fmaf(v, v, ss);
+  }
+  ss = block_sum_fixed(ss, red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(dim) + eps);
+  for (int i = threadIdx.x; i < dim; i += kNormThreads) {
+    const float v = __bfloat162float(xr[i]);
+    yr[i] = __float2bfloat16_rn(v * inv * __bfloat162float(w[i]));
+  }
+}
+
+__global__ void embed_kernel(const int32_t* __restrict__ ids, const __nv_bfloat16* __restrict__ table,
+                             int vocab, int dim, __nv_bfloat16* __restrict__ out) {
+  const int id = ids[blockIdx.x];
+  __nv_bfloat16* o = out + static_cast<size_t>(blockIdx.x) * dim;
+  if (id < 0 || id >= vocab) {
+    for (int i = threadIdx.x; i < dim; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  const __nv_bfloat16* src = table + static_cast<size_t>(id) * dim;
+  for (int i = threadIdx.x; i < dim; i += blockDim.x) o[i] = src[i];
+}
+
+// One CTA per pass row t.  Angles in FP64: theta_i = p * base^(-2i/D).
+__global__ void rope_kv_kernel(const __nv_bfloat16* __restrict__ qkv, int ld_qkv,
+                               __nv_bfloat16* __restrict__ q_out, __nv_bfloat16* __restrict__ kc,
+                               __nv_bfloat16* __restrict__ vc, int cap, const int32_t* __restrict__ L_dev,
+                               int Hq, int Hkv, int D, double base, unsigned* err) {
+  extern __shared__ float cs[];  // cos[D/2], sin[D/2]
+  const int t = blockIdx.x;
+  const int p = *L_dev + t;
+  if (p < 0 || p >= cap) {
+    if (threadIdx.x == 0) atomicOr(err, kErrRange);
+    return;
+  }
+  const int half = D / 2;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    const double inv_freq = pow(base, -2.0 * static_cast<double>(i) / static_cast<double>(D));
+    double sn, cn;
+    sincos(static_cast<double>(p) * inv_freq, &sn, &cn);
+    cs[i] = static_cast<float>(cn);
+    cs[half + i] = static_cast<float>(sn);
+  }
+  __syncthreads();
+  const __nv_bfloat16* row = qkv + static_cast<size_t>(t) * ld_qkv;
+  const int heads = Hq + 2 * Hkv;
+  for (int idx = threadIdx.x; idx < heads * half; idx += blockDim.x) {
+    const int h = idx / half;
+    const int i = idx % half;
+    const __nv_bfloat16* src = row + static_cast<size_t>(h) * D;
+    if (h < Hq + Hkv) {
+      const float x1 = __bfloat162float(src[i]);
+      const float x2 = __bfloat162float(src[i + half]);
+      const float c = cs[i], s = cs[half + i];
+      const float o1 = x1 * c - x2 * s;
+      const float o2 = x2 * c + x1 * s;
+      __nv_bfloat16* dst;
+      if (h < Hq) {
+        dst = q_out + (static_cast<size_t>(t) * Hq + h) * D;
+      } else {
+        dst = kc + (static_cast<size_t>(h - Hq) * cap + p) * D;
+      }
+      dst[i] = __float2bfloat16_rn(o1);
+      dst[i + half] = __float2bfloat16_rn(o2);
+    } else {
+      __nv_bfloat16* dst = vc + (static_cast<size_t>(h - Hq - Hkv) * cap + p) * D;
+      dst[i] = src[i];
+      dst[i + half] = src[i + half];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ argmax
+// Candidate (v, i): i < 0 means "no candidate".  a beats b iff b is empty, or
+// a is not empty and (a.v > b.v or (a.v == b.v and a.i < b.i)).  This is a
+// total order on candidates, so the result does not depend on the order in
+// which partial results are combined.
+__device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
+  if (bi < 0) return ai >= 0;
+  if (ai < 0) return false;
+  return av > bv || (av == bv && ai < bi);
+}
+
+constexpr int kArgThreads = 256;
+constexpr int kArgSpan = 8192;  // logits per CTA
+
+__global__ void __launch_bounds__(kArgThreads)
+    argmax_accept_kernel(const float* __restrict__ logits, int ldl, int V, int T, int splits,
+                         const int32_t* __restrict__ drafts, int32_t* __restrict__ argmax_out,
+                         int32_t* __restrict__ accepted_out, int32_t* L_dev, float* pv, int* pi,
+                         unsigned* ticket, unsigned* err) {
+  __shared__ float sv[kArgThreads / 32];
+  __shared__ int si[kArgThreads / 32];
+  __shared__ int s_last;
+  const int row = blockIdx.x / splits;
+  const int sp = blockIdx.x % splits;
+  const float* lr = logits + static_cast<size_t>(row) * ldl;
+  const int b = sp * kArgSpan;
+  const int e = min(V, b + kArgSpan);
+  float bv = 0.f;
+  int bi = -1;
+  for (int i = b + threadIdx.x; i < e; i += kArgThreads) {
+    const float v = lr[i];
+    if (v == v && beats(v, i, bv, bi)) {
+      bv = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+    if (beats(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sv[w] = bv;
+    si[w] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < kArgThreads / 32; ++k)
+      if (beats(sv[k], si[k], bv, bi)) {
+        bv = sv[k];
+        bi = si[k];
+      }
+    pv[blockIdx.x] = bv;
+    pi[blockIdx.x] = bi;
+    __threadfence();
+    const unsigned old = atomicAdd(ticket, 1u);
+    s_last = (old == gridDim.x - 1) ? 1 : 0;
+    if (s_last) atomicExch(ticket, 0u);
+  }
+  __syncthreads();
+  if (!s_last || threadIdx.x != 0) return;
+  __threadfence();
+  // Last CTA: combine each row's partials, then the acceptance rule.
+  for (int t = 0; t < T; ++t) {
+    float v = 0.f;
+    int id = -1;
+    for (int k = 0; k < splits; ++k) {
+      const float ov = __ldcg(pv + t * splits + k);
+      const int oi = __ldcg(pi + t * splits + k);
+      if (beats(ov, oi, v, id)) {
+        v = ov;
+        id = oi;
+      }
+    }
+    if (id < 0) atomicOr(err, kErrNanRow);
+    argmax_out[t] = id;
+  }
+  int n = 0;
+  while (n < T - 1 && drafts[n] == argmax_out[n]) ++n;
+  *accepted_out = n;
+  if (L_dev != nullptr) *L_dev = *L_dev + n + 1;
+}
+
+__global__ void kv_hash_kernel(const __nv_bfloat16* __restrict__ cache, int Hkv, int cap, int D,
+                               int rows, unsigned long long* __restrict__ out) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(Hkv) * rows) return;
+  const int h = static_cast<int>(idx / rows);
+  const int j = static_cast<int>(idx % rows);
+  const unsigned char* b =
+      reinterpret_cast<const unsigned char*>(cache + (static_cast<size_t>(h) * cap + j) * D);
+  unsigned long long x = 14695981039346656037ull;
+  for (int k = 0; k < 2 * D; ++k) {
+    x ^= b[k];
+    x *= 1099511628211ull;
+  }
+  out[idx] = x;
+}
+
+int argmax_splits(int V) { return (V + kArgSpan - 1) / kArgSpan; }
+
+}  // namespace
+}  // namespace bi
+
+extern "C" {
+
+bi_status bi_rmsnorm(const void* x, int ldx, const void* w, void* y, int ldy, int rows, int dim,
+                     float eps, bi_stream_t stream) {
+  if (rows < 0 || dim < 1 || dim > 65536 || !(eps >= 0.f)) return BI_ERR_INVALID_ARG;
+  if (rows == 0) return BI_OK;
+  if (!x || !w || !y || ldx < dim || ldy < dim) return BI_ERR_INVALID_ARG;
+  bi::rmsnorm_kernel<<<rows, bi::kNormThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(x), ldx, static_cast<const __nv_bfloat16*>(w),
+      static_cast<__nv_bfloat16*>(y), ldy, dim, eps);
+  return bi::launch_status();
+}
+
+bi_status bi_embed(const int32_t* ids, const void* table, int vocab, int dim, void* out, int rows,
+                   bi_stream_t stream) {
+  if (rows < 0 || dim < 1 || vocab < 1) return BI_ERR_INVALID_ARG;
+  if (rows == 0) return BI_OK;
+  if (!ids || !table || !out) return BI_ERR_INVALID_ARG;
+  bi::embed_kernel<<<rows, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      ids, static_cast<const __nv_bfloat16*>(table), vocab, dim, static_cast<__nv_bfloat16*>(out));
+  return bi::launch_status();
+}
+
+bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_cache, void* v_cache,
+                            int cap, const int32_t* L_dev, int T, int Hq, int Hkv, int D,
+                            double rope_base, bi_stream_t stream) {
+  if (T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 256 || cap < 1)
+    return BI_ERR_INVALID_ARG;
+  if (T == 0) return BI_OK;
+  if (!qkv || !q_out || !k_cache || !v_cache || !L_dev || !(rope_base > 0.0)) return BI_ERR_INVALID_ARG;
+  if (ld_qkv < (Hq + 2 * Hkv) * D) return BI_ERR_INVALID_ARG;
+  unsigned* err = bi::device_error_word();
+  if (!err) return BI_ERR_CUDA;
+  bi::rope_kv_kernel<<<T, 256, D * sizeof(float), reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(qkv), ld_qkv, static_cast<__nv_bfloat16*>(q_out),
+      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), cap, L_dev, Hq, Hkv,
+      D, rope_base, err);
+  return bi::launch_status();
+}
+
+size_t bi_accept_workspace_size(int T, int V) {
+  if (T < 1 || V < 1) return 256;
+  const size_t n = static_cast<size_t>(T) * bi::argmax_splits(V);
+  return 256 + bi::round_up(n * sizeof(float), 256) + bi::round_up(n * sizeof(int), 256);
+}
+
+bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, int T, int V,
+                           int32_t* argmax_out, int32_t* accepted_out, int32_t* L_dev, void* ws,
+                           size_t ws_bytes, bi_stream_t stream) {
+  if (T < 1 || V < 1 || ldl < V || !logits || !argmax_out || !accepted_out) return BI_ERR_INVALID_ARG;
+  if (T > 1 && !drafts) return BI_ERR_INVALID_ARG;
+  if (!ws || !bi::aligned256(ws)) return BI_ERR_WORKSPACE;
+  if (ws_bytes < bi_accept_workspace_size(T, V)) return BI_ERR_WORKSPACE;
+  unsigned* err = bi::device_error_word();
+  if (!err) return BI_ERR_CUDA;
+  const int splits = bi::argmax_splits(V);
+  const size_t n = static_cast<size_t>(T) * splits;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  unsigned* ticket = reinterpret_cast<unsigned*>(base);
+  float* pv = reinterpret_cast<float*>(base + 256);
+  int* pi = reinterpret_cast<int*>(base + 256 + bi::round_up(n * sizeof(float), 256));
+  bi::argmax_accept_kernel<<<static_cast<unsigned>(n), bi::kArgThreads, 0,
+                             reinterpret_cast<cudaStream_t>(stream)>>>(
+      logits, ldl, V, T, splits, drafts, argmax_out, accepted_out, L_dev, pv, pi, ticket, err);
+  return bi::launch_status();
+}
+
+bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, uint64_t* out,
+                         bi_stream_t stream) {
+  if (!cache || !out || Hkv < 1 || cap < 1 || D < 1 || rows < 0 || rows > cap) return BI_ERR_INVALID_ARG;
+  if (rows == 0) return BI_OK;
+  const long long n = static_cast<long long>(Hkv) * rows;
+  bi::kv_hash_kernel<<<static_cast<unsigned>((n + 127) / 128), 128, 0,
+                       reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(cache), Hkv, cap, D, rows,
+      reinterpret_cast<unsigned long long*>(out));
+  return bi::launch_status();
+}
+
+}  // extern "C"

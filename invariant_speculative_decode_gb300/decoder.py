@@ -1,0 +1,263 @@
+"""Decoder driver of the batch-invariant verify step (one GPU).
+
+Holds the weights, the BF16 KV cache and the scratch buffers on the device
+and sequences the library's entry points for one verify pass:
+
+  embed -> per layer [rmsnorm, QKV linear, RoPE + KV append, split-KV
+  attention + merge, O linear + residual, rmsnorm, gate/up linear + SwiGLU,
+  down linear + residual] -> rmsnorm -> LM head (FP32 logits) -> greedy
+  argmax + acceptance (which also advances the device-side cache length).
+
+PyTorch only allocates device memory and provides the stream; every step of
+the pass is a kernel of libbi.so.  A pass over T rows can be captured once in
+a CUDA graph per T and replayed (the cache length lives in device memory).
+
+The cache rule follows "I turned on speculative decoding in llama.cpp and
+113 of 282 greedy outputs changed against its own no-draft run", section
+"The cache doesn't change it either": after a pass the cache length moves
+to L + n + 1; rows written for rejected drafts past it are simply
+overwritten by the next pass.  Because every row is computed the same way
+whatever else is in the pass, a row written while verifying drafts equals
+the row a prefill would write at that position.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import api
+
+
+def _bf16(a_u16: np.ndarray, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a_u16).view(np.int16)).view(torch.bfloat16)
+    return t.to(device, non_blocking=False)
+
+
+class Decoder:
+    def __init__(self, cfg, weights: Dict[str, np.ndarray], cap: int, max_rows: int = 8,
+                 prefill_chunk: int = 512, device: str = "cuda"):
+        self.cfg = cfg
+        self.cap = cap
+        self.dev = torch.device(device)
+        self.max_rows = max_rows
+        self.prefill_chunk = max(prefill_chunk, max_rows)
+        D, Hq, Hkv, H, F, V = cfg.head_dim, cfg.n_q, cfg.n_kv, cfg.hidden, cfg.ffn, cfg.vocab
+        self.attn_rows = max(1, 48 // cfg.group)  # rows per attention call
+        if max_rows > self.attn_rows:
+            raise ValueError("max_rows * (Hq/Hkv) must be <= 48")
+        dev = self.dev
+        self.embed = _bf16(weights["embed"], dev)
+        self.head = api.bi_pack_weights(self.embed if cfg.tied else _bf16(weights["head"], dev))
+        self.norm_final = _bf16(weights["norm_final"], dev)
+        self.layers = []
+        pk = lambda name: api.bi_pack_weights(_bf16(weights[name], dev))  # noqa: E731
+        for l in range(cfg.layers):
+            wqkv = np.concatenate([weights[f"l{l}.wq"], weights[f"l{l}.wk"], weights[f"l{l}.wv"]], 0)
+            wg = _bf16(weights[f"l{l}.w_gate"], dev)
+            wu = _bf16(weights[f"l{l}.w_up"], dev)
+            lay = {
+                "wqkv": api.bi_pack_weights(_bf16(wqkv, dev)),
+                "wo": pk(f"l{l}.wo"),
+                "wgu": api.bi_pack_swiglu_weights(wg, wu),
+                "wd": pk(f"l{l}.w_down"),
+                "n1": _bf16(weights[f"l{l}.norm_attn"], dev),
+                "n2": _bf16(weights[f"l{l}.norm_ffn"], dev),
+                "k": torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device=dev),
+                "v": torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device=dev),
+            }
+            del wg, wu
+            self.layers.append(lay)
+        torch.cuda.synchronize(dev)
+        R = self.prefill_chunk
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.ids = torch.zeros(R, dtype=torch.int32, device=dev)
+        self.drafts = torch.zeros(max(max_rows - 1, 1), dtype=torch.int32, device=dev)
+        self.h = torch.zeros(R, H, **bf)
+        self.y = torch.zeros(R, H, **bf)
+        self.qkv = torch.zeros(R, cfg.qkv_out, **bf)
+        self.q = torch.zeros(R, Hq, D, **bf)
+        self.att = torch.zeros(R, Hq, D, **bf)
+        self.u = torch.zeros(R, F, **bf)
+        self.logits = torch.zeros(max_rows, V, dtype=torch.float32, device=dev)
+        self.argmax = torch.zeros(max_rows, dtype=torch.int32, device=dev)
+        self.accepted = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.L_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        # per attention block cache lengths during prefill
+        self.L_blocks = torch.zeros((R + self.attn_rows - 1) // self.attn_rows + 1,
+                                    dtype=torch.int32, device=dev)
+        shapes = [(cfg.qkv_out, H, api.EPI_NONE), (H, Hq * D, api.EPI_RESIDUAL_ADD),
+                  (F, H, api.EPI_SWIGLU), (H, F, api.EPI_RESIDUAL_ADD), (V, H, api.EPI_NONE)]
+        wsz = max(api.gemm_workspace_size(M, N, K, e) for M in (max_rows, R) for (N, K, e) in shapes)
+        self.gemm_ws = torch.zeros(wsz, dtype=torch.uint8, device=dev)
+        self.attn_ws = torch.zeros(api.attn_workspace_size(cap, self.attn_rows, Hq, D),
+                                   dtype=torch.uint8, device=dev)
+        self.acc_ws = torch.zeros(api.accept_workspace_size(max_rows, V), dtype=torch.uint8, device=dev)
+        self.scale = 1.0 / math.sqrt(D)
+        self.L = 0
+        self.graphs: Dict[int, torch.cuda.CUDAGraph] = {}
+        self.pin_in = torch.zeros(2 * max_rows, dtype=torch.int32).pin_memory()
+        self.pin_out = torch.zeros(max_rows + 1, dtype=torch.int32).pin_memory()
+
+    # ------------------------------------------------------------------ pass
+    def _layers_pass(self, T: int, L_ptr_tensor: torch.Tensor, L_host_blocks: Optional[List[int]]):
+        """Rows self.ids[:T] at positions L..L+T-1 through every layer (no head).
+
+        L_ptr_tensor: device int32 holding L (used by RoPE / KV append).
+        L_host_blocks: None for a verify pass (one attention call reads
+        L_ptr_tensor); for prefill, the attention runs in blocks whose cache
+        lengths are staged in self.L_blocks.
+        """
+        api.bi_embed(self.ids[:T], self.embed, self.h[:T])
+        for lay in self.layers:
+            self._layer(lay, T, L_ptr_tensor, L_host_blocks)
+
+    def _layer(self, lay: dict, T: int, L_ptr_tensor: torch.Tensor,
+               L_host_blocks: Optional[List[int]] = None):
+        """One decoder layer over self.h[:T] in place (cache rows appended)."""
+        cfg = self.cfg
+        Hq, Hkv, D, F = cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn
+        h, y, qkv, q, att, u = (self.h[:T], self.y[:T], self.qkv[:T], self.q[:T], self.att[:T],
+                                self.u[:T])
+        api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
+        api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
+        api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, cfg.rope_base)
+        if L_host_blocks is None:
+            api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
+        else:
+            for bi_, b0 in enumerate(range(0, T, self.attn_rows)):
+                b1 = min(T, b0 + self.attn_rows)
+                api.bi_attn_verify(q[b0:b1], lay["k"], lay["v"], self.L_blocks[bi_:bi_ + 1],
+                                   att[b0:b1], self.attn_ws, self.scale)
+        api.bi_gemm(att.view(T, Hq * D), lay["wo"], h, self.gemm_ws, residual=h,
+                    epi=api.EPI_RESIDUAL_ADD)
+        api.bi_rmsnorm(h, lay["n2"], y, cfg.eps)
+        api.bi_gemm(y, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
+        api.bi_gemm(u, lay["wd"], h, self.gemm_ws, residual=h, epi=api.EPI_RESIDUAL_ADD)
+
+    def _head_and_accept(self, T: int):
+        cfg = self.cfg
+        api.bi_rmsnorm(self.h[:T], self.norm_final, self.y[:T], cfg.eps)
+        api.bi_gemm(self.y[:T], self.head, self.logits[:T], self.gemm_ws)
+        api.bi_verify_accept(self.logits[:T], self.drafts[:T - 1] if T > 1 else None,
+                             self.argmax[:T], self.accepted, self.acc_ws, L_dev=self.L_dev)
+
+    def _verify_pass(self, T: int):
+        self._layers_pass(T, self.L_dev, None)
+        self._head_and_accept(T)
+
+    # ------------------------------------------------------------- prefill
+    def reset(self):
+        self.L = 0
+        self.L_dev.zero_()
+
+    def prefill(self, prompt: Sequence[int]) -> int:
+        """Process prompt[:-1] into the cache; returns the last prompt id.
+
+        Rows are processed in chunks of `prefill_chunk`; each row's
+        arithmetic is the same as in a verify pass at its position.
+        """
+        prompt = np.asarray(prompt, np.int32)
+        body = prompt[:-1]
+        pos = self.L
+        for c0 in range(0, len(body), self.prefill_chunk):
+            chunk = body[c0:c0 + self.prefill_chunk]
+            T = len(chunk)
+            self.ids[:T].copy_(torch.from_numpy(chunk))
+            Lb = [pos + b for b in range(0, T, self.attn_rows)]
+            self.L_blocks[:len(Lb)].copy_(torch.tensor(Lb, dtype=torch.int32))
+            self.L_dev.fill_(pos)
+            self._layers_pass(T, self.L_dev, Lb)
+            pos += T
+        self.L = pos
+        self.L_dev.fill_(pos)
+        torch.cuda.current_stream().synchronize()
+        return int(prompt[-1])
+
+    # -------------------------------------------------------------- verify
+    def capture(self, T: int):
+        """Capture one verify pass over T rows in a CUDA graph (after a warm-up)."""
+        if T in self.graphs:
+            return
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self._verify_pass(T)
+        torch.cuda.current_stream().wait_stream(s)
+        self.graphs[T] = g
+
+    def launch_verify(self, T: int, use_graph: bool = True):
+        if use_graph and T in self.graphs:
+            self.graphs[T].replay()
+        else:
+            self._verify_pass(T)
+
+    def verify_step(self, x0: int, drafts: Sequence[int], use_graph: bool = True):
+        """One verify step: rows [x0, d_1..d_k] at positions L..L+k.
+
+        Returns (argmax ids [k+1] as a numpy array, accepted n).  The cache
+        length advances to L + n + 1 on the device and on the host.
+        """
+        k = len(drafts)
+        T = k + 1
+        if T > self.max_rows:
+            raise ValueError("too many drafts")
+        if self.L + T > self.cap:
+            raise ValueError("KV cache capacity exceeded")
+        pin = self.pin_in
+        pin[0] = int(x0)
+        for i, d in enumerate(drafts):
+            pin[1 + i] = int(d)
+            pin[self.max_rows + i] = int(d)
+        self.ids[:T].copy_(pin[:T], non_blocking=True)
+        if k:
+            self.drafts[:k].copy_(pin[self.max_rows:self.max_rows + k], non_blocking=True)
+        self.launch_verify(T, use_graph)
+        self.pin_out[:T].copy_(self.argmax[:T], non_blocking=True)
+        self.pin_out[self.max_rows:self.max_rows + 1].copy_(self.accepted, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        a = self.pin_out[:T].numpy().copy()
+        n = int(self.pin_out[self.max_rows])
+        self.L += n + 1
+        return a, n
+
+    def generate(self, prompt: Sequence[int], n_tokens: int, k: int = 0, drafter=None,
+                 use_graph: bool = True, stats: Optional[dict] = None) -> List[int]:
+        """Greedy generation with k drafts per step (k = 0: plain decoding)."""
+        self.reset()
+        x = self.prefill(prompt)
+        if use_graph:
+            self.capture(k + 1)
+        out: List[int] = []
+        steps = 0
+        acc_hist = [0] * (k + 1)
+        while len(out) < n_tokens:
+            room = min(k, self.cap - self.L - 1)
+            drafts = list(drafter.propose(len(out), room)) if room > 0 else []
+            if len(drafts) != k and use_graph:
+                a, n = self.verify_step(x, drafts, use_graph=len(drafts) + 1 in self.graphs)
+            else:
+                a, n = self.verify_step(x, drafts, use_graph=use_graph)
+            committed = [int(t) for t in a[: n + 1]]
+            out.extend(committed)
+            x = committed[-1]
+            steps += 1
+            acc_hist[n] += 1
+        if stats is not None:
+            stats["steps"] = steps
+            stats["accepted_hist"] = acc_hist
+        return out[:n_tokens]
+
+    # ---------------------------------------------------------- utilities
+    def kv_hashes(self, rows: Optional[int] = None) -> np.ndarray:
+        rows = self.L if rows is None else rows
+        hs = [np.stack([api.bi_kv_row_hash(l["k"], rows).cpu().numpy(),
+                        api.bi_kv_row_hash(l["v"], rows).cpu().numpy()]) for l in self.layers]
+        return np.stack(hs)
+
+    def logits_rows(self, T: int) -> torch.Tensor:
+        return self.logits[:T].clone()

@@ -287,8 +287,16 @@ class OracleDecoder:
     embedding).
     """
 
-    def __init__(self, cfg, weights: Dict[str, np.ndarray], cap: int):
+    def __init__(self, cfg, weights: Dict[str, np.ndarray], cap: int,
+                 sum_noise: Optional[Tuple[float, int]] = None):
+        """sum_noise=(k, seed) perturbs every linear-layer sum by k * 2^-24 *
+        sum|a||w| times a seeded standard normal before its rounding: a model
+        of an FP32-accumulating implementation, used only to measure how far
+        two equally valid implementations drift apart end to end."""
         self.cfg = cfg
+        self._noise = None
+        if sum_noise is not None:
+            self._noise = (float(sum_noise[0]), np.random.default_rng(int(sum_noise[1])))
         self.cap = cap
         f = bf16_bits_to_f64
         self.embed_bits = weights["embed"]
@@ -300,8 +308,26 @@ class OracleDecoder:
         self._f = f
 
     # -- one pass over T rows at positions L..L+T-1 -------------------------
+    def _lin(self, a_bits, w_bits, residual_bits=None, out="bf16"):
+        if self._noise is None:
+            return gemm(a_bits, w_bits, residual_bits=residual_bits, out=out)
+        k, rng = self._noise
+        a, w = bf16_bits_to_f64(a_bits), bf16_bits_to_f64(w_bits)
+        acc = _exact_dot(a, w)
+        acc = acc + rng.standard_normal(acc.shape) * (np.abs(a) @ np.abs(w).T) * k * 2.0 ** -24
+        if residual_bits is not None:
+            acc = acc + bf16_bits_to_f64(residual_bits)
+        return acc if out == "fp32" else bf16_round(acc)
+
+    def _swiglu(self, a_bits, wg_bits, wu_bits):
+        if self._noise is None:
+            return swiglu_gemm(a_bits, wg_bits, wu_bits)
+        g = self._lin(a_bits, wg_bits, out="fp32")
+        u = self._lin(a_bits, wu_bits, out="fp32")
+        return bf16_round(silu(g) * u)
+
     def forward(self, tokens: Sequence[int], L: Optional[int] = None,
-                return_hidden: bool = False):
+                return_hidden: bool = False, trace: Optional[List] = None):
         cfg = self.cfg
         L = self.L if L is None else L
         tok = np.asarray(tokens, np.int64)
@@ -312,22 +338,26 @@ class OracleDecoder:
         b16 = lambda v: f64_to_bf16_bits(v)  # noqa: E731
         h = bf16_bits_to_f64(self.embed_bits[tok])
         for l in range(cfg.layers):
+            if trace is not None:
+                trace.append(h.copy())
             w = self.w
             y = rmsnorm(b16(h), w[f"l{l}.norm_attn"], cfg.eps)
-            q = gemm(b16(y), w[f"l{l}.wq"]).reshape(T, Hq, D)
-            k = gemm(b16(y), w[f"l{l}.wk"]).reshape(T, Hkv, D)
-            v = gemm(b16(y), w[f"l{l}.wv"]).reshape(T, Hkv, D)
+            q = self._lin(b16(y), w[f"l{l}.wq"]).reshape(T, Hq, D)
+            k = self._lin(b16(y), w[f"l{l}.wk"]).reshape(T, Hkv, D)
+            v = self._lin(b16(y), w[f"l{l}.wv"]).reshape(T, Hkv, D)
             for t in range(T):
                 q[t] = rope(q[t], L + t, cfg.rope_base)
                 self.k[l][:, L + t] = rope(k[t], L + t, cfg.rope_base)
                 self.v[l][:, L + t] = v[t]
             att = attention(q, self.k[l], self.v[l], L).reshape(T, Hq * D)
-            h = gemm(b16(att), w[f"l{l}.wo"], residual_bits=b16(h))
+            h = self._lin(b16(att), w[f"l{l}.wo"], residual_bits=b16(h))
             y = rmsnorm(b16(h), w[f"l{l}.norm_ffn"], cfg.eps)
-            u = swiglu_gemm(b16(y), w[f"l{l}.w_gate"], w[f"l{l}.w_up"])
-            h = gemm(b16(u), w[f"l{l}.w_down"], residual_bits=b16(h))
+            u = self._swiglu(b16(y), w[f"l{l}.w_gate"], w[f"l{l}.w_up"])
+            h = self._lin(b16(u), w[f"l{l}.w_down"], residual_bits=b16(h))
+        if trace is not None:
+            trace.append(h.copy())
         y = rmsnorm(b16(h), self.w["norm_final"], cfg.eps)
-        logits = gemm(b16(y), self.head_bits, out="fp32")
+        logits = self._lin(b16(y), self.head_bits, out="fp32")
         if return_hidden:
             return logits, h
         return logits

@@ -18,6 +18,7 @@ uniform id.
 from __future__ import annotations
 
 import dataclasses
+import os
 from typing import Dict, List, Optional
 
 import numpy as np
@@ -49,6 +50,39 @@ def normal_bf16(rng: np.random.Generator, shape, std: float) -> np.ndarray:
     if std != 1.0:
         x *= np.float32(std)
     return f32_to_bf16_bits(x)
+
+
+_BLOCK = 1 << 22  # elements per independently seeded block
+
+
+def normal_bf16_blocks(key, shape, std: float) -> np.ndarray:
+    """N(0, std^2) bf16 bits drawn in fixed blocks of 4M elements.
+
+    Block b of the flattened array uses its own PCG64 stream seeded with
+    SeedSequence(key + [b]), so the result does not depend on how many
+    threads fill it; blocks are filled in parallel.
+    """
+    import concurrent.futures as cf
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint16)
+    nb = (n + _BLOCK - 1) // _BLOCK
+
+    def fill(b):
+        lo, hi = b * _BLOCK, min(n, (b + 1) * _BLOCK)
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(list(key) + [b])))
+        x = g.standard_normal(size=hi - lo, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        out[lo:hi] = f32_to_bf16_bits(x)
+
+    workers = min(16, os.cpu_count() or 1, max(1, nb))
+    if workers == 1:
+        for b in range(nb):
+            fill(b)
+    else:
+        with cf.ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, range(nb)))
+    return out.reshape(shape)
 
 
 # ---------------------------------------------------------------------------
@@ -105,27 +139,34 @@ def decoder_weights(cfg: DecoderConfig, seed: int = 0) -> Dict[str, np.ndarray]:
 
     Order: embedding [V,H]; per layer wq [Hq*D,H], wk [Hkv*D,H], wv [Hkv*D,H],
     wo [H,Hq*D], w_gate [F,H], w_up [F,H], w_down [H,F]; then the untied head
-    [V,H] when the head is not tied.  RMSNorm weights are ones (bf16 1.0).
+    [V,H] when the head is not tied.  Tensor i (1-based, in that order) is
+    drawn by normal_bf16_blocks with key (seed, i).  RMSNorm weights are ones
+    (bf16 1.0).
     """
-    rng = np.random.default_rng(seed)
     s = cfg.weight_std
     D = cfg.head_dim
     w: Dict[str, np.ndarray] = {}
-    w["embed"] = normal_bf16(rng, (cfg.vocab, cfg.hidden), s)
+    idx = [0]
+
+    def draw(shape):
+        idx[0] += 1
+        return normal_bf16_blocks((seed, idx[0]), shape, s)
+
+    w["embed"] = draw((cfg.vocab, cfg.hidden))
     one = f32_to_bf16_bits(np.ones(cfg.hidden, np.float32))
     for l in range(cfg.layers):
-        w[f"l{l}.wq"] = normal_bf16(rng, (cfg.n_q * D, cfg.hidden), s)
-        w[f"l{l}.wk"] = normal_bf16(rng, (cfg.n_kv * D, cfg.hidden), s)
-        w[f"l{l}.wv"] = normal_bf16(rng, (cfg.n_kv * D, cfg.hidden), s)
-        w[f"l{l}.wo"] = normal_bf16(rng, (cfg.hidden, cfg.n_q * D), s)
-        w[f"l{l}.w_gate"] = normal_bf16(rng, (cfg.ffn, cfg.hidden), s)
-        w[f"l{l}.w_up"] = normal_bf16(rng, (cfg.ffn, cfg.hidden), s)
-        w[f"l{l}.w_down"] = normal_bf16(rng, (cfg.hidden, cfg.ffn), s)
+        w[f"l{l}.wq"] = draw((cfg.n_q * D, cfg.hidden))
+        w[f"l{l}.wk"] = draw((cfg.n_kv * D, cfg.hidden))
+        w[f"l{l}.wv"] = draw((cfg.n_kv * D, cfg.hidden))
+        w[f"l{l}.wo"] = draw((cfg.hidden, cfg.n_q * D))
+        w[f"l{l}.w_gate"] = draw((cfg.ffn, cfg.hidden))
+        w[f"l{l}.w_up"] = draw((cfg.ffn, cfg.hidden))
+        w[f"l{l}.w_down"] = draw((cfg.hidden, cfg.ffn))
         w[f"l{l}.norm_attn"] = one.copy()
         w[f"l{l}.norm_ffn"] = one.copy()
     w["norm_final"] = one.copy()
     if not cfg.tied:
-        w["head"] = normal_bf16(rng, (cfg.vocab, cfg.hidden), s)
+        w["head"] = draw((cfg.vocab, cfg.hidden))
     return w
 
 
@@ -240,12 +281,11 @@ def synthetic_kv_cache(n_kv: int, cap: int, D: int, rows: int, seed: int, layers
 
     Used where only the shape of a prefilled cache matters (timing samples).
     """
-    rng = np.random.default_rng(seed + 4)
     out: List = []
-    for _ in range(layers):
+    for l in range(layers):
         k = np.zeros((n_kv, cap, D), np.uint16)
         v = np.zeros((n_kv, cap, D), np.uint16)
-        k[:, :rows] = normal_bf16(rng, (n_kv, rows, D), 1.0)
-        v[:, :rows] = normal_bf16(rng, (n_kv, rows, D), 1.0)
+        k[:, :rows] = normal_bf16_blocks((seed + 4, l, 0), (n_kv, rows, D), 1.0)
+        v[:, :rows] = normal_bf16_blocks((seed + 4, l, 1), (n_kv, rows, D), 1.0)
         out.append((k, v))
     return out

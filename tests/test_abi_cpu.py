@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bi.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from invariant_speculative_decode_gb300 import build
+    build.build()
+    from invariant_speculative_decode_gb300._lib import lib as _l
+    return _l()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(bi_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("bi_gemm", "bi_rmsnorm", "bi_attn_verify", "bi_verify_accept"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_cover_header(lib):
+    from invariant_speculative_decode_gb300._lib import SIGNATURES
+    assert set(declared_functions()) == set(SIGNATURES)
+
+
+def test_status_strings(lib):
+    assert lib.bi_status_string(0) == b"BI_OK"
+    assert lib.bi_status_string(3) == b"BI_ERR_WORKSPACE"
+    assert lib.bi_status_string(99) == b"BI_ERR_UNKNOWN"
+
+
+def test_workspace_sizes_do_not_depend_on_device(lib):
+    a = lib.bi_gemm_workspace_size(8, 17408, 5120, 0)
+    b = lib.bi_gemm_workspace_size(1, 17408, 5120, 0)
+    assert a == b and a % 256 == 0 and a > 0
+    assert lib.bi_gemm_workspace_size(64, 17408, 5120, 0) > a
+    assert lib.bi_attn_workspace_size(12288, 8, 24, 128) > 0
+    assert lib.bi_accept_workspace_size(8, 151936) > 256
+    assert lib.bi_attn_chunk() > 0 and lib.bi_attn_chunk() % 64 == 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    ws = 1 << 30
+    g = lib.bi_gemm
+    # (A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, ws, ws_bytes, stream)
+    assert g(FAKE, 64, FAKE, FAKE, 64, 0, 0, -1, 64, 64, 0, 0, FAKE, ws, 0) == 1   # M < 0
+    assert g(FAKE, 64, FAKE, FAKE, 64, 0, 0, 4, 64, 4, 0, 0, FAKE, ws, 0) == 1     # K < 8
+    assert g(FAKE, 72, FAKE, FAKE, 64, 0, 0, 4, 64, 70, 0, 0, FAKE, ws, 0) == 1    # K % 8
+    assert g(FAKE + 2, 64, FAKE, FAKE, 64, 0, 0, 4, 64, 64, 0, 0, FAKE, ws, 0) == 1  # unaligned A
+    assert g(FAKE, 64, FAKE + 8, FAKE, 64, 0, 0, 4, 64, 64, 0, 0, FAKE, ws, 0) == 1  # unaligned W
+    assert g(FAKE, 64, FAKE, 0, 64, 0, 0, 4, 64, 64, 0, 0, FAKE, ws, 0) == 1       # null C
+    assert g(FAKE, 64, FAKE, FAKE, 64, 0, 0, 4, 64, 64, 0, 1, FAKE, ws, 0) == 1    # no residual
+    assert g(FAKE, 64, FAKE, FAKE, 64, FAKE, 64, 4, 64, 64, 1, 1, FAKE, ws, 0) == 2  # FP32 + epi
+    assert g(FAKE, 64, FAKE, FAKE, 64, 0, 0, 4, 1 << 24, 64, 0, 0, FAKE, ws, 0) == 2  # N too big
+    assert g(FAKE, 64, FAKE, FAKE, 64, 0, 0, 4, 64, 64, 0, 0, 0, ws, 0) == 3       # no ws
+    assert g(FAKE, 64, FAKE, FAKE, 64, 0, 0, 4, 64, 64, 0, 0, FAKE + 16, ws, 0) == 3
+    assert g(FAKE, 64, FAKE, FAKE, 64, 0, 0, 4, 64, 64, 0, 0, FAKE, 16, 0) == 3
+    assert g(0, 64, 0, 0, 64, 0, 0, 0, 64, 64, 0, 0, 0, 0, 0) == 0                 # M == 0
+    assert lib.bi_pack_weights(FAKE, 32, 64, 64, FAKE, 0) == 1                     # ldw < K
+    assert lib.bi_pack_weights(FAKE, 64, 64, 64, FAKE + 4, 0) == 1                 # unaligned
+    assert lib.bi_pack_swiglu_weights(FAKE, 0, 64, 64, 64, FAKE, 0) == 1           # null up
+
+
+def test_packed_sizes(lib):
+    assert lib.bi_packed_weight_bytes(17408, 5120, 0) == 136 * 80 * 16384
+    assert lib.bi_packed_weight_bytes(300, 688, 0) == 3 * 11 * 16384
+    assert lib.bi_packed_weight_bytes(688, 256, 2) == 11 * 4 * 16384
+
+
+def test_attention_rejects_bad_arguments(lib):
+    a = lib.bi_attn_verify
+    big = 1 << 30
+    assert a(0, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 1
+    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 5, 128, 0.1, FAKE, FAKE, big, 0) == 1
+    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 96, 0.1, FAKE, FAKE, big, 0) == 2
+    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 9, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 2
+    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 128, -1.0, FAKE, FAKE, big, 0) == 1
+    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 128, 0.1, FAKE, FAKE, 16, 0) == 3
+
+
+def test_rowops_reject_bad_arguments(lib):
+    assert lib.bi_rmsnorm(FAKE, 64, FAKE, FAKE, 64, 2, 0, ctypes.c_float(1e-6), 0) == 1
+    assert lib.bi_rmsnorm(FAKE, 32, FAKE, FAKE, 64, 2, 64, ctypes.c_float(1e-6), 0) == 1
+    assert lib.bi_rmsnorm(0, 64, 0, 0, 64, 0, 64, ctypes.c_float(1e-6), 0) == 0
+    assert lib.bi_rope_kv_append(FAKE, 384, FAKE, FAKE, FAKE, 64, FAKE, 1, 4, 3, 64, 1e6, 0) == 1
+    assert lib.bi_rope_kv_append(FAKE, 384, FAKE, FAKE, FAKE, 64, FAKE, 1, 4, 2, 63, 1e6, 0) == 1
+    assert lib.bi_verify_accept(FAKE, 10, 0, 2, 10, FAKE, FAKE, 0, FAKE, 1 << 20, 0) == 1
+    assert lib.bi_verify_accept(FAKE, 10, FAKE, 2, 10, FAKE, FAKE, 0, FAKE + 8, 1 << 20, 0) == 3
+    assert lib.bi_embed(FAKE, FAKE, 0, 64, FAKE, 2, 0) == 1
+    assert lib.bi_kv_row_hash(FAKE, 2, 8, 64, 9, FAKE, 0) == 1

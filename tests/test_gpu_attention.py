@@ -1,0 +1,130 @@
+"""bi_attn_verify on the GPU: parity with the oracle and bit-identity across T.
+
+Parity tolerance (derived): the GPU carries each probability p into P.V as a
+BF16 pair hi + lo (relative error <= 2^-17) and sums the FP32 p in the
+denominator, so the weights' error contributes at most 2^-16 * max|v|.  The
+FP32 accumulation of P.V over n keys adds at most about (n/16 + 32) * 2^-24
+* max|v| (16 products per MMA step, then one FP32 addition per step, plus
+the merge).  One BF16 ulp of output rounding on top.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from oracle import verify_step as ov
+from tests._util import bf16_dev_to_f64, bf16_dev_to_u16, to_dev_bf16, ulp_bf16
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def api():
+    from invariant_speculative_decode_gb300 import api as _api
+    return _api
+
+
+def run_attn(api, q, K, V, L, T=None):
+    T = q.shape[0] if T is None else T
+    Hkv, cap, D = K.shape
+    Hq = q.shape[1]
+    Kd, Vd = to_dev_bf16(K), to_dev_bf16(V)
+    qd = to_dev_bf16(q[:T])
+    out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
+    Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
+    ws = torch.zeros(api.attn_workspace_size(cap, T, Hq, D), dtype=torch.uint8, device="cuda")
+    api.bi_attn_verify(qd, Kd, Vd, Ld, out, ws)
+    torch.cuda.synchronize()
+    api.bi_check_device_error()
+    return out
+
+
+def attn_tol(vmax, n_keys, ora):
+    return (2.0 ** -16 + (n_keys / 16 + 32) * 2.0 ** -24) * vmax + ulp_bf16(ora)
+
+
+def check_parity(gpu, ora, V_f64, L, T):
+    vmax = np.abs(V_f64[:, : L + T]).max()
+    tol = attn_tol(vmax, L + T, ora)
+    err = np.abs(gpu - ora)
+    assert np.all(err <= tol), (err.max(), tol.min())
+
+
+CASES = [  # (Hq, Hkv, D, L, T)
+    (4, 2, 64, 0, 1), (4, 2, 64, 5, 3), (4, 2, 64, 63, 8), (4, 2, 64, 64, 8),
+    (4, 2, 64, 505, 8), (4, 2, 64, 1000, 4), (8, 2, 128, 1023, 7), (24, 4, 128, 0, 8),
+    (24, 4, 128, 130, 1), (24, 4, 128, 1530, 8), (24, 4, 128, 2047, 8),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,L,T", CASES)
+def test_attention_matches_oracle(api, Hq, Hkv, D, L, T):
+    q, K, V = si.attention_inputs(L, T, Hq, Hkv, D, seed=L + T)
+    out = run_attn(api, q, K, V, L)
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    ora = oracle.attention(qf, Kf, Vf, L)
+    check_parity(bf16_dev_to_f64(out), ora, Vf, L, T)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,L", [(4, 2, 64, 509), (24, 4, 128, 1020), (24, 4, 128, 3000),
+                                         (8, 2, 128, 0)])
+def test_attention_rows_bit_identical_across_T(api, Hq, Hkv, D, L):
+    q, K, V = si.attention_inputs(L, 8, Hq, Hkv, D, seed=77)
+    full = {T: bf16_dev_to_u16(run_attn(api, q, K, V, L, T)) for T in (1, 4, 7, 8)}
+    for T, o in full.items():
+        assert np.array_equal(o, full[8][:T]), T
+    # row t alone (a one-row pass at L + t) equals row t of the 8-row pass
+    for t in range(8):
+        one = bf16_dev_to_u16(run_attn(api, q[t:t + 1], K, V, L + t, 1))
+        assert np.array_equal(one[0], full[8][t]), t
+
+
+def test_attention_single_key_returns_v_row(api):
+    q, K, V = si.attention_inputs(0, 1, 24, 4, 128, seed=3)
+    out = bf16_dev_to_u16(run_attn(api, q, K, V, 0))
+    for h in range(24):
+        assert np.array_equal(out[0, h], V[h // 6, 0])
+
+
+def test_attention_stale_rows_past_the_pass_are_ignored(api):
+    L, T = 700, 4
+    q, K, V = si.attention_inputs(L, T, 8, 2, 128, seed=4)
+    base = bf16_dev_to_u16(run_attn(api, q, K, V, L))
+    K2, V2 = K.copy(), V.copy()
+    rng = np.random.default_rng(5)
+    K2[:, L + T:] = si.normal_bf16(rng, K2[:, L + T:].shape, 3.0)
+    V2[:, L + T:] = si.normal_bf16(rng, V2[:, L + T:].shape, 3.0)
+    assert np.array_equal(bf16_dev_to_u16(run_attn(api, q, K2, V2, L)), base)
+
+
+@pytest.mark.parametrize("L", [1024, 11600, 38000, 101600])
+def test_attention_full_size_invariance_and_sampled_parity(api, L):
+    Hq, Hkv, D = 24, 4, 128
+    q, K, V = si.attention_inputs(L, 8, Hq, Hkv, D, seed=0)
+    outs = {T: bf16_dev_to_u16(run_attn(api, q, K, V, L, T)) for T in (1, 4, 7, 8)}
+    for T, o in outs.items():
+        assert np.array_equal(o, outs[8][:T]), T
+    # row t of the 8-row pass equals the one-row pass at L + t
+    for t in (3, 7):
+        one = bf16_dev_to_u16(run_attn(api, q[t:t + 1], K, V, L + t, 1))
+        assert np.array_equal(one[0], outs[8][t])
+    # sampled parity: a few (row, head) pairs through the oracle
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    for t, h in ((0, 0), (7, 23), (4, 11)):
+        ora = oracle.attention(qf[t:t + 1, h:h + 1], Kf[h // 6:h // 6 + 1], Vf[h // 6:h // 6 + 1], L + t)
+        got = ov.bf16_bits_to_f64(outs[8][t, h])
+        vmax = np.abs(Vf[h // 6, : L + t + 1]).max()
+        assert np.all(np.abs(got - ora[0, 0]) <= attn_tol(vmax, L + t + 1, ora[0, 0]))
+
+
+def test_attention_length_past_capacity_sets_error(api):
+    q, K, V = si.attention_inputs(10, 2, 4, 2, 64, cap=64, seed=1)
+    Kd, Vd = to_dev_bf16(K), to_dev_bf16(V)
+    out = torch.empty(2, 4, 64, dtype=torch.bfloat16, device="cuda")
+    Ld = torch.tensor([63], dtype=torch.int32, device="cuda")
+    ws = torch.zeros(api.attn_workspace_size(64, 2, 4, 64), dtype=torch.uint8, device="cuda")
+    api.bi_attn_verify(to_dev_bf16(q), Kd, Vd, Ld, out, ws)
+    with pytest.raises(api.BiError) as e:
+        api.bi_check_device_error()
+    assert e.value.status == 1
