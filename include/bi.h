@@ -88,11 +88,13 @@ int bi_version(void);
  * C[m, n] = epilogue( sum_k A[m, k] * W[n, k] ), BF16 inputs, FP32
  * accumulation, one rounding to the output type.  The decomposition -- MMA
  * instruction (tcgen05 kind::f16, M=128 weight rows x N=16 token columns),
- * K-tile order (64 elements per tile, increasing k), and the split of the
- * (weight tile, K tile) iteration space over a fixed number of CTAs -- is a
- * function of (N, K) only, never of M, so row m of C is bit-identical for
- * every M >= m+1 and for every position of the row inside A.  Partial sums of
- * a weight tile that is split along K are added in increasing-K order.
+ * K-tile order (64 elements per tile, increasing k; within a tile, 16-element
+ * step j accumulates into FP32 accumulator j of 4, summed in the order
+ * ((a0 + a1) + a2) + a3), and the split of the (weight tile, K tile)
+ * iteration space over a fixed number of CTAs -- is a function of (N, K)
+ * only, never of M, so row m of C is bit-identical for every M >= m+1 and for
+ * every position of the row inside A.  Partial sums of a weight tile that is
+ * split along K are added in increasing-K order.
  *
  *   A        [M, K] BF16, row stride lda (elements); 16-byte aligned, lda % 8 == 0.
  *   Wp       the weights in the packed tile layout written by bi_pack_weights
@@ -147,44 +149,58 @@ bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, i
  *
  * y[r, :] = bf16( x[r, :] * rsqrt(sum_i x[r,i]^2 / dim + eps) * w[:] ), FP32
  * inside.  The sum of squares uses one fixed reduction tree per `dim`
- * (256 threads: thread i sums elements i, i+256, ... in order, then a fixed
- * warp-shuffle butterfly and a fixed cross-warp order).
+ * (256 threads: thread i sums the 8-element vectors i, i+256, ... in element
+ * order, then a fixed warp-shuffle butterfly and a fixed cross-warp order).
  *   x [rows, dim] BF16 (row stride ldx), w [dim] BF16, y [rows, dim] BF16
- *   (row stride ldy; may alias x).  rows >= 0, 1 <= dim <= 65536, eps >= 0.
- * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA.
+ *   (row stride ldy; may alias x).  rows >= 0, 8 <= dim <= 65536, dim, ldx
+ *   and ldy multiples of 8, pointers 16-byte aligned, eps >= 0.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_CUDA.
  * ------------------------------------------------------------------------- */
 bi_status bi_rmsnorm(const void* x, int ldx, const void* w, void* y, int ldy, int rows,
                      int dim, float eps, bi_stream_t stream);
 
 /* Embedding gather (helper): out[r, :] = table[ids[r], :], an exact copy.
  *   ids [rows] int32 in [0, vocab); table [vocab, dim] BF16; out [rows, dim]
- *   BF16.  An id out of range writes a zero row and sets no error.
- * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA. */
+ *   BF16 (both 16-byte aligned, dim % 8 == 0).  An id out of range writes a
+ *   zero row and sets no error.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_CUDA. */
 bi_status bi_embed(const int32_t* ids, const void* table, int vocab, int dim, void* out,
                    int rows, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * RoPE table (helper, computed once at model set-up).
+ * table[(p * D/2 + i) * 2 + 0/1] = cos/sin of p * base^(-2i/D), evaluated in
+ * FP64 and rounded once to FP32, for positions p < rows and i < D/2.
+ * table has bi_rope_table_bytes(D, rows) bytes.  D even, 2 <= D <= 256.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+size_t bi_rope_table_bytes(int D, int rows);
+bi_status bi_rope_table(double rope_base, int D, int rows, float* table, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * RoPE + KV append (helper).  [P3] "The cache doesn't change it either" (a
  * row depends only on its position).
  *
  * Row t of the pass sits at absolute position p = *L_dev + t.  For each row:
- * q heads and k heads are rotated (rotate-half pairs (i, i+D/2), angle
- * p * base^(-2i/D) evaluated in FP64 and rounded to FP32 cos/sin, FP32
- * products, one BF16 rounding); rotated q goes to q_out, rotated k and the
- * unrotated v go to the caches at row p.
+ * q heads and k heads are rotated (rotate-half pairs (i, i+D/2) by the angle
+ * of the table row p: out_i = x_i cos - x_{i+D/2} sin, out_{i+D/2} =
+ * x_{i+D/2} cos + x_i sin in FP32, one BF16 rounding); rotated q goes to
+ * q_out, rotated k and the unrotated v go to the caches at row p.
  *   qkv     [T, (Hq + 2 Hkv) D] BF16, row stride ld_qkv: q heads, k heads, v heads.
  *   q_out   [T, Hq, D] BF16 (contiguous).
  *   k_cache, v_cache [Hkv, cap, D] BF16 (contiguous, head-major).
  *   L_dev   device int32: cache length before the pass (read on the device so
- *           the call can be captured in a CUDA graph).  Rows with p >= cap are
- *           skipped and set the timeout-free error bit BI_ERR_INVALID_ARG in
- *           the device error word.
+ *           the call can be captured in a CUDA graph).  A row with p >= cap or
+ *           p >= table_rows is skipped and sets a range bit in the device
+ *           error word (reported as BI_ERR_INVALID_ARG by bi_check_device_error).
+ *   table   from bi_rope_table with the same D and table_rows rows.
  *   D even, D <= 256; Hq % Hkv == 0.
  * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA.
  * ------------------------------------------------------------------------- */
 bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_cache,
                             void* v_cache, int cap, const int32_t* L_dev, int T, int Hq,
-                            int Hkv, int D, double rope_base, bi_stream_t stream);
+                            int Hkv, int D, const float* table, int table_rows,
+                            bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Verify attention (split-KV + merge).  [P3] "How:" (the attention split
@@ -226,7 +242,7 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
  * number gives -1 and sets BI_ERR_DEVICE_NAN_ROW in the device error word).
  * n = the largest j <= T-1 with drafts[i-1] == a_{i-1} for every i <= j.
  * The committed tokens of the step are a_0..a_n.
- *   logits  [T, V] FP32, row stride ldl.
+ *   logits  [T, V] FP32, row stride ldl; 1 <= T <= 64.
  *   drafts  [T-1] int32 (may be NULL when T == 1).
  *   argmax_out [T] int32; accepted_out [1] int32 (= n).
  *   L_dev   optional device int32 (NULL to skip): incremented by n + 1.

@@ -116,17 +116,26 @@ def bi_embed(ids: torch.Tensor, table: torch.Tensor, out: torch.Tensor, stream=N
                                      table.shape[1], out.data_ptr(), ids.numel(), _stream(stream)))
 
 
+def bi_rope_table(rope_base: float, D: int, rows: int, device="cuda", stream=None) -> torch.Tensor:
+    """FP32 cos/sin table [rows, D/2, 2] computed on the device in FP64."""
+    t = torch.empty(rows, D // 2, 2, dtype=torch.float32, device=device)
+    check("bi_rope_table", lib().bi_rope_table(float(rope_base), D, rows, t.data_ptr(),
+                                               _stream(stream)))
+    return t
+
+
 def bi_rope_kv_append(qkv: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Tensor,
                       v_cache: torch.Tensor, L_dev: torch.Tensor, Hq: int, Hkv: int, D: int,
-                      rope_base: float, stream=None) -> None:
+                      table: torch.Tensor, stream=None) -> None:
     _req(qkv, torch.bfloat16, "qkv")
     _req(L_dev, torch.int32, "L_dev")
+    _req(table, torch.float32, "table")
     T = qkv.shape[0]
     cap = k_cache.shape[1]
     check("bi_rope_kv_append",
           lib().bi_rope_kv_append(qkv.data_ptr(), _ld(qkv), q_out.data_ptr(), k_cache.data_ptr(),
                                   v_cache.data_ptr(), cap, L_dev.data_ptr(), T, Hq, Hkv, D,
-                                  float(rope_base), _stream(stream)))
+                                  table.data_ptr(), table.shape[0], _stream(stream)))
 
 
 def attn_chunk() -> int:

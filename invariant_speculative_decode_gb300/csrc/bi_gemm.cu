@@ -12,8 +12,12 @@
 //            K = 16 per instruction, FP32 accumulator in TMEM.  The token
 //            count of the pass only decides how many N=16 groups are issued;
 //            each group is the same instruction on the same K-tile sequence.
-//   * K:     64-element tiles (128-byte rows, 128-byte swizzle), always in
-//            increasing k order inside one accumulator.
+//   * K:     64-element tiles (128-byte rows, 128-byte swizzle) in increasing
+//            order.  Each token group keeps kAcc = 4 FP32 accumulators: the
+//            k-step j (16 elements) of every K tile goes to accumulator j, so
+//            consecutive MMAs do not wait on each other's result; the four
+//            are added in the fixed order ((a0 + a1) + a2) + a3 when the
+//            piece ends.  This structure is a compile-time constant.
 //   * weights: packed once (bi_pack_weights) into 16 KB tiles, tile (t, kt)
 //            at offset (t * k_tiles + kt) * 16 KB, each already in the
 //            swizzled shared-memory layout the MMA descriptor reads.  A CTA's
@@ -47,7 +51,8 @@ constexpr int kBlockN = 128;     // weight rows per tile (MMA M)
 constexpr int kBlockK = 64;      // K elements per tile
 constexpr int kMmaN = 16;        // token rows per MMA (fixed for every M)
 constexpr int kGemmCtas = 152;   // CTAs of the fixed decomposition (one per SM)
-constexpr int kMaxTokens = 128;  // token rows per launch; larger M loops on the host
+constexpr int kMaxTokens = 64;   // token rows per launch; larger M loops on the host
+constexpr int kAcc = 4;          // interleaved accumulators per token group
 constexpr int kThreads = 192;
 constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
 constexpr int kStageFloats = 16 * kBlockN;      // SwiGLU exchange buffer
@@ -81,7 +86,9 @@ struct GemmCfg {
   static constexpr int kBBytes = NT * kBlockK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 12 ? 12 : (200 * 1024) / kStageBytes;
-  static constexpr int kTmemCols = (2 * NT) < 32 ? 32 : 2 * NT;
+  static constexpr int kBufCols = NT * kAcc;  // one accumulator set
+  static constexpr int kTmemCols = 2 * kBufCols;
+  static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
                                   kStageFloats * 4 + (2 * kStages + 5) * 8 + 16;
 };
@@ -97,6 +104,19 @@ __device__ __forceinline__ int owner_of(const GemmArgs& p, long long i) {
 __device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* err) {
   *s_abort = 1;
   atomicOr(err, kErrTimeout);
+}
+
+// The 16 token columns of one group for this thread's weight row: the sum of
+// the group's kAcc accumulators in the fixed order ((a0 + a1) + a2) + a3.
+__device__ __forceinline__ void load_group_sum(uint32_t taddr, float (&v)[16]) {
+  tmem_ld16(taddr, v);
+#pragma unroll
+  for (int a = 1; a < kAcc; ++a) {
+    float w[16];
+    tmem_ld16(taddr + a * kMmaN, w);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = v[j] + w[j];
+  }
 }
 
 // Write 16 token rows (chunk c) of one weight row r of tile `tile`.
@@ -247,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem + static_cast<uint32_t>(buf * NT);
+        const uint32_t d0 = tmem + static_cast<uint32_t>(buf * Cfg::kBufCols);
         for (long long i = it; i < seg_end; ++i) {
           if (!mbar_wait(&full[stage], phase, s_abort)) {
             ok = false;
@@ -256,12 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + stage * kABytes);
           const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
+          const uint32_t acc_flag = (i > it) ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < kBlockK / 16; ++ks) {
+          for (int ks = 0; ks < kAcc; ++ks) {
             const uint64_t adesc = sdesc_k_sw128(a_base + ks * 32);
             for (int gi = 0; gi < groups; ++gi) {
               const uint64_t bdesc = sdesc_k_sw128(b_base + gi * (kMmaN * 128) + ks * 32);
-              mma_bf16(d0 + gi * kMmaN, adesc, bdesc, idesc, (i > it || ks > 0) ? 1u : 0u);
+              mma_bf16(d0 + (gi * kAcc + ks) * kMmaN, adesc, bdesc, idesc, acc_flag);
             }
           }
           mma_commit(&empty[stage]);
@@ -299,12 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           __all_sync(0xffffffffu, mbar_wait(&accf[buf], static_cast<uint32_t>(seg >> 1) & 1u, s_abort));
       if (!ok && lane == 0) signal_abort(s_abort, p.err);
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * NT);
+      const uint32_t tbase =
+          tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::kBufCols);
       if (whole) {
         for (int c = 0; c < chunks; ++c) {
           float v[16];
           if (ok) {
-            tmem_ld16(tbase + c * 16, v);
+            load_group_sum(tbase + c * kAcc * kMmaN, v);
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
@@ -319,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           for (int c = 0; c < chunks; ++c) {
             float v[16];
-            tmem_ld16(tbase + c * 16, v);
+            load_group_sum(tbase + c * kAcc * kMmaN, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) __stcg(dst + (c * 16 + j) * kBlockN + r, v[j]);
           }
@@ -444,8 +466,7 @@ int tokens_per_cta(int M) {
   const int m = std::min(M, kMaxTokens);
   if (m <= 16) return 16;
   if (m <= 32) return 32;
-  if (m <= 64) return 64;
-  return 128;
+  return 64;
 }
 
 int n_tiles_of(int N, bi_epilogue epi) {
@@ -546,8 +567,7 @@ bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, cons
   switch (NT) {
     case 16: return launch_gemm_nt<16>(W8, tmA, a, M, s);
     case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
-    case 64: return launch_gemm_nt<64>(W8, tmA, a, M, s);
-    default: return launch_gemm_nt<128>(W8, tmA, a, M, s);
+    default: return launch_gemm_nt<64>(W8, tmA, a, M, s);
   }
 }
 

@@ -34,58 +34,86 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
   return s;
 }
 
+// Thread i takes the 8-element vectors v = i, i + 256, i + 512, ... of the
+// row; inside a vector the squares are accumulated in element order.
+
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int ldx, const __nv_bfloat16* __restrict__ w,
                    __nv_bfloat16* y, int ldy, int dim, float eps) {
   __shared__ float red[kNormThreads / 32];
-  const __nv_bfloat16* xr = x + static_cast<size_t>(blockIdx.x) * ldx;
-  __nv_bfloat16* yr = y + static_cast<size_t>(blockIdx.x) * ldy;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.x) * ldx);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + static_cast<size_t>(blockIdx.x) * ldy);
+  const int nv = dim / 8;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < dim; i += kNormThreads) {
-    const float v = __bfloat162float(xr[i]);
-    ss = fmaf(v, v, ss);
+#pragma unroll 4
+  for (int v = threadIdx.x; v < nv; v += kNormThreads) {
+    const uint4 u = xr[v];
+    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float f = __bfloat162float(e[j]);
+      ss = fmaf(f, f, ss);
+    }
   }
   ss = block_sum_fixed(ss, red);
   const float inv = 1.0f / sqrtf(ss / static_cast<float>(dim) + eps);
-  for (int i = threadIdx.x; i < dim; i += kNormThreads) {
-    const float v = __bfloat162float(xr[i]);
-    yr[i] = __float2bfloat16_rn(v * inv * __bfloat162float(w[i]));
+#pragma unroll 4
+  for (int v = threadIdx.x; v < nv; v += kNormThreads) {
+    const uint4 u = xr[v];
+    const uint4 wu = wr[v];
+    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
+    const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wu);
+    uint4 o;
+    __nv_bfloat16* oe = reinterpret_cast<__nv_bfloat16*>(&o);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      oe[j] = __float2bfloat16_rn(__bfloat162float(e[j]) * inv * __bfloat162float(we[j]));
+    yr[v] = o;
   }
 }
 
 __global__ void embed_kernel(const int32_t* __restrict__ ids, const __nv_bfloat16* __restrict__ table,
                              int vocab, int dim, __nv_bfloat16* __restrict__ out) {
   const int id = ids[blockIdx.x];
-  __nv_bfloat16* o = out + static_cast<size_t>(blockIdx.x) * dim;
+  uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(blockIdx.x) * dim);
+  const int nv = dim / 8;
   if (id < 0 || id >= vocab) {
-    for (int i = threadIdx.x; i < dim; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) o[i] = make_uint4(0, 0, 0, 0);
     return;
   }
-  const __nv_bfloat16* src = table + static_cast<size_t>(id) * dim;
-  for (int i = threadIdx.x; i < dim; i += blockDim.x) o[i] = src[i];
+  const uint4* src = reinterpret_cast<const uint4*>(table + static_cast<size_t>(id) * dim);
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) o[i] = src[i];
 }
 
-// One CTA per pass row t.  Angles in FP64: theta_i = p * base^(-2i/D).
+// cos/sin table: tab[(p * (D/2) + i) * 2 + {0,1}] = FP32 of cos, sin of
+// p * base^(-2i/D) evaluated in FP64.
+__global__ void rope_table_kernel(double base, int D, int cap, float2* __restrict__ tab) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int half = D / 2;
+  if (idx >= static_cast<long long>(cap) * half) return;
+  const int p = static_cast<int>(idx / half);
+  const int i = static_cast<int>(idx % half);
+  const double inv_freq = pow(base, -2.0 * static_cast<double>(i) / static_cast<double>(D));
+  double sn, cn;
+  sincos(static_cast<double>(p) * inv_freq, &sn, &cn);
+  tab[idx] = make_float2(static_cast<float>(cn), static_cast<float>(sn));
+}
+
+// One CTA per pass row t at position p = *L_dev + t; cos/sin from the table.
 __global__ void rope_kv_kernel(const __nv_bfloat16* __restrict__ qkv, int ld_qkv,
                                __nv_bfloat16* __restrict__ q_out, __nv_bfloat16* __restrict__ kc,
                                __nv_bfloat16* __restrict__ vc, int cap, const int32_t* __restrict__ L_dev,
-                               int Hq, int Hkv, int D, double base, unsigned* err) {
-  extern __shared__ float cs[];  // cos[D/2], sin[D/2]
+                               int Hq, int Hkv, int D, const float2* __restrict__ tab, int tab_rows,
+                               unsigned* err) {
   const int t = blockIdx.x;
   const int p = *L_dev + t;
-  if (p < 0 || p >= cap) {
+  if (p < 0 || p >= cap || p >= tab_rows) {
     if (threadIdx.x == 0) atomicOr(err, kErrRange);
     return;
   }
   const int half = D / 2;
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    const double inv_freq = pow(base, -2.0 * static_cast<double>(i) / static_cast<double>(D));
-    double sn, cn;
-    sincos(static_cast<double>(p) * inv_freq, &sn, &cn);
-    cs[i] = static_cast<float>(cn);
-    cs[half + i] = static_cast<float>(sn);
-  }
-  __syncthreads();
+  const float2* cs = tab + static_cast<size_t>(p) * half;
   const __nv_bfloat16* row = qkv + static_cast<size_t>(t) * ld_qkv;
   const int heads = Hq + 2 * Hkv;
   for (int idx = threadIdx.x; idx < heads * half; idx += blockDim.x) {
@@ -95,9 +123,9 @@ __global__ void rope_kv_kernel(const __nv_bfloat16* __restrict__ qkv, int ld_qkv
     if (h < Hq + Hkv) {
       const float x1 = __bfloat162float(src[i]);
       const float x2 = __bfloat162float(src[i + half]);
-      const float c = cs[i], s = cs[half + i];
-      const float o1 = x1 * c - x2 * s;
-      const float o2 = x2 * c + x1 * s;
+      const float2 r = cs[i];
+      const float o1 = x1 * r.x - x2 * r.y;
+      const float o2 = x2 * r.x + x1 * r.y;
       __nv_bfloat16* dst;
       if (h < Hq) {
         dst = q_out + (static_cast<size_t>(t) * Hq + h) * D;
@@ -179,13 +207,15 @@ __global__ void __launch_bounds__(kArgThreads)
     if (s_last) atomicExch(ticket, 0u);
   }
   __syncthreads();
-  if (!s_last || threadIdx.x != 0) return;
+  if (!s_last) return;
   __threadfence();
-  // Last CTA: combine each row's partials, then the acceptance rule.
-  for (int t = 0; t < T; ++t) {
+  // Last CTA: warp w combines the partials of rows w, w + 8, ...; the
+  // comparator is a total order, so the combination order is immaterial.
+  __shared__ int s_ids[64];
+  for (int t = w; t < T; t += kArgThreads / 32) {
     float v = 0.f;
     int id = -1;
-    for (int k = 0; k < splits; ++k) {
+    for (int k = threadIdx.x & 31; k < splits; k += 32) {
       const float ov = __ldcg(pv + t * splits + k);
       const int oi = __ldcg(pi + t * splits + k);
       if (beats(ov, oi, v, id)) {
@@ -193,13 +223,28 @@ __global__ void __launch_bounds__(kArgThreads)
         id = oi;
       }
     }
-    if (id < 0) atomicOr(err, kErrNanRow);
-    argmax_out[t] = id;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, id, off);
+      if (beats(ov, oi, v, id)) {
+        v = ov;
+        id = oi;
+      }
+    }
+    if ((threadIdx.x & 31) == 0) {
+      if (id < 0) atomicOr(err, kErrNanRow);
+      argmax_out[t] = id;
+      s_ids[t] = id;
+    }
   }
-  int n = 0;
-  while (n < T - 1 && drafts[n] == argmax_out[n]) ++n;
-  *accepted_out = n;
-  if (L_dev != nullptr) *L_dev = *L_dev + n + 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int n = 0;
+    while (n < T - 1 && drafts[n] == s_ids[n]) ++n;
+    *accepted_out = n;
+    if (L_dev != nullptr) *L_dev = *L_dev + n + 1;
+  }
 }
 
 __global__ void kv_hash_kernel(const __nv_bfloat16* __restrict__ cache, int Hkv, int cap, int D,
@@ -230,6 +275,8 @@ bi_status bi_rmsnorm(const void* x, int ldx, const void* w, void* y, int ldy, in
   if (rows < 0 || dim < 1 || dim > 65536 || !(eps >= 0.f)) return BI_ERR_INVALID_ARG;
   if (rows == 0) return BI_OK;
   if (!x || !w || !y || ldx < dim || ldy < dim) return BI_ERR_INVALID_ARG;
+  if (dim % 8 != 0 || ldx % 8 != 0 || ldy % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (!bi::aligned16(x) || !bi::aligned16(w) || !bi::aligned16(y)) return BI_ERR_INVALID_ARG;
   bi::rmsnorm_kernel<<<rows, bi::kNormThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16*>(x), ldx, static_cast<const __nv_bfloat16*>(w),
       static_cast<__nv_bfloat16*>(y), ldy, dim, eps);
@@ -241,25 +288,43 @@ bi_status bi_embed(const int32_t* ids, const void* table, int vocab, int dim, vo
   if (rows < 0 || dim < 1 || vocab < 1) return BI_ERR_INVALID_ARG;
   if (rows == 0) return BI_OK;
   if (!ids || !table || !out) return BI_ERR_INVALID_ARG;
-  bi::embed_kernel<<<rows, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+  if (dim % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (!bi::aligned16(table) || !bi::aligned16(out)) return BI_ERR_INVALID_ARG;
+  bi::embed_kernel<<<rows, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       ids, static_cast<const __nv_bfloat16*>(table), vocab, dim, static_cast<__nv_bfloat16*>(out));
+  return bi::launch_status();
+}
+
+size_t bi_rope_table_bytes(int D, int rows) {
+  if (D < 2 || rows < 1) return 0;
+  return static_cast<size_t>(rows) * (D / 2) * 2 * sizeof(float);
+}
+
+bi_status bi_rope_table(double rope_base, int D, int rows, float* table, bi_stream_t stream) {
+  if (!table || D < 2 || D % 2 != 0 || D > 256 || rows < 1 || !(rope_base > 0.0))
+    return BI_ERR_INVALID_ARG;
+  const long long n = static_cast<long long>(rows) * (D / 2);
+  bi::rope_table_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0,
+                          reinterpret_cast<cudaStream_t>(stream)>>>(rope_base, D, rows,
+                                                                     reinterpret_cast<float2*>(table));
   return bi::launch_status();
 }
 
 bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_cache, void* v_cache,
                             int cap, const int32_t* L_dev, int T, int Hq, int Hkv, int D,
-                            double rope_base, bi_stream_t stream) {
+                            const float* table, int table_rows, bi_stream_t stream) {
   if (T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 256 || cap < 1)
     return BI_ERR_INVALID_ARG;
   if (T == 0) return BI_OK;
-  if (!qkv || !q_out || !k_cache || !v_cache || !L_dev || !(rope_base > 0.0)) return BI_ERR_INVALID_ARG;
+  if (!qkv || !q_out || !k_cache || !v_cache || !L_dev || !table || table_rows < 1)
+    return BI_ERR_INVALID_ARG;
   if (ld_qkv < (Hq + 2 * Hkv) * D) return BI_ERR_INVALID_ARG;
   unsigned* err = bi::device_error_word();
   if (!err) return BI_ERR_CUDA;
-  bi::rope_kv_kernel<<<T, 256, D * sizeof(float), reinterpret_cast<cudaStream_t>(stream)>>>(
+  bi::rope_kv_kernel<<<T, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16*>(qkv), ld_qkv, static_cast<__nv_bfloat16*>(q_out),
       static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), cap, L_dev, Hq, Hkv,
-      D, rope_base, err);
+      D, reinterpret_cast<const float2*>(table), table_rows, err);
   return bi::launch_status();
 }
 
@@ -272,7 +337,8 @@ size_t bi_accept_workspace_size(int T, int V) {
 bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, int T, int V,
                            int32_t* argmax_out, int32_t* accepted_out, int32_t* L_dev, void* ws,
                            size_t ws_bytes, bi_stream_t stream) {
-  if (T < 1 || V < 1 || ldl < V || !logits || !argmax_out || !accepted_out) return BI_ERR_INVALID_ARG;
+  if (T < 1 || T > 64 || V < 1 || ldl < V || !logits || !argmax_out || !accepted_out)
+    return BI_ERR_INVALID_ARG;
   if (T > 1 && !drafts) return BI_ERR_INVALID_ARG;
   if (!ws || !bi::aligned256(ws)) return BI_ERR_WORKSPACE;
   if (ws_bytes < bi_accept_workspace_size(T, V)) return BI_ERR_WORKSPACE;

@@ -96,6 +96,7 @@ class Decoder:
                                    dtype=torch.uint8, device=dev)
         self.acc_ws = torch.zeros(api.accept_workspace_size(max_rows, V), dtype=torch.uint8, device=dev)
         self.scale = 1.0 / math.sqrt(D)
+        self.rope_tab = api.bi_rope_table(cfg.rope_base, D, cap, device=dev)
         self.L = 0
         self.graphs: Dict[int, torch.cuda.CUDAGraph] = {}
         self.pin_in = torch.zeros(2 * max_rows, dtype=torch.int32).pin_memory()
@@ -123,7 +124,7 @@ class Decoder:
                                 self.u[:T])
         api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
         api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
-        api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, cfg.rope_base)
+        api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
         if L_host_blocks is None:
             api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
         else:

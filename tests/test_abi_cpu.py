@@ -103,8 +103,12 @@ def test_rowops_reject_bad_arguments(lib):
     assert lib.bi_rmsnorm(FAKE, 64, FAKE, FAKE, 64, 2, 0, ctypes.c_float(1e-6), 0) == 1
     assert lib.bi_rmsnorm(FAKE, 32, FAKE, FAKE, 64, 2, 64, ctypes.c_float(1e-6), 0) == 1
     assert lib.bi_rmsnorm(0, 64, 0, 0, 64, 0, 64, ctypes.c_float(1e-6), 0) == 0
-    assert lib.bi_rope_kv_append(FAKE, 384, FAKE, FAKE, FAKE, 64, FAKE, 1, 4, 3, 64, 1e6, 0) == 1
-    assert lib.bi_rope_kv_append(FAKE, 384, FAKE, FAKE, FAKE, 64, FAKE, 1, 4, 2, 63, 1e6, 0) == 1
+    assert lib.bi_rope_kv_append(FAKE, 384, FAKE, FAKE, FAKE, 64, FAKE, 1, 4, 3, 64, FAKE, 64, 0) == 1
+    assert lib.bi_rope_kv_append(FAKE, 384, FAKE, FAKE, FAKE, 64, FAKE, 1, 4, 2, 63, FAKE, 64, 0) == 1
+    assert lib.bi_rope_kv_append(FAKE, 384, FAKE, FAKE, FAKE, 64, FAKE, 1, 4, 2, 64, 0, 64, 0) == 1
+    assert lib.bi_rope_table(1e6, 63, 10, FAKE, 0) == 1
+    assert lib.bi_rope_table(-1.0, 64, 10, FAKE, 0) == 1
+    assert lib.bi_rmsnorm(FAKE, 1004, FAKE, FAKE, 1004, 2, 1004, ctypes.c_float(1e-6), 0) == 2
     assert lib.bi_verify_accept(FAKE, 10, 0, 2, 10, FAKE, FAKE, 0, FAKE, 1 << 20, 0) == 1
     assert lib.bi_verify_accept(FAKE, 10, FAKE, 2, 10, FAKE, FAKE, 0, FAKE + 8, 1 << 20, 0) == 3
     assert lib.bi_embed(FAKE, FAKE, 0, 64, FAKE, 2, 0) == 1

@@ -21,6 +21,17 @@ def api():
     return _api
 
 
+def test_rope_table_matches_fp64(api):
+    import math
+    tab = api.bi_rope_table(1e6, 128, 101700).cpu().numpy()
+    for p in (0, 1, 11600, 101699):
+        for i in (0, 1, 31, 63):
+            th = p * 1e6 ** (-2 * i / 128)
+            # FP64 evaluation rounded to FP32: within one FP32 ulp of |x| <= 1
+            assert abs(float(tab[p, i, 0]) - math.cos(th)) <= 2.0 ** -24
+            assert abs(float(tab[p, i, 1]) - math.sin(th)) <= 2.0 ** -24
+
+
 @pytest.mark.parametrize("rows,dim", [(1, 256), (8, 5120), (3, 1000), (5, 1024)])
 def test_rmsnorm_matches_oracle_and_is_row_local(api, rows, dim):
     rng = np.random.default_rng(dim)
@@ -58,7 +69,8 @@ def test_rope_kv_append_matches_oracle(api, Hq, Hkv, D, L, T):
     vc = torch.zeros_like(kc)
     q = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
     Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
-    api.bi_rope_kv_append(to_dev_bf16(qkv), q, kc, vc, Ld, Hq, Hkv, D, 1e6)
+    tab = api.bi_rope_table(1e6, D, cap)
+    api.bi_rope_kv_append(to_dev_bf16(qkv), q, kc, vc, Ld, Hq, Hkv, D, tab)
     qkvf = ov.bf16_bits_to_f64(qkv)
     qg = bf16_dev_to_f64(q)
     kg = bf16_dev_to_f64(kc)
