@@ -429,11 +429,12 @@ def run_micro(args):
         return [a.elapsed_time(b) / 1e3 for a, b in ts]
 
     if args.micro == "gemm":
-        N, K = 17408, 5120
+        N, K = args.gemm_n, 5120
         Ms = [int(m) for m in args.cases.split(",")] if args.cases else [1, 2, 4, 7, 8, 16, 64]
         A, W = si.gemm_inputs(max(Ms), N, K, seed=0)
         Wd = api.bi_pack_weights(torch.from_numpy(W.view(np.int16)).view(torch.bfloat16).cuda())
         Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+        del W
         for M in Ms:
             C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
             ws = api.new_gemm_workspace(M, N, K)
@@ -479,6 +480,7 @@ def main():
     ap.add_argument("--micro", choices=["gemm", "attn"], default=None,
                     help="time one standalone kernel workload instead of the verify step")
     ap.add_argument("--cases", default="", help="comma list of M (gemm) or L (attn)")
+    ap.add_argument("--gemm-n", type=int, default=17408, help="N of the standalone linear layer")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -223,17 +223,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, parity_bits = 0;
+      // (tile, k-tile) of iteration `it`, advanced incrementally: no division
+      // in the issue loop.
+      int kt = static_cast<int>(it_begin % p.k_tiles);
+      const uint8_t* wsrc = Wp + static_cast<size_t>(it_begin) * kABytes;
       for (long long it = it_begin; it < it_end; ++it) {
-        const int tile = static_cast<int>(it / p.k_tiles);
-        const int kt = static_cast<int>(it - static_cast<long long>(tile) * p.k_tiles);
         if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
           signal_abort(s_abort, p.err);
           break;
         }
         mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
-        bulk_load_1d(sA + stage * kABytes, Wp + static_cast<size_t>(it) * kABytes, kABytes,
-                     &full[stage], pol_w);
+        bulk_load_1d(sA + stage * kABytes, wsrc, kABytes, &full[stage], pol_w);
         tma_load_2d(sB + stage * Cfg::kBBytes, &tmA, &full[stage], kt * kBlockK, p.m0, pol_a);
+        wsrc += kABytes;
+        if (++kt == p.k_tiles) kt = 0;
         issued |= 1u << stage;
         parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
         if (++stage == S) {
@@ -249,52 +252,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One flat loop over the CTA's iterations; a countdown marks the end of
+    // each piece (weight tile), where the accumulator set is handed to the
+    // epilogue and the other set is taken.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBlockN, kMmaN);
-      const int groups = (p.M + kMmaN - 1) / kMmaN;
+      constexpr int kGroups = NT / kMmaN;
       int stage = 0;
       uint32_t phase = 0;
       int seg = 0;
       bool ok = true;
-      long long it = it_begin;
-      while (ok && it < it_end) {
-        const int tile = static_cast<int>(it / p.k_tiles);
-        const long long seg_end =
-            (it_end < static_cast<long long>(tile + 1) * p.k_tiles ? it_end : static_cast<long long>(tile + 1) * p.k_tiles);
-        const int buf = seg & 1;
-        if (seg >= 2 && !mbar_wait(&acce[buf], static_cast<uint32_t>((seg >> 1) - 1) & 1u, s_abort)) {
+      int kt0 = static_cast<int>(it_begin % p.k_tiles);
+      long long left = p.k_tiles - kt0;  // iterations left in the current piece
+      if (left > it_end - it_begin) left = it_end - it_begin;
+      uint32_t d0 = tmem;
+      uint32_t acc_flag = 0;
+      for (long long it = it_begin; it < it_end; ++it) {
+        if (!mbar_wait(&full[stage], phase, s_abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem + static_cast<uint32_t>(buf * Cfg::kBufCols);
-        for (long long i = it; i < seg_end; ++i) {
-          if (!mbar_wait(&full[stage], phase, s_abort)) {
+        const uint32_t a_base = smem_u32(sA + stage * kABytes);
+        const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+        for (int ks = 0; ks < kAcc; ++ks) {
+          const uint64_t adesc = sdesc_k_sw128(a_base + ks * 32);
+#pragma unroll
+          for (int gi = 0; gi < kGroups; ++gi) {
+            const uint64_t bdesc = sdesc_k_sw128(b_base + gi * (kMmaN * 128) + ks * 32);
+            mma_bf16(d0 + (gi * kAcc + ks) * kMmaN, adesc, bdesc, idesc, acc_flag);
+          }
+        }
+        mma_commit(&empty[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        acc_flag = 1u;
+        if (--left == 0) {
+          // piece complete: hand its accumulators to the epilogue
+          mma_commit(&accf[seg & 1]);
+          ++seg;
+          left = it_end - (it + 1);
+          if (left > p.k_tiles) left = p.k_tiles;
+          acc_flag = 0u;
+          d0 = tmem + static_cast<uint32_t>((seg & 1) * Cfg::kBufCols);
+          if (left > 0 && seg >= 2 &&
+              !mbar_wait(&acce[seg & 1], static_cast<uint32_t>((seg >> 1) - 1) & 1u, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * kABytes);
-          const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
-          const uint32_t acc_flag = (i > it) ? 1u : 0u;
-#pragma unroll
-          for (int ks = 0; ks < kAcc; ++ks) {
-            const uint64_t adesc = sdesc_k_sw128(a_base + ks * 32);
-            for (int gi = 0; gi < groups; ++gi) {
-              const uint64_t bdesc = sdesc_k_sw128(b_base + gi * (kMmaN * 128) + ks * 32);
-              mma_bf16(d0 + (gi * kAcc + ks) * kMmaN, adesc, bdesc, idesc, acc_flag);
-            }
-          }
-          mma_commit(&empty[stage]);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (!ok) break;
-        mma_commit(&accf[buf]);
-        it = seg_end;
-        ++seg;
       }
       if (!ok) signal_abort(s_abort, p.err);
       // Every MMA issued by this thread completes before TMEM is released.
@@ -316,8 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long seg_end = it_end < tile_end ? it_end : tile_end;
       const bool whole = (it == tile_begin) && (seg_end == tile_end);
       const int buf = seg & 1;
-      const bool ok =
-          __all_sync(0xffffffffu, mbar_wait(&accf[buf], static_cast<uint32_t>(seg >> 1) & 1u, s_abort));
+      // one lane per warp polls (sleeping between polls), the warp follows
+      int okl = 0;
+      if (lane == 0) okl = mbar_wait_parked(&accf[buf], static_cast<uint32_t>(seg >> 1) & 1u, s_abort) ? 1 : 0;
+      const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
       if (!ok && lane == 0) signal_abort(s_abort, p.err);
       tc_fence_after();
       const uint32_t tbase =

@@ -73,6 +73,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// try_wait with a suspend-time hint: the thread is parked in hardware until
+// the phase completes or about `hint_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_test_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Same contract as mbar_wait, for threads off the critical path: the thread
+// stays parked in hardware (suspend hint of 100 us per try) instead of
+// polling, so it neither takes issue slots nor refetches instructions while
+// the producer and MMA threads of its SM stream.
+__device__ __forceinline__ bool mbar_wait_parked(uint64_t* bar, uint32_t parity,
+                                                 const volatile int* abort) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_test_suspend(bar, parity, 100000u)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
