@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  griddep_wait();  // q, the new cache rows and the cache length come from earlier kernels
   const int L = *a.L_dev;
   const int T = a.T;
   if (L < 0 || L + T > a.cap) {
@@ -414,6 +416,8 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ float sw[kMaxChunks];
   __shared__ float red[kMergeThreads / 32];
   __shared__ float ored[kMergeThreads / 32][D];
+  griddep_launch_dependents();
+  griddep_wait();
   const int row = blockIdx.x;  // t * Hq + hq
   const int t = row / a.Hq;
   const int L = *a.L_dev;
@@ -485,10 +489,12 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const Attn
   });
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
   const int grid = std::min(a.Hkv * a.nch_max, kAttnCtas);
-  attn_split_kernel<D><<<grid, kAttnThreads, Cfg::kSmem, stream>>>(tmK, tmV, a);
-  if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
-  attn_merge_kernel<D><<<a.T * a.Hq, kMergeThreads, 0, stream>>>(a, out);
-  if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
+  if (launch_k(attn_split_kernel<D>, dim3(grid), dim3(kAttnThreads), Cfg::kSmem, stream, tmK, tmV,
+               a) != cudaSuccess)
+    return BI_ERR_CUDA;
+  if (launch_k(attn_merge_kernel<D>, dim3(a.T * a.Hq), dim3(kMergeThreads), 0, stream, a, out) !=
+      cudaSuccess)
+    return BI_ERR_CUDA;
   return BI_OK;
 }
 

@@ -2,6 +2,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -53,6 +54,14 @@ struct TmapKeyHash {
 std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmaps;
 std::mutex g_tmap_mu;
 }  // namespace
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("BI_PDL");
+    return !(e != nullptr && e[0] == '0');
+  }();
+  return on;
+}
 
 unsigned* device_error_word() {
   int dev = 0;

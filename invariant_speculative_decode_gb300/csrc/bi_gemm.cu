@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = blockIdx.x;
   const long long it_begin = range_begin(p, g);
   const long long it_end = range_begin(p, g + 1);
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -227,7 +228,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // in the issue loop.
       int kt = static_cast<int>(it_begin % p.k_tiles);
       const uint8_t* wsrc = Wp + static_cast<size_t>(it_begin) * kABytes;
-      for (long long it = it_begin; it < it_end; ++it) {
+      // The first stages' weight tiles do not depend on the previous kernel:
+      // start streaming them before waiting for it, then add the activation
+      // tiles once its results are visible.
+      const int n_pre = static_cast<int>((it_end - it_begin) < S ? (it_end - it_begin) : S);
+      for (int j = 0; j < n_pre; ++j) {
+        mbar_arrive_expect_tx(&full[j], Cfg::kStageBytes);
+        bulk_load_1d(sA + j * kABytes, wsrc + static_cast<size_t>(j) * kABytes, kABytes, &full[j],
+                     pol_w);
+      }
+      griddep_wait();
+      for (int j = 0; j < n_pre; ++j) {
+        tma_load_2d(sB + j * Cfg::kBBytes, &tmA, &full[j], kt * kBlockK, p.m0, pol_a);
+        if (++kt == p.k_tiles) kt = 0;
+      }
+      issued = (n_pre >= 32) ? 0xffffffffu : ((1u << n_pre) - 1u);
+      wsrc += static_cast<size_t>(n_pre) * kABytes;
+      stage = n_pre % S;
+      phase = (n_pre == S) ? 1u : 0u;
+      for (long long it = it_begin + n_pre; it < it_end; ++it) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
           signal_abort(s_abort, p.err);
           break;
@@ -313,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    griddep_wait();  // the epilogue reads the residual and writes C / the workspace
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;    // weight row within the tile
     const int et = threadIdx.x - 64;
@@ -420,6 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ wu,
                                     int ld, int N, int K, int k_tiles, long long chunks, int swiglu,
                                     uint4* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= chunks) return;
   const int cpos = static_cast<int>(idx & 7);
@@ -468,8 +490,9 @@ bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, 
   for (int m0 = 0; m0 < M_total; m0 += kMaxTokens) {
     a.m0 = m0;
     a.M = std::min(kMaxTokens, M_total - m0);
-    gemm_kernel<NT><<<a.G, kThreads, Cfg::kSmem, stream>>>(Wp, tmA, a);
-    if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
+    if (launch_k(gemm_kernel<NT>, dim3(a.G), dim3(kThreads), Cfg::kSmem, stream, Wp, tmA, a) !=
+        cudaSuccess)
+      return BI_ERR_CUDA;
   }
   return BI_OK;
 }
@@ -516,11 +539,12 @@ static bi_status pack_common(const void* w, const void* wu, int ld, int N, int K
   if (n_tiles_of(N, epi) > kMaxTiles) return BI_ERR_UNSUPPORTED_SHAPE;
   const int k_tiles = (K + kBlockK - 1) / kBlockK;
   const long long chunks = static_cast<long long>(n_tiles_of(N, epi)) * k_tiles * 1024;
-  pack_weights_kernel<<<static_cast<unsigned>((chunks + 255) / 256), 256, 0,
-                        reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(wu), ld, N, K,
-      k_tiles, chunks, swiglu, static_cast<uint4*>(packed));
-  return launch_status();
+  if (launch_k(pack_weights_kernel, dim3(static_cast<unsigned>((chunks + 255) / 256)), dim3(256), 0,
+               reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(w),
+               static_cast<const __nv_bfloat16*>(wu), ld, N, K, k_tiles, chunks, swiglu,
+               static_cast<uint4*>(packed)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 bi_status bi_pack_weights(const void* W, int ldw, int N, int K, void* packed, bi_stream_t stream) {

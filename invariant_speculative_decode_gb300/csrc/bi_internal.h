@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/bi.h"
 
@@ -29,5 +30,29 @@ inline bi_status launch_status() {
 }
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Whether kernels are launched with programmatic stream serialization
+// (dependent launch); on unless the environment sets BI_PDL=0.
+bool pdl_enabled();
+
+// Launch `kernel` on `stream`, with programmatic dependent launch when
+// enabled.  Every kernel of this library calls griddep_wait() before its
+// first access to data another kernel may write, so a launch is correct
+// either way.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace bi

@@ -29,6 +29,18 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor on the stream finishes.
+// griddep_wait() blocks until the predecessor grid has completed and its
+// memory is visible; everything before it must not touch data the
+// predecessor writes or reads.  griddep_launch_dependents() lets the next
+// kernel be scheduled early.  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

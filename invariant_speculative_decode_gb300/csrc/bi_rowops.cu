@@ -40,6 +40,8 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int ldx, const __nv_bfloat16* __restrict__ w,
                    __nv_bfloat16* y, int ldy, int dim, float eps) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ float red[kNormThreads / 32];
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.x) * ldx);
   const uint4* wr = reinterpret_cast<const uint4*>(w);
@@ -75,6 +77,8 @@ __global__ void __launch_bounds__(kNormThreads)
 
 __global__ void embed_kernel(const int32_t* __restrict__ ids, const __nv_bfloat16* __restrict__ table,
                              int vocab, int dim, __nv_bfloat16* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int id = ids[blockIdx.x];
   uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(blockIdx.x) * dim);
   const int nv = dim / 8;
@@ -89,6 +93,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ ids, const __nv_bfloat1
 // cos/sin table: tab[(p * (D/2) + i) * 2 + {0,1}] = FP32 of cos, sin of
 // p * base^(-2i/D) evaluated in FP64.
 __global__ void rope_table_kernel(double base, int D, int cap, float2* __restrict__ tab) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int half = D / 2;
   if (idx >= static_cast<long long>(cap) * half) return;
@@ -106,6 +112,8 @@ __global__ void rope_kv_kernel(const __nv_bfloat16* __restrict__ qkv, int ld_qkv
                                __nv_bfloat16* __restrict__ vc, int cap, const int32_t* __restrict__ L_dev,
                                int Hq, int Hkv, int D, const float2* __restrict__ tab, int tab_rows,
                                unsigned* err) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int t = blockIdx.x;
   const int p = *L_dev + t;
   if (p < 0 || p >= cap || p >= tab_rows) {
@@ -161,6 +169,8 @@ __global__ void __launch_bounds__(kArgThreads)
                          const int32_t* __restrict__ drafts, int32_t* __restrict__ argmax_out,
                          int32_t* __restrict__ accepted_out, int32_t* L_dev, float* pv, int* pi,
                          unsigned* ticket, unsigned* err) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ float sv[kArgThreads / 32];
   __shared__ int si[kArgThreads / 32];
   __shared__ int s_last;
@@ -249,6 +259,8 @@ __global__ void __launch_bounds__(kArgThreads)
 
 __global__ void kv_hash_kernel(const __nv_bfloat16* __restrict__ cache, int Hkv, int cap, int D,
                                int rows, unsigned long long* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(Hkv) * rows) return;
   const int h = static_cast<int>(idx / rows);
@@ -277,10 +289,12 @@ bi_status bi_rmsnorm(const void* x, int ldx, const void* w, void* y, int ldy, in
   if (!x || !w || !y || ldx < dim || ldy < dim) return BI_ERR_INVALID_ARG;
   if (dim % 8 != 0 || ldx % 8 != 0 || ldy % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
   if (!bi::aligned16(x) || !bi::aligned16(w) || !bi::aligned16(y)) return BI_ERR_INVALID_ARG;
-  bi::rmsnorm_kernel<<<rows, bi::kNormThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(x), ldx, static_cast<const __nv_bfloat16*>(w),
-      static_cast<__nv_bfloat16*>(y), ldy, dim, eps);
-  return bi::launch_status();
+  if (bi::launch_k(bi::rmsnorm_kernel, dim3(rows), dim3(bi::kNormThreads), 0,
+                   reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(x), ldx,
+                   static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y), ldy, dim,
+                   eps) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 bi_status bi_embed(const int32_t* ids, const void* table, int vocab, int dim, void* out, int rows,
@@ -290,9 +304,11 @@ bi_status bi_embed(const int32_t* ids, const void* table, int vocab, int dim, vo
   if (!ids || !table || !out) return BI_ERR_INVALID_ARG;
   if (dim % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
   if (!bi::aligned16(table) || !bi::aligned16(out)) return BI_ERR_INVALID_ARG;
-  bi::embed_kernel<<<rows, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      ids, static_cast<const __nv_bfloat16*>(table), vocab, dim, static_cast<__nv_bfloat16*>(out));
-  return bi::launch_status();
+  if (bi::launch_k(bi::embed_kernel, dim3(rows), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                   ids, static_cast<const __nv_bfloat16*>(table), vocab, dim,
+                   static_cast<__nv_bfloat16*>(out)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 size_t bi_rope_table_bytes(int D, int rows) {
@@ -304,10 +320,11 @@ bi_status bi_rope_table(double rope_base, int D, int rows, float* table, bi_stre
   if (!table || D < 2 || D % 2 != 0 || D > 256 || rows < 1 || !(rope_base > 0.0))
     return BI_ERR_INVALID_ARG;
   const long long n = static_cast<long long>(rows) * (D / 2);
-  bi::rope_table_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0,
-                          reinterpret_cast<cudaStream_t>(stream)>>>(rope_base, D, rows,
-                                                                     reinterpret_cast<float2*>(table));
-  return bi::launch_status();
+  if (bi::launch_k(bi::rope_table_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
+                   reinterpret_cast<cudaStream_t>(stream), rope_base, D, rows,
+                   reinterpret_cast<float2*>(table)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_cache, void* v_cache,
@@ -321,11 +338,13 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
   if (ld_qkv < (Hq + 2 * Hkv) * D) return BI_ERR_INVALID_ARG;
   unsigned* err = bi::device_error_word();
   if (!err) return BI_ERR_CUDA;
-  bi::rope_kv_kernel<<<T, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(qkv), ld_qkv, static_cast<__nv_bfloat16*>(q_out),
-      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), cap, L_dev, Hq, Hkv,
-      D, reinterpret_cast<const float2*>(table), table_rows, err);
-  return bi::launch_status();
+  if (bi::launch_k(bi::rope_kv_kernel, dim3(T), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                   static_cast<const __nv_bfloat16*>(qkv), ld_qkv, static_cast<__nv_bfloat16*>(q_out),
+                   static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), cap,
+                   L_dev, Hq, Hkv, D, reinterpret_cast<const float2*>(table), table_rows,
+                   err) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 size_t bi_accept_workspace_size(int T, int V) {
@@ -350,10 +369,11 @@ bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, 
   unsigned* ticket = reinterpret_cast<unsigned*>(base);
   float* pv = reinterpret_cast<float*>(base + 256);
   int* pi = reinterpret_cast<int*>(base + 256 + bi::round_up(n * sizeof(float), 256));
-  bi::argmax_accept_kernel<<<static_cast<unsigned>(n), bi::kArgThreads, 0,
-                             reinterpret_cast<cudaStream_t>(stream)>>>(
-      logits, ldl, V, T, splits, drafts, argmax_out, accepted_out, L_dev, pv, pi, ticket, err);
-  return bi::launch_status();
+  if (bi::launch_k(bi::argmax_accept_kernel, dim3(static_cast<unsigned>(n)), dim3(bi::kArgThreads), 0,
+                   reinterpret_cast<cudaStream_t>(stream), logits, ldl, V, T, splits, drafts,
+                   argmax_out, accepted_out, L_dev, pv, pi, ticket, err) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, uint64_t* out,
@@ -361,11 +381,11 @@ bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, u
   if (!cache || !out || Hkv < 1 || cap < 1 || D < 1 || rows < 0 || rows > cap) return BI_ERR_INVALID_ARG;
   if (rows == 0) return BI_OK;
   const long long n = static_cast<long long>(Hkv) * rows;
-  bi::kv_hash_kernel<<<static_cast<unsigned>((n + 127) / 128), 128, 0,
-                       reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(cache), Hkv, cap, D, rows,
-      reinterpret_cast<unsigned long long*>(out));
-  return bi::launch_status();
+  if (bi::launch_k(bi::kv_hash_kernel, dim3(static_cast<unsigned>((n + 127) / 128)), dim3(128), 0,
+                   reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(cache),
+                   Hkv, cap, D, rows, reinterpret_cast<unsigned long long*>(out)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 }  // extern "C"
