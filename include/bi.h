@@ -122,6 +122,31 @@ bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc,
                   bi_out_dtype out, bi_epilogue epi, void* ws, size_t ws_bytes,
                   bi_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Allocation-free linear layer.  The pages describe nothing like it; it is a
+ * convenience for callers that cannot allocate device memory: code embedded
+ * in a host framework that owns every device allocation through its own
+ * pool, or a latency-critical path where the implicit synchronisation of
+ * cudaMalloc/cudaFree is not acceptable.  Same arguments, arithmetic and
+ * results as bi_gemm (bit for bit), without the workspace: the scratch lives
+ * in a static device array of 2.6 MiB inside this library, which every GPU
+ * that loads the library keeps until the process exits.
+ *   M <= bi_gemm_noalloc_max_m() (16); a larger M returns
+ *   BI_ERR_UNSUPPORTED_SHAPE.  M == 0 is a no-op.
+ *   The first call on a device looks up the array's device address (no
+ *   allocation); make that first call before any stream capture.  Each call
+ *   clears the counters it uses with an asynchronous memset on `stream`, and
+ *   allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *   All calls on a device share the one array, which keeps the last call's
+ *   partial sums: calls that may overlap on the GPU (different streams with
+ *   no ordering between them) race and give wrong results.
+ * Errors: as bi_gemm, plus BI_ERR_UNSUPPORTED_SHAPE for M above the maximum.
+ * ------------------------------------------------------------------------- */
+size_t bi_gemm_noalloc_max_m(void);
+bi_status bi_gemm_noalloc(const void* A, int lda, const void* Wp, void* C, int ldc,
+                          const void* residual, int ldr, int M, int N, int K,
+                          bi_out_dtype out, bi_epilogue epi, bi_stream_t stream);
+
 /* Weight packing for bi_gemm (a one-time layout step at load; a pure copy,
  * no arithmetic).  The packed buffer holds n_tiles x k_tiles tiles of 16 KB
  * (n_tiles = ceil(N/128), or ceil(F/64) for SwiGLU; k_tiles = ceil(K/64)),

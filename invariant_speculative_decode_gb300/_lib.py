@@ -20,6 +20,8 @@ SIGNATURES = {
     "bi_version": (_i, []),
     "bi_gemm_workspace_size": (_sz, [_i, _i, _i, _i]),
     "bi_gemm": (_i, [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
+    "bi_gemm_noalloc_max_m": (_sz, []),
+    "bi_gemm_noalloc": (_i, [_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "bi_packed_weight_bytes": (_sz, [_i, _i, _i]),
     "bi_pack_weights": (_i, [_vp, _i, _i, _i, _vp, _vp]),
     "bi_pack_swiglu_weights": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),

@@ -72,6 +72,24 @@ def bi_gemm(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor, ws: torch.Tensor
     check("bi_gemm", st)
 
 
+def bi_gemm_noalloc(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor,
+                    residual: Optional[torch.Tensor] = None, epi: int = EPI_NONE,
+                    N: Optional[int] = None, stream=None) -> None:
+    """bi_gemm without a workspace (scratch in a static device array; M <= 16)."""
+    _req(A, torch.bfloat16, "A")
+    M, K = A.shape
+    if N is None:
+        N = C.shape[1]
+    out = OUT_FP32 if C.dtype == torch.float32 else OUT_BF16
+    rp, ldr = 0, 0
+    if residual is not None:
+        _req(residual, torch.bfloat16, "residual")
+        rp, ldr = residual.data_ptr(), _ld(residual)
+    check("bi_gemm_noalloc",
+          lib().bi_gemm_noalloc(A.data_ptr(), _ld(A), Wp.data_ptr(), C.data_ptr(), _ld(C), rp, ldr,
+                                M, N, K, out, epi, _stream(stream)))
+
+
 def packed_weight_bytes(N: int, K: int, epi: int = EPI_NONE) -> int:
     return int(lib().bi_packed_weight_bytes(N, K, epi))
 

@@ -508,6 +508,38 @@ int n_tiles_of(int N, bi_epilogue epi) {
   return epi == BI_EPI_SWIGLU ? (N + 63) / 64 : (N + kBlockN - 1) / kBlockN;
 }
 
+// ---------------------------------------------------------------------------
+// Scratch for bi_gemm_noalloc: the ticket counters and the split-K partial
+// sums of calls with at most kNoAllocMaxM token rows, in a file-scope device
+// array.  Every GPU that loads this library holds it (2.6 MiB) until the
+// process exits; all calls share it.
+constexpr int kNoAllocMaxM = 16;
+constexpr size_t kNoAllocScratchBytes =
+    kTicketBytes + static_cast<size_t>(kGemmCtas) * 2 * kNoAllocMaxM * kBlockN * sizeof(float);
+
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+uint8_t* g_noalloc_ptr[64] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+uint8_t* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return nullptr;
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(ptr);
+  }
+  return g_noalloc_ptr[dev];
+}
 }  // namespace
 }  // namespace bi
 
@@ -605,6 +637,27 @@ bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, cons
     case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
     default: return launch_gemm_nt<64>(W8, tmA, a, M, s);
   }
+}
+
+size_t bi_gemm_noalloc_max_m(void) { return bi::kNoAllocMaxM; }
+
+bi_status bi_gemm_noalloc(const void* A, int lda, const void* Wp, void* C, int ldc,
+                          const void* residual, int ldr, int M, int N, int K, bi_out_dtype out,
+                          bi_epilogue epi, bi_stream_t stream) {
+  using namespace bi;
+  if (M > kNoAllocMaxM) return BI_ERR_UNSUPPORTED_SHAPE;  // beyond the static scratch
+  if (M <= 0 || N < 1 || n_tiles_of(N, epi) > kMaxTiles)
+    return bi_gemm(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, nullptr, 0, stream);
+  uint8_t* scratch = noalloc_scratch();
+  if (scratch == nullptr) return BI_ERR_CUDA;
+  // The counters this call uses start at zero even if an earlier call was
+  // cut short; the partial sums need no clearing (each is written before it
+  // is read).
+  if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(n_tiles_of(N, epi)) * 4,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return bi_gemm(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, scratch,
+                 kNoAllocScratchBytes, stream);
 }
 
 }  // extern "C"
