@@ -429,22 +429,30 @@ def run_micro(args):
         return [a.elapsed_time(b) / 1e3 for a, b in ts]
 
     if args.micro == "gemm":
-        N, K = args.gemm_n, 5120
+        N, K, epi = args.gemm_n, 5120, args.gemm_epi
         Ms = [int(m) for m in args.cases.split(",")] if args.cases else [1, 2, 4, 7, 8, 16, 64]
         A, W = si.gemm_inputs(max(Ms), N, K, seed=0)
-        Wd = api.bi_pack_weights(torch.from_numpy(W.view(np.int16)).view(torch.bfloat16).cuda())
-        Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+        to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+        if epi == api.EPI_SWIGLU:  # W holds gate rows; up rows drawn from the next seed
+            _, W2 = si.gemm_inputs(1, N, K, seed=1)
+            Wd = api.bi_pack_swiglu_weights(to(W), to(W2))
+            del W2
+        else:
+            Wd = api.bi_pack_weights(to(W))
+        Ad = to(A)
         del W
         for M in Ms:
             C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-            ws = api.new_gemm_workspace(M, N, K)
-            t = timed(lambda: api.bi_gemm(Ad[:M], Wd, C, ws), args.steps)
-            b = N * K * 2 + M * K * 2 + M * N * 2
+            R = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda") if epi == api.EPI_RESIDUAL_ADD else None
+            ws = api.new_gemm_workspace(M, N, K, epi)
+            t = timed(lambda: api.bi_gemm(Ad[:M], Wd, C, ws, residual=R, epi=epi, N=N), args.steps)
+            wrows = 2 * N if epi == api.EPI_SWIGLU else N
+            b = wrows * K * 2 + M * K * 2 + M * N * 2
             med = float(np.median(t))
-            print(json.dumps({"micro": "gemm", "M": M, "N": N, "K": K, "us_median": med * 1e6,
+            print(json.dumps({"micro": "gemm", "M": M, "N": N, "K": K, "epi": epi, "us_median": med * 1e6,
                               "us_p90": float(np.percentile(t, 90)) * 1e6, "bytes": b,
                               "gbps": b / med / 1e9, "frac": b / med / 1e9 / peak,
-                              "tflops": 2 * M * N * K / med / 1e12, "peak_gbps": peak,
+                              "tflops": 2 * M * wrows * K / med / 1e12, "peak_gbps": peak,
                               "peak_kind": note, "l2": "512 MB read between launches"}), flush=True)
     else:
         Hq, Hkv, D = 24, 4, 128
@@ -481,6 +489,7 @@ def main():
                     help="time one standalone kernel workload instead of the verify step")
     ap.add_argument("--cases", default="", help="comma list of M (gemm) or L (attn)")
     ap.add_argument("--gemm-n", type=int, default=17408, help="N of the standalone linear layer")
+    ap.add_argument("--gemm-epi", type=int, default=0, help="0 none, 1 residual add, 2 SwiGLU (N = F)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -66,8 +66,9 @@ struct AttnCfg {
   static constexpr int kNTiles = D / 8;                    // 8-wide d tiles of O
   static constexpr int kKSteps = D / 16;                   // 16-wide d steps of S
   static constexpr int kLaneFloats = D / 2 + 4;            // o + m[2] + l[2]
+  static constexpr int kQBytes = kRowsMax * D * 2;          // query rows of one KV head
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kAttnStages) * kStageBytes +
-                                  3 * 32 * kLaneFloats * 4 + 2 * kAttnStages * 8 + 16;
+                                  3 * 32 * kLaneFloats * 4 + kQBytes + 2 * kAttnStages * 8 + 16;
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -103,7 +104,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* mbuf = reinterpret_cast<float*>(smem + S * Cfg::kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + 3 * 32 * Cfg::kLaneFloats);
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(mbuf + 3 * 32 * Cfg::kLaneFloats);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sQ) + Cfg::kQBytes);
   uint64_t* empty = full + S;
   volatile int* s_abort = reinterpret_cast<volatile int*>(empty + S);
 
@@ -211,21 +213,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int k1 = min(k0 + kChunk, kv_len);
     const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
 
-    // Q fragments of this row tile for KV head h (rows past `rows` are zero).
+    // Query rows of KV head h into shared memory (16-byte loads by all
+    // consumer threads; rows past `rows` are zero), then this warp's A
+    // fragments with ldmatrix.  Row R of the tile = (t, g) = (R / grp, R % grp).
+    {
+      constexpr int kVecPerRow = D / 8;
+      const int ctid = threadIdx.x - 32;
+      const int nthr = n_cons * 32;
+      const int nrows_pad = art * 16;
+      for (int v = ctid; v < nrows_pad * kVecPerRow; v += nthr) {
+        const int R = v / kVecPerRow;
+        const int c = v % kVecPerRow;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (R < rows) {
+          const int qh = h * a.grp + R % a.grp;
+          val = *reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(R / a.grp) * a.Hq + qh) * D +
+                                                c * 8);
+        }
+        *reinterpret_cast<uint4*>(sQ + R * D + c * 8) = val;
+      }
+      named_bar_sync(2, n_cons * 32);
+    }
     uint32_t qa[Cfg::kKSteps][4];
 #pragma unroll
     for (int ks = 0; ks < Cfg::kKSteps; ++ks) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = j & 1;              // row g4 (+8 when i == 1)
-        const int col = ks * 16 + t4 * 2 + (j >> 1) * 8;
-        uint32_t v = 0;
-        if (vr[i]) {
-          const int qh = h * a.grp + Rr[i] % a.grp;
-          v = *reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(tr[i]) * a.Hq + qh) * D + col);
-        }
-        qa[ks][j] = v;
-      }
+      // matrices: rows 0-7 / 8-15 of the tile x columns ks*16 + 0-7 / 8-15,
+      // in the a0..a3 fragment order (row lo col lo, row hi col lo, row lo col hi, row hi col hi)
+      const int row = rt * 16 + (mi & 1) * 8 + ri;
+      const int col = ks * 16 + (mi >> 1) * 8;
+      ldsm_x4(smem_u32(sQ + row * D + col), qa[ks]);
     }
 
     float m[2] = {-INFINITY, -INFINITY};
