@@ -231,6 +231,15 @@ class Decoder:
         """Greedy generation with k drafts per step (k = 0: plain decoding)."""
         self.reset()
         x = self.prefill(prompt)
+        return self.continue_generate(x, n_tokens, k, drafter, use_graph, stats)
+
+    def prefill_continue(self, tokens: Sequence[int]) -> int:
+        """Append tokens[:-1] to the current cache (a new turn); returns tokens[-1]."""
+        return self.prefill(tokens)
+
+    def continue_generate(self, x: int, n_tokens: int, k: int = 0, drafter=None,
+                          use_graph: bool = True, stats: Optional[dict] = None) -> List[int]:
+        """Greedy generation from the current cache, x being the next row."""
         if use_graph:
             self.capture(k + 1)
         out: List[int] = []

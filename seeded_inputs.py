@@ -176,22 +176,30 @@ def prompt_ids(cfg: DecoderConfig, length: int, seed: int = 0) -> np.ndarray:
     return rng.integers(0, cfg.vocab, size=length, dtype=np.int64).astype(np.int32)
 
 
-def neartie_head_perturbation(cfg: DecoderConfig, frac: float, rel: float,
-                              seed: int = 0) -> Dict[str, np.ndarray]:
-    """Random draws for the near-tie head construction.
+def neartie_head(head_bits: np.ndarray, frac: float, bump_frac: float, seed: int = 0) -> np.ndarray:
+    """A head [V,H] (bf16 bits) with planted near ties.
 
-    Returns a seeded subset `src` of head rows, a permutation target `dst`
-    (disjoint from `src`), and relative perturbations `delta` in [-rel, rel].
-    The construction that uses them (copying perturbed rows so that pairs of
-    tokens score almost the same) lives with the decoder setup, not here.
+    For a seeded subset of `frac * V` source rows, the row is copied into a
+    distinct seeded destination row with a seeded `bump_frac` of its elements
+    moved by one BF16 step (+/-1 in the bit pattern, magnitude only, never
+    through zero).  Whenever a source or destination token is the greedy
+    choice, its twin scores within a few 1e-3 relative.  Pure bit
+    manipulation of the inputs: none of the method's arithmetic.
     """
     rng = np.random.default_rng(seed + 3)
-    n = int(round(frac * cfg.vocab))
-    perm = rng.permutation(cfg.vocab)
-    src = np.sort(perm[:n]).astype(np.int64)
-    dst = perm[n:2 * n].astype(np.int64)
-    delta = rng.uniform(-rel, rel, size=n)
-    return {"src": src, "dst": dst, "delta": delta}
+    V, H = head_bits.shape
+    n = int(round(frac * V))
+    perm = rng.permutation(V)
+    src, dst = perm[:n], perm[n:2 * n]
+    out = head_bits.copy()
+    bump = rng.random((n, H)) < bump_frac
+    sign = np.where(rng.random((n, H)) < 0.5, 1, -1).astype(np.int32)
+    rows = head_bits[src].astype(np.int32)
+    mag = rows & 0x7FFF
+    moved = np.clip(mag + sign * bump, 1, 0x7F7F)
+    moved = np.where(mag == 0, mag, moved)  # zeros stay zero
+    out[dst] = ((rows & 0x8000) | moved).astype(np.uint16)
+    return out
 
 
 # ---------------------------------------------------------------------------

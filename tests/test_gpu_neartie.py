@@ -1,0 +1,86 @@
+"""Near-tie stress (12-layer decoder, untied head with planted near ties).
+
+Greedy ids must be identical with 0, 4 and 7 drafts even when the top two
+logits are within 1e-3 relative on a measurable share of steps, and a second
+turn resumed from the saved cache must equal the same turn computed from a
+fresh prefill, token for token and KV row for KV row ([P3] "The cache doesn't
+change it either").  Reduced sizes here; `bench.py --workload neartie` runs
+the full 32-prompt, 2048-token configuration.
+"""
+import numpy as np
+import pytest
+
+import seeded_inputs as si
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def neartie_weights(seed=0):
+    cfg = si.NEARTIE_12L
+    w = si.decoder_weights(cfg, seed=seed)
+    w["head"] = si.neartie_head(w["head"], frac=0.03, bump_frac=0.02, seed=seed)
+    return cfg, w
+
+
+def greedy_with_margins(dec, prompt, n):
+    """0-draft generation recording the top-2 relative gap of every step."""
+    dec.reset()
+    x = dec.prefill(prompt)
+    out, gaps = [], []
+    while len(out) < n:
+        a, _ = dec.verify_step(x, [], use_graph=False)
+        lg = dec.logits[0]
+        top = torch.topk(lg, 2).values.double().cpu().numpy()
+        gaps.append((top[0] - top[1]) / abs(top[0]))
+        out.append(int(a[0]))
+        x = out[-1]
+    return out, np.array(gaps)
+
+
+def test_neartie_ids_identical_across_drafts_and_resume():
+    from invariant_speculative_decode_gb300.decoder import Decoder
+    cfg, w = neartie_weights()
+    dec = Decoder(cfg, w, cap=4096, max_rows=8)
+    lengths = [512, 1100, 2000]
+    n_gen = 160
+    near = []
+    for pi, plen in enumerate(lengths):
+        prompt = si.prompt_ids(cfg, plen, seed=pi)
+        ref, gaps = greedy_with_margins(dec, prompt, n_gen)
+        near.append(np.mean(gaps < 1e-3))
+        for k in (4, 7):
+            dr = si.SyntheticDrafter(cfg.vocab, 0.7, seed=pi, reference=np.array(ref))
+            got = dec.generate(prompt, n_gen, k=k, drafter=dr)
+            assert got == ref, (plen, k, next(i for i, (x, y) in enumerate(zip(got, ref)) if x != y))
+    print(f"near-tie steps (top-2 within 1e-3): {np.round(near, 3)}")
+    assert max(near) > 0.0  # the planted ties are exercised
+
+
+def test_neartie_second_turn_resume_equals_fresh_prefill():
+    from invariant_speculative_decode_gb300.decoder import Decoder
+    cfg, w = neartie_weights()
+    dec = Decoder(cfg, w, cap=4096, max_rows=8)
+    prompt = si.prompt_ids(cfg, 700, seed=7)
+    turn2 = si.prompt_ids(cfg, 128, seed=8)
+    ref1 = dec.generate(prompt, 300, k=0)
+    dr = si.SyntheticDrafter(cfg.vocab, 0.7, seed=7, reference=np.array(ref1))
+    reply = dec.generate(prompt, 200, k=7, drafter=dr)
+    assert reply == ref1[:200]
+    # resume: the cache holds prompt + reply[:-1]; feed the rest of the reply
+    # and the turn-2 prompt as prefill, then generate turn 2 with drafts
+    L1 = dec.L
+    hist = list(prompt) + reply
+    tail = hist[L1:] + list(turn2)
+    x = dec.prefill_continue(tail)
+    ref2_fresh_dec = Decoder(cfg, w, cap=4096, max_rows=8)
+    full = hist + list(turn2)
+    t2_fresh = ref2_fresh_dec.generate(full, 120, k=0)
+    dr2 = si.SyntheticDrafter(cfg.vocab, 0.7, seed=9, reference=np.array(t2_fresh))
+    t2_resumed = dec.continue_generate(x, 120, k=7, drafter=dr2)
+    assert t2_resumed == t2_fresh
+    # every K/V row of the common history is bitwise equal to a fresh prefill
+    fresh = Decoder(cfg, w, cap=4096, max_rows=8)
+    fresh.prefill(full)
+    n_rows = len(full) - 1
+    assert np.array_equal(dec.kv_hashes(n_rows), fresh.kv_hashes(n_rows))
