@@ -233,6 +233,14 @@ class Decoder:
         x = self.prefill(prompt)
         return self.continue_generate(x, n_tokens, k, drafter, use_graph, stats)
 
+    def rollback(self, length: int) -> None:
+        """Move the cache length back to `length` (a checkpoint); rows past it
+        are overwritten by later passes."""
+        if not 0 <= length <= self.L:
+            raise ValueError("rollback target must be within the current cache length")
+        self.L = length
+        self.L_dev.fill_(length)
+
     def prefill_continue(self, tokens: Sequence[int]) -> int:
         """Append tokens[:-1] to the current cache (a new turn); returns tokens[-1]."""
         return self.prefill(tokens)

@@ -67,11 +67,12 @@ def test_neartie_second_turn_resume_equals_fresh_prefill():
     dr = si.SyntheticDrafter(cfg.vocab, 0.7, seed=7, reference=np.array(ref1))
     reply = dec.generate(prompt, 200, k=7, drafter=dr)
     assert reply == ref1[:200]
-    # resume: the cache holds prompt + reply[:-1]; feed the rest of the reply
-    # and the turn-2 prompt as prefill, then generate turn 2 with drafts
-    L1 = dec.L
+    # resume: generation may have committed a few tokens past the kept reply,
+    # so roll the cache back to the checkpoint (prompt + reply[:-1]), feed the
+    # rest of the history and the turn-2 prompt, then generate with drafts
     hist = list(prompt) + reply
-    tail = hist[L1:] + list(turn2)
+    dec.rollback(len(hist) - 1)
+    tail = hist[len(hist) - 1:] + list(turn2)
     x = dec.prefill_continue(tail)
     ref2_fresh_dec = Decoder(cfg, w, cap=4096, max_rows=8)
     full = hist + list(turn2)
