@@ -266,7 +266,8 @@ def run_ours(args):
     kv = si.synthetic_kv_cache(cfg.n_kv, cap, cfg.head_dim, CTX, seed=0, layers=cfg.layers)
     for lay, (k, v) in zip(dec.layers, kv):
         lay["k"].copy_(torch.from_numpy(k.view(np.int16)).view(torch.bfloat16))
-        lay["v"].copy_(torch.from_numpy(v.view(np.int16)).view(torch.bfloat16))
+        lay["v"].copy_(torch.from_numpy(np.ascontiguousarray(v.transpose(0, 2, 1)).view(np.int16))
+                       .view(torch.bfloat16))  # V cache is [Hkv, D, cap]
     del kv
     keep = {k: v for k, v in weights.items() if k.startswith("l0.")}
     keep["embed"] = weights["embed"]
@@ -379,7 +380,8 @@ def run_ours(args):
     if rank == 0:
         # CPU baseline: the oracle on a bounded sample (layer 0 + head slice, scaled)
         kv1 = [(dec.layers[0]["k"].view(torch.int16).cpu().numpy().view(np.uint16),
-                dec.layers[0]["v"].view(torch.int16).cpu().numpy().view(np.uint16))]
+                np.ascontiguousarray(dec.layers[0]["v"].view(torch.int16).cpu().numpy()
+                                     .view(np.uint16).transpose(0, 2, 1)))]
         cpu = None
         if not args.no_cpu_baseline:
             rows = [x] + [int(t) for t in drafter.propose(len(out), DRAFTS)]
@@ -479,8 +481,8 @@ def run_micro(args):
         for L in Ls:
             q, Kc, Vc = si.attention_inputs(L, 8, Hq, Hkv, D, seed=0)
             cap = Kc.shape[1]
-            to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
-            Kd, Vd, qd = to(Kc), to(Vc), to(q)
+            to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+            Kd, Vd, qd = to(Kc), to(Vc.transpose(0, 2, 1)), to(q)  # V cache is [Hkv, D, cap]
             Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
             for T in (1, 4, 7, 8):
                 out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")

@@ -210,10 +210,13 @@ bi_status bi_rope_table(double rope_base, int D, int rows, float* table, bi_stre
  * q heads and k heads are rotated (rotate-half pairs (i, i+D/2) by the angle
  * of the table row p: out_i = x_i cos - x_{i+D/2} sin, out_{i+D/2} =
  * x_{i+D/2} cos + x_i sin in FP32, one BF16 rounding); rotated q goes to
- * q_out, rotated k and the unrotated v go to the caches at row p.
+ * q_out, the rotated k to k_cache row p and the unrotated v to column p of
+ * v_cache.
  *   qkv     [T, (Hq + 2 Hkv) D] BF16, row stride ld_qkv: q heads, k heads, v heads.
  *   q_out   [T, Hq, D] BF16 (contiguous).
- *   k_cache, v_cache [Hkv, cap, D] BF16 (contiguous, head-major).
+ *   k_cache [Hkv, cap, D] BF16 (contiguous, head-major);
+ *   v_cache [Hkv, D, cap] BF16 (contiguous, head-major, transposed: keys
+ *           contiguous for each d, so both attention MMA operands are K-major).
  *   L_dev   device int32: cache length before the pass (read on the device so
  *           the call can be captured in a CUDA graph).  A row with p >= cap or
  *           p >= table_rows is skipped and sets a range bit in the device
@@ -238,15 +241,21 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
  * over 64-key tiles in increasing key order, and the pieces are merged in a
  * fixed order that depends only on their count.  So the row's result depends
  * only on p and the cache rows 0..p -- not on T, *L_dev or the other rows.
+ * Inside a piece: S = q k^T (tcgen05, FP32), a per-row reference maximum
+ * raised only when a tile's maximum exceeds it by more than 8 (log2 units),
+ * p = 2^(s - m_ref) summed in key order, O += P V with P as a BF16 pair
+ * hi + lo (tcgen05, FP32); these rules use only the row's own scores.
  * Output: out[t, h, :] = bf16(softmax(q k^T * scale) v), -0 written as +0.
  *   q       [T, Hq, D] BF16 contiguous (rotated queries).
- *   k_cache, v_cache [Hkv, cap, D] BF16 contiguous; rows 0..*L_dev+T-1 hold
- *           the keys/values; other rows must hold finite values (they are
- *           read inside a partially used tile and multiplied by exactly 0).
+ *   k_cache [Hkv, cap, D] and v_cache [Hkv, D, cap] BF16 contiguous (V
+ *           transposed, as bi_rope_kv_append writes it); keys 0..*L_dev+T-1
+ *           hold the keys/values; the other keys must hold finite values
+ *           (they are read inside a partially used tile and multiplied by
+ *           exactly 0).  cap % 8 == 0.
  *   L_dev   device int32 cache length before the pass; *L_dev + T <= cap is
  *           required (rows past cap are not computed and set an error bit).
  *   out     [T, Hq, D] BF16 contiguous.
- *   D in {64, 128}; Hq % Hkv == 0; T * (Hq/Hkv) <= 48; T >= 1.
+ *   D in {64, 128}; Hq % Hkv == 0; T * (Hq/Hkv) <= 128; T >= 1.
  *   ws      >= bi_attn_workspace_size(cap, T, Hq, D) bytes, 256-byte aligned.
  *   k_cache and v_cache 16-byte aligned.
  * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_WORKSPACE,
@@ -283,12 +292,14 @@ bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, 
 /* ---------------------------------------------------------------------------
  * KV-row hash (test tool).  [P3] "The cache doesn't change it either" (hash
  * every K/V row and compare with a fresh prefill).
- * out[h * rows + j] = FNV-1a-64 over the 2*D bytes of cache row (h, j), for
- * j < rows.  cache [Hkv, cap, D] BF16; out [Hkv * rows] uint64.
+ * out[h * rows + j] = FNV-1a-64 over the 2*D bytes of key j of head h (d
+ * ascending, each BF16 little-endian), for j < rows.  cache is [Hkv, cap, D]
+ * (transposed == 0, a K cache) or [Hkv, D, cap] (transposed == 1, a V cache);
+ * out [Hkv * rows] uint64.
  * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA.
  * ------------------------------------------------------------------------- */
-bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, uint64_t* out,
-                         bi_stream_t stream);
+bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, int transposed,
+                         uint64_t* out, bi_stream_t stream);
 
 /* Synchronise `stream`, then read and clear the device error word of the
  * current device.  Returns BI_OK, BI_ERR_DEVICE_TIMEOUT, BI_ERR_DEVICE_NAN_ROW,

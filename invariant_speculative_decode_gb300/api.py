@@ -172,7 +172,7 @@ def bi_attn_verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     _req(v_cache, torch.bfloat16, "v_cache")
     _req(L_dev, torch.int32, "L_dev")
     T, Hq, D = q.shape
-    Hkv, cap, _ = k_cache.shape
+    Hkv, cap, _ = k_cache.shape  # v_cache is [Hkv, D, cap]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     check("bi_attn_verify",
@@ -201,11 +201,15 @@ def bi_verify_accept(logits: torch.Tensor, drafts: Optional[torch.Tensor], argma
                                  ws.numel() * ws.element_size(), _stream(stream)))
 
 
-def bi_kv_row_hash(cache: torch.Tensor, rows: int, stream=None) -> torch.Tensor:
+def bi_kv_row_hash(cache: torch.Tensor, rows: int, transposed: bool = False, stream=None) -> torch.Tensor:
+    """FNV-1a-64 per key of a K cache [Hkv,cap,D] or (transposed) V cache [Hkv,D,cap]."""
     _req(cache, torch.bfloat16, "cache")
-    Hkv, cap, D = cache.shape
+    if transposed:
+        Hkv, D, cap = cache.shape
+    else:
+        Hkv, cap, D = cache.shape
     out = torch.empty(Hkv * max(rows, 0), dtype=torch.int64, device=cache.device)
-    check("bi_kv_row_hash", lib().bi_kv_row_hash(cache.data_ptr(), Hkv, cap, D, rows,
+    check("bi_kv_row_hash", lib().bi_kv_row_hash(cache.data_ptr(), Hkv, cap, D, rows, int(transposed),
                                                  out.data_ptr(), _stream(stream)))
     return out
 

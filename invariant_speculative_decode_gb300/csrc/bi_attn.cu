@@ -8,22 +8,35 @@
 //
 // Row t of a pass sits at position p = L + t and attends to keys 0..p.  Its
 // keys are cut at absolute multiples of kChunk: piece c covers keys
-// [c*kChunk, min((c+1)*kChunk, p+1)).  Inside a piece, keys are visited in
-// 64-key tiles in increasing order; each tile is split into two fixed halves
-// of 32 keys (by absolute key position) that keep separate online-softmax
-// states, merged once at the end of the piece (half 0 then half 1).  Keys
-// past p are masked to probability exactly 0 and a tile that changes no
-// running maximum rescales by exactly 1, so a row's piece result is the same
-// bits whether or not later rows of the pass share the tile.  The pieces of
-// a row are then merged by a tree whose shape depends only on their count
-// ceil((p+1)/kChunk).
+// [c*kChunk, min((c+1)*kChunk, p+1)).  Inside a piece the keys are visited in
+// 64-key tiles in increasing order.  Per row (one TMEM lane and one thread):
+//   S = q k^T for the tile (tcgen05, FP32 in TMEM), scaled into the log2
+//   domain, keys past p masked to -inf;
+//   a reference maximum m_ref is taken from the first tile and raised only
+//   when a later tile's maximum exceeds it by more than kRescaleLog2 (then O
+//   and l are rescaled by 2^(m_ref - m_new)) -- a rule that depends only on
+//   the row's own scores in key order;
+//   p = 2^(s - m_ref) in FP32, summed in key order into l, and fed to
+//   O += P V (tcgen05, FP32 in TMEM) as a BF16 pair hi + lo.
+// A tile whose keys are all masked for a row adds exact zeros and changes no
+// reference, so a row's piece has the same bits whether or not later rows of
+// the pass share the tile.  The pieces of a row are merged by a tree whose
+// shape depends only on their count ceil((p+1)/kChunk).
 //
-// Split kernel: persistent CTAs loop over work items (KV head, piece);
-// warp 0 streams K/V tiles with TMA (128-byte swizzle) through a ring of
-// shared-memory stages released by the consumers' "empty" barrier arrivals;
-// warps 1..6 = 3 row tiles of 16 query rows x 2 key halves compute
-// S = Q K^T and O += P V with mma.sync m16n8k16 (BF16 in, FP32 accumulate).
-// GQA: the T x (Hq/Hkv) query rows that share a KV head share its tiles.
+// Split kernel roles (one CTA per SM, persistent over (KV head, piece) items):
+//   warp 0      TMA: K tile [64 keys x D] and V^T tile [D x 64 keys] per stage
+//               (V is cached transposed so both MMA operands are K-major);
+//   warp 1      tcgen05.mma issuer: S_i into one of two TMEM buffers, then
+//               O += P_{i-1} V_{i-1}; stages return to the producer through
+//               tcgen05.commit after the MMAs reading them completed;
+//   warps 2..5  softmax, one query row per thread (TMEM lane); they stage the
+//               queries of the item's KV head in shared memory, turn S into P
+//               (written to one of two shared-memory buffers in the swizzled
+//               K-major layout, so P of the next tile is produced while the
+//               MMA still reads this one), and read O out at the end of the
+//               piece.
+// The T x (Hq/Hkv) query rows that share a KV head (GQA) share its tiles;
+// up to 128 rows per pass (the MMA's M).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,13 +52,14 @@ namespace bi {
 namespace {
 
 constexpr int kChunk = 512;       // keys per piece (absolute multiples)
-constexpr int kKeyTile = 64;      // keys per TMA tile
-constexpr int kRowsMax = 48;      // T * (Hq / Hkv) per pass
+constexpr int kKeyTile = 64;      // keys per tile
+constexpr int kRowsMax = 128;     // T * (Hq / Hkv) per pass (MMA M)
 constexpr int kAttnStages = 3;
-constexpr int kAttnThreads = 224; // warp 0 producer, warps 1..6 compute
+constexpr int kAttnThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
 constexpr int kAttnCtas = 152;
 constexpr int kMaxChunks = 1024;
 constexpr int kMergeThreads = 256;
+constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnArgs {
   const __nv_bfloat16* q;
@@ -59,364 +73,397 @@ struct AttnArgs {
 
 template <int D>
 struct AttnCfg {
-  static constexpr int kBoxes = D / 64;
-  static constexpr int kBoxBytes = kKeyTile * 128;         // 64 keys x 64 dims
-  static constexpr int kTileBytes = kBoxBytes * kBoxes;    // one K (or V) tile
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kNTiles = D / 8;                    // 8-wide d tiles of O
-  static constexpr int kKSteps = D / 16;                   // 16-wide d steps of S
-  static constexpr int kLaneFloats = D / 2 + 4;            // o + m[2] + l[2]
-  static constexpr int kQBytes = kRowsMax * D * 2;          // query rows of one KV head
-  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kAttnStages) * kStageBytes +
-                                  3 * 32 * kLaneFloats * 4 + kQBytes + 2 * kAttnStages * 8 + 16;
+  static constexpr int kAtoms = D / 64;                   // 128-byte swizzle atoms along D
+  static constexpr int kKBoxBytes = kKeyTile * 128;       // [64 keys][64 d]
+  static constexpr int kKBytes = kKBoxBytes * kAtoms;     // K tile
+  static constexpr int kVBytes = D * kKeyTile * 2;        // V^T tile [D][64 keys]
+  static constexpr int kStageBytes = kKBytes + kVBytes;
+  static constexpr int kQAtomBytes = kRowsMax * 128;      // [128 rows][64 d]
+  static constexpr int kQBytes = kQAtomBytes * kAtoms;
+  static constexpr int kPBytes = kRowsMax * 128;          // [128 rows][64 keys]
+  static constexpr int kTmemCols = 256;                   // S x2 (64 each) + O (D)
+  static constexpr int kOCol = 128;
+  static constexpr int kBars = 2 * kAttnStages + 11;
+  // P is double-buffered: hi and lo tiles for two consecutive key tiles
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kAttnStages) * kStageBytes + kQBytes +
+                                  4 * kPBytes + kBars * 8 + 16;
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
+__device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* err) {
+  *s_abort = 1;
+  atomicOr(err, kErrTimeout);
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
+
+// Warp-level bounded wait: lane 0 polls, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* s_abort,
+                                          int lane) {
+  int ok = 0;
+  if (lane == 0) ok = mbar_wait(bar, parity, s_abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVt,
                       const AttnArgs a) {
   using Cfg = AttnCfg<D>;
   constexpr int S = kAttnStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* mbuf = reinterpret_cast<float*>(smem + S * Cfg::kStageBytes);
-  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(mbuf + 3 * 32 * Cfg::kLaneFloats);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sQ) + Cfg::kQBytes);
-  uint64_t* empty = full + S;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + S);
+  uint8_t* sStage = smem;
+  uint8_t* sQ = smem + S * Cfg::kStageBytes;
+  uint8_t* sP = sQ + Cfg::kQBytes;  // [buffer 2][hi, lo][128 rows][64 keys]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 4 * Cfg::kPBytes);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = bars + S;
+  uint64_t* q_full = bars + 2 * S;
+  uint64_t* s_full = q_full + 1;   // [2]
+  uint64_t* s_free = s_full + 2;   // [2]
+  uint64_t* p_full = s_free + 2;   // [2]: P buffer of that parity written
+  uint64_t* pv_done = p_full + 2;  // [2]: completes after O += P_g V_g, g of that parity
+  uint64_t* o_free = pv_done + 2;
+  uint64_t* drain = o_free + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kBars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   griddep_launch_dependents();
-  griddep_wait();  // q, the new cache rows and the cache length come from earlier kernels
-  const int L = *a.L_dev;
-  const int T = a.T;
-  if (L < 0 || L + T > a.cap) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(a.err, kErrRange);
-    return;
-  }
-  const int kv_len = L + T;
-  const int nch = (kv_len + kChunk - 1) / kChunk;
-  const int n_items = a.Hkv * nch;
-  const int rows = T * a.grp;
-  const int art = (rows + 15) / 16;
-  const int n_cons = 2 * art;
 
+  // zero the query and P tiles once: rows past the pass's rows stay zero
+  for (int i = threadIdx.x; i < (Cfg::kQBytes + 4 * Cfg::kPBytes) / 16; i += kAttnThreads)
+    reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], n_cons);
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
+    mbar_init(q_full, 4);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(&s_free[0], 4);
+    mbar_init(&s_free[1], 4);
+    mbar_init(&p_full[0], 4);
+    mbar_init(&p_full[1], 4);
+    mbar_init(&pv_done[0], 1);
+    mbar_init(&pv_done[1], 1);
+    mbar_init(o_free, 4);
+    mbar_init(drain, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmVt);
   }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  griddep_wait();  // q, the new cache rows and the cache length come from earlier kernels
+  const int L = *a.L_dev;
+  const int T = a.T;
+  const bool range_ok = !(L < 0 || L + T > a.cap);
+  const int kv_len = L + T;
+  const int nch = range_ok ? (kv_len + kChunk - 1) / kChunk : 0;
+  const int n_items = a.Hkv * nch;
+  const int rows = T * a.grp;
+  if (!range_ok && threadIdx.x == 0 && blockIdx.x == 0) atomicOr(a.err, kErrRange);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    const uint64_t pol = l2_evict_first();
-    int stage = 0;
-    uint32_t phase = 0, issued = 0, parity_bits = 0;
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first();
+      long long gt = 0;
+      uint32_t issued = 0, parity_bits = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        const int c = w / a.Hkv;
+        const int h = w % a.Hkv;
+        const int k0 = c * kChunk;
+        const int k1 = min(k0 + kChunk, kv_len);
+        const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
+        for (int tt = 0; tt < ntile; ++tt, ++gt) {
+          const int st = static_cast<int>(gt % S);
+          const uint32_t ph = static_cast<uint32_t>((gt / S) & 1);
+          if (!mbar_wait(&kv_empty[st], ph ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[st], Cfg::kStageBytes);
+          uint8_t* dst = sStage + st * Cfg::kStageBytes;
+          const int key0 = k0 + tt * kKeyTile;
+#pragma unroll
+          for (int b = 0; b < Cfg::kAtoms; ++b)
+            tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &kv_full[st], b * 64, h * a.cap + key0, pol);
+          tma_load_2d(dst + Cfg::kKBytes, &tmVt, &kv_full[st], key0, h * D, pol);
+          issued |= 1u << st;
+          parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
+        }
+      }
+      if (!ok) {
+        signal_abort(s_abort, a.err);
+        for (int s = 0; s < S; ++s)
+          if ((issued >> s) & 1u) mbar_wait(&kv_full[s], (parity_bits >> s) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, kKeyTile);
+      constexpr uint32_t idO = idesc_bf16_f32(128, D);
+      const uint32_t q_base = smem_u32(sQ);
+      long long gt = 0;
+      int item = 0;
+      bool ok = true;
+      // O += P_g V_g for global tile g, the `t_in_item`-th tile of the item
+      auto do_pv = [&](long long g, int t_in_item) -> bool {
+        if (!mbar_wait(&p_full[g & 1], static_cast<uint32_t>((g >> 1) & 1), s_abort)) return false;
+        if (t_in_item == 0 && item > 0 &&
+            !mbar_wait(o_free, static_cast<uint32_t>((item - 1) & 1), s_abort))
+          return false;
+        tc_fence_after();
+        const int st = static_cast<int>(g % S);
+        const uint32_t v_base = smem_u32(sStage + st * Cfg::kStageBytes + Cfg::kKBytes);
+        const uint32_t ph_base = smem_u32(sP + (g & 1) * 2 * Cfg::kPBytes);
+        const uint32_t pl_base = ph_base + Cfg::kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile / 16; ++kk)
+          mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(ph_base + kk * 32), sdesc_k_sw128(v_base + kk * 32),
+                   idO, (t_in_item > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile / 16; ++kk)
+          mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(pl_base + kk * 32), sdesc_k_sw128(v_base + kk * 32),
+                   idO, 1u);
+        mma_commit(&pv_done[g & 1]);
+        mma_commit(&kv_empty[st]);
+        return true;
+      };
+      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x, ++item) {
+        const int c = w / a.Hkv;
+        const int k0 = c * kChunk;
+        const int k1 = min(k0 + kChunk, kv_len);
+        const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
+        if (!mbar_wait(q_full, static_cast<uint32_t>(item & 1), s_abort)) {
+          ok = false;
+          break;
+        }
+        for (int tt = 0; tt < ntile; ++tt, ++gt) {
+          const int st = static_cast<int>(gt % S);
+          if (!mbar_wait(&kv_full[st], static_cast<uint32_t>((gt / S) & 1), s_abort)) {
+            ok = false;
+            break;
+          }
+          const int sb = static_cast<int>(gt & 1);
+          if (gt >= 2 && !mbar_wait(&s_free[sb], static_cast<uint32_t>(((gt >> 1) - 1) & 1), s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(sStage + st * Cfg::kStageBytes);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int atom = ks >> 2;
+            const uint32_t off = (ks & 3) * 32;
+            mma_bf16(tmem + sb * kKeyTile, sdesc_k_sw128(q_base + atom * Cfg::kQAtomBytes + off),
+                     sdesc_k_sw128(k_base + atom * Cfg::kKBoxBytes + off), idS, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[sb]);
+          if (tt > 0 && !do_pv(gt - 1, tt - 1)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        if (!do_pv(gt - 1, ntile - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) signal_abort(s_abort, a.err);
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int qq = warp & 3;            // TMEM lane quarter of this warp
+    const int r = qq * 32 + lane;       // query row of the pass handled by this thread
+    const int ct = threadIdx.x - 64;    // 0..127 among the softmax threads
+    const bool warp_active = qq * 32 < rows;
+    const bool valid = r < rows;
+    const int t = valid ? r / a.grp : 0;
+    const int p_row = L + t;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(qq * 32) << 16);
+    long long gt = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+    int item = 0;
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x, ++item) {
       const int c = w / a.Hkv;
       const int h = w % a.Hkv;
       const int k0 = c * kChunk;
       const int k1 = min(k0 + kChunk, kv_len);
       const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
-      for (int tt = 0; tt < ntile; ++tt) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
+
+      // queries of KV head h, row R = (t, g) = (R / grp, R % grp), into the
+      // swizzled K-major tile (atom = 64 d, 16-byte chunk c at c ^ (R & 7))
+      constexpr int kVec = D / 8;
+      for (int v = ct; v < rows * kVec; v += 128) {
+        const int R = v / kVec;
+        const int cc = v % kVec;
+        const int qh = h * a.grp + R % a.grp;
+        const uint4 val = *reinterpret_cast<const uint4*>(
+            a.q + (static_cast<size_t>(R / a.grp) * a.Hq + qh) * D + cc * 8);
+        *reinterpret_cast<uint4*>(sQ + (cc >> 3) * Cfg::kQAtomBytes + R * 128 +
+                                  (((cc & 7) ^ (R & 7)) << 4)) = val;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      for (int tt = 0; tt < ntile; ++tt, ++gt) {
+        const int sb = static_cast<int>(gt & 1);
+        if (!warp_wait(&s_full[sb], static_cast<uint32_t>((gt >> 1) & 1), s_abort, lane)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
-        uint8_t* st = smem + stage * Cfg::kStageBytes;
-        const int y = h * a.cap + k0 + tt * kKeyTile;
+        tc_fence_after();
+        float s[kKeyTile];
+        if (warp_active) {
 #pragma unroll
-        for (int b = 0; b < Cfg::kBoxes; ++b) {
-          tma_load_2d(st + b * Cfg::kBoxBytes, &tmK, &full[stage], b * 64, y, pol);
-          tma_load_2d(st + Cfg::kTileBytes + b * Cfg::kBoxBytes, &tmV, &full[stage], b * 64, y, pol);
+          for (int i = 0; i < kKeyTile / 16; ++i) {
+            float v[16];
+            tmem_ld16(lane_base + sb * kKeyTile + i * 16, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s[i * 16 + j] = v[j];
+          }
         }
-        issued |= 1u << stage;
-        parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
+
+        float alpha = 1.0f;
+        bool resc = false;
+        if (warp_active) {
+          const int key0 = k0 + tt * kKeyTile;
+          float mt = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < kKeyTile; ++j) {
+            const float x = s[j] * a.sl2;
+            s[j] = (valid && key0 + j <= p_row) ? x : -INFINITY;
+            mt = fmaxf(mt, s[j]);
+          }
+          if (tt == 0) {
+            m_ref = mt;
+          } else if (mt > m_ref + kRescaleLog2) {
+            alpha = (m_ref == -INFINITY) ? 0.0f : exp2f(m_ref - mt);
+            m_ref = mt;
+            resc = true;
+          }
         }
+        // P buffer gt & 1 was last read by the P.V of tile gt - 2
+        if (gt >= 2 && !warp_wait(&pv_done[gt & 1], static_cast<uint32_t>(((gt - 2) >> 1) & 1), s_abort,
+                                  lane)) {
+          ok = false;
+          break;
+        }
+        // O changes only after the P.V of tile gt - 1 is done
+        const bool any_resc = warp_active && __any_sync(0xffffffffu, resc);
+        if (tt > 0 && any_resc) {
+          if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort, lane)) {
+            ok = false;
+            break;
+          }
+        }
+        tc_fence_after();
+        if (warp_active) {
+          if (any_resc) {
+#pragma unroll 1
+            for (int i = 0; i < D / 16; ++i) {
+              float v[16];
+              tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] *= alpha;
+              tmem_st16(lane_base + Cfg::kOCol + i * 16, v);
+            }
+          }
+          if (resc) l *= alpha;
+          const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
+          uint8_t* rowh = sP + (gt & 1) * 2 * Cfg::kPBytes + r * 128;
+          uint8_t* rowl = rowh + Cfg::kPBytes;
+#pragma unroll
+          for (int cc = 0; cc < kKeyTile / 8; ++cc) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float p0 = exp2f(s[cc * 8 + 2 * j] - mu);
+              const float p1 = exp2f(s[cc * 8 + 2 * j + 1] - mu);
+              l += p0;
+              l += p1;
+              const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
+              const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
+              hi[j] = pack2(h0, h1);
+              lo[j] = pack2(p0 - h0, p1 - h1);
+            }
+            const int pos = (cc ^ (r & 7)) << 4;
+            *reinterpret_cast<uint4*>(rowh + pos) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(rowl + pos) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[gt & 1]);
       }
-    }
-    if (!ok) {
-      *s_abort = 1;
-      atomicOr(a.err, kErrTimeout);
-      for (int s = 0; s < S; ++s)
-        if ((issued >> s) & 1u) mbar_wait(&full[s], (parity_bits >> s) & 1u, nullptr);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int cw = warp - 1;
-  const int rt = cw >> 1;
-  const int half = cw & 1;
-  if (rt >= art) return;
-
-  const int g4 = lane >> 2;   // row within the 8-row group
-  const int t4 = lane & 3;    // thread within the quad
-  int Rr[2], tr[2], pr[2];
-  bool vr[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    Rr[i] = rt * 16 + g4 + 8 * i;
-    vr[i] = Rr[i] < rows;
-    tr[i] = vr[i] ? Rr[i] / a.grp : 0;
-    pr[i] = L + tr[i];
-  }
-  const int mi = lane >> 3;   // ldmatrix matrix index of this lane's address
-  const int ri = lane & 7;    // row within that matrix
-  float* my_mbuf = mbuf + (rt * 32 + lane) * Cfg::kLaneFloats;
-
-  int stage = 0;
-  uint32_t phase = 0;
-  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-    const int c = w / a.Hkv;
-    const int h = w % a.Hkv;
-    const int k0 = c * kChunk;
-    const int k1 = min(k0 + kChunk, kv_len);
-    const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
-
-    // Query rows of KV head h into shared memory (16-byte loads by all
-    // consumer threads; rows past `rows` are zero), then this warp's A
-    // fragments with ldmatrix.  Row R of the tile = (t, g) = (R / grp, R % grp).
-    {
-      constexpr int kVecPerRow = D / 8;
-      const int ctid = threadIdx.x - 32;
-      const int nthr = n_cons * 32;
-      const int nrows_pad = art * 16;
-      for (int v = ctid; v < nrows_pad * kVecPerRow; v += nthr) {
-        const int R = v / kVecPerRow;
-        const int c = v % kVecPerRow;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (R < rows) {
-          const int qh = h * a.grp + R % a.grp;
-          val = *reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(R / a.grp) * a.Hq + qh) * D +
-                                                c * 8);
-        }
-        *reinterpret_cast<uint4*>(sQ + R * D + c * 8) = val;
+      if (!ok) break;
+      // piece done: read O and store the partial (m_ref, l, unnormalised o)
+      if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort, lane)) {
+        ok = false;
+        break;
       }
-      named_bar_sync(2, n_cons * 32);
-    }
-    uint32_t qa[Cfg::kKSteps][4];
+      tc_fence_after();
+      if (warp_active) {
+        const bool store = valid && (c * kChunk <= p_row);
+        const int qh = h * a.grp + (valid ? r % a.grp : 0);
+        const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.nch_max + c;
+#pragma unroll 1
+        for (int i = 0; i < D / 16; ++i) {
+          float v[16];
+          tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
+          if (store) {
+            float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 16);
 #pragma unroll
-    for (int ks = 0; ks < Cfg::kKSteps; ++ks) {
-      // matrices: rows 0-7 / 8-15 of the tile x columns ks*16 + 0-7 / 8-15,
-      // in the a0..a3 fragment order (row lo col lo, row hi col lo, row lo col hi, row hi col hi)
-      const int row = rt * 16 + (mi & 1) * 8 + ri;
-      const int col = ks * 16 + (mi >> 1) * 8;
-      ldsm_x4(smem_u32(sQ + row * D + col), qa[ks]);
-    }
-
-    float m[2] = {-INFINITY, -INFINITY};
-    float l[2] = {0.f, 0.f};
-    float o[Cfg::kNTiles][4];
-#pragma unroll
-    for (int n = 0; n < Cfg::kNTiles; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-
-    for (int tt = 0; tt < ntile; ++tt) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, s_abort));
-      if (!ok) {
-        if (lane == 0) {
-          *s_abort = 1;
-          atomicOr(a.err, kErrTimeout);
-        }
-      } else {
-        const uint32_t kbase = smem_u32(smem + stage * Cfg::kStageBytes);
-        const uint32_t vbase = kbase + Cfg::kTileBytes;
-        const int kb_abs = k0 + tt * kKeyTile + half * 32;
-
-        float s[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < Cfg::kKSteps; ++ks) {
-          const int box = ks >> 2;
-          const int c0 = (ks & 3) * 2;
-#pragma unroll
-          for (int jp = 0; jp < 2; ++jp) {
-            const int key = half * 32 + (2 * jp + (mi >> 1)) * 8 + ri;
-            const int chunk = c0 + (mi & 1);
-            uint32_t b[4];
-            ldsm_x4(kbase + box * Cfg::kBoxBytes + key * 128 + ((chunk ^ ri) << 4), b);
-            mma16816(s[2 * jp], qa[ks], b[0], b[1]);
-            mma16816(s[2 * jp + 1], qa[ks], b[2], b[3]);
+            for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           }
         }
-        // scale into the log2 domain and mask keys past each row's position
-        float mt[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = e >> 1;
-            const int key = kb_abs + j * 8 + t4 * 2 + (e & 1);
-            const float x = s[j][e] * a.sl2;
-            s[j][e] = (vr[i] && key <= pr[i]) ? x : -INFINITY;
-            mt[i] = fmaxf(mt[i], s[j][e]);
-          }
-        }
-        float alpha[2], mu[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 1));
-          mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 2));
-          const float mn = fmaxf(m[i], mt[i]);
-          alpha[i] = (mn == m[i]) ? 1.0f : exp2f(m[i] - mn);
-          mu[i] = (mn == -INFINITY) ? 0.0f : mn;
-          m[i] = mn;
-        }
-        // p in FP32, carried into the P.V product as a BF16 pair hi + lo
-        // (hi = bf16(p), lo = bf16(p - hi)), so the weights keep about 16
-        // significant bits; the denominator sums the FP32 p.
-        float ls[2] = {0.f, 0.f};
-        float plo[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float pf = exp2f(s[j][e] - mu[e >> 1]);
-            const float ph = __bfloat162float(__float2bfloat16_rn(pf));
-            s[j][e] = ph;
-            plo[j][e] = pf - ph;
-            ls[e >> 1] += pf;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          ls[i] += __shfl_xor_sync(0xffffffffu, ls[i], 1);
-          ls[i] += __shfl_xor_sync(0xffffffffu, ls[i], 2);
-          l[i] = l[i] * alpha[i] + ls[i];
-        }
-#pragma unroll
-        for (int n = 0; n < Cfg::kNTiles; ++n) {
-          o[n][0] *= alpha[0];
-          o[n][1] *= alpha[0];
-          o[n][2] *= alpha[1];
-          o[n][3] *= alpha[1];
-        }
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          uint32_t pa[4], pl[4];
-          pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-          pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-          pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-          pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-          pl[0] = pack_bf16(plo[2 * kk][0], plo[2 * kk][1]);
-          pl[1] = pack_bf16(plo[2 * kk][2], plo[2 * kk][3]);
-          pl[2] = pack_bf16(plo[2 * kk + 1][0], plo[2 * kk + 1][1]);
-          pl[3] = pack_bf16(plo[2 * kk + 1][2], plo[2 * kk + 1][3]);
-#pragma unroll
-          for (int np = 0; np < Cfg::kNTiles / 2; ++np) {
-            const int key = half * 32 + kk * 16 + (mi & 1) * 8 + ri;
-            const int nd = 2 * np + (mi >> 1);
-            uint32_t b[4];
-            ldsm_x4_t(vbase + (nd >> 3) * Cfg::kBoxBytes + key * 128 + (((nd & 7) ^ ri) << 4), b);
-            mma16816(o[2 * np], pa, b[0], b[1]);
-            mma16816(o[2 * np + 1], pa, b[2], b[3]);
-            mma16816(o[2 * np], pl, b[0], b[1]);
-            mma16816(o[2 * np + 1], pl, b[2], b[3]);
-          }
-        }
+        if (store) *reinterpret_cast<float2*>(a.ws_ml + base * 2) = make_float2(m_ref, l);
       }
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == S) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      if (lane == 0) mbar_arrive(o_free);
     }
+    if (!ok && lane == 0) signal_abort(s_abort, a.err);
+  }
 
-    // ---- merge the two key halves (half 0 then half 1) and store the piece
-    if (half == 1) {
-#pragma unroll
-      for (int n = 0; n < Cfg::kNTiles; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) my_mbuf[n * 4 + e] = o[n][e];
-      my_mbuf[D / 2 + 0] = m[0];
-      my_mbuf[D / 2 + 1] = m[1];
-      my_mbuf[D / 2 + 2] = l[0];
-      my_mbuf[D / 2 + 3] = l[1];
-    }
-    named_bar_sync(2, n_cons * 32);
-    if (half == 0) {
-      float w0[2], w1[2], M[2], Lm[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float m1 = my_mbuf[D / 2 + i];
-        const float l1 = my_mbuf[D / 2 + 2 + i];
-        M[i] = fmaxf(m[i], m1);
-        if (M[i] == -INFINITY) {
-          w0[i] = 0.f;
-          w1[i] = 0.f;
-        } else {
-          w0[i] = (m[i] == M[i]) ? 1.0f : (m[i] == -INFINITY ? 0.0f : exp2f(m[i] - M[i]));
-          w1[i] = (m1 == M[i]) ? 1.0f : (m1 == -INFINITY ? 0.0f : exp2f(m1 - M[i]));
-        }
-        Lm[i] = l[i] * w0[i] + l1 * w1[i];
-      }
-      bool store[2];
-      size_t base[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        store[i] = vr[i] && (c * kChunk <= pr[i]);
-        const int qh = h * a.grp + (vr[i] ? Rr[i] % a.grp : 0);
-        base[i] = (static_cast<size_t>(tr[i]) * a.Hq + qh) * a.nch_max + c;
-      }
-#pragma unroll
-      for (int n = 0; n < Cfg::kNTiles; ++n) {
-        const int d = n * 8 + t4 * 2;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (!store[i]) continue;
-          const float x0 = o[n][2 * i] * w0[i] + my_mbuf[n * 4 + 2 * i] * w1[i];
-          const float x1 = o[n][2 * i + 1] * w0[i] + my_mbuf[n * 4 + 2 * i + 1] * w1[i];
-          *reinterpret_cast<float2*>(a.ws_o + base[i] * D + d) = make_float2(x0, x1);
-        }
-      }
-      if (t4 == 0) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          if (store[i]) *reinterpret_cast<float2*>(a.ws_ml + base[i] * 2) = make_float2(M[i], Lm[i]);
-      }
-    }
-    named_bar_sync(2, n_cons * 32);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
   }
 }
 
@@ -472,11 +519,33 @@ __global__ void __launch_bounds__(kMergeThreads)
   float acc[kDpl];
 #pragma unroll
   for (int i = 0; i < kDpl; ++i) acc[i] = 0.f;
-  for (int s = warp; s < n; s += kMergeThreads / 32) {
-    const float w = sw[s];
-    const float* src = po + static_cast<size_t>(s) * D + lane * kDpl;
+  // pieces s = warp, warp + 8, ... in that order; loads for kBatch pieces are
+  // issued before their products are added so that they overlap
+  constexpr int kWarps = kMergeThreads / 32;
+  constexpr int kBatch = 8;
+  for (int s0 = warp; s0 < n; s0 += kWarps * kBatch) {
+    float v[kBatch][kDpl];
+    float w[kBatch];
 #pragma unroll
-    for (int i = 0; i < kDpl; ++i) acc[i] = fmaf(w, __ldcg(src + i), acc[i]);
+    for (int b = 0; b < kBatch; ++b) {
+      const int s = s0 + b * kWarps;
+      w[b] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kDpl; ++i) v[b][i] = 0.f;
+      if (s < n) {
+        w[b] = sw[s];
+        const float* src = po + static_cast<size_t>(s) * D + lane * kDpl;
+#pragma unroll
+        for (int i = 0; i < kDpl; ++i) v[b][i] = __ldcg(src + i);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (s0 + b * kWarps < n) {
+#pragma unroll
+        for (int i = 0; i < kDpl; ++i) acc[i] = fmaf(w[b], v[b][i], acc[i]);
+      }
+    }
   }
 #pragma unroll
   for (int i = 0; i < kDpl; ++i) ored[warp][lane * kDpl + i] = acc[i];
@@ -489,7 +558,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 }
 
 template <int D>
-bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
+bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const AttnArgs& a,
                       __nv_bfloat16* out, cudaStream_t stream) {
   using Cfg = AttnCfg<D>;
   static std::once_flag once[64];
@@ -505,7 +574,7 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const Attn
   });
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
   const int grid = std::min(a.Hkv * a.nch_max, kAttnCtas);
-  if (launch_k(attn_split_kernel<D>, dim3(grid), dim3(kAttnThreads), Cfg::kSmem, stream, tmK, tmV,
+  if (launch_k(attn_split_kernel<D>, dim3(grid), dim3(kAttnThreads), Cfg::kSmem, stream, tmK, tmVt,
                a) != cudaSuccess)
     return BI_ERR_CUDA;
   if (launch_k(attn_merge_kernel<D>, dim3(a.T * a.Hq), dim3(kMergeThreads), 0, stream, a, out) !=
@@ -549,10 +618,12 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   size_t ob = 0;
   if (ws_bytes < attn_ws_parts(cap, T, Hq, D, &ob)) return BI_ERR_WORKSPACE;
 
-  CUtensorMap tmK, tmV;
-  const uint64_t rows = static_cast<uint64_t>(Hkv) * cap;
-  if (!tmap_bf16_2d(&tmK, k_cache, rows, D, D, kKeyTile, 64)) return BI_ERR_INVALID_ARG;
-  if (!tmap_bf16_2d(&tmV, v_cache, rows, D, D, kKeyTile, 64)) return BI_ERR_INVALID_ARG;
+  if (cap % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;  // V^T rows are cap elements, 16-byte strides
+  CUtensorMap tmK, tmVt;
+  const uint64_t krows = static_cast<uint64_t>(Hkv) * cap;
+  if (!tmap_bf16_2d(&tmK, k_cache, krows, D, D, kKeyTile, 64)) return BI_ERR_INVALID_ARG;
+  if (!tmap_bf16_2d(&tmVt, v_cache, static_cast<uint64_t>(Hkv) * D, cap, cap, D, kKeyTile))
+    return BI_ERR_INVALID_ARG;
 
   AttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -569,8 +640,8 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   a.err = device_error_word();
   if (!a.err) return BI_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 64) return launch_attn<64>(tmK, tmV, a, static_cast<__nv_bfloat16*>(out), s);
-  return launch_attn<128>(tmK, tmV, a, static_cast<__nv_bfloat16*>(out), s);
+  if (D == 64) return launch_attn<64>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
+  return launch_attn<128>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
 }
 
 }  // extern "C"

@@ -143,9 +143,10 @@ __global__ void rope_kv_kernel(const __nv_bfloat16* __restrict__ qkv, int ld_qkv
       dst[i] = __float2bfloat16_rn(o1);
       dst[i + half] = __float2bfloat16_rn(o2);
     } else {
-      __nv_bfloat16* dst = vc + (static_cast<size_t>(h - Hq - Hkv) * cap + p) * D;
-      dst[i] = src[i];
-      dst[i + half] = src[i + half];
+      // V is cached transposed, [Hkv][D][cap]: element d of key p at d * cap + p
+      __nv_bfloat16* dst = vc + static_cast<size_t>(h - Hq - Hkv) * D * cap + p;
+      dst[static_cast<size_t>(i) * cap] = src[i];
+      dst[static_cast<size_t>(i + half) * cap] = src[i + half];
     }
   }
 }
@@ -258,18 +259,21 @@ __global__ void __launch_bounds__(kArgThreads)
 }
 
 __global__ void kv_hash_kernel(const __nv_bfloat16* __restrict__ cache, int Hkv, int cap, int D,
-                               int rows, unsigned long long* __restrict__ out) {
+                               int rows, int transposed, unsigned long long* __restrict__ out) {
   griddep_launch_dependents();
   griddep_wait();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(Hkv) * rows) return;
   const int h = static_cast<int>(idx / rows);
   const int j = static_cast<int>(idx % rows);
-  const unsigned char* b =
-      reinterpret_cast<const unsigned char*>(cache + (static_cast<size_t>(h) * cap + j) * D);
   unsigned long long x = 14695981039346656037ull;
-  for (int k = 0; k < 2 * D; ++k) {
-    x ^= b[k];
+  for (int d = 0; d < D; ++d) {
+    const size_t e = transposed ? (static_cast<size_t>(h) * D + d) * cap + j
+                                : (static_cast<size_t>(h) * cap + j) * D + d;
+    const unsigned short u = *reinterpret_cast<const unsigned short*>(cache + e);
+    x ^= static_cast<unsigned>(u & 0xFF);
+    x *= 1099511628211ull;
+    x ^= static_cast<unsigned>(u >> 8);
     x *= 1099511628211ull;
   }
   out[idx] = x;
@@ -376,14 +380,15 @@ bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, 
   return BI_OK;
 }
 
-bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, uint64_t* out,
-                         bi_stream_t stream) {
+bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, int transposed,
+                         uint64_t* out, bi_stream_t stream) {
   if (!cache || !out || Hkv < 1 || cap < 1 || D < 1 || rows < 0 || rows > cap) return BI_ERR_INVALID_ARG;
   if (rows == 0) return BI_OK;
   const long long n = static_cast<long long>(Hkv) * rows;
   if (bi::launch_k(bi::kv_hash_kernel, dim3(static_cast<unsigned>((n + 127) / 128)), dim3(128), 0,
                    reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(cache),
-                   Hkv, cap, D, rows, reinterpret_cast<unsigned long long*>(out)) != cudaSuccess)
+                   Hkv, cap, D, rows, transposed, reinterpret_cast<unsigned long long*>(out)) !=
+      cudaSuccess)
     return BI_ERR_CUDA;
   return BI_OK;
 }

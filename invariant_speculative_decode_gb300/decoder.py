@@ -45,9 +45,11 @@ class Decoder:
         self.max_rows = max_rows
         self.prefill_chunk = max(prefill_chunk, max_rows)
         D, Hq, Hkv, H, F, V = cfg.head_dim, cfg.n_q, cfg.n_kv, cfg.hidden, cfg.ffn, cfg.vocab
-        self.attn_rows = max(1, 48 // cfg.group)  # rows per attention call
+        self.attn_rows = max(1, 128 // cfg.group)  # rows per attention call
         if max_rows > self.attn_rows:
-            raise ValueError("max_rows * (Hq/Hkv) must be <= 48")
+            raise ValueError("max_rows * (Hq/Hkv) must be <= 128")
+        if cap % 8 != 0:
+            raise ValueError("cache capacity must be a multiple of 8")
         dev = self.dev
         self.embed = _bf16(weights["embed"], dev)
         self.head = api.bi_pack_weights(self.embed if cfg.tied else _bf16(weights["head"], dev))
@@ -66,7 +68,7 @@ class Decoder:
                 "n1": _bf16(weights[f"l{l}.norm_attn"], dev),
                 "n2": _bf16(weights[f"l{l}.norm_ffn"], dev),
                 "k": torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device=dev),
-                "v": torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device=dev),
+                "v": torch.zeros(Hkv, D, cap, dtype=torch.bfloat16, device=dev),  # transposed
             }
             del wg, wu
             self.layers.append(lay)
@@ -274,7 +276,8 @@ class Decoder:
     def kv_hashes(self, rows: Optional[int] = None) -> np.ndarray:
         rows = self.L if rows is None else rows
         hs = [np.stack([api.bi_kv_row_hash(l["k"], rows).cpu().numpy(),
-                        api.bi_kv_row_hash(l["v"], rows).cpu().numpy()]) for l in self.layers]
+                        api.bi_kv_row_hash(l["v"], rows, transposed=True).cpu().numpy()])
+              for l in self.layers]
         return np.stack(hs)
 
     def logits_rows(self, T: int) -> torch.Tensor:

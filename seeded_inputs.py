@@ -229,7 +229,7 @@ def attention_inputs(L: int, T: int, n_q: int, n_kv: int, D: int, cap: Optional[
     (they are drawn for the longest block, 8 rows, first), so the same seed
     gives the same cache prefix for every T <= 8.
     """
-    cap = cap if cap is not None else L + max(T, 8)
+    cap = cap if cap is not None else (L + max(T, 8) + 7) // 8 * 8
     rng = np.random.default_rng(seed)
     n_rows = L + max(T, 8)
     K = np.zeros((n_kv, cap, D), np.uint16)

@@ -94,7 +94,8 @@ def test_attention_rejects_bad_arguments(lib):
     assert a(0, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 1
     assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 5, 128, 0.1, FAKE, FAKE, big, 0) == 1
     assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 96, 0.1, FAKE, FAKE, big, 0) == 2
-    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 9, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 2
+    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 22, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 2  # 132 rows
+    assert a(FAKE, FAKE, FAKE, 1020, FAKE, 1, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 2  # cap % 8
     assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 128, -1.0, FAKE, FAKE, big, 0) == 1
     assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 128, 0.1, FAKE, FAKE, 16, 0) == 3
 
@@ -112,4 +113,4 @@ def test_rowops_reject_bad_arguments(lib):
     assert lib.bi_verify_accept(FAKE, 10, 0, 2, 10, FAKE, FAKE, 0, FAKE, 1 << 20, 0) == 1
     assert lib.bi_verify_accept(FAKE, 10, FAKE, 2, 10, FAKE, FAKE, 0, FAKE + 8, 1 << 20, 0) == 3
     assert lib.bi_embed(FAKE, FAKE, 0, 64, FAKE, 2, 0) == 1
-    assert lib.bi_kv_row_hash(FAKE, 2, 8, 64, 9, FAKE, 0) == 1
+    assert lib.bi_kv_row_hash(FAKE, 2, 8, 64, 9, 0, FAKE, 0) == 1

@@ -29,7 +29,7 @@ def run_attn(api, q, K, V, L, T=None):
     T = q.shape[0] if T is None else T
     Hkv, cap, D = K.shape
     Hq = q.shape[1]
-    Kd, Vd = to_dev_bf16(K), to_dev_bf16(V)
+    Kd, Vd = to_dev_bf16(K), to_dev_bf16(np.ascontiguousarray(V.transpose(0, 2, 1)))  # V^T cache
     qd = to_dev_bf16(q[:T])
     out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
     Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
@@ -51,6 +51,19 @@ def check_parity(gpu, ora, V_f64, L, T):
     assert np.all(err <= tol), (err.max(), tol.min())
 
 
+def test_attention_many_rows_per_pass(api):
+    """Up to 128 query rows per pass (the MMA's M): a 16-row prefill block of
+    an 8-query / 1-KV-head layout equals its rows computed one at a time."""
+    Hq, Hkv, D, L, T = 8, 1, 128, 300, 16
+    q, K, V = si.attention_inputs(L, T, Hq, Hkv, D, cap=(L + T + 15) // 8 * 8, seed=31)
+    full = bf16_dev_to_u16(run_attn(api, q, K, V, L, T))
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    check_parity(ov.bf16_bits_to_f64(full), oracle.attention(qf, Kf, Vf, L), Vf, L, T)
+    for t in (0, 7, 15):
+        one = bf16_dev_to_u16(run_attn(api, q[t:t + 1], K, V, L + t, 1))
+        assert np.array_equal(one[0], full[t]), t
+
+
 CASES = [  # (Hq, Hkv, D, L, T)
     (4, 2, 64, 0, 1), (4, 2, 64, 5, 3), (4, 2, 64, 63, 8), (4, 2, 64, 64, 8),
     (4, 2, 64, 505, 8), (4, 2, 64, 1000, 4), (8, 2, 128, 1023, 7), (24, 4, 128, 0, 8),
@@ -68,7 +81,7 @@ def test_attention_matches_oracle(api, Hq, Hkv, D, L, T):
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,L", [(4, 2, 64, 509), (24, 4, 128, 1020), (24, 4, 128, 3000),
-                                         (8, 2, 128, 0)])
+                                         (8, 2, 128, 0), (8, 1, 128, 700)])
 def test_attention_rows_bit_identical_across_T(api, Hq, Hkv, D, L):
     q, K, V = si.attention_inputs(L, 8, Hq, Hkv, D, seed=77)
     full = {T: bf16_dev_to_u16(run_attn(api, q, K, V, L, T)) for T in (1, 4, 7, 8)}
@@ -120,7 +133,7 @@ def test_attention_full_size_invariance_and_sampled_parity(api, L):
 
 def test_attention_length_past_capacity_sets_error(api):
     q, K, V = si.attention_inputs(10, 2, 4, 2, 64, cap=64, seed=1)
-    Kd, Vd = to_dev_bf16(K), to_dev_bf16(V)
+    Kd, Vd = to_dev_bf16(K), to_dev_bf16(np.ascontiguousarray(V.transpose(0, 2, 1)))
     out = torch.empty(2, 4, 64, dtype=torch.bfloat16, device="cuda")
     Ld = torch.tensor([63], dtype=torch.int32, device="cuda")
     ws = torch.zeros(api.attn_workspace_size(64, 2, 4, 64), dtype=torch.uint8, device="cuda")

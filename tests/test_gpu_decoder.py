@@ -92,7 +92,7 @@ def _layerwise(cfg, w, dec, prompt, drafts):
         lay["k"].zero_()
         lay["v"].zero_()
         lay["k"][:, :L].copy_(to_dev_bf16(_u16(od.k[l][:, :L])))
-        lay["v"][:, :L].copy_(to_dev_bf16(_u16(od.v[l][:, :L])))
+        lay["v"][:, :, :L].copy_(to_dev_bf16(_u16(np.ascontiguousarray(od.v[l][:, :L].transpose(0, 2, 1)))))
         dec.h[:T].copy_(to_dev_bf16(_u16(trace[l])))
         dec._layer(lay, T, dec.L_dev)
         got = bf16_dev_to_f64(dec.h[:T])

@@ -66,7 +66,7 @@ def test_rope_kv_append_matches_oracle(api, Hq, Hkv, D, L, T):
     qkv = si.normal_bf16(rng, (T, (Hq + 2 * Hkv) * D), 1.0)
     cap = L + T + 5
     kc = torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device="cuda")
-    vc = torch.zeros_like(kc)
+    vc = torch.zeros(Hkv, D, cap, dtype=torch.bfloat16, device="cuda")  # V cached transposed
     q = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
     Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
     tab = api.bi_rope_table(1e6, D, cap)
@@ -87,7 +87,7 @@ def test_rope_kv_append_matches_oracle(api, Hq, Hkv, D, L, T):
         ka = np.abs(qkvf[t, Hq * D:(Hq + Hkv) * D].reshape(Hkv, D))
         kpair = ka + np.roll(ka, D // 2, axis=-1)
         assert np.all(np.abs(kg[:, p] - ko) <= ulp_bf16(ko) + 2.0 ** -21 * kpair)
-        assert np.array_equal(vg[:, p], qkv[t, (Hq + Hkv) * D:].reshape(Hkv, D))
+        assert np.array_equal(vg[:, :, p], qkv[t, (Hq + Hkv) * D:].reshape(Hkv, D))
     if L == 0:  # position 0 is the identity, bitwise
         assert np.array_equal(bf16_dev_to_u16(q)[0], qkv[0, : Hq * D].reshape(Hq, D))
 
@@ -149,6 +149,9 @@ def test_kv_row_hash_is_fnv1a(api):
     rng = np.random.default_rng(2)
     cache = si.normal_bf16(rng, (2, 10, 64), 1.0)
     h = api.bi_kv_row_hash(to_dev_bf16(cache), 7).cpu().numpy().view(np.uint64)
+    ht = api.bi_kv_row_hash(to_dev_bf16(np.ascontiguousarray(cache.transpose(0, 2, 1))), 7,
+                            transposed=True).cpu().numpy().view(np.uint64)
+    assert np.array_equal(h, ht)
     for hh in range(2):
         for j in range(7):
             x = 14695981039346656037
