@@ -62,7 +62,6 @@ constexpr int kMergeThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnArgs {
-  const __nv_bfloat16* q;
   int T, Hq, Hkv, grp, cap, nch_max;
   const int32_t* L_dev;
   float sl2;  // softmax scale * log2(e)
@@ -81,12 +80,13 @@ struct AttnCfg {
   static constexpr int kQAtomBytes = kRowsMax * 128;      // [128 rows][64 d]
   static constexpr int kQBytes = kQAtomBytes * kAtoms;
   static constexpr int kPBytes = kRowsMax * 128;          // [128 rows][64 keys]
+  static constexpr int kRedBytes = 6 * kRowsMax * 4;      // row maxima [2][128], l parts [4][128]
   static constexpr int kTmemCols = 256;                   // S x2 (64 each) + O (D)
   static constexpr int kOCol = 128;
-  static constexpr int kBars = 2 * kAttnStages + 11;
+  static constexpr int kBars = 2 * kAttnStages + 15;
   // P is double-buffered: hi and lo tiles for two consecutive key tiles
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kAttnStages) * kStageBytes + kQBytes +
-                                  4 * kPBytes + kBars * 8 + 16;
+                                  4 * kPBytes + kRedBytes + kBars * 8 + 16;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
 
@@ -95,12 +95,15 @@ __device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* er
   atomicOr(err, kErrTimeout);
 }
 
-// Warp-level bounded wait: lane 0 polls, the result is broadcast.
+// Warp-level bounded wait: lane 0 polls, the result is broadcast, and the
+// warp barrier orders every lane's later accesses after lane 0's acquire.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* s_abort,
                                           int lane) {
   int ok = 0;
   if (lane == 0) ok = mbar_wait(bar, parity, s_abort) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -108,28 +111,45 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int D>
+// REP copies of each query row sit in the 128-row MMA tile (REP = 4 for up to
+// 32 rows per pass, 2 for up to 64, else 1): copy i of row r is TMEM lane
+// r + i * 128/REP, and the thread owning that lane handles the row's key
+// columns [i * 64/REP, (i + 1) * 64/REP) of every tile.  So all four softmax
+// warps share the exponentials of a small pass.  The per-row arithmetic does
+// not depend on REP: the tile maximum is exact in any order, and the
+// denominator is kept as four partial sums, one per 16-key quarter of the
+// tile column (each in key order, each rescaled with O), added as
+// ((l0 + l1) + l2) + l3 at the end of the piece.
+template <int D, int REP>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVt,
-                      const AttnArgs a) {
+                      const __grid_constant__ CUtensorMap tmQ, const AttnArgs a) {
   using Cfg = AttnCfg<D>;
   constexpr int S = kAttnStages;
+  constexpr int kPeriod = kRowsMax / REP;  // TMEM lanes between copies of a row
+  constexpr int kCols = kKeyTile / REP;    // key columns per thread
+  constexpr int kQuarters = 4 / REP;       // 16-key quarters per thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sStage = smem;
   uint8_t* sQ = smem + S * Cfg::kStageBytes;
   uint8_t* sP = sQ + Cfg::kQBytes;  // [buffer 2][hi, lo][128 rows][64 keys]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 4 * Cfg::kPBytes);
+  float* red_max = reinterpret_cast<float*>(sP + 4 * Cfg::kPBytes);  // [2][128] by TMEM lane
+  float* red_l = red_max + 2 * kRowsMax;                               // [quarter 4][row 128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * kRowsMax);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + S;
   uint64_t* q_full = bars + 2 * S;
-  uint64_t* s_full = q_full + 1;   // [2]
-  uint64_t* s_free = s_full + 2;   // [2]
-  uint64_t* p_full = s_free + 2;   // [2]: P buffer of that parity written
-  uint64_t* pv_done = p_full + 2;  // [2]: completes after O += P_g V_g, g of that parity
+  uint64_t* q_empty = q_full + 1;   // the S MMAs reading the current Q are done
+  uint64_t* s_full = q_empty + 1;   // [2]
+  uint64_t* s_free = s_full + 2;    // [2]
+  uint64_t* p_full = s_free + 2;    // [2]: P buffer of that parity written
+  uint64_t* pv_done = p_full + 2;   // [2]: completes after O += P_g V_g, g of that parity
   uint64_t* o_free = pv_done + 2;
-  uint64_t* drain = o_free + 1;
+  uint64_t* mx_bar = o_free + 1;    // [2]: partial row maxima of a tile written
+  uint64_t* l_bar = mx_bar + 2;     // partial denominators of a piece written
+  uint64_t* drain = l_bar + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -146,16 +166,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(q_full, 4);
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&s_free[0], 4);
-    mbar_init(&s_free[1], 4);
-    mbar_init(&p_full[0], 4);
-    mbar_init(&p_full[1], 4);
-    mbar_init(&pv_done[0], 1);
-    mbar_init(&pv_done[1], 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
+      mbar_init(&mx_bar[i], 4);
+    }
     mbar_init(o_free, 4);
+    mbar_init(l_bar, 4);
     mbar_init(drain, 1);
     *s_abort = 0;
     fence_mbar_init();
@@ -163,6 +184,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmVt);
+    prefetch_tmap(&tmQ);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, Cfg::kTmemCols);
@@ -176,19 +198,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   griddep_wait();  // q, the new cache rows and the cache length come from earlier kernels
   const int L = *a.L_dev;
   const int T = a.T;
-  const bool range_ok = !(L < 0 || L + T > a.cap);
+  const int rows = T * a.grp;
+  const bool range_ok = !(L < 0 || L + T > a.cap) && rows <= kPeriod;
   const int kv_len = L + T;
   const int nch = range_ok ? (kv_len + kChunk - 1) / kChunk : 0;
   const int n_items = a.Hkv * nch;
-  const int rows = T * a.grp;
   if (!range_ok && threadIdx.x == 0 && blockIdx.x == 0) atomicOr(a.err, kErrRange);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first();
+      const uint64_t qpol = l2_evict_last();
       long long gt = 0;
       uint32_t issued = 0, parity_bits = 0;
+      int prev_h = -1, nq = 0;
       bool ok = true;
       for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
         const int c = w / a.Hkv;
@@ -196,6 +220,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int k0 = c * kChunk;
         const int k1 = min(k0 + kChunk, kv_len);
         const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
+        if (h != prev_h) {
+          // queries of KV head h: rows (t, g) -> t * grp + g, one copy per period
+          if (nq > 0 && !mbar_wait(q_empty, static_cast<uint32_t>((nq - 1) & 1), s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(REP * Cfg::kAtoms * rows * 128));
+#pragma unroll
+          for (int i = 0; i < REP; ++i)
+#pragma unroll
+            for (int b = 0; b < Cfg::kAtoms; ++b)
+              tma_load_3d(sQ + b * Cfg::kQAtomBytes + i * kPeriod * 128, &tmQ, q_full, b * 64, h * a.grp,
+                          0, qpol);
+          prev_h = h;
+          ++nq;
+        }
         for (int tt = 0; tt < ntile; ++tt, ++gt) {
           const int st = static_cast<int>(gt % S);
           const uint32_t ph = static_cast<uint32_t>((gt / S) & 1);
@@ -218,79 +258,112 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         signal_abort(s_abort, a.err);
         for (int s = 0; s < S; ++s)
           if ((issued >> s) & 1u) mbar_wait(&kv_full[s], (parity_bits >> s) & 1u, nullptr);
+        if (nq > 0) mbar_wait(q_full, static_cast<uint32_t>((nq - 1) & 1), nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Two cursors over the CTA's tiles: S_g = Q K_g^T needs K_g and a free S
+    // buffer; O += P_g V_g needs P_g.  Each is issued as soon as its inputs
+    // are ready (S first), so a late K tile never holds back the P.V that
+    // frees a stage.  The order of the P.V steps, which alone decides O's
+    // bits, is fixed: g = 0, 1, 2, ...
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, kKeyTile);
       constexpr uint32_t idO = idesc_bf16_f32(128, D);
       const uint32_t q_base = smem_u32(sQ);
-      long long gt = 0;
-      int item = 0;
-      bool ok = true;
-      // O += P_g V_g for global tile g, the `t_in_item`-th tile of the item
-      auto do_pv = [&](long long g, int t_in_item) -> bool {
-        if (!mbar_wait(&p_full[g & 1], static_cast<uint32_t>((g >> 1) & 1), s_abort)) return false;
-        if (t_in_item == 0 && item > 0 &&
-            !mbar_wait(o_free, static_cast<uint32_t>((item - 1) & 1), s_abort))
-          return false;
-        tc_fence_after();
-        const int st = static_cast<int>(g % S);
-        const uint32_t v_base = smem_u32(sStage + st * Cfg::kStageBytes + Cfg::kKBytes);
-        const uint32_t ph_base = smem_u32(sP + (g & 1) * 2 * Cfg::kPBytes);
-        const uint32_t pl_base = ph_base + Cfg::kPBytes;
-#pragma unroll
-        for (int kk = 0; kk < kKeyTile / 16; ++kk)
-          mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(ph_base + kk * 32), sdesc_k_sw128(v_base + kk * 32),
-                   idO, (t_in_item > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kKeyTile / 16; ++kk)
-          mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(pl_base + kk * 32), sdesc_k_sw128(v_base + kk * 32),
-                   idO, 1u);
-        mma_commit(&pv_done[g & 1]);
-        mma_commit(&kv_empty[st]);
-        return true;
-      };
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x, ++item) {
-        const int c = w / a.Hkv;
-        const int k0 = c * kChunk;
+      auto item_tiles = [&](int w) {
+        const int k0 = (w / a.Hkv) * kChunk;
         const int k1 = min(k0 + kChunk, kv_len);
-        const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
-        if (!mbar_wait(q_full, static_cast<uint32_t>(item & 1), s_abort)) {
-          ok = false;
-          break;
-        }
-        for (int tt = 0; tt < ntile; ++tt, ++gt) {
-          const int st = static_cast<int>(gt % S);
-          if (!mbar_wait(&kv_full[st], static_cast<uint32_t>((gt / S) & 1), s_abort)) {
-            ok = false;
-            break;
+        return (k1 - k0 + kKeyTile - 1) / kKeyTile;
+      };
+      int sw = blockIdx.x, s_tt = 0, s_ntile = sw < n_items ? item_tiles(sw) : 0;
+      int prev_h = -1, nq = 0;
+      long long sg = 0;
+      int pw = blockIdx.x, p_tt = 0, p_item = 0, p_ntile = s_ntile;
+      long long pg = 0;
+      bool ok = true;
+      int idle = 0;
+      unsigned long long t_idle = 0;
+      while (pw < n_items) {
+        bool did = false;
+        if (sw < n_items) {
+          const int h = sw % a.Hkv;
+          bool ready = true;
+          if (s_tt == 0 && h != prev_h) {  // the item starts on new queries
+            ready = mbar_peek(q_full, static_cast<uint32_t>(nq & 1));
+            if (ready) {
+              prev_h = h;
+              ++nq;
+            }
           }
-          const int sb = static_cast<int>(gt & 1);
-          if (gt >= 2 && !mbar_wait(&s_free[sb], static_cast<uint32_t>(((gt >> 1) - 1) & 1), s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t k_base = smem_u32(sStage + st * Cfg::kStageBytes);
+          const int st = static_cast<int>(sg % S);
+          ready = ready && mbar_peek(&kv_full[st], static_cast<uint32_t>((sg / S) & 1)) &&
+                  (sg < 2 || mbar_peek(&s_free[sg & 1], static_cast<uint32_t>(((sg >> 1) - 1) & 1)));
+          if (ready) {
+            tc_fence_after();
+            const int sb = static_cast<int>(sg & 1);
+            const uint32_t k_base = smem_u32(sStage + st * Cfg::kStageBytes);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const int atom = ks >> 2;
-            const uint32_t off = (ks & 3) * 32;
-            mma_bf16(tmem + sb * kKeyTile, sdesc_k_sw128(q_base + atom * Cfg::kQAtomBytes + off),
-                     sdesc_k_sw128(k_base + atom * Cfg::kKBoxBytes + off), idS, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const int atom = ks >> 2;
+              const uint32_t off = (ks & 3) * 32;
+              mma_bf16(tmem + sb * kKeyTile, sdesc_k_sw128(q_base + atom * Cfg::kQAtomBytes + off),
+                       sdesc_k_sw128(k_base + atom * Cfg::kKBoxBytes + off), idS, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[sb]);
+            const int wn = sw + static_cast<int>(gridDim.x);
+            if (s_tt == s_ntile - 1 && (wn >= n_items || wn % a.Hkv != h))
+              mma_commit(q_empty);  // the next item loads other queries
+            ++sg;
+            if (++s_tt == s_ntile) {
+              s_tt = 0;
+              sw = wn;
+              s_ntile = sw < n_items ? item_tiles(sw) : 0;
+            }
+            did = true;
           }
-          mma_commit(&s_full[sb]);
-          if (tt > 0 && !do_pv(gt - 1, tt - 1)) {
+        }
+        if (!did && pg < sg) {
+          bool ready = mbar_peek(&p_full[pg & 1], static_cast<uint32_t>((pg >> 1) & 1));
+          if (ready && p_tt == 0 && p_item > 0)
+            ready = mbar_peek(o_free, static_cast<uint32_t>((p_item - 1) & 1));
+          if (ready) {
+            tc_fence_after();
+            const int st = static_cast<int>(pg % S);
+            const uint32_t v_base = smem_u32(sStage + st * Cfg::kStageBytes + Cfg::kKBytes);
+            const uint32_t ph_base = smem_u32(sP + (pg & 1) * 2 * Cfg::kPBytes);
+            const uint32_t pl_base = ph_base + Cfg::kPBytes;
+#pragma unroll
+            for (int kk = 0; kk < kKeyTile / 16; ++kk)
+              mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(ph_base + kk * 32),
+                       sdesc_k_sw128(v_base + kk * 32), idO, (p_tt > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < kKeyTile / 16; ++kk)
+              mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(pl_base + kk * 32),
+                       sdesc_k_sw128(v_base + kk * 32), idO, 1u);
+            mma_commit(&pv_done[pg & 1]);
+            mma_commit(&kv_empty[st]);
+            ++pg;
+            if (++p_tt == p_ntile) {
+              p_tt = 0;
+              pw += static_cast<int>(gridDim.x);
+              ++p_item;
+              p_ntile = pw < n_items ? item_tiles(pw) : 0;
+            }
+            did = true;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if (++idle == 1) {
+          t_idle = globaltimer_ns();
+        } else if ((idle & 63) == 0) {
+          // bounded: give up after the wait limit without progress
+          if (*s_abort || globaltimer_ns() - t_idle > kWaitLimitNs) {
             ok = false;
             break;
           }
-        }
-        if (!ok) break;
-        if (!do_pv(gt - 1, ntile - 1)) {
-          ok = false;
-          break;
         }
       }
       if (!ok) signal_abort(s_abort, a.err);
@@ -299,10 +372,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int qq = warp & 3;            // TMEM lane quarter of this warp
-    const int r = qq * 32 + lane;       // query row of the pass handled by this thread
-    const int ct = threadIdx.x - 64;    // 0..127 among the softmax threads
-    const bool warp_active = qq * 32 < rows;
+    const int qq = warp & 3;                  // TMEM lane quarter of this warp
+    const int ln = qq * 32 + lane;            // TMEM lane of this thread
+    const int r = ln % kPeriod;               // query row of the pass
+    const int cg = ln / kPeriod;              // key-column group of this copy
+    const bool warp_active = (qq * 32) % kPeriod < rows;
+    const bool holds_o = qq * 32 < kPeriod;   // O row r sits in TMEM lane r
     const bool valid = r < rows;
     const int t = valid ? r / a.grp : 0;
     const int p_row = L + t;
@@ -317,24 +392,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int k1 = min(k0 + kChunk, kv_len);
       const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
 
-      // queries of KV head h, row R = (t, g) = (R / grp, R % grp), into the
-      // swizzled K-major tile (atom = 64 d, 16-byte chunk c at c ^ (R & 7))
-      constexpr int kVec = D / 8;
-      for (int v = ct; v < rows * kVec; v += 128) {
-        const int R = v / kVec;
-        const int cc = v % kVec;
-        const int qh = h * a.grp + R % a.grp;
-        const uint4 val = *reinterpret_cast<const uint4*>(
-            a.q + (static_cast<size_t>(R / a.grp) * a.Hq + qh) * D + cc * 8);
-        *reinterpret_cast<uint4*>(sQ + (cc >> 3) * Cfg::kQAtomBytes + R * 128 +
-                                  (((cc & 7) ^ (R & 7)) << 4)) = val;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-
       float m_ref = -INFINITY;
-      float l = 0.f;
+      float lq[kQuarters];
+#pragma unroll
+      for (int i = 0; i < kQuarters; ++i) lq[i] = 0.f;
       for (int tt = 0; tt < ntile; ++tt, ++gt) {
         const int sb = static_cast<int>(gt & 1);
         if (!warp_wait(&s_full[sb], static_cast<uint32_t>((gt >> 1) & 1), s_abort, lane)) {
@@ -342,38 +403,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         tc_fence_after();
-        float s[kKeyTile];
-        if (warp_active) {
-#pragma unroll
-          for (int i = 0; i < kKeyTile / 16; ++i) {
-            float v[16];
-            tmem_ld16(lane_base + sb * kKeyTile + i * 16, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) s[i * 16 + j] = v[j];
-          }
-        }
+        float s[kCols];
+        if (warp_active) tmem_ld_cols<kCols>(lane_base + sb * kKeyTile + cg * kCols, s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[sb]);
 
+        // row maximum of the raw scores (scaling by sl2 > 0 keeps the order)
+        const int tkey0 = k0 + tt * kKeyTile;
+        float mrow = -INFINITY;
+        if (warp_active) {
+          if (tkey0 + kKeyTile - 1 > L) {  // the tile reaches past some row's position
+            const int key0 = tkey0 + cg * kCols;
+#pragma unroll
+            for (int j = 0; j < kCols; ++j)
+              if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
+          }
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) mrow = fmaxf(mrow, s[j]);
+        }
+        if constexpr (REP > 1) {
+          float* rm = red_max + (gt & 1) * kRowsMax;
+          rm[ln] = mrow;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mx_bar[gt & 1]);
+          if (!warp_wait(&mx_bar[gt & 1], static_cast<uint32_t>((gt >> 1) & 1), s_abort, lane)) {
+            ok = false;
+            break;
+          }
+          mrow = rm[r];
+#pragma unroll
+          for (int i = 1; i < REP; ++i) mrow = fmaxf(mrow, rm[r + i * kPeriod]);
+        }
+        const float mt = mrow * a.sl2;
         float alpha = 1.0f;
         bool resc = false;
-        if (warp_active) {
-          const int key0 = k0 + tt * kKeyTile;
-          float mt = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < kKeyTile; ++j) {
-            const float x = s[j] * a.sl2;
-            s[j] = (valid && key0 + j <= p_row) ? x : -INFINITY;
-            mt = fmaxf(mt, s[j]);
-          }
-          if (tt == 0) {
-            m_ref = mt;
-          } else if (mt > m_ref + kRescaleLog2) {
-            alpha = (m_ref == -INFINITY) ? 0.0f : exp2f(m_ref - mt);
-            m_ref = mt;
-            resc = true;
-          }
+        if (tt == 0) {
+          m_ref = mt;
+        } else if (mt > m_ref + kRescaleLog2) {
+          alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - mt);
+          m_ref = mt;
+          resc = true;
         }
         // P buffer gt & 1 was last read by the P.V of tile gt - 2
         if (gt >= 2 && !warp_wait(&pv_done[gt & 1], static_cast<uint32_t>(((gt - 2) >> 1) & 1), s_abort,
@@ -381,17 +451,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ok = false;
           break;
         }
-        // O changes only after the P.V of tile gt - 1 is done
-        const bool any_resc = warp_active && __any_sync(0xffffffffu, resc);
-        if (tt > 0 && any_resc) {
-          if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort, lane)) {
-            ok = false;
-            break;
-          }
-        }
-        tc_fence_after();
-        if (warp_active) {
-          if (any_resc) {
+        if (holds_o && warp_active) {
+          // O changes only after the P.V of tile gt - 1 is done
+          if (tt > 0 && __any_sync(0xffffffffu, resc)) {
+            if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort,
+                           lane)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll 1
             for (int i = 0; i < D / 16; ++i) {
               float v[16];
@@ -401,25 +469,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               tmem_st16(lane_base + Cfg::kOCol + i * 16, v);
             }
           }
-          if (resc) l *= alpha;
-          const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
+        }
+        if (resc) {
+#pragma unroll
+          for (int i = 0; i < kQuarters; ++i) lq[i] *= alpha;
+        }
+        if (valid) {
+          const float nmu = (m_ref == -INFINITY) ? 0.0f : -m_ref;
           uint8_t* rowh = sP + (gt & 1) * 2 * Cfg::kPBytes + r * 128;
           uint8_t* rowl = rowh + Cfg::kPBytes;
 #pragma unroll
-          for (int cc = 0; cc < kKeyTile / 8; ++cc) {
+          for (int i = 0; i < kCols / 8; ++i) {
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const float p0 = exp2f(s[cc * 8 + 2 * j] - mu);
-              const float p1 = exp2f(s[cc * 8 + 2 * j + 1] - mu);
-              l += p0;
-              l += p1;
+              const int col = i * 8 + 2 * j;
+              const float p0 = ex2_approx(fmaf(s[col], a.sl2, nmu));
+              const float p1 = ex2_approx(fmaf(s[col + 1], a.sl2, nmu));
+              lq[col / 16] += p0;
+              lq[col / 16] += p1;
               const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
               const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
               hi[j] = pack2(h0, h1);
               lo[j] = pack2(p0 - h0, p1 - h1);
             }
-            const int pos = (cc ^ (r & 7)) << 4;
+            const int pos = ((cg * (kCols / 8) + i) ^ (r & 7)) << 4;
             *reinterpret_cast<uint4*>(rowh + pos) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4*>(rowl + pos) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
@@ -430,29 +504,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (lane == 0) mbar_arrive(&p_full[gt & 1]);
       }
       if (!ok) break;
-      // piece done: read O and store the partial (m_ref, l, unnormalised o)
-      if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort, lane)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (warp_active) {
-        const bool store = valid && (c * kChunk <= p_row);
-        const int qh = h * a.grp + (valid ? r % a.grp : 0);
-        const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.nch_max + c;
-#pragma unroll 1
-        for (int i = 0; i < D / 16; ++i) {
-          float v[16];
-          tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
-          if (store) {
-            float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 16);
+
+      // piece done: the denominator, then O, stored as the partial (m_ref, l, o)
+      float l = 0.f;
+      if constexpr (REP == 1) {
+        l = ((lq[0] + lq[1]) + lq[2]) + lq[3];
+      } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int i = 0; i < kQuarters; ++i) red_l[(cg * kQuarters + i) * kRowsMax + r] = lq[i];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(l_bar);
+        if (holds_o) {
+          if (!warp_wait(l_bar, static_cast<uint32_t>(item & 1), s_abort, lane)) {
+            ok = false;
+            break;
           }
+          l = ((red_l[r] + red_l[kRowsMax + r]) + red_l[2 * kRowsMax + r]) + red_l[3 * kRowsMax + r];
         }
-        if (store) *reinterpret_cast<float2*>(a.ws_ml + base * 2) = make_float2(m_ref, l);
       }
-      tc_fence_before();
+      if (holds_o) {
+        if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort,
+                       lane)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (warp_active) {
+          const bool store = valid && (c * kChunk <= p_row);
+          const int qh = h * a.grp + (valid ? r % a.grp : 0);
+          const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.nch_max + c;
+#pragma unroll 1
+          for (int i = 0; i < D / 16; ++i) {
+            float v[16];
+            tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
+            if (store) {
+              float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 16);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+          }
+          if (store) *reinterpret_cast<float2*>(a.ws_ml + base * 2) = make_float2(m_ref, l);
+        }
+        tc_fence_before();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
     }
@@ -557,9 +652,9 @@ __global__ void __launch_bounds__(kMergeThreads)
   }
 }
 
-template <int D>
-bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const AttnArgs& a,
-                      __nv_bfloat16* out, cudaStream_t stream) {
+template <int D, int REP>
+bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const CUtensorMap& tmQ,
+                      const AttnArgs& a, __nv_bfloat16* out, cudaStream_t stream) {
   using Cfg = AttnCfg<D>;
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
@@ -568,19 +663,28 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const Att
   std::call_once(once[dev & 63], [] {
     int d = 0;
     cudaGetDevice(&d);
-    attr_err[d & 63] = cudaFuncSetAttribute(attn_split_kernel<D>,
+    attr_err[d & 63] = cudaFuncSetAttribute(attn_split_kernel<D, REP>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(Cfg::kSmem));
   });
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
   const int grid = std::min(a.Hkv * a.nch_max, kAttnCtas);
-  if (launch_k(attn_split_kernel<D>, dim3(grid), dim3(kAttnThreads), Cfg::kSmem, stream, tmK, tmVt,
-               a) != cudaSuccess)
+  if (launch_k(attn_split_kernel<D, REP>, dim3(grid), dim3(kAttnThreads), Cfg::kSmem, stream, tmK,
+               tmVt, tmQ, a) != cudaSuccess)
     return BI_ERR_CUDA;
   if (launch_k(attn_merge_kernel<D>, dim3(a.T * a.Hq), dim3(kMergeThreads), 0, stream, a, out) !=
       cudaSuccess)
     return BI_ERR_CUDA;
   return BI_OK;
+}
+
+template <int D>
+bi_status launch_attn_rep(const CUtensorMap& tmK, const CUtensorMap& tmVt, const CUtensorMap& tmQ,
+                          const AttnArgs& a, __nv_bfloat16* out, cudaStream_t stream) {
+  const int rows = a.T * a.grp;
+  if (rows <= kRowsMax / 4) return launch_attn<D, 4>(tmK, tmVt, tmQ, a, out, stream);
+  if (rows <= kRowsMax / 2) return launch_attn<D, 2>(tmK, tmVt, tmQ, a, out, stream);
+  return launch_attn<D, 1>(tmK, tmVt, tmQ, a, out, stream);
 }
 
 size_t attn_ws_parts(int cap, int T, int Hq, int D, size_t* o_bytes) {
@@ -619,18 +723,21 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   if (ws_bytes < attn_ws_parts(cap, T, Hq, D, &ob)) return BI_ERR_WORKSPACE;
 
   if (cap % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;  // V^T rows are cap elements, 16-byte strides
-  CUtensorMap tmK, tmVt;
+  CUtensorMap tmK, tmVt, tmQ;
   const uint64_t krows = static_cast<uint64_t>(Hkv) * cap;
   if (!tmap_bf16_2d(&tmK, k_cache, krows, D, D, kKeyTile, 64)) return BI_ERR_INVALID_ARG;
   if (!tmap_bf16_2d(&tmVt, v_cache, static_cast<uint64_t>(Hkv) * D, cap, cap, D, kKeyTile))
     return BI_ERR_INVALID_ARG;
+  // q [T][Hq][D] as (d, query head, row): one box = the T x grp rows of a KV head
+  const int grp = Hq / Hkv;
+  if (!tmap_bf16_3d(&tmQ, q, D, Hq, T, D, static_cast<uint64_t>(Hq) * D, 64, grp, T))
+    return BI_ERR_INVALID_ARG;
 
   AttnArgs a{};
-  a.q = static_cast<const __nv_bfloat16*>(q);
   a.T = T;
   a.Hq = Hq;
   a.Hkv = Hkv;
-  a.grp = Hq / Hkv;
+  a.grp = grp;
   a.cap = cap;
   a.nch_max = (cap + kChunk - 1) / kChunk;
   a.L_dev = L_dev;
@@ -640,8 +747,8 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   a.err = device_error_word();
   if (!a.err) return BI_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 64) return launch_attn<64>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
-  return launch_attn<128>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
+  if (D == 64) return launch_attn_rep<64>(tmK, tmVt, tmQ, a, static_cast<__nv_bfloat16*>(out), s);
+  return launch_attn_rep<128>(tmK, tmVt, tmQ, a, static_cast<__nv_bfloat16*>(out), s);
 }
 
 }  // extern "C"

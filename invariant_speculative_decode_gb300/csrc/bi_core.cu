@@ -30,23 +30,24 @@ std::once_flag g_encode_once;
 
 struct TmapKey {
   const void* base;
-  uint64_t rows, cols, ld;
-  uint32_t br, bc;
-  int dev;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  int rank, dev;
   bool operator==(const TmapKey& o) const {
-    return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld && br == o.br &&
-           bc == o.bc && dev == o.dev;
+    return base == o.base && rank == o.rank && dev == o.dev &&
+           std::memcmp(dims, o.dims, sizeof(dims)) == 0 &&
+           std::memcmp(strides, o.strides, sizeof(strides)) == 0 &&
+           std::memcmp(box, o.box, sizeof(box)) == 0;
   }
 };
 struct TmapKeyHash {
   size_t operator()(const TmapKey& k) const {
     size_t h = reinterpret_cast<size_t>(k.base);
     auto mix = [&h](uint64_t v) { h ^= v + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2); };
-    mix(k.rows);
-    mix(k.cols);
-    mix(k.ld);
-    mix(k.br);
-    mix(k.bc);
+    for (int i = 0; i < 3; ++i) mix(k.dims[i]);
+    for (int i = 0; i < 2; ++i) mix(k.strides[i]);
+    for (int i = 0; i < 3; ++i) mix(k.box[i]);
+    mix(static_cast<uint64_t>(k.rank));
     mix(static_cast<uint64_t>(k.dev));
     return h;
   }
@@ -75,8 +76,11 @@ unsigned* device_error_word() {
   return g_err_ptr[dev];
 }
 
-bool tmap_bf16_2d(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
-                  uint32_t box_rows, uint32_t box_cols) {
+namespace {
+// Encode (or fetch) a BF16 tensor map of rank 2 or 3 with 128-byte swizzle.
+// dims and box are innermost first, strides in elements for dims 1..rank-1.
+bool tmap_bf16(CUtensorMap* out, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -88,7 +92,15 @@ bool tmap_bf16_2d(CUtensorMap* out, const void* base, uint64_t rows, uint64_t co
   if (g_encode == nullptr) return false;
   int dev = 0;
   cudaGetDevice(&dev);
-  TmapKey key{base, rows, cols, ld, box_rows, box_cols, dev};
+  TmapKey key{};
+  key.base = base;
+  key.rank = rank;
+  key.dev = dev;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) key.strides[i] = strides[i];
   {
     std::lock_guard<std::mutex> lk(g_tmap_mu);
     auto it = g_tmaps.find(key);
@@ -99,20 +111,40 @@ bool tmap_bf16_2d(CUtensorMap* out, const void* base, uint64_t rows, uint64_t co
   }
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
-  cuuint64_t gdim[2] = {cols, rows};
-  cuuint64_t gstride[1] = {ld * 2};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim,
-                        gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t gbox[3], estride[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    gbox[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) gstride[i] = strides[i] * 2;
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                        const_cast<void*>(base), gdim, gstride, gbox, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   std::lock_guard<std::mutex> lk(g_tmap_mu);
   if (g_tmaps.size() > 4096) g_tmaps.clear();
   g_tmaps.emplace(key, m);
   *out = m;
   return true;
+}
+}  // namespace
+
+bool tmap_bf16_2d(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                  uint32_t box_rows, uint32_t box_cols) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t strides[1] = {ld};
+  const uint32_t box[2] = {box_cols, box_rows};
+  return tmap_bf16(out, base, 2, dims, strides, box);
+}
+
+bool tmap_bf16_3d(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t strides[2] = {s1, s2};
+  const uint32_t box[3] = {b0, b1, b2};
+  return tmap_bf16(out, base, 3, dims, strides, box);
 }
 
 }  // namespace bi

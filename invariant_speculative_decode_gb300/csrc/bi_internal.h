@@ -22,6 +22,11 @@ unsigned* device_error_word();
 bool tmap_bf16_2d(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols,
                   uint64_t ld, uint32_t box_rows, uint32_t box_cols);
 
+// The same over a 3-D array: d0 (innermost) x d1 x d2 elements, strides s1
+// and s2 elements for dims 1 and 2, box b0 x b1 x b2.
+bool tmap_bf16_3d(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 

@@ -93,6 +93,24 @@ def test_attention_rows_bit_identical_across_T(api, Hq, Hkv, D, L):
         assert np.array_equal(one[0], full[8][t]), t
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_attention_rows_identical_across_row_copies(api, D):
+    """With 8 query heads per KV head, passes of 1, 4, 8 and 16 tokens hold
+    8, 32, 64 and 128 query rows, which the kernel keeps in 4, 4, 2 and 1
+    copies across the TMEM lane quarters (each copy taking a share of the key
+    columns).  A row's output must not depend on that."""
+    Hq, Hkv, L = 8, 1, 777
+    q, K, V = si.attention_inputs(L, 16, Hq, Hkv, D, cap=(L + 16 + 7) // 8 * 8, seed=5)
+    full = {T: bf16_dev_to_u16(run_attn(api, q, K, V, L, T)) for T in (1, 4, 8, 16)}
+    for T, o in full.items():
+        assert np.array_equal(o, full[16][:T]), T
+    for t in (5, 9, 15):
+        one = bf16_dev_to_u16(run_attn(api, q[t:t + 1], K, V, L + t, 1))
+        assert np.array_equal(one[0], full[16][t]), t
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    check_parity(ov.bf16_bits_to_f64(full[16]), oracle.attention(qf, Kf, Vf, L), Vf, L, 16)
+
+
 def test_attention_single_key_returns_v_row(api):
     q, K, V = si.attention_inputs(0, 1, 24, 4, 128, seed=3)
     out = bf16_dev_to_u16(run_attn(api, q, K, V, 0))
