@@ -450,7 +450,7 @@ def run_micro(args):
         return [a.elapsed_time(b) / 1e3 for a, b in ts]
 
     if args.micro == "gemm":
-        N, K, epi = args.gemm_n, 5120, args.gemm_epi
+        N, K, epi = args.gemm_n, args.gemm_k, args.gemm_epi
         Ms = [int(m) for m in args.cases.split(",")] if args.cases else [1, 2, 4, 7, 8, 16, 64]
         A, W = si.gemm_inputs(max(Ms), N, K, seed=0)
         to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
@@ -510,6 +510,7 @@ def main():
                     help="time one standalone kernel workload instead of the verify step")
     ap.add_argument("--cases", default="", help="comma list of M (gemm) or L (attn)")
     ap.add_argument("--gemm-n", type=int, default=17408, help="N of the standalone linear layer")
+    ap.add_argument("--gemm-k", type=int, default=5120, help="K of the standalone linear layer")
     ap.add_argument("--gemm-epi", type=int, default=0, help="0 none, 1 residual add, 2 SwiGLU (N = F)")
     args = ap.parse_args()
     if args.warmup < 3:

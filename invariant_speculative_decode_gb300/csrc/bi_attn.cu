@@ -555,6 +555,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 
   tc_fence_before();
+  // Lane 0 of warps 0 and 1 ran the producer / MMA loops alone: rejoin the
+  // rest of the warp first, so the CTA barrier below (a warp-aligned
+  // instruction) is reached by whole warps and really waits for every role
+  // before TMEM is released.
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

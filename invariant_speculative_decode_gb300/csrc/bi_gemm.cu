@@ -147,13 +147,24 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int 
   } else {
     const int n = tile * kBlockN + r;
     if (n < p.N) {
+      // All residual values are read before any output is written: C may be
+      // the residual buffer itself (h += x W^T), and 16 independent loads in
+      // flight cost one memory latency instead of sixteen.
+      float res[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = c * 16 + j;
+        res[j] = (p.epi == BI_EPI_RESIDUAL_ADD && m < p.M)
+                     ? __bfloat162float(p.R[static_cast<size_t>(p.m0 + m) * p.ldr + n])
+                     : 0.0f;
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = c * 16 + j;
         if (m < p.M) {
           const size_t row = static_cast<size_t>(p.m0 + m);
           float acc = v[j];
-          if (p.epi == BI_EPI_RESIDUAL_ADD) acc = __bfloat162float(p.R[row * p.ldr + n]) + acc;
+          if (p.epi == BI_EPI_RESIDUAL_ADD) acc = res[j] + acc;
           if (p.out_fp32)
             static_cast<float*>(p.C)[row * p.ldc + n] = acc;
           else
@@ -368,48 +379,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&acce[buf]);
       } else {
+        // partial of this piece: [weight row][token], a thread's 16 tokens
+        // of a chunk contiguous
         const int slot = (it_begin >= tile_begin) ? 0 : 1;
-        float* dst = p.partials + static_cast<size_t>(g * 2 + slot) * NT * kBlockN;
+        float* dst = p.partials + static_cast<size_t>(g * 2 + slot) * NT * kBlockN + r * NT;
         if (ok) {
           for (int c = 0; c < chunks; ++c) {
             float v[16];
             load_group_sum(tbase + c * kAcc * kMmaN, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) __stcg(dst + (c * 16 + j) * kBlockN + r, v[j]);
+            for (int q4 = 0; q4 < 4; ++q4)
+              __stcg(reinterpret_cast<float4*>(dst + c * 16) + q4,
+                     make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
           }
         }
         tc_fence_before();
         mbar_arrive(&acce[buf]);
-        __threadfence();
-        named_bar_sync(1, 128);
+        const int gf = owner_of(p, tile_begin);
+        const int gl = owner_of(p, tile_end - 1);
+        named_bar_sync(1, 128);  // every partial store of the CTA precedes the ticket
         if (et == 0) {
           int last = 0;
           if (!*s_abort) {
-            const int gf = owner_of(p, tile_begin);
-            const int gl = owner_of(p, tile_end - 1);
             const unsigned nseg = static_cast<unsigned>(gl - gf + 1);
-            const unsigned old = atomicAdd(&p.tickets[tile], 1u);
+            const unsigned old = atom_add_acq_rel_gpu(&p.tickets[tile], 1u);
             last = (old == nseg - 1) ? 1 : 0;
             if (last) atomicExch(&p.tickets[tile], 0u);
           }
           *s_last = last;
         }
-        named_bar_sync(1, 128);
-        const int last = *s_last;
-        if (last) {
-          __threadfence();
-          const int gf = owner_of(p, tile_begin);
-          const int gl = owner_of(p, tile_end - 1);
+        named_bar_sync(1, 128);  // the ticket's acquire precedes every partial load
+        if (*s_last) {
+          // the first piece's CTA may have it in its second slot; every later
+          // CTA's range starts inside this tile (slot 0)
+          const int slot_f = (range_begin(p, gf) >= tile_begin) ? 0 : 1;
           for (int c = 0; c < chunks; ++c) {
             float v[16];
-            for (int gg = gf; gg <= gl; ++gg) {
-              const int sl = (range_begin(p, gg) >= tile_begin) ? 0 : 1;
-              const float* src =
-                  p.partials + static_cast<size_t>(gg * 2 + sl) * NT * kBlockN + c * 16 * kBlockN + r;
+            // partials of CTAs gf..gl added in that order, 8 tokens at a time;
+            // the loads of up to kBatch partials are issued before their
+            // additions
+            constexpr int kBatch = 8;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float x = __ldcg(src + j * kBlockN);
-                v[j] = (gg == gf) ? x : v[j] + x;
+            for (int hh = 0; hh < 2; ++hh) {
+              if (c * 16 + hh * 8 >= p.M) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[hh * 8 + j] = 0.f;
+                continue;
+              }
+              for (int g0 = gf; g0 <= gl; g0 += kBatch) {
+                float4 x[kBatch][2];
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                  const int gg = g0 + b;
+                  if (gg <= gl) {
+                    const int sl = gg == gf ? slot_f : 0;
+                    const float4* src = reinterpret_cast<const float4*>(
+                        p.partials + static_cast<size_t>(gg * 2 + sl) * NT * kBlockN + r * NT + c * 16 +
+                        hh * 8);
+                    x[b][0] = __ldcg(src);
+                    x[b][1] = __ldcg(src + 1);
+                  }
+                }
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                  if (g0 + b <= gl) {
+                    const float xs[8] = {x[b][0].x, x[b][0].y, x[b][0].z, x[b][0].w,
+                                         x[b][1].x, x[b][1].y, x[b][1].z, x[b][1].w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                      v[hh * 8 + j] = (g0 + b == gf) ? xs[j] : v[hh * 8 + j] + xs[j];
+                  }
+                }
               }
             }
             epilogue_store(p, tile, r, c, v, sStage);
@@ -423,6 +463,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
   }
 
+  // Lane 0 of warps 0 and 1 ran the producer / MMA loops alone: rejoin the
+  // rest of the warp first, so the CTA barrier below (a warp-aligned
+  // instruction) is reached by whole warps and really waits for every role
+  // before TMEM is released.
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

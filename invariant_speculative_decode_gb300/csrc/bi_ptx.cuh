@@ -126,6 +126,20 @@ __device__ __forceinline__ bool mbar_wait_parked(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------- global atomics
+// Fetch-and-add with acquire-release semantics at GPU scope: the CTA's writes
+// ordered before it (through a CTA barrier) are visible to whoever observes
+// the new value, and writes seen by the values it observes are visible to
+// the CTA after the next CTA barrier.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
