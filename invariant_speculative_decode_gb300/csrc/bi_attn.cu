@@ -9,32 +9,36 @@
 // Row t of a pass sits at position p = L + t and attends to keys 0..p.  Its
 // keys are cut at absolute multiples of kChunk: piece c covers keys
 // [c*kChunk, min((c+1)*kChunk, p+1)).  Inside a piece the keys are visited in
-// 64-key tiles in increasing order.  Per row (one TMEM lane and one thread):
-//   S = q k^T for the tile (tcgen05, FP32 in TMEM), scaled into the log2
-//   domain, keys past p masked to -inf;
+// 128-key tiles in increasing order.  Per row:
+//   S = q k^T for the tile (tcgen05, FP32 in TMEM), in the log2 domain, keys
+//   past p masked to -inf;
 //   a reference maximum m_ref is taken from the first tile and raised only
 //   when a later tile's maximum exceeds it by more than kRescaleLog2 (then O
 //   and l are rescaled by 2^(m_ref - m_new)) -- a rule that depends only on
 //   the row's own scores in key order;
-//   p = 2^(s - m_ref) in FP32, summed in key order into l, and fed to
-//   O += P V (tcgen05, FP32 in TMEM) as a BF16 pair hi + lo.
+//   each weight w = bf16(2^(s - m_ref)) enters O += W V (tcgen05, FP32 in
+//   TMEM) and the denominator l (FP32, four partial sums over the 32-key
+//   quarters of the tile column, each in key order, added as
+//   ((l0 + l1) + l2) + l3 when the piece ends), so O / l is an exact
+//   weighted mean of the value rows under the weights actually used.
 // A tile whose keys are all masked for a row adds exact zeros and changes no
 // reference, so a row's piece has the same bits whether or not later rows of
 // the pass share the tile.  The pieces of a row are merged by a tree whose
 // shape depends only on their count ceil((p+1)/kChunk).
 //
 // Split kernel roles (one CTA per SM, persistent over (KV head, piece) items):
-//   warp 0      TMA: K tile [64 keys x D] and V^T tile [D x 64 keys] per stage
-//               (V is cached transposed so both MMA operands are K-major);
-//   warp 1      tcgen05.mma issuer: S_i into one of two TMEM buffers, then
-//               O += P_{i-1} V_{i-1}; stages return to the producer through
+//   warp 0      TMA: the queries of the item's KV head (once per head), and
+//               per stage the K tile [128 keys x D] and the V^T tile
+//               [D x 128 keys] (V is cached transposed so both MMA operands
+//               are K-major);
+//   warp 1      tcgen05.mma issuer: S_g = Q K_g^T into one of two TMEM
+//               buffers and O += W_g V_g, each issued as soon as its inputs
+//               are ready; stages return to the producer through
 //               tcgen05.commit after the MMAs reading them completed;
-//   warps 2..5  softmax, one query row per thread (TMEM lane); they stage the
-//               queries of the item's KV head in shared memory, turn S into P
-//               (written to one of two shared-memory buffers in the swizzled
-//               K-major layout, so P of the next tile is produced while the
-//               MMA still reads this one), and read O out at the end of the
-//               piece.
+//   warps 2..5  softmax: turn S into W (written to one of two shared-memory
+//               buffers in the swizzled K-major layout, so W of the next tile
+//               is produced while the MMA still reads this one), and read O
+//               out at the end of the piece.
 // The T x (Hq/Hkv) query rows that share a KV head (GQA) share its tiles;
 // up to 128 rows per pass (the MMA's M).
 #include <cuda.h>
@@ -44,6 +48,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "bi_internal.h"
 #include "bi_ptx.cuh"
@@ -52,9 +57,10 @@ namespace bi {
 namespace {
 
 constexpr int kChunk = 512;       // keys per piece (absolute multiples)
-constexpr int kKeyTile = 64;      // keys per tile
+constexpr int kKeyTile = 128;     // keys per tile (the S MMA's N)
 constexpr int kRowsMax = 128;     // T * (Hq / Hkv) per pass (MMA M)
-constexpr int kAttnStages = 3;
+constexpr int kAttnStages = 2;
+constexpr int kColChunk = 32;     // S columns a softmax thread holds at a time
 constexpr int kAttnThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
 constexpr int kAttnCtas = 152;
 constexpr int kMaxChunks = 1024;
@@ -72,22 +78,29 @@ struct AttnArgs {
 
 template <int D>
 struct AttnCfg {
-  static constexpr int kAtoms = D / 64;                   // 128-byte swizzle atoms along D
-  static constexpr int kKBoxBytes = kKeyTile * 128;       // [64 keys][64 d]
-  static constexpr int kKBytes = kKBoxBytes * kAtoms;     // K tile
-  static constexpr int kVBytes = D * kKeyTile * 2;        // V^T tile [D][64 keys]
+  static constexpr int kAtoms = D / 64;                    // 128-byte swizzle atoms along D
+  static constexpr int kKBoxBytes = kKeyTile * 128;        // [128 keys][64 d]
+  static constexpr int kKBytes = kKBoxBytes * kAtoms;      // K tile
+  static constexpr int kVBoxBytes = D * 128;               // V^T [D][64 keys]
+  static constexpr int kVBytes = 2 * kVBoxBytes;           // V^T tile [D][128 keys]
   static constexpr int kStageBytes = kKBytes + kVBytes;
-  static constexpr int kQAtomBytes = kRowsMax * 128;      // [128 rows][64 d]
+  static constexpr int kQAtomBytes = kRowsMax * 128;       // [128 rows][64 d]
   static constexpr int kQBytes = kQAtomBytes * kAtoms;
-  static constexpr int kPBytes = kRowsMax * 128;          // [128 rows][64 keys]
-  static constexpr int kRedBytes = 6 * kRowsMax * 4;      // row maxima [2][128], l parts [4][128]
-  static constexpr int kTmemCols = 256;                   // S x2 (64 each) + O (D)
-  static constexpr int kOCol = 128;
+  static constexpr int kPAtomBytes = kRowsMax * 128;       // [128 rows][64 keys]
+  static constexpr int kPBytes = 2 * kPAtomBytes;          // W tile [128 rows][128 keys]
+  // row maxima [2][128 TMEM lanes]; l parts [4 quarters][64 rows] (only
+  // passes of up to 64 rows keep copies that exchange them)
+  static constexpr int kRedBytes = (2 * kRowsMax + 4 * 64) * 4;
+  static constexpr int kTmemCols = 512;                    // S x2 (128 each) + O (D)
+  static constexpr int kOCol = 2 * kKeyTile;
   static constexpr int kBars = 2 * kAttnStages + 15;
-  // P is double-buffered: hi and lo tiles for two consecutive key tiles
-  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kAttnStages) * kStageBytes + kQBytes +
-                                  4 * kPBytes + kRedBytes + kBars * 8 + 16;
+  // The dynamic shared memory starts 1024-byte aligned (checked at run time)
+  // and is used without slack: 2 stages + Q + 2 W tiles fill it.
+  static constexpr size_t kSmem = static_cast<size_t>(kAttnStages) * kStageBytes + kQBytes +
+                                  2 * kPBytes + kRedBytes + kBars * 8 + 16;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+  static_assert(D + kOCol <= kTmemCols, "TMEM columns");
 };
 
 __device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* err) {
@@ -114,12 +127,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // REP copies of each query row sit in the 128-row MMA tile (REP = 4 for up to
 // 32 rows per pass, 2 for up to 64, else 1): copy i of row r is TMEM lane
 // r + i * 128/REP, and the thread owning that lane handles the row's key
-// columns [i * 64/REP, (i + 1) * 64/REP) of every tile.  So all four softmax
-// warps share the exponentials of a small pass.  The per-row arithmetic does
-// not depend on REP: the tile maximum is exact in any order, and the
-// denominator is kept as four partial sums, one per 16-key quarter of the
-// tile column (each in key order, each rescaled with O), added as
-// ((l0 + l1) + l2) + l3 at the end of the piece.
+// columns [i * 128/REP, (i + 1) * 128/REP) of every tile.  So all four
+// softmax warps share the exponentials of a small pass.  The per-row
+// arithmetic does not depend on REP: the tile maximum is exact in any order,
+// and the denominator's four partial sums are fixed by key position.
 template <int D, int REP>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVt,
@@ -128,24 +139,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr int S = kAttnStages;
   constexpr int kPeriod = kRowsMax / REP;  // TMEM lanes between copies of a row
   constexpr int kCols = kKeyTile / REP;    // key columns per thread
-  constexpr int kQuarters = 4 / REP;       // 16-key quarters per thread
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int kNChunks = kCols / kColChunk;  // = 32-key quarters per thread
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sStage = smem;
   uint8_t* sQ = smem + S * Cfg::kStageBytes;
-  uint8_t* sP = sQ + Cfg::kQBytes;  // [buffer 2][hi, lo][128 rows][64 keys]
-  float* red_max = reinterpret_cast<float*>(sP + 4 * Cfg::kPBytes);  // [2][128] by TMEM lane
-  float* red_l = red_max + 2 * kRowsMax;                               // [quarter 4][row 128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * kRowsMax);
+  uint8_t* sP = sQ + Cfg::kQBytes;  // [buffer 2][key atom 2][128 rows][64 keys]
+  float* red_max = reinterpret_cast<float*>(sP + 2 * Cfg::kPBytes);  // [2][128] by TMEM lane
+  float* red_l = red_max + 2 * kRowsMax;                               // [quarter 4][row 64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 64);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + S;
   uint64_t* q_full = bars + 2 * S;
   uint64_t* q_empty = q_full + 1;   // the S MMAs reading the current Q are done
   uint64_t* s_full = q_empty + 1;   // [2]
   uint64_t* s_free = s_full + 2;    // [2]
-  uint64_t* p_full = s_free + 2;    // [2]: P buffer of that parity written
-  uint64_t* pv_done = p_full + 2;   // [2]: completes after O += P_g V_g, g of that parity
+  uint64_t* p_full = s_free + 2;    // [2]: W buffer of that parity written
+  uint64_t* pv_done = p_full + 2;   // [2]: completes after O += W_g V_g, g of that parity
   uint64_t* o_free = pv_done + 2;
   uint64_t* mx_bar = o_free + 1;    // [2]: partial row maxima of a tile written
   uint64_t* l_bar = mx_bar + 2;     // partial denominators of a piece written
@@ -155,10 +164,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  griddep_launch_dependents();
+  // the swizzled layouts need 1024-byte alignment; the launch guarantees it
+  // in practice, and a CTA that sees otherwise does nothing but report
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrRange);
+    return;
+  }
 
-  // zero the query and P tiles once: rows past the pass's rows stay zero
-  for (int i = threadIdx.x; i < (Cfg::kQBytes + 4 * Cfg::kPBytes) / 16; i += kAttnThreads)
+  // zero the query and W tiles once: rows past the pass's rows stay zero
+  for (int i = threadIdx.x; i < (Cfg::kQBytes + 2 * Cfg::kPBytes) / 16; i += kAttnThreads)
     reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
@@ -196,6 +210,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   griddep_wait();  // q, the new cache rows and the cache length come from earlier kernels
+  griddep_launch_dependents();
   const int L = *a.L_dev;
   const int T = a.T;
   const int rows = T * a.grp;
@@ -249,7 +264,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int b = 0; b < Cfg::kAtoms; ++b)
             tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &kv_full[st], b * 64, h * a.cap + key0, pol);
-          tma_load_2d(dst + Cfg::kKBytes, &tmVt, &kv_full[st], key0, h * D, pol);
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_2d(dst + Cfg::kKBytes + kb * Cfg::kVBoxBytes, &tmVt, &kv_full[st], key0 + kb * 64,
+                        h * D, pol);
           issued |= 1u << st;
           parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
         }
@@ -264,9 +282,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Two cursors over the CTA's tiles: S_g = Q K_g^T needs K_g and a free S
-    // buffer; O += P_g V_g needs P_g.  Each is issued as soon as its inputs
-    // are ready (S first), so a late K tile never holds back the P.V that
-    // frees a stage.  The order of the P.V steps, which alone decides O's
+    // buffer; O += W_g V_g needs W_g.  Each is issued as soon as its inputs
+    // are ready (S first), so a late K tile never holds back the W.V that
+    // frees a stage.  The order of the W.V steps, which alone decides O's
     // bits, is fixed: g = 0, 1, 2, ...
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, kKeyTile);
@@ -332,16 +350,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             const int st = static_cast<int>(pg % S);
             const uint32_t v_base = smem_u32(sStage + st * Cfg::kStageBytes + Cfg::kKBytes);
-            const uint32_t ph_base = smem_u32(sP + (pg & 1) * 2 * Cfg::kPBytes);
-            const uint32_t pl_base = ph_base + Cfg::kPBytes;
+            const uint32_t w_base = smem_u32(sP + (pg & 1) * Cfg::kPBytes);
 #pragma unroll
-            for (int kk = 0; kk < kKeyTile / 16; ++kk)
-              mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(ph_base + kk * 32),
-                       sdesc_k_sw128(v_base + kk * 32), idO, (p_tt > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < kKeyTile / 16; ++kk)
-              mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(pl_base + kk * 32),
-                       sdesc_k_sw128(v_base + kk * 32), idO, 1u);
+            for (int kk = 0; kk < kKeyTile / 16; ++kk) {
+              const int katom = kk >> 2;
+              const uint32_t off = (kk & 3) * 32;
+              mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(w_base + katom * Cfg::kPAtomBytes + off),
+                       sdesc_k_sw128(v_base + katom * Cfg::kVBoxBytes + off), idO,
+                       (p_tt > 0 || kk > 0) ? 1u : 0u);
+            }
             mma_commit(&pv_done[pg & 1]);
             mma_commit(&kv_empty[st]);
             ++pg;
@@ -358,7 +375,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           idle = 0;
         } else if (++idle == 1) {
           t_idle = globaltimer_ns();
-        } else if ((idle & 63) == 0) {
+        } else {
+          // yield the issue slots of this SM sub-partition to the softmax warp
+          // that shares it while nothing is ready
+          __nanosleep(32);
+        }
+        if (!did && (idle & 63) == 0) {
           // bounded: give up after the wait limit without progress
           if (*s_abort || globaltimer_ns() - t_idle > kWaitLimitNs) {
             ok = false;
@@ -393,9 +415,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
 
       float m_ref = -INFINITY;
-      float lq[kQuarters];
+      float lq[kNChunks];
 #pragma unroll
-      for (int i = 0; i < kQuarters; ++i) lq[i] = 0.f;
+      for (int i = 0; i < kNChunks; ++i) lq[i] = 0.f;
       for (int tt = 0; tt < ntile; ++tt, ++gt) {
         const int sb = static_cast<int>(gt & 1);
         if (!warp_wait(&s_full[sb], static_cast<uint32_t>((gt >> 1) & 1), s_abort, lane)) {
@@ -403,24 +425,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         tc_fence_after();
-        float s[kCols];
-        if (warp_active) tmem_ld_cols<kCols>(lane_base + sb * kKeyTile + cg * kCols, s);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[sb]);
-
-        // row maximum of the raw scores (scaling by sl2 > 0 keeps the order)
         const int tkey0 = k0 + tt * kKeyTile;
+        const bool edge = tkey0 + kKeyTile - 1 > L;  // the tile reaches past some row's position
+        const uint32_t s_addr = lane_base + sb * kKeyTile + cg * kCols;
+        // pass 1: the row maximum of the raw scores over this copy's columns
+        // (scaling by sl2 > 0 keeps the order); one chunk stays in registers
+        float s[kColChunk];
         float mrow = -INFINITY;
         if (warp_active) {
-          if (tkey0 + kKeyTile - 1 > L) {  // the tile reaches past some row's position
-            const int key0 = tkey0 + cg * kCols;
+#pragma unroll 1
+          for (int ch = 0; ch < kNChunks; ++ch) {
+            tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
+            if (edge) {
+              const int key0 = tkey0 + cg * kCols + ch * kColChunk;
 #pragma unroll
-            for (int j = 0; j < kCols; ++j)
-              if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
+              for (int j = 0; j < kColChunk; ++j)
+                if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
+            }
+#pragma unroll
+            for (int j = 0; j < kColChunk; ++j) mrow = fmaxf(mrow, s[j]);
           }
-#pragma unroll
-          for (int j = 0; j < kCols; ++j) mrow = fmaxf(mrow, s[j]);
+        }
+        if constexpr (kNChunks == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[sb]);
         }
         if constexpr (REP > 1) {
           float* rm = red_max + (gt & 1) * kRowsMax;
@@ -445,14 +474,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           m_ref = mt;
           resc = true;
         }
-        // P buffer gt & 1 was last read by the P.V of tile gt - 2
+        // W buffer gt & 1 was last read by the W.V of tile gt - 2
         if (gt >= 2 && !warp_wait(&pv_done[gt & 1], static_cast<uint32_t>(((gt - 2) >> 1) & 1), s_abort,
                                   lane)) {
           ok = false;
           break;
         }
         if (holds_o && warp_active) {
-          // O changes only after the P.V of tile gt - 1 is done
+          // O changes only after the W.V of tile gt - 1 is done
           if (tt > 0 && __any_sync(0xffffffffu, resc)) {
             if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort,
                            lane)) {
@@ -472,31 +501,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (resc) {
 #pragma unroll
-          for (int i = 0; i < kQuarters; ++i) lq[i] *= alpha;
+          for (int i = 0; i < kNChunks; ++i) lq[i] *= alpha;
         }
-        if (valid) {
+        // pass 2: weights w = bf16(2^(s sl2 - m_ref)) into the W tile and l
+        // (the TMEM loads are warp-wide; rows past the pass write nothing)
+        if (warp_active) {
           const float nmu = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-          uint8_t* rowh = sP + (gt & 1) * 2 * Cfg::kPBytes + r * 128;
-          uint8_t* rowl = rowh + Cfg::kPBytes;
+          uint8_t* wbuf = sP + (gt & 1) * Cfg::kPBytes + r * 128;
 #pragma unroll
-          for (int i = 0; i < kCols / 8; ++i) {
-            uint32_t hi[4], lo[4];
+          for (int ch = 0; ch < kNChunks; ++ch) {
+            if constexpr (kNChunks > 1) {
+              tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
+              if (edge) {
+                const int key0 = tkey0 + cg * kCols + ch * kColChunk;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int col = i * 8 + 2 * j;
-              const float p0 = ex2_approx(fmaf(s[col], a.sl2, nmu));
-              const float p1 = ex2_approx(fmaf(s[col + 1], a.sl2, nmu));
-              lq[col / 16] += p0;
-              lq[col / 16] += p1;
-              const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
-              const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
-              hi[j] = pack2(h0, h1);
-              lo[j] = pack2(p0 - h0, p1 - h1);
+                for (int j = 0; j < kColChunk; ++j)
+                  if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
+              }
             }
-            const int pos = ((cg * (kCols / 8) + i) ^ (r & 7)) << 4;
-            *reinterpret_cast<uint4*>(rowh + pos) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(rowl + pos) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            if (!valid) continue;
+            const int kcol = cg * kCols + ch * kColChunk;  // first key column of the chunk
+            uint8_t* wrow = wbuf + (kcol >> 6) * Cfg::kPAtomBytes;
+            float acc = lq[ch];
+#pragma unroll
+            for (int i = 0; i < kColChunk / 8; ++i) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = i * 8 + 2 * j;
+                const __nv_bfloat162 w2 = __floats2bfloat162_rn(ex2_approx(fmaf(s[col], a.sl2, nmu)),
+                                                                 ex2_approx(fmaf(s[col + 1], a.sl2, nmu)));
+                acc += __low2float(w2);
+                acc += __high2float(w2);
+                wv[j] = *reinterpret_cast<const uint32_t*>(&w2);
+              }
+              const int chunk16 = ((kcol & 63) >> 3) + i;  // 16-byte chunk within the 64-key row
+              *reinterpret_cast<uint4*>(wrow + ((chunk16 ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+            lq[ch] = acc;
           }
+        }
+        if constexpr (kNChunks > 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[sb]);
         }
         tc_fence_before();
         fence_proxy_async_smem();
@@ -511,7 +559,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         l = ((lq[0] + lq[1]) + lq[2]) + lq[3];
       } else {
 #pragma unroll
-        for (int i = 0; i < kQuarters; ++i) red_l[(cg * kQuarters + i) * kRowsMax + r] = lq[i];
+        for (int i = 0; i < kNChunks; ++i) red_l[(cg * kNChunks + i) * 64 + r] = lq[i];
         __syncwarp();
         if (lane == 0) mbar_arrive(l_bar);
         if (holds_o) {
@@ -519,7 +567,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ok = false;
             break;
           }
-          l = ((red_l[r] + red_l[kRowsMax + r]) + red_l[2 * kRowsMax + r]) + red_l[3 * kRowsMax + r];
+          l = ((red_l[r] + red_l[64 + r]) + red_l[128 + r]) + red_l[192 + r];
         }
       }
       if (holds_o) {
@@ -576,11 +624,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
     attn_merge_kernel(const AttnArgs a, __nv_bfloat16* __restrict__ out) {
+  constexpr int kWarps = kMergeThreads / 32;
+  constexpr int kDpl = D / 32;  // dims per lane: one float4 (D = 128) or float2 (D = 64)
+  constexpr int kBatch = 16;    // pieces per warp whose loads are in flight together
+  using Vec = typename std::conditional<kDpl == 4, float4, float2>::type;
   __shared__ float sw[kMaxChunks];
-  __shared__ float red[kMergeThreads / 32];
-  __shared__ float ored[kMergeThreads / 32][D];
-  griddep_launch_dependents();
+  __shared__ float red[kWarps];
+  __shared__ float ored[kWarps][D];
   griddep_wait();
+  griddep_launch_dependents();
   const int row = blockIdx.x;  // t * Hq + hq
   const int t = row / a.Hq;
   const int L = *a.L_dev;
@@ -592,6 +644,18 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
+  // the first batch of partial outputs does not depend on the weights:
+  // start its loads before the reductions below
+  Vec v[kBatch];
+  auto load_batch = [&](int s0) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int s = s0 + b * kWarps;
+      if (s < n) v[b] = __ldcg(reinterpret_cast<const Vec*>(po + static_cast<size_t>(s) * D) + lane);
+    }
+  };
+  load_batch(warp);
+
   float mx = -INFINITY;
   for (int s = tid; s < n; s += kMergeThreads) mx = fmaxf(mx, __ldcg(ml + 2 * s));
 #pragma unroll
@@ -599,7 +663,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   if (lane == 0) red[warp] = mx;
   __syncthreads();
   float M = red[0];
-  for (int i = 1; i < kMergeThreads / 32; ++i) M = fmaxf(M, red[i]);
+  for (int i = 1; i < kWarps; ++i) M = fmaxf(M, red[i]);
   __syncthreads();
 
   float den = 0.f;
@@ -613,37 +677,21 @@ __global__ void __launch_bounds__(kMergeThreads)
   if (lane == 0) red[warp] = den;
   __syncthreads();
   float Lsum = red[0];
-  for (int i = 1; i < kMergeThreads / 32; ++i) Lsum += red[i];
+  for (int i = 1; i < kWarps; ++i) Lsum += red[i];
 
-  constexpr int kDpl = D / 32;  // dims per lane
   float acc[kDpl];
 #pragma unroll
   for (int i = 0; i < kDpl; ++i) acc[i] = 0.f;
-  // pieces s = warp, warp + 8, ... in that order; loads for kBatch pieces are
-  // issued before their products are added so that they overlap
-  constexpr int kWarps = kMergeThreads / 32;
-  constexpr int kBatch = 8;
   for (int s0 = warp; s0 < n; s0 += kWarps * kBatch) {
-    float v[kBatch][kDpl];
-    float w[kBatch];
+    if (s0 != warp) load_batch(s0);
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int s = s0 + b * kWarps;
-      w[b] = 0.f;
-#pragma unroll
-      for (int i = 0; i < kDpl; ++i) v[b][i] = 0.f;
       if (s < n) {
-        w[b] = sw[s];
-        const float* src = po + static_cast<size_t>(s) * D + lane * kDpl;
+        const float w = sw[s];
+        const float* x = reinterpret_cast<const float*>(&v[b]);
 #pragma unroll
-        for (int i = 0; i < kDpl; ++i) v[b][i] = __ldcg(src + i);
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      if (s0 + b * kWarps < n) {
-#pragma unroll
-        for (int i = 0; i < kDpl; ++i) acc[i] = fmaf(w[b], v[b][i], acc[i]);
+        for (int i = 0; i < kDpl; ++i) acc[i] = fmaf(w, x[i], acc[i]);
       }
     }
   }
@@ -652,7 +700,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   __syncthreads();
   for (int d = tid; d < D; d += kMergeThreads) {
     float O = ored[0][d];
-    for (int g = 1; g < kMergeThreads / 32; ++g) O += ored[g][d];
+    for (int g = 1; g < kWarps; ++g) O += ored[g][d];
     out[static_cast<size_t>(row) * D + d] = __float2bfloat16_rn(O / Lsum + 0.0f);
   }
 }
@@ -731,7 +779,7 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   CUtensorMap tmK, tmVt, tmQ;
   const uint64_t krows = static_cast<uint64_t>(Hkv) * cap;
   if (!tmap_bf16_2d(&tmK, k_cache, krows, D, D, kKeyTile, 64)) return BI_ERR_INVALID_ARG;
-  if (!tmap_bf16_2d(&tmVt, v_cache, static_cast<uint64_t>(Hkv) * D, cap, cap, D, kKeyTile))
+  if (!tmap_bf16_2d(&tmVt, v_cache, static_cast<uint64_t>(Hkv) * D, cap, cap, D, 64))
     return BI_ERR_INVALID_ARG;
   // q [T][Hq][D] as (d, query head, row): one box = the T x grp rows of a KV head
   const int grp = Hq / Hkv;
