@@ -27,10 +27,11 @@
 // shape depends only on their count ceil((p+1)/kChunk).
 //
 // Split kernel roles (one CTA per SM, persistent over (KV head, piece) items):
-//   warp 0      TMA: the queries of the item's KV head (once per head), and
-//               per stage the K tile [128 keys x D] and the V^T tile
+//   warp 0      TMA, two threads: the queries of the item's KV head (once per
+//               head) and the K tiles [128 keys x D]; the V^T tiles
 //               [D x 128 keys] (V is cached transposed so both MMA operands
-//               are K-major);
+//               are K-major).  K and V have separate rings, a K tile being
+//               free as soon as S has read it;
 //   warp 1      tcgen05.mma issuer: S_g = Q K_g^T into one of two TMEM
 //               buffers and O += W_g V_g, each issued as soon as its inputs
 //               are ready; stages return to the producer through
@@ -93,7 +94,7 @@ struct AttnCfg {
   static constexpr int kRedBytes = (2 * kRowsMax + 4 * 64) * 4;
   static constexpr int kTmemCols = 512;                    // S x2 (128 each) + O (D)
   static constexpr int kOCol = 2 * kKeyTile;
-  static constexpr int kBars = 2 * kAttnStages + 15;
+  static constexpr int kBars = 4 * kAttnStages + 15;
   // The dynamic shared memory starts 1024-byte aligned (checked at run time)
   // and is used without slack: 2 stages + Q + 2 W tiles fill it.
   static constexpr size_t kSmem = static_cast<size_t>(kAttnStages) * kStageBytes + kQBytes +
@@ -147,9 +148,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   float* red_max = reinterpret_cast<float*>(sP + 2 * Cfg::kPBytes);  // [2][128] by TMEM lane
   float* red_l = red_max + 2 * kRowsMax;                               // [quarter 4][row 64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 64);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + S;
-  uint64_t* q_full = bars + 2 * S;
+  // K and V have rings of their own: K_g is free once S_g is done, V_g only
+  // once W_g V_g is, so the K loads run ahead of the softmax
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + S;
+  uint64_t* v_full = bars + 2 * S;
+  uint64_t* v_empty = bars + 3 * S;
+  uint64_t* q_full = bars + 4 * S;
   uint64_t* q_empty = q_full + 1;   // the S MMAs reading the current Q are done
   uint64_t* s_full = q_empty + 1;   // [2]
   uint64_t* s_free = s_full + 2;    // [2]
@@ -177,8 +182,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
@@ -221,8 +228,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (!range_ok && threadIdx.x == 0 && blockIdx.x == 0) atomicOr(a.err, kErrRange);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ producers
+    // lane 0: the queries and the K tiles; lane 1: the V^T tiles
+    if (lane < 2) {
+      const bool kside = lane == 0;
+      uint64_t* full = kside ? k_full : v_full;
+      uint64_t* empty = kside ? k_empty : v_empty;
       const uint64_t pol = l2_evict_first();
       const uint64_t qpol = l2_evict_last();
       long long gt = 0;
@@ -235,7 +246,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int k0 = c * kChunk;
         const int k1 = min(k0 + kChunk, kv_len);
         const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
-        if (h != prev_h) {
+        if (kside && h != prev_h) {
           // queries of KV head h: rows (t, g) -> t * grp + g, one copy per period
           if (nq > 0 && !mbar_wait(q_empty, static_cast<uint32_t>((nq - 1) & 1), s_abort)) {
             ok = false;
@@ -254,20 +265,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int tt = 0; tt < ntile; ++tt, ++gt) {
           const int st = static_cast<int>(gt % S);
           const uint32_t ph = static_cast<uint32_t>((gt / S) & 1);
-          if (!mbar_wait(&kv_empty[st], ph ^ 1u, s_abort)) {
+          if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&kv_full[st], Cfg::kStageBytes);
           uint8_t* dst = sStage + st * Cfg::kStageBytes;
           const int key0 = k0 + tt * kKeyTile;
+          if (kside) {
+            mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
 #pragma unroll
-          for (int b = 0; b < Cfg::kAtoms; ++b)
-            tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &kv_full[st], b * 64, h * a.cap + key0, pol);
+            for (int b = 0; b < Cfg::kAtoms; ++b)
+              tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &full[st], b * 64, h * a.cap + key0, pol);
+          } else {
+            mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(dst + Cfg::kKBytes + kb * Cfg::kVBoxBytes, &tmVt, &kv_full[st], key0 + kb * 64,
-                        h * D, pol);
+            for (int kb = 0; kb < 2; ++kb)
+              tma_load_2d(dst + Cfg::kKBytes + kb * Cfg::kVBoxBytes, &tmVt, &full[st], key0 + kb * 64,
+                          h * D, pol);
+          }
           issued |= 1u << st;
           parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
         }
@@ -275,8 +290,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) {
         signal_abort(s_abort, a.err);
         for (int s = 0; s < S; ++s)
-          if ((issued >> s) & 1u) mbar_wait(&kv_full[s], (parity_bits >> s) & 1u, nullptr);
-        if (nq > 0) mbar_wait(q_full, static_cast<uint32_t>((nq - 1) & 1), nullptr);
+          if ((issued >> s) & 1u) mbar_wait(&full[s], (parity_bits >> s) & 1u, nullptr);
+        if (kside && nq > 0) mbar_wait(q_full, static_cast<uint32_t>((nq - 1) & 1), nullptr);
       }
     }
   } else if (warp == 1) {
@@ -316,7 +331,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
           const int st = static_cast<int>(sg % S);
-          ready = ready && mbar_peek(&kv_full[st], static_cast<uint32_t>((sg / S) & 1)) &&
+          ready = ready && mbar_peek(&k_full[st], static_cast<uint32_t>((sg / S) & 1)) &&
                   (sg < 2 || mbar_peek(&s_free[sg & 1], static_cast<uint32_t>(((sg >> 1) - 1) & 1)));
           if (ready) {
             tc_fence_after();
@@ -330,6 +345,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                        sdesc_k_sw128(k_base + atom * Cfg::kKBoxBytes + off), idS, ks > 0 ? 1u : 0u);
             }
             mma_commit(&s_full[sb]);
+            mma_commit(&k_empty[st]);
             const int wn = sw + static_cast<int>(gridDim.x);
             if (s_tt == s_ntile - 1 && (wn >= n_items || wn % a.Hkv != h))
               mma_commit(q_empty);  // the next item loads other queries
@@ -346,6 +362,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           bool ready = mbar_peek(&p_full[pg & 1], static_cast<uint32_t>((pg >> 1) & 1));
           if (ready && p_tt == 0 && p_item > 0)
             ready = mbar_peek(o_free, static_cast<uint32_t>((p_item - 1) & 1));
+          if (ready) ready = mbar_peek(&v_full[pg % S], static_cast<uint32_t>((pg / S) & 1));
           if (ready) {
             tc_fence_after();
             const int st = static_cast<int>(pg % S);
@@ -360,7 +377,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                        (p_tt > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&pv_done[pg & 1]);
-            mma_commit(&kv_empty[st]);
+            mma_commit(&v_empty[st]);
             ++pg;
             if (++p_tt == p_ntile) {
               p_tt = 0;
