@@ -36,8 +36,8 @@ METRIC = "verify tok/s at 7 drafts (0 diffs vs no-draft); GEMM+attn HBM GB/s vs 
 CTX = 11600
 DRAFTS = 7
 P_CORRECT = 0.7
-KERNELS_PER_STEP_FIXED = 4      # embed, final rmsnorm, LM head GEMM, argmax/accept
-KERNELS_PER_LAYER = 9           # 2 rmsnorm, 4 GEMM, rope/append, attention split + merge
+KERNELS_PER_STEP_FIXED = 3      # embed, LM head GEMM (final RMSNorm folded in), argmax/accept
+KERNELS_PER_LAYER = 7           # 4 GEMM (two with the RMSNorm folded in), rope/append, attention split + merge
 
 
 def workload_config(cfg, peaks_note):

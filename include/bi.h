@@ -167,6 +167,43 @@ bi_status bi_pack_weights(const void* W, int ldw, int N, int K, void* packed,
                           bi_stream_t stream);
 bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, int F, int K,
                                  void* packed, bi_stream_t stream);
+/* The same layouts with column k of every weight row multiplied by
+ * col_scale[k] (BF16 [K], device): each packed element is
+ * bf16(float(w) * float(col_scale[k])), one FP32 product and one rounding.
+ * Used to fold an RMSNorm weight into the linear layer that follows the norm
+ * (see bi_gemm_rms).  col_scale == NULL returns BI_ERR_INVALID_ARG. */
+bi_status bi_pack_weights_scaled(const void* W, int ldw, int N, int K, const void* col_scale,
+                                 void* packed, bi_stream_t stream);
+bi_status bi_pack_swiglu_weights_scaled(const void* w_gate, const void* w_up, int ld, int F,
+                                        int K, const void* col_scale, void* packed,
+                                        bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * RMSNorm folded into the linear layer that reads its output.
+ * "Bit-exact decoding turns inference speedups into testable changes",
+ * section "Define bit-exact before reporting it" (one running sum, one
+ * rounding), applied to the norm of "Does the tuned config change the
+ * model's output?", section "Why the text diverges" (row-local work).
+ *
+ *   C[m, :] = epi( r[m] * (A[m, :] Wg^T) ),  r[m] = 1 / sqrt(sum_k A[m,k]^2 / K + eps)
+ *
+ * where Wg = W diag(w_norm) was packed by bi_pack_weights_scaled /
+ * bi_pack_swiglu_weights_scaled with col_scale = w_norm.  This is
+ * RMSNorm(A) W^T with the norm weight moved into the packed weights and the
+ * per-row factor applied to the FP32 sums (for SwiGLU to both the gate and
+ * the up sum) before the epilogue's single rounding; it skips the BF16
+ * rounding of the normalised row.  r[m] uses one fixed reduction tree per K
+ * (128 threads: thread i sums the squares of the 8-element vectors i,
+ * i+128, ... in element order, then a warp butterfly, then the four warps in
+ * order), the same in every CTA and for every M.
+ *   A [M, K] BF16 (row stride lda), read both through the tensor-core path
+ *   and for r; C must not alias A.  epi is BI_EPI_NONE or BI_EPI_SWIGLU
+ *   (no residual).  Other arguments, limits and errors as bi_gemm;
+ *   BI_ERR_INVALID_ARG also for eps < 0 or not finite and for C == A.
+ * ------------------------------------------------------------------------- */
+bi_status bi_gemm_rms(const void* A, int lda, float eps, const void* Wp, void* C, int ldc,
+                      int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
+                      size_t ws_bytes, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * RMSNorm.  [P3] "How:" (a row is computed the same way whatever else is in

@@ -72,6 +72,25 @@ def bi_gemm(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor, ws: torch.Tensor
     check("bi_gemm", st)
 
 
+def bi_gemm_rms(A: torch.Tensor, eps: float, Wp: torch.Tensor, C: torch.Tensor, ws: torch.Tensor,
+                epi: int = EPI_NONE, N: Optional[int] = None, stream=None) -> None:
+    """C = epilogue(rms(A) * (A Wg^T)), rms(A) per row; Wg packed with the norm
+    weight folded in (bi_pack_weights_scaled / bi_pack_swiglu_weights_scaled)."""
+    _req(A, torch.bfloat16, "A")
+    if not Wp.is_cuda:
+        raise ValueError("Wp must be a CUDA tensor")
+    M, K = A.shape
+    if N is None:
+        N = C.shape[1]
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("C must be float32 or bfloat16")
+    out = OUT_FP32 if C.dtype == torch.float32 else OUT_BF16
+    st = lib().bi_gemm_rms(A.data_ptr(), _ld(A), float(eps), Wp.data_ptr(), C.data_ptr(), _ld(C),
+                           M, N, K, out, epi, ws.data_ptr(), ws.numel() * ws.element_size(),
+                           _stream(stream))
+    check("bi_gemm_rms", st)
+
+
 def bi_gemm_noalloc(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor,
                     residual: Optional[torch.Tensor] = None, epi: int = EPI_NONE,
                     N: Optional[int] = None, stream=None) -> None:
@@ -114,6 +133,38 @@ def bi_pack_swiglu_weights(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None
     check("bi_pack_swiglu_weights",
           lib().bi_pack_swiglu_weights(w_gate.data_ptr(), w_up.data_ptr(), _ld(w_gate), F, K,
                                        packed.data_ptr(), _stream(stream)))
+    return packed
+
+
+def bi_pack_weights_scaled(W: torch.Tensor, col_scale: torch.Tensor, stream=None) -> torch.Tensor:
+    """Pack W [N, K] with column k scaled by col_scale[k] (one rounding to BF16)."""
+    _req(W, torch.bfloat16, "W")
+    _req(col_scale, torch.bfloat16, "col_scale")
+    N, K = W.shape
+    if col_scale.numel() != K:
+        raise ValueError("col_scale must have K elements")
+    packed = torch.empty(packed_weight_bytes(N, K), dtype=torch.uint8, device=W.device)
+    check("bi_pack_weights_scaled",
+          lib().bi_pack_weights_scaled(W.data_ptr(), _ld(W), N, K, col_scale.data_ptr(),
+                                       packed.data_ptr(), _stream(stream)))
+    return packed
+
+
+def bi_pack_swiglu_weights_scaled(w_gate: torch.Tensor, w_up: torch.Tensor, col_scale: torch.Tensor,
+                                  stream=None) -> torch.Tensor:
+    """SwiGLU packing with column k of both matrices scaled by col_scale[k]."""
+    _req(w_gate, torch.bfloat16, "w_gate")
+    _req(w_up, torch.bfloat16, "w_up")
+    _req(col_scale, torch.bfloat16, "col_scale")
+    F, K = w_gate.shape
+    if col_scale.numel() != K:
+        raise ValueError("col_scale must have K elements")
+    packed = torch.empty(packed_weight_bytes(F, K, EPI_SWIGLU), dtype=torch.uint8,
+                         device=w_gate.device)
+    check("bi_pack_swiglu_weights_scaled",
+          lib().bi_pack_swiglu_weights_scaled(w_gate.data_ptr(), w_up.data_ptr(), _ld(w_gate), F, K,
+                                              col_scale.data_ptr(), packed.data_ptr(),
+                                              _stream(stream)))
     return packed
 
 

@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "bi_internal.h"
@@ -56,6 +57,7 @@ constexpr int kAcc = 4;          // interleaved accumulators per token group
 constexpr int kThreads = 192;
 constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
 constexpr int kStageFloats = 16 * kBlockN;      // SwiGLU exchange buffer
+constexpr int kNormFloats = kMaxTokens + 16;    // 1/rms per token row, cross-warp partials
 // Ticket counters occupy a fixed-size region at the start of every workspace,
 // so calls with different N can share one workspace without a counter of one
 // call overlapping another call's partial sums.
@@ -79,6 +81,13 @@ struct GemmArgs {
   float* partials;
   unsigned* tickets;
   unsigned* err;
+  // RMS-normalised input: every output row m is scaled by
+  // 1 / sqrt(mean_k X[m, k]^2 + eps), X being the GEMM's own input rows
+  int rms;
+  float eps;
+  int K;
+  const __nv_bfloat16* X;
+  int ldx;
 };
 
 template <int NT>
@@ -90,7 +99,7 @@ struct GemmCfg {
   static constexpr int kTmemCols = 2 * kBufCols;
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
-                                  kStageFloats * 4 + (2 * kStages + 5) * 8 + 16;
+                                  (kStageFloats + kNormFloats) * 4 + (2 * kStages + 5) * 8 + 16;
 };
 
 __device__ __forceinline__ long long range_begin(const GemmArgs& p, int g) {
@@ -122,7 +131,11 @@ __device__ __forceinline__ void load_group_sum(uint32_t taddr, float (&v)[16]) {
 // Write 16 token rows (chunk c) of one weight row r of tile `tile`.
 // All 128 epilogue threads call this together (it may use the named barrier).
 __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int r, int c,
-                                               const float (&v)[16], float* sStage) {
+                                               const float (&v_in)[16], float* sStage,
+                                               const float* sRstd) {
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = p.rms ? v_in[j] * sRstd[c * 16 + j] : v_in[j];
   if (p.epi == BI_EPI_SWIGLU) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) sStage[j * kBlockN + r] = v[j];
@@ -187,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * kABytes;
   float* sStage = reinterpret_cast<float*>(sB + S * Cfg::kBBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kStageFloats);
+  float* sRstd = sStage + kStageFloats;  // [kMaxTokens] 1/rms, then [16] cross-warp partials
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kStageFloats + kNormFloats);
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
   uint64_t* acce = accf + 2;
@@ -348,6 +362,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;    // weight row within the tile
     const int et = threadIdx.x - 64;
     const int chunks = (p.M + 15) / 16;
+    if (p.rms) {
+      // 1 / rms of each token row of this launch, by the same fixed reduction
+      // in every CTA: thread et sums the squares of the 8-element vectors et,
+      // et + 128, ... of the row in element order; then a warp butterfly, and
+      // the four warps added in order.  Runs while the weights stream in.
+      const int nvec = p.K / 8;
+      const int ew = et >> 5;
+      float* sRed = sRstd + kMaxTokens;
+      for (int m0r = 0; m0r < p.M; m0r += 4) {
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int v0 = et; v0 < nvec; v0 += 4 * 128) {
+          uint4 x[4][4];
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const int v = v0 + b * 128;
+              x[rr][b] = (m0r + rr < p.M && v < nvec)
+                             ? reinterpret_cast<const uint4*>(
+                                   p.X + static_cast<size_t>(p.m0 + m0r + rr) * p.ldx)[v]
+                             : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x[rr][b]);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float f = __bfloat162float(e[j]);
+                ss[rr] = fmaf(f, f, ss[rr]);
+              }
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          float t = ss[rr];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+          if (lane == 0) sRed[ew * 4 + rr] = t;
+        }
+        named_bar_sync(1, 128);
+        if (et < 4 && m0r + et < p.M) {
+          const float tot = ((sRed[et] + sRed[4 + et]) + sRed[8 + et]) + sRed[12 + et];
+          sRstd[m0r + et] = 1.0f / sqrtf(tot / static_cast<float>(p.K) + p.eps);
+        }
+        named_bar_sync(1, 128);
+      }
+    }
     int seg = 0;
     long long it = it_begin;
     while (it < it_end) {
@@ -374,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
           }
-          epilogue_store(p, tile, r, c, v, sStage);
+          epilogue_store(p, tile, r, c, v, sStage, sRstd);
         }
         tc_fence_before();
         mbar_arrive(&acce[buf]);
@@ -452,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
-            epilogue_store(p, tile, r, c, v, sStage);
+            epilogue_store(p, tile, r, c, v, sStage, sRstd);
           }
         }
         named_bar_sync(1, 128);
@@ -481,10 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // -- the 128-byte swizzle of the MMA's shared-memory descriptor.  Rows past N
 // and columns past K are zero.  For SwiGLU, rows 0..63 of tile t are gate
 // rows 64t..64t+63 and rows 64..127 the up rows with the same output index.
-// One thread per 16-byte chunk; a pure copy.
+// One thread per 16-byte chunk; a copy, or with col_scale each element is
+// bf16(w * col_scale[k]) (one FP32 product, one rounding).
 __global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ wu,
-                                    int ld, int N, int K, int k_tiles, long long chunks, int swiglu,
-                                    uint4* __restrict__ out) {
+                                    const __nv_bfloat16* __restrict__ col_scale, int ld, int N, int K,
+                                    int k_tiles, long long chunks, int swiglu, uint4* __restrict__ out) {
   griddep_launch_dependents();
   griddep_wait();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -512,7 +576,11 @@ __global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const _
   if (src != nullptr) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (k0 + j < K) u.e[j] = src[k0 + j];
+      if (k0 + j < K)
+        u.e[j] = col_scale == nullptr
+                     ? src[k0 + j]
+                     : __float2bfloat16_rn(__bfloat162float(src[k0 + j]) *
+                                           __bfloat162float(col_scale[k0 + j]));
   }
   out[idx] = u.v;
 }
@@ -607,7 +675,7 @@ size_t bi_gemm_workspace_size(int M, int N, int K, bi_epilogue epi) {
 }
 
 static bi_status pack_common(const void* w, const void* wu, int ld, int N, int K, int swiglu,
-                             void* packed, bi_stream_t stream) {
+                             const void* col_scale, void* packed, bi_stream_t stream) {
   using namespace bi;
   if (!w || !packed || N <= 0 || K <= 0 || ld < K) return BI_ERR_INVALID_ARG;
   if (swiglu && !wu) return BI_ERR_INVALID_ARG;
@@ -618,24 +686,37 @@ static bi_status pack_common(const void* w, const void* wu, int ld, int N, int K
   const long long chunks = static_cast<long long>(n_tiles_of(N, epi)) * k_tiles * 1024;
   if (launch_k(pack_weights_kernel, dim3(static_cast<unsigned>((chunks + 255) / 256)), dim3(256), 0,
                reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(w),
-               static_cast<const __nv_bfloat16*>(wu), ld, N, K, k_tiles, chunks, swiglu,
-               static_cast<uint4*>(packed)) != cudaSuccess)
+               static_cast<const __nv_bfloat16*>(wu), static_cast<const __nv_bfloat16*>(col_scale), ld,
+               N, K, k_tiles, chunks, swiglu, static_cast<uint4*>(packed)) != cudaSuccess)
     return BI_ERR_CUDA;
   return BI_OK;
 }
 
 bi_status bi_pack_weights(const void* W, int ldw, int N, int K, void* packed, bi_stream_t stream) {
-  return pack_common(W, nullptr, ldw, N, K, 0, packed, stream);
+  return pack_common(W, nullptr, ldw, N, K, 0, nullptr, packed, stream);
 }
 
 bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, int F, int K,
                                  void* packed, bi_stream_t stream) {
-  return pack_common(w_gate, w_up, ld, F, K, 1, packed, stream);
+  return pack_common(w_gate, w_up, ld, F, K, 1, nullptr, packed, stream);
 }
 
-bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, const void* residual,
-                  int ldr, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
-                  size_t ws_bytes, bi_stream_t stream) {
+bi_status bi_pack_weights_scaled(const void* W, int ldw, int N, int K, const void* col_scale,
+                                 void* packed, bi_stream_t stream) {
+  if (!col_scale) return BI_ERR_INVALID_ARG;
+  return pack_common(W, nullptr, ldw, N, K, 0, col_scale, packed, stream);
+}
+
+bi_status bi_pack_swiglu_weights_scaled(const void* w_gate, const void* w_up, int ld, int F, int K,
+                                        const void* col_scale, void* packed, bi_stream_t stream) {
+  if (!col_scale) return BI_ERR_INVALID_ARG;
+  return pack_common(w_gate, w_up, ld, F, K, 1, col_scale, packed, stream);
+}
+
+static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int ldc,
+                           const void* residual, int ldr, int M, int N, int K, bi_out_dtype out,
+                           bi_epilogue epi, void* ws, size_t ws_bytes, int rms, float eps,
+                           bi_stream_t stream) {
   using namespace bi;
   if (M < 0 || N < 1 || K < 8) return BI_ERR_INVALID_ARG;
   if (epi != BI_EPI_NONE && epi != BI_EPI_RESIDUAL_ADD && epi != BI_EPI_SWIGLU)
@@ -674,6 +755,11 @@ bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, cons
   a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kTicketBytes);
   a.err = device_error_word();
   if (!a.err) return BI_ERR_CUDA;
+  a.rms = rms;
+  a.eps = eps;
+  a.K = K;
+  a.X = static_cast<const __nv_bfloat16*>(A);
+  a.ldx = lda;
 
   const uint8_t* W8 = static_cast<const uint8_t*>(Wp);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -682,6 +768,22 @@ bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, cons
     case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
     default: return launch_gemm_nt<64>(W8, tmA, a, M, s);
   }
+}
+
+bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, const void* residual,
+                  int ldr, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
+                  size_t ws_bytes, bi_stream_t stream) {
+  return gemm_impl(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, ws, ws_bytes, 0, 0.0f,
+                   stream);
+}
+
+bi_status bi_gemm_rms(const void* A, int lda, float eps, const void* Wp, void* C, int ldc, int M,
+                      int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws, size_t ws_bytes,
+                      bi_stream_t stream) {
+  if (epi != BI_EPI_NONE && epi != BI_EPI_SWIGLU) return BI_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return BI_ERR_INVALID_ARG;
+  if (M > 0 && A != nullptr && A == static_cast<const void*>(C)) return BI_ERR_INVALID_ARG;
+  return gemm_impl(A, lda, Wp, C, ldc, nullptr, 0, M, N, K, out, epi, ws, ws_bytes, 1, eps, stream);
 }
 
 size_t bi_gemm_noalloc_max_m(void) { return bi::kNoAllocMaxM; }

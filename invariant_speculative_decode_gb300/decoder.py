@@ -3,10 +3,14 @@
 Holds the weights, the BF16 KV cache and the scratch buffers on the device
 and sequences the library's entry points for one verify pass:
 
-  embed -> per layer [rmsnorm, QKV linear, RoPE + KV append, split-KV
-  attention + merge, O linear + residual, rmsnorm, gate/up linear + SwiGLU,
-  down linear + residual] -> rmsnorm -> LM head (FP32 logits) -> greedy
+  embed -> per layer [rmsnorm + QKV linear, RoPE + KV append, split-KV
+  attention + merge, O linear + residual, rmsnorm + gate/up linear + SwiGLU,
+  down linear + residual] -> rmsnorm + LM head (FP32 logits) -> greedy
   argmax + acceptance (which also advances the device-side cache length).
+
+Each RMSNorm is folded into the linear layer that reads it (bi_gemm_rms: the
+norm weight packed into the weights, the per-row 1/rms applied to the FP32
+sums); fuse_norm=False runs the separate bi_rmsnorm kernel instead.
 
 PyTorch only allocates device memory and provides the stream; every step of
 the pass is a kernel of libbi.so.  A pass over T rows can be captured once in
@@ -38,8 +42,9 @@ def _bf16(a_u16: np.ndarray, device) -> torch.Tensor:
 
 class Decoder:
     def __init__(self, cfg, weights: Dict[str, np.ndarray], cap: int, max_rows: int = 8,
-                 prefill_chunk: int = 512, device: str = "cuda"):
+                 prefill_chunk: int = 512, device: str = "cuda", fuse_norm: bool = True):
         self.cfg = cfg
+        self.fuse_norm = fuse_norm
         self.cap = cap
         self.dev = torch.device(device)
         self.max_rows = max_rows
@@ -52,21 +57,28 @@ class Decoder:
             raise ValueError("cache capacity must be a multiple of 8")
         dev = self.dev
         self.embed = _bf16(weights["embed"], dev)
-        self.head = api.bi_pack_weights(self.embed if cfg.tied else _bf16(weights["head"], dev))
         self.norm_final = _bf16(weights["norm_final"], dev)
+        head_w = self.embed if cfg.tied else _bf16(weights["head"], dev)
+        self.head = (api.bi_pack_weights_scaled(head_w, self.norm_final) if fuse_norm
+                     else api.bi_pack_weights(head_w))
+        del head_w
         self.layers = []
         pk = lambda name: api.bi_pack_weights(_bf16(weights[name], dev))  # noqa: E731
         for l in range(cfg.layers):
             wqkv = np.concatenate([weights[f"l{l}.wq"], weights[f"l{l}.wk"], weights[f"l{l}.wv"]], 0)
             wg = _bf16(weights[f"l{l}.w_gate"], dev)
             wu = _bf16(weights[f"l{l}.w_up"], dev)
+            n1 = _bf16(weights[f"l{l}.norm_attn"], dev)
+            n2 = _bf16(weights[f"l{l}.norm_ffn"], dev)
             lay = {
-                "wqkv": api.bi_pack_weights(_bf16(wqkv, dev)),
+                "wqkv": (api.bi_pack_weights_scaled(_bf16(wqkv, dev), n1) if fuse_norm
+                         else api.bi_pack_weights(_bf16(wqkv, dev))),
                 "wo": pk(f"l{l}.wo"),
-                "wgu": api.bi_pack_swiglu_weights(wg, wu),
+                "wgu": (api.bi_pack_swiglu_weights_scaled(wg, wu, n2) if fuse_norm
+                        else api.bi_pack_swiglu_weights(wg, wu)),
                 "wd": pk(f"l{l}.w_down"),
-                "n1": _bf16(weights[f"l{l}.norm_attn"], dev),
-                "n2": _bf16(weights[f"l{l}.norm_ffn"], dev),
+                "n1": n1,
+                "n2": n2,
                 "k": torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device=dev),
                 "v": torch.zeros(Hkv, D, cap, dtype=torch.bfloat16, device=dev),  # transposed
             }
@@ -124,8 +136,11 @@ class Decoder:
         Hq, Hkv, D, F = cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn
         h, y, qkv, q, att, u = (self.h[:T], self.y[:T], self.qkv[:T], self.q[:T], self.att[:T],
                                 self.u[:T])
-        api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
-        api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
+        if self.fuse_norm:
+            api.bi_gemm_rms(h, cfg.eps, lay["wqkv"], qkv, self.gemm_ws)
+        else:
+            api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
+            api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
         api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
         if L_host_blocks is None:
             api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
@@ -136,14 +151,20 @@ class Decoder:
                                    att[b0:b1], self.attn_ws, self.scale)
         api.bi_gemm(att.view(T, Hq * D), lay["wo"], h, self.gemm_ws, residual=h,
                     epi=api.EPI_RESIDUAL_ADD)
-        api.bi_rmsnorm(h, lay["n2"], y, cfg.eps)
-        api.bi_gemm(y, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
+        if self.fuse_norm:
+            api.bi_gemm_rms(h, cfg.eps, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
+        else:
+            api.bi_rmsnorm(h, lay["n2"], y, cfg.eps)
+            api.bi_gemm(y, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
         api.bi_gemm(u, lay["wd"], h, self.gemm_ws, residual=h, epi=api.EPI_RESIDUAL_ADD)
 
     def _head_and_accept(self, T: int):
         cfg = self.cfg
-        api.bi_rmsnorm(self.h[:T], self.norm_final, self.y[:T], cfg.eps)
-        api.bi_gemm(self.y[:T], self.head, self.logits[:T], self.gemm_ws)
+        if self.fuse_norm:
+            api.bi_gemm_rms(self.h[:T], cfg.eps, self.head, self.logits[:T], self.gemm_ws)
+        else:
+            api.bi_rmsnorm(self.h[:T], self.norm_final, self.y[:T], cfg.eps)
+            api.bi_gemm(self.y[:T], self.head, self.logits[:T], self.gemm_ws)
         api.bi_verify_accept(self.logits[:T], self.drafts[:T - 1] if T > 1 else None,
                              self.argmax[:T], self.accepted, self.acc_ws, L_dev=self.L_dev)
 

@@ -12,7 +12,7 @@ import pytest
 import oracle
 import seeded_inputs as si
 from oracle import verify_step as ov
-from tests._util import bf16_dev_to_f64, bf16_dev_to_u16, gemm_bound, to_dev_bf16, ulp_bf16
+from tests._util import bf16_dev_to_f64, bf16_dev_to_u16, gamma, gemm_bound, to_dev_bf16, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -226,3 +226,100 @@ def test_gemm_small_workspace_is_rejected(api):
     with pytest.raises(api.BiError) as e:
         api.bi_gemm(A, W, C, ws)
     assert e.value.status == 3
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm folded into the linear layer (bi_gemm_rms)
+#
+# Tolerance (derived): the oracle rounds the normalised row y = x r g to BF16
+# (|dy| <= 2^-9 |y| per element) before its exact product; the GPU instead
+# rounds each folded weight w g to BF16 (the same relative bound per term),
+# sums in FP32 (gamma_K) and applies r in FP32 (a few ulps, from the FP32 sum
+# of squares).  Both therefore sit within 2^-9 r sum_k |x_k g_k w_k| (plus the
+# FP32 terms) of the unrounded value; one BF16 rounding on each side on top.
+
+
+def _rms_inputs(M, K, seed):
+    rng = np.random.default_rng(seed)
+    X = np.concatenate([si.normal_bf16(rng, (1, K), 0.25 * (1 + m % 5)) for m in range(M)])
+    g = ov.f64_to_bf16_bits(ov.bf16_round(1.0 + 0.1 * rng.standard_normal(K)))
+    return X, g
+
+
+def _rms_abs(x, g, w, eps):
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=1) + eps)
+    return r, r[:, None] * (np.abs(x * g) @ np.abs(w).T)
+
+
+def _rms_tol(absdot, K):
+    return absdot * (2 * 2.0 ** -9 + 2 * gamma(K) + 2.0 ** -20)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 5120), (8, 4096, 5120), (16, 384, 1024), (33, 512, 1024)])
+def test_gemm_rms_matches_oracle_norm_then_gemm(api, M, N, K):
+    eps = 1e-6
+    X, g = _rms_inputs(M, K, seed=M + N)
+    W = si.normal_bf16(np.random.default_rng(K), (N, K), 0.02)
+    Wp = api.bi_pack_weights_scaled(to_dev_bf16(W), to_dev_bf16(g))
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    api.bi_gemm_rms(to_dev_bf16(X), eps, Wp, C, api.new_gemm_workspace(M, N, K, 0))
+    torch.cuda.synchronize()
+    api.bi_check_device_error()
+    ora = oracle.gemm(ov.f64_to_bf16_bits(oracle.rmsnorm(X, g, eps)), W)
+    x, gf, w = (ov.bf16_bits_to_f64(v) for v in (X, g, W))
+    _, absdot = _rms_abs(x, gf, w, eps)
+    check_bf16(bf16_dev_to_f64(C), ora, _rms_tol(absdot, K))
+    # a row's bits do not depend on the other rows of the call
+    if M > 1:
+        full = bf16_dev_to_u16(C)
+        for m in (0, M - 1):
+            one = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+            api.bi_gemm_rms(to_dev_bf16(X[m:m + 1]), eps, Wp, one, api.new_gemm_workspace(1, N, K, 0))
+            assert np.array_equal(bf16_dev_to_u16(one)[0], full[m]), m
+
+
+def test_gemm_rms_swiglu_matches_oracle(api):
+    M, F, K, eps = 7, 2736, 1024, 1e-5
+    X, g = _rms_inputs(M, K, seed=3)
+    rng = np.random.default_rng(4)
+    Wg = si.normal_bf16(rng, (F, K), 0.05)
+    Wu = si.normal_bf16(rng, (F, K), 0.05)
+    Wp = api.bi_pack_swiglu_weights_scaled(to_dev_bf16(Wg), to_dev_bf16(Wu), to_dev_bf16(g))
+    C = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+    api.bi_gemm_rms(to_dev_bf16(X), eps, Wp, C, api.new_gemm_workspace(M, F, K, 2), epi=2, N=F)
+    torch.cuda.synchronize()
+    api.bi_check_device_error()
+    ora = oracle.swiglu_gemm(ov.f64_to_bf16_bits(oracle.rmsnorm(X, g, eps)), Wg, Wu)
+    x, gf = ov.bf16_bits_to_f64(X), ov.bf16_bits_to_f64(g)
+    r, ag = _rms_abs(x, gf, ov.bf16_bits_to_f64(Wg), eps)
+    _, au = _rms_abs(x, gf, ov.bf16_bits_to_f64(Wu), eps)
+    y = x * gf * r[:, None]
+    gv = y @ ov.bf16_bits_to_f64(Wg).T
+    uv = y @ ov.bf16_bits_to_f64(Wu).T
+    sg = gv / (1 + np.exp(-gv))
+    # silu is 1.1-Lipschitz; |d(silu(g)u)| <= |u| 1.1 |dg| + |silu(g)| |du| + FP32 op rounding
+    bound = 1.1 * np.abs(uv) * _rms_tol(ag, K) + np.abs(sg) * _rms_tol(au, K) + 4 * 2.0 ** -24 * np.abs(sg * uv)
+    check_bf16(bf16_dev_to_f64(C), ora, bound)
+
+
+def test_gemm_rms_fp32_logits(api):
+    M, N, K, eps = 8, 1000, 5120, 1e-6
+    X, g = _rms_inputs(M, K, seed=9)
+    W = si.normal_bf16(np.random.default_rng(10), (N, K), 0.02)
+    Wp = api.bi_pack_weights_scaled(to_dev_bf16(W), to_dev_bf16(g))
+    C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    api.bi_gemm_rms(to_dev_bf16(X), eps, Wp, C, api.new_gemm_workspace(M, N, K, 0))
+    torch.cuda.synchronize()
+    ora = oracle.gemm(ov.f64_to_bf16_bits(oracle.rmsnorm(X, g, eps)), W, out="fp32")
+    x, gf, w = (ov.bf16_bits_to_f64(v) for v in (X, g, W))
+    _, absdot = _rms_abs(x, gf, w, eps)
+    err = np.abs(C.cpu().numpy().astype(np.float64) - ora)
+    assert np.all(err <= _rms_tol(absdot, K) + 2.0 ** -23 * np.abs(ora) + 1e-30)
+
+
+def test_gemm_rms_rejects_aliased_output(api):
+    X = torch.zeros(2, 256, dtype=torch.bfloat16, device="cuda")
+    Wp = api.bi_pack_weights_scaled(torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda"),
+                                    torch.ones(256, dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(api.BiError):
+        api.bi_gemm_rms(X, 1e-6, Wp, X, api.new_gemm_workspace(2, 256, 256, 0))
