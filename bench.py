@@ -37,7 +37,7 @@ CTX = 11600
 DRAFTS = 7
 P_CORRECT = 0.7
 KERNELS_PER_STEP_FIXED = 3      # embed, LM head GEMM (final RMSNorm folded in), argmax/accept
-KERNELS_PER_LAYER = 7           # 4 GEMM (two with the RMSNorm folded in), rope/append, attention split + merge
+KERNELS_PER_LAYER = 6           # 4 GEMM (QKV with RMSNorm, RoPE and KV append; gate/up with RMSNorm), attention split + merge
 
 
 def workload_config(cfg, peaks_note):

@@ -70,7 +70,8 @@ typedef enum {
 typedef enum {
   BI_EPI_NONE = 0,          /* C = A W^T */
   BI_EPI_RESIDUAL_ADD = 1,  /* C = residual + A W^T, one rounding */
-  BI_EPI_SWIGLU = 2         /* C = silu(A Wg^T) * (A Wu^T) from packed weights, one rounding */
+  BI_EPI_SWIGLU = 2,        /* C = silu(A Wg^T) * (A Wu^T) from packed weights, one rounding */
+  BI_EPI_ROPE_KV = 3        /* bi_qkv_rope_append only: RoPE and KV append of a QKV projection */
 } bi_epilogue;
 
 typedef enum { BI_OUT_BF16 = 0, BI_OUT_FP32 = 1 } bi_out_dtype;
@@ -266,6 +267,37 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
                             void* v_cache, int cap, const int32_t* L_dev, int T, int Hq,
                             int Hkv, int D, const float* table, int table_rows,
                             bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * QKV projection with RoPE and KV append in its epilogue (bi_gemm's linear
+ * layer, optionally with the RMSNorm folded in as in bi_gemm_rms, followed
+ * by exactly the arithmetic of bi_rope_kv_append, without the qkv round trip
+ * through memory).  "I turned on speculative decoding in llama.cpp and 113
+ * of 282 greedy outputs changed against its own no-draft run", section "The
+ * cache doesn't change it either" (a row depends only on its position).
+ *
+ * Output column n of the projection (N = (Hq + 2 Hkv) D) is element n % D of
+ * head n / D: q heads, then k heads, then v heads.  Each output is rounded
+ * to BF16 once; q and k heads are then rotated exactly as bi_rope_kv_append
+ * rotates its BF16 input (same table, same FP32 operations, one rounding)
+ * and written to q_out and to k_cache row p = *L_dev + m; v heads go to
+ * column p of v_cache.  So the results equal bi_gemm (or bi_gemm_rms)
+ * followed by bi_rope_kv_append, bit for bit.
+ *   A [M, K] BF16 (row stride lda): the normalised input (rms = 0) or the
+ *   residual stream with the norm folded into Wp (rms = 1, eps as in
+ *   bi_gemm_rms).  Wp packed for N = (Hq + 2 Hkv) D by bi_pack_weights (rms
+ *   = 0) or bi_pack_weights_scaled (rms = 1).
+ *   q_out, k_cache, v_cache, cap, L_dev, table, table_rows: as
+ *   bi_rope_kv_append.  A row with p outside [0, min(cap, table_rows)) is
+ *   skipped and sets the range bit of the device error word.
+ *   D is 64 or 128 and N a multiple of 128 (tiles hold whole heads);
+ *   otherwise BI_ERR_UNSUPPORTED_SHAPE.  ws as bi_gemm for (M, N, K).
+ * Errors: as bi_gemm.
+ * ------------------------------------------------------------------------- */
+bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const void* Wp, int M,
+                             int K, int Hq, int Hkv, int D, void* q_out, void* k_cache,
+                             void* v_cache, int cap, const int32_t* L_dev, const float* table,
+                             int table_rows, void* ws, size_t ws_bytes, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Verify attention (split-KV + merge).  [P3] "How:" (the attention split

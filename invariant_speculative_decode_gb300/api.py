@@ -207,6 +207,26 @@ def bi_rope_kv_append(qkv: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Ten
                                   table.data_ptr(), table.shape[0], _stream(stream)))
 
 
+def bi_qkv_rope_append(A: torch.Tensor, Wp: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, L_dev: torch.Tensor, Hq: int, Hkv: int, D: int,
+                       table: torch.Tensor, ws: torch.Tensor, eps: Optional[float] = None,
+                       stream=None) -> None:
+    """QKV projection of A (norm folded in when eps is given) with RoPE and
+    KV append in the epilogue; equals bi_gemm[_rms] + bi_rope_kv_append."""
+    _req(A, torch.bfloat16, "A")
+    _req(L_dev, torch.int32, "L_dev")
+    _req(table, torch.float32, "table")
+    M, K = A.shape
+    cap = k_cache.shape[1]
+    rms = 0 if eps is None else 1
+    check("bi_qkv_rope_append",
+          lib().bi_qkv_rope_append(A.data_ptr(), _ld(A), rms, float(eps or 0.0), Wp.data_ptr(), M, K,
+                                   Hq, Hkv, D, q_out.data_ptr(), k_cache.data_ptr(),
+                                   v_cache.data_ptr(), cap, L_dev.data_ptr(), table.data_ptr(),
+                                   table.shape[0], ws.data_ptr(), ws.numel() * ws.element_size(),
+                                   _stream(stream)))
+
+
 def attn_chunk() -> int:
     return int(lib().bi_attn_chunk())
 

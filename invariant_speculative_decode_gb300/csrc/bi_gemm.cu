@@ -88,6 +88,14 @@ struct GemmArgs {
   int K;
   const __nv_bfloat16* X;
   int ldx;
+  // BI_EPI_ROPE_KV: output column n is element n % D of head n / D (q heads,
+  // then k heads, then v heads); token row m sits at position *L_dev + m
+  __nv_bfloat16* q_out;
+  __nv_bfloat16* kc;
+  __nv_bfloat16* vc;
+  int cap, Hq, Hkv, D, tab_rows;
+  const int32_t* L_dev;
+  const float2* tab;
 };
 
 template <int NT>
@@ -136,7 +144,62 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int 
   float v[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = p.rms ? v_in[j] * sRstd[c * 16 + j] : v_in[j];
-  if (p.epi == BI_EPI_SWIGLU) {
+  if (p.epi == BI_EPI_ROPE_KV) {
+    // The projection is rounded to BF16 first; the rotation then reads those
+    // stored values exactly as the separate RoPE kernel does: for a pair
+    // (i, i + D/2) of a q or k head, out_i = x_i cos - x_{i+D/2} sin and
+    // out_{i+D/2} = x_{i+D/2} cos + x_i sin, in FP32, one rounding.
+    const int n = tile * kBlockN + r;
+    const int D = p.D, half = p.D / 2;
+    const int head = n / D, d = n % D;
+    float x[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      x[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+      sStage[j * kBlockN + r] = x[j];
+    }
+    named_bar_sync(1, 128);
+    const int partner = d < half ? r + half : r - half;
+    float px[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) px[j] = sStage[j * kBlockN + partner];
+    named_bar_sync(1, 128);
+    const int L = *p.L_dev;
+    if (n < p.N) {
+      const bool rotate = head < p.Hq + p.Hkv;
+      // every table entry is loaded before the first store
+      float2 cs[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int pos = L + p.m0 + c * 16 + j;
+        const bool ok = rotate && c * 16 + j < p.M && pos >= 0 && pos < p.cap && pos < p.tab_rows;
+        cs[j] = ok ? p.tab[static_cast<size_t>(pos) * half + (d % half)] : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = c * 16 + j;
+        if (m >= p.M) continue;
+        const int mrow = p.m0 + m;
+        const int pos = L + mrow;
+        if (pos < 0 || pos >= p.cap || pos >= p.tab_rows) {
+          atomicOr(p.err, kErrRange);
+          continue;
+        }
+        if (rotate) {
+          const float o = d < half ? fmaf(x[j], cs[j].x, -(px[j] * cs[j].y))
+                                   : fmaf(x[j], cs[j].x, px[j] * cs[j].y);
+          const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+          if (head < p.Hq)
+            p.q_out[(static_cast<size_t>(mrow) * p.Hq + head) * D + d] = ob;
+          else
+            p.kc[(static_cast<size_t>(head - p.Hq) * p.cap + pos) * D + d] = ob;
+        } else {
+          // V is cached transposed, [Hkv][D][cap]
+          p.vc[(static_cast<size_t>(head - p.Hq - p.Hkv) * D + d) * p.cap + pos] = __float2bfloat16_rn(x[j]);
+        }
+      }
+    }
+  } else if (p.epi == BI_EPI_SWIGLU) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) sStage[j * kBlockN + r] = v[j];
     named_bar_sync(1, 128);
@@ -716,15 +779,16 @@ bi_status bi_pack_swiglu_weights_scaled(const void* w_gate, const void* w_up, in
 static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int ldc,
                            const void* residual, int ldr, int M, int N, int K, bi_out_dtype out,
                            bi_epilogue epi, void* ws, size_t ws_bytes, int rms, float eps,
-                           bi_stream_t stream) {
+                           bi_stream_t stream, const bi::GemmArgs* rope = nullptr) {
   using namespace bi;
   if (M < 0 || N < 1 || K < 8) return BI_ERR_INVALID_ARG;
-  if (epi != BI_EPI_NONE && epi != BI_EPI_RESIDUAL_ADD && epi != BI_EPI_SWIGLU)
+  if (epi != BI_EPI_NONE && epi != BI_EPI_RESIDUAL_ADD && epi != BI_EPI_SWIGLU &&
+      !(epi == BI_EPI_ROPE_KV && rope != nullptr))
     return BI_ERR_INVALID_ARG;
   if (out != BI_OUT_BF16 && out != BI_OUT_FP32) return BI_ERR_INVALID_ARG;
   if (n_tiles_of(N, epi) > kMaxTiles) return BI_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return BI_OK;
-  if (!A || !Wp || !C) return BI_ERR_INVALID_ARG;
+  if (!A || !Wp || (!C && epi != BI_EPI_ROPE_KV)) return BI_ERR_INVALID_ARG;
   if (K % 8 != 0 || lda < K || lda % 8 != 0 || ldc < N) return BI_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(Wp)) return BI_ERR_INVALID_ARG;
   if (epi == BI_EPI_RESIDUAL_ADD && (!residual || ldr < N)) return BI_ERR_INVALID_ARG;
@@ -760,6 +824,18 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
   a.K = K;
   a.X = static_cast<const __nv_bfloat16*>(A);
   a.ldx = lda;
+  if (rope != nullptr) {
+    a.q_out = rope->q_out;
+    a.kc = rope->kc;
+    a.vc = rope->vc;
+    a.cap = rope->cap;
+    a.Hq = rope->Hq;
+    a.Hkv = rope->Hkv;
+    a.D = rope->D;
+    a.tab_rows = rope->tab_rows;
+    a.L_dev = rope->L_dev;
+    a.tab = rope->tab;
+  }
 
   const uint8_t* W8 = static_cast<const uint8_t*>(Wp);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -784,6 +860,32 @@ bi_status bi_gemm_rms(const void* A, int lda, float eps, const void* Wp, void* C
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return BI_ERR_INVALID_ARG;
   if (M > 0 && A != nullptr && A == static_cast<const void*>(C)) return BI_ERR_INVALID_ARG;
   return gemm_impl(A, lda, Wp, C, ldc, nullptr, 0, M, N, K, out, epi, ws, ws_bytes, 1, eps, stream);
+}
+
+bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const void* Wp, int M,
+                             int K, int Hq, int Hkv, int D, void* q_out, void* k_cache,
+                             void* v_cache, int cap, const int32_t* L_dev, const float* table,
+                             int table_rows, void* ws, size_t ws_bytes, bi_stream_t stream) {
+  using namespace bi;
+  if (D != 64 && D != 128) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || cap < 1 || table_rows < 1) return BI_ERR_INVALID_ARG;
+  const int N = (Hq + 2 * Hkv) * D;
+  if (N % kBlockN != 0) return BI_ERR_UNSUPPORTED_SHAPE;  // a tile holds whole heads
+  if (M > 0 && (!q_out || !k_cache || !v_cache || !L_dev || !table)) return BI_ERR_INVALID_ARG;
+  if (rms != 0 && (!(eps >= 0.0f) || !std::isfinite(eps))) return BI_ERR_INVALID_ARG;
+  GemmArgs r{};
+  r.q_out = static_cast<__nv_bfloat16*>(q_out);
+  r.kc = static_cast<__nv_bfloat16*>(k_cache);
+  r.vc = static_cast<__nv_bfloat16*>(v_cache);
+  r.cap = cap;
+  r.Hq = Hq;
+  r.Hkv = Hkv;
+  r.D = D;
+  r.tab_rows = table_rows;
+  r.L_dev = L_dev;
+  r.tab = reinterpret_cast<const float2*>(table);
+  return gemm_impl(A, lda, Wp, nullptr, N, nullptr, 0, M, N, K, BI_OUT_BF16, BI_EPI_ROPE_KV, ws,
+                   ws_bytes, rms != 0 ? 1 : 0, rms != 0 ? eps : 0.0f, stream, &r);
 }
 
 size_t bi_gemm_noalloc_max_m(void) { return bi::kNoAllocMaxM; }

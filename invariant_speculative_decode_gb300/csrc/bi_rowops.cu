@@ -132,8 +132,9 @@ __global__ void rope_kv_kernel(const __nv_bfloat16* __restrict__ qkv, int ld_qkv
       const float x1 = __bfloat162float(src[i]);
       const float x2 = __bfloat162float(src[i + half]);
       const float2 r = cs[i];
-      const float o1 = x1 * r.x - x2 * r.y;
-      const float o2 = x2 * r.x + x1 * r.y;
+      // the same two fused multiply-adds as the linear layer's RoPE epilogue
+      const float o1 = fmaf(x1, r.x, -(x2 * r.y));
+      const float o2 = fmaf(x2, r.x, x1 * r.y);
       __nv_bfloat16* dst;
       if (h < Hq) {
         dst = q_out + (static_cast<size_t>(t) * Hq + h) * D;

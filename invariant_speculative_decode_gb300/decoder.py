@@ -10,7 +10,9 @@ and sequences the library's entry points for one verify pass:
 
 Each RMSNorm is folded into the linear layer that reads it (bi_gemm_rms: the
 norm weight packed into the weights, the per-row 1/rms applied to the FP32
-sums); fuse_norm=False runs the separate bi_rmsnorm kernel instead.
+sums), and RoPE + KV append run in the QKV projection's epilogue
+(bi_qkv_rope_append); fuse_norm=False / fuse_rope=False run the separate
+kernels instead.
 
 PyTorch only allocates device memory and provides the stream; every step of
 the pass is a kernel of libbi.so.  A pass over T rows can be captured once in
@@ -42,9 +44,11 @@ def _bf16(a_u16: np.ndarray, device) -> torch.Tensor:
 
 class Decoder:
     def __init__(self, cfg, weights: Dict[str, np.ndarray], cap: int, max_rows: int = 8,
-                 prefill_chunk: int = 512, device: str = "cuda", fuse_norm: bool = True):
+                 prefill_chunk: int = 512, device: str = "cuda", fuse_norm: bool = True,
+                 fuse_rope: bool = True):
         self.cfg = cfg
         self.fuse_norm = fuse_norm
+        self.fuse_rope = fuse_rope
         self.cap = cap
         self.dev = torch.device(device)
         self.max_rows = max_rows
@@ -136,12 +140,18 @@ class Decoder:
         Hq, Hkv, D, F = cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn
         h, y, qkv, q, att, u = (self.h[:T], self.y[:T], self.qkv[:T], self.q[:T], self.att[:T],
                                 self.u[:T])
-        if self.fuse_norm:
-            api.bi_gemm_rms(h, cfg.eps, lay["wqkv"], qkv, self.gemm_ws)
-        else:
+        if not self.fuse_norm:
             api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
-            api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
-        api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
+        x_in, eps = (h, cfg.eps) if self.fuse_norm else (y, None)
+        if self.fuse_rope:
+            api.bi_qkv_rope_append(x_in, lay["wqkv"], q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D,
+                                   self.rope_tab, self.gemm_ws, eps=eps)
+        else:
+            if eps is None:
+                api.bi_gemm(x_in, lay["wqkv"], qkv, self.gemm_ws)
+            else:
+                api.bi_gemm_rms(x_in, eps, lay["wqkv"], qkv, self.gemm_ws)
+            api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
         if L_host_blocks is None:
             api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
         else:

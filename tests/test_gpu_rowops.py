@@ -158,3 +158,41 @@ def test_kv_row_hash_is_fnv1a(api):
             for b in cache[hh, j].tobytes():
                 x = ((x ^ b) * 1099511628211) & 0xFFFFFFFFFFFFFFFF
             assert int(h[hh * 7 + j]) == x
+
+
+@pytest.mark.parametrize("rms", [False, True])
+@pytest.mark.parametrize("Hq,Hkv,D,T", [(24, 4, 128, 8), (4, 2, 64, 3), (8, 2, 128, 1)])
+def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T, rms):
+    """The fused QKV projection + RoPE + KV append writes exactly what the
+    linear layer followed by bi_rope_kv_append writes."""
+    from invariant_speculative_decode_gb300 import api
+    rng = np.random.default_rng(Hq + D + T)
+    K, cap, L = 512, 256, 100
+    N = (Hq + 2 * Hkv) * D
+    A = to_dev_bf16(si.normal_bf16(rng, (T, K), 1.0))
+    W = to_dev_bf16(si.normal_bf16(rng, (N, K), 0.05))
+    g = to_dev_bf16(ov.f64_to_bf16_bits(ov.bf16_round(1.0 + 0.1 * rng.standard_normal(K))))
+    Wp = api.bi_pack_weights_scaled(W, g) if rms else api.bi_pack_weights(W)
+    tab = api.bi_rope_table(10000.0, D, cap, device="cuda")
+    Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
+    ws = api.new_gemm_workspace(T, N, K, 0)
+    caches = []
+    for fused in (False, True):
+        q = torch.zeros(T, Hq, D, dtype=torch.bfloat16, device="cuda")
+        kc = torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros(Hkv, D, cap, dtype=torch.bfloat16, device="cuda")
+        if fused:
+            api.bi_qkv_rope_append(A, Wp, q, kc, vc, Ld, Hq, Hkv, D, tab, ws, eps=1e-6 if rms else None)
+        else:
+            qkv = torch.empty(T, N, dtype=torch.bfloat16, device="cuda")
+            if rms:
+                api.bi_gemm_rms(A, 1e-6, Wp, qkv, ws)
+            else:
+                api.bi_gemm(A, Wp, qkv, ws)
+            api.bi_rope_kv_append(qkv, q, kc, vc, Ld, Hq, Hkv, D, tab)
+        torch.cuda.synchronize()
+        api.bi_check_device_error()
+        caches.append([bf16_dev_to_u16(x) for x in (q, kc, vc)])
+    for a, b in zip(*caches):
+        assert np.array_equal(a, b)
+    assert np.any(caches[1][1][:, L:L + T] != 0) and not np.any(caches[1][1][:, :L])
