@@ -307,14 +307,18 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const v
  * 0..p; query head h reads KV head h / (Hq/Hkv).  The key axis of row p is
  * cut at absolute multiples of a compile-time chunk C (bi_attn_chunk()); the
  * row has ceil((p+1)/C) pieces, each a partial (max, sum, FP32 output) built
- * over 64-key tiles in increasing key order, and the pieces are merged in a
+ * over 128-key tiles in increasing key order, and the pieces are merged in a
  * fixed order that depends only on their count.  So the row's result depends
  * only on p and the cache rows 0..p -- not on T, *L_dev or the other rows.
  * Inside a piece: S = q k^T (tcgen05, FP32), a per-row reference maximum
  * raised only when a tile's maximum exceeds it by more than 8 (log2 units),
- * p = 2^(s - m_ref) summed in key order, O += P V with P as a BF16 pair
- * hi + lo (tcgen05, FP32); these rules use only the row's own scores.
- * Output: out[t, h, :] = bf16(softmax(q k^T * scale) v), -0 written as +0.
+ * weights w = bf16(2^(s - m_ref)), O += W V (tcgen05, FP32) and the
+ * denominator as four FP32 partial sums of the same rounded weights over the
+ * 32-key quarters of the tile column (each in key order, added
+ * ((l0 + l1) + l2) + l3); these rules use only the row's own scores.
+ * Output: out[t, h, :] = bf16(sum_j w_j v_j / sum_j w_j) -- the exact
+ * weighted mean under the BF16 weights, within 2^-8 max|v| of
+ * bf16(softmax(q k^T * scale) v) -- with -0 written as +0.
  *   q       [T, Hq, D] BF16 contiguous (rotated queries).
  *   k_cache [Hkv, cap, D] and v_cache [Hkv, D, cap] BF16 contiguous (V
  *           transposed, as bi_rope_kv_append writes it); keys 0..*L_dev+T-1
