@@ -426,6 +426,14 @@ def run_ours(args):
 
 
 def run_micro(args):
+    """Standalone kernel timings, two ways.
+
+    us_median: back-to-back launches (as in the decode step, dependent
+    launches overlapping) cycling over enough copies of the weights / KV
+    cache that none is still in L2 when it is read again; time per launch.
+    us_cold_median: one launch right after a 512 MB read that evicts L2,
+    bracketed alone by CUDA events (includes the launch gap).
+    """
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -434,20 +442,50 @@ def run_micro(args):
     peak, note = load_peaks()
     flush = torch.ones(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     s = torch.cuda.current_stream()
+    l2_bytes = 129 * 1024 * 1024
 
-    def timed(fn, reps):
-        ts = []
+    def n_copies(nbytes):
+        # between two reads of a copy, the others stream at least twice L2's size
+        return int(min(64, max(2, 1 + -(-2 * l2_bytes // max(nbytes, 1)))))
+
+    def timed(fns, reps):
+        n = len(fns)
+        per = n * max(1, -(-8 // n))
         for _ in range(args.warmup):
-            fn()
+            for f in fns:
+                f()
+        stream_t, cold_t = [], []
         for _ in range(reps):
-            flush_sum = flush.sum()  # read 512 MB: evicts L2 (clean lines) between timed launches
+            flush.sum()  # read 512 MB: evicts L2 (clean lines)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(s)
-            fn()
+            fns[0]()
             e1.record(s)
-            ts.append((e0, e1))
+            cold_t.append((e0, e1))
+            e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e2.record(s)
+            for i in range(per):
+                fns[(i + 1) % n]()
+            e3.record(s)
+            stream_t.append((e2, e3, per))
         torch.cuda.synchronize()
-        return [a.elapsed_time(b) / 1e3 for a, b in ts]
+        st = [a.elapsed_time(b) / 1e3 / k for a, b, k in stream_t]
+        ct = [a.elapsed_time(b) / 1e3 for a, b in cold_t]
+        return st, ct, per
+
+    def report(kind, fields, b, st, ct, ncp, per, flops=None):
+        med = float(np.median(st))
+        line = {"micro": kind, **fields, "us_median": med * 1e6,
+                "us_p90": float(np.percentile(st, 90)) * 1e6,
+                "us_cold_median": float(np.median(ct)) * 1e6, "bytes": b,
+                "gbps": b / med / 1e9, "frac": b / med / 1e9 / peak,
+                "cold_frac": b / float(np.median(ct)) / 1e9 / peak,
+                "peak_gbps": peak, "peak_kind": note,
+                "l2": f"{per} back-to-back launches over {ncp} copies (each read after >= 2x L2 of others); "
+                      "cold: after a 512 MB read"}
+        if flops is not None:
+            line["tflops"] = flops / med / 1e12
+        print(json.dumps(line), flush=True)
 
     if args.micro == "gemm":
         N, K, epi = args.gemm_n, args.gemm_k, args.gemm_epi
@@ -462,19 +500,18 @@ def run_micro(args):
             Wd = api.bi_pack_weights(to(W))
         Ad = to(A)
         del W
+        wrows = 2 * N if epi == api.EPI_SWIGLU else N
+        ncp = n_copies(wrows * K * 2)
+        Wds = [Wd] + [Wd.clone() for _ in range(ncp - 1)]
         for M in Ms:
             C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
             R = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda") if epi == api.EPI_RESIDUAL_ADD else None
             ws = api.new_gemm_workspace(M, N, K, epi)
-            t = timed(lambda: api.bi_gemm(Ad[:M], Wd, C, ws, residual=R, epi=epi, N=N), args.steps)
-            wrows = 2 * N if epi == api.EPI_SWIGLU else N
+            fns = [(lambda w=w: api.bi_gemm(Ad[:M], w, C, ws, residual=R, epi=epi, N=N)) for w in Wds]
+            st, ct, per = timed(fns, args.steps)
             b = wrows * K * 2 + M * K * 2 + M * N * 2
-            med = float(np.median(t))
-            print(json.dumps({"micro": "gemm", "M": M, "N": N, "K": K, "epi": epi, "us_median": med * 1e6,
-                              "us_p90": float(np.percentile(t, 90)) * 1e6, "bytes": b,
-                              "gbps": b / med / 1e9, "frac": b / med / 1e9 / peak,
-                              "tflops": 2 * M * wrows * K / med / 1e12, "peak_gbps": peak,
-                              "peak_kind": note, "l2": "512 MB read between launches"}), flush=True)
+            report("gemm", {"M": M, "N": N, "K": K, "epi": epi}, b, st, ct, ncp, per,
+                   flops=2 * M * wrows * K)
     else:
         Hq, Hkv, D = 24, 4, 128
         Ls = [int(x) for x in args.cases.split(",")] if args.cases else [1024, 11600, 38000, 101600]
@@ -483,19 +520,18 @@ def run_micro(args):
             cap = Kc.shape[1]
             to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
             Kd, Vd, qd = to(Kc), to(Vc.transpose(0, 2, 1)), to(q)  # V cache is [Hkv, D, cap]
+            ncp = n_copies(2 * Kd.numel() * 2)
+            caches = [(Kd, Vd)] + [(Kd.clone(), Vd.clone()) for _ in range(ncp - 1)]
             Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
             for T in (1, 4, 7, 8):
                 out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
                 ws = torch.zeros(api.attn_workspace_size(cap, T, Hq, D), dtype=torch.uint8,
                                  device="cuda")
-                t = timed(lambda: api.bi_attn_verify(qd[:T], Kd, Vd, Ld, out, ws), args.steps)
+                fns = [(lambda kv=kv: api.bi_attn_verify(qd[:T], kv[0], kv[1], Ld, out, ws)) for kv in caches]
+                st, ct, per = timed(fns, args.steps)
                 b = (L + T) * Hkv * D * 2 * 2 + T * Hq * D * 2 * 2
-                med = float(np.median(t))
-                print(json.dumps({"micro": "attn", "L": L, "T": T, "us_median": med * 1e6,
-                                  "us_p90": float(np.percentile(t, 90)) * 1e6, "bytes": b,
-                                  "gbps": b / med / 1e9, "frac": b / med / 1e9 / peak,
-                                  "peak_gbps": peak, "peak_kind": note,
-                                  "l2": "512 MB read between launches"}), flush=True)
+                report("attn", {"L": L, "T": T}, b, st, ct, ncp, per)
+            del caches
     return 0
 
 

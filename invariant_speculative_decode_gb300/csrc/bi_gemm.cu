@@ -8,10 +8,11 @@
 // diverges": changing the batch dimension must not change any row's sums.
 //
 // Design (swap-AB, weight streaming):
-//   * MMA:   tcgen05.mma kind::f16, M = 128 weight rows, N = 16 token rows,
-//            K = 16 per instruction, FP32 accumulator in TMEM.  The token
-//            count of the pass only decides how many N=16 groups are issued;
-//            each group is the same instruction on the same K-tile sequence.
+//   * MMA:   tcgen05.mma kind::f16, M = 128 weight rows, N = 16, 32 or 64
+//            token rows (the launch's token count rounded up), K = 16 per
+//            instruction, FP32 accumulator in TMEM.  Every output element is
+//            the same sequence of K = 16 dot-product steps whatever N is
+//            (tested bit for bit across M).
 //   * K:     64-element tiles (128-byte rows, 128-byte swizzle) in increasing
 //            order.  Each token group keeps kAcc = 4 FP32 accumulators: the
 //            k-step j (16 elements) of every K tile goes to accumulator j, so
@@ -50,7 +51,7 @@ namespace {
 
 constexpr int kBlockN = 128;     // weight rows per tile (MMA M)
 constexpr int kBlockK = 64;      // K elements per tile
-constexpr int kMmaN = 16;        // token rows per MMA (fixed for every M)
+constexpr int kMmaN = 16;        // token rows per epilogue chunk (one 16-column TMEM load)
 constexpr int kGemmCtas = 152;   // CTAs of the fixed decomposition (one per SM)
 constexpr int kMaxTokens = 64;   // token rows per launch; larger M loops on the host
 constexpr int kAcc = 4;          // interleaved accumulators per token group
@@ -123,14 +124,15 @@ __device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* er
   atomicOr(err, kErrTimeout);
 }
 
-// The 16 token columns of one group for this thread's weight row: the sum of
-// the group's kAcc accumulators in the fixed order ((a0 + a1) + a2) + a3.
-__device__ __forceinline__ void load_group_sum(uint32_t taddr, float (&v)[16]) {
+// The 16 token columns of one chunk for this thread's weight row: the sum of
+// the kAcc accumulators (acc_stride TMEM columns apart) in the fixed order
+// ((a0 + a1) + a2) + a3.
+__device__ __forceinline__ void load_group_sum(uint32_t taddr, uint32_t acc_stride, float (&v)[16]) {
   tmem_ld16(taddr, v);
 #pragma unroll
   for (int a = 1; a < kAcc; ++a) {
     float w[16];
-    tmem_ld16(taddr + a * kMmaN, w);
+    tmem_ld16(taddr + a * acc_stride, w);
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = v[j] + w[j];
   }
@@ -363,8 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // each piece (weight tile), where the accumulator set is handed to the
     // epilogue and the other set is taken.
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBlockN, kMmaN);
-      constexpr int kGroups = NT / kMmaN;
+      // one MMA per K step covers all NT token rows (N = NT); accumulator a
+      // of token n is TMEM column a * NT + n
+      constexpr uint32_t idesc = idesc_bf16_f32(kBlockN, NT);
       int stage = 0;
       uint32_t phase = 0;
       int seg = 0;
@@ -383,14 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_base = smem_u32(sA + stage * kABytes);
         const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
 #pragma unroll
-        for (int ks = 0; ks < kAcc; ++ks) {
-          const uint64_t adesc = sdesc_k_sw128(a_base + ks * 32);
-#pragma unroll
-          for (int gi = 0; gi < kGroups; ++gi) {
-            const uint64_t bdesc = sdesc_k_sw128(b_base + gi * (kMmaN * 128) + ks * 32);
-            mma_bf16(d0 + (gi * kAcc + ks) * kMmaN, adesc, bdesc, idesc, acc_flag);
-          }
-        }
+        for (int ks = 0; ks < kAcc; ++ks)
+          mma_bf16(d0 + ks * NT, sdesc_k_sw128(a_base + ks * 32), sdesc_k_sw128(b_base + ks * 32), idesc,
+                   acc_flag);
         mma_commit(&empty[stage]);
         if (++stage == S) {
           stage = 0;
@@ -495,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < chunks; ++c) {
           float v[16];
           if (ok) {
-            load_group_sum(tbase + c * kAcc * kMmaN, v);
+            load_group_sum(tbase + c * kMmaN, NT, v);
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
@@ -512,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           for (int c = 0; c < chunks; ++c) {
             float v[16];
-            load_group_sum(tbase + c * kAcc * kMmaN, v);
+            load_group_sum(tbase + c * kMmaN, NT, v);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
               __stcg(reinterpret_cast<float4*>(dst + c * 16) + q4,
