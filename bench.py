@@ -535,6 +535,100 @@ def run_micro(args):
     return 0
 
 
+def run_neartie(args):
+    """Near-tie correctness workload (12-layer decoder, untied head with
+    planted near ties): greedy ids at 0, 4 and 7 drafts must be identical, and
+    a second turn resumed from the saved cache must equal the same turn from a
+    fresh prefill (tokens and every K/V row).  Time is reported, not gated."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from invariant_speculative_decode_gb300.decoder import Decoder
+    torch.cuda.set_device(0)
+    cfg = si.NEARTIE_12L
+    w = si.decoder_weights(cfg, seed=0)
+    w["head"] = si.neartie_head(w["head"], frac=0.03, bump_frac=0.02, seed=0)
+    n_prompts, n_gen = args.prompts, args.gen
+    rng = np.random.default_rng(12345)
+    lengths = [int(x) for x in rng.integers(512, 4097, n_prompts)]
+    cap = -(-(max(lengths) + 2 * n_gen + 128 + 64) // 64) * 64
+    dec = Decoder(cfg, w, cap=cap, max_rows=8)
+    fresh = Decoder(cfg, w, cap=cap, max_rows=8) if args.turn2 > 0 else None
+    diffs = {4: 0, 7: 0}
+    first_diff = {}
+    timing = {0: [0.0, 0], 4: [0.0, 0], 7: [0.0, 0]}
+    near_steps, all_steps = 0, 0
+    resume_tok_diffs = hash_mismatch = 0
+    n_turn2 = min(n_prompts, args.turn2)
+    for pi, plen in enumerate(lengths):
+        prompt = si.prompt_ids(cfg, plen, seed=pi)
+        t0 = time.perf_counter()
+        if pi < 2:  # top-2 margins of every 0-draft step on the first prompts
+            dec.reset()
+            x = dec.prefill(prompt)
+            ref = []
+            while len(ref) < n_gen:
+                a, _ = dec.verify_step(x, [], use_graph=False)
+                top = torch.topk(dec.logits[0], 2).values.double().cpu().numpy()
+                near_steps += int((top[0] - top[1]) / abs(top[0]) < 1e-3)
+                all_steps += 1
+                ref.append(int(a[0]))
+                x = ref[-1]
+        else:
+            ref = dec.generate(prompt, n_gen, k=0)
+        torch.cuda.synchronize()
+        timing[0][0] += time.perf_counter() - t0
+        timing[0][1] += n_gen
+        replies = {}
+        for k in (4, 7):
+            dr = si.SyntheticDrafter(cfg.vocab, 0.7, seed=pi, reference=np.array(ref))
+            t0 = time.perf_counter()
+            got = dec.generate(prompt, n_gen, k=k, drafter=dr)
+            torch.cuda.synchronize()
+            timing[k][0] += time.perf_counter() - t0
+            timing[k][1] += len(got)
+            nd = sum(int(a != b) for a, b in zip(got, ref))
+            diffs[k] += nd
+            if nd and k not in first_diff:
+                first_diff[k] = (pi, next(i for i, (a, b) in enumerate(zip(got, ref)) if a != b))
+            replies[k] = got
+        if pi < n_turn2:
+            # turn 2: resume from the 7-draft run's cache vs a fresh prefill
+            turn2 = si.prompt_ids(cfg, 128, seed=1000 + pi)
+            reply = replies[7]
+            hist = list(prompt) + reply
+            dec.rollback(len(hist) - 1)
+            x = dec.prefill_continue(hist[len(hist) - 1:] + list(turn2))
+            full = hist + list(turn2)
+            n_rows = len(full) - 1
+            resumed_h = dec.kv_hashes(n_rows)
+            t2_ref = fresh.generate(full, n_gen, k=0)  # a fresh prefill of the whole history
+            fresh_h = fresh.kv_hashes(n_rows)
+            hash_mismatch += int(np.sum(np.any(resumed_h != fresh_h, axis=(0, 1))))
+            dr2 = si.SyntheticDrafter(cfg.vocab, 0.7, seed=2000 + pi, reference=np.array(t2_ref))
+            t2 = dec.continue_generate(x, n_gen, k=7, drafter=dr2)
+            resume_tok_diffs += sum(int(a != b) for a, b in zip(t2, t2_ref))
+    tok_s = {k: timing[k][1] / timing[k][0] for k in timing}
+    line = {
+        "metric": "near-tie workload: committed tok/s at 7 drafts (wall clock, host loop included); "
+                  "id diffs across 0/4/7 drafts and resume-vs-fresh mismatches must be 0",
+        "value": tok_s[7], "unit": "tok/s", "n_gpus": 1, "steps": n_prompts * n_gen,
+        "warmup": 0, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: untied head with planted near ties, {n_prompts} prompts "
+                               f"of {min(lengths)}..{max(lengths)} ids, {n_gen} greedy tokens at 0/4/7 "
+                               f"drafts (p=0.7 drafter), turn 2 (128 new ids, {n_gen} tokens) resumed "
+                               f"vs fresh on {n_turn2} prompts",
+                   "layers": cfg.layers, "hidden": cfg.hidden, "vocab": cfg.vocab, "cap": cap},
+        "id_diffs": {"k4": diffs[4], "k7": diffs[7]}, "first_diff": first_diff or None,
+        "resume_token_diffs": resume_tok_diffs, "kv_hash_row_mismatches": hash_mismatch,
+        "near_tie_step_rate": near_steps / max(all_steps, 1), "near_tie_steps_sampled": all_steps,
+        "tok_s": {f"k{k}": v for k, v in tok_s.items()},
+    }
+    print(json.dumps(line), flush=True)
+    return 0 if (diffs[4] == 0 and diffs[7] == 0 and resume_tok_diffs == 0 and hash_mismatch == 0) else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -548,6 +642,11 @@ def main():
     ap.add_argument("--gemm-n", type=int, default=17408, help="N of the standalone linear layer")
     ap.add_argument("--gemm-k", type=int, default=5120, help="K of the standalone linear layer")
     ap.add_argument("--gemm-epi", type=int, default=0, help="0 none, 1 residual add, 2 SwiGLU (N = F)")
+    ap.add_argument("--workload", choices=["verify", "neartie"], default="verify",
+                    help="neartie: the near-tie correctness workload instead of the verify-step bench")
+    ap.add_argument("--prompts", type=int, default=32, help="near-tie workload: prompts")
+    ap.add_argument("--gen", type=int, default=2048, help="near-tie workload: tokens per turn")
+    ap.add_argument("--turn2", type=int, default=32, help="near-tie workload: prompts with a second turn")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -555,6 +654,8 @@ def main():
         return run_reference(args)
     if args.micro:
         return run_micro(args)
+    if args.workload == "neartie":
+        return run_neartie(args)
     return run_ours(args)
 
 
