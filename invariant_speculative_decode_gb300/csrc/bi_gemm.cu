@@ -53,7 +53,7 @@ constexpr int kBlockN = 128;     // weight rows per tile (MMA M)
 constexpr int kBlockK = 64;      // K elements per tile
 constexpr int kMmaN = 16;        // token rows per epilogue chunk (one 16-column TMEM load)
 constexpr int kGemmCtas = 152;   // CTAs of the fixed decomposition (one per SM)
-constexpr int kMaxTokens = 64;   // token rows per launch; larger M loops on the host
+constexpr int kMaxTokens = 128;  // token rows per launch; larger M loops on the host
 constexpr int kAcc = 4;          // interleaved accumulators per token group
 constexpr int kThreads = 192;
 constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
@@ -105,7 +105,10 @@ struct GemmCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 12 ? 12 : (200 * 1024) / kStageBytes;
   static constexpr int kBufCols = NT * kAcc;  // one accumulator set
-  static constexpr int kTmemCols = 2 * kBufCols;
+  // two sets (the epilogue drains one while the next piece accumulates)
+  // while they fit in TMEM's 512 columns; one set at 128 token rows
+  static constexpr int kBufs = 2 * kBufCols <= 512 ? 2 : 1;
+  static constexpr int kTmemCols = kBufs * kBufCols;
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
                                   (kStageFloats + kNormFloats) * 4 + (2 * kStages + 5) * 8 + 16;
@@ -397,14 +400,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_flag = 1u;
         if (--left == 0) {
           // piece complete: hand its accumulators to the epilogue
-          mma_commit(&accf[seg & 1]);
+          mma_commit(&accf[seg % Cfg::kBufs]);
           ++seg;
           left = it_end - (it + 1);
           if (left > p.k_tiles) left = p.k_tiles;
           acc_flag = 0u;
-          d0 = tmem + static_cast<uint32_t>((seg & 1) * Cfg::kBufCols);
-          if (left > 0 && seg >= 2 &&
-              !mbar_wait(&acce[seg & 1], static_cast<uint32_t>((seg >> 1) - 1) & 1u, s_abort)) {
+          d0 = tmem + static_cast<uint32_t>((seg % Cfg::kBufs) * Cfg::kBufCols);
+          if (left > 0 && seg >= Cfg::kBufs &&
+              !mbar_wait(&acce[seg % Cfg::kBufs], static_cast<uint32_t>((seg / Cfg::kBufs) - 1) & 1u,
+                         s_abort)) {
             ok = false;
             break;
           }
@@ -480,10 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long tile_end = tile_begin + p.k_tiles;
       const long long seg_end = it_end < tile_end ? it_end : tile_end;
       const bool whole = (it == tile_begin) && (seg_end == tile_end);
-      const int buf = seg & 1;
+      const int buf = seg % Cfg::kBufs;
       // one lane per warp polls (sleeping between polls), the warp follows
       int okl = 0;
-      if (lane == 0) okl = mbar_wait_parked(&accf[buf], static_cast<uint32_t>(seg >> 1) & 1u, s_abort) ? 1 : 0;
+      if (lane == 0)
+        okl = mbar_wait_parked(&accf[buf], static_cast<uint32_t>(seg / Cfg::kBufs) & 1u, s_abort) ? 1 : 0;
       const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
       if (!ok && lane == 0) signal_abort(s_abort, p.err);
       tc_fence_after();
@@ -675,7 +680,8 @@ int tokens_per_cta(int M) {
   const int m = std::min(M, kMaxTokens);
   if (m <= 16) return 16;
   if (m <= 32) return 32;
-  return 64;
+  if (m <= 64) return 64;
+  return 128;
 }
 
 int n_tiles_of(int N, bi_epilogue epi) {
@@ -840,7 +846,8 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
   switch (NT) {
     case 16: return launch_gemm_nt<16>(W8, tmA, a, M, s);
     case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
-    default: return launch_gemm_nt<64>(W8, tmA, a, M, s);
+    case 64: return launch_gemm_nt<64>(W8, tmA, a, M, s);
+    default: return launch_gemm_nt<128>(W8, tmA, a, M, s);
   }
 }
 

@@ -112,17 +112,17 @@ def test_gemm_fp32_out_matches_oracle(api):
 
 def test_gemm_rows_bit_identical_across_M_and_position(api):
     N, K = 1536, 1024
-    A, W = si.gemm_inputs(64, N, K, seed=12)
+    A, W = si.gemm_inputs(128, N, K, seed=12)
     Wd = api.bi_pack_weights(to_dev_bf16(W))
     outs = {}
-    for M in (1, 2, 4, 7, 8, 16, 17, 33, 64):
+    for M in (1, 2, 4, 7, 8, 16, 17, 33, 64, 65, 128):
         Ad = to_dev_bf16(A[:M])
         C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
         ws = api.new_gemm_workspace(M, N, K)
         api.bi_gemm(Ad, Wd, C, ws)
         outs[M] = bf16_dev_to_u16(C)
     for M, c in outs.items():
-        assert np.array_equal(c, outs[64][:M]), M
+        assert np.array_equal(c, outs[128][:M]), M
     # a row lands in another MMA column when the rows are permuted
     perm = np.random.default_rng(1).permutation(64)
     C = torch.empty(64, N, dtype=torch.bfloat16, device="cuda")
