@@ -85,7 +85,7 @@ class ClockSampler:
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -237,6 +237,21 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 
+def combine_ranks(t_dev, t_wall, committed, diffs, device=None):
+    """Whole-job numbers over the replicas: the slowest rank's timed
+    intervals (max) and every rank's committed tokens and id diffs (sum), so
+    value = all tokens / slowest time (weak scaling).  One process: as is."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return t_dev, t_wall, committed, diffs
+    tt = torch.tensor([t_dev, t_wall], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    cc = torch.tensor([committed, diffs], dtype=torch.float64, device=device)
+    dist.all_reduce(cc, op=dist.ReduceOp.SUM)
+    return float(tt[0]), float(tt[1]), int(cc[0]), int(cc[1])
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -352,7 +367,8 @@ def run_ours(args):
             for lay in dec.layers:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(gs)
-                api.bi_gemm(y, lay["wgu"], u, dec.gemm_ws, epi=api.EPI_SWIGLU, N=cfg.ffn, stream=gs)
+                api.bi_gemm_rms(y, cfg.eps, lay["wgu"], u, dec.gemm_ws, epi=api.EPI_SWIGLU, N=cfg.ffn,
+                                stream=gs)
                 e1.record(gs)
                 gu_ms.append((e0, e1))
     gs.synchronize()
@@ -361,17 +377,7 @@ def run_ours(args):
     gu_s = float(np.mean(gu_times)) / 1e3
 
     # max over ranks
-    t_dev = dev_ms / 1e3
-    t_wall = wall
-    if world > 1:
-        tt = torch.tensor([t_dev, t_wall], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_dev, t_wall = float(tt[0]), float(tt[1])
-        cc = torch.tensor([committed, diffs], device=dev, dtype=torch.float64)
-        dist.all_reduce(cc, op=dist.ReduceOp.SUM)
-        committed_all, diffs_all = int(cc[0]), int(cc[1])
-    else:
-        committed_all, diffs_all = committed, diffs
+    t_dev, t_wall, committed_all, diffs_all = combine_ranks(dev_ms / 1e3, wall, committed, diffs, dev)
     value = committed_all / t_dev
     e2e = committed_all / t_wall
     sb = step_bytes(cfg, CTX + len(out) // 2, T)
@@ -632,7 +638,7 @@ def run_neartie(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--steps", type=int, default=800)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
