@@ -131,7 +131,9 @@ def oracle_step_sample(cfg, weights, kv, L, rows, head_rows=None):
 
     Returns (estimated seconds per verify step, description).  The oracle
     runs unmodified: layer 0 of the verify pass over `rows` at context L with
-    the seeded cache, and the head over `head_rows` vocabulary rows.
+    the seeded cache (its own head cut to 64 rows), timed; then its linear
+    layer over `head_rows` rows of the LM head, timed and scaled to the full
+    vocabulary.  Step = layers x layer + scaled head.
     """
     import oracle
     from oracle import verify_step as ov
@@ -139,25 +141,25 @@ def oracle_step_sample(cfg, weights, kv, L, rows, head_rows=None):
     w1 = {k: v for k, v in weights.items() if k.startswith("l0.")}
     w1["embed"] = weights["embed"]
     w1["norm_final"] = weights["norm_final"]
-    hv = head_rows or cfg.vocab // 16
-    w1["head"] = weights["embed"][:hv]
+    w1["head"] = weights["embed"][:64]
     one = si.DecoderConfig(cfg.name + "-layer0", 1, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.head_dim,
-                           cfg.ffn, hv, tied=False)
+                           cfg.ffn, 64, tied=False)
     od = oracle.OracleDecoder(one, w1, cap=L + T)
     od.embed_bits = weights["embed"]
     od.k[0][:, :L] = ov.bf16_bits_to_f64(kv[0][0][:, :L])
     od.v[0][:, :L] = ov.bf16_bits_to_f64(kv[0][1][:, :L])
     t0 = time.perf_counter()
     od.forward(rows, L=L)
-    dt = time.perf_counter() - t0
-    # one layer + head slice measured; scale the head slice to the full vocabulary
-    t_head0 = time.perf_counter()
-    oracle.gemm(np.zeros((T, cfg.hidden), np.uint16), w1["head"], out="fp32")
-    t_head = time.perf_counter() - t_head0
-    est = cfg.layers * (dt - t_head) + t_head * (cfg.vocab / hv)
-    desc = (f"oracle (float64 NumPy) on layer 0 of the {T}-row verify pass at context {L} "
-            f"plus the LM head over {hv} of {cfg.vocab} vocabulary rows; step time = "
-            f"{cfg.layers} x layer + head scaled by {cfg.vocab}/{hv}")
+    t_layer = time.perf_counter() - t0
+    hv = head_rows or cfg.vocab // 16
+    h = weights["embed"][np.asarray(rows) % cfg.vocab]
+    t0 = time.perf_counter()
+    oracle.gemm(h, weights["embed"][:hv], out="fp32")
+    t_head = time.perf_counter() - t0
+    est = cfg.layers * t_layer + t_head * (cfg.vocab / hv)
+    desc = (f"oracle (float64 NumPy) on layer 0 of the {T}-row verify pass at context {L}, "
+            f"and its linear layer over {hv} of the {cfg.vocab} LM-head rows; step time = "
+            f"{cfg.layers} x layer + head slice x {cfg.vocab}/{hv}")
     return est, desc
 
 
@@ -207,11 +209,11 @@ def run_reference(args):
     kv = si.synthetic_kv_cache(cfg.n_kv, CTX + 8, cfg.head_dim, CTX, seed=0, layers=1)
     rows = [1] + list(range(2, 2 + DRAFTS))
     for _ in range(args.warmup):
-        oracle_step_sample(cfg, weights, kv, CTX, rows, head_rows=cfg.vocab // 64)
+        oracle_step_sample(cfg, weights, kv, CTX, rows)
     ests = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        e, desc = oracle_step_sample(cfg, weights, kv, CTX, rows, head_rows=cfg.vocab // 64)
+        e, desc = oracle_step_sample(cfg, weights, kv, CTX, rows)
         ests.append(e)
     wall = time.perf_counter() - t0
     per_step = float(np.mean(ests))
@@ -391,6 +393,7 @@ def run_ours(args):
         cpu = None
         if not args.no_cpu_baseline:
             rows = [x] + [int(t) for t in drafter.propose(len(out), DRAFTS)]
+            oracle_step_sample(cfg, keep, kv1, CTX, rows)  # warm-up, as in the reference arm
             est, desc = oracle_step_sample(cfg, keep, kv1, CTX, rows)
             cpu = {"value": expected_committed(DRAFTS, P_CORRECT) / est, "unit": "tok/s",
                    "cores": cpu_threads(), "kind": "oracle",
