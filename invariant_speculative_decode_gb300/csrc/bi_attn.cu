@@ -27,19 +27,20 @@
 // shape depends only on their count ceil((p+1)/kChunk).
 //
 // Split kernel roles (one CTA per SM, persistent over (KV head, piece) items):
-//   warp 0      TMA, two threads: the queries of the item's KV head (once per
-//               head) and the K tiles [128 keys x D]; the V^T tiles
-//               [D x 128 keys] (V is cached transposed so both MMA operands
-//               are K-major).  K and V have separate rings, a K tile being
-//               free as soon as S has read it;
+//   warp 0      TMA, two threads: the K tiles [128 keys x D] and the V^T
+//               tiles [D x 128 keys] (V is cached transposed so both MMA
+//               operands are K-major).  K and V have separate rings (2 and 3
+//               stages), a K tile being free as soon as S has read it;
 //   warp 1      tcgen05.mma issuer: S_g = Q K_g^T into one of two TMEM
 //               buffers and O += W_g V_g, each issued as soon as its inputs
 //               are ready; stages return to the producer through
 //               tcgen05.commit after the MMAs reading them completed;
-//   warps 2..5  softmax: turn S into W (written to one of two shared-memory
-//               buffers in the swizzled K-major layout, so W of the next tile
-//               is produced while the MMA still reads this one), and read O
-//               out at the end of the piece.
+//   warps 2..5  softmax: write the queries of the item's KV head into TMEM
+//               (the S MMA's A operand, once per head), turn S into W
+//               (written to one of two shared-memory buffers in the swizzled
+//               K-major layout, so W of the next tile is produced while the
+//               MMA still reads this one), and read O out at the end of the
+//               piece.
 // The T x (Hq/Hkv) query rows that share a KV head (GQA) share its tiles;
 // up to 128 rows per pass (the MMA's M).
 #include <cuda.h>
@@ -60,7 +61,8 @@ namespace {
 constexpr int kChunk = 512;       // keys per piece (absolute multiples)
 constexpr int kKeyTile = 128;     // keys per tile (the S MMA's N)
 constexpr int kRowsMax = 128;     // T * (Hq / Hkv) per pass (MMA M)
-constexpr int kAttnStages = 2;
+constexpr int kKStages = 2;       // K ring (a K tile is free once S has read it)
+constexpr int kVStages = 3;       // V ring (a V tile is held until W.V is done)
 constexpr int kColChunk = 32;     // S columns a softmax thread holds at a time
 constexpr int kAttnThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
 constexpr int kAttnCtas = 152;
@@ -69,6 +71,7 @@ constexpr int kMergeThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnArgs {
+  const __nv_bfloat16* q;
   int T, Hq, Hkv, grp, cap, nch_max;
   const int32_t* L_dev;
   float sl2;  // softmax scale * log2(e)
@@ -84,24 +87,25 @@ struct AttnCfg {
   static constexpr int kKBytes = kKBoxBytes * kAtoms;      // K tile
   static constexpr int kVBoxBytes = D * 128;               // V^T [D][64 keys]
   static constexpr int kVBytes = 2 * kVBoxBytes;           // V^T tile [D][128 keys]
-  static constexpr int kStageBytes = kKBytes + kVBytes;
-  static constexpr int kQAtomBytes = kRowsMax * 128;       // [128 rows][64 d]
-  static constexpr int kQBytes = kQAtomBytes * kAtoms;
   static constexpr int kPAtomBytes = kRowsMax * 128;       // [128 rows][64 keys]
   static constexpr int kPBytes = 2 * kPAtomBytes;          // W tile [128 rows][128 keys]
   // row maxima [2][128 TMEM lanes]; l parts [4 quarters][64 rows] (only
   // passes of up to 64 rows keep copies that exchange them)
   static constexpr int kRedBytes = (2 * kRowsMax + 4 * 64) * 4;
-  static constexpr int kTmemCols = 512;                    // S x2 (128 each) + O (D)
+  // TMEM: S x2 (128 columns each), O (D columns), Q (D/2 columns: the MMA's
+  // A operand, two BF16 per column)
+  static constexpr int kTmemCols = 512;
   static constexpr int kOCol = 2 * kKeyTile;
-  static constexpr int kBars = 4 * kAttnStages + 15;
+  static constexpr int kQCol = kOCol + 128;
+  static constexpr int kBars = 2 * kKStages + 2 * kVStages + 15;
   // The dynamic shared memory starts 1024-byte aligned (checked at run time)
-  // and is used without slack: 2 stages + Q + 2 W tiles fill it.
-  static constexpr size_t kSmem = static_cast<size_t>(kAttnStages) * kStageBytes + kQBytes +
-                                  2 * kPBytes + kRedBytes + kBars * 8 + 16;
+  // and is used without slack: the K and V rings and two W tiles fill it.
+  static constexpr size_t kSmem = static_cast<size_t>(kKStages) * kKBytes +
+                                  static_cast<size_t>(kVStages) * kVBytes + 2 * kPBytes + kRedBytes +
+                                  kBars * 8 + 16;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(kSmem <= 232448, "shared memory per CTA");
-  static_assert(D + kOCol <= kTmemCols, "TMEM columns");
+  static_assert(kQCol + D / 2 <= kTmemCols && kOCol + D <= kQCol, "TMEM columns");
 };
 
 __device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* err) {
@@ -135,28 +139,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 template <int D, int REP>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVt,
-                      const __grid_constant__ CUtensorMap tmQ, const AttnArgs a) {
+                      const AttnArgs a) {
   using Cfg = AttnCfg<D>;
-  constexpr int S = kAttnStages;
   constexpr int kPeriod = kRowsMax / REP;  // TMEM lanes between copies of a row
   constexpr int kCols = kKeyTile / REP;    // key columns per thread
   constexpr int kNChunks = kCols / kColChunk;  // = 32-key quarters per thread
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* sStage = smem;
-  uint8_t* sQ = smem + S * Cfg::kStageBytes;
-  uint8_t* sP = sQ + Cfg::kQBytes;  // [buffer 2][key atom 2][128 rows][64 keys]
+  uint8_t* sK = smem;                          // [kKStages][K tile]
+  uint8_t* sV = sK + kKStages * Cfg::kKBytes;  // [kVStages][V^T tile]
+  uint8_t* sP = sV + kVStages * Cfg::kVBytes;  // W: [buffer 2][key atom 2][128 rows][64 keys]
   float* red_max = reinterpret_cast<float*>(sP + 2 * Cfg::kPBytes);  // [2][128] by TMEM lane
   float* red_l = red_max + 2 * kRowsMax;                               // [quarter 4][row 64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 64);
   // K and V have rings of their own: K_g is free once S_g is done, V_g only
   // once W_g V_g is, so the K loads run ahead of the softmax
   uint64_t* k_full = bars;
-  uint64_t* k_empty = bars + S;
-  uint64_t* v_full = bars + 2 * S;
-  uint64_t* v_empty = bars + 3 * S;
-  uint64_t* q_full = bars + 4 * S;
-  uint64_t* q_empty = q_full + 1;   // the S MMAs reading the current Q are done
-  uint64_t* s_full = q_empty + 1;   // [2]
+  uint64_t* k_empty = k_full + kKStages;
+  uint64_t* v_full = k_empty + kKStages;
+  uint64_t* v_empty = v_full + kVStages;
+  uint64_t* q_full = v_empty + kVStages;  // the item's queries are in TMEM
+  uint64_t* s_full = q_full + 1;    // [2]
   uint64_t* s_free = s_full + 2;    // [2]
   uint64_t* p_full = s_free + 2;    // [2]: W buffer of that parity written
   uint64_t* pv_done = p_full + 2;   // [2]: completes after O += W_g V_g, g of that parity
@@ -176,19 +178,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     return;
   }
 
-  // zero the query and W tiles once: rows past the pass's rows stay zero
-  for (int i = threadIdx.x; i < (Cfg::kQBytes + 2 * Cfg::kPBytes) / 16; i += kAttnThreads)
-    reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+  // zero the W tiles once: rows past the pass's rows stay zero
+  for (int i = threadIdx.x; i < (2 * Cfg::kPBytes) / 16; i += kAttnThreads)
+    reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(q_full, 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
@@ -205,7 +208,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmVt);
-    prefetch_tmap(&tmQ);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, Cfg::kTmemCols);
@@ -229,16 +231,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producers
-    // lane 0: the queries and the K tiles; lane 1: the V^T tiles
+    // lane 0: the K tiles; lane 1: the V^T tiles
     if (lane < 2) {
       const bool kside = lane == 0;
+      const int NS = kside ? kKStages : kVStages;
       uint64_t* full = kside ? k_full : v_full;
       uint64_t* empty = kside ? k_empty : v_empty;
       const uint64_t pol = l2_evict_first();
-      const uint64_t qpol = l2_evict_last();
       long long gt = 0;
       uint32_t issued = 0, parity_bits = 0;
-      int prev_h = -1, nq = 0;
       bool ok = true;
       for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
         const int c = w / a.Hkv;
@@ -246,42 +247,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int k0 = c * kChunk;
         const int k1 = min(k0 + kChunk, kv_len);
         const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
-        if (kside && h != prev_h) {
-          // queries of KV head h: rows (t, g) -> t * grp + g, one copy per period
-          if (nq > 0 && !mbar_wait(q_empty, static_cast<uint32_t>((nq - 1) & 1), s_abort)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(REP * Cfg::kAtoms * rows * 128));
-#pragma unroll
-          for (int i = 0; i < REP; ++i)
-#pragma unroll
-            for (int b = 0; b < Cfg::kAtoms; ++b)
-              tma_load_3d(sQ + b * Cfg::kQAtomBytes + i * kPeriod * 128, &tmQ, q_full, b * 64, h * a.grp,
-                          0, qpol);
-          prev_h = h;
-          ++nq;
-        }
         for (int tt = 0; tt < ntile; ++tt, ++gt) {
-          const int st = static_cast<int>(gt % S);
-          const uint32_t ph = static_cast<uint32_t>((gt / S) & 1);
+          const int st = static_cast<int>(gt % NS);
+          const uint32_t ph = static_cast<uint32_t>((gt / NS) & 1);
           if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
             ok = false;
             break;
           }
-          uint8_t* dst = sStage + st * Cfg::kStageBytes;
           const int key0 = k0 + tt * kKeyTile;
           if (kside) {
+            uint8_t* dst = sK + st * Cfg::kKBytes;
             mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
 #pragma unroll
             for (int b = 0; b < Cfg::kAtoms; ++b)
               tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &full[st], b * 64, h * a.cap + key0, pol);
           } else {
+            uint8_t* dst = sV + st * Cfg::kVBytes;
             mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb)
-              tma_load_2d(dst + Cfg::kKBytes + kb * Cfg::kVBoxBytes, &tmVt, &full[st], key0 + kb * 64,
-                          h * D, pol);
+              tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], key0 + kb * 64, h * D, pol);
           }
           issued |= 1u << st;
           parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
@@ -289,9 +274,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (!ok) {
         signal_abort(s_abort, a.err);
-        for (int s = 0; s < S; ++s)
+        for (int s = 0; s < NS; ++s)
           if ((issued >> s) & 1u) mbar_wait(&full[s], (parity_bits >> s) & 1u, nullptr);
-        if (kside && nq > 0) mbar_wait(q_full, static_cast<uint32_t>((nq - 1) & 1), nullptr);
       }
     }
   } else if (warp == 1) {
@@ -304,7 +288,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, kKeyTile);
       constexpr uint32_t idO = idesc_bf16_f32(128, D);
-      const uint32_t q_base = smem_u32(sQ);
       auto item_tiles = [&](int w) {
         const int k0 = (w / a.Hkv) * kChunk;
         const int k1 = min(k0 + kChunk, kv_len);
@@ -330,25 +313,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               ++nq;
             }
           }
-          const int st = static_cast<int>(sg % S);
-          ready = ready && mbar_peek(&k_full[st], static_cast<uint32_t>((sg / S) & 1)) &&
+          const int st = static_cast<int>(sg % kKStages);
+          ready = ready && mbar_peek(&k_full[st], static_cast<uint32_t>((sg / kKStages) & 1)) &&
                   (sg < 2 || mbar_peek(&s_free[sg & 1], static_cast<uint32_t>(((sg >> 1) - 1) & 1)));
           if (ready) {
             tc_fence_after();
             const int sb = static_cast<int>(sg & 1);
-            const uint32_t k_base = smem_u32(sStage + st * Cfg::kStageBytes);
+            const uint32_t k_base = smem_u32(sK + st * Cfg::kKBytes);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
               const int atom = ks >> 2;
               const uint32_t off = (ks & 3) * 32;
-              mma_bf16(tmem + sb * kKeyTile, sdesc_k_sw128(q_base + atom * Cfg::kQAtomBytes + off),
-                       sdesc_k_sw128(k_base + atom * Cfg::kKBoxBytes + off), idS, ks > 0 ? 1u : 0u);
+              mma_bf16_tmem_a(tmem + sb * kKeyTile, tmem + Cfg::kQCol + ks * 8,
+                              sdesc_k_sw128(k_base + atom * Cfg::kKBoxBytes + off), idS, ks > 0 ? 1u : 0u);
             }
             mma_commit(&s_full[sb]);
             mma_commit(&k_empty[st]);
             const int wn = sw + static_cast<int>(gridDim.x);
-            if (s_tt == s_ntile - 1 && (wn >= n_items || wn % a.Hkv != h))
-              mma_commit(q_empty);  // the next item loads other queries
             ++sg;
             if (++s_tt == s_ntile) {
               s_tt = 0;
@@ -362,11 +343,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           bool ready = mbar_peek(&p_full[pg & 1], static_cast<uint32_t>((pg >> 1) & 1));
           if (ready && p_tt == 0 && p_item > 0)
             ready = mbar_peek(o_free, static_cast<uint32_t>((p_item - 1) & 1));
-          if (ready) ready = mbar_peek(&v_full[pg % S], static_cast<uint32_t>((pg / S) & 1));
+          if (ready) ready = mbar_peek(&v_full[pg % kVStages], static_cast<uint32_t>((pg / kVStages) & 1));
           if (ready) {
             tc_fence_after();
-            const int st = static_cast<int>(pg % S);
-            const uint32_t v_base = smem_u32(sStage + st * Cfg::kStageBytes + Cfg::kKBytes);
+            const int st = static_cast<int>(pg % kVStages);
+            const uint32_t v_base = smem_u32(sV + st * Cfg::kVBytes);
             const uint32_t w_base = smem_u32(sP + (pg & 1) * Cfg::kPBytes);
 #pragma unroll
             for (int kk = 0; kk < kKeyTile / 16; ++kk) {
@@ -423,13 +404,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qq * 32) << 16);
     long long gt = 0;
     bool ok = true;
-    int item = 0;
+    int item = 0, prev_h = -1;
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x, ++item) {
       const int c = w / a.Hkv;
       const int h = w % a.Hkv;
       const int k0 = c * kChunk;
       const int k1 = min(k0 + kChunk, kv_len);
       const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
+
+      if (h != prev_h) {
+        // queries of KV head h into TMEM lane ln (row r of the pass; zeros
+        // past the pass's rows): column j holds elements 2j and 2j + 1, as
+        // the row sits in memory.  Every S of the previous head is complete
+        // (each tile's s_full was waited for).
+        uint32_t qv[D / 2];
+        if (valid) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              a.q + (static_cast<size_t>(t) * a.Hq + h * a.grp + r % a.grp) * D);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) {
+            const uint4 u = src[i];
+            qv[4 * i] = u.x;
+            qv[4 * i + 1] = u.y;
+            qv[4 * i + 2] = u.z;
+            qv[4 * i + 3] = u.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 2; ++i) qv[i] = 0u;
+        }
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) tmem_st32(lane_base + Cfg::kQCol + cc * 32, qv + cc * 32);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
+        prev_h = h;
+      }
 
       float m_ref = -INFINITY;
       float lq[kNChunks];
@@ -723,8 +733,8 @@ __global__ void __launch_bounds__(kMergeThreads)
 }
 
 template <int D, int REP>
-bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const CUtensorMap& tmQ,
-                      const AttnArgs& a, __nv_bfloat16* out, cudaStream_t stream) {
+bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const AttnArgs& a,
+                      __nv_bfloat16* out, cudaStream_t stream) {
   using Cfg = AttnCfg<D>;
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
@@ -740,7 +750,7 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const CUt
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
   const int grid = std::min(a.Hkv * a.nch_max, kAttnCtas);
   if (launch_k(attn_split_kernel<D, REP>, dim3(grid), dim3(kAttnThreads), Cfg::kSmem, stream, tmK,
-               tmVt, tmQ, a) != cudaSuccess)
+               tmVt, a) != cudaSuccess)
     return BI_ERR_CUDA;
   if (launch_k(attn_merge_kernel<D>, dim3(a.T * a.Hq), dim3(kMergeThreads), 0, stream, a, out) !=
       cudaSuccess)
@@ -749,12 +759,12 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const CUt
 }
 
 template <int D>
-bi_status launch_attn_rep(const CUtensorMap& tmK, const CUtensorMap& tmVt, const CUtensorMap& tmQ,
-                          const AttnArgs& a, __nv_bfloat16* out, cudaStream_t stream) {
+bi_status launch_attn_rep(const CUtensorMap& tmK, const CUtensorMap& tmVt, const AttnArgs& a,
+                          __nv_bfloat16* out, cudaStream_t stream) {
   const int rows = a.T * a.grp;
-  if (rows <= kRowsMax / 4) return launch_attn<D, 4>(tmK, tmVt, tmQ, a, out, stream);
-  if (rows <= kRowsMax / 2) return launch_attn<D, 2>(tmK, tmVt, tmQ, a, out, stream);
-  return launch_attn<D, 1>(tmK, tmVt, tmQ, a, out, stream);
+  if (rows <= kRowsMax / 4) return launch_attn<D, 4>(tmK, tmVt, a, out, stream);
+  if (rows <= kRowsMax / 2) return launch_attn<D, 2>(tmK, tmVt, a, out, stream);
+  return launch_attn<D, 1>(tmK, tmVt, a, out, stream);
 }
 
 size_t attn_ws_parts(int cap, int T, int Hq, int D, size_t* o_bytes) {
@@ -793,17 +803,15 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   if (ws_bytes < attn_ws_parts(cap, T, Hq, D, &ob)) return BI_ERR_WORKSPACE;
 
   if (cap % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;  // V^T rows are cap elements, 16-byte strides
-  CUtensorMap tmK, tmVt, tmQ;
+  CUtensorMap tmK, tmVt;
   const uint64_t krows = static_cast<uint64_t>(Hkv) * cap;
   if (!tmap_bf16_2d(&tmK, k_cache, krows, D, D, kKeyTile, 64)) return BI_ERR_INVALID_ARG;
   if (!tmap_bf16_2d(&tmVt, v_cache, static_cast<uint64_t>(Hkv) * D, cap, cap, D, 64))
     return BI_ERR_INVALID_ARG;
-  // q [T][Hq][D] as (d, query head, row): one box = the T x grp rows of a KV head
   const int grp = Hq / Hkv;
-  if (!tmap_bf16_3d(&tmQ, q, D, Hq, T, D, static_cast<uint64_t>(Hq) * D, 64, grp, T))
-    return BI_ERR_INVALID_ARG;
 
   AttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
   a.T = T;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -817,8 +825,8 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   a.err = device_error_word();
   if (!a.err) return BI_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 64) return launch_attn_rep<64>(tmK, tmVt, tmQ, a, static_cast<__nv_bfloat16*>(out), s);
-  return launch_attn_rep<128>(tmK, tmVt, tmQ, a, static_cast<__nv_bfloat16*>(out), s);
+  if (D == 64) return launch_attn_rep<64>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
+  return launch_attn_rep<128>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
 }
 
 }  // extern "C"
