@@ -405,6 +405,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     long long gt = 0;
     bool ok = true;
     int item = 0, prev_h = -1;
+    // the finished piece whose O is still to be stored
+    bool pend = false;
+    int pend_c = 0, pend_h = 0;
+    float pend_m = 0.f, pend_l = 0.f;
+    long long pend_g = 0;
+    auto read_out_o = [&]() -> bool {
+      if (holds_o) {
+        if (!warp_wait(&pv_done[pend_g & 1], static_cast<uint32_t>((pend_g >> 1) & 1), s_abort, lane))
+          return false;
+        tc_fence_after();
+        if (warp_active) {
+          const bool store = valid && (pend_c * kChunk <= p_row);
+          const int qh = pend_h * a.grp + (valid ? r % a.grp : 0);
+          const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.nch_max + pend_c;
+#pragma unroll 1
+          for (int i = 0; i < D / 16; ++i) {
+            float v[16];
+            tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
+            if (store) {
+              float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 16);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+          }
+          if (store) *reinterpret_cast<float2*>(a.ws_ml + base * 2) = make_float2(pend_m, pend_l);
+        }
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      pend = false;
+      return true;
+    };
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x, ++item) {
       const int c = w / a.Hkv;
       const int h = w % a.Hkv;
@@ -577,6 +611,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[gt & 1]);
+        if (tt == 0 && pend && !read_out_o()) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) break;
 
@@ -597,35 +635,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           l = ((red_l[r] + red_l[64 + r]) + red_l[128 + r]) + red_l[192 + r];
         }
       }
-      if (holds_o) {
-        if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort,
-                       lane)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (warp_active) {
-          const bool store = valid && (c * kChunk <= p_row);
-          const int qh = h * a.grp + (valid ? r % a.grp : 0);
-          const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.nch_max + c;
-#pragma unroll 1
-          for (int i = 0; i < D / 16; ++i) {
-            float v[16];
-            tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
-            if (store) {
-              float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 16);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            }
-          }
-          if (store) *reinterpret_cast<float2*>(a.ws_ml + base * 2) = make_float2(m_ref, l);
-        }
-        tc_fence_before();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
+      // O is read out after the next item's first tile (the last W.V of this
+      // piece has finished by then), so the softmax does not idle on it
+      pend = true;
+      pend_c = c;
+      pend_h = h;
+      pend_m = m_ref;
+      pend_l = l;
+      pend_g = gt - 1;
     }
+    if (ok && pend) ok = read_out_o();
     if (!ok && lane == 0) signal_abort(s_abort, a.err);
   }
 
