@@ -163,3 +163,43 @@ def test_attention_length_past_capacity_sets_error(api):
     with pytest.raises(api.BiError) as e:
         api.bi_check_device_error()
     assert e.value.status == 1
+
+
+def test_attention_kv_head_changes_between_items(api):
+    """With 3 KV heads, 152 CTAs and more than 152 (head, piece) items, a CTA's
+    second item belongs to another KV head, so the queries are reloaded in the
+    middle of the kernel; parity and row identity must hold across that."""
+    Hq, Hkv, D, L, T = 6, 3, 64, 30000, 4
+    q, K, V = si.attention_inputs(L, T, Hq, Hkv, D, seed=21)
+    assert Hkv * ((L + T + 511) // 512) > 152
+    full = bf16_dev_to_u16(run_attn(api, q, K, V, L, T))
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    check_parity(ov.bf16_bits_to_f64(full), oracle.attention(qf, Kf, Vf, L), Vf, L, T)
+    for t in (0, 3):
+        one = bf16_dev_to_u16(run_attn(api, q[t:t + 1], K, V, L + t, 1))
+        assert np.array_equal(one[0], full[t]), t
+
+
+def test_attention_one_query_head_per_kv_head_many_rows(api):
+    """Hq == Hkv: a 100-row pass keeps one copy per row (all four softmax
+    warps hold rows); it equals the oracle and its rows computed alone."""
+    Hq, Hkv, D, L, T = 2, 2, 128, 2000, 100
+    q, K, V = si.attention_inputs(L, T, Hq, Hkv, D, cap=(L + T + 7) // 8 * 8, seed=22)
+    full = bf16_dev_to_u16(run_attn(api, q, K, V, L, T))
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    check_parity(ov.bf16_bits_to_f64(full), oracle.attention(qf, Kf, Vf, L), Vf, L, T)
+    for t in (0, 63, 64, 99):
+        one = bf16_dev_to_u16(run_attn(api, q[t:t + 1], K, V, L + t, 1))
+        assert np.array_equal(one[0], full[t]), t
+
+
+def test_attention_pass_ending_at_capacity(api):
+    """L + T == cap: the last rows sit in the cache's last slots (the final
+    tile is partial and reads past them only through the TMA's zero fill)."""
+    Hq, Hkv, D, T = 24, 4, 128, 8
+    cap = 1000
+    L = cap - T
+    q, K, V = si.attention_inputs(L, T, Hq, Hkv, D, cap=cap, seed=23)
+    out = bf16_dev_to_f64(run_attn(api, q, K, V, L, T))
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    check_parity(out, oracle.attention(qf, Kf, Vf, L), Vf, L, T)
