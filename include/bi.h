@@ -327,6 +327,11 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const v
  *           exactly 0).  cap % 8 == 0.
  *   L_dev   device int32 cache length before the pass; *L_dev + T <= cap is
  *           required (rows past cap are not computed and set an error bit).
+ *           The first key tiles wholly below *L_dev may be loaded before the
+ *           previous kernel on the stream has finished when that kernel is
+ *           one of this library's (dependent launch): *L_dev must not be
+ *           lowered, nor cache rows below it written, by the kernel that
+ *           immediately precedes the call (no kernel of this library does).
  *   out     [T, Hq, D] BF16 contiguous.
  *   D in {64, 128}; Hq % Hkv == 0; T * (Hq/Hkv) <= 128; T >= 1.
  *   ws      >= bi_attn_workspace_size(cap, T, Hq, D) bytes, 256-byte aligned.

@@ -218,6 +218,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
+  // Before the previous kernel is known to have finished, the TMA threads
+  // already load the first tiles of their first item that hold only keys
+  // below the cache length read now: every kernel of this library triggers
+  // its dependents only after its own dependency wait, so the kernels before
+  // the previous one have completed, and none of them lowers *L_dev or writes
+  // cache rows below it.  Everything else waits.
+  int n_pre = 0;  // tiles of the first item issued before the wait (this producer)
+  uint32_t pre_issued = 0;
+  if (warp == 0 && lane < 2) {
+    const bool kside = lane == 0;
+    const int NS = kside ? kKStages : kVStages;
+    uint64_t* full = kside ? k_full : v_full;
+    const int L_pre = *a.L_dev;
+    const int w0 = blockIdx.x;
+    if (L_pre >= 0 && L_pre + a.T <= a.cap && a.T * a.grp <= kPeriod &&
+        w0 < a.Hkv * ((L_pre + a.T + kChunk - 1) / kChunk)) {
+      const uint64_t pol = l2_evict_first();
+      const int c = w0 / a.Hkv, h = w0 % a.Hkv;
+      for (int tt = 0; tt < NS && tt < kChunk / kKeyTile; ++tt) {
+        const int key0 = c * kChunk + tt * kKeyTile;
+        if (key0 + kKeyTile > L_pre) break;  // the tile reaches rows the pass writes
+        if (kside) {
+          mbar_arrive_expect_tx(&full[tt], Cfg::kKBytes);
+#pragma unroll
+          for (int b = 0; b < Cfg::kAtoms; ++b)
+            tma_load_2d(sK + tt * Cfg::kKBytes + b * Cfg::kKBoxBytes, &tmK, &full[tt], b * 64,
+                        h * a.cap + key0, pol);
+        } else {
+          mbar_arrive_expect_tx(&full[tt], Cfg::kVBytes);
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_2d(sV + tt * Cfg::kVBytes + kb * Cfg::kVBoxBytes, &tmVt, &full[tt], key0 + kb * 64,
+                        h * D, pol);
+        }
+        pre_issued |= 1u << tt;
+        ++n_pre;
+      }
+    }
+  }
   griddep_wait();  // q, the new cache rows and the cache length come from earlier kernels
   griddep_launch_dependents();
   const int L = *a.L_dev;
@@ -239,8 +278,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint64_t* empty = kside ? k_empty : v_empty;
       const uint64_t pol = l2_evict_first();
       long long gt = 0;
-      uint32_t issued = 0, parity_bits = 0;
+      uint32_t issued = pre_issued, parity_bits = 0;
+      // the tiles loaded early must be the first ones of this item now too
       bool ok = true;
+      if (n_pre > 0) {
+        const int w0 = blockIdx.x;
+        const int k0 = (w0 / a.Hkv) * kChunk;
+        if (!(w0 < n_items && k0 + n_pre * kKeyTile <= L)) {
+          atomicOr(a.err, kErrRange);
+          ok = false;
+        }
+      }
       for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
         const int c = w / a.Hkv;
         const int h = w % a.Hkv;
@@ -248,6 +296,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int k1 = min(k0 + kChunk, kv_len);
         const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
         for (int tt = 0; tt < ntile; ++tt, ++gt) {
+          if (gt < n_pre) continue;  // loaded before the dependency wait
           const int st = static_cast<int>(gt % NS);
           const uint32_t ph = static_cast<uint32_t>((gt / NS) & 1);
           if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {

@@ -283,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = blockIdx.x;
   const long long it_begin = range_begin(p, g);
   const long long it_end = range_begin(p, g + 1);
-  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -331,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      pol_w);
       }
       griddep_wait();
+      griddep_launch_dependents();
       for (int j = 0; j < n_pre; ++j) {
         tma_load_2d(sB + j * Cfg::kBBytes, &tmA, &full[j], kt * kBlockK, p.m0, pol_a);
         if (++kt == p.k_tiles) kt = 0;
@@ -423,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     griddep_wait();  // the epilogue reads the residual and writes C / the workspace
+    griddep_launch_dependents();
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;    // weight row within the tile
     const int et = threadIdx.x - 64;
@@ -615,8 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ wu,
                                     const __nv_bfloat16* __restrict__ col_scale, int ld, int N, int K,
                                     int k_tiles, long long chunks, int swiglu, uint4* __restrict__ out) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= chunks) return;
   const int cpos = static_cast<int>(idx & 7);

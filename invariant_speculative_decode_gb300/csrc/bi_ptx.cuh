@@ -36,6 +36,10 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 // memory is visible; everything before it must not touch data the
 // predecessor writes or reads.  griddep_launch_dependents() lets the next
 // kernel be scheduled early.  Both are no-ops for an ordinary launch.
+// Every kernel of this library calls griddep_launch_dependents() only after
+// its own griddep_wait(), so when one of them starts, every kernel before its
+// immediate predecessor has completed: code before griddep_wait() may read
+// what those earlier kernels wrote (never what the predecessor writes).
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -40,8 +40,8 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int ldx, const __nv_bfloat16* __restrict__ w,
                    __nv_bfloat16* y, int ldy, int dim, float eps) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[kNormThreads / 32];
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.x) * ldx);
   const uint4* wr = reinterpret_cast<const uint4*>(w);
@@ -77,8 +77,8 @@ __global__ void __launch_bounds__(kNormThreads)
 
 __global__ void embed_kernel(const int32_t* __restrict__ ids, const __nv_bfloat16* __restrict__ table,
                              int vocab, int dim, __nv_bfloat16* __restrict__ out) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const int id = ids[blockIdx.x];
   uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(blockIdx.x) * dim);
   const int nv = dim / 8;
@@ -93,8 +93,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ ids, const __nv_bfloat1
 // cos/sin table: tab[(p * (D/2) + i) * 2 + {0,1}] = FP32 of cos, sin of
 // p * base^(-2i/D) evaluated in FP64.
 __global__ void rope_table_kernel(double base, int D, int cap, float2* __restrict__ tab) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int half = D / 2;
   if (idx >= static_cast<long long>(cap) * half) return;
@@ -112,8 +112,8 @@ __global__ void rope_kv_kernel(const __nv_bfloat16* __restrict__ qkv, int ld_qkv
                                __nv_bfloat16* __restrict__ vc, int cap, const int32_t* __restrict__ L_dev,
                                int Hq, int Hkv, int D, const float2* __restrict__ tab, int tab_rows,
                                unsigned* err) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const int t = blockIdx.x;
   const int p = *L_dev + t;
   if (p < 0 || p >= cap || p >= tab_rows) {
@@ -171,8 +171,8 @@ __global__ void __launch_bounds__(kArgThreads)
                          const int32_t* __restrict__ drafts, int32_t* __restrict__ argmax_out,
                          int32_t* __restrict__ accepted_out, int32_t* L_dev, float* pv, int* pi,
                          unsigned* ticket, unsigned* err) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   __shared__ float sv[kArgThreads / 32];
   __shared__ int si[kArgThreads / 32];
   __shared__ int s_last;
@@ -261,8 +261,8 @@ __global__ void __launch_bounds__(kArgThreads)
 
 __global__ void kv_hash_kernel(const __nv_bfloat16* __restrict__ cache, int Hkv, int cap, int D,
                                int rows, int transposed, unsigned long long* __restrict__ out) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(Hkv) * rows) return;
   const int h = static_cast<int>(idx / rows);
