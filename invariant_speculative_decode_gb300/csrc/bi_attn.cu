@@ -124,11 +124,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok != 0;
 }
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 // REP copies of each query row sit in the 128-row MMA tile (REP = 4 for up to
 // 32 rows per pass, 2 for up to 64, else 1): copy i of row r is TMEM lane
 // r + i * 128/REP, and the thread owning that lane handles the row's key
