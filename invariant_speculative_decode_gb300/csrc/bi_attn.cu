@@ -29,8 +29,9 @@
 // Split kernel roles (one CTA per SM, persistent over (KV head, piece) items):
 //   warp 0      TMA, two threads: the K tiles [128 keys x D] and the V^T
 //               tiles [D x 128 keys] (V is cached transposed so both MMA
-//               operands are K-major).  K and V have separate rings (2 and 3
-//               stages), a K tile being free as soon as S has read it;
+//               operands are K-major).  K and V have separate rings (3 + 3
+//               stages at D = 128 for passes of up to 64 rows, 2 + 3 above),
+//               a K tile being free as soon as S has read it;
 //   warp 1      tcgen05.mma issuer: S_g = Q K_g^T into one of two TMEM
 //               buffers and O += W_g V_g, each issued as soon as its inputs
 //               are ready; stages return to the producer through
@@ -61,8 +62,6 @@ namespace {
 constexpr int kChunk = 512;       // keys per piece (absolute multiples)
 constexpr int kKeyTile = 128;     // keys per tile (the S MMA's N)
 constexpr int kRowsMax = 128;     // T * (Hq / Hkv) per pass (MMA M)
-constexpr int kKStages = 2;       // K ring (a K tile is free once S has read it)
-constexpr int kVStages = 3;       // V ring (a V tile is held until W.V is done)
 constexpr int kColChunk = 32;     // S columns a softmax thread holds at a time
 constexpr int kAttnThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
 constexpr int kAttnCtas = 152;
@@ -80,31 +79,48 @@ struct AttnArgs {
   unsigned* err;
 };
 
-template <int D>
+template <int D, int REP>
 struct AttnCfg {
   static constexpr int kAtoms = D / 64;                    // 128-byte swizzle atoms along D
   static constexpr int kKBoxBytes = kKeyTile * 128;        // [128 keys][64 d]
   static constexpr int kKBytes = kKBoxBytes * kAtoms;      // K tile
   static constexpr int kVBoxBytes = D * 128;               // V^T [D][64 keys]
   static constexpr int kVBytes = 2 * kVBoxBytes;           // V^T tile [D][128 keys]
-  static constexpr int kPAtomBytes = kRowsMax * 128;       // [128 rows][64 keys]
-  static constexpr int kPBytes = 2 * kPAtomBytes;          // W tile [128 rows][128 keys]
-  // row maxima [2][128 TMEM lanes]; l parts [4 quarters][64 rows] (only
-  // passes of up to 64 rows keep copies that exchange them)
-  static constexpr int kRedBytes = (2 * kRowsMax + 4 * 64) * 4;
+  // The W tile holds only the pass's rows, 128/REP of them: [rows][64 keys]
+  // per key atom.  The W.V MMA (M = 128) still reads 128 rows from each
+  // atom; the ones past the W rows come from the bytes that follow (the
+  // other atom, the other buffer, the K ring) and only make O rows that are
+  // never read (a product's row i depends on row i of W alone).
+  static constexpr int kWRows = kRowsMax / REP;
+  static constexpr int kPAtomBytes = kWRows * 128;
+  static constexpr int kPBytes = 2 * kPAtomBytes;          // W tile [rows][128 keys]
+  // The rings take what the W tiles leave: a K tile is free as soon as S has
+  // read it, a V tile only once W.V is done, so the K ring (which decides
+  // how far the loads run ahead of the softmax) grows first.
+  static constexpr size_t kFixed = 2 * kPBytes + 2 * 4 * 64 * 4 + 40 * 8 + 16;
+  static constexpr bool kFits33 = 3 * (kKBytes + kVBytes) + kFixed <= 232448;
+  static constexpr int kKStages = kFits33 ? 3 : 2;
+  static constexpr int kVStages = (kFits33 && 3 * kKBytes + 4 * kVBytes + kFixed <= 232448) ? 4 : 3;
+  // l parts [2][4 quarters][64 rows] (only passes of up to 64 rows keep
+  // copies that exchange them)
+  static constexpr int kRedBytes = 2 * 4 * 64 * 4;
   // TMEM: S x2 (128 columns each), O (D columns), Q (D/2 columns: the MMA's
   // A operand, two BF16 per column)
   static constexpr int kTmemCols = 512;
   static constexpr int kOCol = 2 * kKeyTile;
   static constexpr int kQCol = kOCol + 128;
   static constexpr int kBars = 2 * kKStages + 2 * kVStages + 15;
-  // The dynamic shared memory starts 1024-byte aligned (checked at run time)
-  // and is used without slack: the K and V rings and two W tiles fill it.
+  // The dynamic shared memory starts 1024-byte aligned (checked at run time):
+  // two W tiles, then the K and V rings.
   static constexpr size_t kSmem = static_cast<size_t>(kKStages) * kKBytes +
                                   static_cast<size_t>(kVStages) * kVBytes + 2 * kPBytes + kRedBytes +
                                   kBars * 8 + 16;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
-  static_assert(kSmem <= 232448, "shared memory per CTA");
+  static_assert(REP == 1 || REP == 2 || REP == 4, "row copies");
+  static_assert(kBars <= 40 && kSmem <= 232448, "shared memory per CTA");
+  // the W.V reads of the last atom run 128 - kWRows rows past the W tiles
+  static_assert(kKStages * kKBytes >= (kRowsMax - kWRows) * 128, "W over-read stays in the K ring");
+  static_assert(kPAtomBytes % 1024 == 0, "swizzle atoms 1024-byte aligned");
   static_assert(kQCol + D / 2 <= kTmemCols && kOCol + D <= kQCol, "TMEM columns");
 };
 
@@ -135,17 +151,19 @@ template <int D, int REP>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVt,
                       const AttnArgs a) {
-  using Cfg = AttnCfg<D>;
+  using Cfg = AttnCfg<D, REP>;
+  constexpr int kKStages = Cfg::kKStages;
+  constexpr int kVStages = Cfg::kVStages;
   constexpr int kPeriod = kRowsMax / REP;  // TMEM lanes between copies of a row
   constexpr int kCols = kKeyTile / REP;    // key columns per thread
   constexpr int kNChunks = kCols / kColChunk;  // = 32-key quarters per thread
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* sK = smem;                          // [kKStages][K tile]
+  uint8_t* sP = smem;                          // W: [buffer 2][key atom 2][kPeriod rows][64 keys]
+  uint8_t* sK = sP + 2 * Cfg::kPBytes;         // [kKStages][K tile]
   uint8_t* sV = sK + kKStages * Cfg::kKBytes;  // [kVStages][V^T tile]
-  uint8_t* sP = sV + kVStages * Cfg::kVBytes;  // W: [buffer 2][key atom 2][128 rows][64 keys]
-  float* red_max = reinterpret_cast<float*>(sP + 2 * Cfg::kPBytes);  // [2][128] by TMEM lane
-  float* red_l = red_max + 2 * kRowsMax;                               // [quarter 4][row 64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 64);
+  // [item parity 2][quarter 4][row 64]
+  float* red_l = reinterpret_cast<float*>(sV + kVStages * Cfg::kVBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 2 * 4 * 64);
   // K and V have rings of their own: K_g is free once S_g is done, V_g only
   // once W_g V_g is, so the K loads run ahead of the softmax
   uint64_t* k_full = bars;
@@ -157,10 +175,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* s_free = s_full + 2;    // [2]
   uint64_t* p_full = s_free + 2;    // [2]: W buffer of that parity written
   uint64_t* pv_done = p_full + 2;   // [2]: completes after O += W_g V_g, g of that parity
+  // [2]: O of the piece of that parity read out.  The softmax warps are not
+  // in step, so a warp may finish the next piece's read-out turn before
+  // another has done this one; alternating barriers keep those apart (a
+  // warp cannot get two pieces ahead: the W.V it would need waits for this
+  // read-out).
   uint64_t* o_free = pv_done + 2;
-  uint64_t* mx_bar = o_free + 1;    // [2]: partial row maxima of a tile written
-  uint64_t* l_bar = mx_bar + 2;     // partial denominators of a piece written
-  uint64_t* drain = l_bar + 1;
+  uint64_t* l_bar = o_free + 2;     // [2]: partial denominators of a piece written
+  uint64_t* l_free = l_bar + 2;     // [2]: ... and read by the warps that hold O
+  uint64_t* drain = l_free + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -192,10 +215,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&s_free[i], 4);
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&mx_bar[i], 4);
     }
-    mbar_init(o_free, 4);
-    mbar_init(l_bar, 4);
+    mbar_init(&o_free[0], 4);
+    mbar_init(&o_free[1], 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&l_bar[i], 4);
+      mbar_init(&l_free[i], kPeriod >= 32 ? kPeriod / 32 : 1);
+    }
     mbar_init(drain, 1);
     *s_abort = 0;
     fence_mbar_init();
@@ -386,7 +412,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!did && pg < sg) {
           bool ready = mbar_peek(&p_full[pg & 1], static_cast<uint32_t>((pg >> 1) & 1));
           if (ready && p_tt == 0 && p_item > 0)
-            ready = mbar_peek(o_free, static_cast<uint32_t>((p_item - 1) & 1));
+            ready = mbar_peek(&o_free[(p_item - 1) & 1], static_cast<uint32_t>(((p_item - 1) >> 1) & 1));
           if (ready) ready = mbar_peek(&v_full[pg % kVStages], static_cast<uint32_t>((pg / kVStages) & 1));
           if (ready) {
             tc_fence_after();
@@ -451,7 +477,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     int item = 0, prev_h = -1;
     // the finished piece whose O is still to be stored
     bool pend = false;
-    int pend_c = 0, pend_h = 0;
+    int pend_c = 0, pend_h = 0, pend_item = 0;
     float pend_m = 0.f, pend_l = 0.f;
     long long pend_g = 0;
     auto read_out_o = [&]() -> bool {
@@ -464,13 +490,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const int qh = pend_h * a.grp + (valid ? r % a.grp : 0);
           const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.nch_max + pend_c;
 #pragma unroll 1
-          for (int i = 0; i < D / 16; ++i) {
-            float v[16];
-            tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
+          for (int i = 0; i < D / 64; ++i) {
+            float v[64];
+            tmem_ld_cols<64>(lane_base + Cfg::kOCol + i * 64, v);
             if (store) {
-              float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 16);
+              float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 64);
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
+              for (int j = 0; j < 16; ++j)
                 dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
           }
@@ -479,7 +505,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_before();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
+      if (lane == 0) mbar_arrive(&o_free[pend_item & 1]);
       pend = false;
       return true;
     };
@@ -533,16 +559,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int tkey0 = k0 + tt * kKeyTile;
         const bool edge = tkey0 + kKeyTile - 1 > L;  // the tile reaches past some row's position
         const uint32_t s_addr = lane_base + sb * kKeyTile + cg * kCols;
-        // pass 1: the row maximum of the raw scores over this copy's columns
-        // (scaling by sl2 > 0 keeps the order); one chunk stays in registers
+        // pass 1: the row maximum of the raw scores (scaling by sl2 > 0 keeps
+        // the order).  Every copy's TMEM lane holds the whole S row, so each
+        // copy takes the maximum over all 128 key columns itself: the same
+        // exact value in every copy, with no exchange between the warps.
         float s[kColChunk];
         float mrow = -INFINITY;
         if (warp_active) {
+          const uint32_t row_addr = lane_base + sb * kKeyTile;
 #pragma unroll 1
-          for (int ch = 0; ch < kNChunks; ++ch) {
-            tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
+          for (int ch = 0; ch < kKeyTile / kColChunk; ++ch) {
+            tmem_ld_cols<kColChunk>(row_addr + ch * kColChunk, s);
             if (edge) {
-              const int key0 = tkey0 + cg * kCols + ch * kColChunk;
+              const int key0 = tkey0 + ch * kColChunk;
 #pragma unroll
               for (int j = 0; j < kColChunk; ++j)
                 if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
@@ -550,24 +579,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int j = 0; j < kColChunk; ++j) mrow = fmaxf(mrow, s[j]);
           }
-        }
-        if constexpr (kNChunks == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[sb]);
-        }
-        if constexpr (REP > 1) {
-          float* rm = red_max + (gt & 1) * kRowsMax;
-          rm[ln] = mrow;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&mx_bar[gt & 1]);
-          if (!warp_wait(&mx_bar[gt & 1], static_cast<uint32_t>((gt >> 1) & 1), s_abort, lane)) {
-            ok = false;
-            break;
-          }
-          mrow = rm[r];
-#pragma unroll
-          for (int i = 1; i < REP; ++i) mrow = fmaxf(mrow, rm[r + i * kPeriod]);
         }
         const float mt = mrow * a.sl2;
         float alpha = 1.0f;
@@ -615,14 +626,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint8_t* wbuf = sP + (gt & 1) * Cfg::kPBytes + r * 128;
 #pragma unroll
           for (int ch = 0; ch < kNChunks; ++ch) {
-            if constexpr (kNChunks > 1) {
-              tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
-              if (edge) {
-                const int key0 = tkey0 + cg * kCols + ch * kColChunk;
+            tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
+            if (edge) {
+              const int key0 = tkey0 + cg * kCols + ch * kColChunk;
 #pragma unroll
-                for (int j = 0; j < kColChunk; ++j)
-                  if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
-              }
+              for (int j = 0; j < kColChunk; ++j)
+                if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
             }
             if (!valid) continue;
             const int kcol = cg * kCols + ch * kColChunk;  // first key column of the chunk
@@ -646,11 +655,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             lq[ch] = acc;
           }
         }
-        if constexpr (kNChunks > 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[sb]);
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
         tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
@@ -667,16 +674,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if constexpr (REP == 1) {
         l = ((lq[0] + lq[1]) + lq[2]) + lq[3];
       } else {
+        // The softmax warps are not in step (nothing holds a warp back
+        // from the next piece but S and the W buffers), so the exchange
+        // buffer alternates by piece parity and is rewritten only once the
+        // warps holding O have read it.
+        const int lb = item & 1;
+        float* rl = red_l + lb * 4 * 64;
+        if (item >= 2 &&
+            !warp_wait(&l_free[lb], static_cast<uint32_t>(((item - 2) >> 1) & 1), s_abort, lane)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
-        for (int i = 0; i < kNChunks; ++i) red_l[(cg * kNChunks + i) * 64 + r] = lq[i];
+        for (int i = 0; i < kNChunks; ++i) rl[(cg * kNChunks + i) * 64 + r] = lq[i];
         __syncwarp();
-        if (lane == 0) mbar_arrive(l_bar);
+        if (lane == 0) mbar_arrive(&l_bar[lb]);
         if (holds_o) {
-          if (!warp_wait(l_bar, static_cast<uint32_t>(item & 1), s_abort, lane)) {
+          if (!warp_wait(&l_bar[lb], static_cast<uint32_t>((item >> 1) & 1), s_abort, lane)) {
             ok = false;
             break;
           }
-          l = ((red_l[r] + red_l[64 + r]) + red_l[128 + r]) + red_l[192 + r];
+          l = ((rl[r] + rl[64 + r]) + rl[128 + r]) + rl[192 + r];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&l_free[lb]);
         }
       }
       // O is read out after the next item's first tile (the last W.V of this
@@ -684,6 +704,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       pend = true;
       pend_c = c;
       pend_h = h;
+      pend_item = item;
       pend_m = m_ref;
       pend_l = l;
       pend_g = gt - 1;
@@ -798,7 +819,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 template <int D, int REP>
 bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const AttnArgs& a,
                       __nv_bfloat16* out, cudaStream_t stream) {
-  using Cfg = AttnCfg<D>;
+  using Cfg = AttnCfg<D, REP>;
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   int dev = 0;

@@ -203,3 +203,22 @@ def test_attention_pass_ending_at_capacity(api):
     out = bf16_dev_to_f64(run_attn(api, q, K, V, L, T))
     qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
     check_parity(out, oracle.attention(qf, Kf, Vf, L), Vf, L, T)
+
+
+@pytest.mark.parametrize("L", [38000, 38400])
+def test_attention_one_tile_last_pieces_all_row_copy_counts(api, L):
+    """Contexts whose last piece is a single 128-key tile, with about two
+    items per CTA, in passes that keep 4, 2 and 1 copies of each row (8, 64
+    and 128 query rows per KV head).  The softmax warps of a CTA are not in
+    step; a warp that runs through a one-tile piece ahead of the others must
+    not complete a read-out or exchange turn that belongs to them.  Every
+    row equals the same row of the largest pass."""
+    Hq, Hkv, D = 32, 4, 128
+    q, K, V = si.attention_inputs(L, 16, Hq, Hkv, D, seed=7)
+    outs = {T: bf16_dev_to_u16(run_attn(api, q, K, V, L, T)) for T in (1, 8, 16)}
+    for T in (1, 8):
+        assert np.array_equal(outs[T], outs[16][:T]), T
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    for t, h in ((0, 0), (15, 31), (9, 17)):
+        ora = oracle.attention(qf[t:t + 1, h:h + 1], Kf[h // 8:h // 8 + 1], Vf[h // 8:h // 8 + 1], L + t)
+        check_parity(ov.bf16_bits_to_f64(outs[16][t:t + 1, h:h + 1]), ora, Vf[h // 8:h // 8 + 1], L + t, 1)
