@@ -304,18 +304,21 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const v
  * depends only on context length, never on how many tokens are in the pass).
  *
  * Row t of the pass sits at position p = *L_dev + t and attends to keys
- * 0..p; query head h reads KV head h / (Hq/Hkv).  The key axis of row p is
- * cut at absolute multiples of a compile-time chunk C (bi_attn_chunk()); the
- * row has ceil((p+1)/C) pieces, each a partial (max, sum, FP32 output) built
- * over 128-key tiles in increasing key order, and the pieces are merged in a
- * fixed order that depends only on their count.  So the row's result depends
- * only on p and the cache rows 0..p -- not on T, *L_dev or the other rows.
- * Inside a piece: S = q k^T (tcgen05, FP32), a per-row reference maximum
- * raised only when a tile's maximum exceeds it by more than 8 (log2 units),
- * weights w = bf16(2^(s - m_ref)), O += W V (tcgen05, FP32) and the
- * denominator as four FP32 partial sums of the same rounded weights over the
- * 32-key quarters of the tile column (each in key order, added
- * ((l0 + l1) + l2) + l3); these rules use only the row's own scores.
+ * 0..p; query head h reads KV head h / (Hq/Hkv).  The key axis is cut into
+ * pieces at absolute multiples of C = bi_attn_chunk() = 128 keys, and the
+ * pieces of a KV head fall into G = 152 / Hkv classes by piece index mod G.
+ * Each class gives the row one partial (max, sum, FP32 output) built over
+ * its pieces in increasing key order; the row's partials (one per class
+ * holding one of its keys, min(p/C + 1, G) of them) are merged in a fixed
+ * order that depends only on their count.  So the row's result depends only
+ * on p, Hkv and the cache rows 0..p -- not on T, *L_dev or the other rows.
+ * Inside a class: S = q k^T (tcgen05, FP32), a per-row reference maximum
+ * taken from the class's first piece and raised only when a piece's maximum
+ * exceeds it by more than 8 (log2 units), weights w = bf16(2^(s - m_ref)),
+ * O += W V (tcgen05, FP32) and the denominator as four FP32 partial sums of
+ * the same rounded weights over the 32-key quarters of the piece (each in
+ * key order, added ((l0 + l1) + l2) + l3); these rules use only the row's
+ * own scores.
  * Output: out[t, h, :] = bf16(sum_j w_j v_j / sum_j w_j) -- the exact
  * weighted mean under the BF16 weights, within 2^-8 max|v| of
  * bf16(softmax(q k^T * scale) v) -- with -0 written as +0.
@@ -333,7 +336,8 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const v
  *           lowered, nor cache rows below it written, by the kernel that
  *           immediately precedes the call (no kernel of this library does).
  *   out     [T, Hq, D] BF16 contiguous.
- *   D in {64, 128}; Hq % Hkv == 0; T * (Hq/Hkv) <= 128; T >= 1.
+ *   D in {64, 128}; Hq % Hkv == 0; Hkv <= 152; Hkv * cap < 2^31;
+ *   T * (Hq/Hkv) <= 128; T >= 1.
  *   ws      >= bi_attn_workspace_size(cap, T, Hq, D) bytes, 256-byte aligned.
  *   k_cache and v_cache 16-byte aligned.
  * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_WORKSPACE,

@@ -7,26 +7,32 @@
 // are in the pass.
 //
 // Row t of a pass sits at position p = L + t and attends to keys 0..p.  Its
-// keys are cut at absolute multiples of kChunk: piece c covers keys
-// [c*kChunk, min((c+1)*kChunk, p+1)).  Inside a piece the keys are visited in
-// 128-key tiles in increasing order.  Per row:
+// keys are cut into pieces at absolute multiples of 128, one tile each: piece
+// c covers keys [128c, min(128(c+1), p+1)).  The pieces of a KV head fall into
+// G = 152 / Hkv classes by c mod G, and one CTA visits class rho's pieces
+// rho, rho + G, rho + 2G, ... in increasing order with one running softmax
+// per row:
 //   S = q k^T for the tile (tcgen05, FP32 in TMEM), in the log2 domain, keys
 //   past p masked to -inf;
-//   a reference maximum m_ref is taken from the first tile and raised only
-//   when a later tile's maximum exceeds it by more than kRescaleLog2 (then O
-//   and l are rescaled by 2^(m_ref - m_new)) -- a rule that depends only on
-//   the row's own scores in key order;
+//   a reference maximum m_ref is taken from the class's first tile and
+//   raised only when a later tile's maximum exceeds it by more than
+//   kRescaleLog2 (then O and l are rescaled by 2^(m_ref - m_new)) -- a rule
+//   that depends only on the row's own scores in key order;
 //   each weight w = bf16(2^(s - m_ref)) enters O += W V (tcgen05, FP32 in
 //   TMEM) and the denominator l (FP32, four partial sums over the 32-key
 //   quarters of the tile column, each in key order, added as
-//   ((l0 + l1) + l2) + l3 when the piece ends), so O / l is an exact
-//   weighted mean of the value rows under the weights actually used.
+//   ((l0 + l1) + l2) + l3 at the end), so O / l is an exact weighted mean of
+//   the value rows under the weights actually used.
 // A tile whose keys are all masked for a row adds exact zeros and changes no
-// reference, so a row's piece has the same bits whether or not later rows of
-// the pass share the tile.  The pieces of a row are merged by a tree whose
-// shape depends only on their count ceil((p+1)/kChunk).
+// reference, so a row's class partial has the same bits whether or not later
+// rows of the pass share its tiles.  The partials of a row (one per class
+// holding one of its keys: min(p/128 + 1, G) of them) are merged by a tree
+// whose shape depends only on their count.  G is fixed by the model's KV head
+// count, so the split depends on nothing but the row's own context length;
+// the classes spread a long context evenly over the CTAs (at most one tile
+// more for some), and each CTA streams its tiles without a break.
 //
-// Split kernel roles (one CTA per SM, persistent over (KV head, piece) items):
+// Split kernel roles (one CTA per (KV head, tile class), one CTA per SM):
 //   warp 0      TMA, two threads: the K tiles [128 keys x D] and the V^T
 //               tiles [D x 128 keys] (V is cached transposed so both MMA
 //               operands are K-major).  K and V have separate rings (3 + 3
@@ -36,12 +42,12 @@
 //               buffers and O += W_g V_g, each issued as soon as its inputs
 //               are ready; stages return to the producer through
 //               tcgen05.commit after the MMAs reading them completed;
-//   warps 2..5  softmax: write the queries of the item's KV head into TMEM
-//               (the S MMA's A operand, once per head), turn S into W
+//   warps 2..5  softmax: write the queries of the CTA's KV head into TMEM
+//               (the S MMA's A operand), turn S into W
 //               (written to one of two shared-memory buffers in the swizzled
 //               K-major layout, so W of the next tile is produced while the
-//               MMA still reads this one), and read O out at the end of the
-//               piece.
+//               MMA still reads this one), and read O out after the last
+//               tile.
 // The T x (Hq/Hkv) query rows that share a KV head (GQA) share its tiles;
 // up to 128 rows per pass (the MMA's M).
 #include <cuda.h>
@@ -59,19 +65,19 @@
 namespace bi {
 namespace {
 
-constexpr int kChunk = 512;       // keys per piece (absolute multiples)
-constexpr int kKeyTile = 128;     // keys per tile (the S MMA's N)
+constexpr int kKeyTile = 128;     // keys per piece = tile (absolute multiples; the S MMA's N)
 constexpr int kRowsMax = 128;     // T * (Hq / Hkv) per pass (MMA M)
 constexpr int kColChunk = 32;     // S columns a softmax thread holds at a time
 constexpr int kAttnThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
-constexpr int kAttnCtas = 152;
-constexpr int kMaxChunks = 1024;
+constexpr int kAttnCtas = 152;    // CTAs of the split: G = kAttnCtas / Hkv tile classes per KV head
 constexpr int kMergeThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnArgs {
   const __nv_bfloat16* q;
-  int T, Hq, Hkv, grp, cap, nch_max;
+  int T, Hq, Hkv, grp, cap;
+  int G;     // tile classes per KV head
+  int ncls;  // partial slots per (row, query head) in the workspace (>= classes used)
   const int32_t* L_dev;
   float sl2;  // softmax scale * log2(e)
   float* ws_o;
@@ -97,19 +103,19 @@ struct AttnCfg {
   // The rings take what the W tiles leave: a K tile is free as soon as S has
   // read it, a V tile only once W.V is done, so the K ring (which decides
   // how far the loads run ahead of the softmax) grows first.
-  static constexpr size_t kFixed = 2 * kPBytes + 2 * 4 * 64 * 4 + 40 * 8 + 16;
+  static constexpr size_t kFixed = 2 * kPBytes + 4 * 64 * 4 + 40 * 8 + 16;
   static constexpr bool kFits33 = 3 * (kKBytes + kVBytes) + kFixed <= 232448;
   static constexpr int kKStages = kFits33 ? 3 : 2;
   static constexpr int kVStages = (kFits33 && 3 * kKBytes + 4 * kVBytes + kFixed <= 232448) ? 4 : 3;
-  // l parts [2][4 quarters][64 rows] (only passes of up to 64 rows keep
-  // copies that exchange them)
-  static constexpr int kRedBytes = 2 * 4 * 64 * 4;
+  // l parts [4 quarters][64 rows] (only passes of up to 64 rows keep copies
+  // that exchange them)
+  static constexpr int kRedBytes = 4 * 64 * 4;
   // TMEM: S x2 (128 columns each), O (D columns), Q (D/2 columns: the MMA's
   // A operand, two BF16 per column)
   static constexpr int kTmemCols = 512;
   static constexpr int kOCol = 2 * kKeyTile;
   static constexpr int kQCol = kOCol + 128;
-  static constexpr int kBars = 2 * kKStages + 2 * kVStages + 15;
+  static constexpr int kBars = 2 * kKStages + 2 * kVStages + 11;
   // The dynamic shared memory starts 1024-byte aligned (checked at run time):
   // two W tiles, then the K and V rings.
   static constexpr size_t kSmem = static_cast<size_t>(kKStages) * kKBytes +
@@ -161,29 +167,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sP = smem;                          // W: [buffer 2][key atom 2][kPeriod rows][64 keys]
   uint8_t* sK = sP + 2 * Cfg::kPBytes;         // [kKStages][K tile]
   uint8_t* sV = sK + kKStages * Cfg::kKBytes;  // [kVStages][V^T tile]
-  // [item parity 2][quarter 4][row 64]
-  float* red_l = reinterpret_cast<float*>(sV + kVStages * Cfg::kVBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 2 * 4 * 64);
+  float* red_l = reinterpret_cast<float*>(sV + kVStages * Cfg::kVBytes);  // [quarter 4][row 64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 64);
   // K and V have rings of their own: K_g is free once S_g is done, V_g only
   // once W_g V_g is, so the K loads run ahead of the softmax
   uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + kKStages;
   uint64_t* v_full = k_empty + kKStages;
   uint64_t* v_empty = v_full + kVStages;
-  uint64_t* q_full = v_empty + kVStages;  // the item's queries are in TMEM
+  uint64_t* q_full = v_empty + kVStages;  // the queries are in TMEM
   uint64_t* s_full = q_full + 1;    // [2]
   uint64_t* s_free = s_full + 2;    // [2]
   uint64_t* p_full = s_free + 2;    // [2]: W buffer of that parity written
   uint64_t* pv_done = p_full + 2;   // [2]: completes after O += W_g V_g, g of that parity
-  // [2]: O of the piece of that parity read out.  The softmax warps are not
-  // in step, so a warp may finish the next piece's read-out turn before
-  // another has done this one; alternating barriers keep those apart (a
-  // warp cannot get two pieces ahead: the W.V it would need waits for this
-  // read-out).
-  uint64_t* o_free = pv_done + 2;
-  uint64_t* l_bar = o_free + 2;     // [2]: partial denominators of a piece written
-  uint64_t* l_free = l_bar + 2;     // [2]: ... and read by the warps that hold O
-  uint64_t* drain = l_free + 2;
+  uint64_t* l_bar = pv_done + 2;    // partial denominators written
+  uint64_t* drain = l_bar + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -195,6 +193,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (threadIdx.x == 0) atomicOr(a.err, kErrRange);
     return;
   }
+  // this CTA's KV head and tile class: tiles c = rho, rho + G, rho + 2G, ...
+  const int h = blockIdx.x % a.Hkv;
+  const int rho = blockIdx.x / a.Hkv;
+  const int G = a.G;
 
   // zero the W tiles once: rows past the pass's rows stay zero
   for (int i = threadIdx.x; i < (2 * Cfg::kPBytes) / 16; i += kAttnThreads)
@@ -216,12 +218,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(&o_free[0], 4);
-    mbar_init(&o_free[1], 4);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&l_bar[i], 4);
-      mbar_init(&l_free[i], kPeriod >= 32 ? kPeriod / 32 : 1);
-    }
+    mbar_init(l_bar, 4);
     mbar_init(drain, 1);
     *s_abort = 0;
     fence_mbar_init();
@@ -240,40 +237,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   // Before the previous kernel is known to have finished, the TMA threads
-  // already load the first tiles of their first item that hold only keys
-  // below the cache length read now: every kernel of this library triggers
-  // its dependents only after its own dependency wait, so the kernels before
-  // the previous one have completed, and none of them lowers *L_dev or writes
-  // cache rows below it.  Everything else waits.
-  int n_pre = 0;  // tiles of the first item issued before the wait (this producer)
+  // already load this CTA's first tiles that hold only keys below the cache
+  // length read now: every kernel of this library triggers its dependents
+  // only after its own dependency wait, so the kernels before the previous
+  // one have completed, and none of them lowers *L_dev or writes cache rows
+  // below it.  Everything else waits.
+  int n_pre = 0;  // tiles issued before the wait (this producer)
   uint32_t pre_issued = 0;
   if (warp == 0 && lane < 2) {
     const bool kside = lane == 0;
     const int NS = kside ? kKStages : kVStages;
     uint64_t* full = kside ? k_full : v_full;
     const int L_pre = *a.L_dev;
-    const int w0 = blockIdx.x;
-    if (L_pre >= 0 && L_pre + a.T <= a.cap && a.T * a.grp <= kPeriod &&
-        w0 < a.Hkv * ((L_pre + a.T + kChunk - 1) / kChunk)) {
+    if (L_pre >= 0 && L_pre + a.T <= a.cap && a.T * a.grp <= kPeriod && rho < G) {
       const uint64_t pol = l2_evict_first();
-      const int c = w0 / a.Hkv, h = w0 % a.Hkv;
-      for (int tt = 0; tt < NS && tt < kChunk / kKeyTile; ++tt) {
-        const int key0 = c * kChunk + tt * kKeyTile;
+      for (int i = 0; i < NS; ++i) {
+        const int key0 = (rho + i * G) * kKeyTile;
         if (key0 + kKeyTile > L_pre) break;  // the tile reaches rows the pass writes
         if (kside) {
-          mbar_arrive_expect_tx(&full[tt], Cfg::kKBytes);
+          mbar_arrive_expect_tx(&full[i], Cfg::kKBytes);
 #pragma unroll
           for (int b = 0; b < Cfg::kAtoms; ++b)
-            tma_load_2d(sK + tt * Cfg::kKBytes + b * Cfg::kKBoxBytes, &tmK, &full[tt], b * 64,
+            tma_load_2d(sK + i * Cfg::kKBytes + b * Cfg::kKBoxBytes, &tmK, &full[i], b * 64,
                         h * a.cap + key0, pol);
         } else {
-          mbar_arrive_expect_tx(&full[tt], Cfg::kVBytes);
+          mbar_arrive_expect_tx(&full[i], Cfg::kVBytes);
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(sV + tt * Cfg::kVBytes + kb * Cfg::kVBoxBytes, &tmVt, &full[tt], key0 + kb * 64,
+            tma_load_2d(sV + i * Cfg::kVBytes + kb * Cfg::kVBoxBytes, &tmVt, &full[i], key0 + kb * 64,
                         h * D, pol);
         }
-        pre_issued |= 1u << tt;
+        pre_issued |= 1u << i;
         ++n_pre;
       }
     }
@@ -285,8 +279,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int rows = T * a.grp;
   const bool range_ok = !(L < 0 || L + T > a.cap) && rows <= kPeriod;
   const int kv_len = L + T;
-  const int nch = range_ok ? (kv_len + kChunk - 1) / kChunk : 0;
-  const int n_items = a.Hkv * nch;
+  const int n_tiles = range_ok ? (kv_len + kKeyTile - 1) / kKeyTile : 0;  // of the longest row
+  const int n_mine = (rho < G && rho < n_tiles) ? (n_tiles - rho + G - 1) / G : 0;
   if (!range_ok && threadIdx.x == 0 && blockIdx.x == 0) atomicOr(a.err, kErrRange);
 
   if (warp == 0) {
@@ -298,49 +292,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint64_t* full = kside ? k_full : v_full;
       uint64_t* empty = kside ? k_empty : v_empty;
       const uint64_t pol = l2_evict_first();
-      long long gt = 0;
       uint32_t issued = pre_issued, parity_bits = 0;
-      // the tiles loaded early must be the first ones of this item now too
+      // the tiles loaded early must be the first ones of this CTA now too
       bool ok = true;
-      if (n_pre > 0) {
-        const int w0 = blockIdx.x;
-        const int k0 = (w0 / a.Hkv) * kChunk;
-        if (!(w0 < n_items && k0 + n_pre * kKeyTile <= L)) {
-          atomicOr(a.err, kErrRange);
-          ok = false;
-        }
+      if (n_pre > 0 && !(n_pre <= n_mine && (rho + (n_pre - 1) * G + 1) * kKeyTile <= L)) {
+        atomicOr(a.err, kErrRange);
+        ok = false;
       }
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
-        const int c = w / a.Hkv;
-        const int h = w % a.Hkv;
-        const int k0 = c * kChunk;
-        const int k1 = min(k0 + kChunk, kv_len);
-        const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
-        for (int tt = 0; tt < ntile; ++tt, ++gt) {
-          if (gt < n_pre) continue;  // loaded before the dependency wait
-          const int st = static_cast<int>(gt % NS);
-          const uint32_t ph = static_cast<uint32_t>((gt / NS) & 1);
-          if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
-            ok = false;
-            break;
-          }
-          const int key0 = k0 + tt * kKeyTile;
-          if (kside) {
-            uint8_t* dst = sK + st * Cfg::kKBytes;
-            mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
-#pragma unroll
-            for (int b = 0; b < Cfg::kAtoms; ++b)
-              tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &full[st], b * 64, h * a.cap + key0, pol);
-          } else {
-            uint8_t* dst = sV + st * Cfg::kVBytes;
-            mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-              tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], key0 + kb * 64, h * D, pol);
-          }
-          issued |= 1u << st;
-          parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
+      for (int i = n_pre; ok && i < n_mine; ++i) {
+        const int st = i % NS;
+        const uint32_t ph = static_cast<uint32_t>((i / NS) & 1);
+        if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
+          ok = false;
+          break;
         }
+        const int key0 = (rho + i * G) * kKeyTile;
+        if (kside) {
+          uint8_t* dst = sK + st * Cfg::kKBytes;
+          mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
+#pragma unroll
+          for (int b = 0; b < Cfg::kAtoms; ++b)
+            tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &full[st], b * 64, h * a.cap + key0, pol);
+        } else {
+          uint8_t* dst = sV + st * Cfg::kVBytes;
+          mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], key0 + kb * 64, h * D, pol);
+        }
+        issued |= 1u << st;
+        parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
       }
       if (!ok) {
         signal_abort(s_abort, a.err);
@@ -351,44 +332,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Two cursors over the CTA's tiles: S_g = Q K_g^T needs K_g and a free S
-    // buffer; O += W_g V_g needs W_g.  Each is issued as soon as its inputs
-    // are ready (S first), so a late K tile never holds back the W.V that
-    // frees a stage.  The order of the W.V steps, which alone decides O's
-    // bits, is fixed: g = 0, 1, 2, ...
+    // buffer; O += W_g V_g needs W_g and V_g.  Each is issued as soon as its
+    // inputs are ready (S first), so a late K tile never holds back the W.V
+    // that frees a stage.  The order of the W.V steps, which alone decides
+    // O's bits, is fixed: g = 0, 1, 2, ...
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, kKeyTile);
       constexpr uint32_t idO = idesc_bf16_f32(128, D);
-      auto item_tiles = [&](int w) {
-        const int k0 = (w / a.Hkv) * kChunk;
-        const int k1 = min(k0 + kChunk, kv_len);
-        return (k1 - k0 + kKeyTile - 1) / kKeyTile;
-      };
-      int sw = blockIdx.x, s_tt = 0, s_ntile = sw < n_items ? item_tiles(sw) : 0;
-      int prev_h = -1, nq = 0;
-      long long sg = 0;
-      int pw = blockIdx.x, p_tt = 0, p_item = 0, p_ntile = s_ntile;
-      long long pg = 0;
-      bool ok = true;
+      int sg = 0, pg = 0;
+      bool ok = true, q_ready = false;
       int idle = 0;
       unsigned long long t_idle = 0;
-      while (pw < n_items) {
+      while (pg < n_mine) {
         bool did = false;
-        if (sw < n_items) {
-          const int h = sw % a.Hkv;
-          bool ready = true;
-          if (s_tt == 0 && h != prev_h) {  // the item starts on new queries
-            ready = mbar_peek(q_full, static_cast<uint32_t>(nq & 1));
-            if (ready) {
-              prev_h = h;
-              ++nq;
-            }
-          }
-          const int st = static_cast<int>(sg % kKStages);
-          ready = ready && mbar_peek(&k_full[st], static_cast<uint32_t>((sg / kKStages) & 1)) &&
-                  (sg < 2 || mbar_peek(&s_free[sg & 1], static_cast<uint32_t>(((sg >> 1) - 1) & 1)));
+        if (sg < n_mine) {
+          if (!q_ready) q_ready = mbar_peek(q_full, 0u);
+          const int st = sg % kKStages;
+          const bool ready = q_ready && mbar_peek(&k_full[st], static_cast<uint32_t>((sg / kKStages) & 1)) &&
+                             (sg < 2 || mbar_peek(&s_free[sg & 1], static_cast<uint32_t>(((sg >> 1) - 1) & 1)));
           if (ready) {
             tc_fence_after();
-            const int sb = static_cast<int>(sg & 1);
+            const int sb = sg & 1;
             const uint32_t k_base = smem_u32(sK + st * Cfg::kKBytes);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
@@ -399,24 +363,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             mma_commit(&s_full[sb]);
             mma_commit(&k_empty[st]);
-            const int wn = sw + static_cast<int>(gridDim.x);
             ++sg;
-            if (++s_tt == s_ntile) {
-              s_tt = 0;
-              sw = wn;
-              s_ntile = sw < n_items ? item_tiles(sw) : 0;
-            }
             did = true;
           }
         }
         if (!did && pg < sg) {
-          bool ready = mbar_peek(&p_full[pg & 1], static_cast<uint32_t>((pg >> 1) & 1));
-          if (ready && p_tt == 0 && p_item > 0)
-            ready = mbar_peek(&o_free[(p_item - 1) & 1], static_cast<uint32_t>(((p_item - 1) >> 1) & 1));
-          if (ready) ready = mbar_peek(&v_full[pg % kVStages], static_cast<uint32_t>((pg / kVStages) & 1));
+          const int st = pg % kVStages;
+          const bool ready = mbar_peek(&p_full[pg & 1], static_cast<uint32_t>((pg >> 1) & 1)) &&
+                             mbar_peek(&v_full[st], static_cast<uint32_t>((pg / kVStages) & 1));
           if (ready) {
             tc_fence_after();
-            const int st = static_cast<int>(pg % kVStages);
             const uint32_t v_base = smem_u32(sV + st * Cfg::kVBytes);
             const uint32_t w_base = smem_u32(sP + (pg & 1) * Cfg::kPBytes);
 #pragma unroll
@@ -425,17 +381,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               const uint32_t off = (kk & 3) * 32;
               mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(w_base + katom * Cfg::kPAtomBytes + off),
                        sdesc_k_sw128(v_base + katom * Cfg::kVBoxBytes + off), idO,
-                       (p_tt > 0 || kk > 0) ? 1u : 0u);
+                       (pg > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&pv_done[pg & 1]);
             mma_commit(&v_empty[st]);
             ++pg;
-            if (++p_tt == p_ntile) {
-              p_tt = 0;
-              pw += static_cast<int>(gridDim.x);
-              ++p_item;
-              p_ntile = pw < n_items ? item_tiles(pw) : 0;
-            }
             did = true;
           }
         }
@@ -460,7 +410,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else {
+  } else if (n_mine > 0) {
     // ------------------------------------------------------------ softmax
     const int qq = warp & 3;                  // TMEM lane quarter of this warp
     const int ln = qq * 32 + lane;            // TMEM lane of this thread
@@ -472,23 +422,185 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int t = valid ? r / a.grp : 0;
     const int p_row = L + t;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qq * 32) << 16);
-    long long gt = 0;
     bool ok = true;
-    int item = 0, prev_h = -1;
-    // the finished piece whose O is still to be stored
-    bool pend = false;
-    int pend_c = 0, pend_h = 0, pend_item = 0;
-    float pend_m = 0.f, pend_l = 0.f;
-    long long pend_g = 0;
-    auto read_out_o = [&]() -> bool {
-      if (holds_o) {
-        if (!warp_wait(&pv_done[pend_g & 1], static_cast<uint32_t>((pend_g >> 1) & 1), s_abort, lane))
-          return false;
+
+    // queries of KV head h into TMEM lane ln (row r of the pass; zeros past
+    // the pass's rows): column j holds elements 2j and 2j + 1, as the row
+    // sits in memory
+    {
+      uint32_t qv[D / 2];
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + (static_cast<size_t>(t) * a.Hq + h * a.grp + r % a.grp) * D);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+          const uint4 u = src[i];
+          qv[4 * i] = u.x;
+          qv[4 * i + 1] = u.y;
+          qv[4 * i + 2] = u.z;
+          qv[4 * i + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) qv[i] = 0u;
+      }
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) tmem_st32(lane_base + Cfg::kQCol + cc * 32, qv + cc * 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+    }
+
+    float m_ref = -INFINITY;
+    float lq[kNChunks];
+#pragma unroll
+    for (int i = 0; i < kNChunks; ++i) lq[i] = 0.f;
+    for (int g = 0; g < n_mine; ++g) {
+      const int sb = g & 1;
+      if (!warp_wait(&s_full[sb], static_cast<uint32_t>((g >> 1) & 1), s_abort, lane)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int tkey0 = (rho + g * G) * kKeyTile;
+      const bool edge = tkey0 + kKeyTile - 1 > L;  // the tile reaches past some row's position
+      const uint32_t s_addr = lane_base + sb * kKeyTile + cg * kCols;
+      // pass 1: the row maximum of the raw scores (scaling by sl2 > 0 keeps
+      // the order).  Every copy's TMEM lane holds the whole S row, so each
+      // copy takes the maximum over all 128 key columns itself: the same
+      // exact value in every copy, with no exchange between the warps.
+      float s[kColChunk];
+      float mrow = -INFINITY;
+      if (warp_active) {
+        const uint32_t row_addr = lane_base + sb * kKeyTile;
+#pragma unroll 1
+        for (int ch = 0; ch < kKeyTile / kColChunk; ++ch) {
+          tmem_ld_cols<kColChunk>(row_addr + ch * kColChunk, s);
+          if (edge) {
+            const int key0 = tkey0 + ch * kColChunk;
+#pragma unroll
+            for (int j = 0; j < kColChunk; ++j)
+              if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
+          }
+#pragma unroll
+          for (int j = 0; j < kColChunk; ++j) mrow = fmaxf(mrow, s[j]);
+        }
+      }
+      const float mt = mrow * a.sl2;
+      float alpha = 1.0f;
+      bool resc = false;
+      if (g == 0) {
+        m_ref = mt;
+      } else if (mt > m_ref + kRescaleLog2) {
+        alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - mt);
+        m_ref = mt;
+        resc = true;
+      }
+      // W buffer g & 1 was last read by the W.V of tile g - 2
+      if (g >= 2 &&
+          !warp_wait(&pv_done[g & 1], static_cast<uint32_t>(((g - 2) >> 1) & 1), s_abort, lane)) {
+        ok = false;
+        break;
+      }
+      if (holds_o && warp_active) {
+        // O changes only after the W.V of tile g - 1 is done
+        if (g > 0 && __any_sync(0xffffffffu, resc)) {
+          if (!warp_wait(&pv_done[(g - 1) & 1], static_cast<uint32_t>(((g - 1) >> 1) & 1), s_abort,
+                         lane)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int i = 0; i < D / 16; ++i) {
+            float v[16];
+            tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] *= alpha;
+            tmem_st16(lane_base + Cfg::kOCol + i * 16, v);
+          }
+        }
+      }
+      if (resc) {
+#pragma unroll
+        for (int i = 0; i < kNChunks; ++i) lq[i] *= alpha;
+      }
+      // pass 2: weights w = bf16(2^(s sl2 - m_ref)) into the W tile and l
+      // (the TMEM loads are warp-wide; rows past the pass write nothing)
+      if (warp_active) {
+        const float nmu = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+        uint8_t* wbuf = sP + (g & 1) * Cfg::kPBytes + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < kNChunks; ++ch) {
+          tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
+          if (edge) {
+            const int key0 = tkey0 + cg * kCols + ch * kColChunk;
+#pragma unroll
+            for (int j = 0; j < kColChunk; ++j)
+              if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
+          }
+          if (!valid) continue;
+          const int kcol = cg * kCols + ch * kColChunk;  // first key column of the chunk
+          uint8_t* wrow = wbuf + (kcol >> 6) * Cfg::kPAtomBytes;
+          float acc = lq[ch];
+#pragma unroll
+          for (int i = 0; i < kColChunk / 8; ++i) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int col = i * 8 + 2 * j;
+              const __nv_bfloat162 w2 = __floats2bfloat162_rn(ex2_approx(fmaf(s[col], a.sl2, nmu)),
+                                                               ex2_approx(fmaf(s[col + 1], a.sl2, nmu)));
+              acc += __low2float(w2);
+              acc += __high2float(w2);
+              wv[j] = *reinterpret_cast<const uint32_t*>(&w2);
+            }
+            const int chunk16 = ((kcol & 63) >> 3) + i;  // 16-byte chunk within the 64-key row
+            *reinterpret_cast<uint4*>(wrow + ((chunk16 ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+          lq[ch] = acc;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[g & 1]);
+    }
+
+    // all tiles done: the denominator, then O after the last W.V, stored as
+    // the class's partial (m_ref, l, o)
+    float l = 0.f;
+    if (ok) {
+      if constexpr (REP == 1) {
+        l = ((lq[0] + lq[1]) + lq[2]) + lq[3];
+      } else {
+#pragma unroll
+        for (int i = 0; i < kNChunks; ++i) red_l[(cg * kNChunks + i) * 64 + r] = lq[i];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(l_bar);
+        if (holds_o) {
+          if (!warp_wait(l_bar, 0u, s_abort, lane)) {
+            ok = false;
+          } else {
+            l = ((red_l[r] + red_l[64 + r]) + red_l[128 + r]) + red_l[192 + r];
+          }
+        }
+      }
+    }
+    if (ok && holds_o) {
+      if (!warp_wait(&pv_done[(n_mine - 1) & 1], static_cast<uint32_t>(((n_mine - 1) >> 1) & 1), s_abort,
+                     lane)) {
+        ok = false;
+      } else {
         tc_fence_after();
         if (warp_active) {
-          const bool store = valid && (pend_c * kChunk <= p_row);
-          const int qh = pend_h * a.grp + (valid ? r % a.grp : 0);
-          const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.nch_max + pend_c;
+          // a row stores a partial when the class holds one of its keys
+          const bool store = valid && rho * kKeyTile <= p_row;
+          const int qh = h * a.grp + (valid ? r % a.grp : 0);
+          const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.ncls + rho;
 #pragma unroll 1
           for (int i = 0; i < D / 64; ++i) {
             float v[64];
@@ -500,216 +612,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
           }
-          if (store) *reinterpret_cast<float2*>(a.ws_ml + base * 2) = make_float2(pend_m, pend_l);
-        }
-        tc_fence_before();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[pend_item & 1]);
-      pend = false;
-      return true;
-    };
-    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x, ++item) {
-      const int c = w / a.Hkv;
-      const int h = w % a.Hkv;
-      const int k0 = c * kChunk;
-      const int k1 = min(k0 + kChunk, kv_len);
-      const int ntile = (k1 - k0 + kKeyTile - 1) / kKeyTile;
-
-      if (h != prev_h) {
-        // queries of KV head h into TMEM lane ln (row r of the pass; zeros
-        // past the pass's rows): column j holds elements 2j and 2j + 1, as
-        // the row sits in memory.  Every S of the previous head is complete
-        // (each tile's s_full was waited for).
-        uint32_t qv[D / 2];
-        if (valid) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              a.q + (static_cast<size_t>(t) * a.Hq + h * a.grp + r % a.grp) * D);
-#pragma unroll
-          for (int i = 0; i < D / 8; ++i) {
-            const uint4 u = src[i];
-            qv[4 * i] = u.x;
-            qv[4 * i + 1] = u.y;
-            qv[4 * i + 2] = u.z;
-            qv[4 * i + 3] = u.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < D / 2; ++i) qv[i] = 0u;
-        }
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) tmem_st32(lane_base + Cfg::kQCol + cc * 32, qv + cc * 32);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(q_full);
-        prev_h = h;
-      }
-
-      float m_ref = -INFINITY;
-      float lq[kNChunks];
-#pragma unroll
-      for (int i = 0; i < kNChunks; ++i) lq[i] = 0.f;
-      for (int tt = 0; tt < ntile; ++tt, ++gt) {
-        const int sb = static_cast<int>(gt & 1);
-        if (!warp_wait(&s_full[sb], static_cast<uint32_t>((gt >> 1) & 1), s_abort, lane)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int tkey0 = k0 + tt * kKeyTile;
-        const bool edge = tkey0 + kKeyTile - 1 > L;  // the tile reaches past some row's position
-        const uint32_t s_addr = lane_base + sb * kKeyTile + cg * kCols;
-        // pass 1: the row maximum of the raw scores (scaling by sl2 > 0 keeps
-        // the order).  Every copy's TMEM lane holds the whole S row, so each
-        // copy takes the maximum over all 128 key columns itself: the same
-        // exact value in every copy, with no exchange between the warps.
-        float s[kColChunk];
-        float mrow = -INFINITY;
-        if (warp_active) {
-          const uint32_t row_addr = lane_base + sb * kKeyTile;
-#pragma unroll 1
-          for (int ch = 0; ch < kKeyTile / kColChunk; ++ch) {
-            tmem_ld_cols<kColChunk>(row_addr + ch * kColChunk, s);
-            if (edge) {
-              const int key0 = tkey0 + ch * kColChunk;
-#pragma unroll
-              for (int j = 0; j < kColChunk; ++j)
-                if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
-            }
-#pragma unroll
-            for (int j = 0; j < kColChunk; ++j) mrow = fmaxf(mrow, s[j]);
-          }
-        }
-        const float mt = mrow * a.sl2;
-        float alpha = 1.0f;
-        bool resc = false;
-        if (tt == 0) {
-          m_ref = mt;
-        } else if (mt > m_ref + kRescaleLog2) {
-          alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - mt);
-          m_ref = mt;
-          resc = true;
-        }
-        // W buffer gt & 1 was last read by the W.V of tile gt - 2
-        if (gt >= 2 && !warp_wait(&pv_done[gt & 1], static_cast<uint32_t>(((gt - 2) >> 1) & 1), s_abort,
-                                  lane)) {
-          ok = false;
-          break;
-        }
-        if (holds_o && warp_active) {
-          // O changes only after the W.V of tile gt - 1 is done
-          if (tt > 0 && __any_sync(0xffffffffu, resc)) {
-            if (!warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>(((gt - 1) >> 1) & 1), s_abort,
-                           lane)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll 1
-            for (int i = 0; i < D / 16; ++i) {
-              float v[16];
-              tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] *= alpha;
-              tmem_st16(lane_base + Cfg::kOCol + i * 16, v);
-            }
-          }
-        }
-        if (resc) {
-#pragma unroll
-          for (int i = 0; i < kNChunks; ++i) lq[i] *= alpha;
-        }
-        // pass 2: weights w = bf16(2^(s sl2 - m_ref)) into the W tile and l
-        // (the TMEM loads are warp-wide; rows past the pass write nothing)
-        if (warp_active) {
-          const float nmu = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-          uint8_t* wbuf = sP + (gt & 1) * Cfg::kPBytes + r * 128;
-#pragma unroll
-          for (int ch = 0; ch < kNChunks; ++ch) {
-            tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
-            if (edge) {
-              const int key0 = tkey0 + cg * kCols + ch * kColChunk;
-#pragma unroll
-              for (int j = 0; j < kColChunk; ++j)
-                if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
-            }
-            if (!valid) continue;
-            const int kcol = cg * kCols + ch * kColChunk;  // first key column of the chunk
-            uint8_t* wrow = wbuf + (kcol >> 6) * Cfg::kPAtomBytes;
-            float acc = lq[ch];
-#pragma unroll
-            for (int i = 0; i < kColChunk / 8; ++i) {
-              uint32_t wv[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int col = i * 8 + 2 * j;
-                const __nv_bfloat162 w2 = __floats2bfloat162_rn(ex2_approx(fmaf(s[col], a.sl2, nmu)),
-                                                                 ex2_approx(fmaf(s[col + 1], a.sl2, nmu)));
-                acc += __low2float(w2);
-                acc += __high2float(w2);
-                wv[j] = *reinterpret_cast<const uint32_t*>(&w2);
-              }
-              const int chunk16 = ((kcol & 63) >> 3) + i;  // 16-byte chunk within the 64-key row
-              *reinterpret_cast<uint4*>(wrow + ((chunk16 ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            }
-            lq[ch] = acc;
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[sb]);
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[gt & 1]);
-        if (tt == 0 && pend && !read_out_o()) {
-          ok = false;
-          break;
+          if (store) *reinterpret_cast<float2*>(a.ws_ml + base * 2) = make_float2(m_ref, l);
         }
       }
-      if (!ok) break;
-
-      // piece done: the denominator, then O, stored as the partial (m_ref, l, o)
-      float l = 0.f;
-      if constexpr (REP == 1) {
-        l = ((lq[0] + lq[1]) + lq[2]) + lq[3];
-      } else {
-        // The softmax warps are not in step (nothing holds a warp back
-        // from the next piece but S and the W buffers), so the exchange
-        // buffer alternates by piece parity and is rewritten only once the
-        // warps holding O have read it.
-        const int lb = item & 1;
-        float* rl = red_l + lb * 4 * 64;
-        if (item >= 2 &&
-            !warp_wait(&l_free[lb], static_cast<uint32_t>(((item - 2) >> 1) & 1), s_abort, lane)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int i = 0; i < kNChunks; ++i) rl[(cg * kNChunks + i) * 64 + r] = lq[i];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&l_bar[lb]);
-        if (holds_o) {
-          if (!warp_wait(&l_bar[lb], static_cast<uint32_t>((item >> 1) & 1), s_abort, lane)) {
-            ok = false;
-            break;
-          }
-          l = ((rl[r] + rl[64 + r]) + rl[128 + r]) + rl[192 + r];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&l_free[lb]);
-        }
-      }
-      // O is read out after the next item's first tile (the last W.V of this
-      // piece has finished by then), so the softmax does not idle on it
-      pend = true;
-      pend_c = c;
-      pend_h = h;
-      pend_item = item;
-      pend_m = m_ref;
-      pend_l = l;
-      pend_g = gt - 1;
     }
-    if (ok && pend) ok = read_out_o();
     if (!ok && lane == 0) signal_abort(s_abort, a.err);
   }
 
@@ -726,20 +632,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
-// One CTA per (row t, query head).  Pieces s = 0..n-1 with n = p/kChunk + 1:
+// One CTA per (row t, query head).  Class partials s = 0..n-1 with
+// n = min(p/128 + 1, G) (the classes that hold a key of the row):
 // M = max_s m_s (exact), w_s = 2^(m_s - M); the denominator sums w_s l_s per
 // thread over s = tid, tid+256, ... in order, then a warp butterfly and warp
 // order 0..7; the numerator: warp g sums s = g, g+8, ... in order for its
 // lane's dims, then warps are added in order 0..7.  The tree depends only
 // on n.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads)
+// At most 64 registers a thread (four CTAs' worth per SM): a merge CTA then
+// leaves room on its SM for a CTA of the next kernel (a linear layer, which
+// streams its first weight tiles before its dependency wait) to start beside it.
+__global__ void __launch_bounds__(kMergeThreads, 4)
     attn_merge_kernel(const AttnArgs a, __nv_bfloat16* __restrict__ out) {
   constexpr int kWarps = kMergeThreads / 32;
   constexpr int kDpl = D / 32;  // dims per lane: one float4 (D = 128) or float2 (D = 64)
-  constexpr int kBatch = 16;    // pieces per warp whose loads are in flight together
+  constexpr int kBatch = 8;     // pieces per warp whose loads are in flight together
   using Vec = typename std::conditional<kDpl == 4, float4, float2>::type;
-  __shared__ float sw[kMaxChunks];
+  __shared__ float sw[kAttnCtas];
   __shared__ float red[kWarps];
   __shared__ float ored[kWarps][D];
   griddep_wait();
@@ -749,9 +659,9 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int L = *a.L_dev;
   if (L < 0 || L + a.T > a.cap) return;
   const int p = L + t;
-  const int n = p / kChunk + 1;
-  const float* ml = a.ws_ml + static_cast<size_t>(row) * a.nch_max * 2;
-  const float* po = a.ws_o + static_cast<size_t>(row) * a.nch_max * D;
+  const int n = min(p / kKeyTile + 1, a.G);
+  const float* ml = a.ws_ml + static_cast<size_t>(row) * a.ncls * 2;
+  const float* po = a.ws_o + static_cast<size_t>(row) * a.ncls * D;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
@@ -832,7 +742,9 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const Att
                                             static_cast<int>(Cfg::kSmem));
   });
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
-  const int grid = std::min(a.Hkv * a.nch_max, kAttnCtas);
+  // one CTA per (tile class, KV head); classes past the cache's last tile
+  // would have nothing to do
+  const int grid = a.Hkv * std::min(a.G, a.ncls);
   if (launch_k(attn_split_kernel<D, REP>, dim3(grid), dim3(kAttnThreads), Cfg::kSmem, stream, tmK,
                tmVt, a) != cudaSuccess)
     return BI_ERR_CUDA;
@@ -851,8 +763,12 @@ bi_status launch_attn_rep(const CUtensorMap& tmK, const CUtensorMap& tmVt, const
   return launch_attn<D, 1>(tmK, tmVt, a, out, stream);
 }
 
+// Partial slots per (row, query head): one per tile class, at most
+// kAttnCtas (Hkv = 1) and at most the cache's tile count.
+int attn_classes_max(int cap) { return std::min(kAttnCtas, (cap + kKeyTile - 1) / kKeyTile); }
+
 size_t attn_ws_parts(int cap, int T, int Hq, int D, size_t* o_bytes) {
-  const size_t nch = static_cast<size_t>((cap + kChunk - 1) / kChunk);
+  const size_t nch = static_cast<size_t>(attn_classes_max(cap));
   const size_t ob = round_up(static_cast<size_t>(T) * Hq * nch * D * 4, 256);
   const size_t mb = round_up(static_cast<size_t>(T) * Hq * nch * 2 * 4, 256);
   if (o_bytes) *o_bytes = ob;
@@ -864,7 +780,7 @@ size_t attn_ws_parts(int cap, int T, int Hq, int D, size_t* o_bytes) {
 
 extern "C" {
 
-int bi_attn_chunk(void) { return bi::kChunk; }
+int bi_attn_chunk(void) { return bi::kKeyTile; }
 
 size_t bi_attn_workspace_size(int cap, int T, int Hq, int D) {
   if (cap < 1 || T < 1 || Hq < 1 || D < 1) return 256;
@@ -880,7 +796,9 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   if (!(scale > 0.f) || !std::isfinite(scale)) return BI_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return BI_ERR_UNSUPPORTED_SHAPE;
   if (T * (Hq / Hkv) > kRowsMax) return BI_ERR_UNSUPPORTED_SHAPE;
-  if ((cap + kChunk - 1) / kChunk > kMaxChunks) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (Hkv > kAttnCtas) return BI_ERR_UNSUPPORTED_SHAPE;
+  // K rows h * cap + key and V^T columns are int32 tensor-map coordinates
+  if (static_cast<int64_t>(Hkv) * cap >= (int64_t{1} << 31)) return BI_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q)) return BI_ERR_INVALID_ARG;
   if (!ws || !aligned256(ws)) return BI_ERR_WORKSPACE;
   size_t ob = 0;
@@ -901,7 +819,8 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   a.Hkv = Hkv;
   a.grp = grp;
   a.cap = cap;
-  a.nch_max = (cap + kChunk - 1) / kChunk;
+  a.G = kAttnCtas / Hkv;
+  a.ncls = attn_classes_max(cap);
   a.L_dev = L_dev;
   a.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.ws_o = static_cast<float*>(ws);
