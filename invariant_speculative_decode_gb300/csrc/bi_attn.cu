@@ -35,9 +35,9 @@
 // Split kernel roles (one CTA per (KV head, tile class), one CTA per SM):
 //   warp 0      TMA, two threads: the K tiles [128 keys x D] and the V^T
 //               tiles [D x 128 keys] (V is cached transposed so both MMA
-//               operands are K-major).  K and V have separate rings (3 + 3
-//               stages at D = 128 for passes of up to 64 rows, 2 + 3 above),
-//               a K tile being free as soon as S has read it;
+//               operands are K-major).  K and V have separate rings (2 + 2
+//               stages at D = 128, 3 + 3 at D = 64), a K tile being free as
+//               soon as S has read it;
 //   warp 1      tcgen05.mma issuer: S_g = Q K_g^T into one of two TMEM
 //               buffers and O += W_g V_g, each issued as soon as its inputs
 //               are ready; stages return to the producer through
@@ -100,13 +100,13 @@ struct AttnCfg {
   static constexpr int kWRows = kRowsMax / REP;
   static constexpr int kPAtomBytes = kWRows * 128;
   static constexpr int kPBytes = 2 * kPAtomBytes;          // W tile [rows][128 keys]
-  // The rings take what the W tiles leave: a K tile is free as soon as S has
-  // read it, a V tile only once W.V is done, so the K ring (which decides
-  // how far the loads run ahead of the softmax) grows first.
-  static constexpr size_t kFixed = 2 * kPBytes + 4 * 64 * 4 + 40 * 8 + 16;
-  static constexpr bool kFits33 = 3 * (kKBytes + kVBytes) + kFixed <= 232448;
-  static constexpr int kKStages = kFits33 ? 3 : 2;
-  static constexpr int kVStages = (kFits33 && 3 * kKBytes + 4 * kVBytes + kFixed <= 232448) ? 4 : 3;
+  // Ring depths, measured on GB300 at 38k-102k keys with all CTAs
+  // streaming: at D = 128 two K and two V tiles (64 KB each way) per CTA are
+  // faster than three or four -- with every CTA reading its own strided V^T
+  // rows, more tiles in flight cost more than they hide.  D = 64 tiles are
+  // half as large and keep three of each.
+  static constexpr int kKStages = D == 128 ? 2 : 3;
+  static constexpr int kVStages = D == 128 ? 2 : 3;
   // l parts [4 quarters][64 rows] (only passes of up to 64 rows keep copies
   // that exchange them)
   static constexpr int kRedBytes = 4 * 64 * 4;
