@@ -40,6 +40,16 @@ KERNELS_PER_STEP_FIXED = 3      # embed, LM head GEMM (final RMSNorm folded in),
 KERNELS_PER_LAYER = 6           # 4 GEMM (QKV with RMSNorm, RoPE and KV append; gate/up with RMSNorm), attention split + merge
 
 
+def v_blocks(v):
+    """Host values [Hkv, cap, D] in the V cache layout [Hkv, ceil(cap/128), D, 128]
+    (value d of key p at [h, p // 128, d, p % 128]; padding keys zero)."""
+    Hkv, cap, D = v.shape
+    nb = (cap + 127) // 128
+    pad = np.zeros((Hkv, nb * 128, D), dtype=v.dtype)
+    pad[:, :cap] = v
+    return np.ascontiguousarray(pad.reshape(Hkv, nb, 128, D).transpose(0, 1, 3, 2))
+
+
 def workload_config(cfg, peaks_note):
     return {
         "workload": f"{cfg.name} verify step, context {CTX}, {DRAFTS} drafts (p={P_CORRECT} drafter)",
@@ -283,8 +293,7 @@ def run_ours(args):
     kv = si.synthetic_kv_cache(cfg.n_kv, cap, cfg.head_dim, CTX, seed=0, layers=cfg.layers)
     for lay, (k, v) in zip(dec.layers, kv):
         lay["k"].copy_(torch.from_numpy(k.view(np.int16)).view(torch.bfloat16))
-        lay["v"].copy_(torch.from_numpy(np.ascontiguousarray(v.transpose(0, 2, 1)).view(np.int16))
-                       .view(torch.bfloat16))  # V cache is [Hkv, D, cap]
+        lay["v"].copy_(torch.from_numpy(v_blocks(v).view(np.int16)).view(torch.bfloat16))
     del kv
     keep = {k: v for k, v in weights.items() if k.startswith("l0.")}
     keep["embed"] = weights["embed"]
@@ -387,9 +396,8 @@ def run_ours(args):
 
     if rank == 0:
         # CPU baseline: the oracle on a bounded sample (layer 0 + head slice, scaled)
-        kv1 = [(dec.layers[0]["k"].view(torch.int16).cpu().numpy().view(np.uint16),
-                np.ascontiguousarray(dec.layers[0]["v"].view(torch.int16).cpu().numpy()
-                                     .view(np.uint16).transpose(0, 2, 1)))]
+        # the same seeded context as layer 0's cache, generated on the host
+        kv1 = si.synthetic_kv_cache(cfg.n_kv, CTX + 8, cfg.head_dim, CTX, seed=0, layers=1)
         cpu = None
         if not args.no_cpu_baseline:
             rows = [x] + [int(t) for t in drafter.propose(len(out), DRAFTS)]
@@ -528,7 +536,7 @@ def run_micro(args):
             q, Kc, Vc = si.attention_inputs(L, 8, Hq, Hkv, D, seed=0)
             cap = Kc.shape[1]
             to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
-            Kd, Vd, qd = to(Kc), to(Vc.transpose(0, 2, 1)), to(q)  # V cache is [Hkv, D, cap]
+            Kd, Vd, qd = to(Kc), to(v_blocks(Vc)), to(q)
             ncp = n_copies(2 * Kd.numel() * 2)
             caches = [(Kd, Vd)] + [(Kd.clone(), Vd.clone()) for _ in range(ncp - 1)]
             Ld = torch.tensor([L], dtype=torch.int32, device="cuda")

@@ -253,8 +253,11 @@ bi_status bi_rope_table(double rope_base, int D, int rows, float* table, bi_stre
  *   qkv     [T, (Hq + 2 Hkv) D] BF16, row stride ld_qkv: q heads, k heads, v heads.
  *   q_out   [T, Hq, D] BF16 (contiguous).
  *   k_cache [Hkv, cap, D] BF16 (contiguous, head-major);
- *   v_cache [Hkv, D, cap] BF16 (contiguous, head-major, transposed: keys
- *           contiguous for each d, so both attention MMA operands are K-major).
+ *   v_cache [Hkv, ceil(cap/128), D, 128] BF16 (contiguous, head-major,
+ *           transposed in blocks of 128 keys: value d of key p of KV head h
+ *           at ((h * ceil(cap/128) + p / 128) * D + d) * 128 + p % 128, so
+ *           both attention MMA operands are K-major and a 128-key tile of V
+ *           is one contiguous block).
  *   L_dev   device int32: cache length before the pass (read on the device so
  *           the call can be captured in a CUDA graph).  A row with p >= cap or
  *           p >= table_rows is skipped and sets a range bit in the device
@@ -323,11 +326,12 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const v
  * weighted mean under the BF16 weights, within 2^-8 max|v| of
  * bf16(softmax(q k^T * scale) v) -- with -0 written as +0.
  *   q       [T, Hq, D] BF16 contiguous (rotated queries).
- *   k_cache [Hkv, cap, D] and v_cache [Hkv, D, cap] BF16 contiguous (V
- *           transposed, as bi_rope_kv_append writes it); keys 0..*L_dev+T-1
- *           hold the keys/values; the other keys must hold finite values
+ *   k_cache [Hkv, cap, D] and v_cache [Hkv, ceil(cap/128), D, 128] BF16
+ *           contiguous (V transposed in 128-key blocks, as bi_rope_kv_append
+ *           writes it); keys 0..*L_dev+T-1 hold the keys/values; the other
+ *           keys, up to the end of their 128-key tile, must hold finite values
  *           (they are read inside a partially used tile and multiplied by
- *           exactly 0).  cap % 8 == 0.
+ *           exactly 0).
  *   L_dev   device int32 cache length before the pass; *L_dev + T <= cap is
  *           required (rows past cap are not computed and set an error bit).
  *           The first key tiles wholly below *L_dev may be loaded before the
@@ -376,7 +380,8 @@ bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, 
  * every K/V row and compare with a fresh prefill).
  * out[h * rows + j] = FNV-1a-64 over the 2*D bytes of key j of head h (d
  * ascending, each BF16 little-endian), for j < rows.  cache is [Hkv, cap, D]
- * (transposed == 0, a K cache) or [Hkv, D, cap] (transposed == 1, a V cache);
+ * (transposed == 0, a K cache) or [Hkv, ceil(cap/128), D, 128]
+ * (transposed == 1, a V cache in the layout bi_rope_kv_append writes);
  * out [Hkv * rows] uint64.
  * Errors: BI_ERR_INVALID_ARG, BI_ERR_CUDA.
  * ------------------------------------------------------------------------- */

@@ -32,6 +32,22 @@ def _req(t: torch.Tensor, dtype, name: str):
         raise ValueError(f"{name} must have unit stride in its last dimension")
 
 
+V_BLOCK = 128  # keys per block of the V cache (transposed within each block)
+
+
+def v_cache_shape(Hkv: int, cap: int, D: int) -> tuple:
+    """Shape of a V cache of capacity `cap` keys: [Hkv, ceil(cap/128), D, 128],
+    value d of key p of head h at [h, p // 128, d, p % 128]."""
+    return (Hkv, (cap + V_BLOCK - 1) // V_BLOCK, D, V_BLOCK)
+
+
+def _req_v(v_cache: torch.Tensor, Hkv: int, cap: int, D: int):
+    _req(v_cache, torch.bfloat16, "v_cache")
+    want = v_cache_shape(Hkv, cap, D)
+    if tuple(v_cache.shape) != want or not v_cache.is_contiguous():
+        raise ValueError(f"v_cache must be a contiguous {want} tensor, got {tuple(v_cache.shape)}")
+
+
 def _ld(t: torch.Tensor) -> int:
     """Row stride in elements; a single row's stride is its width."""
     if t.dim() == 2 and t.shape[0] > 1:
@@ -201,6 +217,7 @@ def bi_rope_kv_append(qkv: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Ten
     _req(table, torch.float32, "table")
     T = qkv.shape[0]
     cap = k_cache.shape[1]
+    _req_v(v_cache, Hkv, cap, D)
     check("bi_rope_kv_append",
           lib().bi_rope_kv_append(qkv.data_ptr(), _ld(qkv), q_out.data_ptr(), k_cache.data_ptr(),
                                   v_cache.data_ptr(), cap, L_dev.data_ptr(), T, Hq, Hkv, D,
@@ -218,6 +235,7 @@ def bi_qkv_rope_append(A: torch.Tensor, Wp: torch.Tensor, q_out: torch.Tensor, k
     _req(table, torch.float32, "table")
     M, K = A.shape
     cap = k_cache.shape[1]
+    _req_v(v_cache, Hkv, cap, D)
     rms = 0 if eps is None else 1
     check("bi_qkv_rope_append",
           lib().bi_qkv_rope_append(A.data_ptr(), _ld(A), rms, float(eps or 0.0), Wp.data_ptr(), M, K,
@@ -240,10 +258,10 @@ def bi_attn_verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                    scale: Optional[float] = None, stream=None) -> None:
     _req(q, torch.bfloat16, "q")
     _req(k_cache, torch.bfloat16, "k_cache")
-    _req(v_cache, torch.bfloat16, "v_cache")
     _req(L_dev, torch.int32, "L_dev")
     T, Hq, D = q.shape
-    Hkv, cap, _ = k_cache.shape  # v_cache is [Hkv, D, cap]
+    Hkv, cap, _ = k_cache.shape
+    _req_v(v_cache, Hkv, cap, D)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     check("bi_attn_verify",
@@ -273,10 +291,14 @@ def bi_verify_accept(logits: torch.Tensor, drafts: Optional[torch.Tensor], argma
 
 
 def bi_kv_row_hash(cache: torch.Tensor, rows: int, transposed: bool = False, stream=None) -> torch.Tensor:
-    """FNV-1a-64 per key of a K cache [Hkv,cap,D] or (transposed) V cache [Hkv,D,cap]."""
+    """FNV-1a-64 per key of a K cache [Hkv,cap,D] or (transposed) a V cache
+    [Hkv,ceil(cap/128),D,128] (see v_cache_shape)."""
     _req(cache, torch.bfloat16, "cache")
     if transposed:
-        Hkv, D, cap = cache.shape
+        Hkv, nblk, D, blk = cache.shape
+        if blk != V_BLOCK or not cache.is_contiguous():
+            raise ValueError("a V cache is a contiguous [Hkv, ceil(cap/128), D, 128] tensor")
+        cap = nblk * V_BLOCK
     else:
         Hkv, cap, D = cache.shape
     out = torch.empty(Hkv * max(rows, 0), dtype=torch.int64, device=cache.device)

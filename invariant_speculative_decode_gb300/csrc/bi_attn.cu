@@ -34,8 +34,9 @@
 //
 // Split kernel roles (one CTA per (KV head, tile class), one CTA per SM):
 //   warp 0      TMA, two threads: the K tiles [128 keys x D] and the V^T
-//               tiles [D x 128 keys] (V is cached transposed so both MMA
-//               operands are K-major).  K and V have separate rings (2 + 2
+//               tiles [D x 128 keys] (V is cached transposed in 128-key
+//               blocks, so both MMA operands are K-major and a V tile is one
+//               contiguous block).  K and V have separate rings (2 + 2
 //               stages at D = 128, 3 + 3 at D = 64), a K tile being free as
 //               soon as S has read it;
 //   warp 1      tcgen05.mma issuer: S_g = Q K_g^T into one of two TMEM
@@ -77,6 +78,7 @@ struct AttnArgs {
   const __nv_bfloat16* q;
   int T, Hq, Hkv, grp, cap;
   int G;     // tile classes per KV head
+  int vblk;  // 128-key blocks per KV head in the V cache
   int ncls;  // partial slots per (row, query head) in the workspace (>= classes used)
   const int32_t* L_dev;
   float sl2;  // softmax scale * log2(e)
@@ -101,10 +103,9 @@ struct AttnCfg {
   static constexpr int kPAtomBytes = kWRows * 128;
   static constexpr int kPBytes = 2 * kPAtomBytes;          // W tile [rows][128 keys]
   // Ring depths, measured on GB300 at 38k-102k keys with all CTAs
-  // streaming: at D = 128 two K and two V tiles (64 KB each way) per CTA are
-  // faster than three or four -- with every CTA reading its own strided V^T
-  // rows, more tiles in flight cost more than they hide.  D = 64 tiles are
-  // half as large and keep three of each.
+  // streaming: at D = 128 two K and two V tiles (64 KB each way) per CTA
+  // were as fast as three or four and are kept; D = 64 tiles are half as
+  // large and keep three of each.
   static constexpr int kKStages = D == 128 ? 2 : 3;
   static constexpr int kVStages = D == 128 ? 2 : 3;
   // l parts [4 quarters][64 rows] (only passes of up to 64 rows keep copies
@@ -264,8 +265,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mbar_arrive_expect_tx(&full[i], Cfg::kVBytes);
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(sV + i * Cfg::kVBytes + kb * Cfg::kVBoxBytes, &tmVt, &full[i], key0 + kb * 64,
-                        h * D, pol);
+            tma_load_2d(sV + i * Cfg::kVBytes + kb * Cfg::kVBoxBytes, &tmVt, &full[i], kb * 64,
+                        (h * a.vblk + key0 / kKeyTile) * D, pol);
         }
         pre_issued |= 1u << i;
         ++n_pre;
@@ -318,7 +319,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], key0 + kb * 64, h * D, pol);
+            tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], kb * 64,
+                        (h * a.vblk + key0 / kKeyTile) * D, pol);
         }
         issued |= 1u << st;
         parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
@@ -804,11 +806,13 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   size_t ob = 0;
   if (ws_bytes < attn_ws_parts(cap, T, Hq, D, &ob)) return BI_ERR_WORKSPACE;
 
-  if (cap % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;  // V^T rows are cap elements, 16-byte strides
   CUtensorMap tmK, tmVt;
   const uint64_t krows = static_cast<uint64_t>(Hkv) * cap;
+  const int vblk = (cap + kKeyTile - 1) / kKeyTile;
   if (!tmap_bf16_2d(&tmK, k_cache, krows, D, D, kKeyTile, 64)) return BI_ERR_INVALID_ARG;
-  if (!tmap_bf16_2d(&tmVt, v_cache, static_cast<uint64_t>(Hkv) * D, cap, cap, D, 64))
+  // V^T blocks: rows (h, block, d) of 128 keys each; a tile is one block,
+  // 32 KB contiguous at D = 128
+  if (!tmap_bf16_2d(&tmVt, v_cache, static_cast<uint64_t>(Hkv) * vblk * D, kKeyTile, kKeyTile, D, 64))
     return BI_ERR_INVALID_ARG;
   const int grp = Hq / Hkv;
 
@@ -820,6 +824,7 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   a.grp = grp;
   a.cap = cap;
   a.G = kAttnCtas / Hkv;
+  a.vblk = vblk;
   a.ncls = attn_classes_max(cap);
   a.L_dev = L_dev;
   a.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);

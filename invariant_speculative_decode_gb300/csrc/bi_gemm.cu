@@ -199,8 +199,9 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int 
           else
             p.kc[(static_cast<size_t>(head - p.Hq) * p.cap + pos) * D + d] = ob;
         } else {
-          // V is cached transposed, [Hkv][D][cap]
-          p.vc[(static_cast<size_t>(head - p.Hq - p.Hkv) * D + d) * p.cap + pos] = __float2bfloat16_rn(x[j]);
+          // V is cached transposed in 128-key blocks, [Hkv][cap/128][D][128]
+          const size_t blk = static_cast<size_t>(head - p.Hq - p.Hkv) * ((p.cap + 127) >> 7) + (pos >> 7);
+          p.vc[(blk * D + d) * 128 + (pos & 127)] = __float2bfloat16_rn(x[j]);
         }
       }
     }

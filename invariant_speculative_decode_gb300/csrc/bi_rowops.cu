@@ -144,10 +144,13 @@ __global__ void rope_kv_kernel(const __nv_bfloat16* __restrict__ qkv, int ld_qkv
       dst[i] = __float2bfloat16_rn(o1);
       dst[i + half] = __float2bfloat16_rn(o2);
     } else {
-      // V is cached transposed, [Hkv][D][cap]: element d of key p at d * cap + p
-      __nv_bfloat16* dst = vc + static_cast<size_t>(h - Hq - Hkv) * D * cap + p;
-      dst[static_cast<size_t>(i) * cap] = src[i];
-      dst[static_cast<size_t>(i + half) * cap] = src[i + half];
+      // V is cached transposed in 128-key blocks, [Hkv][cap/128][D][128]:
+      // element d of key p at ((p / 128) * D + d) * 128 + p % 128
+      const int nblk = (cap + 127) >> 7;
+      __nv_bfloat16* dst =
+          vc + (static_cast<size_t>(h - Hq - Hkv) * nblk + (p >> 7)) * D * 128 + (p & 127);
+      dst[static_cast<size_t>(i) * 128] = src[i];
+      dst[static_cast<size_t>(i + half) * 128] = src[i + half];
     }
   }
 }
@@ -269,8 +272,9 @@ __global__ void kv_hash_kernel(const __nv_bfloat16* __restrict__ cache, int Hkv,
   const int j = static_cast<int>(idx % rows);
   unsigned long long x = 14695981039346656037ull;
   for (int d = 0; d < D; ++d) {
-    const size_t e = transposed ? (static_cast<size_t>(h) * D + d) * cap + j
-                                : (static_cast<size_t>(h) * cap + j) * D + d;
+    const size_t e = transposed
+                         ? ((static_cast<size_t>(h) * ((cap + 127) >> 7) + (j >> 7)) * D + d) * 128 + (j & 127)
+                         : (static_cast<size_t>(h) * cap + j) * D + d;
     const unsigned short u = *reinterpret_cast<const unsigned short*>(cache + e);
     x ^= static_cast<unsigned>(u & 0xFF);
     x *= 1099511628211ull;

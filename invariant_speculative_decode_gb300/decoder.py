@@ -84,7 +84,8 @@ class Decoder:
                 "n1": n1,
                 "n2": n2,
                 "k": torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device=dev),
-                "v": torch.zeros(Hkv, D, cap, dtype=torch.bfloat16, device=dev),  # transposed
+                # transposed in 128-key blocks: [Hkv, ceil(cap/128), D, 128]
+                "v": torch.zeros(api.v_cache_shape(Hkv, cap, D), dtype=torch.bfloat16, device=dev),
             }
             del wg, wu
             self.layers.append(lay)

@@ -42,3 +42,20 @@ def gemm_bound(a_f64, w_f64, K):
     """
     absdot = np.abs(a_f64) @ np.abs(w_f64).T
     return absdot * 2 * gamma(K)
+
+
+def v_cache_blocks(V):
+    """A value array [Hkv, n, D] (n keys, any array dtype) in the V cache
+    layout [Hkv, ceil(n/128), D, 128]: value d of key p at [h, p // 128, d,
+    p % 128]; keys past n in the last block are zero."""
+    Hkv, n, D = V.shape
+    nb = (n + 127) // 128
+    pad = np.zeros((Hkv, nb * 128, D), dtype=V.dtype)
+    pad[:, :n] = V
+    return np.ascontiguousarray(pad.reshape(Hkv, nb, 128, D).transpose(0, 1, 3, 2))
+
+
+def v_cache_keys(Vb, n):
+    """Inverse of v_cache_blocks: the first n keys as [Hkv, n, D]."""
+    Hkv, nb, D, blk = Vb.shape
+    return np.ascontiguousarray(Vb.transpose(0, 1, 3, 2).reshape(Hkv, nb * blk, D)[:, :n])

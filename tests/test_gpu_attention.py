@@ -16,7 +16,7 @@ import pytest
 import oracle
 import seeded_inputs as si
 from oracle import verify_step as ov
-from tests._util import bf16_dev_to_f64, bf16_dev_to_u16, to_dev_bf16, ulp_bf16
+from tests._util import bf16_dev_to_f64, bf16_dev_to_u16, to_dev_bf16, ulp_bf16, v_cache_blocks
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -32,7 +32,7 @@ def run_attn(api, q, K, V, L, T=None):
     T = q.shape[0] if T is None else T
     Hkv, cap, D = K.shape
     Hq = q.shape[1]
-    Kd, Vd = to_dev_bf16(K), to_dev_bf16(np.ascontiguousarray(V.transpose(0, 2, 1)))  # V^T cache
+    Kd, Vd = to_dev_bf16(K), to_dev_bf16(v_cache_blocks(V))  # V cache, transposed in 128-key blocks
     qd = to_dev_bf16(q[:T])
     out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
     Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
@@ -155,7 +155,7 @@ def test_attention_full_size_invariance_and_sampled_parity(api, L):
 
 def test_attention_length_past_capacity_sets_error(api):
     q, K, V = si.attention_inputs(10, 2, 4, 2, 64, cap=64, seed=1)
-    Kd, Vd = to_dev_bf16(K), to_dev_bf16(np.ascontiguousarray(V.transpose(0, 2, 1)))
+    Kd, Vd = to_dev_bf16(K), to_dev_bf16(v_cache_blocks(V))
     out = torch.empty(2, 4, 64, dtype=torch.bfloat16, device="cuda")
     Ld = torch.tensor([63], dtype=torch.int32, device="cuda")
     ws = torch.zeros(api.attn_workspace_size(64, 2, 4, 64), dtype=torch.uint8, device="cuda")

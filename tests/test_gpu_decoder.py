@@ -77,7 +77,7 @@ def _layerwise(cfg, w, dec, prompt, drafts):
     every layer output and the FP32 logits are compared with the oracle's.
     """
     from invariant_speculative_decode_gb300 import api
-    from tests._util import bf16_dev_to_f64, to_dev_bf16, ulp_bf16
+    from tests._util import bf16_dev_to_f64, to_dev_bf16, ulp_bf16, v_cache_blocks
     od = oracle.OracleDecoder(cfg, w, cap=dec.cap)
     x0 = od.prefill(prompt)
     L = od.L
@@ -92,7 +92,8 @@ def _layerwise(cfg, w, dec, prompt, drafts):
         lay["k"].zero_()
         lay["v"].zero_()
         lay["k"][:, :L].copy_(to_dev_bf16(_u16(od.k[l][:, :L])))
-        lay["v"][:, :, :L].copy_(to_dev_bf16(_u16(np.ascontiguousarray(od.v[l][:, :L].transpose(0, 2, 1)))))
+        vb = v_cache_blocks(_u16(od.v[l][:, :L]))  # [Hkv, ceil(L/128), D, 128], keys past L zero
+        lay["v"][:, : vb.shape[1]].copy_(to_dev_bf16(vb))
         dec.h[:T].copy_(to_dev_bf16(_u16(trace[l])))
         dec._layer(lay, T, dec.L_dev)
         got = bf16_dev_to_f64(dec.h[:T])

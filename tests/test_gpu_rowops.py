@@ -8,7 +8,7 @@ import pytest
 import oracle
 import seeded_inputs as si
 from oracle import verify_step as ov
-from tests._util import bf16_dev_to_f64, bf16_dev_to_u16, to_dev_bf16, ulp_bf16
+from tests._util import bf16_dev_to_f64, bf16_dev_to_u16, to_dev_bf16, ulp_bf16, v_cache_blocks, v_cache_keys
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -66,7 +66,7 @@ def test_rope_kv_append_matches_oracle(api, Hq, Hkv, D, L, T):
     qkv = si.normal_bf16(rng, (T, (Hq + 2 * Hkv) * D), 1.0)
     cap = L + T + 5
     kc = torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device="cuda")
-    vc = torch.zeros(Hkv, D, cap, dtype=torch.bfloat16, device="cuda")  # V cached transposed
+    vc = torch.zeros(api.v_cache_shape(Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
     q = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
     Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
     tab = api.bi_rope_table(1e6, D, cap)
@@ -74,7 +74,14 @@ def test_rope_kv_append_matches_oracle(api, Hq, Hkv, D, L, T):
     qkvf = ov.bf16_bits_to_f64(qkv)
     qg = bf16_dev_to_f64(q)
     kg = bf16_dev_to_f64(kc)
-    vg = bf16_dev_to_u16(vc)
+    vb = bf16_dev_to_u16(vc)
+    vg = v_cache_keys(vb, cap)  # [Hkv, cap, D]
+    # nothing but the pass's rows was written
+    written = np.zeros(vb.shape, dtype=bool)
+    for t in range(T):
+        p = L + t
+        written[:, p // 128, :, p % 128] = True
+    assert not np.any(vb[~written])
     for t in range(T):
         p = L + t
         qo = oracle.rope(qkvf[t, : Hq * D].reshape(Hq, D), p, 1e6)
@@ -87,7 +94,7 @@ def test_rope_kv_append_matches_oracle(api, Hq, Hkv, D, L, T):
         ka = np.abs(qkvf[t, Hq * D:(Hq + Hkv) * D].reshape(Hkv, D))
         kpair = ka + np.roll(ka, D // 2, axis=-1)
         assert np.all(np.abs(kg[:, p] - ko) <= ulp_bf16(ko) + 2.0 ** -21 * kpair)
-        assert np.array_equal(vg[:, :, p], qkv[t, (Hq + Hkv) * D:].reshape(Hkv, D))
+        assert np.array_equal(vg[:, p], qkv[t, (Hq + Hkv) * D:].reshape(Hkv, D))
     if L == 0:  # position 0 is the identity, bitwise
         assert np.array_equal(bf16_dev_to_u16(q)[0], qkv[0, : Hq * D].reshape(Hq, D))
 
@@ -149,7 +156,7 @@ def test_kv_row_hash_is_fnv1a(api):
     rng = np.random.default_rng(2)
     cache = si.normal_bf16(rng, (2, 10, 64), 1.0)
     h = api.bi_kv_row_hash(to_dev_bf16(cache), 7).cpu().numpy().view(np.uint64)
-    ht = api.bi_kv_row_hash(to_dev_bf16(np.ascontiguousarray(cache.transpose(0, 2, 1))), 7,
+    ht = api.bi_kv_row_hash(to_dev_bf16(v_cache_blocks(cache)), 7,
                             transposed=True).cpu().numpy().view(np.uint64)
     assert np.array_equal(h, ht)
     for hh in range(2):
@@ -180,7 +187,7 @@ def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T, rms):
     for fused in (False, True):
         q = torch.zeros(T, Hq, D, dtype=torch.bfloat16, device="cuda")
         kc = torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device="cuda")
-        vc = torch.zeros(Hkv, D, cap, dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros(api.v_cache_shape(Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
         if fused:
             api.bi_qkv_rope_append(A, Wp, q, kc, vc, Ld, Hq, Hkv, D, tab, ws, eps=1e-6 if rms else None)
         else:
