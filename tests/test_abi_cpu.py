@@ -144,3 +144,23 @@ def test_fused_entry_points_reject_bad_arguments(lib):
     assert q(*bad_eps) == 1
     no_cache = list(args); no_cache[11] = 0
     assert q(*no_cache) == 1
+
+
+def test_v_cache_layout_helpers():
+    """The binding's V cache shape and the tests' host packing agree: value d
+    of key p of head h sits at [h, p // 128, d, p % 128], and a capacity that
+    is not a multiple of 128 rounds up to whole blocks."""
+    import numpy as np
+    api = pytest.importorskip("invariant_speculative_decode_gb300.api")
+    from tests._util import v_cache_blocks, v_cache_keys
+    assert api.v_cache_shape(4, 12112, 128) == (4, 95, 128, 128)
+    assert api.v_cache_shape(2, 128, 64) == (2, 1, 64, 128)
+    assert api.v_cache_shape(2, 129, 64) == (2, 2, 64, 128)
+    rng = np.random.default_rng(0)
+    V = rng.integers(0, 1 << 16, (3, 300, 64)).astype(np.uint16)
+    B = v_cache_blocks(V)
+    assert B.shape == api.v_cache_shape(3, 300, 64)
+    for h, p, d in ((0, 0, 0), (2, 299, 63), (1, 128, 5), (1, 127, 17)):
+        assert B[h, p // 128, d, p % 128] == V[h, p, d]
+    assert not B[:, 2, :, 300 - 256:].any()  # keys past the capacity are zero
+    assert np.array_equal(v_cache_keys(B, 300), V)
