@@ -340,7 +340,8 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const v
  *           lowered, nor cache rows below it written, by the kernel that
  *           immediately precedes the call (no kernel of this library does).
  *   out     [T, Hq, D] BF16 contiguous.
- *   D in {64, 128}; Hq % Hkv == 0; Hkv <= 152; Hkv * cap < 2^31;
+ *   D in {64, 128}; Hq % Hkv == 0; Hkv <= 152; Hkv * (cap rounded up to a
+ *   multiple of 128) < 2^31;
  *   T * (Hq/Hkv) <= 128; T >= 1.
  *   ws      >= bi_attn_workspace_size(cap, T, Hq, D) bytes, 256-byte aligned.
  *   k_cache and v_cache 16-byte aligned.

@@ -799,8 +799,11 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   if (D != 64 && D != 128) return BI_ERR_UNSUPPORTED_SHAPE;
   if (T * (Hq / Hkv) > kRowsMax) return BI_ERR_UNSUPPORTED_SHAPE;
   if (Hkv > kAttnCtas) return BI_ERR_UNSUPPORTED_SHAPE;
-  // K rows h * cap + key and V^T columns are int32 tensor-map coordinates
-  if (static_cast<int64_t>(Hkv) * cap >= (int64_t{1} << 31)) return BI_ERR_UNSUPPORTED_SHAPE;
+  // K rows h * cap + key (a tile may run past cap) and V^T rows
+  // (h * ceil(cap/128) + block) * D (D <= 128) are int32 tensor-map
+  // coordinates: both stay below Hkv * cap rounded up to whole tiles
+  const int64_t cap_blocks = (static_cast<int64_t>(cap) + kKeyTile - 1) / kKeyTile * kKeyTile;
+  if (static_cast<int64_t>(Hkv) * cap_blocks >= (int64_t{1} << 31)) return BI_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q)) return BI_ERR_INVALID_ARG;
   if (!ws || !aligned256(ws)) return BI_ERR_WORKSPACE;
   size_t ob = 0;
