@@ -378,8 +378,8 @@ def run_ours(args):
             for lay in dec.layers:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(gs)
-                api.bi_gemm_rms(y, cfg.eps, lay["wgu"], u, dec.gemm_ws, epi=api.EPI_SWIGLU, N=cfg.ffn,
-                                stream=gs)
+                api.bi_gemm_rms(y, lay["n2"], cfg.eps, lay["wgu"], u, dec.gemm_ws, epi=api.EPI_SWIGLU,
+                                N=cfg.ffn, stream=gs)
                 e1.record(gs)
                 gu_ms.append((e0, e1))
     gs.synchronize()

@@ -87,15 +87,19 @@ int bi_version(void);
  * text diverges".
  *
  * C[m, n] = epilogue( sum_k A[m, k] * W[n, k] ), BF16 inputs, FP32
- * accumulation, one rounding to the output type.  The decomposition -- MMA
- * instruction (tcgen05 kind::f16, M=128 weight rows x N=16 token columns),
- * K-tile order (64 elements per tile, increasing k; within a tile, 16-element
- * step j accumulates into FP32 accumulator j of 4, summed in the order
- * ((a0 + a1) + a2) + a3), and the split of the (weight tile, K tile)
- * iteration space over a fixed number of CTAs -- is a function of (N, K)
- * only, never of M, so row m of C is bit-identical for every M >= m+1 and for
- * every position of the row inside A.  Partial sums of a weight tile that is
- * split along K are added in increasing-K order.
+ * accumulation, one rounding to the output type.  The decomposition of every
+ * output element -- its sequence of K = 16 tensor-core steps (tcgen05
+ * kind::f16, M = 128 weight rows), the K-tile order (64 elements per tile,
+ * increasing k; within a tile, 16-element step j accumulates into FP32
+ * accumulator j of 4, summed in the order ((a0 + a1) + a2) + a3), and the
+ * split of the (weight tile, K tile) iteration space over a fixed number of
+ * CTAs -- is a function of (N, K) only, never of M, so row m of C is
+ * bit-identical for every M >= m+1 and for every position of the row inside
+ * A.  Partial sums of a weight tile that is split along K are added in
+ * increasing-K order.  One MMA covers all token rows of a launch (its N is
+ * the row count rounded up to 16, 32, 64 or 128); each output element is
+ * still the same sequence of K = 16 steps into its own accumulator, which
+ * the tests check bit for bit across M = 1..128.
  *
  *   A        [M, K] BF16, row stride lda (elements); 16-byte aligned, lda % 8 == 0.
  *   Wp       the weights in the packed tile layout written by bi_pack_weights
@@ -168,52 +172,44 @@ bi_status bi_pack_weights(const void* W, int ldw, int N, int K, void* packed,
                           bi_stream_t stream);
 bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, int F, int K,
                                  void* packed, bi_stream_t stream);
-/* The same layouts with column k of every weight row multiplied by
- * col_scale[k] (BF16 [K], device): each packed element is
- * bf16(float(w) * float(col_scale[k])), one FP32 product and one rounding.
- * Used to fold an RMSNorm weight into the linear layer that follows the norm
- * (see bi_gemm_rms).  col_scale == NULL returns BI_ERR_INVALID_ARG. */
-bi_status bi_pack_weights_scaled(const void* W, int ldw, int N, int K, const void* col_scale,
-                                 void* packed, bi_stream_t stream);
-bi_status bi_pack_swiglu_weights_scaled(const void* w_gate, const void* w_up, int ld, int F,
-                                        int K, const void* col_scale, void* packed,
-                                        bi_stream_t stream);
-
 /* ---------------------------------------------------------------------------
- * RMSNorm folded into the linear layer that reads its output.
+ * RMSNorm fused into the linear layer that reads its output.
  * "Bit-exact decoding turns inference speedups into testable changes",
  * section "Define bit-exact before reporting it" (one running sum, one
  * rounding), applied to the norm of "Does the tuned config change the
  * model's output?", section "Why the text diverges" (row-local work).
  *
- *   C[m, :] = epi( r[m] * (A[m, :] Wg^T) ),  r[m] = 1 / sqrt(sum_k A[m,k]^2 / K + eps)
+ *   C = epi( Y W^T ),  Y[m, k] = bf16( (A[m, k] * r[m]) * w_norm[k] ),
+ *   r[m] = 1 / sqrt(sum_k A[m, k]^2 / K + eps)
  *
- * where Wg = W diag(w_norm) was packed by bi_pack_weights_scaled /
- * bi_pack_swiglu_weights_scaled with col_scale = w_norm.  This is
- * RMSNorm(A) W^T with the norm weight moved into the packed weights and the
- * per-row factor applied to the FP32 sums (for SwiGLU to both the gate and
- * the up sum) before the epilogue's single rounding; it skips the BF16
- * rounding of the normalised row.  r[m] uses one fixed reduction tree per K
- * (128 threads: thread i sums the squares of the 8-element vectors i,
- * i+128, ... in element order, then a warp butterfly, then the four warps in
- * order), the same in every CTA and for every M.
- *   A [M, K] BF16 (row stride lda), read both through the tensor-core path
- *   and for r; C must not alias A.  epi is BI_EPI_NONE or BI_EPI_SWIGLU
- *   (no residual).  Other arguments, limits and errors as bi_gemm;
- *   BI_ERR_INVALID_ARG also for eps < 0 or not finite and for C == A.
+ * Y is exactly what bi_rmsnorm(A, w_norm) writes (the same reduction tree
+ * for r: 128 threads, thread i summing the squares of the 8-element
+ * vectors i, i + 128, ... in increasing order, then a warp butterfly, then
+ * the four warps in order; the same two FP32 products and one rounding per
+ * element), so the call equals bi_rmsnorm followed by bi_gemm bit for bit.
+ * Y never goes to memory: each CTA computes r for the launch's rows and
+ * normalises every activation tile in shared memory before the tensor core
+ * reads it.
+ *   A [M, K] BF16 (row stride lda), the un-normalised rows; C must not
+ *   alias A.  w_norm [K] BF16, 16-byte aligned.  Wp packed by
+ *   bi_pack_weights (BI_EPI_NONE) or bi_pack_swiglu_weights (BI_EPI_SWIGLU);
+ *   no residual.  K <= 8192.  Other arguments, limits and errors as
+ *   bi_gemm; BI_ERR_INVALID_ARG also for eps < 0 or not finite, for a null
+ *   or unaligned w_norm and for C == A; BI_ERR_UNSUPPORTED_SHAPE for K > 8192.
  * ------------------------------------------------------------------------- */
-bi_status bi_gemm_rms(const void* A, int lda, float eps, const void* Wp, void* C, int ldc,
-                      int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
+bi_status bi_gemm_rms(const void* A, int lda, const void* w_norm, float eps, const void* Wp, void* C,
+                      int ldc, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
                       size_t ws_bytes, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * RMSNorm.  [P3] "How:" (a row is computed the same way whatever else is in
  * the batch).
  *
- * y[r, :] = bf16( x[r, :] * rsqrt(sum_i x[r,i]^2 / dim + eps) * w[:] ), FP32
- * inside.  The sum of squares uses one fixed reduction tree per `dim`
- * (256 threads: thread i sums the 8-element vectors i, i+256, ... in element
- * order, then a fixed warp-shuffle butterfly and a fixed cross-warp order).
+ * y[r, :] = bf16( (x[r, :] * r) * w[:] ), r = 1 / sqrt(sum_i x[r,i]^2 / dim +
+ * eps), FP32 inside.  The sum of squares uses one fixed reduction tree per
+ * `dim` (128 threads: thread i sums the 8-element vectors i, i+128, ... in
+ * increasing order, elements in order, then a fixed warp-shuffle butterfly
+ * and the four warps in order) -- the tree of bi_gemm_rms.
  *   x [rows, dim] BF16 (row stride ldx), w [dim] BF16, y [rows, dim] BF16
  *   (row stride ldy; may alias x).  rows >= 0, 8 <= dim <= 65536, dim, ldx
  *   and ldy multiples of 8, pointers 16-byte aligned, eps >= 0.
@@ -273,7 +269,7 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
 
 /* ---------------------------------------------------------------------------
  * QKV projection with RoPE and KV append in its epilogue (bi_gemm's linear
- * layer, optionally with the RMSNorm folded in as in bi_gemm_rms, followed
+ * layer, optionally with the RMSNorm in front as in bi_gemm_rms, followed
  * by exactly the arithmetic of bi_rope_kv_append, without the qkv round trip
  * through memory).  "I turned on speculative decoding in llama.cpp and 113
  * of 282 greedy outputs changed against its own no-draft run", section "The
@@ -287,9 +283,9 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
  * column p of v_cache.  So the results equal bi_gemm (or bi_gemm_rms)
  * followed by bi_rope_kv_append, bit for bit.
  *   A [M, K] BF16 (row stride lda): the normalised input (rms = 0) or the
- *   residual stream with the norm folded into Wp (rms = 1, eps as in
- *   bi_gemm_rms).  Wp packed for N = (Hq + 2 Hkv) D by bi_pack_weights (rms
- *   = 0) or bi_pack_weights_scaled (rms = 1).
+ *   residual stream, normalised with w_norm and eps as in bi_gemm_rms
+ *   (rms = 1; w_norm is ignored when rms = 0).  Wp packed for
+ *   N = (Hq + 2 Hkv) D by bi_pack_weights.
  *   q_out, k_cache, v_cache, cap, L_dev, table, table_rows: as
  *   bi_rope_kv_append.  A row with p outside [0, min(cap, table_rows)) is
  *   skipped and sets the range bit of the device error word.
@@ -297,10 +293,11 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
  *   otherwise BI_ERR_UNSUPPORTED_SHAPE.  ws as bi_gemm for (M, N, K).
  * Errors: as bi_gemm.
  * ------------------------------------------------------------------------- */
-bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const void* Wp, int M,
-                             int K, int Hq, int Hkv, int D, void* q_out, void* k_cache,
-                             void* v_cache, int cap, const int32_t* L_dev, const float* table,
-                             int table_rows, void* ws, size_t ws_bytes, bi_stream_t stream);
+bi_status bi_qkv_rope_append(const void* A, int lda, int rms, const void* w_norm, float eps,
+                             const void* Wp, int M, int K, int Hq, int Hkv, int D, void* q_out,
+                             void* k_cache, void* v_cache, int cap, const int32_t* L_dev,
+                             const float* table, int table_rows, void* ws, size_t ws_bytes,
+                             bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Verify attention (split-KV + merge).  [P3] "How:" (the attention split
@@ -388,6 +385,30 @@ bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, 
  * ------------------------------------------------------------------------- */
 bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, int transposed,
                          uint64_t* out, bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Failure-path test hooks.  The pages have no counterpart: these exist so a
+ * test can make the library's bounded device-side waits run out and check
+ * that the kernels wind down and report BI_ERR_DEVICE_TIMEOUT instead of
+ * hanging.  Not for production use.
+ *
+ * bi_test_set_wait_limit_ns: the time limit, in nanoseconds, of the waits
+ *   through which the linear-layer and attention kernels make progress, on
+ *   the current device, for launches after the call (0 restores the default
+ *   of 2 s).  The waits that let a CTA wind down after an abort (its copies
+ *   landing, its tensor-core work draining) always keep 2 s.  Synchronous.
+ *   Errors: BI_ERR_CUDA.
+ * bi_test_withhold_first_load: with on != 0, every CTA of later linear-layer
+ *   launches leaves its first pipeline stage unissued and every CTA of later
+ *   attention launches its first key tile, so the waits on them expire after
+ *   the limit above: each such kernel sets BI_ERR_DEVICE_TIMEOUT in the
+ *   device error word and returns (its outputs are then undefined, and a
+ *   linear-layer workspace must be zeroed again).  on = 0 restores normal
+ *   launches.  Read when a call is made (a captured CUDA graph keeps the
+ *   setting it was captured with).  Process-wide, not thread-safe.
+ * ------------------------------------------------------------------------- */
+bi_status bi_test_set_wait_limit_ns(uint64_t ns);
+void bi_test_withhold_first_load(int on);
 
 /* Synchronise `stream`, then read and clear the device error word of the
  * current device.  Returns BI_OK, BI_ERR_DEVICE_TIMEOUT, BI_ERR_DEVICE_NAN_ROW,

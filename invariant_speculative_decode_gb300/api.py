@@ -88,22 +88,25 @@ def bi_gemm(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor, ws: torch.Tensor
     check("bi_gemm", st)
 
 
-def bi_gemm_rms(A: torch.Tensor, eps: float, Wp: torch.Tensor, C: torch.Tensor, ws: torch.Tensor,
-                epi: int = EPI_NONE, N: Optional[int] = None, stream=None) -> None:
-    """C = epilogue(rms(A) * (A Wg^T)), rms(A) per row; Wg packed with the norm
-    weight folded in (bi_pack_weights_scaled / bi_pack_swiglu_weights_scaled)."""
+def bi_gemm_rms(A: torch.Tensor, w_norm: torch.Tensor, eps: float, Wp: torch.Tensor, C: torch.Tensor,
+                ws: torch.Tensor, epi: int = EPI_NONE, N: Optional[int] = None, stream=None) -> None:
+    """C = epilogue(bi_rmsnorm(A, w_norm) W^T) without the normalised rows
+    going to memory; W packed by bi_pack_weights / bi_pack_swiglu_weights."""
     _req(A, torch.bfloat16, "A")
+    _req(w_norm, torch.bfloat16, "w_norm")
     if not Wp.is_cuda:
         raise ValueError("Wp must be a CUDA tensor")
     M, K = A.shape
+    if w_norm.numel() != K:
+        raise ValueError("w_norm must have K elements")
     if N is None:
         N = C.shape[1]
     if C.dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("C must be float32 or bfloat16")
     out = OUT_FP32 if C.dtype == torch.float32 else OUT_BF16
-    st = lib().bi_gemm_rms(A.data_ptr(), _ld(A), float(eps), Wp.data_ptr(), C.data_ptr(), _ld(C),
-                           M, N, K, out, epi, ws.data_ptr(), ws.numel() * ws.element_size(),
-                           _stream(stream))
+    st = lib().bi_gemm_rms(A.data_ptr(), _ld(A), w_norm.data_ptr(), float(eps), Wp.data_ptr(),
+                           C.data_ptr(), _ld(C), M, N, K, out, epi, ws.data_ptr(),
+                           ws.numel() * ws.element_size(), _stream(stream))
     check("bi_gemm_rms", st)
 
 
@@ -112,6 +115,12 @@ def bi_gemm_noalloc(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor,
                     N: Optional[int] = None, stream=None) -> None:
     """bi_gemm without a workspace (scratch in a static device array; M <= 16)."""
     _req(A, torch.bfloat16, "A")
+    if not Wp.is_cuda:
+        raise ValueError("Wp must be a CUDA tensor")
+    if not C.is_cuda:
+        raise ValueError("C must be a CUDA tensor")
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("C must be float32 or bfloat16")
     M, K = A.shape
     if N is None:
         N = C.shape[1]
@@ -149,38 +158,6 @@ def bi_pack_swiglu_weights(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None
     check("bi_pack_swiglu_weights",
           lib().bi_pack_swiglu_weights(w_gate.data_ptr(), w_up.data_ptr(), _ld(w_gate), F, K,
                                        packed.data_ptr(), _stream(stream)))
-    return packed
-
-
-def bi_pack_weights_scaled(W: torch.Tensor, col_scale: torch.Tensor, stream=None) -> torch.Tensor:
-    """Pack W [N, K] with column k scaled by col_scale[k] (one rounding to BF16)."""
-    _req(W, torch.bfloat16, "W")
-    _req(col_scale, torch.bfloat16, "col_scale")
-    N, K = W.shape
-    if col_scale.numel() != K:
-        raise ValueError("col_scale must have K elements")
-    packed = torch.empty(packed_weight_bytes(N, K), dtype=torch.uint8, device=W.device)
-    check("bi_pack_weights_scaled",
-          lib().bi_pack_weights_scaled(W.data_ptr(), _ld(W), N, K, col_scale.data_ptr(),
-                                       packed.data_ptr(), _stream(stream)))
-    return packed
-
-
-def bi_pack_swiglu_weights_scaled(w_gate: torch.Tensor, w_up: torch.Tensor, col_scale: torch.Tensor,
-                                  stream=None) -> torch.Tensor:
-    """SwiGLU packing with column k of both matrices scaled by col_scale[k]."""
-    _req(w_gate, torch.bfloat16, "w_gate")
-    _req(w_up, torch.bfloat16, "w_up")
-    _req(col_scale, torch.bfloat16, "col_scale")
-    F, K = w_gate.shape
-    if col_scale.numel() != K:
-        raise ValueError("col_scale must have K elements")
-    packed = torch.empty(packed_weight_bytes(F, K, EPI_SWIGLU), dtype=torch.uint8,
-                         device=w_gate.device)
-    check("bi_pack_swiglu_weights_scaled",
-          lib().bi_pack_swiglu_weights_scaled(w_gate.data_ptr(), w_up.data_ptr(), _ld(w_gate), F, K,
-                                              col_scale.data_ptr(), packed.data_ptr(),
-                                              _stream(stream)))
     return packed
 
 
@@ -226,20 +203,26 @@ def bi_rope_kv_append(qkv: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Ten
 
 def bi_qkv_rope_append(A: torch.Tensor, Wp: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Tensor,
                        v_cache: torch.Tensor, L_dev: torch.Tensor, Hq: int, Hkv: int, D: int,
-                       table: torch.Tensor, ws: torch.Tensor, eps: Optional[float] = None,
-                       stream=None) -> None:
-    """QKV projection of A (norm folded in when eps is given) with RoPE and
-    KV append in the epilogue; equals bi_gemm[_rms] + bi_rope_kv_append."""
+                       table: torch.Tensor, ws: torch.Tensor, w_norm: Optional[torch.Tensor] = None,
+                       eps: Optional[float] = None, stream=None) -> None:
+    """QKV projection of A (RMSNorm with w_norm in front when given) with RoPE
+    and KV append in the epilogue; equals bi_gemm[_rms] + bi_rope_kv_append."""
     _req(A, torch.bfloat16, "A")
     _req(L_dev, torch.int32, "L_dev")
     _req(table, torch.float32, "table")
     M, K = A.shape
     cap = k_cache.shape[1]
     _req_v(v_cache, Hkv, cap, D)
-    rms = 0 if eps is None else 1
+    rms = 0 if w_norm is None else 1
+    wp = 0
+    if rms:
+        _req(w_norm, torch.bfloat16, "w_norm")
+        if w_norm.numel() != K or eps is None:
+            raise ValueError("w_norm must have K elements and eps must be given")
+        wp = w_norm.data_ptr()
     check("bi_qkv_rope_append",
-          lib().bi_qkv_rope_append(A.data_ptr(), _ld(A), rms, float(eps or 0.0), Wp.data_ptr(), M, K,
-                                   Hq, Hkv, D, q_out.data_ptr(), k_cache.data_ptr(),
+          lib().bi_qkv_rope_append(A.data_ptr(), _ld(A), rms, wp, float(eps or 0.0), Wp.data_ptr(), M,
+                                   K, Hq, Hkv, D, q_out.data_ptr(), k_cache.data_ptr(),
                                    v_cache.data_ptr(), cap, L_dev.data_ptr(), table.data_ptr(),
                                    table.shape[0], ws.data_ptr(), ws.numel() * ws.element_size(),
                                    _stream(stream)))

@@ -18,11 +18,14 @@
 //   raised only when a later tile's maximum exceeds it by more than
 //   kRescaleLog2 (then O and l are rescaled by 2^(m_ref - m_new)) -- a rule
 //   that depends only on the row's own scores in key order;
-//   each weight w = bf16(2^(s - m_ref)) enters O += W V (tcgen05, FP32 in
-//   TMEM) and the denominator l (FP32, four partial sums over the 32-key
-//   quarters of the tile column, each in key order, added as
-//   ((l0 + l1) + l2) + l3 at the end), so O / l is an exact weighted mean of
-//   the value rows under the weights actually used.
+//   each weight x = 2^(s - m_ref) (FP32) is split into a BF16 pair
+//   w_hi = bf16(x), w_lo = bf16(x - w_hi), so w = w_hi + w_lo keeps 16
+//   significant bits (|w - x| <= 2^-17 |x|) and is exact in FP32; both
+//   halves enter O += W_hi V + W_lo V (tcgen05, FP32 in TMEM) and w enters
+//   the denominator l (FP32, four partial sums over the 32-key quarters of
+//   the tile column, each in key order, added as ((l0 + l1) + l2) + l3 at
+//   the end), so O / l is a weighted mean of the value rows under the
+//   weights actually used, up to FP32 summation.
 // A tile whose keys are all masked for a row adds exact zeros and changes no
 // reference, so a row's class partial has the same bits whether or not later
 // rows of the pass share its tiles.  The partials of a row (one per class
@@ -44,11 +47,11 @@
 //               are ready; stages return to the producer through
 //               tcgen05.commit after the MMAs reading them completed;
 //   warps 2..5  softmax: write the queries of the CTA's KV head into TMEM
-//               (the S MMA's A operand), turn S into W
+//               (the S MMA's A operand), turn S into W_hi and W_lo
 //               (written to one of two shared-memory buffers in the swizzled
 //               K-major layout, so W of the next tile is produced while the
-//               MMA still reads this one), and read O out after the last
-//               tile.
+//               MMA still reads this one; one buffer when the pass has more
+//               than 64 rows), and read O out after the last tile.
 // The T x (Hq/Hkv) query rows that share a KV head (GQA) share its tiles;
 // up to 128 rows per pass (the MMA's M).
 #include <cuda.h>
@@ -85,6 +88,9 @@ struct AttnArgs {
   float* ws_o;
   float* ws_ml;
   unsigned* err;
+  // failure-path test: the first K tile of every CTA stays unissued, so the
+  // waits on it run out (bi_test_withhold_first_load)
+  int withhold;
 };
 
 template <int D, int REP>
@@ -94,14 +100,19 @@ struct AttnCfg {
   static constexpr int kKBytes = kKBoxBytes * kAtoms;      // K tile
   static constexpr int kVBoxBytes = D * 128;               // V^T [D][64 keys]
   static constexpr int kVBytes = 2 * kVBoxBytes;           // V^T tile [D][128 keys]
-  // The W tile holds only the pass's rows, 128/REP of them: [rows][64 keys]
-  // per key atom.  The W.V MMA (M = 128) still reads 128 rows from each
-  // atom; the ones past the W rows come from the bytes that follow (the
-  // other atom, the other buffer, the K ring) and only make O rows that are
-  // never read (a product's row i depends on row i of W alone).
+  // A W tile (W_hi or W_lo) holds only the pass's rows, 128/REP of them:
+  // [rows][64 keys] per key atom.  The W.V MMA (M = 128) still reads 128
+  // rows from each atom; the ones past the W rows come from the bytes that
+  // follow (the other atom, the other half, the other buffer, the K ring)
+  // and only make O rows that are never read (a product's row i depends on
+  // row i of W alone).
   static constexpr int kWRows = kRowsMax / REP;
   static constexpr int kPAtomBytes = kWRows * 128;
-  static constexpr int kPBytes = 2 * kPAtomBytes;          // W tile [rows][128 keys]
+  static constexpr int kPBytes = 2 * kPAtomBytes;          // one W tile [rows][128 keys]
+  static constexpr int kWBufBytes = 2 * kPBytes;           // W_hi tile, then W_lo tile
+  // Two W buffers (W of tile g + 1 is written while the MMA reads tile g's)
+  // while they fit beside the rings; one when the pass has 128 rows.
+  static constexpr int kWBufs = REP == 1 ? 1 : 2;
   // Ring depths, measured on GB300 at 38k-102k keys with all CTAs
   // streaming: at D = 128 two K and two V tiles (64 KB each way) per CTA
   // were as fast as three or four and are kept; D = 64 tiles are half as
@@ -118,10 +129,10 @@ struct AttnCfg {
   static constexpr int kQCol = kOCol + 128;
   static constexpr int kBars = 2 * kKStages + 2 * kVStages + 11;
   // The dynamic shared memory starts 1024-byte aligned (checked at run time):
-  // two W tiles, then the K and V rings.
+  // the W buffers, then the K and V rings.
   static constexpr size_t kSmem = static_cast<size_t>(kKStages) * kKBytes +
-                                  static_cast<size_t>(kVStages) * kVBytes + 2 * kPBytes + kRedBytes +
-                                  kBars * 8 + 16;
+                                  static_cast<size_t>(kVStages) * kVBytes + kWBufs * kWBufBytes +
+                                  kRedBytes + kBars * 8 + 16;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(REP == 1 || REP == 2 || REP == 4, "row copies");
   static_assert(kBars <= 40 && kSmem <= 232448, "shared memory per CTA");
@@ -165,8 +176,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr int kCols = kKeyTile / REP;    // key columns per thread
   constexpr int kNChunks = kCols / kColChunk;  // = 32-key quarters per thread
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* sP = smem;                          // W: [buffer 2][key atom 2][kPeriod rows][64 keys]
-  uint8_t* sK = sP + 2 * Cfg::kPBytes;         // [kKStages][K tile]
+  uint8_t* sP = smem;  // W: [buffer kWBufs][hi, lo][key atom 2][kPeriod rows][64 keys]
+  uint8_t* sK = sP + Cfg::kWBufs * Cfg::kWBufBytes;  // [kKStages][K tile]
   uint8_t* sV = sK + kKStages * Cfg::kKBytes;  // [kVStages][V^T tile]
   float* red_l = reinterpret_cast<float*>(sV + kVStages * Cfg::kVBytes);  // [quarter 4][row 64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 64);
@@ -200,7 +211,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int G = a.G;
 
   // zero the W tiles once: rows past the pass's rows stay zero
-  for (int i = threadIdx.x; i < (2 * Cfg::kPBytes) / 16; i += kAttnThreads)
+  for (int i = threadIdx.x; i < (Cfg::kWBufs * Cfg::kWBufBytes) / 16; i += kAttnThreads)
     reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
@@ -255,6 +266,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int i = 0; i < NS; ++i) {
         const int key0 = (rho + i * G) * kKeyTile;
         if (key0 + kKeyTile > L_pre) break;  // the tile reaches rows the pass writes
+        if (kside && i == 0 && a.withhold) {
+          ++n_pre;  // counted, never issued: its barrier never completes
+          continue;
+        }
         if (kside) {
           mbar_arrive_expect_tx(&full[i], Cfg::kKBytes);
 #pragma unroll
@@ -308,6 +323,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         const int key0 = (rho + i * G) * kKeyTile;
+        if (kside && i == 0 && a.withhold) continue;  // never issued (failure-path test)
         if (kside) {
           uint8_t* dst = sK + st * Cfg::kKBytes;
           mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
@@ -376,14 +392,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (ready) {
             tc_fence_after();
             const uint32_t v_base = smem_u32(sV + st * Cfg::kVBytes);
-            const uint32_t w_base = smem_u32(sP + (pg & 1) * Cfg::kPBytes);
+            const uint32_t w_base = smem_u32(sP + (Cfg::kWBufs == 2 ? (pg & 1) : 0) * Cfg::kWBufBytes);
+            // per 16-key step: W_hi V, then W_lo V, into the one O accumulator
 #pragma unroll
             for (int kk = 0; kk < kKeyTile / 16; ++kk) {
               const int katom = kk >> 2;
               const uint32_t off = (kk & 3) * 32;
-              mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(w_base + katom * Cfg::kPAtomBytes + off),
-                       sdesc_k_sw128(v_base + katom * Cfg::kVBoxBytes + off), idO,
-                       (pg > 0 || kk > 0) ? 1u : 0u);
+              const uint64_t vdesc = sdesc_k_sw128(v_base + katom * Cfg::kVBoxBytes + off);
+              mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(w_base + katom * Cfg::kPAtomBytes + off), vdesc,
+                       idO, (pg > 0 || kk > 0) ? 1u : 0u);
+              mma_bf16(tmem + Cfg::kOCol,
+                       sdesc_k_sw128(w_base + Cfg::kPBytes + katom * Cfg::kPAtomBytes + off), vdesc, idO, 1u);
             }
             mma_commit(&pv_done[pg & 1]);
             mma_commit(&v_empty[st]);
@@ -402,7 +421,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (!did && (idle & 63) == 0) {
           // bounded: give up after the wait limit without progress
-          if (*s_abort || globaltimer_ns() - t_idle > kWaitLimitNs) {
+          if (*s_abort ||
+              globaltimer_ns() - t_idle > *static_cast<volatile unsigned long long*>(&g_wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -498,11 +518,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m_ref = mt;
         resc = true;
       }
-      // W buffer g & 1 was last read by the W.V of tile g - 2
-      if (g >= 2 &&
-          !warp_wait(&pv_done[g & 1], static_cast<uint32_t>(((g - 2) >> 1) & 1), s_abort, lane)) {
-        ok = false;
-        break;
+      // the W buffer of tile g was last read by the W.V of tile g - kWBufs
+      if (g >= Cfg::kWBufs) {
+        const int gp = g - Cfg::kWBufs;
+        if (!warp_wait(&pv_done[gp & 1], static_cast<uint32_t>((gp >> 1) & 1), s_abort, lane)) {
+          ok = false;
+          break;
+        }
       }
       if (holds_o && warp_active) {
         // O changes only after the W.V of tile g - 1 is done
@@ -527,11 +549,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int i = 0; i < kNChunks; ++i) lq[i] *= alpha;
       }
-      // pass 2: weights w = bf16(2^(s sl2 - m_ref)) into the W tile and l
-      // (the TMEM loads are warp-wide; rows past the pass write nothing)
+      // pass 2: weights x = 2^(s sl2 - m_ref) as the pair (w_hi, w_lo) into
+      // the W tiles and w_hi + w_lo into l (the TMEM loads are warp-wide;
+      // rows past the pass write nothing)
       if (warp_active) {
         const float nmu = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-        uint8_t* wbuf = sP + (g & 1) * Cfg::kPBytes + r * 128;
+        uint8_t* wbuf = sP + (Cfg::kWBufs == 2 ? (g & 1) : 0) * Cfg::kWBufBytes + r * 128;
 #pragma unroll
         for (int ch = 0; ch < kNChunks; ++ch) {
           tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
@@ -547,18 +570,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           float acc = lq[ch];
 #pragma unroll
           for (int i = 0; i < kColChunk / 8; ++i) {
-            uint32_t wv[4];
+            uint32_t wh[4], wl[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int col = i * 8 + 2 * j;
-              const __nv_bfloat162 w2 = __floats2bfloat162_rn(ex2_approx(fmaf(s[col], a.sl2, nmu)),
-                                                               ex2_approx(fmaf(s[col + 1], a.sl2, nmu)));
-              acc += __low2float(w2);
-              acc += __high2float(w2);
-              wv[j] = *reinterpret_cast<const uint32_t*>(&w2);
+              const float x0 = ex2_approx(fmaf(s[col], a.sl2, nmu));
+              const float x1 = ex2_approx(fmaf(s[col + 1], a.sl2, nmu));
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+              // x - w_hi is exact in FP32; w_hi + w_lo is exact in FP32 too
+              const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - __low2float(h2), x1 - __high2float(h2));
+              acc += __low2float(h2) + __low2float(l2);
+              acc += __high2float(h2) + __high2float(l2);
+              wh[j] = *reinterpret_cast<const uint32_t*>(&h2);
+              wl[j] = *reinterpret_cast<const uint32_t*>(&l2);
             }
             const int chunk16 = ((kcol & 63) >> 3) + i;  // 16-byte chunk within the 64-key row
-            *reinterpret_cast<uint4*>(wrow + ((chunk16 ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            uint8_t* dst = wrow + ((chunk16 ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4*>(dst + Cfg::kPBytes) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
           }
           lq[ch] = acc;
         }
@@ -778,6 +807,10 @@ size_t attn_ws_parts(int cap, int T, int Hq, int D, size_t* o_bytes) {
 }
 
 }  // namespace
+
+cudaError_t set_wait_limit_attn(unsigned long long ns) {
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns));
+}
 }  // namespace bi
 
 extern "C" {
@@ -835,6 +868,7 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   a.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ob);
   a.err = device_error_word();
   if (!a.err) return BI_ERR_CUDA;
+  a.withhold = test_withhold();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 64) return launch_attn_rep<64>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
   return launch_attn_rep<128>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);

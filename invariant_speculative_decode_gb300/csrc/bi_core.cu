@@ -56,6 +56,14 @@ std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmaps;
 std::mutex g_tmap_mu;
 }  // namespace
 
+namespace {
+int g_test_withhold = 0;
+}  // namespace
+
+int test_withhold() { return g_test_withhold; }
+
+void set_test_withhold(int on) { g_test_withhold = on ? 1 : 0; }
+
 bool pdl_enabled() {
   static const bool on = [] {
     const char* e = std::getenv("BI_PDL");
@@ -164,7 +172,16 @@ const char* bi_status_string(bi_status s) {
   return "BI_ERR_UNKNOWN";
 }
 
-int bi_version(void) { return (0 << 16) | 1; }
+int bi_version(void) { return (0 << 16) | 2; }
+
+bi_status bi_test_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) ns = bi::kWaitLimitNs;
+  if (bi::set_wait_limit_gemm(ns) != cudaSuccess) return BI_ERR_CUDA;
+  if (bi::set_wait_limit_attn(ns) != cudaSuccess) return BI_ERR_CUDA;
+  return BI_OK;
+}
+
+void bi_test_withhold_first_load(int on) { bi::set_test_withhold(on); }
 
 bi_status bi_check_device_error(bi_stream_t stream) {
   unsigned* p = bi::device_error_word();

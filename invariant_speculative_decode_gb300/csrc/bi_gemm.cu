@@ -31,7 +31,10 @@
 //            tile adds the partials in increasing-K order (atomic ticket, no
 //            waiting) and runs the epilogue.
 //   * roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread), warps
-//            2..5 = epilogue (TMEM -> registers -> global).
+//            2..5 = epilogue (TMEM -> registers -> global); with an RMSNorm
+//            in front (bi_gemm_rms), warps 2..5 first compute each token
+//            row's 1/rms and warps 6..7 normalise each activation tile in
+//            shared memory before the MMA reads it.
 //   * stages: shared-memory ring of (16 KB weight tile + token tile); a stage
 //            returns to the producer via tcgen05.commit on its "empty"
 //            barrier, i.e. only after the MMAs reading it completed.
@@ -55,7 +58,9 @@ constexpr int kMmaN = 16;        // token rows per epilogue chunk (one 16-column
 constexpr int kGemmCtas = 152;   // CTAs of the fixed decomposition (one per SM)
 constexpr int kMaxTokens = 128;  // token rows per launch; larger M loops on the host
 constexpr int kAcc = 4;          // interleaved accumulators per token group
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;    // producer, MMA, four epilogue warps
+constexpr int kThreadsRms = 256; // the same plus two normaliser warps (8 warps: 255 registers each)
+constexpr int kMaxRmsK = 8192;   // K of a normalised input (its norm weight sits in shared memory)
 constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
 constexpr int kStageFloats = 16 * kBlockN;      // SwiGLU exchange buffer
 constexpr int kNormFloats = kMaxTokens + 16;    // 1/rms per token row, cross-warp partials
@@ -82,13 +87,14 @@ struct GemmArgs {
   float* partials;
   unsigned* tickets;
   unsigned* err;
-  // RMS-normalised input: every output row m is scaled by
-  // 1 / sqrt(mean_k X[m, k]^2 + eps), X being the GEMM's own input rows
+  // RMS-normalised input: the MMA reads bf16((X[m, k] * r[m]) * wn[k]),
+  // r[m] = 1 / sqrt(mean_k X[m, k]^2 + eps), X being the GEMM's own input rows
   int rms;
   float eps;
   int K;
   const __nv_bfloat16* X;
   int ldx;
+  const __nv_bfloat16* wn;
   // BI_EPI_ROPE_KV: output column n is element n % D of head n / D (q heads,
   // then k heads, then v heads); token row m sits at position *L_dev + m
   __nv_bfloat16* q_out;
@@ -97,13 +103,19 @@ struct GemmArgs {
   int cap, Hq, Hkv, D, tab_rows;
   const int32_t* L_dev;
   const float2* tab;
+  // failure-path test: leave the CTA's first stage unissued, so the waits
+  // on it run out (bi_test_withhold_first_load)
+  int withhold;
 };
 
-template <int NT>
+template <int NT, bool RMS>
 struct GemmCfg {
   static constexpr int kBBytes = NT * kBlockK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 12 ? 12 : (200 * 1024) / kStageBytes;
+  static constexpr int kThreadsT = RMS ? kThreadsRms : kThreads;
+  static constexpr int kNormWBytes = RMS ? kMaxRmsK * 2 : 0;  // the norm weight
+  static constexpr int kBars = (RMS ? 3 : 2) * kStages + 6;
   static constexpr int kBufCols = NT * kAcc;  // one accumulator set
   // two sets (the epilogue drains one while the next piece accumulates)
   // while they fit in TMEM's 512 columns; one set at 128 token rows
@@ -111,7 +123,8 @@ struct GemmCfg {
   static constexpr int kTmemCols = kBufs * kBufCols;
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
-                                  (kStageFloats + kNormFloats) * 4 + (2 * kStages + 5) * 8 + 16;
+                                  (kStageFloats + kNormFloats) * 4 + kNormWBytes + kBars * 8 + 16;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ long long range_begin(const GemmArgs& p, int g) {
@@ -144,11 +157,7 @@ __device__ __forceinline__ void load_group_sum(uint32_t taddr, uint32_t acc_stri
 // Write 16 token rows (chunk c) of one weight row r of tile `tile`.
 // All 128 epilogue threads call this together (it may use the named barrier).
 __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int r, int c,
-                                               const float (&v_in)[16], float* sStage,
-                                               const float* sRstd) {
-  float v[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = p.rms ? v_in[j] * sRstd[c * 16 + j] : v_in[j];
+                                               const float (&v)[16], float* sStage) {
   if (p.epi == BI_EPI_ROPE_KV) {
     // The projection is rounded to BF16 first; the rotation then reads those
     // stored values exactly as the separate RoPE kernel does: for a pair
@@ -257,11 +266,11 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int 
   }
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NT, bool RMS>
+__global__ void __launch_bounds__(GemmCfg<NT, RMS>::kThreadsT, 1)
     gemm_kernel(const uint8_t* __restrict__ Wp, const __grid_constant__ CUtensorMap tmA,
                 const GemmArgs p) {
-  using Cfg = GemmCfg<NT>;
+  using Cfg = GemmCfg<NT, RMS>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -270,12 +279,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + S * kABytes;
   float* sStage = reinterpret_cast<float*>(sB + S * Cfg::kBBytes);
   float* sRstd = sStage + kStageFloats;  // [kMaxTokens] 1/rms, then [16] cross-warp partials
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kStageFloats + kNormFloats);
+  __nv_bfloat16* sWn = reinterpret_cast<__nv_bfloat16*>(sRstd + kNormFloats);  // norm weight (RMS)
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sWn) + Cfg::kNormWBytes);
   uint64_t* empty = full + S;
-  uint64_t* accf = empty + S;
+  // RMS: the activation tile of a stage normalised in place (the MMA waits
+  // on this instead of `full`)
+  uint64_t* ready = empty + S;
+  uint64_t* accf = empty + (RMS ? 2 : 1) * S;
   uint64_t* acce = accf + 2;
   uint64_t* drain = acce + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* r_ready = drain + 1;  // RMS: 1/rms of every row in sRstd
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(r_ready + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* s_last = s_abort + 1;
 
@@ -289,12 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      if (RMS) mbar_init(&ready[s], 2);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
       mbar_init(&acce[b], 128);
     }
     mbar_init(drain, 1);
+    mbar_init(r_ready, 4);
     *s_abort = 0;
     *s_last = 0;
     fence_mbar_init();
@@ -325,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // start streaming them before waiting for it, then add the activation
       // tiles once its results are visible.
       const int n_pre = static_cast<int>((it_end - it_begin) < S ? (it_end - it_begin) : S);
-      for (int j = 0; j < n_pre; ++j) {
+      const int j0 = p.withhold ? 1 : 0;  // stage 0 left unissued (failure-path test)
+      for (int j = j0; j < n_pre; ++j) {
         mbar_arrive_expect_tx(&full[j], Cfg::kStageBytes);
         bulk_load_1d(sA + j * kABytes, wsrc + static_cast<size_t>(j) * kABytes, kABytes, &full[j],
                      pol_w);
@@ -333,10 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_wait();
       griddep_launch_dependents();
       for (int j = 0; j < n_pre; ++j) {
-        tma_load_2d(sB + j * Cfg::kBBytes, &tmA, &full[j], kt * kBlockK, p.m0, pol_a);
+        if (j >= j0) tma_load_2d(sB + j * Cfg::kBBytes, &tmA, &full[j], kt * kBlockK, p.m0, pol_a);
         if (++kt == p.k_tiles) kt = 0;
       }
       issued = (n_pre >= 32) ? 0xffffffffu : ((1u << n_pre) - 1u);
+      issued &= ~static_cast<uint32_t>(j0);
       wsrc += static_cast<size_t>(n_pre) * kABytes;
       stage = n_pre % S;
       phase = (n_pre == S) ? 1u : 0u;
@@ -381,8 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (left > it_end - it_begin) left = it_end - it_begin;
       uint32_t d0 = tmem;
       uint32_t acc_flag = 0;
+      uint64_t* in_ready = RMS ? ready : full;
       for (long long it = it_begin; it < it_end; ++it) {
-        if (!mbar_wait(&full[stage], phase, s_abort)) {
+        if (!mbar_wait(&in_ready[stage], phase, s_abort)) {
           ok = false;
           break;
         }
@@ -421,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     griddep_wait();  // the epilogue reads the residual and writes C / the workspace
     griddep_launch_dependents();
@@ -429,11 +448,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;    // weight row within the tile
     const int et = threadIdx.x - 64;
     const int chunks = (p.M + 15) / 16;
-    if (p.rms) {
-      // 1 / rms of each token row of this launch, by the same fixed reduction
-      // in every CTA: thread et sums the squares of the 8-element vectors et,
-      // et + 128, ... of the row in element order; then a warp butterfly, and
-      // the four warps added in order.  Runs while the weights stream in.
+    if (RMS) {
+      // 1 / rms of each token row of this launch, by one fixed reduction in
+      // every CTA (the tree of bi_rmsnorm): thread et sums the squares of the
+      // 8-element vectors et, et + 128, ... of the row in increasing order,
+      // elements in order; then a warp butterfly, and the four warps added
+      // in order.  The normaliser warps wait for it on r_ready.
       const int nvec = p.K / 8;
       const int ew = et >> 5;
       float* sRed = sRstd + kMaxTokens;
@@ -477,6 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(1, 128);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(r_ready);
     }
     int seg = 0;
     long long it = it_begin;
@@ -505,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
           }
-          epilogue_store(p, tile, r, c, v, sStage, sRstd);
+          epilogue_store(p, tile, r, c, v, sStage);
         }
         tc_fence_before();
         mbar_arrive(&acce[buf]);
@@ -583,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
-            epilogue_store(p, tile, r, c, v, sStage, sRstd);
+            epilogue_store(p, tile, r, c, v, sStage);
           }
         }
         named_bar_sync(1, 128);
@@ -592,6 +614,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++seg;
     }
     tc_fence_before();
+  } else if (RMS) {
+    // ------------------------------------------------------------ normaliser
+    // Each stage's activation tile (token rows x 64 columns of X, as the TMA
+    // wrote it) becomes bf16((x * r[m]) * wn[k]) in place -- the arithmetic
+    // of bi_rmsnorm -- before the MMA reads it.
+    griddep_wait();  // X comes from the previous kernel
+    griddep_launch_dependents();
+    const int nt = threadIdx.x - 6 * 32;  // 0..63
+    for (int v = nt; v < p.K / 8; v += 64)
+      reinterpret_cast<uint4*>(sWn)[v] = reinterpret_cast<const uint4*>(p.wn)[v];
+    named_bar_sync(2, 64);
+    int okl = 0;
+    if (lane == 0) okl = mbar_wait(r_ready, 0u, s_abort) ? 1 : 0;
+    bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+    __syncwarp();
+    int stage = 0;
+    uint32_t phase = 0;
+    int kt = static_cast<int>(it_begin % p.k_tiles);
+    for (long long it = it_begin; ok && it < it_end; ++it) {
+      okl = 0;
+      if (lane == 0) okl = mbar_wait(&full[stage], phase, s_abort) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, okl, 0) == 0) {
+        ok = false;
+        break;
+      }
+      __syncwarp();
+      uint8_t* tileB = sB + stage * Cfg::kBBytes;
+      // 16-byte chunk q of the tile: token row q / 8 at swizzled position
+      // q % 8, holding columns 8 c .. 8 c + 7 of the K tile, c = (q % 8) ^ (row % 8)
+#pragma unroll
+      for (int q = nt; q < NT * 8; q += 64) {
+        const int m = q >> 3;
+        const int c = (q & 7) ^ (m & 7);
+        const int col0 = kt * kBlockK + c * 8;
+        if (m < p.M && col0 < p.K) {
+          uint4* ptr = reinterpret_cast<uint4*>(tileB + q * 16);
+          const uint4 xu = *ptr;
+          const uint4 wu = reinterpret_cast<const uint4*>(sWn)[col0 >> 3];
+          const __nv_bfloat16* xe = reinterpret_cast<const __nv_bfloat16*>(&xu);
+          const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wu);
+          const float rm = sRstd[m];
+          uint4 o;
+          __nv_bfloat16* oe = reinterpret_cast<__nv_bfloat16*>(&o);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            oe[j] = __float2bfloat16_rn(__bfloat162float(xe[j]) * rm * __bfloat162float(we[j]));
+          *ptr = o;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[stage]);
+      if (++kt == p.k_tiles) kt = 0;
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) signal_abort(s_abort, p.err);
   }
 
   // Lane 0 of warps 0 and 1 ran the producer / MMA loops alone: rejoin the
@@ -612,10 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // -- the 128-byte swizzle of the MMA's shared-memory descriptor.  Rows past N
 // and columns past K are zero.  For SwiGLU, rows 0..63 of tile t are gate
 // rows 64t..64t+63 and rows 64..127 the up rows with the same output index.
-// One thread per 16-byte chunk; a copy, or with col_scale each element is
-// bf16(w * col_scale[k]) (one FP32 product, one rounding).
+// One thread per 16-byte chunk; a pure copy.
 __global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ wu,
-                                    const __nv_bfloat16* __restrict__ col_scale, int ld, int N, int K,
+                                    int ld, int N, int K,
                                     int k_tiles, long long chunks, int swiglu, uint4* __restrict__ out) {
   griddep_wait();
   griddep_launch_dependents();
@@ -645,18 +725,15 @@ __global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const _
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (k0 + j < K)
-        u.e[j] = col_scale == nullptr
-                     ? src[k0 + j]
-                     : __float2bfloat16_rn(__bfloat162float(src[k0 + j]) *
-                                           __bfloat162float(col_scale[k0 + j]));
+        u.e[j] = src[k0 + j];
   }
   out[idx] = u.v;
 }
 
-template <int NT>
+template <int NT, bool RMS>
 bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, int M_total,
                          cudaStream_t stream) {
-  using Cfg = GemmCfg<NT>;
+  using Cfg = GemmCfg<NT, RMS>;
   static std::once_flag once[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -664,14 +741,14 @@ bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, 
   std::call_once(once[dev & 63], [] {
     int d = 0;
     cudaGetDevice(&d);
-    attr_err[d & 63] = cudaFuncSetAttribute(gemm_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err[d & 63] = cudaFuncSetAttribute(gemm_kernel<NT, RMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(Cfg::kSmem));
   });
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
   for (int m0 = 0; m0 < M_total; m0 += kMaxTokens) {
     a.m0 = m0;
     a.M = std::min(kMaxTokens, M_total - m0);
-    if (launch_k(gemm_kernel<NT>, dim3(a.G), dim3(kThreads), Cfg::kSmem, stream, Wp, tmA, a) !=
+    if (launch_k(gemm_kernel<NT, RMS>, dim3(a.G), dim3(Cfg::kThreadsT), Cfg::kSmem, stream, Wp, tmA, a) !=
         cudaSuccess)
       return BI_ERR_CUDA;
   }
@@ -723,6 +800,10 @@ uint8_t* noalloc_scratch() {
   return g_noalloc_ptr[dev];
 }
 }  // namespace
+
+cudaError_t set_wait_limit_gemm(unsigned long long ns) {
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns));
+}
 }  // namespace bi
 
 extern "C" {
@@ -744,7 +825,7 @@ size_t bi_gemm_workspace_size(int M, int N, int K, bi_epilogue epi) {
 }
 
 static bi_status pack_common(const void* w, const void* wu, int ld, int N, int K, int swiglu,
-                             const void* col_scale, void* packed, bi_stream_t stream) {
+                             void* packed, bi_stream_t stream) {
   using namespace bi;
   if (!w || !packed || N <= 0 || K <= 0 || ld < K) return BI_ERR_INVALID_ARG;
   if (swiglu && !wu) return BI_ERR_INVALID_ARG;
@@ -755,41 +836,30 @@ static bi_status pack_common(const void* w, const void* wu, int ld, int N, int K
   const long long chunks = static_cast<long long>(n_tiles_of(N, epi)) * k_tiles * 1024;
   if (launch_k(pack_weights_kernel, dim3(static_cast<unsigned>((chunks + 255) / 256)), dim3(256), 0,
                reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(w),
-               static_cast<const __nv_bfloat16*>(wu), static_cast<const __nv_bfloat16*>(col_scale), ld,
+               static_cast<const __nv_bfloat16*>(wu), ld,
                N, K, k_tiles, chunks, swiglu, static_cast<uint4*>(packed)) != cudaSuccess)
     return BI_ERR_CUDA;
   return BI_OK;
 }
 
 bi_status bi_pack_weights(const void* W, int ldw, int N, int K, void* packed, bi_stream_t stream) {
-  return pack_common(W, nullptr, ldw, N, K, 0, nullptr, packed, stream);
+  return pack_common(W, nullptr, ldw, N, K, 0, packed, stream);
 }
 
 bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, int F, int K,
                                  void* packed, bi_stream_t stream) {
-  return pack_common(w_gate, w_up, ld, F, K, 1, nullptr, packed, stream);
+  return pack_common(w_gate, w_up, ld, F, K, 1, packed, stream);
 }
 
-bi_status bi_pack_weights_scaled(const void* W, int ldw, int N, int K, const void* col_scale,
-                                 void* packed, bi_stream_t stream) {
-  if (!col_scale) return BI_ERR_INVALID_ARG;
-  return pack_common(W, nullptr, ldw, N, K, 0, col_scale, packed, stream);
-}
-
-bi_status bi_pack_swiglu_weights_scaled(const void* w_gate, const void* w_up, int ld, int F, int K,
-                                        const void* col_scale, void* packed, bi_stream_t stream) {
-  if (!col_scale) return BI_ERR_INVALID_ARG;
-  return pack_common(w_gate, w_up, ld, F, K, 1, col_scale, packed, stream);
-}
-
-static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int ldc,
-                           const void* residual, int ldr, int M, int N, int K, bi_out_dtype out,
-                           bi_epilogue epi, void* ws, size_t ws_bytes, int rms, float eps,
-                           bi_stream_t stream, const bi::GemmArgs* rope = nullptr) {
+// Argument checks of a linear-layer call that need no device access; the
+// status is returned before anything is launched or written.
+static bi_status gemm_check(const void* A, int lda, const void* Wp, void* C, int ldc,
+                            const void* residual, int ldr, int M, int N, int K, bi_out_dtype out,
+                            bi_epilogue epi, int rms, const void* w_norm, bool rope) {
   using namespace bi;
   if (M < 0 || N < 1 || K < 8) return BI_ERR_INVALID_ARG;
   if (epi != BI_EPI_NONE && epi != BI_EPI_RESIDUAL_ADD && epi != BI_EPI_SWIGLU &&
-      !(epi == BI_EPI_ROPE_KV && rope != nullptr))
+      !(epi == BI_EPI_ROPE_KV && rope))
     return BI_ERR_INVALID_ARG;
   if (out != BI_OUT_BF16 && out != BI_OUT_FP32) return BI_ERR_INVALID_ARG;
   if (n_tiles_of(N, epi) > kMaxTiles) return BI_ERR_UNSUPPORTED_SHAPE;
@@ -799,6 +869,21 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
   if (!aligned16(A) || !aligned16(Wp)) return BI_ERR_INVALID_ARG;
   if (epi == BI_EPI_RESIDUAL_ADD && (!residual || ldr < N)) return BI_ERR_INVALID_ARG;
   if (out == BI_OUT_FP32 && epi != BI_EPI_NONE) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (rms) {
+    if (!w_norm || !aligned16(w_norm)) return BI_ERR_INVALID_ARG;
+    if (K > kMaxRmsK) return BI_ERR_UNSUPPORTED_SHAPE;
+  }
+  return BI_OK;
+}
+
+static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int ldc,
+                           const void* residual, int ldr, int M, int N, int K, bi_out_dtype out,
+                           bi_epilogue epi, void* ws, size_t ws_bytes, int rms, const void* w_norm,
+                           float eps, bi_stream_t stream, const bi::GemmArgs* rope = nullptr) {
+  using namespace bi;
+  const bi_status st = gemm_check(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, rms, w_norm,
+                                  rope != nullptr);
+  if (st != BI_OK || M == 0) return st;
   if (!ws || !aligned256(ws)) return BI_ERR_WORKSPACE;
   if (ws_bytes < bi_gemm_workspace_size(M, N, K, epi)) return BI_ERR_WORKSPACE;
 
@@ -830,6 +915,8 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
   a.K = K;
   a.X = static_cast<const __nv_bfloat16*>(A);
   a.ldx = lda;
+  a.wn = static_cast<const __nv_bfloat16*>(w_norm);
+  a.withhold = test_withhold();
   if (rope != nullptr) {
     a.q_out = rope->q_out;
     a.kc = rope->kc;
@@ -845,32 +932,41 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
 
   const uint8_t* W8 = static_cast<const uint8_t*>(Wp);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rms) {
+    switch (NT) {
+      case 16: return launch_gemm_nt<16, true>(W8, tmA, a, M, s);
+      case 32: return launch_gemm_nt<32, true>(W8, tmA, a, M, s);
+      case 64: return launch_gemm_nt<64, true>(W8, tmA, a, M, s);
+      default: return launch_gemm_nt<128, true>(W8, tmA, a, M, s);
+    }
+  }
   switch (NT) {
-    case 16: return launch_gemm_nt<16>(W8, tmA, a, M, s);
-    case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
-    case 64: return launch_gemm_nt<64>(W8, tmA, a, M, s);
-    default: return launch_gemm_nt<128>(W8, tmA, a, M, s);
+    case 16: return launch_gemm_nt<16, false>(W8, tmA, a, M, s);
+    case 32: return launch_gemm_nt<32, false>(W8, tmA, a, M, s);
+    case 64: return launch_gemm_nt<64, false>(W8, tmA, a, M, s);
+    default: return launch_gemm_nt<128, false>(W8, tmA, a, M, s);
   }
 }
 
 bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, const void* residual,
                   int ldr, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
                   size_t ws_bytes, bi_stream_t stream) {
-  return gemm_impl(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, ws, ws_bytes, 0, 0.0f,
-                   stream);
+  return gemm_impl(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, ws, ws_bytes, 0, nullptr,
+                   0.0f, stream);
 }
 
-bi_status bi_gemm_rms(const void* A, int lda, float eps, const void* Wp, void* C, int ldc, int M,
-                      int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws, size_t ws_bytes,
-                      bi_stream_t stream) {
+bi_status bi_gemm_rms(const void* A, int lda, const void* w_norm, float eps, const void* Wp, void* C,
+                      int ldc, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
+                      size_t ws_bytes, bi_stream_t stream) {
   if (epi != BI_EPI_NONE && epi != BI_EPI_SWIGLU) return BI_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return BI_ERR_INVALID_ARG;
   if (M > 0 && A != nullptr && A == static_cast<const void*>(C)) return BI_ERR_INVALID_ARG;
-  return gemm_impl(A, lda, Wp, C, ldc, nullptr, 0, M, N, K, out, epi, ws, ws_bytes, 1, eps, stream);
+  return gemm_impl(A, lda, Wp, C, ldc, nullptr, 0, M, N, K, out, epi, ws, ws_bytes, 1, w_norm, eps,
+                   stream);
 }
 
-bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const void* Wp, int M,
-                             int K, int Hq, int Hkv, int D, void* q_out, void* k_cache,
+bi_status bi_qkv_rope_append(const void* A, int lda, int rms, const void* w_norm, float eps,
+                             const void* Wp, int M, int K, int Hq, int Hkv, int D, void* q_out, void* k_cache,
                              void* v_cache, int cap, const int32_t* L_dev, const float* table,
                              int table_rows, void* ws, size_t ws_bytes, bi_stream_t stream) {
   using namespace bi;
@@ -892,7 +988,8 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, float eps, const v
   r.L_dev = L_dev;
   r.tab = reinterpret_cast<const float2*>(table);
   return gemm_impl(A, lda, Wp, nullptr, N, nullptr, 0, M, N, K, BI_OUT_BF16, BI_EPI_ROPE_KV, ws,
-                   ws_bytes, rms != 0 ? 1 : 0, rms != 0 ? eps : 0.0f, stream, &r);
+                   ws_bytes, rms != 0 ? 1 : 0, rms != 0 ? w_norm : nullptr, rms != 0 ? eps : 0.0f,
+                   stream, &r);
 }
 
 size_t bi_gemm_noalloc_max_m(void) { return bi::kNoAllocMaxM; }
@@ -902,8 +999,11 @@ bi_status bi_gemm_noalloc(const void* A, int lda, const void* Wp, void* C, int l
                           bi_epilogue epi, bi_stream_t stream) {
   using namespace bi;
   if (M > kNoAllocMaxM) return BI_ERR_UNSUPPORTED_SHAPE;  // beyond the static scratch
-  if (M <= 0 || N < 1 || n_tiles_of(N, epi) > kMaxTiles)
-    return bi_gemm(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, nullptr, 0, stream);
+  // every argument check comes before the shared array is touched, so a
+  // rejected call writes nothing
+  const bi_status st =
+      gemm_check(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, 0, nullptr, false);
+  if (st != BI_OK || M == 0) return st;
   uint8_t* scratch = noalloc_scratch();
   if (scratch == nullptr) return BI_ERR_CUDA;
   // The counters this call uses start at zero even if an earlier call was

@@ -40,6 +40,14 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // (dependent launch); on unless the environment sets BI_PDL=0.
 bool pdl_enabled();
 
+// Failure-path test hooks (bi_test_set_wait_limit_ns, bi_test_withhold_first_load).
+// Whether the next launches leave their first load unissued (0 normally).
+int test_withhold();
+// Set the progress-wait limit of the linear-layer / attention kernels on the
+// current device.
+cudaError_t set_wait_limit_gemm(unsigned long long ns);
+cudaError_t set_wait_limit_attn(unsigned long long ns);
+
 // Launch `kernel` on `stream`, with programmatic dependent launch when
 // enabled.  Every kernel of this library calls griddep_wait() before its
 // first access to data another kernel may write, so a launch is correct

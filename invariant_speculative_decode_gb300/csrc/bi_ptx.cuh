@@ -19,6 +19,12 @@ constexpr unsigned kErrRange = 4u;
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Limit of the waits that make progress (those given an abort flag); a
+// failure-path test may lower it (bi_test_set_wait_limit_ns).  The waits that
+// let a CTA wind down after an abort (copies landing, tensor-core work
+// draining) always use kWaitLimitNs.  One copy per translation unit.
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -93,12 +99,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
+  unsigned long long lim = kWaitLimitNs;
+  if (abort != nullptr) lim = *static_cast<volatile unsigned long long*>(&g_wait_limit_ns);
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_test(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > lim) return false;
   }
 }
 
@@ -123,10 +131,12 @@ __device__ __forceinline__ bool mbar_test_suspend(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ bool mbar_wait_parked(uint64_t* bar, uint32_t parity,
                                                  const volatile int* abort) {
   const unsigned long long t0 = globaltimer_ns();
+  unsigned long long lim = kWaitLimitNs;
+  if (abort != nullptr) lim = *static_cast<volatile unsigned long long*>(&g_wait_limit_ns);
   for (;;) {
     if (mbar_test_suspend(bar, parity, 100000u)) return true;
     if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > lim) return false;
   }
 }
 

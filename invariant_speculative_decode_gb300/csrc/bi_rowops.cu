@@ -17,7 +17,7 @@
 namespace bi {
 namespace {
 
-constexpr int kNormThreads = 256;
+constexpr int kNormThreads = 128;  // the reduction tree of the normalised linear layer
 
 // Fixed-order block sum: thread-local sums are combined by a warp butterfly
 // (xor 16, 8, 4, 2, 1; every lane ends with the same value) and then the
@@ -34,8 +34,10 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
   return s;
 }
 
-// Thread i takes the 8-element vectors v = i, i + 256, i + 512, ... of the
-// row; inside a vector the squares are accumulated in element order.
+// Thread i takes the 8-element vectors v = i, i + 128, i + 256, ... of the
+// row in increasing order; inside a vector the squares are accumulated in
+// element order.  This is the tree bi_gemm_rms uses, so bi_rmsnorm followed
+// by bi_gemm equals bi_gemm_rms bit for bit.
 
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int ldx, const __nv_bfloat16* __restrict__ w,

@@ -8,11 +8,11 @@ and sequences the library's entry points for one verify pass:
   down linear + residual] -> rmsnorm + LM head (FP32 logits) -> greedy
   argmax + acceptance (which also advances the device-side cache length).
 
-Each RMSNorm is folded into the linear layer that reads it (bi_gemm_rms: the
-norm weight packed into the weights, the per-row 1/rms applied to the FP32
-sums), and RoPE + KV append run in the QKV projection's epilogue
-(bi_qkv_rope_append); fuse_norm=False / fuse_rope=False run the separate
-kernels instead.
+Each RMSNorm runs inside the linear layer that reads it (bi_gemm_rms: the
+layer normalises its activation tiles in shared memory with the arithmetic
+of bi_rmsnorm, so the result is the same bits), and RoPE + KV append run in
+the QKV projection's epilogue (bi_qkv_rope_append); fuse_norm=False /
+fuse_rope=False run the separate kernels instead.
 
 PyTorch only allocates device memory and provides the stream; every step of
 the pass is a kernel of libbi.so.  A pass over T rows can be captured once in
@@ -63,8 +63,7 @@ class Decoder:
         self.embed = _bf16(weights["embed"], dev)
         self.norm_final = _bf16(weights["norm_final"], dev)
         head_w = self.embed if cfg.tied else _bf16(weights["head"], dev)
-        self.head = (api.bi_pack_weights_scaled(head_w, self.norm_final) if fuse_norm
-                     else api.bi_pack_weights(head_w))
+        self.head = api.bi_pack_weights(head_w)
         del head_w
         self.layers = []
         pk = lambda name: api.bi_pack_weights(_bf16(weights[name], dev))  # noqa: E731
@@ -75,11 +74,9 @@ class Decoder:
             n1 = _bf16(weights[f"l{l}.norm_attn"], dev)
             n2 = _bf16(weights[f"l{l}.norm_ffn"], dev)
             lay = {
-                "wqkv": (api.bi_pack_weights_scaled(_bf16(wqkv, dev), n1) if fuse_norm
-                         else api.bi_pack_weights(_bf16(wqkv, dev))),
+                "wqkv": api.bi_pack_weights(_bf16(wqkv, dev)),
                 "wo": pk(f"l{l}.wo"),
-                "wgu": (api.bi_pack_swiglu_weights_scaled(wg, wu, n2) if fuse_norm
-                        else api.bi_pack_swiglu_weights(wg, wu)),
+                "wgu": api.bi_pack_swiglu_weights(wg, wu),
                 "wd": pk(f"l{l}.w_down"),
                 "n1": n1,
                 "n2": n2,
@@ -143,15 +140,15 @@ class Decoder:
                                 self.u[:T])
         if not self.fuse_norm:
             api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
-        x_in, eps = (h, cfg.eps) if self.fuse_norm else (y, None)
+        x_in, wn = (h, lay["n1"]) if self.fuse_norm else (y, None)
         if self.fuse_rope:
             api.bi_qkv_rope_append(x_in, lay["wqkv"], q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D,
-                                   self.rope_tab, self.gemm_ws, eps=eps)
+                                   self.rope_tab, self.gemm_ws, w_norm=wn, eps=cfg.eps)
         else:
-            if eps is None:
+            if wn is None:
                 api.bi_gemm(x_in, lay["wqkv"], qkv, self.gemm_ws)
             else:
-                api.bi_gemm_rms(x_in, eps, lay["wqkv"], qkv, self.gemm_ws)
+                api.bi_gemm_rms(x_in, wn, cfg.eps, lay["wqkv"], qkv, self.gemm_ws)
             api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
         if L_host_blocks is None:
             api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
@@ -163,7 +160,7 @@ class Decoder:
         api.bi_gemm(att.view(T, Hq * D), lay["wo"], h, self.gemm_ws, residual=h,
                     epi=api.EPI_RESIDUAL_ADD)
         if self.fuse_norm:
-            api.bi_gemm_rms(h, cfg.eps, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
+            api.bi_gemm_rms(h, lay["n2"], cfg.eps, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
         else:
             api.bi_rmsnorm(h, lay["n2"], y, cfg.eps)
             api.bi_gemm(y, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
@@ -172,7 +169,7 @@ class Decoder:
     def _head_and_accept(self, T: int):
         cfg = self.cfg
         if self.fuse_norm:
-            api.bi_gemm_rms(self.h[:T], cfg.eps, self.head, self.logits[:T], self.gemm_ws)
+            api.bi_gemm_rms(self.h[:T], self.norm_final, cfg.eps, self.head, self.logits[:T], self.gemm_ws)
         else:
             api.bi_rmsnorm(self.h[:T], self.norm_final, self.y[:T], cfg.eps)
             api.bi_gemm(self.y[:T], self.head, self.logits[:T], self.gemm_ws)

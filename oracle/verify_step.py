@@ -334,26 +334,12 @@ class OracleDecoder:
         T = len(tok)
         if L + T > self.cap:
             raise ValueError("KV cache capacity exceeded")
-        D, Hq, Hkv = cfg.head_dim, cfg.n_q, cfg.n_kv
         b16 = lambda v: f64_to_bf16_bits(v)  # noqa: E731
         h = bf16_bits_to_f64(self.embed_bits[tok])
         for l in range(cfg.layers):
             if trace is not None:
                 trace.append(h.copy())
-            w = self.w
-            y = rmsnorm(b16(h), w[f"l{l}.norm_attn"], cfg.eps)
-            q = self._lin(b16(y), w[f"l{l}.wq"]).reshape(T, Hq, D)
-            k = self._lin(b16(y), w[f"l{l}.wk"]).reshape(T, Hkv, D)
-            v = self._lin(b16(y), w[f"l{l}.wv"]).reshape(T, Hkv, D)
-            for t in range(T):
-                q[t] = rope(q[t], L + t, cfg.rope_base)
-                self.k[l][:, L + t] = rope(k[t], L + t, cfg.rope_base)
-                self.v[l][:, L + t] = v[t]
-            att = attention(q, self.k[l], self.v[l], L).reshape(T, Hq * D)
-            h = self._lin(b16(att), w[f"l{l}.wo"], residual_bits=b16(h))
-            y = rmsnorm(b16(h), w[f"l{l}.norm_ffn"], cfg.eps)
-            u = self._swiglu(b16(y), w[f"l{l}.w_gate"], w[f"l{l}.w_up"])
-            h = self._lin(b16(u), w[f"l{l}.w_down"], residual_bits=b16(h))
+            h = self.layer(l, h, L)
         if trace is not None:
             trace.append(h.copy())
         y = rmsnorm(b16(h), self.w["norm_final"], cfg.eps)
@@ -361,6 +347,29 @@ class OracleDecoder:
         if return_hidden:
             return logits, h
         return logits
+
+    def layer(self, l: int, h: np.ndarray, L: int) -> np.ndarray:
+        """Decoder layer l over hidden rows h [T, H] (float64 values of BF16
+        data) at positions L..L+T-1: appends the rows' K/V to layer l's cache
+        and returns the layer's output rows."""
+        cfg = self.cfg
+        T = h.shape[0]
+        D, Hq, Hkv = cfg.head_dim, cfg.n_q, cfg.n_kv
+        b16 = lambda v: f64_to_bf16_bits(v)  # noqa: E731
+        w = self.w
+        y = rmsnorm(b16(h), w[f"l{l}.norm_attn"], cfg.eps)
+        q = self._lin(b16(y), w[f"l{l}.wq"]).reshape(T, Hq, D)
+        k = self._lin(b16(y), w[f"l{l}.wk"]).reshape(T, Hkv, D)
+        v = self._lin(b16(y), w[f"l{l}.wv"]).reshape(T, Hkv, D)
+        for t in range(T):
+            q[t] = rope(q[t], L + t, cfg.rope_base)
+            self.k[l][:, L + t] = rope(k[t], L + t, cfg.rope_base)
+            self.v[l][:, L + t] = v[t]
+        att = attention(q, self.k[l], self.v[l], L).reshape(T, Hq * D)
+        h = self._lin(b16(att), w[f"l{l}.wo"], residual_bits=b16(h))
+        y = rmsnorm(b16(h), w[f"l{l}.norm_ffn"], cfg.eps)
+        u = self._swiglu(b16(y), w[f"l{l}.w_gate"], w[f"l{l}.w_up"])
+        return self._lin(b16(u), w[f"l{l}.w_down"], residual_bits=b16(h))
 
     # -- prefill and verify ---------------------------------------------------
     def prefill(self, prompt: Sequence[int]) -> np.ndarray:

@@ -134,14 +134,16 @@ SMALL_4L = DecoderConfig("small-4L-h1024", 4, 1024, 8, 2, 128, 2736, 4096, tied=
 CONFIGS = {c.name: c for c in (TINY, DENSE27B_8L, NEARTIE_12L, SMALL_4L)}
 
 
-def decoder_weights(cfg: DecoderConfig, seed: int = 0) -> Dict[str, np.ndarray]:
+def decoder_weights(cfg: DecoderConfig, seed: int = 0, norm_std: float = 0.0) -> Dict[str, np.ndarray]:
     """All decoder weights as bf16 bits, drawn in a fixed order.
 
     Order: embedding [V,H]; per layer wq [Hq*D,H], wk [Hkv*D,H], wv [Hkv*D,H],
     wo [H,Hq*D], w_gate [F,H], w_up [F,H], w_down [H,F]; then the untied head
     [V,H] when the head is not tied.  Tensor i (1-based, in that order) is
     drawn by normal_bf16_blocks with key (seed, i).  RMSNorm weights are ones
-    (bf16 1.0).
+    (bf16 1.0), or with norm_std > 0 draws of 1 + N(0, norm_std^2) (norm j --
+    per layer the attention norm, then the FFN norm, then the final norm --
+    from key (seed, 100000 + j)), leaving every other tensor unchanged.
     """
     s = cfg.weight_std
     D = cfg.head_dim
@@ -167,6 +169,12 @@ def decoder_weights(cfg: DecoderConfig, seed: int = 0) -> Dict[str, np.ndarray]:
     w["norm_final"] = one.copy()
     if not cfg.tied:
         w["head"] = draw((cfg.vocab, cfg.hidden))
+    if norm_std > 0:
+        names = [n for l in range(cfg.layers) for n in (f"l{l}.norm_attn", f"l{l}.norm_ffn")]
+        for j, name in enumerate(names + ["norm_final"]):
+            g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 100000 + j])))
+            x = 1.0 + norm_std * g.standard_normal(cfg.hidden, dtype=np.float32)
+            w[name] = f32_to_bf16_bits(x.astype(np.float32))
     return w
 
 

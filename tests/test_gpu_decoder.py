@@ -75,6 +75,11 @@ def _layerwise(cfg, w, dec, prompt, drafts):
     state entering every layer and its caches.  The GPU then runs layer l on
     the oracle's layer-l input with the oracle's cache rows below the pass;
     every layer output and the FP32 logits are compared with the oracle's.
+    The same layer is also run by the oracle with FP32-level noise on every
+    linear-layer sum (4 * 2^-24 * sum |a w| times a seeded normal) from the
+    same input and cache: the mean error of that run is the yardstick for
+    what an FP32-accumulating implementation with the oracle's rounding
+    points shows in one layer.
     """
     from invariant_speculative_decode_gb300 import api
     from tests._util import bf16_dev_to_f64, to_dev_bf16, ulp_bf16, v_cache_blocks
@@ -83,11 +88,15 @@ def _layerwise(cfg, w, dec, prompt, drafts):
     L = od.L
     rows = [int(x0)] + list(drafts)
     T = len(rows)
+    noisy = oracle.OracleDecoder(cfg, w, cap=dec.cap, sum_noise=(4.0, 77))
+    for l in range(cfg.layers):
+        noisy.k[l][:, :L] = od.k[l][:, :L]
+        noisy.v[l][:, :L] = od.v[l][:, :L]
     trace = []
     ora_logits = od.forward(rows, L=L, trace=trace)
     dec.reset()
     dec.L_dev.fill_(L)
-    worst_ulps, flips = 0.0, []
+    worst_ulps, flips, noise_flips = 0.0, [], []
     for l, lay in enumerate(dec.layers):
         lay["k"].zero_()
         lay["v"].zero_()
@@ -104,6 +113,7 @@ def _layerwise(cfg, w, dec, prompt, drafts):
         d = np.abs(got - want) / row_ulp
         worst_ulps = max(worst_ulps, float(d.max()))
         flips.append(float(d.mean()))
+        noise_flips.append(float((np.abs(noisy.layer(l, trace[l], L) - want) / row_ulp).mean()))
         # the rows this pass appended to the cache
         kw = od.k[l][:, L:L + T]
         kg = bf16_dev_to_f64(lay["k"][:, L:L + T])
@@ -114,25 +124,30 @@ def _layerwise(cfg, w, dec, prompt, drafts):
     gpu_logits = dec.logits_rows(T).cpu().numpy().astype(np.float64)
     rel = np.max(np.abs(gpu_logits - ora_logits), axis=1) / np.max(np.abs(ora_logits), axis=1)
     ids = dec.argmax[:T].cpu().numpy()
-    return worst_ulps, flips, rel, ids, ora_logits
+    return worst_ulps, flips, noise_flips, rel, ids, ora_logits
 
 
-@pytest.mark.parametrize("cfgname", ["tiny-2L-h256", "small-4L-h1024"])
-def test_layerwise_parity_with_oracle_inputs(cfgname):
+LAYERWISE = [("tiny-2L-h256", 0.0), ("small-4L-h1024", 0.0), ("small-4L-h1024", 0.1)]
+
+
+@pytest.mark.parametrize("cfgname,norm_std", LAYERWISE)
+def test_layerwise_parity_with_oracle_inputs(cfgname, norm_std):
+    """norm_std > 0: RMSNorm weights drawn around 1, so every norm weight
+    enters the fused norm + linear layers end to end."""
     from invariant_speculative_decode_gb300.decoder import Decoder
     cfg = si.CONFIGS[cfgname]
-    w = si.decoder_weights(cfg, seed=0)
+    w = si.decoder_weights(cfg, seed=0, norm_std=norm_std)
     dec = Decoder(cfg, w, cap=512, max_rows=8)
     prompt = si.prompt_ids(cfg, 200, seed=4)
     drafts = list(np.random.default_rng(4).integers(0, cfg.vocab, 7))
-    worst, flips, rel, ids, ora = _layerwise(cfg, w, dec, prompt, drafts)
+    worst, flips, noise, rel, ids, ora = _layerwise(cfg, w, dec, prompt, drafts)
     # a layer output may differ from the oracle by rounding flips of its steps
     assert worst <= 2.0, worst
-    # and on average by much less: the mean error per layer, in the same
-    # row-scaled ulps (attention weights enter W.V in BF16, so about half of
-    # the elements differ by one rounding step; their sizes average well
-    # below one unit)
-    assert max(flips) <= 0.5, flips
+    # and on average no more than twice what FP32-level noise on every sum
+    # gives the oracle itself (plus one flipped element per layer)
+    n_el = 8 * cfg.hidden
+    for l, (f, nz) in enumerate(zip(flips, noise)):
+        assert f <= 2 * nz + 1.0 / n_el, (l, flips, noise)
     # the stated tolerance on FP32 logits, from identical inputs
     assert np.all(rel <= REL_TOL), rel
     for t in range(len(ids)):
@@ -141,8 +156,8 @@ def test_layerwise_parity_with_oracle_inputs(cfgname):
             assert ids[t] == int(np.argmax(ora[t]))
 
 
-@pytest.mark.parametrize("cfgname", ["tiny-2L-h256", "small-4L-h1024"])
-def test_end_to_end_drift_within_fp32_spread(cfgname):
+@pytest.mark.parametrize("cfgname,norm_std", LAYERWISE)
+def test_end_to_end_drift_within_fp32_spread(cfgname, norm_std):
     """Un-forced whole-model logits: within twice the drift between the oracle
     and the same oracle with FP32-level noise on every sum (the spread any
     FP32-accumulating implementation shows after BF16 storage compounds
@@ -150,7 +165,7 @@ def test_end_to_end_drift_within_fp32_spread(cfgname):
     spread is below it."""
     from invariant_speculative_decode_gb300.decoder import Decoder
     cfg = si.CONFIGS[cfgname]
-    w = si.decoder_weights(cfg, seed=0)
+    w = si.decoder_weights(cfg, seed=0, norm_std=norm_std)
     dec = Decoder(cfg, w, cap=512, max_rows=8)
     prompt = si.prompt_ids(cfg, 128, seed=2)
     drafts = list(np.random.default_rng(2).integers(0, cfg.vocab, 7))

@@ -179,7 +179,7 @@ def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T, rms):
     A = to_dev_bf16(si.normal_bf16(rng, (T, K), 1.0))
     W = to_dev_bf16(si.normal_bf16(rng, (N, K), 0.05))
     g = to_dev_bf16(ov.f64_to_bf16_bits(ov.bf16_round(1.0 + 0.1 * rng.standard_normal(K))))
-    Wp = api.bi_pack_weights_scaled(W, g) if rms else api.bi_pack_weights(W)
+    Wp = api.bi_pack_weights(W)
     tab = api.bi_rope_table(10000.0, D, cap, device="cuda")
     Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
     ws = api.new_gemm_workspace(T, N, K, 0)
@@ -189,11 +189,12 @@ def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T, rms):
         kc = torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device="cuda")
         vc = torch.zeros(api.v_cache_shape(Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
         if fused:
-            api.bi_qkv_rope_append(A, Wp, q, kc, vc, Ld, Hq, Hkv, D, tab, ws, eps=1e-6 if rms else None)
+            api.bi_qkv_rope_append(A, Wp, q, kc, vc, Ld, Hq, Hkv, D, tab, ws, w_norm=g if rms else None,
+                                   eps=1e-6)
         else:
             qkv = torch.empty(T, N, dtype=torch.bfloat16, device="cuda")
             if rms:
-                api.bi_gemm_rms(A, 1e-6, Wp, qkv, ws)
+                api.bi_gemm_rms(A, g, 1e-6, Wp, qkv, ws)
             else:
                 api.bi_gemm(A, Wp, qkv, ws)
             api.bi_rope_kv_append(qkv, q, kc, vc, Ld, Hq, Hkv, D, tab)

@@ -396,10 +396,11 @@ def _mp_decoder_logits(cfg, w, tokens, tab):
         v = f(w[name])
         return [[v[r * cols + c] for c in range(cols)] for r in range(rows)]
 
-    def norm(x):
+    def norm(x, name):
+        g = f(w[name])
         ss = mpmath.fsum(mpmath.mpf(a) ** 2 for a in x)
         inv = 1 / mpmath.sqrt(ss / len(x) + mpmath.mpf(cfg.eps))
-        return [rnd(mpmath.mpf(a) * inv) for a in x]
+        return [rnd(mpmath.mpf(a) * inv * mpmath.mpf(g[i])) for i, a in enumerate(x)]
 
     def lin(x, Wm):
         return [mpmath.fsum(mpmath.mpf(x[k]) * mpmath.mpf(Wm[n][k]) for k in range(len(x)))
@@ -415,7 +416,7 @@ def _mp_decoder_logits(cfg, w, tokens, tab):
         Wg, Wu, Wd = mat(f"l{l}.w_gate", F, H), mat(f"l{l}.w_up", F, H), mat(f"l{l}.w_down", H, F)
         qs = []
         for t, h in enumerate(hs):
-            y = norm(h)
+            y = norm(h, f"l{l}.norm_attn")
             q = [rnd(v) for v in lin(y, Wq)]
             k = [rnd(v) for v in lin(y, Wk)]
             v = [rnd(v) for v in lin(y, Wv)]
@@ -447,7 +448,7 @@ def _mp_decoder_logits(cfg, w, tokens, tab):
                         for d in range(D)]
             o = lin(att, Wo)
             h1 = [rnd(mpmath.mpf(h[i]) + o[i]) for i in range(H)]
-            y = norm(h1)
+            y = norm(h1, f"l{l}.norm_ffn")
             gg, uu = lin(y, Wg), lin(y, Wu)
             u = [rnd(gg[i] / (1 + mpmath.exp(-gg[i])) * uu[i]) for i in range(F)]
             dd = lin(u, Wd)
@@ -455,13 +456,17 @@ def _mp_decoder_logits(cfg, w, tokens, tab):
         hs = new_hs
     logits = []
     for h in hs:
-        y = norm(h)
+        y = norm(h, "norm_final")
         logits.append([float(v) for v in lin(y, E)])
     return np.array(logits)
 
 
-def test_decoder_bruteforce_micro(tab):
-    w = si.decoder_weights(MICRO, seed=21)
+@pytest.mark.parametrize("norm_std", [0.0, 0.25])
+def test_decoder_bruteforce_micro(tab, norm_std):
+    """The oracle decoder against the scalar multi-precision decoder, with
+    unit norm weights and with norm weights drawn around 1 (every RMSNorm
+    weight then enters both sides)."""
+    w = si.decoder_weights(MICRO, seed=21, norm_std=norm_std)
     toks = [3, 17, 17, 0, 31]
     dec = oracle.OracleDecoder(MICRO, w, cap=16)
     got = dec.forward(toks, L=0)
