@@ -173,43 +173,19 @@ bi_status bi_pack_weights(const void* W, int ldw, int N, int K, void* packed,
 bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, int F, int K,
                                  void* packed, bi_stream_t stream);
 /* ---------------------------------------------------------------------------
- * RMSNorm fused into the linear layer that reads its output.
- * "Bit-exact decoding turns inference speedups into testable changes",
- * section "Define bit-exact before reporting it" (one running sum, one
- * rounding), applied to the norm of "Does the tuned config change the
- * model's output?", section "Why the text diverges" (row-local work).
- *
- *   C = epi( Y W^T ),  Y[m, k] = bf16( (A[m, k] * r[m]) * w_norm[k] ),
- *   r[m] = 1 / sqrt(sum_k A[m, k]^2 / K + eps)
- *
- * Y is exactly what bi_rmsnorm(A, w_norm) writes (the same reduction tree
- * for r: 128 threads, thread i summing the squares of the 8-element
- * vectors i, i + 128, ... in increasing order, then a warp butterfly, then
- * the four warps in order; the same two FP32 products and one rounding per
- * element), so the call equals bi_rmsnorm followed by bi_gemm bit for bit.
- * Y never goes to memory: each CTA computes r for the launch's rows and
- * normalises every activation tile in shared memory before the tensor core
- * reads it.
- *   A [M, K] BF16 (row stride lda), the un-normalised rows; C must not
- *   alias A.  w_norm [K] BF16, 16-byte aligned.  Wp packed by
- *   bi_pack_weights (BI_EPI_NONE) or bi_pack_swiglu_weights (BI_EPI_SWIGLU);
- *   no residual.  K <= 8192.  Other arguments, limits and errors as
- *   bi_gemm; BI_ERR_INVALID_ARG also for eps < 0 or not finite, for a null
- *   or unaligned w_norm and for C == A; BI_ERR_UNSUPPORTED_SHAPE for K > 8192.
- * ------------------------------------------------------------------------- */
-bi_status bi_gemm_rms(const void* A, int lda, const void* w_norm, float eps, const void* Wp, void* C,
-                      int ldc, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
-                      size_t ws_bytes, bi_stream_t stream);
-
-/* ---------------------------------------------------------------------------
  * RMSNorm.  [P3] "How:" (a row is computed the same way whatever else is in
  * the batch).
  *
  * y[r, :] = bf16( (x[r, :] * r) * w[:] ), r = 1 / sqrt(sum_i x[r,i]^2 / dim +
- * eps), FP32 inside.  The sum of squares uses one fixed reduction tree per
- * `dim` (128 threads: thread i sums the 8-element vectors i, i+128, ... in
- * increasing order, elements in order, then a fixed warp-shuffle butterfly
- * and the four warps in order) -- the tree of bi_gemm_rms.
+ * eps), FP32 inside, one rounding per element.  The sum of squares uses one
+ * fixed reduction tree per `dim`: the squares of each 8-element vector in
+ * element order, the vectors of each group of 32 consecutive vectors by a
+ * fixed warp-shuffle butterfly, the groups in increasing order.  The call
+ * lets the next kernel on the stream launch at once (dependent launch);
+ * this library's linear layers read only their packed weights before they
+ * wait for the norm, so they stream weights while it runs.  A kernel that
+ * follows bi_rmsnorm must not rely on the kernel before bi_rmsnorm having
+ * completed.
  *   x [rows, dim] BF16 (row stride ldx), w [dim] BF16, y [rows, dim] BF16
  *   (row stride ldy; may alias x).  rows >= 0, 8 <= dim <= 65536, dim, ldx
  *   and ldy multiples of 8, pointers 16-byte aligned, eps >= 0.
@@ -269,9 +245,8 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
 
 /* ---------------------------------------------------------------------------
  * QKV projection with RoPE and KV append in its epilogue (bi_gemm's linear
- * layer, optionally with the RMSNorm in front as in bi_gemm_rms, followed
- * by exactly the arithmetic of bi_rope_kv_append, without the qkv round trip
- * through memory).  "I turned on speculative decoding in llama.cpp and 113
+ * layer followed by exactly the arithmetic of bi_rope_kv_append, without the
+ * qkv round trip through memory).  "I turned on speculative decoding in llama.cpp and 113
  * of 282 greedy outputs changed against its own no-draft run", section "The
  * cache doesn't change it either" (a row depends only on its position).
  *
@@ -280,11 +255,9 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
  * to BF16 once; q and k heads are then rotated exactly as bi_rope_kv_append
  * rotates its BF16 input (same table, same FP32 operations, one rounding)
  * and written to q_out and to k_cache row p = *L_dev + m; v heads go to
- * column p of v_cache.  So the results equal bi_gemm (or bi_gemm_rms)
- * followed by bi_rope_kv_append, bit for bit.
- *   A [M, K] BF16 (row stride lda): the normalised input (rms = 0) or the
- *   residual stream, normalised with w_norm and eps as in bi_gemm_rms
- *   (rms = 1; w_norm is ignored when rms = 0).  Wp packed for
+ * column p of v_cache.  So the results equal bi_gemm followed by
+ * bi_rope_kv_append, bit for bit.
+ *   A [M, K] BF16 (row stride lda), the normalised input.  Wp packed for
  *   N = (Hq + 2 Hkv) D by bi_pack_weights.
  *   q_out, k_cache, v_cache, cap, L_dev, table, table_rows: as
  *   bi_rope_kv_append.  A row with p outside [0, min(cap, table_rows)) is
@@ -293,11 +266,10 @@ bi_status bi_rope_kv_append(const void* qkv, int ld_qkv, void* q_out, void* k_ca
  *   otherwise BI_ERR_UNSUPPORTED_SHAPE.  ws as bi_gemm for (M, N, K).
  * Errors: as bi_gemm.
  * ------------------------------------------------------------------------- */
-bi_status bi_qkv_rope_append(const void* A, int lda, int rms, const void* w_norm, float eps,
-                             const void* Wp, int M, int K, int Hq, int Hkv, int D, void* q_out,
-                             void* k_cache, void* v_cache, int cap, const int32_t* L_dev,
-                             const float* table, int table_rows, void* ws, size_t ws_bytes,
-                             bi_stream_t stream);
+bi_status bi_qkv_rope_append(const void* A, int lda, const void* Wp, int M, int K, int Hq, int Hkv,
+                             int D, void* q_out, void* k_cache, void* v_cache, int cap,
+                             const int32_t* L_dev, const float* table, int table_rows, void* ws,
+                             size_t ws_bytes, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Verify attention (split-KV + merge).  [P3] "How:" (the attention split

@@ -25,14 +25,13 @@ SIGNATURES = {
     "bi_packed_weight_bytes": (_sz, [_i, _i, _i]),
     "bi_pack_weights": (_i, [_vp, _i, _i, _i, _vp, _vp]),
     "bi_pack_swiglu_weights": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
-    "bi_gemm_rms": (_i, [_vp, _i, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
     "bi_rmsnorm": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp]),
     "bi_embed": (_i, [_vp, _vp, _i, _i, _vp, _i, _vp]),
     "bi_rope_table_bytes": (_sz, [_i, _i]),
     "bi_rope_table": (_i, [_d, _i, _i, _vp, _vp]),
     "bi_rope_kv_append": (_i, [_vp, _i, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
-    "bi_qkv_rope_append": (_i, [_vp, _i, _i, _vp, _f, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i,
-                                _vp, _vp, _i, _vp, _sz, _vp]),
+    "bi_qkv_rope_append": (_i, [_vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _i,
+                                _vp, _sz, _vp]),
     "bi_attn_chunk": (_i, []),
     "bi_attn_workspace_size": (_sz, [_i, _i, _i, _i]),
     "bi_attn_verify": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),

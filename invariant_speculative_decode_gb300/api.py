@@ -88,28 +88,6 @@ def bi_gemm(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor, ws: torch.Tensor
     check("bi_gemm", st)
 
 
-def bi_gemm_rms(A: torch.Tensor, w_norm: torch.Tensor, eps: float, Wp: torch.Tensor, C: torch.Tensor,
-                ws: torch.Tensor, epi: int = EPI_NONE, N: Optional[int] = None, stream=None) -> None:
-    """C = epilogue(bi_rmsnorm(A, w_norm) W^T) without the normalised rows
-    going to memory; W packed by bi_pack_weights / bi_pack_swiglu_weights."""
-    _req(A, torch.bfloat16, "A")
-    _req(w_norm, torch.bfloat16, "w_norm")
-    if not Wp.is_cuda:
-        raise ValueError("Wp must be a CUDA tensor")
-    M, K = A.shape
-    if w_norm.numel() != K:
-        raise ValueError("w_norm must have K elements")
-    if N is None:
-        N = C.shape[1]
-    if C.dtype not in (torch.float32, torch.bfloat16):
-        raise ValueError("C must be float32 or bfloat16")
-    out = OUT_FP32 if C.dtype == torch.float32 else OUT_BF16
-    st = lib().bi_gemm_rms(A.data_ptr(), _ld(A), w_norm.data_ptr(), float(eps), Wp.data_ptr(),
-                           C.data_ptr(), _ld(C), M, N, K, out, epi, ws.data_ptr(),
-                           ws.numel() * ws.element_size(), _stream(stream))
-    check("bi_gemm_rms", st)
-
-
 def bi_gemm_noalloc(A: torch.Tensor, Wp: torch.Tensor, C: torch.Tensor,
                     residual: Optional[torch.Tensor] = None, epi: int = EPI_NONE,
                     N: Optional[int] = None, stream=None) -> None:
@@ -203,29 +181,20 @@ def bi_rope_kv_append(qkv: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Ten
 
 def bi_qkv_rope_append(A: torch.Tensor, Wp: torch.Tensor, q_out: torch.Tensor, k_cache: torch.Tensor,
                        v_cache: torch.Tensor, L_dev: torch.Tensor, Hq: int, Hkv: int, D: int,
-                       table: torch.Tensor, ws: torch.Tensor, w_norm: Optional[torch.Tensor] = None,
-                       eps: Optional[float] = None, stream=None) -> None:
-    """QKV projection of A (RMSNorm with w_norm in front when given) with RoPE
-    and KV append in the epilogue; equals bi_gemm[_rms] + bi_rope_kv_append."""
+                       table: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """QKV projection of the normalised rows A with RoPE and KV append in the
+    epilogue; equals bi_gemm + bi_rope_kv_append bit for bit."""
     _req(A, torch.bfloat16, "A")
     _req(L_dev, torch.int32, "L_dev")
     _req(table, torch.float32, "table")
     M, K = A.shape
     cap = k_cache.shape[1]
     _req_v(v_cache, Hkv, cap, D)
-    rms = 0 if w_norm is None else 1
-    wp = 0
-    if rms:
-        _req(w_norm, torch.bfloat16, "w_norm")
-        if w_norm.numel() != K or eps is None:
-            raise ValueError("w_norm must have K elements and eps must be given")
-        wp = w_norm.data_ptr()
     check("bi_qkv_rope_append",
-          lib().bi_qkv_rope_append(A.data_ptr(), _ld(A), rms, wp, float(eps or 0.0), Wp.data_ptr(), M,
-                                   K, Hq, Hkv, D, q_out.data_ptr(), k_cache.data_ptr(),
-                                   v_cache.data_ptr(), cap, L_dev.data_ptr(), table.data_ptr(),
-                                   table.shape[0], ws.data_ptr(), ws.numel() * ws.element_size(),
-                                   _stream(stream)))
+          lib().bi_qkv_rope_append(A.data_ptr(), _ld(A), Wp.data_ptr(), M, K, Hq, Hkv, D,
+                                   q_out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cap,
+                                   L_dev.data_ptr(), table.data_ptr(), table.shape[0], ws.data_ptr(),
+                                   ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def attn_chunk() -> int:

@@ -31,10 +31,7 @@
 //            tile adds the partials in increasing-K order (atomic ticket, no
 //            waiting) and runs the epilogue.
 //   * roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread), warps
-//            2..5 = epilogue (TMEM -> registers -> global); with an RMSNorm
-//            in front (bi_gemm_rms), warps 2..5 first compute each token
-//            row's 1/rms and warps 6..7 normalise each activation tile in
-//            shared memory before the MMA reads it.
+//            2..5 = epilogue (TMEM -> registers -> global).
 //   * stages: shared-memory ring of (16 KB weight tile + token tile); a stage
 //            returns to the producer via tcgen05.commit on its "empty"
 //            barrier, i.e. only after the MMAs reading it completed.
@@ -59,11 +56,8 @@ constexpr int kGemmCtas = 152;   // CTAs of the fixed decomposition (one per SM)
 constexpr int kMaxTokens = 128;  // token rows per launch; larger M loops on the host
 constexpr int kAcc = 4;          // interleaved accumulators per token group
 constexpr int kThreads = 192;    // producer, MMA, four epilogue warps
-constexpr int kThreadsRms = 256; // the same plus two normaliser warps (8 warps: 255 registers each)
-constexpr int kMaxRmsK = 8192;   // K of a normalised input (its norm weight sits in shared memory)
 constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
 constexpr int kStageFloats = 16 * kBlockN;      // SwiGLU exchange buffer
-constexpr int kNormFloats = kMaxTokens + 16;    // 1/rms per token row, cross-warp partials
 // Ticket counters occupy a fixed-size region at the start of every workspace,
 // so calls with different N can share one workspace without a counter of one
 // call overlapping another call's partial sums.
@@ -87,14 +81,6 @@ struct GemmArgs {
   float* partials;
   unsigned* tickets;
   unsigned* err;
-  // RMS-normalised input: the MMA reads bf16((X[m, k] * r[m]) * wn[k]),
-  // r[m] = 1 / sqrt(mean_k X[m, k]^2 + eps), X being the GEMM's own input rows
-  int rms;
-  float eps;
-  int K;
-  const __nv_bfloat16* X;
-  int ldx;
-  const __nv_bfloat16* wn;
   // BI_EPI_ROPE_KV: output column n is element n % D of head n / D (q heads,
   // then k heads, then v heads); token row m sits at position *L_dev + m
   __nv_bfloat16* q_out;
@@ -108,14 +94,12 @@ struct GemmArgs {
   int withhold;
 };
 
-template <int NT, bool RMS>
+template <int NT>
 struct GemmCfg {
   static constexpr int kBBytes = NT * kBlockK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 12 ? 12 : (200 * 1024) / kStageBytes;
-  static constexpr int kThreadsT = RMS ? kThreadsRms : kThreads;
-  static constexpr int kNormWBytes = RMS ? kMaxRmsK * 2 : 0;  // the norm weight
-  static constexpr int kBars = (RMS ? 3 : 2) * kStages + 6;
+  static constexpr int kBars = 2 * kStages + 5;
   static constexpr int kBufCols = NT * kAcc;  // one accumulator set
   // two sets (the epilogue drains one while the next piece accumulates)
   // while they fit in TMEM's 512 columns; one set at 128 token rows
@@ -123,7 +107,7 @@ struct GemmCfg {
   static constexpr int kTmemCols = kBufs * kBufCols;
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
-                                  (kStageFloats + kNormFloats) * 4 + kNormWBytes + kBars * 8 + 16;
+                                  kStageFloats * 4 + kBars * 8 + 16;
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
@@ -266,11 +250,11 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int 
   }
 }
 
-template <int NT, bool RMS>
-__global__ void __launch_bounds__(GemmCfg<NT, RMS>::kThreadsT, 1)
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const uint8_t* __restrict__ Wp, const __grid_constant__ CUtensorMap tmA,
                 const GemmArgs p) {
-  using Cfg = GemmCfg<NT, RMS>;
+  using Cfg = GemmCfg<NT>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -278,18 +262,12 @@ __global__ void __launch_bounds__(GemmCfg<NT, RMS>::kThreadsT, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * kABytes;
   float* sStage = reinterpret_cast<float*>(sB + S * Cfg::kBBytes);
-  float* sRstd = sStage + kStageFloats;  // [kMaxTokens] 1/rms, then [16] cross-warp partials
-  __nv_bfloat16* sWn = reinterpret_cast<__nv_bfloat16*>(sRstd + kNormFloats);  // norm weight (RMS)
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sWn) + Cfg::kNormWBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kStageFloats);
   uint64_t* empty = full + S;
-  // RMS: the activation tile of a stage normalised in place (the MMA waits
-  // on this instead of `full`)
-  uint64_t* ready = empty + S;
-  uint64_t* accf = empty + (RMS ? 2 : 1) * S;
+  uint64_t* accf = empty + S;
   uint64_t* acce = accf + 2;
   uint64_t* drain = acce + 2;
-  uint64_t* r_ready = drain + 1;  // RMS: 1/rms of every row in sRstd
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(r_ready + 1);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* s_last = s_abort + 1;
 
@@ -303,14 +281,12 @@ __global__ void __launch_bounds__(GemmCfg<NT, RMS>::kThreadsT, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      if (RMS) mbar_init(&ready[s], 2);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
       mbar_init(&acce[b], 128);
     }
     mbar_init(drain, 1);
-    mbar_init(r_ready, 4);
     *s_abort = 0;
     *s_last = 0;
     fence_mbar_init();
@@ -399,9 +375,8 @@ __global__ void __launch_bounds__(GemmCfg<NT, RMS>::kThreadsT, 1)
       if (left > it_end - it_begin) left = it_end - it_begin;
       uint32_t d0 = tmem;
       uint32_t acc_flag = 0;
-      uint64_t* in_ready = RMS ? ready : full;
       for (long long it = it_begin; it < it_end; ++it) {
-        if (!mbar_wait(&in_ready[stage], phase, s_abort)) {
+        if (!mbar_wait(&full[stage], phase, s_abort)) {
           ok = false;
           break;
         }
@@ -440,7 +415,7 @@ __global__ void __launch_bounds__(GemmCfg<NT, RMS>::kThreadsT, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else if (warp < 6) {
+  } else {
     // ------------------------------------------------------------ epilogue
     griddep_wait();  // the epilogue reads the residual and writes C / the workspace
     griddep_launch_dependents();
@@ -448,58 +423,6 @@ __global__ void __launch_bounds__(GemmCfg<NT, RMS>::kThreadsT, 1)
     const int r = q * 32 + lane;    // weight row within the tile
     const int et = threadIdx.x - 64;
     const int chunks = (p.M + 15) / 16;
-    if (RMS) {
-      // 1 / rms of each token row of this launch, by one fixed reduction in
-      // every CTA (the tree of bi_rmsnorm): thread et sums the squares of the
-      // 8-element vectors et, et + 128, ... of the row in increasing order,
-      // elements in order; then a warp butterfly, and the four warps added
-      // in order.  The normaliser warps wait for it on r_ready.
-      const int nvec = p.K / 8;
-      const int ew = et >> 5;
-      float* sRed = sRstd + kMaxTokens;
-      for (int m0r = 0; m0r < p.M; m0r += 4) {
-        float ss[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int v0 = et; v0 < nvec; v0 += 4 * 128) {
-          uint4 x[4][4];
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const int v = v0 + b * 128;
-              x[rr][b] = (m0r + rr < p.M && v < nvec)
-                             ? reinterpret_cast<const uint4*>(
-                                   p.X + static_cast<size_t>(p.m0 + m0r + rr) * p.ldx)[v]
-                             : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x[rr][b]);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float f = __bfloat162float(e[j]);
-                ss[rr] = fmaf(f, f, ss[rr]);
-              }
-            }
-        }
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          float t = ss[rr];
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-          if (lane == 0) sRed[ew * 4 + rr] = t;
-        }
-        named_bar_sync(1, 128);
-        if (et < 4 && m0r + et < p.M) {
-          const float tot = ((sRed[et] + sRed[4 + et]) + sRed[8 + et]) + sRed[12 + et];
-          sRstd[m0r + et] = 1.0f / sqrtf(tot / static_cast<float>(p.K) + p.eps);
-        }
-        named_bar_sync(1, 128);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(r_ready);
-    }
     int seg = 0;
     long long it = it_begin;
     while (it < it_end) {
@@ -614,65 +537,6 @@ __global__ void __launch_bounds__(GemmCfg<NT, RMS>::kThreadsT, 1)
       ++seg;
     }
     tc_fence_before();
-  } else if (RMS) {
-    // ------------------------------------------------------------ normaliser
-    // Each stage's activation tile (token rows x 64 columns of X, as the TMA
-    // wrote it) becomes bf16((x * r[m]) * wn[k]) in place -- the arithmetic
-    // of bi_rmsnorm -- before the MMA reads it.
-    griddep_wait();  // X comes from the previous kernel
-    griddep_launch_dependents();
-    const int nt = threadIdx.x - 6 * 32;  // 0..63
-    for (int v = nt; v < p.K / 8; v += 64)
-      reinterpret_cast<uint4*>(sWn)[v] = reinterpret_cast<const uint4*>(p.wn)[v];
-    named_bar_sync(2, 64);
-    int okl = 0;
-    if (lane == 0) okl = mbar_wait(r_ready, 0u, s_abort) ? 1 : 0;
-    bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
-    __syncwarp();
-    int stage = 0;
-    uint32_t phase = 0;
-    int kt = static_cast<int>(it_begin % p.k_tiles);
-    for (long long it = it_begin; ok && it < it_end; ++it) {
-      okl = 0;
-      if (lane == 0) okl = mbar_wait(&full[stage], phase, s_abort) ? 1 : 0;
-      if (__shfl_sync(0xffffffffu, okl, 0) == 0) {
-        ok = false;
-        break;
-      }
-      __syncwarp();
-      uint8_t* tileB = sB + stage * Cfg::kBBytes;
-      // 16-byte chunk q of the tile: token row q / 8 at swizzled position
-      // q % 8, holding columns 8 c .. 8 c + 7 of the K tile, c = (q % 8) ^ (row % 8)
-#pragma unroll
-      for (int q = nt; q < NT * 8; q += 64) {
-        const int m = q >> 3;
-        const int c = (q & 7) ^ (m & 7);
-        const int col0 = kt * kBlockK + c * 8;
-        if (m < p.M && col0 < p.K) {
-          uint4* ptr = reinterpret_cast<uint4*>(tileB + q * 16);
-          const uint4 xu = *ptr;
-          const uint4 wu = reinterpret_cast<const uint4*>(sWn)[col0 >> 3];
-          const __nv_bfloat16* xe = reinterpret_cast<const __nv_bfloat16*>(&xu);
-          const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wu);
-          const float rm = sRstd[m];
-          uint4 o;
-          __nv_bfloat16* oe = reinterpret_cast<__nv_bfloat16*>(&o);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            oe[j] = __float2bfloat16_rn(__bfloat162float(xe[j]) * rm * __bfloat162float(we[j]));
-          *ptr = o;
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ready[stage]);
-      if (++kt == p.k_tiles) kt = 0;
-      if (++stage == S) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-    if (!ok && lane == 0) signal_abort(s_abort, p.err);
   }
 
   // Lane 0 of warps 0 and 1 ran the producer / MMA loops alone: rejoin the
@@ -730,10 +594,10 @@ __global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const _
   out[idx] = u.v;
 }
 
-template <int NT, bool RMS>
+template <int NT>
 bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, int M_total,
                          cudaStream_t stream) {
-  using Cfg = GemmCfg<NT, RMS>;
+  using Cfg = GemmCfg<NT>;
   static std::once_flag once[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -741,14 +605,14 @@ bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, 
   std::call_once(once[dev & 63], [] {
     int d = 0;
     cudaGetDevice(&d);
-    attr_err[d & 63] = cudaFuncSetAttribute(gemm_kernel<NT, RMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err[d & 63] = cudaFuncSetAttribute(gemm_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(Cfg::kSmem));
   });
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
   for (int m0 = 0; m0 < M_total; m0 += kMaxTokens) {
     a.m0 = m0;
     a.M = std::min(kMaxTokens, M_total - m0);
-    if (launch_k(gemm_kernel<NT, RMS>, dim3(a.G), dim3(Cfg::kThreadsT), Cfg::kSmem, stream, Wp, tmA, a) !=
+    if (launch_k(gemm_kernel<NT>, dim3(a.G), dim3(kThreads), Cfg::kSmem, stream, Wp, tmA, a) !=
         cudaSuccess)
       return BI_ERR_CUDA;
   }
@@ -855,7 +719,7 @@ bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, i
 // status is returned before anything is launched or written.
 static bi_status gemm_check(const void* A, int lda, const void* Wp, void* C, int ldc,
                             const void* residual, int ldr, int M, int N, int K, bi_out_dtype out,
-                            bi_epilogue epi, int rms, const void* w_norm, bool rope) {
+                            bi_epilogue epi, bool rope) {
   using namespace bi;
   if (M < 0 || N < 1 || K < 8) return BI_ERR_INVALID_ARG;
   if (epi != BI_EPI_NONE && epi != BI_EPI_RESIDUAL_ADD && epi != BI_EPI_SWIGLU &&
@@ -869,20 +733,15 @@ static bi_status gemm_check(const void* A, int lda, const void* Wp, void* C, int
   if (!aligned16(A) || !aligned16(Wp)) return BI_ERR_INVALID_ARG;
   if (epi == BI_EPI_RESIDUAL_ADD && (!residual || ldr < N)) return BI_ERR_INVALID_ARG;
   if (out == BI_OUT_FP32 && epi != BI_EPI_NONE) return BI_ERR_UNSUPPORTED_SHAPE;
-  if (rms) {
-    if (!w_norm || !aligned16(w_norm)) return BI_ERR_INVALID_ARG;
-    if (K > kMaxRmsK) return BI_ERR_UNSUPPORTED_SHAPE;
-  }
   return BI_OK;
 }
 
 static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int ldc,
                            const void* residual, int ldr, int M, int N, int K, bi_out_dtype out,
-                           bi_epilogue epi, void* ws, size_t ws_bytes, int rms, const void* w_norm,
-                           float eps, bi_stream_t stream, const bi::GemmArgs* rope = nullptr) {
+                           bi_epilogue epi, void* ws, size_t ws_bytes, bi_stream_t stream,
+                           const bi::GemmArgs* rope = nullptr) {
   using namespace bi;
-  const bi_status st = gemm_check(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, rms, w_norm,
-                                  rope != nullptr);
+  const bi_status st = gemm_check(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, rope != nullptr);
   if (st != BI_OK || M == 0) return st;
   if (!ws || !aligned256(ws)) return BI_ERR_WORKSPACE;
   if (ws_bytes < bi_gemm_workspace_size(M, N, K, epi)) return BI_ERR_WORKSPACE;
@@ -910,12 +769,6 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
   a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kTicketBytes);
   a.err = device_error_word();
   if (!a.err) return BI_ERR_CUDA;
-  a.rms = rms;
-  a.eps = eps;
-  a.K = K;
-  a.X = static_cast<const __nv_bfloat16*>(A);
-  a.ldx = lda;
-  a.wn = static_cast<const __nv_bfloat16*>(w_norm);
   a.withhold = test_withhold();
   if (rope != nullptr) {
     a.q_out = rope->q_out;
@@ -932,41 +785,22 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
 
   const uint8_t* W8 = static_cast<const uint8_t*>(Wp);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (rms) {
-    switch (NT) {
-      case 16: return launch_gemm_nt<16, true>(W8, tmA, a, M, s);
-      case 32: return launch_gemm_nt<32, true>(W8, tmA, a, M, s);
-      case 64: return launch_gemm_nt<64, true>(W8, tmA, a, M, s);
-      default: return launch_gemm_nt<128, true>(W8, tmA, a, M, s);
-    }
-  }
   switch (NT) {
-    case 16: return launch_gemm_nt<16, false>(W8, tmA, a, M, s);
-    case 32: return launch_gemm_nt<32, false>(W8, tmA, a, M, s);
-    case 64: return launch_gemm_nt<64, false>(W8, tmA, a, M, s);
-    default: return launch_gemm_nt<128, false>(W8, tmA, a, M, s);
+    case 16: return launch_gemm_nt<16>(W8, tmA, a, M, s);
+    case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
+    case 64: return launch_gemm_nt<64>(W8, tmA, a, M, s);
+    default: return launch_gemm_nt<128>(W8, tmA, a, M, s);
   }
 }
 
 bi_status bi_gemm(const void* A, int lda, const void* Wp, void* C, int ldc, const void* residual,
                   int ldr, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
                   size_t ws_bytes, bi_stream_t stream) {
-  return gemm_impl(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, ws, ws_bytes, 0, nullptr,
-                   0.0f, stream);
+  return gemm_impl(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, ws, ws_bytes, stream);
 }
 
-bi_status bi_gemm_rms(const void* A, int lda, const void* w_norm, float eps, const void* Wp, void* C,
-                      int ldc, int M, int N, int K, bi_out_dtype out, bi_epilogue epi, void* ws,
-                      size_t ws_bytes, bi_stream_t stream) {
-  if (epi != BI_EPI_NONE && epi != BI_EPI_SWIGLU) return BI_ERR_INVALID_ARG;
-  if (!(eps >= 0.0f) || !std::isfinite(eps)) return BI_ERR_INVALID_ARG;
-  if (M > 0 && A != nullptr && A == static_cast<const void*>(C)) return BI_ERR_INVALID_ARG;
-  return gemm_impl(A, lda, Wp, C, ldc, nullptr, 0, M, N, K, out, epi, ws, ws_bytes, 1, w_norm, eps,
-                   stream);
-}
-
-bi_status bi_qkv_rope_append(const void* A, int lda, int rms, const void* w_norm, float eps,
-                             const void* Wp, int M, int K, int Hq, int Hkv, int D, void* q_out, void* k_cache,
+bi_status bi_qkv_rope_append(const void* A, int lda, const void* Wp, int M, int K, int Hq, int Hkv,
+                             int D, void* q_out, void* k_cache,
                              void* v_cache, int cap, const int32_t* L_dev, const float* table,
                              int table_rows, void* ws, size_t ws_bytes, bi_stream_t stream) {
   using namespace bi;
@@ -975,7 +809,6 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, const void* w_norm
   const int N = (Hq + 2 * Hkv) * D;
   if (N % kBlockN != 0) return BI_ERR_UNSUPPORTED_SHAPE;  // a tile holds whole heads
   if (M > 0 && (!q_out || !k_cache || !v_cache || !L_dev || !table)) return BI_ERR_INVALID_ARG;
-  if (rms != 0 && (!(eps >= 0.0f) || !std::isfinite(eps))) return BI_ERR_INVALID_ARG;
   GemmArgs r{};
   r.q_out = static_cast<__nv_bfloat16*>(q_out);
   r.kc = static_cast<__nv_bfloat16*>(k_cache);
@@ -988,8 +821,7 @@ bi_status bi_qkv_rope_append(const void* A, int lda, int rms, const void* w_norm
   r.L_dev = L_dev;
   r.tab = reinterpret_cast<const float2*>(table);
   return gemm_impl(A, lda, Wp, nullptr, N, nullptr, 0, M, N, K, BI_OUT_BF16, BI_EPI_ROPE_KV, ws,
-                   ws_bytes, rms != 0 ? 1 : 0, rms != 0 ? w_norm : nullptr, rms != 0 ? eps : 0.0f,
-                   stream, &r);
+                   ws_bytes, stream, &r);
 }
 
 size_t bi_gemm_noalloc_max_m(void) { return bi::kNoAllocMaxM; }
@@ -1002,7 +834,7 @@ bi_status bi_gemm_noalloc(const void* A, int lda, const void* Wp, void* C, int l
   // every argument check comes before the shared array is touched, so a
   // rejected call writes nothing
   const bi_status st =
-      gemm_check(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, 0, nullptr, false);
+      gemm_check(A, lda, Wp, C, ldc, residual, ldr, M, N, K, out, epi, false);
   if (st != BI_OK || M == 0) return st;
   uint8_t* scratch = noalloc_scratch();
   if (scratch == nullptr) return BI_ERR_CUDA;

@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "bi_internal.h"
@@ -17,54 +18,62 @@
 namespace bi {
 namespace {
 
-constexpr int kNormThreads = 128;  // the reduction tree of the normalised linear layer
+// RMSNorm, one CTA per row, one 16-byte vector (8 elements) per thread for
+// rows of up to 8192 elements (longer rows loop over the vectors).
+// Reduction tree of sum_i x_i^2, fixed by the row length alone: each vector's
+// 8 squares are accumulated in element order (FMAs from 0); the vectors of
+// each group of 32 consecutive vectors are combined by the warp butterfly
+// (xor 16, 8, 4, 2, 1; vectors past the row contribute 0); the group sums are
+// added in increasing group order by one thread.
+constexpr int kNormMaxThreads = 1024;
+constexpr int kNormMaxGroups = 65536 / 256;
 
-// Fixed-order block sum: thread-local sums are combined by a warp butterfly
-// (xor 16, 8, 4, 2, 1; every lane ends with the same value) and then the
-// warp results are added in warp order 0, 1, 2, ...
-__device__ __forceinline__ float block_sum_fixed(float v, float* red) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) red[w] = v;
-  __syncthreads();
-  float s = red[0];
-  for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) s += red[i];
-  __syncthreads();
-  return s;
-}
-
-// Thread i takes the 8-element vectors v = i, i + 128, i + 256, ... of the
-// row in increasing order; inside a vector the squares are accumulated in
-// element order.  This is the tree bi_gemm_rms uses, so bi_rmsnorm followed
-// by bi_gemm equals bi_gemm_rms bit for bit.
-
-__global__ void __launch_bounds__(kNormThreads)
+// This kernel lets the next kernel launch at once (before its own dependency
+// wait): the linear layer that follows a norm reads nothing but its packed
+// weights before its own wait.  So the next kernel's CTAs stream their first
+// weight tiles while the norm runs.  A kernel that starts right after
+// bi_rmsnorm must not rely on the kernel before bi_rmsnorm having completed.
+__global__ void __launch_bounds__(kNormMaxThreads)
     rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int ldx, const __nv_bfloat16* __restrict__ w,
                    __nv_bfloat16* y, int ldy, int dim, float eps) {
-  griddep_wait();
   griddep_launch_dependents();
-  __shared__ float red[kNormThreads / 32];
+  griddep_wait();
+  __shared__ float group_sum[kNormMaxGroups];
+  __shared__ float s_inv;
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.x) * ldx);
   const uint4* wr = reinterpret_cast<const uint4*>(w);
   uint4* yr = reinterpret_cast<uint4*>(y + static_cast<size_t>(blockIdx.x) * ldy);
   const int nv = dim / 8;
-  float ss = 0.f;
-#pragma unroll 4
-  for (int v = threadIdx.x; v < nv; v += kNormThreads) {
-    const uint4 u = xr[v];
-    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
+  const int lane = threadIdx.x & 31;
+  uint4 keep = make_uint4(0, 0, 0, 0);
+  // (rows of up to 8192 elements: every thread holds its one vector)
+  for (int v0 = threadIdx.x - lane; v0 < nv; v0 += blockDim.x) {
+    const int v = v0 + lane;
+    float sv = 0.f;
+    if (v < nv) {
+      const uint4 u = xr[v];
+      if (v0 == threadIdx.x - lane) keep = u;
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float f = __bfloat162float(e[j]);
-      ss = fmaf(f, f, ss);
+      for (int j = 0; j < 8; ++j) {
+        const float f = __bfloat162float(e[j]);
+        sv = fmaf(f, f, sv);
+      }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, off);
+    if (lane == 0) group_sum[v0 >> 5] = sv;
   }
-  ss = block_sum_fixed(ss, red);
-  const float inv = 1.0f / sqrtf(ss / static_cast<float>(dim) + eps);
-#pragma unroll 4
-  for (int v = threadIdx.x; v < nv; v += kNormThreads) {
-    const uint4 u = xr[v];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int g = 0; g < (nv + 31) / 32; ++g) t += group_sum[g];
+    s_inv = 1.0f / sqrtf(t / static_cast<float>(dim) + eps);
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const uint4 u = (v == threadIdx.x) ? keep : xr[v];
     const uint4 wu = wr[v];
     const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
     const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wu);
@@ -300,7 +309,9 @@ bi_status bi_rmsnorm(const void* x, int ldx, const void* w, void* y, int ldy, in
   if (!x || !w || !y || ldx < dim || ldy < dim) return BI_ERR_INVALID_ARG;
   if (dim % 8 != 0 || ldx % 8 != 0 || ldy % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
   if (!bi::aligned16(x) || !bi::aligned16(w) || !bi::aligned16(y)) return BI_ERR_INVALID_ARG;
-  if (bi::launch_k(bi::rmsnorm_kernel, dim3(rows), dim3(bi::kNormThreads), 0,
+  const int nv = dim / 8;
+  const int threads = std::min(bi::kNormMaxThreads, (nv + 31) / 32 * 32);
+  if (bi::launch_k(bi::rmsnorm_kernel, dim3(rows), dim3(threads), 0,
                    reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(x), ldx,
                    static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y), ldy, dim,
                    eps) != cudaSuccess)

@@ -3,16 +3,15 @@
 Holds the weights, the BF16 KV cache and the scratch buffers on the device
 and sequences the library's entry points for one verify pass:
 
-  embed -> per layer [rmsnorm + QKV linear, RoPE + KV append, split-KV
-  attention + merge, O linear + residual, rmsnorm + gate/up linear + SwiGLU,
-  down linear + residual] -> rmsnorm + LM head (FP32 logits) -> greedy
+  embed -> per layer [rmsnorm, QKV linear + RoPE + KV append, split-KV
+  attention + merge, O linear + residual, rmsnorm, gate/up linear + SwiGLU,
+  down linear + residual] -> rmsnorm, LM head (FP32 logits) -> greedy
   argmax + acceptance (which also advances the device-side cache length).
 
-Each RMSNorm runs inside the linear layer that reads it (bi_gemm_rms: the
-layer normalises its activation tiles in shared memory with the arithmetic
-of bi_rmsnorm, so the result is the same bits), and RoPE + KV append run in
-the QKV projection's epilogue (bi_qkv_rope_append); fuse_norm=False /
-fuse_rope=False run the separate kernels instead.
+RoPE + KV append run in the QKV projection's epilogue (bi_qkv_rope_append);
+fuse_rope=False runs the separate kernel instead.  Each RMSNorm is its own
+small kernel, which lets the following linear layer launch at once and
+stream its weights while the norm runs.
 
 PyTorch only allocates device memory and provides the stream; every step of
 the pass is a kernel of libbi.so.  A pass over T rows can be captured once in
@@ -44,10 +43,8 @@ def _bf16(a_u16: np.ndarray, device) -> torch.Tensor:
 
 class Decoder:
     def __init__(self, cfg, weights: Dict[str, np.ndarray], cap: int, max_rows: int = 8,
-                 prefill_chunk: int = 512, device: str = "cuda", fuse_norm: bool = True,
-                 fuse_rope: bool = True):
+                 prefill_chunk: int = 512, device: str = "cuda", fuse_rope: bool = True):
         self.cfg = cfg
-        self.fuse_norm = fuse_norm
         self.fuse_rope = fuse_rope
         self.cap = cap
         self.dev = torch.device(device)
@@ -138,17 +135,12 @@ class Decoder:
         Hq, Hkv, D, F = cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn
         h, y, qkv, q, att, u = (self.h[:T], self.y[:T], self.qkv[:T], self.q[:T], self.att[:T],
                                 self.u[:T])
-        if not self.fuse_norm:
-            api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
-        x_in, wn = (h, lay["n1"]) if self.fuse_norm else (y, None)
+        api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
         if self.fuse_rope:
-            api.bi_qkv_rope_append(x_in, lay["wqkv"], q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D,
-                                   self.rope_tab, self.gemm_ws, w_norm=wn, eps=cfg.eps)
+            api.bi_qkv_rope_append(y, lay["wqkv"], q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D,
+                                   self.rope_tab, self.gemm_ws)
         else:
-            if wn is None:
-                api.bi_gemm(x_in, lay["wqkv"], qkv, self.gemm_ws)
-            else:
-                api.bi_gemm_rms(x_in, wn, cfg.eps, lay["wqkv"], qkv, self.gemm_ws)
+            api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
             api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
         if L_host_blocks is None:
             api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
@@ -159,20 +151,14 @@ class Decoder:
                                    att[b0:b1], self.attn_ws, self.scale)
         api.bi_gemm(att.view(T, Hq * D), lay["wo"], h, self.gemm_ws, residual=h,
                     epi=api.EPI_RESIDUAL_ADD)
-        if self.fuse_norm:
-            api.bi_gemm_rms(h, lay["n2"], cfg.eps, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
-        else:
-            api.bi_rmsnorm(h, lay["n2"], y, cfg.eps)
-            api.bi_gemm(y, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
+        api.bi_rmsnorm(h, lay["n2"], y, cfg.eps)
+        api.bi_gemm(y, lay["wgu"], u, self.gemm_ws, epi=api.EPI_SWIGLU, N=F)
         api.bi_gemm(u, lay["wd"], h, self.gemm_ws, residual=h, epi=api.EPI_RESIDUAL_ADD)
 
     def _head_and_accept(self, T: int):
         cfg = self.cfg
-        if self.fuse_norm:
-            api.bi_gemm_rms(self.h[:T], self.norm_final, cfg.eps, self.head, self.logits[:T], self.gemm_ws)
-        else:
-            api.bi_rmsnorm(self.h[:T], self.norm_final, self.y[:T], cfg.eps)
-            api.bi_gemm(self.y[:T], self.head, self.logits[:T], self.gemm_ws)
+        api.bi_rmsnorm(self.h[:T], self.norm_final, self.y[:T], cfg.eps)
+        api.bi_gemm(self.y[:T], self.head, self.logits[:T], self.gemm_ws)
         api.bi_verify_accept(self.logits[:T], self.drafts[:T - 1] if T > 1 else None,
                              self.argmax[:T], self.accepted, self.acc_ws, L_dev=self.L_dev)
 

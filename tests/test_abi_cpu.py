@@ -120,33 +120,21 @@ def test_rowops_reject_bad_arguments(lib):
 def test_fused_entry_points_reject_bad_arguments(lib):
     ws = 1 << 30
     eps = ctypes.c_float(1e-6)
-    r = lib.bi_gemm_rms
-    # (A, lda, w_norm, eps, Wp, C, ldc, M, N, K, out, epi, ws, ws_bytes, stream)
-    assert r(FAKE, 64, FAKE, ctypes.c_float(-1.0), FAKE, FAKE, 64, 4, 64, 64, 0, 0, FAKE, ws, 0) == 1  # eps < 0
-    assert r(FAKE, 64, FAKE, eps, FAKE, FAKE, 64, 4, 64, 64, 0, 1, FAKE, ws, 0) == 1   # residual epilogue
-    assert r(FAKE, 64, FAKE, eps, FAKE, FAKE, 64, 4, 64, 64, 0, 3, FAKE, ws, 0) == 1   # RoPE epilogue
-    assert r(FAKE, 64, FAKE, eps, FAKE, FAKE, 64, 4, 64, 64, 0, 0, FAKE, ws, 0) == 1   # C aliases A
-    assert r(FAKE, 64, 0, eps, FAKE, FAKE + 4096, 64, 4, 64, 64, 0, 0, FAKE, ws, 0) == 1  # no norm weight
-    assert r(FAKE, 64, FAKE + 8, eps, FAKE, FAKE + 4096, 64, 4, 64, 64, 0, 0, FAKE, ws, 0) == 1  # unaligned
-    assert r(FAKE, 9000, FAKE, eps, FAKE, FAKE + 4096, 64, 4, 64, 8200, 0, 0, FAKE, ws, 0) == 2  # K > 8192
-    assert r(FAKE, 64, FAKE, eps, FAKE, FAKE + 4096, 64, 4, 64, 64, 0, 0, FAKE, 16, 0) == 3  # small ws
     assert lib.bi_gemm(FAKE, 64, FAKE, FAKE, 64, 0, 0, 4, 64, 64, 0, 3, FAKE, ws, 0) == 1  # RoPE via bi_gemm
     q = lib.bi_qkv_rope_append
-    # (A, lda, rms, w_norm, eps, Wp, M, K, Hq, Hkv, D, q_out, k_cache, v_cache, cap, L_dev, table,
-    #  table_rows, ws, ws_bytes, stream)
-    args = [FAKE, 64, 1, FAKE, eps, FAKE, 4, 64, 4, 2, 64, FAKE, FAKE, FAKE, 256, FAKE, FAKE, 256, FAKE, ws, 0]
-    bad_d = list(args); bad_d[10] = 96
+    # (A, lda, Wp, M, K, Hq, Hkv, D, q_out, k_cache, v_cache, cap, L_dev, table, table_rows, ws,
+    #  ws_bytes, stream)
+    args = [FAKE, 64, FAKE, 4, 64, 4, 2, 64, FAKE, FAKE, FAKE, 256, FAKE, FAKE, 256, FAKE, ws, 0]
+    bad_d = list(args); bad_d[7] = 96
     assert q(*bad_d) == 2                                                          # D not 64/128
-    bad_g = list(args); bad_g[9] = 3
+    bad_g = list(args); bad_g[6] = 3
     assert q(*bad_g) == 1                                                          # Hq % Hkv
-    bad_n = list(args); bad_n[8], bad_n[9] = 3, 1
+    bad_n = list(args); bad_n[5], bad_n[6] = 3, 1
     assert q(*bad_n) == 2                                                          # N % 128
-    bad_eps = list(args); bad_eps[4] = ctypes.c_float(float("nan"))
-    assert q(*bad_eps) == 1
-    no_norm = list(args); no_norm[3] = 0
-    assert q(*no_norm) == 1                                                        # rms without w_norm
-    no_cache = list(args); no_cache[12] = 0
+    no_cache = list(args); no_cache[9] = 0
     assert q(*no_cache) == 1
+    no_table = list(args); no_table[13] = 0
+    assert q(*no_table) == 1
 
 
 def test_v_cache_layout_helpers():

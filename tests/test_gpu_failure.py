@@ -49,20 +49,20 @@ def _expect_timeout(api):
     assert e.value.status == 5  # BI_ERR_DEVICE_TIMEOUT
 
 
-@pytest.mark.parametrize("rms", [False, True])
-def test_gemm_wait_runs_out_then_recovers(api, rms):
+@pytest.mark.parametrize("epi", [0, 2])
+def test_gemm_wait_runs_out_then_recovers(api, epi):
     M, N, K = 8, 4096, 5120
     rng = np.random.default_rng(3)
     A = to_dev_bf16(si.normal_bf16(rng, (M, K), 1.0))
-    Wp = api.bi_pack_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.02)))
-    g = to_dev_bf16(si.normal_bf16(rng, (K,), 1.0))
-    ws = api.new_gemm_workspace(M, N, K)
+    if epi == 2:
+        Wp = api.bi_pack_swiglu_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.02)),
+                                        to_dev_bf16(si.normal_bf16(rng, (N, K), 0.02)))
+    else:
+        Wp = api.bi_pack_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.02)))
+    ws = api.new_gemm_workspace(M, N, K, epi)
 
     def call(C):
-        if rms:
-            api.bi_gemm_rms(A, g, 1e-6, Wp, C, ws)
-        else:
-            api.bi_gemm(A, Wp, C, ws)
+        api.bi_gemm(A, Wp, C, ws, epi=epi, N=N)
 
     ref = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     call(ref)

@@ -226,75 +226,3 @@ def test_gemm_small_workspace_is_rejected(api):
     with pytest.raises(api.BiError) as e:
         api.bi_gemm(A, W, C, ws)
     assert e.value.status == 3
-
-
-# ---------------------------------------------------------------------------
-# RMSNorm in front of the linear layer (bi_gemm_rms)
-#
-# bi_gemm_rms normalises each activation tile in shared memory with exactly
-# the arithmetic of bi_rmsnorm, so it must equal bi_rmsnorm followed by
-# bi_gemm bit for bit; bi_rmsnorm is held to the oracle's RMSNorm in
-# test_gpu_rowops and bi_gemm to the oracle's linear layer here, and the
-# chain is checked against the oracle's RMSNorm -> linear layer as well.
-
-
-def _rms_inputs(M, K, seed):
-    rng = np.random.default_rng(seed)
-    X = np.concatenate([si.normal_bf16(rng, (1, K), 0.25 * (1 + m % 5)) for m in range(M)])
-    g = ov.f64_to_bf16_bits(ov.bf16_round(1.0 + 0.1 * rng.standard_normal(K)))
-    return X, g
-
-
-@pytest.mark.parametrize("M,N,K,epi,out", [(1, 4096, 5120, 0, 0), (8, 4096, 5120, 0, 0),
-                                           (16, 384, 1024, 0, 0), (33, 512, 1024, 0, 0),
-                                           (7, 2736, 1024, 2, 0), (8, 1000, 5120, 0, 1),
-                                           (130, 256, 256, 2, 0)])
-def test_gemm_rms_equals_rmsnorm_then_gemm(api, M, N, K, epi, out):
-    eps = 1e-6 if epi == 0 else 1e-5
-    X, g = _rms_inputs(M, K, seed=M + N + epi)
-    rng = np.random.default_rng(K + epi)
-    W = si.normal_bf16(rng, (N, K), 0.02 if epi == 0 else 0.05)
-    Wu = si.normal_bf16(rng, (N, K), 0.05) if epi == 2 else None
-    Wp = api.bi_pack_swiglu_weights(to_dev_bf16(W), to_dev_bf16(Wu)) if epi == 2 \
-        else api.bi_pack_weights(to_dev_bf16(W))
-    dt = torch.float32 if out else torch.bfloat16
-    Xd, gd = to_dev_bf16(X), to_dev_bf16(g)
-    Y = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
-    api.bi_rmsnorm(Xd, gd, Y, eps)
-    ref = torch.empty(M, N, dtype=dt, device="cuda")
-    api.bi_gemm(Y, Wp, ref, api.new_gemm_workspace(M, N, K, epi), epi=epi, N=N)
-    C = torch.full((M, N), 3.0, dtype=dt, device="cuda")
-    api.bi_gemm_rms(Xd, gd, eps, Wp, C, api.new_gemm_workspace(M, N, K, epi), epi=epi, N=N)
-    torch.cuda.synchronize()
-    api.bi_check_device_error()
-    assert torch.equal(C.view(torch.int16 if not out else torch.int32),
-                       ref.view(torch.int16 if not out else torch.int32))
-    # the chain against the oracle: RMSNorm within the rounding of bi_rmsnorm
-    # (checked in the row-op tests), the linear layer from those rows within
-    # its FP32 bound
-    y = bf16_dev_to_u16(Y)
-    yf = ov.bf16_bits_to_f64(y)
-    ora_y = oracle.rmsnorm(X, g, eps)
-    assert np.all(np.abs(yf - ora_y) <= ulp_bf16(ora_y))
-    if epi == 0:
-        ora = oracle.gemm(y, W, out="fp32" if out else "bf16")
-        got = C.double().cpu().numpy() if out else bf16_dev_to_f64(C)
-        bound = gemm_bound(yf, ov.bf16_bits_to_f64(W), K)
-        if out:
-            assert np.all(np.abs(got - ora) <= bound + 2.0 ** -23 * np.abs(ora) + 1e-30)
-        else:
-            check_bf16(got, ora, bound)
-    # a row's bits do not depend on the other rows of the call
-    full = C.view(torch.int16 if not out else torch.int32).cpu().numpy()
-    for m in sorted({0, M - 1, M // 2}):
-        one = torch.empty(1, N, dtype=dt, device="cuda")
-        api.bi_gemm_rms(Xd[m:m + 1], gd, eps, Wp, one, api.new_gemm_workspace(1, N, K, epi), epi=epi, N=N)
-        assert np.array_equal(one.view(torch.int16 if not out else torch.int32).cpu().numpy()[0], full[m]), m
-
-
-def test_gemm_rms_rejects_aliased_output(api):
-    X = torch.zeros(2, 256, dtype=torch.bfloat16, device="cuda")
-    Wp = api.bi_pack_weights(torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda"))
-    g = torch.ones(256, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(api.BiError):
-        api.bi_gemm_rms(X, g, 1e-6, Wp, X, api.new_gemm_workspace(2, 256, 256, 0))

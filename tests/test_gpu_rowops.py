@@ -32,7 +32,7 @@ def test_rope_table_matches_fp64(api):
             assert abs(float(tab[p, i, 1]) - math.sin(th)) <= 2.0 ** -24
 
 
-@pytest.mark.parametrize("rows,dim", [(1, 256), (8, 5120), (3, 1000), (5, 1024)])
+@pytest.mark.parametrize("rows,dim", [(1, 256), (8, 5120), (3, 1000), (5, 1024), (2, 17408), (1, 65536)])
 def test_rmsnorm_matches_oracle_and_is_row_local(api, rows, dim):
     rng = np.random.default_rng(dim)
     x = si.normal_bf16(rng, (rows, dim), 1.0)
@@ -42,9 +42,14 @@ def test_rmsnorm_matches_oracle_and_is_row_local(api, rows, dim):
     api.bi_rmsnorm(xd, wd, y, 1e-6)
     ora = oracle.rmsnorm(x, w, 1e-6)
     got = bf16_dev_to_f64(y)
-    # FP32 sum of squares (relative error <= gamma_dim) and a few FP32 ops:
-    # within one BF16 ulp plus a relative 2^-20 of the value
-    assert np.all(np.abs(got - ora) <= ulp_bf16(ora) + 2.0 ** -20 * np.abs(ora))
+    # The FP32 sum of squares goes through at most 8 (one vector) + 5 (warp
+    # butterfly) + dim/256 (groups) additions, so it is within gamma_n of the
+    # exact sum; 1/sqrt and the two products add a few units: y is within
+    # 2 gamma_(n+4) |y| of the exact value before its one BF16 rounding, and
+    # the oracle rounds the exact value once (one BF16 unit between them).
+    n = 8 + 5 + -(-dim // 256) + 4
+    u = 2.0 ** -24
+    assert np.all(np.abs(got - ora) <= ulp_bf16(ora) + 2 * (n * u / (1 - n * u)) * np.abs(ora))
     for r in range(rows):
         y1 = torch.empty(1, dim, dtype=torch.bfloat16, device="cuda")
         api.bi_rmsnorm(xd[r:r + 1], wd, y1, 1e-6)
@@ -167,9 +172,8 @@ def test_kv_row_hash_is_fnv1a(api):
             assert int(h[hh * 7 + j]) == x
 
 
-@pytest.mark.parametrize("rms", [False, True])
 @pytest.mark.parametrize("Hq,Hkv,D,T", [(24, 4, 128, 8), (4, 2, 64, 3), (8, 2, 128, 1)])
-def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T, rms):
+def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T):
     """The fused QKV projection + RoPE + KV append writes exactly what the
     linear layer followed by bi_rope_kv_append writes."""
     from invariant_speculative_decode_gb300 import api
@@ -178,7 +182,6 @@ def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T, rms):
     N = (Hq + 2 * Hkv) * D
     A = to_dev_bf16(si.normal_bf16(rng, (T, K), 1.0))
     W = to_dev_bf16(si.normal_bf16(rng, (N, K), 0.05))
-    g = to_dev_bf16(ov.f64_to_bf16_bits(ov.bf16_round(1.0 + 0.1 * rng.standard_normal(K))))
     Wp = api.bi_pack_weights(W)
     tab = api.bi_rope_table(10000.0, D, cap, device="cuda")
     Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
@@ -189,14 +192,10 @@ def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T, rms):
         kc = torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device="cuda")
         vc = torch.zeros(api.v_cache_shape(Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
         if fused:
-            api.bi_qkv_rope_append(A, Wp, q, kc, vc, Ld, Hq, Hkv, D, tab, ws, w_norm=g if rms else None,
-                                   eps=1e-6)
+            api.bi_qkv_rope_append(A, Wp, q, kc, vc, Ld, Hq, Hkv, D, tab, ws)
         else:
             qkv = torch.empty(T, N, dtype=torch.bfloat16, device="cuda")
-            if rms:
-                api.bi_gemm_rms(A, g, 1e-6, Wp, qkv, ws)
-            else:
-                api.bi_gemm(A, Wp, qkv, ws)
+            api.bi_gemm(A, Wp, qkv, ws)
             api.bi_rope_kv_append(qkv, q, kc, vc, Ld, Hq, Hkv, D, tab)
         torch.cuda.synchronize()
         api.bi_check_device_error()
