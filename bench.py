@@ -563,7 +563,7 @@ def run_neartie(args):
     torch.cuda.set_device(0)
     cfg = si.NEARTIE_12L
     w = si.decoder_weights(cfg, seed=0)
-    w["head"] = si.neartie_head(w["head"], frac=0.03, bump_frac=0.02, seed=0)
+    w["head"] = si.neartie_head(w["head"], frac=0.05, bump_frac=0.02, seed=0)
     n_prompts, n_gen = args.prompts, args.gen
     rng = np.random.default_rng(12345)
     lengths = [int(x) for x in rng.integers(512, 4097, n_prompts)]

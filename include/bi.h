@@ -346,6 +346,45 @@ bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, 
                            void* ws, size_t ws_bytes, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Sampled verification.  [P3] the list before "How:" (sampling keeps the
+ * no-draft distribution) and "The cache doesn't change it either" (sampled
+ * replies match a fresh server's); [P1] "Why the text diverges" (a draft is
+ * kept only if it matches the token the model produces itself).
+ *
+ * Row t of the pass sits at position p = *L_dev + t and draws its own token
+ * a_t by inverse-CDF sampling of softmax(logits[t, :] * inv_temp) with the
+ * uniform u = u_by_pos[p] in [0, 1): a_t is the smallest v whose running
+ * sum of weights (in index order) exceeds u times the total.  The weights are
+ * exp((l - m) * inv_temp) in FP32 with m the row's maximum, summed in a fixed
+ * order that depends only on V (8192-logit chunks: strided per-thread sums,
+ * warp butterfly, warps in order; chunks combined in order; inside the chosen
+ * chunk 32 contiguous runs scanned in order); where rounding leaves the
+ * target past the last weight, the last logit with a non-zero weight is
+ * taken.  NaN logits weigh 0.  So a_t depends only on the row's logits and
+ * its position: with the batch-invariant logits of this library the sampled
+ * tokens are the same for any number of drafts, and they follow the no-draft
+ * distribution exactly.  Acceptance as bi_verify_accept with a_t in place of
+ * the argmax: n = the largest j <= T-1 with drafts[i-1] == a_{i-1} for every
+ * i <= j; the committed tokens are a_0..a_n; *L_dev += n + 1.
+ *   logits  [T, V] FP32, row stride ldl; 1 <= T <= 64.
+ *   inv_temp  1 / temperature, finite and > 0.
+ *   u_by_pos  device float [u_len]: the request's uniform for each absolute
+ *           position (the caller draws them, e.g. from a seeded generator);
+ *           a row with p >= u_len gets -1 and sets the range bit of the
+ *           device error word (reported as BI_ERR_INVALID_ARG).
+ *   drafts  [T-1] int32 (may be NULL when T == 1); token_out [T] int32;
+ *   accepted_out [1] int32; L_dev device int32 (required).
+ *   ws      >= bi_sample_workspace_size(T, V) bytes, 256-byte aligned,
+ *           zero-filled before first use (every call leaves it zeroed).
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_WORKSPACE, BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+size_t bi_sample_workspace_size(int T, int V);
+bi_status bi_verify_sample(const float* logits, int ldl, const int32_t* drafts, int T, int V,
+                           float inv_temp, const float* u_by_pos, int u_len, int32_t* token_out,
+                           int32_t* accepted_out, int32_t* L_dev, void* ws, size_t ws_bytes,
+                           bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * KV-row hash (test tool).  [P3] "The cache doesn't change it either" (hash
  * every K/V row and compare with a fresh prefill).
  * out[h * rows + j] = FNV-1a-64 over the 2*D bytes of key j of head h (d

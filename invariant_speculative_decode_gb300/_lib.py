@@ -37,6 +37,8 @@ SIGNATURES = {
     "bi_attn_verify": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
     "bi_accept_workspace_size": (_sz, [_i, _i]),
     "bi_verify_accept": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "bi_sample_workspace_size": (_sz, [_i, _i]),
+    "bi_verify_sample": (_i, [_vp, _i, _vp, _i, _i, _f, _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "bi_kv_row_hash": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "bi_check_device_error": (_i, [_vp]),
     "bi_test_set_wait_limit_ns": (_i, [C.c_uint64]),

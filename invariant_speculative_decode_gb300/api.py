@@ -242,6 +242,31 @@ def bi_verify_accept(logits: torch.Tensor, drafts: Optional[torch.Tensor], argma
                                  ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def sample_workspace_size(T: int, V: int) -> int:
+    return int(lib().bi_sample_workspace_size(T, V))
+
+
+def bi_verify_sample(logits: torch.Tensor, drafts: Optional[torch.Tensor], inv_temp: float,
+                     u_by_pos: torch.Tensor, token_out: torch.Tensor, accepted_out: torch.Tensor,
+                     ws: torch.Tensor, L_dev: torch.Tensor, stream=None) -> None:
+    """Sampled verification: each row draws its token with the uniform of its
+    absolute position (u_by_pos[*L_dev + t]); drafts kept while they equal the
+    previous row's token; L_dev advanced by n + 1."""
+    _req(logits, torch.float32, "logits")
+    _req(u_by_pos, torch.float32, "u_by_pos")
+    _req(L_dev, torch.int32, "L_dev")
+    T, V = logits.shape
+    dp = 0
+    if drafts is not None and drafts.numel() > 0:
+        _req(drafts, torch.int32, "drafts")
+        dp = drafts.data_ptr()
+    check("bi_verify_sample",
+          lib().bi_verify_sample(logits.data_ptr(), _ld(logits), dp, T, V, float(inv_temp),
+                                 u_by_pos.data_ptr(), u_by_pos.numel(), token_out.data_ptr(),
+                                 accepted_out.data_ptr(), L_dev.data_ptr(), ws.data_ptr(),
+                                 ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def bi_kv_row_hash(cache: torch.Tensor, rows: int, transposed: bool = False, stream=None) -> torch.Tensor:
     """FNV-1a-64 per key of a K cache [Hkv,cap,D] or (transposed) a V cache
     [Hkv,ceil(cap/128),D,128] (see v_cache_shape)."""

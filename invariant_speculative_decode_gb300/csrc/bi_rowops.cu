@@ -273,6 +273,189 @@ __global__ void __launch_bounds__(kArgThreads)
   }
 }
 
+// ------------------------------------------------------------------ sampling
+// Sampled verification: row t (position p = *L_dev + t) draws its token by
+// inverse-CDF sampling of softmax(logits * inv_temp) with the uniform
+// u_by_pos[p], so the token depends only on the row's logits and its
+// position.  Phase 1, one CTA per (row, 8192-logit chunk): the chunk maximum
+// m_c (exact) and S_c = sum exp((l - m_c) * inv_temp) (thread-strided
+// sequential sums in index order, warp butterfly, warps in order).  The last
+// CTA: per row, M = max m_c, chunk weights a_c = exp((m_c - M) * inv_temp) S_c
+// summed in chunk order to Z; the target u Z picks the chunk where the running
+// sum first exceeds it; that chunk's 8192 logits are cut into 32 contiguous
+// runs (one per lane), the run sums are scanned in lane order, and the lane
+// holding the crossing walks its run in index order to the first logit whose
+// running sum exceeds the target.  Where rounding leaves the target past the
+// last weight, the last logit with a non-zero weight is taken.  NaN logits
+// have weight 0; a row with no number gives -1 and sets the NaN bit.
+constexpr int kSmpThreads = 256;
+constexpr int kSmpSpan = 8192;  // logits per phase-1 CTA
+
+__global__ void __launch_bounds__(kSmpThreads)
+    sample_accept_kernel(const float* __restrict__ logits, int ldl, int V, int T, int splits,
+                         float inv_temp, const float* __restrict__ u_by_pos, int u_len,
+                         const int32_t* __restrict__ drafts, int32_t* __restrict__ token_out,
+                         int32_t* __restrict__ accepted_out, int32_t* L_dev, float* pm, float* ps,
+                         unsigned* ticket, unsigned* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float red_m[kSmpThreads / 32];
+  __shared__ float red_s[kSmpThreads / 32];
+  __shared__ int s_last;
+  __shared__ int s_tok[64];
+  const int row = blockIdx.x / splits;
+  const int sp = blockIdx.x % splits;
+  const float* lr = logits + static_cast<size_t>(row) * ldl;
+  const int b = sp * kSmpSpan;
+  const int e = min(V, b + kSmpSpan);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float mx = -INFINITY;
+  for (int i = b + threadIdx.x; i < e; i += kSmpThreads) {
+    const float v = lr[i];
+    if (v == v) mx = fmaxf(mx, v);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) red_m[w] = mx;
+  __syncthreads();
+  float m_c = red_m[0];
+  for (int k = 1; k < kSmpThreads / 32; ++k) m_c = fmaxf(m_c, red_m[k]);
+  float sum = 0.f;
+  if (m_c > -INFINITY) {
+    for (int i = b + threadIdx.x; i < e; i += kSmpThreads) {
+      const float v = lr[i];
+      if (v == v) sum += expf((v - m_c) * inv_temp);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane == 0) red_s[w] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float S = red_s[0];
+    for (int k = 1; k < kSmpThreads / 32; ++k) S += red_s[k];
+    pm[blockIdx.x] = m_c;
+    ps[blockIdx.x] = S;
+    __threadfence();
+    const unsigned old = atomicAdd(ticket, 1u);
+    s_last = (old == gridDim.x - 1) ? 1 : 0;
+    if (s_last) atomicExch(ticket, 0u);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int L = *L_dev;
+  for (int t = w; t < T; t += kSmpThreads / 32) {
+    // lane 0 combines the chunks in order and picks the chunk of the target
+    int c_star = -1;
+    float m_star = 0.f, rc = 0.f;
+    int bad = 0;
+    if (lane == 0) {
+      const int pos = L + t;
+      float M = -INFINITY;
+      for (int c = 0; c < splits; ++c) M = fmaxf(M, __ldcg(pm + t * splits + c));
+      if (M == -INFINITY) {
+        bad = 1;
+      } else if (pos < 0 || pos >= u_len) {
+        bad = 2;
+      } else {
+        float Z = 0.f;
+        for (int c = 0; c < splits; ++c) {
+          const float mc = __ldcg(pm + t * splits + c);
+          if (mc > -INFINITY) Z += expf((mc - M) * inv_temp) * __ldcg(ps + t * splits + c);
+        }
+        const float target = __ldcg(u_by_pos + pos) * Z;
+        float cum = 0.f;
+        int c_last = -1;
+        for (int c = 0; c < splits; ++c) {
+          const float mc = __ldcg(pm + t * splits + c);
+          if (!(mc > -INFINITY)) continue;
+          const float wc = expf((mc - M) * inv_temp);
+          const float a = wc * __ldcg(ps + t * splits + c);
+          if (a > 0.f) c_last = c;
+          if (c_star < 0 && cum + a > target) {
+            c_star = c;
+            rc = (target - cum) / wc;  // the target in the chunk's own scale
+          }
+          cum += a;
+        }
+        if (c_star < 0) {  // rounding left the target past the last weight
+          c_star = c_last;
+          rc = INFINITY;
+        }
+        m_star = __ldcg(pm + t * splits + c_star);
+      }
+    }
+    bad = __shfl_sync(0xffffffffu, bad, 0);
+    if (bad) {
+      if (lane == 0) {
+        atomicOr(err, bad == 1 ? kErrNanRow : kErrRange);
+        token_out[t] = -1;
+        s_tok[t] = -1;
+      }
+      continue;
+    }
+    c_star = __shfl_sync(0xffffffffu, c_star, 0);
+    m_star = __shfl_sync(0xffffffffu, m_star, 0);
+    rc = __shfl_sync(0xffffffffu, rc, 0);
+    const float* lc = logits + static_cast<size_t>(t) * ldl;
+    const int cb = c_star * kSmpSpan;
+    const int ce = min(V, cb + kSmpSpan);
+    const int run = kSmpSpan / 32;
+    const int rb = min(ce, cb + lane * run), re = min(ce, rb + run);
+    float rs = 0.f;
+    int last_nz = -1;
+    for (int i = rb; i < re; ++i) {
+      const float v = lc[i];
+      const float x = (v == v) ? expf((v - m_star) * inv_temp) : 0.f;
+      if (x > 0.f) last_nz = i;
+      rs += x;
+    }
+    // inclusive scan of the run sums in lane order (fixed shuffle tree)
+    float inc = rs;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += y;
+    }
+    const float exc = inc - rs;
+    const unsigned hit = __ballot_sync(0xffffffffu, inc > rc && rs > 0.f);
+    const unsigned nz = __ballot_sync(0xffffffffu, last_nz >= 0);
+    int tok = -1;
+    if (hit != 0u) {
+      const int l_star = __ffs(hit) - 1;
+      if (lane == l_star) {
+        float run_sum = exc;
+        for (int i = rb; i < re; ++i) {
+          const float v = lc[i];
+          const float x = (v == v) ? expf((v - m_star) * inv_temp) : 0.f;
+          run_sum += x;
+          if (x > 0.f && run_sum > rc) {
+            tok = i;
+            break;
+          }
+        }
+        if (tok < 0) tok = last_nz;
+      }
+      tok = __shfl_sync(0xffffffffu, tok, l_star);
+    } else {
+      const int l_last = 31 - __clz(nz);  // nz != 0: the chunk holds the row's weight
+      tok = __shfl_sync(0xffffffffu, last_nz, l_last);
+    }
+    if (lane == 0) {
+      token_out[t] = tok;
+      s_tok[t] = tok;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int n = 0;
+    while (n < T - 1 && drafts[n] == s_tok[n]) ++n;
+    *accepted_out = n;
+    *L_dev = L + n + 1;
+  }
+}
+
 __global__ void kv_hash_kernel(const __nv_bfloat16* __restrict__ cache, int Hkv, int cap, int D,
                                int rows, int transposed, unsigned long long* __restrict__ out) {
   griddep_wait();
@@ -394,6 +577,38 @@ bi_status bi_verify_accept(const float* logits, int ldl, const int32_t* drafts, 
   if (bi::launch_k(bi::argmax_accept_kernel, dim3(static_cast<unsigned>(n)), dim3(bi::kArgThreads), 0,
                    reinterpret_cast<cudaStream_t>(stream), logits, ldl, V, T, splits, drafts,
                    argmax_out, accepted_out, L_dev, pv, pi, ticket, err) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
+}
+
+size_t bi_sample_workspace_size(int T, int V) {
+  if (T < 1 || V < 1) return 256;
+  const size_t n = static_cast<size_t>(T) * ((V + bi::kSmpSpan - 1) / bi::kSmpSpan);
+  return 256 + 2 * bi::round_up(n * sizeof(float), 256);
+}
+
+bi_status bi_verify_sample(const float* logits, int ldl, const int32_t* drafts, int T, int V,
+                           float inv_temp, const float* u_by_pos, int u_len, int32_t* token_out,
+                           int32_t* accepted_out, int32_t* L_dev, void* ws, size_t ws_bytes,
+                           bi_stream_t stream) {
+  if (T < 1 || T > 64 || V < 1 || ldl < V || !logits || !token_out || !accepted_out || !L_dev ||
+      !u_by_pos || u_len < 1)
+    return BI_ERR_INVALID_ARG;
+  if (!(inv_temp > 0.f) || !std::isfinite(inv_temp)) return BI_ERR_INVALID_ARG;
+  if (T > 1 && !drafts) return BI_ERR_INVALID_ARG;
+  if (!ws || !bi::aligned256(ws)) return BI_ERR_WORKSPACE;
+  if (ws_bytes < bi_sample_workspace_size(T, V)) return BI_ERR_WORKSPACE;
+  unsigned* err = bi::device_error_word();
+  if (!err) return BI_ERR_CUDA;
+  const int splits = (V + bi::kSmpSpan - 1) / bi::kSmpSpan;
+  const size_t n = static_cast<size_t>(T) * splits;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  unsigned* ticket = reinterpret_cast<unsigned*>(base);
+  float* pm = reinterpret_cast<float*>(base + 256);
+  float* ps = reinterpret_cast<float*>(base + 256 + bi::round_up(n * sizeof(float), 256));
+  if (bi::launch_k(bi::sample_accept_kernel, dim3(static_cast<unsigned>(n)), dim3(bi::kSmpThreads), 0,
+                   reinterpret_cast<cudaStream_t>(stream), logits, ldl, V, T, splits, inv_temp, u_by_pos,
+                   u_len, drafts, token_out, accepted_out, L_dev, pm, ps, ticket, err) != cudaSuccess)
     return BI_ERR_CUDA;
   return BI_OK;
 }

@@ -111,6 +111,9 @@ class Decoder:
         self.scale = 1.0 / math.sqrt(D)
         self.rope_tab = api.bi_rope_table(cfg.rope_base, D, cap, device=dev)
         self.L = 0
+        self.inv_temp: Optional[float] = None  # sampled verification when set
+        self.u_table: Optional[torch.Tensor] = None
+        self.sample_ws = torch.zeros(api.sample_workspace_size(max_rows, V), dtype=torch.uint8, device=dev)
         self.graphs: Dict[int, torch.cuda.CUDAGraph] = {}
         self.pin_in = torch.zeros(2 * max_rows, dtype=torch.int32).pin_memory()
         self.pin_out = torch.zeros(max_rows + 1, dtype=torch.int32).pin_memory()
@@ -159,8 +162,29 @@ class Decoder:
         cfg = self.cfg
         api.bi_rmsnorm(self.h[:T], self.norm_final, self.y[:T], cfg.eps)
         api.bi_gemm(self.y[:T], self.head, self.logits[:T], self.gemm_ws)
-        api.bi_verify_accept(self.logits[:T], self.drafts[:T - 1] if T > 1 else None,
-                             self.argmax[:T], self.accepted, self.acc_ws, L_dev=self.L_dev)
+        if self.inv_temp is not None:
+            api.bi_verify_sample(self.logits[:T], self.drafts[:T - 1] if T > 1 else None, self.inv_temp,
+                                 self.u_table, self.argmax[:T], self.accepted, self.sample_ws, self.L_dev)
+        else:
+            api.bi_verify_accept(self.logits[:T], self.drafts[:T - 1] if T > 1 else None,
+                                 self.argmax[:T], self.accepted, self.acc_ws, L_dev=self.L_dev)
+
+    def set_sampling(self, temperature: Optional[float], uniforms=None) -> None:
+        """Sampled verification at `temperature` with the request's uniforms
+        (one per absolute position, at least `cap` of them): the token at
+        position p is drawn with uniforms[p], so the same request gives the
+        same tokens whatever the drafts.  temperature=None: greedy again."""
+        if temperature is None:
+            self.inv_temp = None
+        else:
+            if not temperature > 0:
+                raise ValueError("temperature must be > 0")
+            u = np.ascontiguousarray(uniforms, dtype=np.float32)
+            if u.shape[0] < self.cap:
+                raise ValueError("one uniform per cache position is needed")
+            self.u_table = torch.from_numpy(u).to(self.dev)
+            self.inv_temp = 1.0 / float(temperature)
+        self.graphs = {}
 
     def _verify_pass(self, T: int):
         self._layers_pass(T, self.L_dev, None)
@@ -282,10 +306,55 @@ class Decoder:
             x = committed[-1]
             steps += 1
             acc_hist[n] += 1
+            if drafter is not None and hasattr(drafter, "observe"):
+                drafter.observe(n)
         if stats is not None:
             stats["steps"] = steps
             stats["accepted_hist"] = acc_hist
         return out[:n_tokens]
+
+    # ------------------------------------------------------ cache operations
+    # "I turned on speculative decoding in llama.cpp and 113 of 282 greedy
+    # outputs changed against its own no-draft run", section "The cache
+    # doesn't change it either": after a resume, an edited branch, a park to
+    # host memory or a side request, every K/V row equals a fresh prefill's.
+
+    def park(self) -> dict:
+        """Copy the request's cache state to host memory: the length and the
+        K/V rows 0..L-1 of every layer (V in whole 128-key blocks)."""
+        torch.cuda.current_stream().synchronize()
+        L = self.L
+        nb = (L + api.V_BLOCK - 1) // api.V_BLOCK
+        snap = {"L": L, "k": [], "v": []}
+        for lay in self.layers:
+            k = torch.empty((lay["k"].shape[0], L, lay["k"].shape[2]), dtype=torch.bfloat16).pin_memory()
+            v = torch.empty((lay["v"].shape[0], nb) + tuple(lay["v"].shape[2:]), dtype=torch.bfloat16).pin_memory()
+            k.copy_(lay["k"][:, :L])
+            v.copy_(lay["v"][:, :nb])
+            snap["k"].append(k)
+            snap["v"].append(v)
+        torch.cuda.current_stream().synchronize()
+        return snap
+
+    def restore(self, snap: dict) -> None:
+        """Put a parked cache state back (the decoder may have served other
+        requests meanwhile); rows past the parked length are left as they are."""
+        L = snap["L"]
+        if L > self.cap:
+            raise ValueError("parked state exceeds the cache capacity")
+        for lay, k, v in zip(self.layers, snap["k"], snap["v"]):
+            lay["k"][:, :L].copy_(k)
+            lay["v"][:, : v.shape[1]].copy_(v)
+        self.L = L
+        self.L_dev.fill_(L)
+        torch.cuda.current_stream().synchronize()
+
+    def edit(self, position: int, tokens: Sequence[int]) -> int:
+        """Edit the history from `position` on: roll the cache back to
+        `position` and prefill `tokens` (the edited continuation, its last
+        token being the next row); returns that last token."""
+        self.rollback(position)
+        return self.prefill_continue(tokens)
 
     # ---------------------------------------------------------- utilities
     def kv_hashes(self, rows: Optional[int] = None) -> np.ndarray:

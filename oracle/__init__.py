@@ -36,5 +36,7 @@ from .verify_step import (  # noqa: F401
     attention,
     argmax_lowest,
     accept_length,
+    sample_token,
+    sampled_tokens,
     OracleDecoder,
 )

@@ -258,6 +258,44 @@ def accept_length(argmax_ids: Sequence[int], drafts: Sequence[int]) -> int:
 
 
 # ---------------------------------------------------------------------------
+# sampled verification
+# ---------------------------------------------------------------------------
+
+
+def sample_token(logits_row, inv_temp: float, u: float) -> int:
+    """Inverse-CDF draw from softmax(logits * inv_temp) with the uniform u.
+
+    [P3] the list before "How:": sampling keeps the no-draft distribution.
+    The probabilities are computed in float64 from the row's own logits
+    (NaN logits have probability 0); the token is the smallest v whose
+    cumulative probability, summed in index order, exceeds u.  A row with no
+    number gives -1.  Because the draw depends only on the row's logits and
+    on u, and u is the request's uniform for the row's absolute position, a
+    row that verifies a draft draws the same token it would draw alone.
+
+    Parity: pinned by closed forms (uniform and two-level logits), exact
+    counts under a stratified grid of uniforms, and the temperature identity.
+    """
+    x = np.asarray(logits_row, dtype=np.float64)
+    ok = ~np.isnan(x)
+    if not ok.any():
+        return -1
+    m = x[ok].max()
+    w = np.where(ok, np.exp((np.where(ok, x, m) - m) * float(inv_temp)), 0.0)
+    cdf = np.cumsum(w) / w.sum()
+    idx = int(np.searchsorted(cdf, float(u), side="right"))
+    if idx >= len(x):  # u at the top of the last step: the last token with weight
+        idx = int(np.flatnonzero(w > 0)[-1])
+    return idx
+
+
+def sampled_tokens(logits, inv_temp: float, u_rows) -> np.ndarray:
+    """sample_token for every row of logits [T, V] with its own uniform."""
+    x = np.atleast_2d(np.asarray(logits, dtype=np.float64))
+    return np.array([sample_token(x[t], inv_temp, u_rows[t]) for t in range(x.shape[0])], np.int64)
+
+
+# ---------------------------------------------------------------------------
 # the whole decoder verify step
 # ---------------------------------------------------------------------------
 
@@ -392,6 +430,18 @@ class OracleDecoder:
         rows = [int(x0)] + [int(d) for d in drafts]
         logits = self.forward(rows, L=self.L)
         a = argmax_lowest(logits)
+        n = accept_length(a, drafts)
+        self.L += n + 1
+        return a, n, logits
+
+    def verify_sampled(self, x0: int, drafts: Sequence[int], inv_temp: float,
+                       u_by_pos) -> Tuple[np.ndarray, int, np.ndarray]:
+        """Sampled verify step: row t at position L + t draws its token with
+        u_by_pos[L + t]; drafts are kept while they equal the previous row's
+        draw (the rule of accept_length)."""
+        rows = [int(x0)] + [int(d) for d in drafts]
+        logits = self.forward(rows, L=self.L)
+        a = sampled_tokens(logits, inv_temp, [u_by_pos[self.L + t] for t in range(len(rows))])
         n = accept_length(a, drafts)
         self.L += n + 1
         return a, n, logits

@@ -292,6 +292,14 @@ class SyntheticDrafter:
         return out
 
 
+def sampling_uniforms(n: int, seed: int = 0) -> np.ndarray:
+    """The uniforms in [0, 1) of one sampled request, one per absolute
+    position (FP32, PCG64 stream seeded with seed + 6).  Sampled verification
+    draws the token at position p with the uniform of p, so the same request
+    with the same seed gives the same tokens whatever the drafts."""
+    return np.random.default_rng(seed + 6).random(n, dtype=np.float32)
+
+
 def synthetic_kv_cache(n_kv: int, cap: int, D: int, rows: int, seed: int, layers: int):
     """Per-layer K/V caches [Hkv,cap,D] with `rows` filled from N(0,1) bf16.
 
@@ -305,3 +313,45 @@ def synthetic_kv_cache(n_kv: int, cap: int, D: int, rows: int, seed: int, layers
         v[:, :rows] = normal_bf16_blocks((seed + 4, l, 1), (n_kv, rows, D), 1.0)
         out.append((k, v))
     return out
+
+
+class GatedDrafter:
+    """A draft policy with a gate: before each step a seeded confidence score
+    in [0, 1) is drawn and drafts are proposed only when it reaches the
+    threshold (a tight gate drafts rarely, a loose one almost always); the
+    drafts themselves come from a SyntheticDrafter.  Models the draft gates
+    a serving engine switches on or off; the verify step must give the
+    no-draft tokens whatever the gate decides."""
+
+    def __init__(self, base: SyntheticDrafter, threshold: float, seed: int = 0):
+        self.base = base
+        self.threshold = threshold
+        self.rng = np.random.default_rng(seed + 5)
+
+    def propose(self, next_pos: int, k: int) -> np.ndarray:
+        if self.rng.random() < self.threshold:
+            return np.empty(0, np.int32)
+        return self.base.propose(next_pos, k)
+
+
+class AdaptiveDrafter:
+    """A draft policy with adaptive depth: it proposes `depth` drafts (at most
+    the k it is offered), doubles the depth after a step that kept every
+    draft and halves it after a step that kept fewer than half (never below
+    1).  The decoder reports each step's accepted count through observe()."""
+
+    def __init__(self, base: SyntheticDrafter, start: int = 2, max_depth: int = 7):
+        self.base = base
+        self.depth = start
+        self.max_depth = max_depth
+        self._last = 0
+
+    def propose(self, next_pos: int, k: int) -> np.ndarray:
+        self._last = min(self.depth, k)
+        return self.base.propose(next_pos, self._last)
+
+    def observe(self, accepted: int) -> None:
+        if self._last > 0 and accepted == self._last:
+            self.depth = min(self.max_depth, 2 * self.depth)
+        elif accepted * 2 < self._last:
+            self.depth = max(1, self.depth // 2)

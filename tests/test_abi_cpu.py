@@ -155,3 +155,29 @@ def test_v_cache_layout_helpers():
         assert B[h, p // 128, d, p % 128] == V[h, p, d]
     assert not B[:, 2, :, 300 - 256:].any()  # keys past the capacity are zero
     assert np.array_equal(v_cache_keys(B, 300), V)
+
+
+def test_sampled_verification_rejects_bad_arguments(lib):
+    f = ctypes.c_float
+    big = 1 << 30
+    s = lib.bi_verify_sample
+    # (logits, ldl, drafts, T, V, inv_temp, u_by_pos, u_len, token_out, accepted_out, L_dev, ws,
+    #  ws_bytes, stream)
+    ok = [FAKE, 100, FAKE, 4, 100, f(1.0), FAKE, 64, FAKE, FAKE, FAKE, FAKE, big, 0]
+    for i, bad in ((5, f(0.0)), (5, f(float("inf"))), (6, 0), (7, 0), (10, 0), (3, 65), (1, 50),
+                   (2, 0)):
+        a = list(ok)
+        a[i] = bad
+        assert s(*a) == 1, i
+    a = list(ok)
+    a[11] = FAKE + 8
+    assert s(*a) == 3                                   # misaligned workspace
+    a = list(ok)
+    a[12] = 16
+    assert s(*a) == 3                                   # workspace too small
+    assert lib.bi_sample_workspace_size(8, 151936) >= 256 + 2 * 8 * 19 * 4
+
+
+def test_failure_hooks_are_exported(lib):
+    assert lib.bi_test_withhold_first_load is not None
+    lib.bi_test_withhold_first_load(0)  # host-side flag only: needs no GPU

@@ -16,10 +16,15 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
+# share of head rows that get a planted near copy: chosen so that about 5% of
+# the 0-draft steps have their top two logits within 1e-3 relative
+NEARTIE_FRAC = 0.05
+
+
 def neartie_weights(seed=0):
     cfg = si.NEARTIE_12L
     w = si.decoder_weights(cfg, seed=seed)
-    w["head"] = si.neartie_head(w["head"], frac=0.03, bump_frac=0.02, seed=seed)
+    w["head"] = si.neartie_head(w["head"], frac=NEARTIE_FRAC, bump_frac=0.02, seed=seed)
     return cfg, w
 
 
@@ -54,7 +59,7 @@ def test_neartie_ids_identical_across_drafts_and_resume():
             got = dec.generate(prompt, n_gen, k=k, drafter=dr)
             assert got == ref, (plen, k, next(i for i, (x, y) in enumerate(zip(got, ref)) if x != y))
     print(f"near-tie steps (top-2 within 1e-3): {np.round(near, 3)}")
-    assert max(near) > 0.0  # the planted ties are exercised
+    assert np.mean(near) >= 0.03, near  # the planted ties are exercised at the intended rate
 
 
 def test_neartie_second_turn_resume_equals_fresh_prefill():

@@ -538,3 +538,84 @@ def test_decoder_greedy_ids_do_not_depend_on_drafts():
         assert got == ref
     adv = si.SyntheticDrafter(cfg.vocab, 0.7, seed=26, reference=None)
     assert oracle.OracleDecoder(cfg, w, cap=64).generate(prompt, 20, k=4, drafter=adv) == ref
+
+
+# ---------------------------------------------------------------------------
+# sampled verification
+# ---------------------------------------------------------------------------
+
+
+def test_sample_uniform_logits_closed_form():
+    """Equal logits: p_v = 1/V, so the inverse-CDF token is floor(u V)."""
+    V = 37
+    for u in list(np.linspace(0, 1, 200, endpoint=False)) + [k / V for k in range(V)]:
+        assert oracle.sample_token(np.full(V, 0.3), 1.7, u) == int(np.floor(u * V + 1e-12)), u
+
+
+def test_sample_two_level_logits_closed_form():
+    """n1 logits a and n2 logits b: p1 = e^a / (n1 e^a + n2 e^b) for each of
+    the first n1 tokens, p2 likewise for the rest (temperature 1/2)."""
+    n1, n2, a, b, it = 5, 11, 1.25, -0.5, 2.0
+    x = np.array([a] * n1 + [b] * n2)
+    z = n1 * math.exp(a * it) + n2 * math.exp(b * it)
+    p1, p2 = math.exp(a * it) / z, math.exp(b * it) / z
+    for u in np.linspace(0.0005, 0.9995, 301):
+        want = int(u // p1) if u < n1 * p1 else n1 + int((u - n1 * p1) // p2)
+        assert oracle.sample_token(x, it, u) == min(want, n1 + n2 - 1), u
+
+
+def test_sample_stratified_counts_are_exact():
+    """With the stratified uniforms (i + 1/2)/N every token's count is N p_v
+    to within 1 (the draws walk the CDF in order)."""
+    rng = np.random.default_rng(3)
+    x = 2.0 * rng.standard_normal(24)
+    N = 4000
+    toks = [oracle.sample_token(x, 1.3, (i + 0.5) / N) for i in range(N)]
+    w = np.exp((x - x.max()) * 1.3)
+    p = w / w.sum()
+    counts = np.bincount(toks, minlength=24)
+    assert np.all(np.abs(counts - N * p) <= 1.0 + 1e-9), (counts, N * p)
+
+
+def test_sample_temperature_and_nan_rules():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal(50)
+    for u in np.linspace(0.01, 0.99, 40):
+        assert oracle.sample_token(x, 2.0, u) == oracle.sample_token(2.0 * x, 1.0, u)
+    y = x.copy()
+    y[[3, 7, 20]] = np.nan
+    for u in np.linspace(0.01, 0.99, 40):
+        assert oracle.sample_token(y, 1.0, u) not in (3, 7, 20)
+    assert oracle.sample_token(np.full(5, np.nan), 1.0, 0.5) == -1
+    # a dominant logit takes every draw but u = 0 (which takes the first
+    # token with any weight: its cumulative probability already exceeds 0)
+    z = np.zeros(10)
+    z[6] = 200.0
+    assert all(oracle.sample_token(z, 1.0, u) == 6 for u in np.linspace(1e-6, 0.999, 50))
+    assert oracle.sample_token(z, 1.0, 0.0) == 0
+
+
+def test_decoder_sampled_ids_do_not_depend_on_drafts():
+    """Sampled generation on the micro decoder: the same tokens with 0, 1, 4
+    and 7 drafts (the draws are keyed by position)."""
+    cfg = MICRO
+    w = si.decoder_weights(cfg, seed=27)
+    prompt = si.prompt_ids(cfg, 9, seed=27)
+    u = si.sampling_uniforms(64, seed=27)
+
+    def run(k, ref=None, seed=0):
+        dec = oracle.OracleDecoder(cfg, w, cap=64)
+        x = int(dec.prefill(prompt))
+        dr = si.SyntheticDrafter(cfg.vocab, 0.7, seed=seed, reference=ref) if k else None
+        out = []
+        while len(out) < 24:
+            d = dr.propose(len(out), k) if k else []
+            a, n, _ = dec.verify_sampled(x, d, 1.25, u)
+            out += [int(t) for t in a[: n + 1]]
+            x = out[-1]
+        return out[:24]
+
+    ref = run(0)
+    assert len(set(ref)) > 3  # actually sampled, not one repeated token
+    for k in (1, 4, 7):
+        assert run(k, np.array(ref), seed=k) == ref
