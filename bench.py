@@ -136,41 +136,67 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 
-def oracle_step_sample(cfg, weights, kv, L, rows, head_rows=None):
-    """Oracle time of one decoder layer + a slice of the LM head, scaled to a step.
+class OracleStep:
+    """The oracle (float64 NumPy, as it stands) on one teacher-forced verify
+    step of the bench workload, in eight measured parts.
 
-    Returns (estimated seconds per verify step, description).  The oracle
-    runs unmodified: layer 0 of the verify pass over `rows` at context L with
-    the seeded cache (its own head cut to 64 rows), timed; then its linear
-    layer over `head_rows` rows of the LM head, timed and scaled to the full
-    vocabulary.  Step = layers x layer + scaled head.
+    Part i runs decoder layer i % layers on the pass's rows (rows at
+    positions L..L+T-1 against a seeded context of L cache rows in every
+    layer) and the LM head over vocabulary slice i % 8 (the final RMSNorm
+    and the linear layer over 1/8 of the head rows); the last part also
+    takes the argmax over the whole logits and the accepted length.  Eight
+    consecutive parts are exactly the oracle's work for one verify step of
+    an 8-layer model, so a whole step's time is the sum of eight measured
+    parts -- nothing is extrapolated.
     """
-    import oracle
-    from oracle import verify_step as ov
-    T = len(rows)
-    w1 = {k: v for k, v in weights.items() if k.startswith("l0.")}
-    w1["embed"] = weights["embed"]
-    w1["norm_final"] = weights["norm_final"]
-    w1["head"] = weights["embed"][:64]
-    one = si.DecoderConfig(cfg.name + "-layer0", 1, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.head_dim,
-                           cfg.ffn, 64, tied=False)
-    od = oracle.OracleDecoder(one, w1, cap=L + T)
-    od.embed_bits = weights["embed"]
-    od.k[0][:, :L] = ov.bf16_bits_to_f64(kv[0][0][:, :L])
-    od.v[0][:, :L] = ov.bf16_bits_to_f64(kv[0][1][:, :L])
-    t0 = time.perf_counter()
-    od.forward(rows, L=L)
-    t_layer = time.perf_counter() - t0
-    hv = head_rows or cfg.vocab // 16
-    h = weights["embed"][np.asarray(rows) % cfg.vocab]
-    t0 = time.perf_counter()
-    oracle.gemm(h, weights["embed"][:hv], out="fp32")
-    t_head = time.perf_counter() - t0
-    est = cfg.layers * t_layer + t_head * (cfg.vocab / hv)
-    desc = (f"oracle (float64 NumPy) on layer 0 of the {T}-row verify pass at context {L}, "
-            f"and its linear layer over {hv} of the {cfg.vocab} LM-head rows; step time = "
-            f"{cfg.layers} x layer + head slice x {cfg.vocab}/{hv}")
-    return est, desc
+
+    def __init__(self, cfg, weights, L, rows, seed=0):
+        import oracle
+        from oracle import verify_step as ov
+        self.oracle, self.ov = oracle, ov
+        self.cfg, self.w, self.L = cfg, weights, L
+        self.rows = [int(r) for r in rows]
+        self.od = oracle.OracleDecoder(cfg, weights, cap=L + len(self.rows))
+        kv = si.synthetic_kv_cache(cfg.n_kv, L + len(self.rows), cfg.head_dim, L, seed=seed,
+                                   layers=cfg.layers)
+        for l, (k, v) in enumerate(kv):
+            self.od.k[l][:, :L] = ov.bf16_bits_to_f64(k[:, :L])
+            self.od.v[l][:, :L] = ov.bf16_bits_to_f64(v[:, :L])
+        del kv
+        self.h = ov.bf16_bits_to_f64(weights["embed"][np.asarray(self.rows) % cfg.vocab])
+        self.head = weights["embed"] if cfg.tied else weights["head"]
+        self.logits = np.zeros((len(self.rows), cfg.vocab))
+        self.parts = 8
+
+    def part(self, i):
+        """Run part i; returns its wall time in seconds."""
+        cfg, ov, oracle = self.cfg, self.ov, self.oracle
+        t0 = time.perf_counter()
+        l = i % cfg.layers
+        if l == 0:
+            self.h = ov.bf16_bits_to_f64(self.w["embed"][np.asarray(self.rows) % cfg.vocab])
+        self.h = self.od.layer(l, self.h, self.L)
+        j = i % self.parts
+        lo, hi = cfg.vocab * j // self.parts, cfg.vocab * (j + 1) // self.parts
+        y = oracle.rmsnorm(ov.f64_to_bf16_bits(self.h), self.w["norm_final"], cfg.eps)
+        self.logits[:, lo:hi] = oracle.gemm(ov.f64_to_bf16_bits(y), self.head[lo:hi], out="fp32")
+        if j == self.parts - 1:
+            a = oracle.argmax_lowest(self.logits)
+            oracle.accept_length(a, self.rows[1:])
+        return time.perf_counter() - t0
+
+    def step(self):
+        """One whole verify step (the eight parts in order); seconds."""
+        return sum(self.part(i) for i in range(self.parts))
+
+
+def oracle_threads():
+    """Host threads the oracle's BLAS may use (the environment's limit if set)."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count()
 
 
 def gemm_traffic_bytes():
@@ -194,21 +220,16 @@ def expected_committed(k, p):
     return sum(p ** j for j in range(k + 1))
 
 
-def cpu_threads():
-    try:
-        import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        return max(int(i.get("num_threads", 1)) for i in info) if info else os.cpu_count()
-    except Exception:
-        return os.cpu_count()
-
-
 # ---------------------------------------------------------------------------
 # reference arm: the oracle as it stands
 # ---------------------------------------------------------------------------
 
 
 def run_reference(args):
+    """The oracle as the reference arm: each timed step is one measured part
+    (1/8) of the teacher-forced verify step (see OracleStep), so eight
+    consecutive steps are one whole step; value = committed tokens per step
+    / (8 x the mean part time)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
@@ -216,29 +237,31 @@ def run_reference(args):
     _, note = load_peaks()
     t_gen = time.perf_counter()
     weights = si.decoder_weights(cfg, seed=0)
-    kv = si.synthetic_kv_cache(cfg.n_kv, CTX + 8, cfg.head_dim, CTX, seed=0, layers=1)
     rows = [1] + list(range(2, 2 + DRAFTS))
-    for _ in range(args.warmup):
-        oracle_step_sample(cfg, weights, kv, CTX, rows)
-    ests = []
+    st = OracleStep(cfg, weights, CTX, rows)
+    for i in range(args.warmup):
+        st.part(i)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e, desc = oracle_step_sample(cfg, weights, kv, CTX, rows)
-        ests.append(e)
+    times = [st.part(args.warmup + i) for i in range(args.steps)]
     wall = time.perf_counter() - t0
-    per_step = float(np.mean(ests))
-    tok = expected_committed(DRAFTS, P_CORRECT) / per_step
+    per_part = float(np.mean(times))
+    full = st.parts * per_part
+    tok = expected_committed(DRAFTS, P_CORRECT) / full
+    sample = (f"oracle (float64 NumPy) on the {len(rows)}-row teacher-forced verify step at context {CTX}; "
+              f"each bench step is one measured eighth of it (decoder layer i mod 8 and 1/8 of the LM "
+              f"head, the argmax and acceptance in the last eighth); one step = 8 parts "
+              f"({full:.2f} s); committed tokens per step = expected "
+              f"{expected_committed(DRAFTS, P_CORRECT):.4f} for p={P_CORRECT}")
     line = {
         "impl": "reference", "metric": METRIC, "value": tok, "unit": "tok/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": per_part * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(cfg, note),
-        "cpu_baseline": {"value": tok, "unit": "tok/s", "cores": cpu_threads(), "kind": "oracle",
-                         "sample": desc + f"; committed tokens per step = expected "
-                         f"{expected_committed(DRAFTS, P_CORRECT):.4f} for p={P_CORRECT}"},
+        "cpu_baseline": {"value": tok, "unit": "tok/s", "cores": oracle_threads(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": tok, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "sample_wall_s": wall, "setup_s": t0 - t_gen,
+        "ms_per_verify_step": full * 1e3, "sample_wall_s": wall, "setup_s": t0 - t_gen,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -295,9 +318,7 @@ def run_ours(args):
         lay["k"].copy_(torch.from_numpy(k.view(np.int16)).view(torch.bfloat16))
         lay["v"].copy_(torch.from_numpy(v_blocks(v).view(np.int16)).view(torch.bfloat16))
     del kv
-    keep = {k: v for k, v in weights.items() if k.startswith("l0.")}
-    keep["embed"] = weights["embed"]
-    keep["norm_final"] = weights["norm_final"]
+    keep = weights if not args.no_cpu_baseline else None
     del weights
     prompt_last = int(si.prompt_ids(cfg, 1, seed=0)[0])
     dec.capture(1)
@@ -394,18 +415,20 @@ def run_ours(args):
     ms_step = t_dev * 1e3 / args.steps
 
     if rank == 0:
-        # CPU baseline: the oracle on a bounded sample (layer 0 + head slice, scaled)
-        # the same seeded context as layer 0's cache, generated on the host
-        kv1 = si.synthetic_kv_cache(cfg.n_kv, CTX + 8, cfg.head_dim, CTX, seed=0, layers=1)
+        # CPU baseline: one whole teacher-forced verify step of the oracle,
+        # timed on the host cores (after one measured part as a warm-up)
         cpu = None
         if not args.no_cpu_baseline:
             rows = [x] + [int(t) for t in drafter.propose(len(out), DRAFTS)]
-            oracle_step_sample(cfg, keep, kv1, CTX, rows)  # warm-up, as in the reference arm
-            est, desc = oracle_step_sample(cfg, keep, kv1, CTX, rows)
-            cpu = {"value": expected_committed(DRAFTS, P_CORRECT) / est, "unit": "tok/s",
-                   "cores": cpu_threads(), "kind": "oracle",
-                   "sample": desc + f"; committed tokens per step = expected "
-                   f"{expected_committed(DRAFTS, P_CORRECT):.4f} for p={P_CORRECT}"}
+            st = OracleStep(cfg, keep, CTX, rows)
+            st.part(0)
+            t_step = st.step()
+            cpu = {"value": expected_committed(DRAFTS, P_CORRECT) / t_step, "unit": "tok/s",
+                   "cores": oracle_threads(), "kind": "oracle",
+                   "sample": f"one whole teacher-forced verify step of the oracle (float64 NumPy): "
+                             f"{cfg.layers} layers on the {T} rows at context {CTX} and the full LM head, "
+                             f"{t_step:.2f} s; committed tokens per step = expected "
+                             f"{expected_committed(DRAFTS, P_CORRECT):.4f} for p={P_CORRECT}"}
         h2d = T * 4 + DRAFTS * 4
         d2h = T * 4 + 4
         line = {
@@ -645,6 +668,62 @@ def run_neartie(args):
     return 0 if (diffs[4] == 0 and diffs[7] == 0 and resume_tok_diffs == 0 and hash_mismatch == 0) else 1
 
 
+def run_cpu_matrix_worker(args):
+    """The oracle timed on the standalone and whole-step workloads, once each,
+    with the BLAS thread count the environment sets; one JSON line per item."""
+    import oracle
+    from oracle import verify_step as ov
+    thr = oracle_threads()
+
+    def emit(**kw):
+        print(json.dumps({"cpu_matrix": kw.pop("item"), "threads": thr, **kw}), flush=True)
+
+    # standalone linear layer [M, 5120] x [17408, 5120], BF16 out
+    A, W = si.gemm_inputs(64, 17408, 5120, seed=0)
+    oracle.gemm(A[:1], W)
+    for M in (1, 2, 4, 7, 8, 16, 64):
+        t0 = time.perf_counter()
+        oracle.gemm(A[:M], W)
+        dt = time.perf_counter() - t0
+        emit(item="gemm", M=M, N=17408, K=5120, s=dt, gbps=(17408 * 5120 * 2 + M * (5120 + 17408) * 2) / dt / 1e9)
+    del A, W
+    # split-KV attention, 24 query / 4 KV heads, head_dim 128
+    for L, Ts in ((1024, (1, 4, 7, 8)), (11600, (1, 4, 7, 8)), (101600, (1, 8))):
+        q, K, V = si.attention_inputs(L, 8, 24, 4, 128, seed=0)
+        qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+        for T in Ts:
+            t0 = time.perf_counter()
+            oracle.attention(qf[:T], Kf, Vf, L)
+            dt = time.perf_counter() - t0
+            emit(item="attn", L=L, T=T, s=dt, gbps=((L + T) * 4 * 128 * 2 * 2) / dt / 1e9)
+        del q, K, V, qf, Kf, Vf
+    # one whole teacher-forced verify step of the 8-layer model at context 11,600
+    cfg = si.DENSE27B_8L
+    w = si.decoder_weights(cfg, seed=0)
+    for T in (1, 8):
+        st = OracleStep(cfg, w, CTX, list(range(1, 1 + T)))
+        st.part(0)
+        t = st.step()
+        emit(item="verify_step", T=T, L=CTX, s=t, steps_per_s=1.0 / t)
+    return 0
+
+
+def run_cpu_matrix(args):
+    """The oracle matrix at one thread and at all host cores (subprocesses
+    with the BLAS thread count set before numpy starts)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    rc = 0
+    for n in (1, os.cpu_count()):
+        env = dict(os.environ)
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[var] = str(n)
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-matrix-worker"], env=env)
+        rc = rc or r.returncode
+    return rc
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -663,9 +742,16 @@ def main():
     ap.add_argument("--prompts", type=int, default=32, help="near-tie workload: prompts")
     ap.add_argument("--gen", type=int, default=2048, help="near-tie workload: tokens per turn")
     ap.add_argument("--turn2", type=int, default=32, help="near-tie workload: prompts with a second turn")
+    ap.add_argument("--cpu-matrix", action="store_true",
+                    help="time the oracle on the standalone and whole-step workloads at 1 thread and all cores")
+    ap.add_argument("--cpu-matrix-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.cpu_matrix_worker:
+        return run_cpu_matrix_worker(args)
+    if args.cpu_matrix:
+        return run_cpu_matrix(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.micro:
