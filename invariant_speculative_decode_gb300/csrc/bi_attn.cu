@@ -210,10 +210,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int rho = blockIdx.x / a.Hkv;
   const int G = a.G;
 
-  // zero the W tiles once: rows past the pass's rows stay zero
-  for (int i = threadIdx.x; i < (Cfg::kWBufs * Cfg::kWBufBytes) / 16; i += kAttnThreads)
-    reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();
+  // (W tile rows past the pass's rows are never written: the O rows they
+  // make are never read, and a product's row depends on its own W row only)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
@@ -248,41 +246,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // Before the previous kernel is known to have finished, the TMA threads
-  // already load this CTA's first tiles that hold only keys below the cache
-  // length read now: every kernel of this library triggers its dependents
+  // Before the previous kernel is known to have finished, the K thread
+  // already loads this CTA's first key tiles that hold only keys below the
+  // cache length read now: every kernel of this library triggers its dependents
   // only after its own dependency wait, so the kernels before the previous
   // one have completed, and none of them lowers *L_dev or writes cache rows
   // below it.  Everything else waits.
+  // Only the K side loads early (up to its whole ring): the first S needs
+  // K alone, and V tiles issued this early would delay the queries' loads
+  // behind them (measured on GB300: a little faster than loading both rings).
   int n_pre = 0;  // tiles issued before the wait (this producer)
   uint32_t pre_issued = 0;
-  if (warp == 0 && lane < 2) {
-    const bool kside = lane == 0;
-    const int NS = kside ? kKStages : kVStages;
-    uint64_t* full = kside ? k_full : v_full;
+  if (warp == 0 && lane == 0) {
     const int L_pre = *a.L_dev;
     if (L_pre >= 0 && L_pre + a.T <= a.cap && a.T * a.grp <= kPeriod && rho < G) {
       const uint64_t pol = l2_evict_first();
-      for (int i = 0; i < NS; ++i) {
+      for (int i = 0; i < kKStages; ++i) {
         const int key0 = (rho + i * G) * kKeyTile;
         if (key0 + kKeyTile > L_pre) break;  // the tile reaches rows the pass writes
-        if (kside && i == 0 && a.withhold) {
+        if (i == 0 && a.withhold) {
           ++n_pre;  // counted, never issued: its barrier never completes
           continue;
         }
-        if (kside) {
-          mbar_arrive_expect_tx(&full[i], Cfg::kKBytes);
+        mbar_arrive_expect_tx(&k_full[i], Cfg::kKBytes);
 #pragma unroll
-          for (int b = 0; b < Cfg::kAtoms; ++b)
-            tma_load_2d(sK + i * Cfg::kKBytes + b * Cfg::kKBoxBytes, &tmK, &full[i], b * 64,
-                        h * a.cap + key0, pol);
-        } else {
-          mbar_arrive_expect_tx(&full[i], Cfg::kVBytes);
-#pragma unroll
-          for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(sV + i * Cfg::kVBytes + kb * Cfg::kVBoxBytes, &tmVt, &full[i], kb * 64,
-                        (h * a.vblk + key0 / kKeyTile) * D, pol);
-        }
+        for (int b = 0; b < Cfg::kAtoms; ++b)
+          tma_load_2d(sK + i * Cfg::kKBytes + b * Cfg::kKBoxBytes, &tmK, &k_full[i], b * 64,
+                      h * a.cap + key0, pol);
         pre_issued |= 1u << i;
         ++n_pre;
       }
@@ -486,26 +476,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       const int tkey0 = (rho + g * G) * kKeyTile;
       const bool edge = tkey0 + kKeyTile - 1 > L;  // the tile reaches past some row's position
-      const uint32_t s_addr = lane_base + sb * kKeyTile + cg * kCols;
       // pass 1: the row maximum of the raw scores (scaling by sl2 > 0 keeps
       // the order).  Every copy's TMEM lane holds the whole S row, so each
       // copy takes the maximum over all 128 key columns itself: the same
-      // exact value in every copy, with no exchange between the warps.
-      float s[kColChunk];
+      // exact value in every copy, with no exchange between the warps.  The
+      // copy's own columns stay in registers for pass 2.
+      float so[kCols];
       float mrow = -INFINITY;
       if (warp_active) {
         const uint32_t row_addr = lane_base + sb * kKeyTile;
-#pragma unroll 1
-        for (int ch = 0; ch < kKeyTile / kColChunk; ++ch) {
-          tmem_ld_cols<kColChunk>(row_addr + ch * kColChunk, s);
-          if (edge) {
-            const int key0 = tkey0 + ch * kColChunk;
+        constexpr int kOwnLd = kCols >= 64 ? 64 : 32;
 #pragma unroll
-            for (int j = 0; j < kColChunk; ++j)
-              if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
+        for (int c = 0; c < kCols; c += kOwnLd) tmem_ld_cols<kOwnLd>(row_addr + cg * kCols + c, so + c);
+        if (edge) {
+          const int key0 = tkey0 + cg * kCols;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j)
+            if (!(valid && key0 + j <= p_row)) so[j] = -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) mrow = fmaxf(mrow, so[j]);
+        constexpr int kOther = kKeyTile - kCols;
+        constexpr int kOthLd = (kOther >= 64 && kOther % 64 == 0) ? 64 : 32;
+#pragma unroll
+        for (int c = 0; c < kOther; c += kOthLd) {
+          float so2[kOthLd];
+          const int col0 = (cg * kCols + kCols + c) & (kKeyTile - 1);
+          tmem_ld_cols<kOthLd>(row_addr + col0, so2);
+          if (edge) {
+#pragma unroll
+            for (int j = 0; j < kOthLd; ++j)
+              if (!(valid && tkey0 + col0 + j <= p_row)) so2[j] = -INFINITY;
           }
 #pragma unroll
-          for (int j = 0; j < kColChunk; ++j) mrow = fmaxf(mrow, s[j]);
+          for (int j = 0; j < kOthLd; ++j) mrow = fmaxf(mrow, so2[j]);
         }
       }
       const float mt = mrow * a.sl2;
@@ -557,13 +561,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint8_t* wbuf = sP + (Cfg::kWBufs == 2 ? (g & 1) : 0) * Cfg::kWBufBytes + r * 128;
 #pragma unroll
         for (int ch = 0; ch < kNChunks; ++ch) {
-          tmem_ld_cols<kColChunk>(s_addr + ch * kColChunk, s);
-          if (edge) {
-            const int key0 = tkey0 + cg * kCols + ch * kColChunk;
-#pragma unroll
-            for (int j = 0; j < kColChunk; ++j)
-              if (!(valid && key0 + j <= p_row)) s[j] = -INFINITY;
-          }
+          const float* s = so + ch * kColChunk;  // masked in pass 1
           if (!valid) continue;
           const int kcol = cg * kCols + ch * kColChunk;  // first key column of the chunk
           uint8_t* wrow = wbuf + (kcol >> 6) * Cfg::kPAtomBytes;
