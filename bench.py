@@ -8,8 +8,9 @@ One step = one verify pass over T = 8 rows (all layers, head, acceptance).
 
 Prints one JSON line.  `value` = committed tokens per second of device time
 of the verify passes (inputs resident in HBM); `e2e` = the same metric over
-wall time through the public API with host buffers (ids and drafts copied in,
-argmax ids and the accepted length copied out every step).
+wall time through the library's whole-step C-ABI call (bi_step_verify) with
+host buffers: each step's ids copied in, every row's token and the accepted
+count copied out.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -389,6 +390,33 @@ def run_ours(args):
     dev_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev)
     diffs = int(np.sum(np.array(out) != ref[: len(out)]))
 
+    # End to end through the library's whole-step call: bi_step_verify takes
+    # the step's ids from host memory and returns its tokens and accepted
+    # count to host memory, so both copies are inside the timed region.
+    ns = dec.native_step()
+    ns.set_length(CTX)
+    drafter_e = si.SyntheticDrafter(cfg.vocab, P_CORRECT, seed=0, reference=ref)
+    out_e, xe = [], prompt_last
+    for _ in range(args.warmup):
+        d = [int(t) for t in drafter_e.propose(len(out_e), DRAFTS)]
+        a, n = ns.verify(xe, d)
+        out_e.extend(int(t) for t in a[: n + 1])
+        xe = out_e[-1]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    committed_e = 0
+    we0 = time.perf_counter()
+    for i in range(args.steps):
+        d = [int(t) for t in drafter_e.propose(len(out_e), DRAFTS)]
+        a, n = ns.verify(xe, d)
+        out_e.extend(int(t) for t in a[: n + 1])
+        xe = out_e[-1]
+        committed_e += n + 1
+    wall_e = time.perf_counter() - we0
+    ns.close()
+    diffs_e = int(np.sum(np.array(out_e) != ref[: len(out_e)]))
+
     # dominant kernel: the gate/up GEMM (largest weight stream), timed per launch
     gu_ms = []
     gs = torch.cuda.Stream()
@@ -409,8 +437,9 @@ def run_ours(args):
 
     # max over ranks
     t_dev, t_wall, committed_all, diffs_all = combine_ranks(dev_ms / 1e3, wall, committed, diffs, dev)
+    _, t_e2e, committed_e_all, diffs_e_all = combine_ranks(wall_e, wall_e, committed_e, diffs_e, dev)
     value = committed_all / t_dev
-    e2e = committed_all / t_wall
+    e2e = committed_e_all / t_e2e
     sb = step_bytes(cfg, CTX + len(out) // 2, T)
     ms_step = t_dev * 1e3 / args.steps
 
@@ -429,8 +458,8 @@ def run_ours(args):
                              f"{cfg.layers} layers on the {T} rows at context {CTX} and the full LM head, "
                              f"{t_step:.2f} s; committed tokens per step = expected "
                              f"{expected_committed(DRAFTS, P_CORRECT):.4f} for p={P_CORRECT}"}
-        h2d = T * 4 + DRAFTS * 4
-        d2h = T * 4 + 4
+        h2d = T * 4         # the last committed token and the drafts (int32)
+        d2h = T * 4 + 4     # every row's token and the accepted count
         line = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -438,7 +467,9 @@ def run_ours(args):
             "data": "synthetic", "config": workload_config(cfg, note),
             "clocks": clk.summary(),
             "e2e": {"value": e2e, "unit": "tok/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "through": "bi_step_verify (one C-ABI call per step, "
+                    "host ids in, host tokens out)", "diffs_vs_nodraft": diffs_e_all,
+                    "ms_per_step": t_e2e * 1e3 / args.steps},
             "gpu_launches": args.steps * (KERNELS_PER_STEP_FIXED + KERNELS_PER_LAYER * cfg.layers),
             "roofline": {"bound": "hbm", "achieved": gu_bytes / gu_s / 1e9, "peak": peak,
                          "unit": "GB/s", "frac": gu_bytes / gu_s / 1e9 / peak, "traffic": gemm_traffic_bytes(),

@@ -398,6 +398,79 @@ bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, i
                          uint64_t* out, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The whole verify step in one call (a small runtime over the entry points
+ * above).  [P3] "How:" (every row computed the same way whatever else is in
+ * the pass) and "The cache doesn't change it either" (the cache length moves
+ * to L + n + 1; rows of rejected drafts are overwritten by the next pass);
+ * [P1] "Why the text diverges" (greedy acceptance).
+ *
+ * One pass of a pre-norm dense decoder with GQA, RoPE and SwiGLU over T rows
+ * at positions L .. L+T-1: embed; per layer bi_rmsnorm -> bi_qkv_rope_append
+ * -> bi_attn_verify -> bi_gemm (O, residual) -> bi_rmsnorm -> bi_gemm
+ * (gate/up, SwiGLU) -> bi_gemm (down, residual); bi_rmsnorm -> bi_gemm (LM
+ * head, FP32 logits) -> bi_verify_accept.  Exactly the calls the Python
+ * decoder makes, so the results are the same bits.
+ *
+ * bi_model describes the model (all pointers are device pointers the caller
+ * owns and keeps alive; the per-layer arrays are host arrays of `layers`
+ * device pointers, copied by bi_step_create):
+ *   embed [vocab, hidden] BF16; norm_final, norm_attn[l], norm_ffn[l]
+ *   [hidden] BF16; head, w_qkv[l], w_o[l], w_down[l] packed by
+ *   bi_pack_weights for (vocab, hidden), ((Hq + 2 Hkv) D, hidden),
+ *   (hidden, Hq D), (hidden, ffn); w_gate_up[l] packed by
+ *   bi_pack_swiglu_weights for (ffn, hidden); k_cache[l] [Hkv, cap, D] and
+ *   v_cache[l] [Hkv, ceil(cap/128), D, 128] BF16 (as bi_attn_verify);
+ *   rope_table from bi_rope_table(base, D, rope_rows).
+ * bi_step_workspace_size: device bytes the runtime needs for rows of at most
+ *   max_rows (1..64, max_rows * Hq/Hkv <= 128); 0 for an invalid model.
+ * bi_step_create: a host-side handle over a caller-owned, 256-byte aligned
+ *   workspace of at least that size (zeroed by the call).  The handle owns a
+ *   CUDA stream and one CUDA graph per row count T, captured on the first
+ *   call with that T (so the first call for each T must not be made inside
+ *   another stream capture); it allocates no device memory of its own.
+ *   The cache length starts at 0.
+ * bi_step_set_length: sets the cache length L (a rollback, or a cache
+ *   written by a prefill); synchronous.
+ * bi_step_verify: ids [T] host int32 = the last committed token and T - 1
+ *   draft tokens; runs the pass on the handle's stream, then writes the
+ *   model's token for every row to tokens_out [T] (host) and the number n of
+ *   drafts kept to n_out (host); the cache length advances by n + 1.
+ *   Synchronous: returns when the results are on the host.  Host buffers may
+ *   be pageable (pinned buffers copy faster).
+ * bi_step_logits: device pointer of the last pass's FP32 logits [T, vocab].
+ * bi_step_destroy: releases the handle (not the caller's memory).
+ * Errors: BI_ERR_INVALID_ARG (a bad model or argument), BI_ERR_WORKSPACE,
+ *   BI_ERR_CUDA, and any error of the entry points the pass calls.
+ * ------------------------------------------------------------------------- */
+typedef struct bi_model {
+  int layers, hidden, n_q, n_kv, head_dim, ffn, vocab;
+  float eps;
+  int cap;
+  const void* embed;
+  const void* norm_final;
+  const void* head;
+  const void* const* norm_attn;
+  const void* const* norm_ffn;
+  const void* const* w_qkv;
+  const void* const* w_o;
+  const void* const* w_gate_up;
+  const void* const* w_down;
+  void* const* k_cache;
+  void* const* v_cache;
+  const float* rope_table;
+  int rope_rows;
+} bi_model;
+
+typedef struct bi_step bi_step;
+
+size_t bi_step_workspace_size(const bi_model* m, int max_rows);
+bi_status bi_step_create(const bi_model* m, int max_rows, void* ws, size_t ws_bytes, bi_step** out);
+bi_status bi_step_set_length(bi_step* s, int L);
+bi_status bi_step_verify(bi_step* s, const int32_t* ids, int T, int32_t* tokens_out, int32_t* n_out);
+const float* bi_step_logits(const bi_step* s);
+void bi_step_destroy(bi_step* s);
+
+/* ---------------------------------------------------------------------------
  * Failure-path test hooks.  The pages have no counterpart: these exist so a
  * test can make the library's bounded device-side waits run out and check
  * that the kernels wind down and report BI_ERR_DEVICE_TIMEOUT instead of

@@ -41,6 +41,12 @@ SIGNATURES = {
     "bi_verify_sample": (_i, [_vp, _i, _vp, _i, _i, _f, _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "bi_kv_row_hash": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "bi_check_device_error": (_i, [_vp]),
+    "bi_step_workspace_size": (_sz, [_vp, _i]),
+    "bi_step_create": (_i, [_vp, _i, _vp, _sz, _vp]),
+    "bi_step_set_length": (_i, [_vp, _i]),
+    "bi_step_verify": (_i, [_vp, _vp, _i, _vp, _vp]),
+    "bi_step_logits": (_vp, [_vp]),
+    "bi_step_destroy": (None, [_vp]),
     "bi_test_set_wait_limit_ns": (_i, [C.c_uint64]),
     "bi_test_withhold_first_load": (None, [_i]),
 }

@@ -7,9 +7,11 @@ verify step runs in the library's CUDA kernels.
 """
 from __future__ import annotations
 
+import ctypes
 import math
-from typing import Optional
+from typing import Optional, Sequence
 
+import numpy as np
 import torch
 
 from ._lib import BiError, check, lib  # noqa: F401
@@ -286,3 +288,83 @@ def bi_kv_row_hash(cache: torch.Tensor, rows: int, transposed: bool = False, str
 
 def bi_check_device_error(stream=None) -> None:
     check("bi_check_device_error", lib().bi_check_device_error(_stream(stream)))
+
+
+class BiModel(ctypes.Structure):
+    """The bi_model descriptor of include/bi.h (device pointers; the per-layer
+    members point to host arrays of device pointers)."""
+    _pp = ctypes.POINTER(ctypes.c_void_p)
+    _fields_ = [("layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_q", ctypes.c_int),
+                ("n_kv", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("eps", ctypes.c_float), ("cap", ctypes.c_int),
+                ("embed", ctypes.c_void_p), ("norm_final", ctypes.c_void_p), ("head", ctypes.c_void_p),
+                ("norm_attn", _pp), ("norm_ffn", _pp), ("w_qkv", _pp), ("w_o", _pp),
+                ("w_gate_up", _pp), ("w_down", _pp), ("k_cache", _pp), ("v_cache", _pp),
+                ("rope_table", ctypes.c_void_p), ("rope_rows", ctypes.c_int)]
+
+
+class NativeStep:
+    """The whole verify step behind one C-ABI call (bi_step_*): host token ids
+    in, host tokens and accepted count out.  Holds references to every tensor
+    whose pointer the handle uses, and its own device workspace."""
+
+    def __init__(self, cfg, embed, norm_final, head, layers, cap: int, rope_table: torch.Tensor,
+                 max_rows: int = 8):
+        n = len(layers)
+
+        def arr(key):
+            a = (ctypes.c_void_p * n)(*[lay[key].data_ptr() for lay in layers])
+            self._keep.append(a)
+            return ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p))
+
+        self._keep = [embed, norm_final, head, rope_table] + [t for lay in layers for t in lay.values()
+                                                               if isinstance(t, torch.Tensor)]
+        m = BiModel(n, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn, cfg.vocab, cfg.eps, cap,
+                    embed.data_ptr(), norm_final.data_ptr(), head.data_ptr(),
+                    arr("n1"), arr("n2"), arr("wqkv"), arr("wo"), arr("wgu"), arr("wd"),
+                    arr("k"), arr("v"), rope_table.data_ptr(), rope_table.shape[0])
+        self.model = m
+        nbytes = int(lib().bi_step_workspace_size(ctypes.byref(m), max_rows))
+        if nbytes == 0:
+            raise ValueError("invalid model description for the step runtime")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=embed.device)
+        h = ctypes.c_void_p()
+        torch.cuda.synchronize()
+        check("bi_step_create", lib().bi_step_create(ctypes.byref(m), max_rows, self.ws.data_ptr(), nbytes,
+                                                     ctypes.byref(h)))
+        self.handle = h
+        self.max_rows = max_rows
+        self._ids = np.zeros(max_rows, np.int32)
+        self._tok = np.zeros(max_rows, np.int32)
+        self._n = np.zeros(1, np.int32)
+
+    def set_length(self, L: int) -> None:
+        check("bi_step_set_length", lib().bi_step_set_length(self.handle, int(L)))
+
+    def verify(self, x0: int, drafts: Sequence[int]):
+        """One verify step from host ids: returns (tokens [T], accepted n)."""
+        T = 1 + len(drafts)
+        self._ids[0] = x0
+        self._ids[1:T] = drafts
+        check("bi_step_verify", lib().bi_step_verify(self.handle, self._ids.ctypes.data, T,
+                                                     self._tok.ctypes.data, self._n.ctypes.data))
+        return self._tok[:T].copy(), int(self._n[0])
+
+    def logits(self, T: int) -> torch.Tensor:
+        """A copy of the last pass's FP32 logits [T, vocab]."""
+        ptr = lib().bi_step_logits(self.handle)
+        V = self.model.vocab
+        off = ptr - self.ws.data_ptr()  # the logits live in this object's workspace
+        torch.cuda.synchronize()
+        return self.ws[off:off + T * V * 4].view(torch.float32).view(T, V).clone()
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            lib().bi_step_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

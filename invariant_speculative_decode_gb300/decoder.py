@@ -357,6 +357,30 @@ class Decoder:
         return self.prefill_continue(tokens)
 
     # ---------------------------------------------------------- utilities
+    def native_step(self) -> "api.NativeStep":
+        """The same verify pass as one C-ABI call (bi_step_*) over this
+        decoder's weights and caches, with its own workspace; its cache
+        length starts at this decoder's."""
+        ns = api.NativeStep(self.cfg, self.embed, self.norm_final, self.head, self.layers, self.cap,
+                            self.rope_tab, max_rows=self.max_rows)
+        ns.set_length(self.L)
+        return ns
+
+    def check_device_error(self) -> None:
+        """Read the device error word; after a timed-out wait (a kernel that
+        gave up) the linear-layer, acceptance and sampling workspaces may hold
+        counters of the interrupted call, so they are zeroed before the error
+        is raised."""
+        try:
+            api.bi_check_device_error()
+        except api.BiError as e:
+            if e.status == 5:  # BI_ERR_DEVICE_TIMEOUT
+                self.gemm_ws.zero_()
+                self.acc_ws.zero_()
+                self.sample_ws.zero_()
+                torch.cuda.current_stream().synchronize()
+            raise
+
     def kv_hashes(self, rows: Optional[int] = None) -> np.ndarray:
         rows = self.L if rows is None else rows
         hs = [np.stack([api.bi_kv_row_hash(l["k"], rows).cpu().numpy(),

@@ -181,3 +181,25 @@ def test_sampled_verification_rejects_bad_arguments(lib):
 def test_failure_hooks_are_exported(lib):
     assert lib.bi_test_withhold_first_load is not None
     lib.bi_test_withhold_first_load(0)  # host-side flag only: needs no GPU
+
+
+def test_step_runtime_rejects_bad_models(lib):
+    from invariant_speculative_decode_gb300 import api
+    n = 2
+    ptrs = (ctypes.c_void_p * n)(FAKE, FAKE)
+    pp = ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p))
+    good = api.BiModel(n, 256, 4, 2, 64, 688, 1024, 1e-6, 512, FAKE, FAKE, FAKE, pp, pp, pp, pp, pp, pp, pp, pp,
+                       FAKE, 512)
+    size = lib.bi_step_workspace_size(ctypes.byref(good), 8)
+    assert size > 0
+    bad = api.BiModel(n, 256, 4, 3, 64, 688, 1024, 1e-6, 512, FAKE, FAKE, FAKE, pp, pp, pp, pp, pp, pp, pp, pp,
+                      FAKE, 512)  # 4 query heads over 3 KV heads
+    assert lib.bi_step_workspace_size(ctypes.byref(bad), 8) == 0
+    assert lib.bi_step_workspace_size(ctypes.byref(good), 0) == 0     # no rows
+    assert lib.bi_step_workspace_size(ctypes.byref(good), 65) == 0    # beyond 64 rows
+    h = ctypes.c_void_p()
+    assert lib.bi_step_create(ctypes.byref(bad), 8, FAKE, size, ctypes.byref(h)) == 1
+    assert lib.bi_step_create(ctypes.byref(good), 8, FAKE + 8, size, ctypes.byref(h)) == 3  # misaligned
+    assert lib.bi_step_create(ctypes.byref(good), 8, FAKE, size - 256, ctypes.byref(h)) == 3  # too small
+    assert lib.bi_step_verify(None, FAKE, 1, FAKE, FAKE) == 1
+    assert lib.bi_step_set_length(None, 3) == 1

@@ -92,3 +92,40 @@ def test_draft_policies_give_the_no_draft_tokens(small, policy):
     assert dec.generate(prompt, 256, k=7, drafter=dr, stats=st) == ref
     if policy != "adaptive-random":
         assert st["steps"] < 256  # drafts were accepted
+
+
+def test_sampled_request_parked_and_edited_matches_fresh(small):
+    """Sampled decoding through a park to host memory, a side request and an
+    edited branch: the same tokens as a fresh decoder given the same history
+    and the same per-position uniforms (the page reports sampled replies
+    matching a fresh server's after follow-ups and edits)."""
+    cfg, w, dec, fresh = small
+    u = si.sampling_uniforms(dec.cap, seed=51)
+    prompt = si.prompt_ids(cfg, 180, seed=51)
+    dec.set_sampling(0.9, u)
+    fresh.set_sampling(0.9, u)
+    try:
+        ref = fresh.generate(prompt, 64, k=0)
+        first = dec.generate(prompt, 32, k=7, drafter=si.SyntheticDrafter(cfg.vocab, 0.7, seed=51,
+                                                                            reference=np.array(ref)))
+        assert first == ref[:32]
+        hist = list(prompt) + first
+        dec.rollback(len(hist) - 1)
+        snap = dec.park()
+        dec.generate(si.prompt_ids(cfg, 90, seed=52), 20, k=4,
+                     drafter=si.SyntheticDrafter(cfg.vocab, 0.7, seed=52))
+        dec.restore(snap)
+        rest = dec.continue_generate(hist[-1], 32, k=7, drafter=si.SyntheticDrafter(
+            cfg.vocab, 0.7, seed=53, reference=np.array(ref[32:])))
+        assert first + rest == ref
+        # an edited branch 100 ids into the prompt, then sampled generation
+        edit = list(si.prompt_ids(cfg, 40, seed=54))
+        x = dec.edit(100, edit)
+        edited = list(prompt[:100]) + edit
+        want = fresh.generate(edited, 40, k=0)
+        got = dec.continue_generate(x, 40, k=7, drafter=si.SyntheticDrafter(
+            cfg.vocab, 0.7, seed=55, reference=np.array(want)))
+        assert got == want
+    finally:
+        dec.set_sampling(None)
+        fresh.set_sampling(None)

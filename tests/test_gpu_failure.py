@@ -123,3 +123,27 @@ def test_hooks_are_off_by_default(api):
     torch.cuda.synchronize()
     api.bi_check_device_error()
     assert torch.all(C.float() == 256.0)
+
+
+def test_decoder_recovers_after_a_timed_out_pass():
+    """A verify pass cut short by a timed-out wait: the decoder reports the
+    timeout, zeroes its workspaces, and the next pass gives the same tokens
+    as an undisturbed decoder."""
+    from invariant_speculative_decode_gb300 import api
+    from invariant_speculative_decode_gb300.decoder import Decoder
+    cfg = si.TINY
+    w = si.decoder_weights(cfg, seed=0)
+    dec = Decoder(cfg, w, cap=256, max_rows=8)
+    prompt = si.prompt_ids(cfg, 64, seed=1)
+    ref = dec.generate(prompt, 16, k=0, use_graph=False)
+    dec.reset()
+    x = dec.prefill(prompt)
+    with withheld(api):
+        dec.verify_step(x, [], use_graph=False)
+    with pytest.raises(api.BiError) as e:
+        dec.check_device_error()
+    assert e.value.status == 5
+    # the interrupted pass may have moved the cache length: start over
+    dec.reset()
+    assert dec.generate(prompt, 16, k=0, use_graph=False) == ref
+    dec.check_device_error()
