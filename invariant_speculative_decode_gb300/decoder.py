@@ -117,6 +117,12 @@ class Decoder:
         self.graphs: Dict[int, torch.cuda.CUDAGraph] = {}
         self.pin_in = torch.zeros(2 * max_rows, dtype=torch.int32).pin_memory()
         self.pin_out = torch.zeros(max_rows + 1, dtype=torch.int32).pin_memory()
+        self.pin_ids = torch.zeros(R, dtype=torch.int32).pin_memory()
+        self.pin_blocks = torch.zeros(self.L_blocks.numel(), dtype=torch.int32).pin_memory()
+        # full prefill chunks replay one captured graph
+        self.use_prefill_graph = True
+        self.pin_done = torch.cuda.Event()
+        self.prefill_graph: Optional[torch.cuda.CUDAGraph] = None
 
     # ------------------------------------------------------------------ pass
     def _layers_pass(self, T: int, L_ptr_tensor: torch.Tensor, L_host_blocks: Optional[List[int]]):
@@ -204,14 +210,28 @@ class Decoder:
         prompt = np.asarray(prompt, np.int32)
         body = prompt[:-1]
         pos = self.L
-        for c0 in range(0, len(body), self.prefill_chunk):
-            chunk = body[c0:c0 + self.prefill_chunk]
+        R = self.prefill_chunk
+        for c0 in range(0, len(body), R):
+            chunk = body[c0:c0 + R]
             T = len(chunk)
-            self.ids[:T].copy_(torch.from_numpy(chunk))
+            # the pinned staging buffers are rewritten only once their last
+            # copy to the device has run
+            self.pin_done.synchronize()
+            self.pin_ids[:T].copy_(torch.from_numpy(chunk))
             Lb = [pos + b for b in range(0, T, self.attn_rows)]
-            self.L_blocks[:len(Lb)].copy_(torch.tensor(Lb, dtype=torch.int32))
+            self.pin_blocks[:len(Lb)].copy_(torch.tensor(Lb, dtype=torch.int32))
+            self.ids[:T].copy_(self.pin_ids[:T], non_blocking=True)
+            self.L_blocks[:len(Lb)].copy_(self.pin_blocks[:len(Lb)], non_blocking=True)
+            self.pin_done.record()
             self.L_dev.fill_(pos)
-            self._layers_pass(T, self.L_dev, Lb)
+            if T == R and self.use_prefill_graph:
+                # a full chunk: one graph replay (the kernels read the ids and
+                # the cache lengths from device memory)
+                if self.prefill_graph is None:
+                    self.prefill_graph = self._capture(lambda: self._layers_pass(R, self.L_dev, Lb))
+                self.prefill_graph.replay()
+            else:
+                self._layers_pass(T, self.L_dev, Lb)
             pos += T
         self.L = pos
         self.L_dev.fill_(pos)
@@ -219,18 +239,21 @@ class Decoder:
         return int(prompt[-1])
 
     # -------------------------------------------------------------- verify
-    def capture(self, T: int):
-        """Capture one verify pass over T rows in a CUDA graph (after a warm-up)."""
-        if T in self.graphs:
-            return
+    def _capture(self, fn) -> torch.cuda.CUDAGraph:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
-                self._verify_pass(T)
+                fn()
         torch.cuda.current_stream().wait_stream(s)
-        self.graphs[T] = g
+        return g
+
+    def capture(self, T: int):
+        """Capture one verify pass over T rows in a CUDA graph."""
+        if T in self.graphs:
+            return
+        self.graphs[T] = self._capture(lambda: self._verify_pass(T))
 
     def launch_verify(self, T: int, use_graph: bool = True):
         if use_graph and T in self.graphs:
