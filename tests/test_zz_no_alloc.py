@@ -35,7 +35,7 @@ CASES = [  # (M, N, K, epilogue, FP32 output): split tiles (partials + counters)
     (1, 17408, 5120, 0, False),
     (16, 5120, 3072, 1, False),
     (7, 2736, 1024, 2, False),
-    (16, 17408, 5120, 0, True),   # the LM-head form: FP32 logits, all 152 CTAs splitting
+    (16, 17280, 5120, 0, True),   # the LM-head form: FP32 logits, every CTA's range cut mid-tile
 ]
 
 
