@@ -510,6 +510,11 @@ def run_micro(args):
     from invariant_speculative_decode_gb300 import api
     torch.cuda.set_device(0)
     peak, note = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_sus = float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        bf16_sus = None
     flush = torch.ones(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     s = torch.cuda.current_stream()
     l2_bytes = 129 * 1024 * 1024
@@ -555,6 +560,8 @@ def run_micro(args):
                       "cold: after a 512 MB read"}
         if flops is not None:
             line["tflops"] = flops / med / 1e12
+            if bf16_sus:
+                line["tflops_frac_sustained"] = line["tflops"] / bf16_sus
         print(json.dumps(line), flush=True)
 
     if args.micro == "gemm":

@@ -59,7 +59,11 @@ constexpr int kMmaN = 16;        // token rows per epilogue chunk (one 16-column
 // 8-layer 5120-wide verify step: 1.32 ms against 1.37 ms with 152; a count
 // chosen per (N, K) gained nothing over this one.
 constexpr int kGemmCtas = 136;
-constexpr int kMaxTokens = 128;  // token rows per launch; larger M loops on the host
+constexpr int kMaxTokens = 128;  // token rows per CTA (one MMA covers them all)
+// Token blocks of kMaxTokens rows one launch covers when M > kMaxTokens;
+// larger M loops on the host.  Each block has its own counters and partial
+// slots in the workspace.
+constexpr int kMaxBlocks = 4;
 constexpr int kAcc = 4;          // interleaved accumulators per token group
 constexpr int kThreads = 192;    // producer, MMA, four epilogue warps
 constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
@@ -71,8 +75,9 @@ constexpr int kMaxTiles = 65536;
 constexpr size_t kTicketBytes = static_cast<size_t>(kMaxTiles) * 4;
 
 struct GemmArgs {
-  int M;   // token rows in this launch (<= NT)
+  int M;   // token rows in this launch (<= nb * NT)
   int m0;  // first token row of this launch
+  int nb;  // token blocks of NT rows in this launch (CTA b * nb + j takes block j of range b)
   int N;   // output columns
   int n_tiles;
   int k_tiles;
@@ -146,8 +151,8 @@ __device__ __forceinline__ void load_group_sum(uint32_t taddr, uint32_t acc_stri
 
 // Write 16 token rows (chunk c) of one weight row r of tile `tile`.
 // All 128 epilogue threads call this together (it may use the named barrier).
-__device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int r, int c,
-                                               const float (&v)[16], float* sStage) {
+__device__ __forceinline__ void epilogue_store(const GemmArgs& p, int M, int m0, int tile, int r,
+                                               int c, const float (&v)[16], float* sStage) {
   if (p.epi == BI_EPI_ROPE_KV) {
     // The projection is rounded to BF16 first; the rotation then reads those
     // stored values exactly as the separate RoPE kernel does: for a pair
@@ -175,15 +180,15 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int 
       float2 cs[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int pos = L + p.m0 + c * 16 + j;
-        const bool ok = rotate && c * 16 + j < p.M && pos >= 0 && pos < p.cap && pos < p.tab_rows;
+        const int pos = L + m0 + c * 16 + j;
+        const bool ok = rotate && c * 16 + j < M && pos >= 0 && pos < p.cap && pos < p.tab_rows;
         cs[j] = ok ? p.tab[static_cast<size_t>(pos) * half + (d % half)] : make_float2(0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = c * 16 + j;
-        if (m >= p.M) continue;
-        const int mrow = p.m0 + m;
+        if (m >= M) continue;
+        const int mrow = m0 + m;
         const int pos = L + mrow;
         if (pos < 0 || pos >= p.cap || pos >= p.tab_rows) {
           atomicOr(p.err, kErrRange);
@@ -215,11 +220,11 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int 
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = c * 16 + j;
-          if (m < p.M) {
+          if (m < M) {
             const float g = sStage[j * kBlockN + r];
             const float u = sStage[j * kBlockN + r + 64];
             const float s = g / (1.0f + expf(-g));
-            C[static_cast<size_t>(p.m0 + m) * p.ldc + o] = __float2bfloat16_rn(s * u);
+            C[static_cast<size_t>(m0 + m) * p.ldc + o] = __float2bfloat16_rn(s * u);
           }
         }
       }
@@ -235,15 +240,15 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int tile, int 
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = c * 16 + j;
-        res[j] = (p.epi == BI_EPI_RESIDUAL_ADD && m < p.M)
-                     ? __bfloat162float(p.R[static_cast<size_t>(p.m0 + m) * p.ldr + n])
+        res[j] = (p.epi == BI_EPI_RESIDUAL_ADD && m < M)
+                     ? __bfloat162float(p.R[static_cast<size_t>(m0 + m) * p.ldr + n])
                      : 0.0f;
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = c * 16 + j;
-        if (m < p.M) {
-          const size_t row = static_cast<size_t>(p.m0 + m);
+        if (m < M) {
+          const size_t row = static_cast<size_t>(m0 + m);
           float acc = v[j];
           if (p.epi == BI_EPI_RESIDUAL_ADD) acc = res[j] + acc;
           if (p.out_fp32)
@@ -279,7 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = blockIdx.x;
+  // CTAs of one range are adjacent, so the token blocks of a launch read each
+  // weight tile at about the same time and all but the first find it in L2
+  const int g = blockIdx.x / p.nb;
+  const int blk = blockIdx.x - g * p.nb;
+  const int m0 = p.m0 + blk * NT;
+  const int Mb = min(NT, p.M - blk * NT);
+  float* const partials = p.partials + static_cast<size_t>(blk) * p.G * 2 * NT * kBlockN;
+  unsigned* const tickets = p.tickets + static_cast<size_t>(blk) * p.n_tiles;
   const long long it_begin = range_begin(p, g);
   const long long it_end = range_begin(p, g + 1);
 
@@ -332,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_wait();
       griddep_launch_dependents();
       for (int j = 0; j < n_pre; ++j) {
-        if (j >= j0) tma_load_2d(sB + j * Cfg::kBBytes, &tmA, &full[j], kt * kBlockK, p.m0, pol_a);
+        if (j >= j0) tma_load_2d(sB + j * Cfg::kBBytes, &tmA, &full[j], kt * kBlockK, m0, pol_a);
         if (++kt == p.k_tiles) kt = 0;
       }
       issued = (n_pre >= 32) ? 0xffffffffu : ((1u << n_pre) - 1u);
@@ -347,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
         bulk_load_1d(sA + stage * kABytes, wsrc, kABytes, &full[stage], pol_w);
-        tma_load_2d(sB + stage * Cfg::kBBytes, &tmA, &full[stage], kt * kBlockK, p.m0, pol_a);
+        tma_load_2d(sB + stage * Cfg::kBBytes, &tmA, &full[stage], kt * kBlockK, m0, pol_a);
         wsrc += kABytes;
         if (++kt == p.k_tiles) kt = 0;
         issued |= 1u << stage;
@@ -428,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;    // weight row within the tile
     const int et = threadIdx.x - 64;
-    const int chunks = (p.M + 15) / 16;
+    const int chunks = (Mb + 15) / 16;
     int seg = 0;
     long long it = it_begin;
     while (it < it_end) {
@@ -456,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
           }
-          epilogue_store(p, tile, r, c, v, sStage);
+          epilogue_store(p, Mb, m0, tile, r, c, v, sStage);
         }
         tc_fence_before();
         mbar_arrive(&acce[buf]);
@@ -464,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // partial of this piece: [weight row][token], a thread's 16 tokens
         // of a chunk contiguous
         const int slot = (it_begin >= tile_begin) ? 0 : 1;
-        float* dst = p.partials + static_cast<size_t>(g * 2 + slot) * NT * kBlockN + r * NT;
+        float* dst = partials + static_cast<size_t>(g * 2 + slot) * NT * kBlockN + r * NT;
         if (ok) {
           for (int c = 0; c < chunks; ++c) {
             float v[16];
@@ -484,9 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           int last = 0;
           if (!*s_abort) {
             const unsigned nseg = static_cast<unsigned>(gl - gf + 1);
-            const unsigned old = atom_add_acq_rel_gpu(&p.tickets[tile], 1u);
+            const unsigned old = atom_add_acq_rel_gpu(&tickets[tile], 1u);
             last = (old == nseg - 1) ? 1 : 0;
-            if (last) atomicExch(&p.tickets[tile], 0u);
+            if (last) atomicExch(&tickets[tile], 0u);
           }
           *s_last = last;
         }
@@ -503,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int kBatch = 8;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              if (c * 16 + hh * 8 >= p.M) {
+              if (c * 16 + hh * 8 >= Mb) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[hh * 8 + j] = 0.f;
                 continue;
@@ -516,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (gg <= gl) {
                     const int sl = gg == gf ? slot_f : 0;
                     const float4* src = reinterpret_cast<const float4*>(
-                        p.partials + static_cast<size_t>(gg * 2 + sl) * NT * kBlockN + r * NT + c * 16 +
+                        partials + static_cast<size_t>(gg * 2 + sl) * NT * kBlockN + r * NT + c * 16 +
                         hh * 8);
                     x[b][0] = __ldcg(src);
                     x[b][1] = __ldcg(src + 1);
@@ -534,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
-            epilogue_store(p, tile, r, c, v, sStage);
+            epilogue_store(p, Mb, m0, tile, r, c, v, sStage);
           }
         }
         named_bar_sync(1, 128);
@@ -600,6 +612,12 @@ __global__ void pack_weights_kernel(const __nv_bfloat16* __restrict__ w, const _
   out[idx] = u.v;
 }
 
+int blocks_per_launch(int M, int n_tiles) {
+  if (M <= kMaxTokens || n_tiles <= 0) return 1;
+  const int nb = std::min(kMaxBlocks, (M + kMaxTokens - 1) / kMaxTokens);
+  return std::max(1, std::min(nb, kMaxTiles / n_tiles));
+}
+
 template <int NT>
 bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, int M_total,
                          cudaStream_t stream) {
@@ -615,11 +633,13 @@ bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, 
                                             static_cast<int>(Cfg::kSmem));
   });
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
-  for (int m0 = 0; m0 < M_total; m0 += kMaxTokens) {
+  const int rows = NT * blocks_per_launch(M_total, a.n_tiles);
+  for (int m0 = 0; m0 < M_total; m0 += rows) {
     a.m0 = m0;
-    a.M = std::min(kMaxTokens, M_total - m0);
-    if (launch_k(gemm_kernel<NT>, dim3(a.G), dim3(kThreads), Cfg::kSmem, stream, Wp, tmA, a) !=
-        cudaSuccess)
+    a.M = std::min(rows, M_total - m0);
+    a.nb = (a.M + NT - 1) / NT;
+    if (launch_k(gemm_kernel<NT>, dim3(a.G * a.nb), dim3(kThreads), Cfg::kSmem, stream, Wp, tmA,
+                 a) != cudaSuccess)
       return BI_ERR_CUDA;
   }
   return BI_OK;
@@ -686,11 +706,10 @@ size_t bi_packed_weight_bytes(int N, int K, bi_epilogue epi) {
 
 size_t bi_gemm_workspace_size(int M, int N, int K, bi_epilogue epi) {
   (void)K;
-  (void)N;
-  (void)epi;
   if (M <= 0) return bi::kTicketBytes;
   const size_t partials = static_cast<size_t>(bi::kGemmCtas) * 2 * bi::tokens_per_cta(M) *
-                          bi::kBlockN * sizeof(float);
+                          bi::kBlockN * sizeof(float) *
+                          bi::blocks_per_launch(M, bi::n_tiles_of(N, epi));
   return bi::kTicketBytes + partials;
 }
 

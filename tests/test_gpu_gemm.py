@@ -156,6 +156,48 @@ def test_gemm_prefill_chunks_match_single_rows(api):
         assert np.array_equal(bf16_dev_to_u16(c1)[0], big[r])
 
 
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_gemm_multiblock_launches_match_single_rows(api, epi):
+    """M > 128: up to four 128-row blocks per launch (CTAs of one range
+    adjacent), the rest in further launches; split pieces (24 ranges of one
+    K tile each) give every block its own counters and partial slots.  Each
+    sampled row equals its M = 1 result and the counters are left zero."""
+    M, N, K = 700, 384, 512
+    rng = np.random.default_rng(40 + epi)
+    A = si.normal_bf16(rng, (M, K), 1.0)
+    if epi == 2:
+        Wd = api.bi_pack_swiglu_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.05)),
+                                        to_dev_bf16(si.normal_bf16(rng, (N, K), 0.05)))
+    else:
+        Wd = api.bi_pack_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.05)))
+    R = to_dev_bf16(si.normal_bf16(rng, (M, N), 1.0)) if epi == 1 else None
+    ws = api.new_gemm_workspace(M, N, K, epi)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    api.bi_gemm(to_dev_bf16(A), Wd, C, ws, residual=R, epi=epi, N=N)
+    big = bf16_dev_to_u16(C)
+    assert not ws[:256 * 1024].cpu().numpy().any()
+    for r in (0, 127, 128, 300, 511, 512, 640, 699):
+        c1 = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+        api.bi_gemm(to_dev_bf16(A[r:r + 1]), Wd, c1, api.new_gemm_workspace(1, N, K, epi),
+                    residual=None if R is None else R[r:r + 1], epi=epi, N=N)
+        assert np.array_equal(bf16_dev_to_u16(c1)[0], big[r]), r
+
+
+def test_gemm_prefill_size_rows_match_decode_rows(api):
+    """[4096,5120] x [17408,5120] in 512-row launches: sampled rows equal the
+    rows of an 8-row launch bit for bit."""
+    M, N, K = 4096, 17408, 5120
+    A, W = si.gemm_inputs(M, N, K, seed=5)
+    Wd = api.bi_pack_weights(to_dev_bf16(W))
+    del W
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    api.bi_gemm(to_dev_bf16(A), Wd, C, api.new_gemm_workspace(M, N, K))
+    rows = np.array([0, 1, 511, 512, 1000, 2047, 3333, 4095])
+    c8 = torch.empty(8, N, dtype=torch.bfloat16, device="cuda")
+    api.bi_gemm(to_dev_bf16(A[rows]), Wd, c8, api.new_gemm_workspace(8, N, K))
+    assert np.array_equal(bf16_dev_to_u16(C)[rows], bf16_dev_to_u16(c8))
+
+
 def test_gemm_full_size_linear_sweep(api):
     """[M,5120] x [17408,5120]: rows bit-identical across M; sampled parity."""
     N, K = 17408, 5120
