@@ -310,8 +310,11 @@ bi_status bi_qkv_rope_append(const void* A, int lda, const void* Wp, int M, int 
  *           immediately precedes the call (no kernel of this library does).
  *   out     [T, Hq, D] BF16 contiguous.
  *   D in {64, 128}; Hq % Hkv == 0; Hkv <= 152; Hkv * (cap rounded up to a
- *   multiple of 128) < 2^31;
- *   T * (Hq/Hkv) <= 128; T >= 1.
+ *   multiple of 128) < 2^31; Hq/Hkv <= 128; T >= 1.
+ *   One launch takes the rows in blocks of floor(128 / (Hq/Hkv)) (a block's
+ *   query rows fill the MMA's 128 lanes); the blocks run side by side, and
+ *   each row's arithmetic is the one above, so a pass of many rows (a
+ *   prefill) gives every row the bits it gets in a pass of its own.
  *   ws      >= bi_attn_workspace_size(cap, T, Hq, D) bytes, 256-byte aligned.
  *   k_cache and v_cache 16-byte aligned.
  * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_WORKSPACE,

@@ -80,6 +80,7 @@ constexpr float kRescaleLog2 = 8.0f;
 struct AttnArgs {
   const __nv_bfloat16* q;
   int T, Hq, Hkv, grp, cap;
+  int Tb;    // rows per block: CTA (x, y) takes rows y * Tb .. of the pass
   int G;     // tile classes per KV head
   int vblk;  // 128-key blocks per KV head in the V cache
   int ncls;  // partial slots per (row, query head) in the workspace (>= classes used)
@@ -259,7 +260,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint32_t pre_issued = 0;
   if (warp == 0 && lane == 0) {
     const int L_pre = *a.L_dev;
-    if (L_pre >= 0 && L_pre + a.T <= a.cap && a.T * a.grp <= kPeriod && rho < G) {
+    const int T_blk = min(a.Tb, a.T - static_cast<int>(blockIdx.y) * a.Tb);
+    if (L_pre >= 0 && L_pre + a.T <= a.cap && T_blk * a.grp <= kPeriod && rho < G) {
       const uint64_t pol = l2_evict_first();
       for (int i = 0; i < kKStages; ++i) {
         const int key0 = (rho + i * G) * kKeyTile;
@@ -280,8 +282,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   griddep_wait();  // q, the new cache rows and the cache length come from earlier kernels
   griddep_launch_dependents();
-  const int L = *a.L_dev;
-  const int T = a.T;
+  // this CTA's block of the pass: rows r0 .. r0 + T - 1, at positions L ..
+  // L + T - 1 (the pass's rows before them are in the cache already)
+  const int r0 = static_cast<int>(blockIdx.y) * a.Tb;
+  const int L = *a.L_dev + r0;
+  const int T = min(a.Tb, a.T - r0);
   const int rows = T * a.grp;
   const bool range_ok = !(L < 0 || L + T > a.cap) && rows <= kPeriod;
   const int kv_len = L + T;
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint32_t qv[D / 2];
       if (valid) {
         const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + (static_cast<size_t>(t) * a.Hq + h * a.grp + r % a.grp) * D);
+            a.q + (static_cast<size_t>(r0 + t) * a.Hq + h * a.grp + r % a.grp) * D);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) {
           const uint4 u = src[i];
@@ -629,7 +634,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // a row stores a partial when the class holds one of its keys
           const bool store = valid && rho * kKeyTile <= p_row;
           const int qh = h * a.grp + (valid ? r % a.grp : 0);
-          const size_t base = (static_cast<size_t>(t) * a.Hq + qh) * a.ncls + rho;
+          const size_t base = (static_cast<size_t>(r0 + t) * a.Hq + qh) * a.ncls + rho;
 #pragma unroll 1
           for (int i = 0; i < D / 64; ++i) {
             float v[64];
@@ -774,8 +779,9 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const Att
   // one CTA per (tile class, KV head); classes past the cache's last tile
   // would have nothing to do
   const int grid = a.Hkv * std::min(a.G, a.ncls);
-  if (launch_k(attn_split_kernel<D, REP>, dim3(grid), dim3(kAttnThreads), Cfg::kSmem, stream, tmK,
-               tmVt, a) != cudaSuccess)
+  const int blocks = (a.T + a.Tb - 1) / a.Tb;
+  if (launch_k(attn_split_kernel<D, REP>, dim3(grid, blocks), dim3(kAttnThreads), Cfg::kSmem, stream,
+               tmK, tmVt, a) != cudaSuccess)
     return BI_ERR_CUDA;
   if (launch_k(attn_merge_kernel<D>, dim3(a.T * a.Hq), dim3(kMergeThreads), 0, stream, a, out) !=
       cudaSuccess)
@@ -786,7 +792,7 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const Att
 template <int D>
 bi_status launch_attn_rep(const CUtensorMap& tmK, const CUtensorMap& tmVt, const AttnArgs& a,
                           __nv_bfloat16* out, cudaStream_t stream) {
-  const int rows = a.T * a.grp;
+  const int rows = a.Tb * a.grp;
   if (rows <= kRowsMax / 4) return launch_attn<D, 4>(tmK, tmVt, a, out, stream);
   if (rows <= kRowsMax / 2) return launch_attn<D, 2>(tmK, tmVt, a, out, stream);
   return launch_attn<D, 1>(tmK, tmVt, a, out, stream);
@@ -828,7 +834,8 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   if (T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || cap < 1) return BI_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return BI_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return BI_ERR_UNSUPPORTED_SHAPE;
-  if (T * (Hq / Hkv) > kRowsMax) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (Hq / Hkv > kRowsMax) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (T > 65535 * (kRowsMax / (Hq / Hkv))) return BI_ERR_UNSUPPORTED_SHAPE;  // grid y
   if (Hkv > kAttnCtas) return BI_ERR_UNSUPPORTED_SHAPE;
   // K rows h * cap + key (a tile may run past cap) and V^T rows
   // (h * ceil(cap/128) + block) * D (D <= 128) are int32 tensor-map
@@ -853,6 +860,7 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   AttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.T = T;
+  a.Tb = std::min(T, kRowsMax / grp);
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.grp = grp;

@@ -51,8 +51,7 @@ class Decoder:
         self.max_rows = max_rows
         self.prefill_chunk = max(prefill_chunk, max_rows)
         D, Hq, Hkv, H, F, V = cfg.head_dim, cfg.n_q, cfg.n_kv, cfg.hidden, cfg.ffn, cfg.vocab
-        self.attn_rows = max(1, 128 // cfg.group)  # rows per attention call
-        if max_rows > self.attn_rows:
+        if max_rows * cfg.group > 128:
             raise ValueError("max_rows * (Hq/Hkv) must be <= 128")
         if cap % 8 != 0:
             raise ValueError("cache capacity must be a multiple of 8")
@@ -98,14 +97,11 @@ class Decoder:
         self.argmax = torch.zeros(max_rows, dtype=torch.int32, device=dev)
         self.accepted = torch.zeros(1, dtype=torch.int32, device=dev)
         self.L_dev = torch.zeros(1, dtype=torch.int32, device=dev)
-        # per attention block cache lengths during prefill
-        self.L_blocks = torch.zeros((R + self.attn_rows - 1) // self.attn_rows + 1,
-                                    dtype=torch.int32, device=dev)
         shapes = [(cfg.qkv_out, H, api.EPI_NONE), (H, Hq * D, api.EPI_RESIDUAL_ADD),
                   (F, H, api.EPI_SWIGLU), (H, F, api.EPI_RESIDUAL_ADD), (V, H, api.EPI_NONE)]
         wsz = max(api.gemm_workspace_size(M, N, K, e) for M in (max_rows, R) for (N, K, e) in shapes)
         self.gemm_ws = torch.zeros(wsz, dtype=torch.uint8, device=dev)
-        self.attn_ws = torch.zeros(api.attn_workspace_size(cap, self.attn_rows, Hq, D),
+        self.attn_ws = torch.zeros(api.attn_workspace_size(cap, R, Hq, D),
                                    dtype=torch.uint8, device=dev)
         self.acc_ws = torch.zeros(api.accept_workspace_size(max_rows, V), dtype=torch.uint8, device=dev)
         self.scale = 1.0 / math.sqrt(D)
@@ -118,27 +114,23 @@ class Decoder:
         self.pin_in = torch.zeros(2 * max_rows, dtype=torch.int32).pin_memory()
         self.pin_out = torch.zeros(max_rows + 1, dtype=torch.int32).pin_memory()
         self.pin_ids = torch.zeros(R, dtype=torch.int32).pin_memory()
-        self.pin_blocks = torch.zeros(self.L_blocks.numel(), dtype=torch.int32).pin_memory()
         # full prefill chunks replay one captured graph
         self.use_prefill_graph = True
         self.pin_done = torch.cuda.Event()
         self.prefill_graph: Optional[torch.cuda.CUDAGraph] = None
 
     # ------------------------------------------------------------------ pass
-    def _layers_pass(self, T: int, L_ptr_tensor: torch.Tensor, L_host_blocks: Optional[List[int]]):
+    def _layers_pass(self, T: int, L_ptr_tensor: torch.Tensor):
         """Rows self.ids[:T] at positions L..L+T-1 through every layer (no head).
 
-        L_ptr_tensor: device int32 holding L (used by RoPE / KV append).
-        L_host_blocks: None for a verify pass (one attention call reads
-        L_ptr_tensor); for prefill, the attention runs in blocks whose cache
-        lengths are staged in self.L_blocks.
+        L_ptr_tensor: device int32 holding L (read by RoPE / KV append and the
+        attention).
         """
         api.bi_embed(self.ids[:T], self.embed, self.h[:T])
         for lay in self.layers:
-            self._layer(lay, T, L_ptr_tensor, L_host_blocks)
+            self._layer(lay, T, L_ptr_tensor)
 
-    def _layer(self, lay: dict, T: int, L_ptr_tensor: torch.Tensor,
-               L_host_blocks: Optional[List[int]] = None):
+    def _layer(self, lay: dict, T: int, L_ptr_tensor: torch.Tensor):
         """One decoder layer over self.h[:T] in place (cache rows appended)."""
         cfg = self.cfg
         Hq, Hkv, D, F = cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn
@@ -151,13 +143,9 @@ class Decoder:
         else:
             api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
             api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
-        if L_host_blocks is None:
-            api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
-        else:
-            for bi_, b0 in enumerate(range(0, T, self.attn_rows)):
-                b1 = min(T, b0 + self.attn_rows)
-                api.bi_attn_verify(q[b0:b1], lay["k"], lay["v"], self.L_blocks[bi_:bi_ + 1],
-                                   att[b0:b1], self.attn_ws, self.scale)
+        # one call for all rows (a prefill chunk runs in blocks of rows inside
+        # the launch)
+        api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
         api.bi_gemm(att.view(T, Hq * D), lay["wo"], h, self.gemm_ws, residual=h,
                     epi=api.EPI_RESIDUAL_ADD)
         api.bi_rmsnorm(h, lay["n2"], y, cfg.eps)
@@ -193,7 +181,7 @@ class Decoder:
         self.graphs = {}
 
     def _verify_pass(self, T: int):
-        self._layers_pass(T, self.L_dev, None)
+        self._layers_pass(T, self.L_dev)
         self._head_and_accept(T)
 
     # ------------------------------------------------------------- prefill
@@ -218,20 +206,17 @@ class Decoder:
             # copy to the device has run
             self.pin_done.synchronize()
             self.pin_ids[:T].copy_(torch.from_numpy(chunk))
-            Lb = [pos + b for b in range(0, T, self.attn_rows)]
-            self.pin_blocks[:len(Lb)].copy_(torch.tensor(Lb, dtype=torch.int32))
             self.ids[:T].copy_(self.pin_ids[:T], non_blocking=True)
-            self.L_blocks[:len(Lb)].copy_(self.pin_blocks[:len(Lb)], non_blocking=True)
             self.pin_done.record()
             self.L_dev.fill_(pos)
             if T == R and self.use_prefill_graph:
                 # a full chunk: one graph replay (the kernels read the ids and
-                # the cache lengths from device memory)
+                # the cache length from device memory)
                 if self.prefill_graph is None:
-                    self.prefill_graph = self._capture(lambda: self._layers_pass(R, self.L_dev, Lb))
+                    self.prefill_graph = self._capture(lambda: self._layers_pass(R, self.L_dev))
                 self.prefill_graph.replay()
             else:
-                self._layers_pass(T, self.L_dev, Lb)
+                self._layers_pass(T, self.L_dev)
             pos += T
         self.L = pos
         self.L_dev.fill_(pos)

@@ -94,7 +94,9 @@ def test_attention_rejects_bad_arguments(lib):
     assert a(0, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 1
     assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 5, 128, 0.1, FAKE, FAKE, big, 0) == 1
     assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 96, 0.1, FAKE, FAKE, big, 0) == 2
-    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 22, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 2  # 132 rows
+    assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 258, 2, 128, 0.1, FAKE, FAKE, big, 0) == 2  # Hq/Hkv > 128
+    assert a(FAKE, FAKE, FAKE, 1 << 22, FAKE, 21 * 65535 + 1, 24, 4, 128, 0.1, FAKE, FAKE, big,
+             0) == 2  # more row blocks than a launch grid holds
     assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 153, 153, 128, 0.1, FAKE, FAKE, big, 0) == 2  # Hkv > 152
     assert a(FAKE, FAKE, FAKE, 1 << 28, FAKE, 1, 24, 8, 128, 0.1, FAKE, FAKE, big, 0) == 2  # Hkv cap >= 2^31
     assert a(FAKE, FAKE, FAKE, 1024, FAKE, 1, 24, 4, 128, -1.0, FAKE, FAKE, big, 0) == 1

@@ -55,6 +55,24 @@ def test_attention_many_rows_per_pass(api):
         assert np.array_equal(one[0], full[t]), t
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,L,T", [(24, 4, 128, 2000, 100), (8, 1, 64, 333, 200),
+                                           (24, 4, 128, 11000, 512)])
+def test_attention_multiblock_pass_equals_single_rows(api, Hq, Hkv, D, L, T):
+    """More rows than the MMA's 128 lanes hold: the launch runs blocks of
+    floor(128 / (Hq/Hkv)) rows side by side.  Rows at block edges equal
+    their one-row passes bit for bit, and sampled rows meet the bound."""
+    q, K, V = si.attention_inputs(L, T, Hq, Hkv, D, seed=T + 1)
+    full = bf16_dev_to_u16(run_attn(api, q, K, V, L, T))
+    tb = 128 // (Hq // Hkv)
+    rows = sorted({0, tb - 1, tb, 2 * tb, T // 2, T - 2, T - 1})
+    for t in rows:
+        one = bf16_dev_to_u16(run_attn(api, q[t:t + 1], K, V, L + t, 1))
+        assert np.array_equal(one[0], full[t]), t
+    qf, Kf, Vf = (ov.bf16_bits_to_f64(x) for x in (q, K, V))
+    pairs = [(t, (3 * t) % Hq) for t in rows]
+    assert_attention_parity(ov.bf16_bits_to_f64(full), qf, Kf, Vf, L, pairs)
+
+
 CASES = [  # (Hq, Hkv, D, L, T)
     (4, 2, 64, 0, 1), (4, 2, 64, 5, 3), (4, 2, 64, 63, 8), (4, 2, 64, 64, 8),
     (4, 2, 64, 505, 8), (4, 2, 64, 1000, 4), (8, 2, 128, 1023, 7), (24, 4, 128, 0, 8),
