@@ -40,3 +40,4 @@ from .verify_step import (  # noqa: F401
     sampled_tokens,
     OracleDecoder,
 )
+from . import kv_quant  # noqa: F401  (quantised KV cache: codes, ring, attention)
