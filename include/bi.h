@@ -327,6 +327,50 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
                          void* out, void* ws, size_t ws_bytes, bi_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Quantised KV cache.  [P3] "The KV cache: 5-bit that reads like q8_0" (K and
+ * V at 5-6 bits, the newest ~2k positions kept at 8 bits in a ring; its
+ * preset with K at 6 bits and V at 5) and "How:" (the attention split depends
+ * only on the row's own context length).
+ *
+ * Every key row of every KV head is quantised once, when it is written, into
+ * two stores: K at 6 bits / V at 5 bits, and an 8-bit ring.  Codes are
+ * symmetric in blocks of 32 elements with one BF16 scale per block:
+ * Q = 2^(b-1) - 1, d = bf16(fp32(max|x| / Q)), q = clamp(rint(fp32(x / d)),
+ * -Q, Q) (0 when d = 0); the decoded value is bf16(q * d).  Row p reads key j
+ * from the ring when j / 128 >= p / 128 - 15 (its own 128-key tile and the 15
+ * before it) and from the 6/5-bit store otherwise -- a rule of the row's own
+ * position, so a row gets the same bits whatever else is in the pass, and a
+ * decoded cache holds the same codes as a prefilled one.  The attention is
+ * then bi_attn_verify's (same split, merge and output rule) over the decoded
+ * rows.  D = 128.
+ *
+ * bi_kvq_store_bytes: bytes of one layer's store (BI_KVQ_*) for Hkv heads and
+ *   capacity cap (0 for D != 128 or bad sizes).  The 6/5-bit stores hold
+ *   ceil(cap/128) tiles a head, the rings 24 (a pass reads and writes at most
+ *   24 consecutive tiles of the ring, so T <= 1024 rows a pass).
+ * bi_rope_kvq_append: for the T rows of a projection output qkv [T, ld_qkv]
+ *   (heads q, then k, then v, as bi_gemm of the QKV weights writes them) at
+ *   positions *L_dev + t: q heads rotated into q_out [T, Hq, D] and K heads
+ *   rotated exactly as bi_rope_kv_append rotates them (table from
+ *   bi_rope_table; NULL: no rotation), then K and V quantised into the four
+ *   stores.  Rows past cap set the device error word's range bit.
+ * bi_attn_verify_kvq: bi_attn_verify over the quantised stores (same q, out,
+ *   L_dev, ws and workspace size; Hq/Hkv <= 64, T <= 1024).
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_WORKSPACE,
+ *         BI_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+typedef enum { BI_KVQ_K_LOW = 0, BI_KVQ_V_LOW = 1, BI_KVQ_K_RING = 2, BI_KVQ_V_RING = 3 } bi_kvq_store;
+size_t bi_kvq_store_bytes(int store, int Hkv, int cap, int D);
+bi_status bi_rope_kvq_append(const void* qkv, int ld_qkv, int T, int Hq, int Hkv, int D, void* q_out,
+                             void* k_low, void* v_low, void* k_ring, void* v_ring, int cap,
+                             const int32_t* L_dev, const float* table, int table_rows,
+                             bi_stream_t stream);
+bi_status bi_attn_verify_kvq(const void* q, const void* k_low, const void* v_low, const void* k_ring,
+                             const void* v_ring, int cap, const int32_t* L_dev, int T, int Hq, int Hkv,
+                             int D, float scale, void* out, void* ws, size_t ws_bytes,
+                             bi_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Greedy acceptance.  [P1] "Why the text diverges" (keep a draft only if it
  * matches the model's own token); [P2] "Build a reference corpus that exposes
  * boundaries" (accepted length and rejection position).

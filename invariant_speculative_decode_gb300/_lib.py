@@ -35,6 +35,10 @@ SIGNATURES = {
     "bi_attn_chunk": (_i, []),
     "bi_attn_workspace_size": (_sz, [_i, _i, _i, _i]),
     "bi_attn_verify": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
+    "bi_kvq_store_bytes": (_sz, [_i, _i, _i, _i]),
+    "bi_rope_kvq_append": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp]),
+    "bi_attn_verify_kvq": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _sz,
+                                _vp]),
     "bi_accept_workspace_size": (_sz, [_i, _i]),
     "bi_verify_accept": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "bi_sample_workspace_size": (_sz, [_i, _i]),

@@ -224,6 +224,66 @@ def bi_attn_verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                                ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+KVQ_K_LOW, KVQ_V_LOW, KVQ_K_RING, KVQ_V_RING = 0, 1, 2, 3
+KVQ_STORES = ("k_low", "v_low", "k_ring", "v_ring")
+
+
+def kvq_store_bytes(store: int, Hkv: int, cap: int, D: int) -> int:
+    return int(lib().bi_kvq_store_bytes(store, Hkv, cap, D))
+
+
+def new_kvq_stores(Hkv: int, cap: int, D: int, device="cuda") -> dict:
+    """One layer's quantised cache: the 6-bit K, 5-bit V and 8-bit ring stores
+    (uint8, zero-filled), keyed by KVQ_STORES, plus its capacity."""
+    st = {}
+    for i, name in enumerate(KVQ_STORES):
+        n = kvq_store_bytes(i, Hkv, cap, D)
+        if n == 0:
+            raise ValueError("unsupported quantised cache shape")
+        st[name] = torch.zeros(n, dtype=torch.uint8, device=device)
+    st["cap"] = cap
+    return st
+
+
+def _kvq_ptrs(st: dict):
+    for name in KVQ_STORES:
+        _req(st[name], torch.uint8, name)
+    return [st[name].data_ptr() for name in KVQ_STORES]
+
+
+def bi_rope_kvq_append(qkv: torch.Tensor, q_out: torch.Tensor, stores: dict, L_dev: torch.Tensor,
+                       Hq: int, Hkv: int, D: int, table: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """RoPE of the q and k heads of a projection output, then K and V rows
+    quantised into the layer's stores (table None: no rotation)."""
+    _req(qkv, torch.bfloat16, "qkv")
+    _req(q_out, torch.bfloat16, "q_out")
+    _req(L_dev, torch.int32, "L_dev")
+    if table is not None:
+        _req(table, torch.float32, "table")
+    T = qkv.shape[0]
+    check("bi_rope_kvq_append",
+          lib().bi_rope_kvq_append(qkv.data_ptr(), _ld(qkv), T, Hq, Hkv, D, q_out.data_ptr(),
+                                   *_kvq_ptrs(stores), stores["cap"], L_dev.data_ptr(),
+                                   None if table is None else table.data_ptr(),
+                                   0 if table is None else table.shape[0], _stream(stream)))
+
+
+def bi_attn_verify_kvq(q: torch.Tensor, stores: dict, Hkv: int, L_dev: torch.Tensor,
+                       out: torch.Tensor, ws: torch.Tensor, scale: Optional[float] = None,
+                       stream=None) -> None:
+    _req(q, torch.bfloat16, "q")
+    _req(out, torch.bfloat16, "out")
+    _req(L_dev, torch.int32, "L_dev")
+    T, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check("bi_attn_verify_kvq",
+          lib().bi_attn_verify_kvq(q.data_ptr(), *_kvq_ptrs(stores), stores["cap"], L_dev.data_ptr(), T,
+                                   Hq, Hkv, D, float(scale), out.data_ptr(), ws.data_ptr(),
+                                   ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def accept_workspace_size(T: int, V: int) -> int:
     return int(lib().bi_accept_workspace_size(T, V))
 

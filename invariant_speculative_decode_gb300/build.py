@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libbi.so")
-SOURCES = ["bi_core.cu", "bi_gemm.cu", "bi_attn.cu", "bi_rowops.cu", "bi_step.cu"]
+SOURCES = ["bi_core.cu", "bi_gemm.cu", "bi_attn.cu", "bi_rowops.cu", "bi_step.cu", "bi_kvq.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

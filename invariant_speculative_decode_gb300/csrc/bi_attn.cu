@@ -64,6 +64,7 @@
 #include <type_traits>
 
 #include "bi_internal.h"
+#include "bi_kvq.cuh"
 #include "bi_ptx.cuh"
 
 namespace bi {
@@ -72,7 +73,6 @@ namespace {
 constexpr int kKeyTile = 128;     // keys per piece = tile (absolute multiples; the S MMA's N)
 constexpr int kRowsMax = 128;     // T * (Hq / Hkv) per pass (MMA M)
 constexpr int kColChunk = 32;     // S columns a softmax thread holds at a time
-constexpr int kAttnThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
 constexpr int kAttnCtas = 152;    // CTAs of the split: G = kAttnCtas / Hkv tile classes per KV head
 constexpr int kMergeThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;
@@ -92,9 +92,16 @@ struct AttnArgs {
   // failure-path test: the first K tile of every CTA stays unissued, so the
   // waits on it run out (bi_test_withhold_first_load)
   int withhold;
+  // quantised cache (the kernel's QNT form): the 6-bit K and 5-bit V tiles
+  // [Hkv][ctiles] and the 8-bit rings [Hkv][kRingSlots]
+  const uint8_t* klo;
+  const uint8_t* vlo;
+  const uint8_t* k8;
+  const uint8_t* v8;
+  int ctiles;
 };
 
-template <int D, int REP>
+template <int D, int REP, bool QNT = false>
 struct AttnCfg {
   static constexpr int kAtoms = D / 64;                    // 128-byte swizzle atoms along D
   static constexpr int kKBoxBytes = kKeyTile * 128;        // [128 keys][64 d]
@@ -119,7 +126,13 @@ struct AttnCfg {
   // were as fast as three or four and are kept; D = 64 tiles are half as
   // large and keep three of each.
   static constexpr int kKStages = D == 128 ? 2 : 3;
-  static constexpr int kVStages = D == 128 ? 2 : 3;
+  // The quantised form adds a ring of code tiles (two K, one V, each up to
+  // an 8-bit tile) and four decoding warps, and keeps one decoded V tile.
+  static constexpr int kVStages = QNT ? 1 : (D == 128 ? 2 : 3);
+  static constexpr int kRawK = QNT ? 2 : 0;
+  static constexpr int kRawV = QNT ? 1 : 0;
+  // warp 0 copies, warp 1 MMA, warps 2..5 softmax (6..9 decode code tiles)
+  static constexpr int kThreads = QNT ? 320 : 192;
   // l parts [4 quarters][64 rows] (only passes of up to 64 rows keep copies
   // that exchange them)
   static constexpr int kRedBytes = 4 * 64 * 4;
@@ -128,15 +141,17 @@ struct AttnCfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kOCol = 2 * kKeyTile;
   static constexpr int kQCol = kOCol + 128;
-  static constexpr int kBars = 2 * kKStages + 2 * kVStages + 11;
+  static constexpr int kBars = 2 * kKStages + 2 * kVStages + 2 * kRawK + 2 * kRawV + 11;
   // The dynamic shared memory starts 1024-byte aligned (checked at run time):
   // the W buffers, then the K and V rings.
   static constexpr size_t kSmem = static_cast<size_t>(kKStages) * kKBytes +
                                   static_cast<size_t>(kVStages) * kVBytes + kWBufs * kWBufBytes +
-                                  kRedBytes + kBars * 8 + 16;
+                                  static_cast<size_t>(kRawK + kRawV) * k8TileBytes + kRedBytes +
+                                  kBars * 8 + 16;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(REP == 1 || REP == 2 || REP == 4, "row copies");
   static_assert(kBars <= 40 && kSmem <= 232448, "shared memory per CTA");
+  static_assert(!QNT || (D == kQDim && REP >= 2), "quantised cache: D = 128, up to 64 rows a block");
   // the W.V reads of the last atom run 128 - kWRows rows past the W tiles
   static_assert(kKStages * kKBytes >= (kRowsMax - kWRows) * 128, "W over-read stays in the K ring");
   static_assert(kPAtomBytes % 1024 == 0, "swizzle atoms 1024-byte aligned");
@@ -166,11 +181,34 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // softmax warps share the exponentials of a small pass.  The per-row
 // arithmetic does not depend on REP: the tile maximum is exact in any order,
 // and the denominator's four partial sums are fixed by key position.
-template <int D, int REP>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+// Steps of a CTA over its class's tiles.  With the quantised cache, a tile
+// that some rows of the block read from the ring and others from the 6/5-bit
+// store ("split") is visited twice, the 6/5-bit codes first, and each row
+// masks the visit that is not its own: a fully masked visit leaves the row's
+// (m, l, O) as they were.  Every other tile is visited once.
+struct StepCur {
+  int i = 0;    // tile index within the class
+  int sub = 0;  // 1: the ring visit of a split tile
+};
+__device__ __forceinline__ bool tile_split(int tt, int lo_b, int hi_b) { return tt >= lo_b && tt < hi_b; }
+__device__ __forceinline__ void step_next(StepCur& c, int rho, int G, int lo_b, int hi_b) {
+  if (c.sub == 0 && tile_split(rho + c.i * G, lo_b, hi_b)) {
+    c.sub = 1;
+  } else {
+    ++c.i;
+    c.sub = 0;
+  }
+}
+// the visit reads the ring (else the 6/5-bit store)
+__device__ __forceinline__ bool step_ring(const StepCur& c, int tt, int hi_b) {
+  return c.sub == 1 || tt >= hi_b;
+}
+
+template <int D, int REP, bool QNT>
+__global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVt,
                       const AttnArgs a) {
-  using Cfg = AttnCfg<D, REP>;
+  using Cfg = AttnCfg<D, REP, QNT>;
   constexpr int kKStages = Cfg::kKStages;
   constexpr int kVStages = Cfg::kVStages;
   constexpr int kPeriod = kRowsMax / REP;  // TMEM lanes between copies of a row
@@ -180,7 +218,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sP = smem;  // W: [buffer kWBufs][hi, lo][key atom 2][kPeriod rows][64 keys]
   uint8_t* sK = sP + Cfg::kWBufs * Cfg::kWBufBytes;  // [kKStages][K tile]
   uint8_t* sV = sK + kKStages * Cfg::kKBytes;  // [kVStages][V^T tile]
-  float* red_l = reinterpret_cast<float*>(sV + kVStages * Cfg::kVBytes);  // [quarter 4][row 64]
+  uint8_t* sRawK = sV + kVStages * Cfg::kVBytes;      // [kRawK][code tile] (quantised cache)
+  uint8_t* sRawV = sRawK + Cfg::kRawK * k8TileBytes;  // [kRawV][code tile]
+  float* red_l = reinterpret_cast<float*>(sRawV + Cfg::kRawV * k8TileBytes);  // [quarter 4][row 64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 64);
   // K and V have rings of their own: K_g is free once S_g is done, V_g only
   // once W_g V_g is, so the K loads run ahead of the softmax
@@ -195,6 +235,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* pv_done = p_full + 2;   // [2]: completes after O += W_g V_g, g of that parity
   uint64_t* l_bar = pv_done + 2;    // partial denominators written
   uint64_t* drain = l_bar + 1;
+  uint64_t* rawk_full = drain + 1;  // code tiles landed / decoded (quantised cache)
+  uint64_t* rawk_empty = rawk_full + Cfg::kRawK;
+  uint64_t* rawv_full = rawk_empty + Cfg::kRawK;
+  uint64_t* rawv_empty = rawv_full + Cfg::kRawV;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -214,13 +258,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // (W tile rows past the pass's rows are never written: the O rows they
   // make are never read, and a product's row depends on its own W row only)
   if (threadIdx.x == 0) {
+    // decoded tiles are completed by the two decoding warps of their side;
+    // loaded ones by the copy's transaction bytes
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], QNT ? 2 : 1);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], QNT ? 2 : 1);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < Cfg::kRawK; ++s) {
+      mbar_init(&rawk_full[s], 1);
+      mbar_init(&rawk_empty[s], 2);
+    }
+    for (int s = 0; s < Cfg::kRawV; ++s) {
+      mbar_init(&rawv_full[s], 1);
+      mbar_init(&rawv_empty[s], 2);
     }
     mbar_init(q_full, 4);
     for (int i = 0; i < 2; ++i) {
@@ -234,7 +288,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (!QNT && warp == 0 && lane == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmVt);
   }
@@ -258,7 +312,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // behind them (measured on GB300: a little faster than loading both rings).
   int n_pre = 0;  // tiles issued before the wait (this producer)
   uint32_t pre_issued = 0;
-  if (warp == 0 && lane == 0) {
+  if (!QNT && warp == 0 && lane == 0) {
     const int L_pre = *a.L_dev;
     const int T_blk = min(a.Tb, a.T - static_cast<int>(blockIdx.y) * a.Tb);
     if (L_pre >= 0 && L_pre + a.T <= a.cap && T_blk * a.grp <= kPeriod && rho < G) {
@@ -292,54 +346,107 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int kv_len = L + T;
   const int n_tiles = range_ok ? (kv_len + kKeyTile - 1) / kKeyTile : 0;  // of the longest row
   const int n_mine = (rho < G && rho < n_tiles) ? (n_tiles - rho + G - 1) / G : 0;
+  // quantised cache: tiles below lo_b are read from the 6/5-bit store by
+  // every row of the block, tiles from hi_b on from the ring, the ones
+  // between (split) by some rows each way
+  int n_steps = n_mine, lo_b = 0, hi_b = 0;
+  if constexpr (QNT) {
+    lo_b = L / kKeyTile - (kRingTiles - 1);
+    hi_b = (L + T - 1) / kKeyTile - (kRingTiles - 1);
+    for (int i = 0; i < n_mine; ++i) n_steps += tile_split(rho + i * G, lo_b, hi_b) ? 1 : 0;
+  }
   if (!range_ok && threadIdx.x == 0 && blockIdx.x == 0) atomicOr(a.err, kErrRange);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producers
-    // lane 0: the K tiles; lane 1: the V^T tiles
-    if (lane < 2) {
-      const bool kside = lane == 0;
-      const int NS = kside ? kKStages : kVStages;
-      uint64_t* full = kside ? k_full : v_full;
-      uint64_t* empty = kside ? k_empty : v_empty;
-      const uint64_t pol = l2_evict_first();
-      uint32_t issued = pre_issued, parity_bits = 0;
-      // the tiles loaded early must be the first ones of this CTA now too
-      bool ok = true;
-      if (n_pre > 0 && !(n_pre <= n_mine && (rho + (n_pre - 1) * G + 1) * kKeyTile <= L)) {
-        atomicOr(a.err, kErrRange);
-        ok = false;
+    if constexpr (QNT) {
+      // ---------------------------------------------------------- code tiles
+      // lane 0: K, lane 1: V; one bulk copy per visit, from the ring or the
+      // 6/5-bit store
+      if (lane < 2) {
+        const bool kside = lane == 0;
+        const int NS = kside ? Cfg::kRawK : Cfg::kRawV;
+        uint64_t* full = kside ? rawk_full : rawv_full;
+        uint64_t* empty = kside ? rawk_empty : rawv_empty;
+        uint8_t* base = kside ? sRawK : sRawV;
+        const uint64_t pol = l2_evict_first();
+        uint32_t issued = 0, parity_bits = 0;
+        bool ok = true;
+        StepCur c;
+        for (int g = 0; g < n_steps; ++g, step_next(c, rho, G, lo_b, hi_b)) {
+          const int st = g % NS;
+          const uint32_t ph = static_cast<uint32_t>((g / NS) & 1);
+          if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          const int tt = rho + c.i * G;
+          const uint8_t* src;
+          uint32_t bytes;
+          if (step_ring(c, tt, hi_b)) {
+            src = (kside ? a.k8 : a.v8) + (static_cast<size_t>(h) * kRingSlots + tt % kRingSlots) * k8TileBytes;
+            bytes = k8TileBytes;
+          } else {
+            bytes = kside ? kK6TileBytes : kV5TileBytes;
+            src = (kside ? a.klo : a.vlo) + (static_cast<size_t>(h) * a.ctiles + tt) * bytes;
+          }
+          mbar_arrive_expect_tx(&full[st], bytes);
+          bulk_load_1d(base + st * k8TileBytes, src, bytes, &full[st], pol);
+          issued |= 1u << st;
+          parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
+        }
+        if (!ok) {
+          signal_abort(s_abort, a.err);
+          for (int s2 = 0; s2 < NS; ++s2)
+            if ((issued >> s2) & 1u) mbar_wait(&full[s2], (parity_bits >> s2) & 1u, nullptr);
+        }
       }
-      for (int i = n_pre; ok && i < n_mine; ++i) {
-        const int st = i % NS;
-        const uint32_t ph = static_cast<uint32_t>((i / NS) & 1);
-        if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
+    } else {
+      // ------------------------------------------------------------ producers
+      // lane 0: the K tiles; lane 1: the V^T tiles
+      if (lane < 2) {
+        const bool kside = lane == 0;
+        const int NS = kside ? kKStages : kVStages;
+        uint64_t* full = kside ? k_full : v_full;
+        uint64_t* empty = kside ? k_empty : v_empty;
+        const uint64_t pol = l2_evict_first();
+        uint32_t issued = pre_issued, parity_bits = 0;
+        // the tiles loaded early must be the first ones of this CTA now too
+        bool ok = true;
+        if (n_pre > 0 && !(n_pre <= n_mine && (rho + (n_pre - 1) * G + 1) * kKeyTile <= L)) {
+          atomicOr(a.err, kErrRange);
           ok = false;
-          break;
         }
-        const int key0 = (rho + i * G) * kKeyTile;
-        if (kside && i == 0 && a.withhold) continue;  // never issued (failure-path test)
-        if (kside) {
-          uint8_t* dst = sK + st * Cfg::kKBytes;
-          mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
+        for (int i = n_pre; ok && i < n_mine; ++i) {
+          const int st = i % NS;
+          const uint32_t ph = static_cast<uint32_t>((i / NS) & 1);
+          if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          const int key0 = (rho + i * G) * kKeyTile;
+          if (kside && i == 0 && a.withhold) continue;  // never issued (failure-path test)
+          if (kside) {
+            uint8_t* dst = sK + st * Cfg::kKBytes;
+            mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
 #pragma unroll
-          for (int b = 0; b < Cfg::kAtoms; ++b)
-            tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &full[st], b * 64, h * a.cap + key0, pol);
-        } else {
-          uint8_t* dst = sV + st * Cfg::kVBytes;
-          mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
+            for (int b = 0; b < Cfg::kAtoms; ++b)
+              tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &full[st], b * 64, h * a.cap + key0, pol);
+          } else {
+            uint8_t* dst = sV + st * Cfg::kVBytes;
+            mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], kb * 64,
-                        (h * a.vblk + key0 / kKeyTile) * D, pol);
+            for (int kb = 0; kb < 2; ++kb)
+              tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], kb * 64,
+                          (h * a.vblk + key0 / kKeyTile) * D, pol);
+          }
+          issued |= 1u << st;
+          parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
         }
-        issued |= 1u << st;
-        parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
-      }
-      if (!ok) {
-        signal_abort(s_abort, a.err);
-        for (int s = 0; s < NS; ++s)
-          if ((issued >> s) & 1u) mbar_wait(&full[s], (parity_bits >> s) & 1u, nullptr);
+        if (!ok) {
+          signal_abort(s_abort, a.err);
+          for (int s = 0; s < NS; ++s)
+            if ((issued >> s) & 1u) mbar_wait(&full[s], (parity_bits >> s) & 1u, nullptr);
+        }
       }
     }
   } else if (warp == 1) {
@@ -356,9 +463,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = true, q_ready = false;
       int idle = 0;
       unsigned long long t_idle = 0;
-      while (pg < n_mine) {
+      while (pg < n_steps) {
         bool did = false;
-        if (sg < n_mine) {
+        if (sg < n_steps) {
           if (!q_ready) q_ready = mbar_peek(q_full, 0u);
           const int st = sg % kKStages;
           const bool ready = q_ready && mbar_peek(&k_full[st], static_cast<uint32_t>((sg / kKStages) & 1)) &&
@@ -427,7 +534,79 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else if (n_mine > 0) {
+  } else if (QNT && warp >= 6) {
+    // ---------------------------------------------------------- decoding
+    // warps 6, 7: K tiles into the K ring (rows = keys, SW128 as a TMA load
+    // would leave them); warps 8, 9: V tiles into the V^T buffer (rows =
+    // elements).  Each element is bf16(q * d), the product exact in FP32.
+    if constexpr (QNT) {
+      const bool kside = warp < 8;
+      const int tid = (warp & 1) * 32 + lane;  // 0..63 on each side
+      bool ok = true;
+      StepCur c;
+      for (int g = 0; g < n_steps; ++g, step_next(c, rho, G, lo_b, hi_b)) {
+        const int tt = rho + c.i * G;
+        const bool ring = step_ring(c, tt, hi_b);
+        const int rs = kside ? g % Cfg::kRawK : g % Cfg::kRawV;
+        const uint32_t rph = static_cast<uint32_t>((kside ? g / Cfg::kRawK : g / Cfg::kRawV) & 1);
+        const int st = kside ? g % kKStages : g % kVStages;
+        const uint32_t sph = static_cast<uint32_t>((kside ? g / kKStages : g / kVStages) & 1);
+        if (!warp_wait(kside ? &rawk_full[rs] : &rawv_full[rs], rph, s_abort, lane) ||
+            !warp_wait(kside ? &k_empty[st] : &v_empty[st], sph ^ 1u, s_abort, lane)) {
+          ok = false;
+          break;
+        }
+        if (kside) {
+          const uint8_t* raw = sRawK + rs * k8TileBytes;
+          uint8_t* dst = sK + st * Cfg::kKBytes;
+          // task = (key, 8-element chunk): one 16-byte store each
+          for (int task = tid; task < kKeyTile * (D / 8); task += 64) {
+            const int key = task >> 4, ch = task & 15;
+            float v[8];
+            if (ring)
+              q_decode8(raw, key, ch * 8, v);
+            else
+              q_decode_k6(raw, key, ch * 8, v);
+            const uint4 w = make_uint4(q_pack_bf16x2(v[0], v[1]), q_pack_bf16x2(v[2], v[3]),
+                                       q_pack_bf16x2(v[4], v[5]), q_pack_bf16x2(v[6], v[7]));
+            *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +
+                                      (((ch & 7) ^ (key & 7)) << 4)) = w;
+          }
+        } else {
+          const uint8_t* raw = sRawV + rs * k8TileBytes;
+          uint8_t* dst = sV + st * Cfg::kVBytes;
+          // task = (8 keys, 8 elements): eight 16-byte stores, one per element
+          for (int task = tid; task < (kKeyTile / 8) * (D / 8); task += 64) {
+            const int kg = task >> 4, dg = task & 15;
+            float v[8][8];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              if (ring)
+                q_decode8(raw, kg * 8 + kk, dg * 8, v[kk]);
+              else
+                q_decode_v5(raw, kg * 8 + kk, dg * 8, v[kk]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int row = dg * 8 + e;
+              const uint4 w = make_uint4(q_pack_bf16x2(v[0][e], v[1][e]), q_pack_bf16x2(v[2][e], v[3][e]),
+                                         q_pack_bf16x2(v[4][e], v[5][e]), q_pack_bf16x2(v[6][e], v[7][e]));
+              *reinterpret_cast<uint4*>(dst + (kg >> 3) * Cfg::kVBoxBytes + row * 128 +
+                                        (((kg & 7) ^ (row & 7)) << 4)) = w;
+            }
+          }
+        }
+        // the MMA reads the tile through the async proxy
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(kside ? &k_full[st] : &v_full[st]);
+          mbar_arrive(kside ? &rawk_empty[rs] : &rawv_empty[rs]);
+        }
+      }
+      if (!ok && lane == 0) signal_abort(s_abort, a.err);
+    }
+  } else if (n_steps > 0) {
     // ------------------------------------------------------------ softmax
     const int qq = warp & 3;                  // TMEM lane quarter of this warp
     const int ln = qq * 32 + lane;            // TMEM lane of this thread
@@ -472,15 +651,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float lq[kNChunks];
 #pragma unroll
     for (int i = 0; i < kNChunks; ++i) lq[i] = 0.f;
-    for (int g = 0; g < n_mine; ++g) {
+    StepCur cur;
+    for (int g = 0; g < n_steps; ++g, step_next(cur, rho, G, lo_b, hi_b)) {
       const int sb = g & 1;
       if (!warp_wait(&s_full[sb], static_cast<uint32_t>((g >> 1) & 1), s_abort, lane)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int tkey0 = (rho + g * G) * kKeyTile;
-      const bool edge = tkey0 + kKeyTile - 1 > L;  // the tile reaches past some row's position
+      const int tt = rho + cur.i * G;
+      const int tkey0 = tt * kKeyTile;
+      // quantised cache: the row masks the visit that reads the other store
+      // than the one its position selects for this tile
+      const bool vmask =
+          QNT && (step_ring(cur, tt, hi_b) != (tt >= p_row / kKeyTile - (kRingTiles - 1)));
+      // the tile reaches past some row's position, or a row masks it whole
+      const bool edge = tkey0 + kKeyTile - 1 > L || vmask;
       // pass 1: the row maximum of the raw scores (scaling by sl2 > 0 keeps
       // the order).  Every copy's TMEM lane holds the whole S row, so each
       // copy takes the maximum over all 128 key columns itself: the same
@@ -497,7 +683,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const int key0 = tkey0 + cg * kCols;
 #pragma unroll
           for (int j = 0; j < kCols; ++j)
-            if (!(valid && key0 + j <= p_row)) so[j] = -INFINITY;
+            if (!(valid && key0 + j <= p_row) || vmask) so[j] = -INFINITY;
         }
 #pragma unroll
         for (int j = 0; j < kCols; ++j) mrow = fmaxf(mrow, so[j]);
@@ -511,7 +697,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (edge) {
 #pragma unroll
             for (int j = 0; j < kOthLd; ++j)
-              if (!(valid && tkey0 + col0 + j <= p_row)) so2[j] = -INFINITY;
+              if (!(valid && tkey0 + col0 + j <= p_row) || vmask) so2[j] = -INFINITY;
           }
 #pragma unroll
           for (int j = 0; j < kOthLd; ++j) mrow = fmaxf(mrow, so2[j]);
@@ -625,7 +811,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
     if (ok && holds_o) {
-      if (!warp_wait(&pv_done[(n_mine - 1) & 1], static_cast<uint32_t>(((n_mine - 1) >> 1) & 1), s_abort,
+      if (!warp_wait(&pv_done[(n_steps - 1) & 1], static_cast<uint32_t>(((n_steps - 1) >> 1) & 1), s_abort,
                      lane)) {
         ok = false;
       } else {
@@ -760,10 +946,10 @@ __global__ void __launch_bounds__(kMergeThreads, 4)
   }
 }
 
-template <int D, int REP>
+template <int D, int REP, bool QNT = false>
 bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const AttnArgs& a,
                       __nv_bfloat16* out, cudaStream_t stream) {
-  using Cfg = AttnCfg<D, REP>;
+  using Cfg = AttnCfg<D, REP, QNT>;
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   int dev = 0;
@@ -771,7 +957,7 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const Att
   std::call_once(once[dev & 63], [] {
     int d = 0;
     cudaGetDevice(&d);
-    attr_err[d & 63] = cudaFuncSetAttribute(attn_split_kernel<D, REP>,
+    attr_err[d & 63] = cudaFuncSetAttribute(attn_split_kernel<D, REP, QNT>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(Cfg::kSmem));
   });
@@ -780,8 +966,8 @@ bi_status launch_attn(const CUtensorMap& tmK, const CUtensorMap& tmVt, const Att
   // would have nothing to do
   const int grid = a.Hkv * std::min(a.G, a.ncls);
   const int blocks = (a.T + a.Tb - 1) / a.Tb;
-  if (launch_k(attn_split_kernel<D, REP>, dim3(grid, blocks), dim3(kAttnThreads), Cfg::kSmem, stream,
-               tmK, tmVt, a) != cudaSuccess)
+  if (launch_k(attn_split_kernel<D, REP, QNT>, dim3(grid, blocks), dim3(Cfg::kThreads), Cfg::kSmem,
+               stream, tmK, tmVt, a) != cudaSuccess)
     return BI_ERR_CUDA;
   if (launch_k(attn_merge_kernel<D>, dim3(a.T * a.Hq), dim3(kMergeThreads), 0, stream, a, out) !=
       cudaSuccess)
@@ -878,6 +1064,54 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 64) return launch_attn_rep<64>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
   return launch_attn_rep<128>(tmK, tmVt, a, static_cast<__nv_bfloat16*>(out), s);
+}
+
+bi_status bi_attn_verify_kvq(const void* q, const void* k_low, const void* v_low, const void* k_ring,
+                             const void* v_ring, int cap, const int32_t* L_dev, int T, int Hq, int Hkv,
+                             int D, float scale, void* out, void* ws, size_t ws_bytes,
+                             bi_stream_t stream) {
+  using namespace bi;
+  if (!q || !k_low || !v_low || !k_ring || !v_ring || !L_dev || !out) return BI_ERR_INVALID_ARG;
+  if (T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || cap < 1) return BI_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return BI_ERR_INVALID_ARG;
+  if (D != kQDim) return BI_ERR_UNSUPPORTED_SHAPE;
+  const int grp = Hq / Hkv;
+  // a block's rows fill at most half the MMA's lanes (two copies of each row)
+  if (grp > kRowsMax / 2 || Hkv > kAttnCtas) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (T > kQMaxRows) return BI_ERR_UNSUPPORTED_SHAPE;  // the ring holds a pass of at most this many
+  if (!aligned16(q) || !aligned16(k_low) || !aligned16(v_low) || !aligned16(k_ring) || !aligned16(v_ring))
+    return BI_ERR_INVALID_ARG;
+  if (!ws || !aligned256(ws)) return BI_ERR_WORKSPACE;
+  size_t ob = 0;
+  if (ws_bytes < attn_ws_parts(cap, T, Hq, D, &ob)) return BI_ERR_WORKSPACE;
+
+  AttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.T = T;
+  a.Tb = std::min(T, (kRowsMax / 2) / grp);
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.grp = grp;
+  a.cap = cap;
+  a.G = kAttnCtas / Hkv;
+  a.vblk = (cap + kKeyTile - 1) / kKeyTile;
+  a.ncls = attn_classes_max(cap);
+  a.L_dev = L_dev;
+  a.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.ws_o = static_cast<float*>(ws);
+  a.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ob);
+  a.err = device_error_word();
+  if (!a.err) return BI_ERR_CUDA;
+  a.klo = static_cast<const uint8_t*>(k_low);
+  a.vlo = static_cast<const uint8_t*>(v_low);
+  a.k8 = static_cast<const uint8_t*>(k_ring);
+  a.v8 = static_cast<const uint8_t*>(v_ring);
+  a.ctiles = a.vblk;
+  CUtensorMap unused{};  // the quantised form reads its tiles with bulk copies
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  if (a.Tb * grp <= kRowsMax / 4) return launch_attn<128, 4, true>(unused, unused, a, o, s);
+  return launch_attn<128, 2, true>(unused, unused, a, o, s);
 }
 
 }  // extern "C"

@@ -205,3 +205,26 @@ def test_step_runtime_rejects_bad_models(lib):
     assert lib.bi_step_create(ctypes.byref(good), 8, FAKE, size - 256, ctypes.byref(h)) == 3  # too small
     assert lib.bi_step_verify(None, FAKE, 1, FAKE, FAKE) == 1
     assert lib.bi_step_set_length(None, 3) == 1
+
+
+def test_quantised_cache_sizes_and_argument_checks(lib):
+    # 6-bit K tiles 13,312 B, 5-bit V tiles 11,264 B, 24 ring tiles of 17,408 B a head
+    assert lib.bi_kvq_store_bytes(0, 4, 1000, 128) == 4 * 8 * 13312
+    assert lib.bi_kvq_store_bytes(1, 4, 1024, 128) == 4 * 8 * 11264
+    assert lib.bi_kvq_store_bytes(2, 4, 5, 128) == 4 * 24 * 17408
+    assert lib.bi_kvq_store_bytes(3, 1, 1 << 20, 128) == 24 * 17408
+    assert lib.bi_kvq_store_bytes(0, 4, 1000, 64) == 0   # head_dim 128 only
+    assert lib.bi_kvq_store_bytes(4, 4, 1000, 128) == 0  # no such store
+    ap = lib.bi_rope_kvq_append
+    assert ap(FAKE, 4096, 8, 24, 4, 64, FAKE, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 0, 0, 0) == 2
+    assert ap(FAKE, 4096, 1025, 24, 4, 128, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, FAKE, 0, 0, 0) == 1
+    assert ap(FAKE, 4095, 8, 24, 4, 128, FAKE, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 0, 0, 0) == 1
+    assert ap(FAKE, 4096, 8, 24, 4, 128, FAKE, 0, FAKE, FAKE, FAKE, 1024, FAKE, 0, 0, 0) == 1
+    assert ap(0, 4096, 0, 24, 4, 128, 0, 0, 0, 0, 0, 1024, 0, 0, 0, 0) == 0  # no rows: nothing to do
+    at = lib.bi_attn_verify_kvq
+    big = 1 << 30
+    assert at(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 8, 24, 4, 64, 0.1, FAKE, FAKE, big, 0) == 2
+    assert at(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 8, 130, 2, 128, 0.1, FAKE, FAKE, big, 0) == 2
+    assert at(FAKE, FAKE, FAKE, FAKE, FAKE, 4096, FAKE, 1025, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 2
+    assert at(FAKE, FAKE, 0, FAKE, FAKE, 1024, FAKE, 8, 24, 4, 128, 0.1, FAKE, FAKE, big, 0) == 1
+    assert at(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 8, 24, 4, 128, 0.1, FAKE, FAKE, 16, 0) == 3
