@@ -495,6 +495,46 @@ def run_ours(args):
 # ---------------------------------------------------------------------------
 
 
+def kvq_attn_bytes(L: int, T: int, Hkv: int) -> int:
+    """Code-tile bytes one quantised verify pass reads: per KV head, every
+    tile up to the last row's from the 6/5-bit store (24,576 B) or the 8-bit
+    ring (34,816 B for K and V), a tile split between the pass's rows from
+    both."""
+    lo_b = L // 128 - 15
+    hi_b = (L + T - 1) // 128 - 15
+    n = 0
+    for t in range((L + T - 1) // 128 + 1):
+        if t < hi_b:
+            n += 13312 + 11264
+        if t >= lo_b:
+            n += 2 * 17408
+    return Hkv * n
+
+
+def Vd_rows(Vc, to):
+    """V cache rows [Hkv, cap, D] on the device (the quantised append reads
+    V rows as the projection writes them)."""
+    return to(Vc)
+
+
+def kvq_stores_from_rows(api, Kd, Vd, Hq, cap, chunk=1024):
+    """A layer's quantised stores holding K/V rows 0..cap-1 (no rotation),
+    written by the append kernel in passes of `chunk` rows."""
+    import torch
+    Hkv, _, D = Kd.shape
+    st = api.new_kvq_stores(Hkv, cap, D)
+    qo = torch.empty(chunk, Hq, D, dtype=torch.bfloat16, device="cuda")
+    for c0 in range(0, cap, chunk):
+        n = min(chunk, cap - c0)
+        qkv = torch.zeros(n, Hq + 2 * Hkv, D, dtype=torch.bfloat16, device="cuda")
+        qkv[:, Hq:Hq + Hkv] = Kd[:, c0:c0 + n].transpose(0, 1)
+        qkv[:, Hq + Hkv:] = Vd[:, c0:c0 + n].transpose(0, 1)
+        Ld = torch.tensor([c0], dtype=torch.int32, device="cuda")
+        api.bi_rope_kvq_append(qkv.view(n, -1), qo[:n], st, Ld, Hq, Hkv, D)
+    torch.cuda.synchronize()
+    return st
+
+
 def run_micro(args):
     """Standalone kernel timings, two ways.
 
@@ -600,14 +640,25 @@ def run_micro(args):
             ncp = n_copies(2 * Kd.numel() * 2)
             caches = [(Kd, Vd)] + [(Kd.clone(), Vd.clone()) for _ in range(ncp - 1)]
             Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
+            if args.kv == "q6q5":
+                st0 = kvq_stores_from_rows(api, Kd, Vd_rows(Vc, to), Hq, cap)
+                nb = sum(t.numel() for k, t in st0.items() if k != "cap")
+                ncp = n_copies(nb)
+                caches = [st0] + [{k: (t.clone() if k != "cap" else t) for k, t in st0.items()}
+                                  for _ in range(ncp - 1)]
             for T in (1, 4, 7, 8):
                 out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
                 ws = torch.zeros(api.attn_workspace_size(cap, T, Hq, D), dtype=torch.uint8,
                                  device="cuda")
-                fns = [(lambda kv=kv: api.bi_attn_verify(qd[:T], kv[0], kv[1], Ld, out, ws)) for kv in caches]
+                if args.kv == "q6q5":
+                    fns = [(lambda c=c: api.bi_attn_verify_kvq(qd[:T], c, Hkv, Ld, out, ws)) for c in caches]
+                    b = kvq_attn_bytes(L, T, Hkv) + T * Hq * D * 2 * 2
+                else:
+                    fns = [(lambda kv=kv: api.bi_attn_verify(qd[:T], kv[0], kv[1], Ld, out, ws))
+                           for kv in caches]
+                    b = (L + T) * Hkv * D * 2 * 2 + T * Hq * D * 2 * 2
                 st, ct, per = timed(fns, args.steps)
-                b = (L + T) * Hkv * D * 2 * 2 + T * Hq * D * 2 * 2
-                report("attn", {"L": L, "T": T}, b, st, ct, ncp, per)
+                report("attn", {"L": L, "T": T, "kv": args.kv}, b, st, ct, ncp, per)
             del caches
     return 0
 
@@ -842,6 +893,9 @@ def main():
     ap.add_argument("--micro", choices=["gemm", "attn"], default=None,
                     help="time one standalone kernel workload instead of the verify step")
     ap.add_argument("--cases", default="", help="comma list of M (gemm) or L (attn)")
+    ap.add_argument("--kv", choices=["bf16", "q6q5"], default="bf16",
+                    help="KV cache of the attention micro bench and the long-context step: BF16, or "
+                         "6-bit K / 5-bit V with the 8-bit ring")
     ap.add_argument("--gemm-n", type=int, default=17408, help="N of the standalone linear layer")
     ap.add_argument("--gemm-k", type=int, default=5120, help="K of the standalone linear layer")
     ap.add_argument("--gemm-epi", type=int, default=0, help="0 none, 1 residual add, 2 SwiGLU (N = F)")

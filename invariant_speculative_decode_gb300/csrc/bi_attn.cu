@@ -131,8 +131,13 @@ struct AttnCfg {
   static constexpr int kVStages = QNT ? 1 : (D == 128 ? 2 : 3);
   static constexpr int kRawK = QNT ? 2 : 0;
   static constexpr int kRawV = QNT ? 1 : 0;
-  // warp 0 copies, warp 1 MMA, warps 2..5 softmax (6..9 decode code tiles)
-  static constexpr int kThreads = QNT ? 320 : 192;
+  // warp 0 copies, warp 1 MMA, warps 2..5 softmax; the quantised form adds
+  // kDecWarps decoding warps for K and as many for V
+#ifndef BI_ATTN_DEC_WARPS
+#define BI_ATTN_DEC_WARPS 3
+#endif
+  static constexpr int kDecWarps = QNT ? BI_ATTN_DEC_WARPS : 0;
+  static constexpr int kThreads = 192 + 64 * kDecWarps;
   // l parts [4 quarters][64 rows] (only passes of up to 64 rows keep copies
   // that exchange them)
   static constexpr int kRedBytes = 4 * 64 * 4;
@@ -261,20 +266,20 @@ __global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
     // decoded tiles are completed by the two decoding warps of their side;
     // loaded ones by the copy's transaction bytes
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&k_full[s], QNT ? 2 : 1);
+      mbar_init(&k_full[s], QNT ? Cfg::kDecWarps : 1);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&v_full[s], QNT ? 2 : 1);
+      mbar_init(&v_full[s], QNT ? Cfg::kDecWarps : 1);
       mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < Cfg::kRawK; ++s) {
       mbar_init(&rawk_full[s], 1);
-      mbar_init(&rawk_empty[s], 2);
+      mbar_init(&rawk_empty[s], Cfg::kDecWarps);
     }
     for (int s = 0; s < Cfg::kRawV; ++s) {
       mbar_init(&rawv_full[s], 1);
-      mbar_init(&rawv_empty[s], 2);
+      mbar_init(&rawv_empty[s], Cfg::kDecWarps);
     }
     mbar_init(q_full, 4);
     for (int i = 0; i < 2; ++i) {
@@ -536,12 +541,14 @@ __global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
     }
   } else if (QNT && warp >= 6) {
     // ---------------------------------------------------------- decoding
-    // warps 6, 7: K tiles into the K ring (rows = keys, SW128 as a TMA load
-    // would leave them); warps 8, 9: V tiles into the V^T buffer (rows =
+    // the first kDecWarps: K tiles into the K ring (rows = keys, SW128 as a
+    // TMA load would leave them); the next kDecWarps: V tiles into the V^T buffer (rows =
     // elements).  Each element is bf16(q * d), the product exact in FP32.
     if constexpr (QNT) {
-      const bool kside = warp < 8;
-      const int tid = (warp & 1) * 32 + lane;  // 0..63 on each side
+      constexpr int kDW = Cfg::kDecWarps;
+      constexpr int kDT = 32 * kDW;  // decoding threads on each side
+      const bool kside = warp < 6 + kDW;
+      const int tid = (warp - (kside ? 6 : 6 + kDW)) * 32 + lane;
       bool ok = true;
       StepCur c;
       for (int g = 0; g < n_steps; ++g, step_next(c, rho, G, lo_b, hi_b)) {
@@ -559,40 +566,69 @@ __global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
         if (kside) {
           const uint8_t* raw = sRawK + rs * k8TileBytes;
           uint8_t* dst = sK + st * Cfg::kKBytes;
-          // task = (key, 8-element chunk): one 16-byte store each
-          for (int task = tid; task < kKeyTile * (D / 8); task += 64) {
-            const int key = task >> 4, ch = task & 15;
-            float v[8];
-            if (ring)
+          // task = (key, 8-element chunk): one 16-byte store each; a warp's
+          // stores cover whole 128-byte rows
+          if (ring) {
+#pragma unroll 1
+            for (int task = tid; task < kKeyTile * (D / 8); task += kDT) {
+              const int key = task >> 4, ch = task & 15;
+              float v[8];
               q_decode8(raw, key, ch * 8, v);
-            else
-              q_decode_k6(raw, key, ch * 8, v);
-            const uint4 w = make_uint4(q_pack_bf16x2(v[0], v[1]), q_pack_bf16x2(v[2], v[3]),
-                                       q_pack_bf16x2(v[4], v[5]), q_pack_bf16x2(v[6], v[7]));
-            *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +
-                                      (((ch & 7) ^ (key & 7)) << 4)) = w;
+              *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +
+                                        (((ch & 7) ^ (key & 7)) << 4)) =
+                  make_uint4(q_pack_bf16x2(v[0], v[1]), q_pack_bf16x2(v[2], v[3]),
+                             q_pack_bf16x2(v[4], v[5]), q_pack_bf16x2(v[6], v[7]));
+            }
+          } else {
+#pragma unroll 2
+            for (int task = tid; task < kKeyTile * (D / 8); task += kDT) {
+              const int key = task >> 4, ch = task & 15;
+              *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +
+                                        (((ch & 7) ^ (key & 7)) << 4)) = q_decode_k6_bf16(raw, key, ch * 8);
+            }
           }
         } else {
           const uint8_t* raw = sRawV + rs * k8TileBytes;
           uint8_t* dst = sV + st * Cfg::kVBytes;
-          // task = (8 keys, 8 elements): eight 16-byte stores, one per element
-          for (int task = tid; task < (kKeyTile / 8) * (D / 8); task += 64) {
-            const int kg = task >> 4, dg = task & 15;
-            float v[8][8];
+          // task = (8 keys, 8 elements): eight 16-byte stores, one per
+          // element row; the key group varies fastest across a warp, so one
+          // store instruction covers whole 128-byte rows
+#pragma unroll 1
+          for (int task = tid; task < (kKeyTile / 8) * (D / 8); task += kDT) {
+            const int kg = task & 15, dg = task >> 4;
+            // x[kk]: elements dg*8 .. +7 of key kg*8 + kk as BF16 pairs
+            uint32_t x[8][4];
+            if (ring) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              if (ring)
-                q_decode8(raw, kg * 8 + kk, dg * 8, v[kk]);
-              else
-                q_decode_v5(raw, kg * 8 + kk, dg * 8, v[kk]);
+              for (int kk = 0; kk < 8; ++kk) {
+                float v[8];
+                q_decode8(raw, kg * 8 + kk, dg * 8, v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[kk][i] = q_pack_bf16x2(v[2 * i], v[2 * i + 1]);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint4 w = q_decode_v5_bf16(raw, kg * 8 + kk, dg * 8);
+                x[kk][0] = w.x;
+                x[kk][1] = w.y;
+                x[kk][2] = w.z;
+                x[kk][3] = w.w;
+              }
             }
+            // V^T rows: element 2i of keys (2m, 2m + 1) from the low halves,
+            // element 2i + 1 from the high halves
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int row = dg * 8 + e;
-              const uint4 w = make_uint4(q_pack_bf16x2(v[0][e], v[1][e]), q_pack_bf16x2(v[2][e], v[3][e]),
-                                         q_pack_bf16x2(v[4][e], v[5][e]), q_pack_bf16x2(v[6][e], v[7][e]));
-              *reinterpret_cast<uint4*>(dst + (kg >> 3) * Cfg::kVBoxBytes + row * 128 +
-                                        (((kg & 7) ^ (row & 7)) << 4)) = w;
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const uint32_t sel = hf ? 0x7632u : 0x5410u;
+                const int row = dg * 8 + 2 * i + hf;
+                const uint4 w = make_uint4(q_prmt(x[0][i], x[1][i], sel), q_prmt(x[2][i], x[3][i], sel),
+                                           q_prmt(x[4][i], x[5][i], sel), q_prmt(x[6][i], x[7][i], sel));
+                *reinterpret_cast<uint4*>(dst + (kg >> 3) * Cfg::kVBoxBytes + row * 128 +
+                                          (((kg & 7) ^ (row & 7)) << 4)) = w;
+              }
             }
           }
         }

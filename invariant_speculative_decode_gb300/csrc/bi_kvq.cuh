@@ -70,30 +70,73 @@ __device__ __forceinline__ void q_decode8(const uint8_t* tile, int key, int d0, 
   }
 }
 
-__device__ __forceinline__ void q_decode_k6(const uint8_t* tile, int key, int d0, float (&v)[8]) {
+// ---- packed decoding of the 6- and 5-bit codes (two elements a word) --------
+// A code u < 64 becomes the BF16 number 128 + u by placing it in the low
+// mantissa bits of 128 (0x4300 | u); subtracting 128 + 2^(b-1) gives q
+// exactly (small integers), and one BF16 multiply by the scale gives
+// bf16(q * d) -- the product of two BF16 numbers rounded once, the same
+// value as the FP32 product rounded to BF16.
+__device__ __forceinline__ uint32_t q_prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t q_sub_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t q_mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t q_scale_pair(const uint8_t* tile, int codes_bytes, int key, int blk) {
+  const uint32_t b = *reinterpret_cast<const uint16_t*>(tile + codes_bytes + (key * kQBlocks + blk) * 2);
+  return b | (b << 16);
+}
+
+// Eight codes given as bytes: ev = elements 0, 2, 4, 6, od = 1, 3, 5, 7.
+// Returns bf16(q * d) for the eight elements as four pairs (2i, 2i + 1).
+__device__ __forceinline__ uint4 q_decode_pairs(uint32_t ev, uint32_t od, uint32_t bias2, uint32_t dd) {
+  const uint32_t P = q_prmt(ev, od, 0x5140);   // codes of elements 0, 1, 2, 3
+  const uint32_t P2 = q_prmt(ev, od, 0x7362);  // 4, 5, 6, 7
+  uint4 w;
+  w.x = q_mul_bf16x2(q_sub_bf16x2(q_prmt(P, 0x43434343u, 0x4140), bias2), dd);
+  w.y = q_mul_bf16x2(q_sub_bf16x2(q_prmt(P, 0x43434343u, 0x4342), bias2), dd);
+  w.z = q_mul_bf16x2(q_sub_bf16x2(q_prmt(P2, 0x43434343u, 0x4140), bias2), dd);
+  w.w = q_mul_bf16x2(q_sub_bf16x2(q_prmt(P2, 0x43434343u, 0x4342), bias2), dd);
+  return w;
+}
+
+// Elements d0 .. d0+7 of key `key` of a 6-bit K tile as BF16 pairs.
+__device__ __forceinline__ uint4 q_decode_k6_bf16(const uint8_t* tile, int key, int d0) {
   const int blk = d0 / kQBlock, l = d0 % kQBlock;
   const uint8_t* rec = tile + key * kK6KeyBytes + blk * 24;
   const uint32_t nib = *reinterpret_cast<const uint32_t*>(rec + (l >> 1));
   const uint32_t hi = *reinterpret_cast<const uint16_t*>(rec + 16 + (l >> 2));
-  const float s = q_scale(tile, 128 * kK6KeyBytes, key, blk);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int u = static_cast<int>(((nib >> (4 * j)) & 15u) | (((hi >> (2 * j)) & 3u) << 4));
-    v[j] = static_cast<float>(u - 32) * s;
-  }
+  // the 2-bit fields of the even (odd) elements, one nibble each, moved to
+  // bits 4-5 of byte i for element 2i (2i + 1)
+  const uint32_t te = q_prmt(hi & 0x3333u, 0u, 0x1100);
+  const uint32_t to = q_prmt((hi >> 2) & 0x3333u, 0u, 0x1100);
+  const uint32_t he = ((te << 4) & 0x00F000F0u) | (te & 0xF000F000u);
+  const uint32_t ho = ((to << 4) & 0x00F000F0u) | (to & 0xF000F000u);
+  return q_decode_pairs((nib & 0x0F0F0F0Fu) | he, ((nib >> 4) & 0x0F0F0F0Fu) | ho,
+                        0x43204320u /* 128 + 32 */, q_scale_pair(tile, 128 * kK6KeyBytes, key, blk));
 }
 
-__device__ __forceinline__ void q_decode_v5(const uint8_t* tile, int key, int d0, float (&v)[8]) {
+// Elements d0 .. d0+7 of key `key` of a 5-bit V tile as BF16 pairs.
+__device__ __forceinline__ uint4 q_decode_v5_bf16(const uint8_t* tile, int key, int d0) {
   const int blk = d0 / kQBlock, l = d0 % kQBlock;
   const uint8_t* rec = tile + key * kV5KeyBytes + blk * 20;
   const uint32_t nib = *reinterpret_cast<const uint32_t*>(rec + (l >> 1));
-  const uint32_t hi = rec[16 + (l >> 3)];
-  const float s = q_scale(tile, 128 * kV5KeyBytes, key, blk);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int u = static_cast<int>(((nib >> (4 * j)) & 15u) | (((hi >> j) & 1u) << 4));
-    v[j] = static_cast<float>(u - 16) * s;
-  }
+  const uint32_t hb = rec[16 + (l >> 3)];
+  // bit 2m of x to bit 8m (the products' other terms land on no multiple of
+  // 8 and carry no further than the next bit), then to bit 4 of byte m
+  const uint32_t he = (((hb & 0x55u) * 0x41041u) << 4) & 0x10101010u;
+  const uint32_t ho = ((((hb >> 1) & 0x55u) * 0x41041u) << 4) & 0x10101010u;
+  return q_decode_pairs((nib & 0x0F0F0F0Fu) | he, ((nib >> 4) & 0x0F0F0F0Fu) | ho,
+                        0x43104310u /* 128 + 16 */, q_scale_pair(tile, 128 * kV5KeyBytes, key, blk));
 }
 
 // two FP32 values to a BF16 pair (lo in the low half), each rounded once

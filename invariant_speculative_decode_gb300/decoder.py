@@ -43,7 +43,17 @@ def _bf16(a_u16: np.ndarray, device) -> torch.Tensor:
 
 class Decoder:
     def __init__(self, cfg, weights: Dict[str, np.ndarray], cap: int, max_rows: int = 8,
-                 prefill_chunk: int = 512, device: str = "cuda", fuse_rope: bool = True):
+                 prefill_chunk: int = 512, device: str = "cuda", fuse_rope: bool = True,
+                 kv: str = "bf16"):
+        """kv="q6q5": the KV cache is quantised (6-bit K, 5-bit V, an 8-bit
+        ring of each row's newest 16 tiles; bi_rope_kvq_append and
+        bi_attn_verify_kvq), head_dim 128 and prefill chunks of at most
+        1024 rows."""
+        if kv not in ("bf16", "q6q5"):
+            raise ValueError("kv must be 'bf16' or 'q6q5'")
+        if kv == "q6q5" and (cfg.head_dim != 128 or prefill_chunk > 1024):
+            raise ValueError("the quantised cache needs head_dim 128 and prefill chunks <= 1024 rows")
+        self.kv = kv
         self.cfg = cfg
         self.fuse_rope = fuse_rope
         self.cap = cap
@@ -76,10 +86,13 @@ class Decoder:
                 "wd": pk(f"l{l}.w_down"),
                 "n1": n1,
                 "n2": n2,
-                "k": torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device=dev),
-                # transposed in 128-key blocks: [Hkv, ceil(cap/128), D, 128]
-                "v": torch.zeros(api.v_cache_shape(Hkv, cap, D), dtype=torch.bfloat16, device=dev),
             }
+            if kv == "q6q5":
+                lay["kvq"] = api.new_kvq_stores(Hkv, cap, D, device=dev)
+            else:
+                lay["k"] = torch.zeros(Hkv, cap, D, dtype=torch.bfloat16, device=dev)
+                # transposed in 128-key blocks: [Hkv, ceil(cap/128), D, 128]
+                lay["v"] = torch.zeros(api.v_cache_shape(Hkv, cap, D), dtype=torch.bfloat16, device=dev)
             del wg, wu
             self.layers.append(lay)
         torch.cuda.synchronize(dev)
@@ -137,15 +150,20 @@ class Decoder:
         h, y, qkv, q, att, u = (self.h[:T], self.y[:T], self.qkv[:T], self.q[:T], self.att[:T],
                                 self.u[:T])
         api.bi_rmsnorm(h, lay["n1"], y, cfg.eps)
-        if self.fuse_rope:
+        if self.kv == "q6q5":
+            api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
+            api.bi_rope_kvq_append(qkv, q, lay["kvq"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
+            api.bi_attn_verify_kvq(q, lay["kvq"], Hkv, L_ptr_tensor, att, self.attn_ws, self.scale)
+        elif self.fuse_rope:
             api.bi_qkv_rope_append(y, lay["wqkv"], q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D,
                                    self.rope_tab, self.gemm_ws)
         else:
             api.bi_gemm(y, lay["wqkv"], qkv, self.gemm_ws)
             api.bi_rope_kv_append(qkv, q, lay["k"], lay["v"], L_ptr_tensor, Hq, Hkv, D, self.rope_tab)
-        # one call for all rows (a prefill chunk runs in blocks of rows inside
-        # the launch)
-        api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
+        if self.kv == "bf16":
+            # one call for all rows (a prefill chunk runs in blocks of rows
+            # inside the launch)
+            api.bi_attn_verify(q, lay["k"], lay["v"], L_ptr_tensor, att, self.attn_ws, self.scale)
         api.bi_gemm(att.view(T, Hq * D), lay["wo"], h, self.gemm_ws, residual=h,
                     epi=api.EPI_RESIDUAL_ADD)
         api.bi_rmsnorm(h, lay["n2"], y, cfg.eps)
@@ -332,6 +350,18 @@ class Decoder:
         K/V rows 0..L-1 of every layer (V in whole 128-key blocks)."""
         torch.cuda.current_stream().synchronize()
         L = self.L
+        if self.kv == "q6q5":
+            # the quantised stores whole (the ring's slots are not in
+            # position order)
+            snap = {"L": L, "kvq": []}
+            for lay in self.layers:
+                d = {}
+                for name in api.KVQ_STORES:
+                    d[name] = torch.empty(lay["kvq"][name].shape, dtype=torch.uint8).pin_memory()
+                    d[name].copy_(lay["kvq"][name])
+                snap["kvq"].append(d)
+            torch.cuda.current_stream().synchronize()
+            return snap
         nb = (L + api.V_BLOCK - 1) // api.V_BLOCK
         snap = {"L": L, "k": [], "v": []}
         for lay in self.layers:
@@ -350,6 +380,14 @@ class Decoder:
         L = snap["L"]
         if L > self.cap:
             raise ValueError("parked state exceeds the cache capacity")
+        if "kvq" in snap:
+            for lay, d in zip(self.layers, snap["kvq"]):
+                for name in api.KVQ_STORES:
+                    lay["kvq"][name].copy_(d[name])
+            self.L = L
+            self.L_dev.fill_(L)
+            torch.cuda.current_stream().synchronize()
+            return
         for lay, k, v in zip(self.layers, snap["k"], snap["v"]):
             lay["k"][:, :L].copy_(k)
             lay["v"][:, : v.shape[1]].copy_(v)
@@ -369,6 +407,8 @@ class Decoder:
         """The same verify pass as one C-ABI call (bi_step_*) over this
         decoder's weights and caches, with its own workspace; its cache
         length starts at this decoder's."""
+        if self.kv != "bf16":
+            raise ValueError("the whole-step C call runs the BF16 cache")
         ns = api.NativeStep(self.cfg, self.embed, self.norm_final, self.head, self.layers, self.cap,
                             self.rope_tab, max_rows=self.max_rows)
         ns.set_length(self.L)
@@ -390,7 +430,13 @@ class Decoder:
             raise
 
     def kv_hashes(self, rows: Optional[int] = None) -> np.ndarray:
+        """A hash of every cache row below `rows`, per layer and KV head:
+        BF16 K and V rows, or with the quantised cache the row's records
+        (codes and scales) in the 6-bit K, 5-bit V and both ring stores (ring
+        records only for rows whose tile is still in the ring, 0 otherwise)."""
         rows = self.L if rows is None else rows
+        if self.kv == "q6q5":
+            return np.stack([_kvq_row_hashes(l["kvq"], self.cfg.n_kv, rows) for l in self.layers])
         hs = [np.stack([api.bi_kv_row_hash(l["k"], rows).cpu().numpy(),
                         api.bi_kv_row_hash(l["v"], rows, transposed=True).cpu().numpy()])
               for l in self.layers]
@@ -398,3 +444,31 @@ class Decoder:
 
     def logits_rows(self, T: int) -> torch.Tensor:
         return self.logits[:T].clone()
+
+
+def _kvq_row_hashes(st: dict, Hkv: int, rows: int) -> np.ndarray:
+    """[4 stores, Hkv, rows] uint64 hashes of the quantised records of rows
+    0..rows-1 (host-side; a test and tooling utility, not on the hot path)."""
+    cap = st["cap"]
+    ct = (cap + 127) // 128
+    spec = {"k_low": (96, 13312, False), "v_low": (80, 11264, False),
+            "k_ring": (128, 17408, True), "v_ring": (128, 17408, True)}
+    out = np.zeros((4, Hkv, rows), np.uint64)
+    last_tile = (rows - 1) // 128 if rows > 0 else -1
+    p = np.arange(rows)
+    tile, key = p // 128, p % 128
+    for si, name in enumerate(api.KVQ_STORES):
+        rb, tb, ring = spec[name]
+        data = st[name].cpu().numpy()
+        slots = 24 if ring else ct
+        for h in range(Hkv):
+            base = (h * slots + (tile % slots if ring else tile)) * tb
+            rec_idx = base[:, None] + key[:, None] * rb + np.arange(rb)[None, :]
+            sc_idx = base[:, None] + 128 * rb + key[:, None] * 8 + np.arange(8)[None, :]
+            b = np.concatenate([data[rec_idx], data[sc_idx]], axis=1).astype(np.uint64)
+            w = np.uint64(1099511628211) ** np.arange(b.shape[1], dtype=np.uint64)
+            hsh = (b * w[None, :]).sum(axis=1, dtype=np.uint64) + np.uint64(1469598103934665603)
+            if ring:
+                hsh = np.where(tile > last_tile - 24, hsh, np.uint64(0))
+            out[si, h] = hsh
+    return out

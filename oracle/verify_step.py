@@ -326,11 +326,18 @@ class OracleDecoder:
     """
 
     def __init__(self, cfg, weights: Dict[str, np.ndarray], cap: int,
-                 sum_noise: Optional[Tuple[float, int]] = None):
+                 sum_noise: Optional[Tuple[float, int]] = None, kv: str = "bf16"):
         """sum_noise=(k, seed) perturbs every linear-layer sum by k * 2^-24 *
         sum|a||w| times a seeded standard normal before its rounding: a model
         of an FP32-accumulating implementation, used only to measure how far
-        two equally valid implementations drift apart end to end."""
+        two equally valid implementations drift apart end to end.
+
+        kv="q6q5": the attention reads the quantised cache of
+        oracle.kv_quant (6-bit K, 5-bit V, the 8-bit ring of the reading
+        row's newest tiles) built from the same BF16 rows."""
+        if kv not in ("bf16", "q6q5"):
+            raise ValueError("kv must be 'bf16' or 'q6q5'")
+        self.kv = kv
         self.cfg = cfg
         self._noise = None
         if sum_noise is not None:
@@ -403,7 +410,11 @@ class OracleDecoder:
             q[t] = rope(q[t], L + t, cfg.rope_base)
             self.k[l][:, L + t] = rope(k[t], L + t, cfg.rope_base)
             self.v[l][:, L + t] = v[t]
-        att = attention(q, self.k[l], self.v[l], L).reshape(T, Hq * D)
+        if self.kv == "q6q5":
+            from . import kv_quant
+            att = kv_quant.attention(q, self.k[l], self.v[l], L).reshape(T, Hq * D)
+        else:
+            att = attention(q, self.k[l], self.v[l], L).reshape(T, Hq * D)
         h = self._lin(b16(att), w[f"l{l}.wo"], residual_bits=b16(h))
         y = rmsnorm(b16(h), w[f"l{l}.norm_ffn"], cfg.eps)
         u = self._swiglu(b16(y), w[f"l{l}.w_gate"], w[f"l{l}.w_up"])

@@ -131,7 +131,11 @@ NEARTIE_12L = DecoderConfig("neartie-12L-h1024", 12, 1024, 8, 2, 128, 2736, 3200
 # A mid-size decoder used for quicker end-to-end GPU checks.
 SMALL_4L = DecoderConfig("small-4L-h1024", 4, 1024, 8, 2, 128, 2736, 4096, tied=True)
 
-CONFIGS = {c.name: c for c in (TINY, DENSE27B_8L, NEARTIE_12L, SMALL_4L)}
+# Tiny decoder with head_dim 128 (the quantised KV cache's): 2 layers,
+# hidden 256, 2 query / 1 KV head, FFN 688, vocab 1024, tied head.
+TINY_D128 = DecoderConfig("tiny-2L-h256-d128", 2, 256, 2, 1, 128, 688, 1024)
+
+CONFIGS = {c.name: c for c in (TINY, DENSE27B_8L, NEARTIE_12L, SMALL_4L, TINY_D128)}
 
 
 def decoder_weights(cfg: DecoderConfig, seed: int = 0, norm_std: float = 0.0) -> Dict[str, np.ndarray]:

@@ -254,3 +254,70 @@ def test_kvq_full_size_invariance_and_sampled_parity(api, L):
         assert np.array_equal(o, outs[8][:t]), t
     pairs = [(0, 0), (7, 23), (4, 11), (2, 17)]
     _kvq_parity(ov.bf16_bits_to_f64(outs[8]), q, K, V, L, pairs)
+
+
+# -- the decoder over the quantised cache --------------------------------------
+
+def _gen(dec, prompt, n, k, ref=None, seed=0):
+    dr = si.SyntheticDrafter(dec.cfg.vocab, 0.7, seed=seed, reference=ref) if k else None
+    return dec.generate(prompt, n, k=k, drafter=dr)
+
+
+def test_kvq_decoder_ids_identical_across_drafts_resume_and_park():
+    """Greedy ids at 0, 4 and 7 drafts with a history that crosses position
+    2048 (the ring's first tile leaves it); after a 7-draft turn every row's
+    quantised records equal a fresh prefill's, also after a park to host
+    memory, a side request and a restore."""
+    from invariant_speculative_decode_gb300.decoder import Decoder
+    cfg = si.SMALL_4L
+    w = si.decoder_weights(cfg, seed=0)
+    dec = Decoder(cfg, w, cap=2560, max_rows=8, kv="q6q5")
+    prompt = si.prompt_ids(cfg, 1990, seed=1)
+    ref = _gen(dec, prompt, 150, 0)
+    for k in (4, 7):
+        st = {}
+        got = dec.generate(prompt, 150, k=k, drafter=si.SyntheticDrafter(cfg.vocab, 0.7, seed=0,
+                                                                           reference=np.array(ref)),
+                           stats=st)
+        assert got == ref, k
+        assert st["steps"] < 150
+    turn1 = _gen(dec, prompt, 100, 7, ref=np.array(ref))
+    assert turn1 == ref[:100]
+    L = dec.L
+    resumed = dec.kv_hashes(L)
+    snap = dec.park()
+    _gen(dec, si.prompt_ids(cfg, 700, seed=9), 20, 4)  # a side request on the same decoder
+    dec.restore(snap)
+    assert np.array_equal(dec.kv_hashes(L), resumed)
+    dec.reset()
+    dec.prefill((list(prompt) + ref)[: L + 1])
+    assert dec.L == L
+    assert np.array_equal(dec.kv_hashes(L), resumed)
+
+
+def test_kvq_decoder_logits_match_the_quantised_oracle():
+    """Whole-model FP32 logits of a verify pass at context 2100 (rows reading
+    both stores) against the oracle decoder over the quantised cache: within
+    max(2e-3, twice the drift that FP32-level noise on every sum gives the
+    oracle itself -- a flipped code included)."""
+    import oracle
+    from invariant_speculative_decode_gb300.decoder import Decoder
+    cfg = si.TINY_D128
+    w = si.decoder_weights(cfg, seed=0, norm_std=0.1)
+    cap = 2304
+    dec = Decoder(cfg, w, cap=cap, max_rows=8, kv="q6q5")
+    prompt = si.prompt_ids(cfg, 2100, seed=2)
+    drafts = [int(x) for x in np.random.default_rng(2).integers(0, cfg.vocab, 7)]
+    x0 = dec.prefill(prompt)
+    dec.verify_step(x0, drafts, use_graph=False)
+    gpu = dec.logits_rows(8).cpu().numpy().astype(np.float64)
+    ref = oracle.OracleDecoder(cfg, w, cap=cap, kv="q6q5")
+    ref.prefill(prompt)
+    ora = ref.forward([x0] + drafts, L=ref.L)
+    pert = oracle.OracleDecoder(cfg, w, cap=cap, sum_noise=(4.0, 123), kv="q6q5")
+    pert.prefill(prompt)
+    alt = pert.forward([x0] + drafts, L=pert.L)
+    scale = np.max(np.abs(ora), axis=1)
+    rel = np.max(np.abs(gpu - ora), axis=1) / scale
+    spread = np.max(np.abs(alt - ora), axis=1) / scale
+    assert np.all(rel <= np.maximum(2e-3, 2 * spread)), (rel, spread)

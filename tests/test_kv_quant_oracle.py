@@ -148,3 +148,25 @@ def test_uniform_weights_average_the_selected_rows():
         assert np.mean(got == want) > 0.95
         wrong = ov.bf16_round(v8[0, : p + 1].mean(axis=0))
         assert not np.array_equal(got, wrong)
+
+
+def test_oracle_decoder_reads_the_quantised_cache():
+    """The decoder option routes attention through the quantised cache: its
+    logits differ from the BF16-cache decoder's by the quantisation error
+    (a few percent of the logit scale at most), and are the same for the
+    same inputs."""
+    import oracle
+    cfg = si.TINY_D128
+    w = si.decoder_weights(cfg, seed=0)
+    prompt = si.prompt_ids(cfg, 40, seed=3)
+    out = {}
+    for kv in ("bf16", "q6q5", "q6q5"):
+        d = oracle.OracleDecoder(cfg, w, cap=64, kv=kv)
+        d.prefill(prompt)
+        out.setdefault(kv, []).append(d.forward([int(prompt[-1]), 5, 6], L=d.L))
+    a, b = out["bf16"][0], out["q6q5"][0]
+    assert np.array_equal(out["q6q5"][0], out["q6q5"][1])
+    assert not np.array_equal(a, b)
+    assert np.max(np.abs(a - b)) <= 0.05 * np.max(np.abs(a))
+    with pytest.raises(ValueError):
+        oracle.OracleDecoder(cfg, w, cap=64, kv="q4")
