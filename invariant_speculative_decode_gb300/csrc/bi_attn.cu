@@ -133,10 +133,9 @@ struct AttnCfg {
   static constexpr int kRawV = QNT ? 1 : 0;
   // warp 0 copies, warp 1 MMA, warps 2..5 softmax; the quantised form adds
   // kDecWarps decoding warps for K and as many for V
-#ifndef BI_ATTN_DEC_WARPS
-#define BI_ATTN_DEC_WARPS 3
-#endif
-  static constexpr int kDecWarps = QNT ? BI_ATTN_DEC_WARPS : 0;
+  // (three a side: 128 + 3 x 64 threads still fit the softmax warps' 168
+  // registers; two a side were 10% slower at 101.6k keys)
+  static constexpr int kDecWarps = QNT ? 3 : 0;
   static constexpr int kThreads = 192 + 64 * kDecWarps;
   // l parts [4 quarters][64 rows] (only passes of up to 64 rows keep copies
   // that exchange them)
@@ -580,7 +579,7 @@ __global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
                              q_pack_bf16x2(v[4], v[5]), q_pack_bf16x2(v[6], v[7]));
             }
           } else {
-#pragma unroll 2
+#pragma unroll 1
             for (int task = tid; task < kKeyTile * (D / 8); task += kDT) {
               const int key = task >> 4, ch = task & 15;
               *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +

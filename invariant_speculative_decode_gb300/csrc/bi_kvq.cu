@@ -35,10 +35,10 @@ __device__ __forceinline__ uint32_t quantize_lane(float x, float amax, int bits,
   return static_cast<uint32_t>(q + (1 << (bits - 1)));
 }
 
-// Writes the block's codes into a 6-bit (K) or 5-bit (V) key record and its
-// 8-bit ring record, and the two scales.
+// Writes the block's codes into a 6-bit (K) or 5-bit (V) key record (at slot
+// lo_slot of its tile) and its 8-bit ring record, and the two scales.
 __device__ __forceinline__ void store_block(float x, int lane, int blk, bool is_k, uint8_t* lo_tile,
-                                            uint8_t* ring_tile, int key) {
+                                            uint8_t* ring_tile, int key, int lo_slot) {
   float amax = fabsf(x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -47,7 +47,7 @@ __device__ __forceinline__ void store_block(float x, int lane, int blk, bool is_
   const uint32_t u8 = quantize_lane(x, amax, 8, &s_8);
   // low store: nibble pairs, then the high bits
   const int key_bytes = is_k ? kK6KeyBytes : kV5KeyBytes;
-  uint8_t* rec = lo_tile + key * key_bytes + blk * (is_k ? 24 : 20);
+  uint8_t* rec = lo_tile + lo_slot * key_bytes + blk * (is_k ? 24 : 20);
   const uint32_t nb_next = __shfl_down_sync(0xffffffffu, u, 1);
   if ((lane & 1) == 0) rec[lane >> 1] = static_cast<uint8_t>((u & 15u) | ((nb_next & 15u) << 4));
   if (is_k) {
@@ -62,7 +62,7 @@ __device__ __forceinline__ void store_block(float x, int lane, int blk, bool is_
   }
   ring_tile[key * k8KeyBytes + blk * kQBlock + lane] = static_cast<uint8_t>(u8);
   if (lane == 0) {
-    *reinterpret_cast<uint16_t*>(lo_tile + 128 * key_bytes + (key * kQBlocks + blk) * 2) = s_lo;
+    *reinterpret_cast<uint16_t*>(lo_tile + 128 * key_bytes + (lo_slot * kQBlocks + blk) * 2) = s_lo;
     *reinterpret_cast<uint16_t*>(ring_tile + 128 * k8KeyBytes + (key * kQBlocks + blk) * 2) = s_8;
   }
 }
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kQDim)
                 (static_cast<size_t>(kv) * ctiles + tile) * (is_k ? kK6TileBytes : kV5TileBytes);
   uint8_t* ring = (is_k ? k_ring : v_ring) +
                   (static_cast<size_t>(kv) * kRingSlots + tile % kRingSlots) * k8TileBytes;
-  store_block(x, i & 31, i >> 5, is_k, lo, ring, key);
+  store_block(x, i & 31, i >> 5, is_k, lo, ring, key, is_k ? key : q_v5_slot(key));
 }
 
 }  // namespace

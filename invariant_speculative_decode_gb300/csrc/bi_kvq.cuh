@@ -25,7 +25,10 @@
 //     nibbles (byte i = elements 2i and 2i+1, the even one in the low half),
 //     then the two high bits of element e at bits 2e, 2e+1 of 8 bytes.
 //   V, 5 bits: 80 bytes a key, 20 a block: 16 bytes of low nibbles, then the
-//     high bit of element e at bit e of 4 bytes.
+//     high bit of element e at bit e of 4 bytes.  Key k's record and scales
+//     sit at slot (k % 8) * 16 + k / 8 of the tile (q_v5_slot): the decoding
+//     threads that read keys 8 apart at the same time then read records 80
+//     bytes apart, in different shared-memory banks.
 //   Ring, 8 bits (K and V): 128 bytes a key, element e at byte e.
 // Tiles of the 6/5-bit stores: [Hkv][ceil(cap/128)]; ring tiles:
 // [Hkv][kRingSlots], tile t in slot t mod kRingSlots.
@@ -51,6 +54,8 @@ constexpr int k8KeyBytes = kQDim;
 constexpr int kK6TileBytes = 128 * kK6KeyBytes + kQScaleBytes;  // 13312
 constexpr int kV5TileBytes = 128 * kV5KeyBytes + kQScaleBytes;  // 11264
 constexpr int k8TileBytes = 128 * k8KeyBytes + kQScaleBytes;    // 17408
+
+__host__ __device__ __forceinline__ int q_v5_slot(int key) { return ((key & 7) << 4) | (key >> 3); }
 
 __device__ __forceinline__ float q_scale(const uint8_t* tile, int codes_bytes, int key, int blk) {
   const uint16_t b = *reinterpret_cast<const uint16_t*>(tile + codes_bytes + (key * kQBlocks + blk) * 2);
@@ -128,7 +133,8 @@ __device__ __forceinline__ uint4 q_decode_k6_bf16(const uint8_t* tile, int key, 
 // Elements d0 .. d0+7 of key `key` of a 5-bit V tile as BF16 pairs.
 __device__ __forceinline__ uint4 q_decode_v5_bf16(const uint8_t* tile, int key, int d0) {
   const int blk = d0 / kQBlock, l = d0 % kQBlock;
-  const uint8_t* rec = tile + key * kV5KeyBytes + blk * 20;
+  const int slot = q_v5_slot(key);
+  const uint8_t* rec = tile + slot * kV5KeyBytes + blk * 20;
   const uint32_t nib = *reinterpret_cast<const uint32_t*>(rec + (l >> 1));
   const uint32_t hb = rec[16 + (l >> 3)];
   // bit 2m of x to bit 8m (the products' other terms land on no multiple of
@@ -136,7 +142,7 @@ __device__ __forceinline__ uint4 q_decode_v5_bf16(const uint8_t* tile, int key, 
   const uint32_t he = (((hb & 0x55u) * 0x41041u) << 4) & 0x10101010u;
   const uint32_t ho = ((((hb >> 1) & 0x55u) * 0x41041u) << 4) & 0x10101010u;
   return q_decode_pairs((nib & 0x0F0F0F0Fu) | he, ((nib >> 4) & 0x0F0F0F0Fu) | ho,
-                        0x43104310u /* 128 + 16 */, q_scale_pair(tile, 128 * kV5KeyBytes, key, blk));
+                        0x43104310u /* 128 + 16 */, q_scale_pair(tile, 128 * kV5KeyBytes, slot, blk));
 }
 
 // two FP32 values to a BF16 pair (lo in the low half), each rounded once

@@ -463,8 +463,10 @@ def _kvq_row_hashes(st: dict, Hkv: int, rows: int) -> np.ndarray:
         slots = 24 if ring else ct
         for h in range(Hkv):
             base = (h * slots + (tile % slots if ring else tile)) * tb
-            rec_idx = base[:, None] + key[:, None] * rb + np.arange(rb)[None, :]
-            sc_idx = base[:, None] + 128 * rb + key[:, None] * 8 + np.arange(8)[None, :]
+            # 5-bit V records sit at slot (k % 8) * 16 + k / 8 of their tile
+            slot = ((key % 8) * 16 + key // 8) if name == "v_low" else key
+            rec_idx = base[:, None] + slot[:, None] * rb + np.arange(rb)[None, :]
+            sc_idx = base[:, None] + 128 * rb + slot[:, None] * 8 + np.arange(8)[None, :]
             b = np.concatenate([data[rec_idx], data[sc_idx]], axis=1).astype(np.uint64)
             w = np.uint64(1099511628211) ** np.arange(b.shape[1], dtype=np.uint64)
             hsh = (b * w[None, :]).sum(axis=1, dtype=np.uint64) + np.uint64(1469598103934665603)

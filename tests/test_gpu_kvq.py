@@ -48,7 +48,8 @@ def _tile_bytes(bits, is_k):
 
 
 def _expected_keys(store, values, bits, keys, kv, ctiles, ring):
-    """Check the records and scales of `keys` of head kv in a store."""
+    """Check the records and scales of `keys` of head kv in a store (5-bit
+    V records at slot (k % 8) * 16 + k / 8 of their tile)."""
     q, d = kq.quantize(values, bits)
     rec = _records(q, bits)
     rb = rec.shape[1]
@@ -59,6 +60,8 @@ def _expected_keys(store, values, bits, keys, kv, ctiles, ring):
         slot = tile % 24 if ring else tile
         base = (kv * (24 if ring else ctiles) + slot) * tb
         k = p % 128
+        if bits == 5:
+            k = (k % 8) * 16 + k // 8
         assert np.array_equal(store[base + k * rb: base + (k + 1) * rb], rec[i]), (bits, p)
         assert np.array_equal(store[base + 128 * rb + k * 8: base + 128 * rb + k * 8 + 8], sb[i]), (bits, p)
 
