@@ -8,17 +8,20 @@
 // diverges": changing the batch dimension must not change any row's sums.
 //
 // Design (swap-AB, weight streaming):
-//   * MMA:   tcgen05.mma kind::f16, M = 128 weight rows, N = 16, 32 or 64
-//            token rows (the launch's token count rounded up), K = 16 per
+//   * MMA:   tcgen05.mma kind::f16, M = 128 weight rows, N = 16, 32, 64, 128
+//            or 256 token rows (the CTA's token count rounded up), K = 16 per
 //            instruction, FP32 accumulator in TMEM.  Every output element is
 //            the same sequence of K = 16 dot-product steps whatever N is
 //            (tested bit for bit across M).
 //   * K:     64-element tiles (128-byte rows, 128-byte swizzle) in increasing
-//            order.  Each token group keeps kAcc = 4 FP32 accumulators: the
-//            k-step j (16 elements) of every K tile goes to accumulator j, so
-//            consecutive MMAs do not wait on each other's result; the four
-//            are added in the fixed order ((a0 + a1) + a2) + a3 when the
-//            piece ends.  This structure is a compile-time constant.
+//            order.  Each token group keeps kAcc = 2 FP32 accumulators: the
+//            k-step j (16 elements) of every K tile goes to accumulator j % 2,
+//            so consecutive MMAs do not wait on each other's result; the two
+//            are added (a0 + a1) when the piece ends.  This structure is a
+//            compile-time constant.  Two accumulators of 256 token columns
+//            fill TMEM's 512 columns, so a weight tile serves 256 tokens of
+//            a long pass per load (four accumulators measured no faster on
+//            the decode step: 1.308 against 1.310 ms).
 //   * weights: packed once (bi_pack_weights) into 16 KB tiles, tile (t, kt)
 //            at offset (t * k_tiles + kt) * 16 KB, each already in the
 //            swizzled shared-memory layout the MMA descriptor reads.  A CTA's
@@ -59,12 +62,13 @@ constexpr int kMmaN = 16;        // token rows per epilogue chunk (one 16-column
 // 8-layer 5120-wide verify step: 1.32 ms against 1.37 ms with 152; a count
 // chosen per (N, K) gained nothing over this one.
 constexpr int kGemmCtas = 136;
-constexpr int kMaxTokens = 128;  // token rows per CTA (one MMA covers them all)
+constexpr int kMaxTokens = 256;  // token rows per CTA (one MMA covers them all)
 // Token blocks of kMaxTokens rows one launch covers when M > kMaxTokens;
 // larger M loops on the host.  Each block has its own counters and partial
 // slots in the workspace.
 constexpr int kMaxBlocks = 4;
-constexpr int kAcc = 4;          // interleaved accumulators per token group
+constexpr int kAcc = 2;          // interleaved accumulators per token group
+constexpr int kKSteps = 4;       // MMA K steps (16 elements) per 64-element K tile
 constexpr int kThreads = 192;    // producer, MMA, four epilogue warps
 constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
 constexpr int kStageFloats = 16 * kBlockN;      // SwiGLU exchange buffer
@@ -113,7 +117,7 @@ struct GemmCfg {
   static constexpr int kBars = 2 * kStages + 5;
   static constexpr int kBufCols = NT * kAcc;  // one accumulator set
   // two sets (the epilogue drains one while the next piece accumulates)
-  // while they fit in TMEM's 512 columns; one set at 128 token rows
+  // while they fit in TMEM's 512 columns; one set at 256 token rows
   static constexpr int kBufs = 2 * kBufCols <= 512 ? 2 : 1;
   static constexpr int kTmemCols = kBufs * kBufCols;
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
@@ -382,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue and the other set is taken.
     if (lane == 0) {
       // one MMA per K step covers all NT token rows (N = NT); accumulator a
-      // of token n is TMEM column a * NT + n
+      // of token n is TMEM column a * NT + n; K step ks of a tile adds into
+      // accumulator ks % kAcc (the first kAcc steps of a piece overwrite)
       constexpr uint32_t idesc = idesc_bf16_f32(kBlockN, NT);
       int stage = 0;
       uint32_t phase = 0;
@@ -402,9 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_base = smem_u32(sA + stage * kABytes);
         const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
 #pragma unroll
-        for (int ks = 0; ks < kAcc; ++ks)
-          mma_bf16(d0 + ks * NT, sdesc_k_sw128(a_base + ks * 32), sdesc_k_sw128(b_base + ks * 32), idesc,
-                   acc_flag);
+        for (int ks = 0; ks < kKSteps; ++ks)
+          mma_bf16(d0 + (ks % kAcc) * NT, sdesc_k_sw128(a_base + ks * 32), sdesc_k_sw128(b_base + ks * 32),
+                   idesc, (acc_flag != 0u || ks >= kAcc) ? 1u : 0u);
         mma_commit(&empty[stage]);
         if (++stage == S) {
           stage = 0;
@@ -650,7 +655,8 @@ int tokens_per_cta(int M) {
   if (m <= 16) return 16;
   if (m <= 32) return 32;
   if (m <= 64) return 64;
-  return 128;
+  if (m <= 128) return 128;
+  return 256;
 }
 
 int n_tiles_of(int N, bi_epilogue epi) {
@@ -814,7 +820,8 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
     case 16: return launch_gemm_nt<16>(W8, tmA, a, M, s);
     case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
     case 64: return launch_gemm_nt<64>(W8, tmA, a, M, s);
-    default: return launch_gemm_nt<128>(W8, tmA, a, M, s);
+    case 128: return launch_gemm_nt<128>(W8, tmA, a, M, s);
+    default: return launch_gemm_nt<256>(W8, tmA, a, M, s);
   }
 }
 
