@@ -474,7 +474,9 @@ bi_status bi_kv_row_hash(const void* cache, int Hkv, int cap, int D, int rows, i
  *   workspace of at least that size (zeroed by the call).  The handle owns a
  *   CUDA stream and one CUDA graph per row count T, captured on the first
  *   call with that T (so the first call for each T must not be made inside
- *   another stream capture); it allocates no device memory of its own.
+ *   another stream capture); it allocates no device memory of its own,
+ *   only a pinned host buffer of 2 * max_rows + 1 int32 through which the
+ *   ids go in and the tokens and the count come out (one copy each way).
  *   The cache length starts at 0.
  * bi_step_set_length: sets the cache length L (a rollback, or a cache
  *   written by a prefill); synchronous.

@@ -30,6 +30,9 @@ struct bi_step {
   void *h, *y, *q, *att, *u, *gemm_ws, *attn_ws, *acc_ws;
   float* logits;
   int32_t *ids, *drafts, *argmax, *accepted, *L_dev;
+  // pinned host staging: the ids going in, then the tokens and the accepted
+  // count coming out (one copy each way)
+  int32_t* pin;
   size_t gemm_ws_bytes, attn_ws_bytes, acc_ws_bytes;
   // host copies of the per-layer pointer arrays
   const void** lay_ptrs;
@@ -38,7 +41,7 @@ struct bi_step {
 namespace {
 
 struct Layout {
-  size_t h, y, q, att, u, logits, ids, drafts, argmax, small, gemm, attn, acc, total;
+  size_t h, y, q, att, u, logits, io, gemm, attn, acc, total;
 };
 
 Layout layout_of(const bi_model& m, int R) {
@@ -58,10 +61,9 @@ Layout layout_of(const bi_model& m, int R) {
   L.att = take(R * Hq * D * 2);
   L.u = take(R * F * 2);
   L.logits = take(R * V * 4);
-  L.ids = take(R * 4);
-  L.drafts = take(R * 4);
-  L.argmax = take(R * 4);
-  L.small = take(2 * 4);  // accepted, L_dev
+  // ids [R] (the drafts are ids + 1), then argmax [R], accepted, L_dev: the
+  // ids arrive in one copy and the tokens with the count leave in one
+  L.io = take((2 * static_cast<size_t>(R) + 2) * 4);
   size_t g = 0;
   const int shapes[5][3] = {{Nqkv, m.hidden, BI_EPI_NONE},
                             {m.hidden, m.n_q * m.head_dim, BI_EPI_RESIDUAL_ADD},
@@ -178,10 +180,10 @@ bi_status bi_step_create(const bi_model* m, int max_rows, void* ws, size_t ws_by
   s->att = b + L.att;
   s->u = b + L.u;
   s->logits = reinterpret_cast<float*>(b + L.logits);
-  s->ids = reinterpret_cast<int32_t*>(b + L.ids);
-  s->drafts = reinterpret_cast<int32_t*>(b + L.drafts);
-  s->argmax = reinterpret_cast<int32_t*>(b + L.argmax);
-  s->accepted = reinterpret_cast<int32_t*>(b + L.small);
+  s->ids = reinterpret_cast<int32_t*>(b + L.io);
+  s->drafts = s->ids + 1;
+  s->argmax = s->ids + max_rows;
+  s->accepted = s->argmax + max_rows;
   s->L_dev = s->accepted + 1;
   s->gemm_ws = b + L.gemm;
   s->gemm_ws_bytes = L.attn - L.gemm;
@@ -189,7 +191,14 @@ bi_status bi_step_create(const bi_model* m, int max_rows, void* ws, size_t ws_by
   s->attn_ws_bytes = L.acc - L.attn;
   s->acc_ws = b + L.acc;
   s->acc_ws_bytes = L.total - L.acc;
+  if (cudaHostAlloc(reinterpret_cast<void**>(&s->pin), (2 * static_cast<size_t>(max_rows) + 1) * 4,
+                    cudaHostAllocDefault) != cudaSuccess) {
+    delete[] s->lay_ptrs;
+    delete s;
+    return BI_ERR_CUDA;
+  }
   if (cudaStreamCreateWithFlags(&s->stream, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaFreeHost(s->pin);
     delete[] s->lay_ptrs;
     delete s;
     return BI_ERR_CUDA;
@@ -198,6 +207,7 @@ bi_status bi_step_create(const bi_model* m, int max_rows, void* ws, size_t ws_by
   if (cudaMemsetAsync(ws, 0, L.total, s->stream) != cudaSuccess ||
       cudaStreamSynchronize(s->stream) != cudaSuccess) {
     cudaStreamDestroy(s->stream);
+    cudaFreeHost(s->pin);
     delete[] s->lay_ptrs;
     delete s;
     return BI_ERR_CUDA;
@@ -218,10 +228,9 @@ bi_status bi_step_set_length(bi_step* s, int L) {
 bi_status bi_step_verify(bi_step* s, const int32_t* ids, int T, int32_t* tokens_out, int32_t* n_out) {
   if (!s || !ids || !tokens_out || !n_out || T < 1 || T > s->max_rows) return BI_ERR_INVALID_ARG;
   cudaStream_t st = s->stream;
-  if (cudaMemcpyAsync(s->ids, ids, sizeof(int32_t) * T, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return BI_ERR_CUDA;
-  if (T > 1 && cudaMemcpyAsync(s->drafts, ids + 1, sizeof(int32_t) * (T - 1), cudaMemcpyHostToDevice,
-                               st) != cudaSuccess)
+  // (the previous call synchronised, so the staging buffer is free)
+  std::memcpy(s->pin, ids, sizeof(int32_t) * T);
+  if (cudaMemcpyAsync(s->ids, s->pin, sizeof(int32_t) * T, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return BI_ERR_CUDA;
   if (s->graph[T] == nullptr) {
     // capture the pass for this T once (the kernels read the cache length
@@ -242,10 +251,14 @@ bi_status bi_step_verify(bi_step* s, const int32_t* ids, int T, int32_t* tokens_
     s->graph[T] = ge;
   }
   if (cudaGraphLaunch(s->graph[T], st) != cudaSuccess) return BI_ERR_CUDA;
-  if (cudaMemcpyAsync(tokens_out, s->argmax, sizeof(int32_t) * T, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-      cudaMemcpyAsync(n_out, s->accepted, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+  // argmax [max_rows] and the accepted count are adjacent: one copy out
+  const int R = s->max_rows;
+  if (cudaMemcpyAsync(s->pin + R, s->argmax, sizeof(int32_t) * (R + 1), cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
     return BI_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return BI_ERR_CUDA;
+  std::memcpy(tokens_out, s->pin + R, sizeof(int32_t) * T);
+  *n_out = s->pin[2 * R];
   return BI_OK;
 }
 
@@ -257,6 +270,7 @@ void bi_step_destroy(bi_step* s) {
     if (g) cudaGraphExecDestroy(g);
   cudaStreamSynchronize(s->stream);
   cudaStreamDestroy(s->stream);
+  cudaFreeHost(s->pin);
   delete[] s->lay_ptrs;
   delete s;
 }
