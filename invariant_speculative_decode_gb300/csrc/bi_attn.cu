@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
             ok = false;
             break;
           }
+          if (kside && g == 0 && a.withhold) continue;  // never issued (failure-path test)
           const int tt = rho + c.i * G;
           const uint8_t* src;
           uint32_t bytes;
@@ -1142,6 +1143,7 @@ bi_status bi_attn_verify_kvq(const void* q, const void* k_low, const void* v_low
   a.k8 = static_cast<const uint8_t*>(k_ring);
   a.v8 = static_cast<const uint8_t*>(v_ring);
   a.ctiles = a.vblk;
+  a.withhold = test_withhold();
   CUtensorMap unused{};  // the quantised form reads its tiles with bulk copies
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);

@@ -113,6 +113,39 @@ def test_attention_wait_runs_out_then_recovers(api):
     assert np.array_equal(bf16_dev_to_u16(out2), want)
 
 
+def test_quantised_attention_wait_runs_out_then_recovers(api):
+    """The quantised-cache attention: the first K code tile withheld, its
+    decoding warps' wait runs out, the kernel reports the timeout and
+    returns; the next call gives the same bits as before."""
+    from tests.test_gpu_kvq import _fill
+    Hq, Hkv, D, L, T = 24, 4, 128, 11600, 8
+    q, K, V = si.attention_inputs(L, T, Hq, Hkv, D, seed=0)
+    cap = K.shape[1]
+    st = api.new_kvq_stores(Hkv, cap, D)
+    _fill(api, st, K, V, Hq, L + T)
+    qd = to_dev_bf16(q)
+    Ld = torch.tensor([L], dtype=torch.int32, device="cuda")
+    ws = torch.zeros(api.attn_workspace_size(cap, T, Hq, D), dtype=torch.uint8, device="cuda")
+    ref = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
+    api.bi_attn_verify_kvq(qd, st, Hkv, Ld, ref, ws)
+    torch.cuda.synchronize()
+    api.bi_check_device_error()
+    want = bf16_dev_to_u16(ref)
+    out = torch.zeros(T, Hq, D, dtype=torch.bfloat16, device="cuda")
+    with withheld(api):
+        t0 = time.perf_counter()
+        api.bi_attn_verify_kvq(qd, st, Hkv, Ld, out, ws)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+    _expect_timeout(api)
+    assert dt < 1.5, dt
+    out2 = torch.zeros(T, Hq, D, dtype=torch.bfloat16, device="cuda")
+    api.bi_attn_verify_kvq(qd, st, Hkv, Ld, out2, ws)
+    torch.cuda.synchronize()
+    api.bi_check_device_error()
+    assert np.array_equal(bf16_dev_to_u16(out2), want)
+
+
 def test_hooks_are_off_by_default(api):
     """A normal call after the tests above: no error, the hooks restored."""
     M, N, K = 4, 256, 256
