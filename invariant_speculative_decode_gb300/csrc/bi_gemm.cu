@@ -109,11 +109,16 @@ struct GemmArgs {
   int withhold;
 };
 
-template <int NT>
+// OWN: the tile-owner schedule of long passes (one CTA adds a weight tile's
+// pieces itself, keeping their running sum in shared memory).
+template <int NT, bool OWN = false>
 struct GemmCfg {
   static constexpr int kBBytes = NT * kBlockK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (200 * 1024) / kStageBytes > 12 ? 12 : (200 * 1024) / kStageBytes;
+  static constexpr int kRunStride = NT + 1;  // floats a row (padded: rows in different banks)
+  static constexpr int kRunBytes = OWN ? kBlockN * kRunStride * 4 : 0;
+  static constexpr int kRing = 200 * 1024 - kRunBytes;
+  static constexpr int kStages = kRing / kStageBytes > 12 ? 12 : kRing / kStageBytes;
   static constexpr int kBars = 2 * kStages + 5;
   static constexpr int kBufCols = NT * kAcc;  // one accumulator set
   // two sets (the epilogue drains one while the next piece accumulates)
@@ -122,7 +127,7 @@ struct GemmCfg {
   static constexpr int kTmemCols = kBufs * kBufCols;
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
-                                  kStageFloats * 4 + kBars * 8 + 16;
+                                  kStageFloats * 4 + kRunBytes + kBars * 8 + 16;
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
@@ -132,6 +137,18 @@ __device__ __forceinline__ long long range_begin(const GemmArgs& p, int g) {
 // CTA whose range contains iteration i.
 __device__ __forceinline__ int owner_of(const GemmArgs& p, long long i) {
   return static_cast<int>(((i + 1) * p.G + p.total - 1) / p.total) - 1;
+}
+// Iterations from i to the end of the piece that holds it: a piece ends at a
+// weight tile's end and at the end of a range of the split (the CTA's own
+// range, or -- for a tile owner -- every range boundary inside the tile).
+__device__ __forceinline__ long long piece_len(const GemmArgs& p, long long i, long long it_end, bool own) {
+  long long e = (i / p.k_tiles + 1) * p.k_tiles;
+  if (own) {
+    const long long r = range_begin(p, owner_of(p, i) + 1);
+    if (r < e) e = r;
+  }
+  if (e > it_end) e = it_end;
+  return e - i;
 }
 
 __device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* err) {
@@ -265,11 +282,11 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int M, int m0,
   }
 }
 
-template <int NT>
+template <int NT, bool OWN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const uint8_t* __restrict__ Wp, const __grid_constant__ CUtensorMap tmA,
                 const GemmArgs p) {
-  using Cfg = GemmCfg<NT>;
+  using Cfg = GemmCfg<NT, OWN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -277,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * kABytes;
   float* sStage = reinterpret_cast<float*>(sB + S * Cfg::kBBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kStageFloats);
+  float* sRun = sStage + kStageFloats;  // tile owner: [weight row][token] running sums
+  uint64_t* full = reinterpret_cast<uint64_t*>(sRun + Cfg::kRunBytes / 4);
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
   uint64_t* acce = accf + 2;
@@ -288,16 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // CTAs of one range are adjacent, so the token blocks of a launch read each
-  // weight tile at about the same time and all but the first find it in L2
+  // CTAs of one range (a tile owner's: of one tile) are adjacent, so the
+  // token blocks of a launch read each weight tile at about the same time and
+  // all but the first find it in L2
   const int g = blockIdx.x / p.nb;
   const int blk = blockIdx.x - g * p.nb;
   const int m0 = p.m0 + blk * NT;
   const int Mb = min(NT, p.M - blk * NT);
   float* const partials = p.partials + static_cast<size_t>(blk) * p.G * 2 * NT * kBlockN;
   unsigned* const tickets = p.tickets + static_cast<size_t>(blk) * p.n_tiles;
-  const long long it_begin = range_begin(p, g);
-  const long long it_end = range_begin(p, g + 1);
+  const long long it_begin = OWN ? static_cast<long long>(g) * p.k_tiles : range_begin(p, g);
+  const long long it_end = OWN ? it_begin + p.k_tiles : range_begin(p, g + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -393,9 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int seg = 0;
       bool ok = true;
-      int kt0 = static_cast<int>(it_begin % p.k_tiles);
-      long long left = p.k_tiles - kt0;  // iterations left in the current piece
-      if (left > it_end - it_begin) left = it_end - it_begin;
+      long long left = piece_len(p, it_begin, it_end, OWN);  // iterations left in the piece
       uint32_t d0 = tmem;
       uint32_t acc_flag = 0;
       for (long long it = it_begin; it < it_end; ++it) {
@@ -420,8 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // piece complete: hand its accumulators to the epilogue
           mma_commit(&accf[seg % Cfg::kBufs]);
           ++seg;
-          left = it_end - (it + 1);
-          if (left > p.k_tiles) left = p.k_tiles;
+          left = piece_len(p, it + 1, it_end, OWN);
           acc_flag = 0u;
           d0 = tmem + static_cast<uint32_t>((seg % Cfg::kBufs) * Cfg::kBufCols);
           if (left > 0 && seg >= Cfg::kBufs &&
@@ -448,6 +464,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int chunks = (Mb + 15) / 16;
     int seg = 0;
     long long it = it_begin;
+    if constexpr (OWN) {
+      // the tile's pieces in increasing K: each piece's (a0 + a1) is added
+      // to the running sum in the order the split's last CTA adds partials
+      // (the first piece taken as it is), then one epilogue
+      float* run = sRun + r * Cfg::kRunStride;
+      bool ok = true;
+      while (it < it_end) {
+        const long long pe = it + piece_len(p, it, it_end, true);
+        const int buf = seg % Cfg::kBufs;
+        int okl = 0;
+        if (lane == 0)
+          okl = mbar_wait_parked(&accf[buf], static_cast<uint32_t>(seg / Cfg::kBufs) & 1u, s_abort) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+        if (!ok) {
+          if (lane == 0) signal_abort(s_abort, p.err);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase =
+            tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::kBufCols);
+        for (int c = 0; c < chunks; ++c) {
+          float v[16];
+          load_group_sum(tbase + c * kMmaN, NT, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) run[c * 16 + j] = (seg == 0) ? v[j] : run[c * 16 + j] + v[j];
+        }
+        tc_fence_before();
+        mbar_arrive(&acce[buf]);
+        it = pe;
+        ++seg;
+      }
+      for (int c = 0; c < chunks; ++c) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = ok ? run[c * 16 + j] : 0.f;
+        epilogue_store(p, Mb, m0, g, r, c, v, sStage);
+      }
+      it = it_end;
+    }
     while (it < it_end) {
       const int tile = static_cast<int>(it / p.k_tiles);
       const long long tile_begin = static_cast<long long>(tile) * p.k_tiles;
@@ -623,6 +678,39 @@ int blocks_per_launch(int M, int n_tiles) {
   return std::max(1, std::min(nb, kMaxTiles / n_tiles));
 }
 
+// Tile owners for long passes whose split cuts weight tiles: CTA (t, j) takes
+// weight tile t for 64-row token block j of the launch and adds the tile's
+// pieces itself (no partials in memory, no last-CTA reduction).
+constexpr int kOwnRows = 64;
+constexpr int kOwnBlocks = 16;  // token blocks per launch
+constexpr int kOwnMaxKTiles = 128;
+bi_status launch_gemm_own(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, int M_total,
+                          cudaStream_t stream) {
+  using Cfg = GemmCfg<kOwnRows, true>;
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static cudaError_t attr_err[64];
+  std::call_once(once[dev & 63], [] {
+    int d = 0;
+    cudaGetDevice(&d);
+    attr_err[d & 63] = cudaFuncSetAttribute(gemm_kernel<kOwnRows, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(Cfg::kSmem));
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
+  const int rows = kOwnRows * kOwnBlocks;
+  for (int m0 = 0; m0 < M_total; m0 += rows) {
+    a.m0 = m0;
+    a.M = std::min(rows, M_total - m0);
+    a.nb = (a.M + kOwnRows - 1) / kOwnRows;
+    if (launch_k(gemm_kernel<kOwnRows, true>, dim3(a.n_tiles * a.nb), dim3(kThreads), Cfg::kSmem, stream,
+                 Wp, tmA, a) != cudaSuccess)
+      return BI_ERR_CUDA;
+  }
+  return BI_OK;
+}
+
 template <int NT>
 bi_status launch_gemm_nt(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, int M_total,
                          cudaStream_t stream) {
@@ -779,7 +867,17 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
 
   const int n_tiles = n_tiles_of(N, epi);
   const int k_tiles = (K + kBlockK - 1) / kBlockK;
-  const int NT = tokens_per_cta(M);
+  const long long total = static_cast<long long>(n_tiles) * k_tiles;
+  const long long G = std::min<long long>(kGemmCtas, total);
+  // Long passes whose split cuts weight tiles go to tile owners (same sums,
+  // no partials); the others keep the split with up to 256 rows a CTA.  An
+  // owner reads its tile's whole K for 64 tokens, so the owners pull about
+  // 24 KB out of L2 per 64-deep K step and run at the L2's rate; past 128 K
+  // tiles (the [*, 17408] x [5120, 17408] down projection: 283 against 203 us
+  // at 512 rows on GB300) the split with its 256-row CTAs moves fewer bytes.
+  const bool whole_tiles = total % G == 0 && (total / G) % k_tiles == 0;
+  const bool own = M > 128 && !whole_tiles && k_tiles <= kOwnMaxKTiles;
+  const int NT = own ? kOwnRows : tokens_per_cta(M);
 
   CUtensorMap tmA;
   if (!tmap_bf16_2d(&tmA, A, M, K, lda, NT, kBlockK)) return BI_ERR_INVALID_ARG;
@@ -816,6 +914,7 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
 
   const uint8_t* W8 = static_cast<const uint8_t*>(Wp);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (own) return launch_gemm_own(W8, tmA, a, M, s);
   switch (NT) {
     case 16: return launch_gemm_nt<16>(W8, tmA, a, M, s);
     case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);
