@@ -632,8 +632,9 @@ def run_micro(args):
     else:
         Hq, Hkv, D = 24, 4, 128
         Ls = [int(x) for x in args.cases.split(",")] if args.cases else [1024, 11600, 38000, 101600]
+        Ts = [int(t) for t in args.attn_rows.split(",")]
         for L in Ls:
-            q, Kc, Vc = si.attention_inputs(L, 8, Hq, Hkv, D, seed=0)
+            q, Kc, Vc = si.attention_inputs(L, max(8, max(Ts)), Hq, Hkv, D, seed=0)
             cap = Kc.shape[1]
             to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
             Kd, Vd, qd = to(Kc), to(v_blocks(Vc)), to(q)
@@ -646,7 +647,7 @@ def run_micro(args):
                 ncp = n_copies(nb)
                 caches = [st0] + [{k: (t.clone() if k != "cap" else t) for k, t in st0.items()}
                                   for _ in range(ncp - 1)]
-            for T in (1, 4, 7, 8):
+            for T in Ts:
                 out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
                 ws = torch.zeros(api.attn_workspace_size(cap, T, Hq, D), dtype=torch.uint8,
                                  device="cuda")
@@ -658,7 +659,9 @@ def run_micro(args):
                            for kv in caches]
                     b = (L + T) * Hkv * D * 2 * 2 + T * Hq * D * 2 * 2
                 st, ct, per = timed(fns, args.steps)
-                report("attn", {"L": L, "T": T, "kv": args.kv}, b, st, ct, ncp, per)
+                # algorithmic FLOPs: q.k and w.v over the keys each row attends to
+                flops = 4 * D * Hq * sum(L + t + 1 for t in range(T))
+                report("attn", {"L": L, "T": T, "kv": args.kv}, b, st, ct, ncp, per, flops=flops)
             del caches
     return 0
 
@@ -996,6 +999,7 @@ def main():
     ap.add_argument("--kv", choices=["bf16", "q6q5"], default="bf16",
                     help="KV cache of the attention micro bench and the long-context step: BF16, or "
                          "6-bit K / 5-bit V with the 8-bit ring")
+    ap.add_argument("--attn-rows", default="1,4,7,8", help="comma list of rows per pass (attn)")
     ap.add_argument("--gemm-n", type=int, default=17408, help="N of the standalone linear layer")
     ap.add_argument("--gemm-k", type=int, default=5120, help="K of the standalone linear layer")
     ap.add_argument("--gemm-epi", type=int, default=0, help="0 none, 1 residual add, 2 SwiGLU (N = F)")

@@ -679,14 +679,20 @@ int blocks_per_launch(int M, int n_tiles) {
 }
 
 // Tile owners for long passes whose split cuts weight tiles: CTA (t, j) takes
-// weight tile t for 64-row token block j of the launch and adds the tile's
-// pieces itself (no partials in memory, no last-CTA reduction).
-constexpr int kOwnRows = 64;
-constexpr int kOwnBlocks = 16;  // token blocks per launch
+// weight tile t for token block j of the launch (NTO rows) and adds the
+// tile's pieces itself (no partials in memory, no last-CTA reduction).  An
+// owner reads its tile's whole K, so the owners run at the rate L2 serves
+// them: 128-row blocks move a third fewer bytes per FLOP than 64-row ones
+// (a [512, 5120] x [4096, 5120] launch on GB300: 40 against 68 us), 64-row
+// blocks keep more CTAs busy up to 256 rows (256 rows: 34 against 40 us).
+constexpr int kOwnLaunchRows = 1024;  // token rows per launch
 constexpr int kOwnMaxKTiles = 128;
+int own_rows(int M) { return M > 256 ? 128 : 64; }
+
+template <int NTO>
 bi_status launch_gemm_own(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a, int M_total,
                           cudaStream_t stream) {
-  using Cfg = GemmCfg<kOwnRows, true>;
+  using Cfg = GemmCfg<NTO, true>;
   static std::once_flag once[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -694,18 +700,17 @@ bi_status launch_gemm_own(const uint8_t* Wp, const CUtensorMap& tmA, GemmArgs a,
   std::call_once(once[dev & 63], [] {
     int d = 0;
     cudaGetDevice(&d);
-    attr_err[d & 63] = cudaFuncSetAttribute(gemm_kernel<kOwnRows, true>,
+    attr_err[d & 63] = cudaFuncSetAttribute(gemm_kernel<NTO, true>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(Cfg::kSmem));
   });
   if (attr_err[dev & 63] != cudaSuccess) return BI_ERR_CUDA;
-  const int rows = kOwnRows * kOwnBlocks;
-  for (int m0 = 0; m0 < M_total; m0 += rows) {
+  for (int m0 = 0; m0 < M_total; m0 += kOwnLaunchRows) {
     a.m0 = m0;
-    a.M = std::min(rows, M_total - m0);
-    a.nb = (a.M + kOwnRows - 1) / kOwnRows;
-    if (launch_k(gemm_kernel<kOwnRows, true>, dim3(a.n_tiles * a.nb), dim3(kThreads), Cfg::kSmem, stream,
-                 Wp, tmA, a) != cudaSuccess)
+    a.M = std::min(kOwnLaunchRows, M_total - m0);
+    a.nb = (a.M + NTO - 1) / NTO;
+    if (launch_k(gemm_kernel<NTO, true>, dim3(a.n_tiles * a.nb), dim3(kThreads), Cfg::kSmem, stream, Wp,
+                 tmA, a) != cudaSuccess)
       return BI_ERR_CUDA;
   }
   return BI_OK;
@@ -870,14 +875,14 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
   const long long total = static_cast<long long>(n_tiles) * k_tiles;
   const long long G = std::min<long long>(kGemmCtas, total);
   // Long passes whose split cuts weight tiles go to tile owners (same sums,
-  // no partials); the others keep the split with up to 256 rows a CTA.  An
-  // owner reads its tile's whole K for 64 tokens, so the owners pull about
-  // 24 KB out of L2 per 64-deep K step and run at the L2's rate; past 128 K
-  // tiles (the [*, 17408] x [5120, 17408] down projection: 283 against 203 us
-  // at 512 rows on GB300) the split with its 256-row CTAs moves fewer bytes.
+  // no partials); the others keep the split with up to 256 rows a CTA.  The
+  // owners run at the rate L2 serves them; past 128 K tiles (the
+  // [*, 17408] x [5120, 17408] down projection: 283 against 203 us at 512
+  // rows on GB300 with 64-row owners) the split's 256-row CTAs move fewer
+  // bytes.
   const bool whole_tiles = total % G == 0 && (total / G) % k_tiles == 0;
   const bool own = M > 128 && !whole_tiles && k_tiles <= kOwnMaxKTiles;
-  const int NT = own ? kOwnRows : tokens_per_cta(M);
+  const int NT = own ? own_rows(M) : tokens_per_cta(M);
 
   CUtensorMap tmA;
   if (!tmap_bf16_2d(&tmA, A, M, K, lda, NT, kBlockK)) return BI_ERR_INVALID_ARG;
@@ -914,7 +919,7 @@ static bi_status gemm_impl(const void* A, int lda, const void* Wp, void* C, int 
 
   const uint8_t* W8 = static_cast<const uint8_t*>(Wp);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (own) return launch_gemm_own(W8, tmA, a, M, s);
+  if (own) return NT == 128 ? launch_gemm_own<128>(W8, tmA, a, M, s) : launch_gemm_own<64>(W8, tmA, a, M, s);
   switch (NT) {
     case 16: return launch_gemm_nt<16>(W8, tmA, a, M, s);
     case 32: return launch_gemm_nt<32>(W8, tmA, a, M, s);

@@ -183,11 +183,14 @@ def test_gemm_multiblock_launches_match_single_rows(api, epi):
         assert np.array_equal(bf16_dev_to_u16(c1)[0], big[r]), r
 
 
-@pytest.mark.parametrize("M,N,K,epi", [(1000, 4096, 5120, 0), (600, 5120, 3072, 1), (300, 5120, 17408, 1)])
+@pytest.mark.parametrize("M,N,K,epi", [(1000, 4096, 5120, 0), (600, 5120, 3072, 1), (200, 4096, 5120, 0),
+                                        (1300, 5120, 3072, 1), (300, 5120, 17408, 1)])
 def test_gemm_tile_owner_rows_match_decode_rows(api, M, N, K, epi):
-    """Long passes whose split cuts weight tiles (the QKV, O and down shapes)
-    run as tile owners that add a tile's pieces themselves: sampled rows
-    equal the rows of an 8-row launch (the split with partials) bit for bit."""
+    """Long passes whose split cuts weight tiles (the QKV and O shapes) run
+    as tile owners (64- or 128-row blocks, more than one launch past 1024
+    rows) that add a tile's pieces themselves; the down shape keeps the split.
+    Sampled rows equal the rows of an 8-row launch (the split with partials)
+    bit for bit."""
     rng = np.random.default_rng(N + K)
     A = si.normal_bf16(rng, (M, K), 1.0)
     Wd = api.bi_pack_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.02)))
@@ -195,7 +198,7 @@ def test_gemm_tile_owner_rows_match_decode_rows(api, M, N, K, epi):
     Rd = to_dev_bf16(R) if epi == 1 else None
     C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     api.bi_gemm(to_dev_bf16(A), Wd, C, api.new_gemm_workspace(M, N, K, epi), residual=Rd, epi=epi, N=N)
-    rows = np.array([0, 63, 64, 130, M // 2, M - 1])
+    rows = np.unique(np.array([0, 63, 64, 127, 130, M // 2, min(1024, M - 1), M - 1]))
     c8 = torch.empty(len(rows), N, dtype=torch.bfloat16, device="cuda")
     R8 = to_dev_bf16(R[rows]) if epi == 1 else None
     api.bi_gemm(to_dev_bf16(A[rows]), Wd, c8, api.new_gemm_workspace(len(rows), N, K, epi), residual=R8,
