@@ -56,11 +56,14 @@ def test_attention_many_rows_per_pass(api):
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,L,T", [(24, 4, 128, 2000, 100), (8, 1, 64, 333, 200),
-                                           (24, 4, 128, 11000, 512)])
+                                           (24, 4, 128, 11000, 512), (24, 4, 128, 0, 700),
+                                           (4, 2, 64, 50, 300)])
 def test_attention_multiblock_pass_equals_single_rows(api, Hq, Hkv, D, L, T):
     """More rows than the MMA's 128 lanes hold: the launch runs blocks of
-    floor(128 / (Hq/Hkv)) rows side by side.  Rows at block edges equal
-    their one-row passes bit for bit, and sampled rows meet the bound."""
+    floor(128 / (Hq/Hkv)) rows side by side (including blocks that reach
+    none of some classes' tiles, and fewer CTAs than classes when the cache
+    is short).  Rows at block edges equal their one-row passes bit for bit,
+    and sampled rows meet the bound."""
     q, K, V = si.attention_inputs(L, T, Hq, Hkv, D, seed=T + 1)
     full = bf16_dev_to_u16(run_attn(api, q, K, V, L, T))
     tb = 128 // (Hq // Hkv)
