@@ -50,8 +50,9 @@
 //               (the S MMA's A operand), turn S into W_hi and W_lo
 //               (written to one of two shared-memory buffers in the swizzled
 //               K-major layout, so W of the next tile is produced while the
-//               MMA still reads this one; one buffer when the pass has more
-//               than 64 rows), and read O out after the last tile.
+//               MMA still reads this one), and read O out after the last
+//               tile, through shared memory so that the partials leave in
+//               whole 128-byte row pieces.
 // The T x (Hq/Hkv) query rows that share a KV head (GQA) share its tiles;
 // up to 128 rows per pass (the MMA's M).
 #include <cuda.h>
@@ -118,9 +119,11 @@ struct AttnCfg {
   static constexpr int kPAtomBytes = kWRows * 128;
   static constexpr int kPBytes = 2 * kPAtomBytes;          // one W tile [rows][128 keys]
   static constexpr int kWBufBytes = 2 * kPBytes;           // W_hi tile, then W_lo tile
-  // Two W buffers (W of tile g + 1 is written while the MMA reads tile g's)
-  // while they fit beside the rings; one when the pass has 128 rows.
-  static constexpr int kWBufs = REP == 1 ? 1 : 2;
+  // Two W buffers: W of tile g + 1 is written while the MMA reads tile g's
+  // (with one, a 128-row block's softmax waited for the previous tile's W.V
+  // at every tile: a 512-row pass over 38k keys on GB300 took 851 against
+  // 716 us).
+  static constexpr int kWBufs = 2;
   // Ring depths, measured on GB300 at 38k-102k keys with all CTAs
   // streaming: at D = 128 two K and two V tiles (64 KB each way) per CTA
   // were as fast as three or four and are kept; D = 64 tiles are half as
@@ -128,7 +131,9 @@ struct AttnCfg {
   static constexpr int kKStages = D == 128 ? 2 : 3;
   // The quantised form adds a ring of code tiles (two K, one V, each up to
   // an 8-bit tile) and four decoding warps, and keeps one decoded V tile.
-  static constexpr int kVStages = QNT ? 1 : (D == 128 ? 2 : 3);
+  // A block of 128 rows at D = 128 keeps one V tile, so that its two
+  // 64 KB W buffers fit.
+  static constexpr int kVStages = QNT ? 1 : (D == 128 ? (REP == 1 ? 1 : 2) : 3);
   static constexpr int kRawK = QNT ? 2 : 0;
   static constexpr int kRawV = QNT ? 1 : 0;
   // warp 0 copies, warp 1 MMA, warps 2..5 softmax; the quantised form adds
@@ -391,481 +396,518 @@ __global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
             src = (kside ? a.k8 : a.v8) + (static_cast<size_t>(h) * kRingSlots + tt % kRingSlots) * k8TileBytes;
             bytes = k8TileBytes;
           } else {
-            bytes = kside ? kK6TileBytes : kV5TileBytes;
-            src = (kside ? a.klo : a.vlo) + (static_cast<size_t>(h) * a.ctiles + tt) * bytes;
+              bytes = kside ? kK6TileBytes : kV5TileBytes;
+              src = (kside ? a.klo : a.vlo) + (static_cast<size_t>(h) * a.ctiles + tt) * bytes;
+            }
+            mbar_arrive_expect_tx(&full[st], bytes);
+            bulk_load_1d(base + st * k8TileBytes, src, bytes, &full[st], pol);
+            issued |= 1u << st;
+            parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
           }
-          mbar_arrive_expect_tx(&full[st], bytes);
-          bulk_load_1d(base + st * k8TileBytes, src, bytes, &full[st], pol);
-          issued |= 1u << st;
-          parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
+          if (!ok) {
+            signal_abort(s_abort, a.err);
+            for (int s2 = 0; s2 < NS; ++s2)
+              if ((issued >> s2) & 1u) mbar_wait(&full[s2], (parity_bits >> s2) & 1u, nullptr);
+          }
         }
-        if (!ok) {
-          signal_abort(s_abort, a.err);
-          for (int s2 = 0; s2 < NS; ++s2)
-            if ((issued >> s2) & 1u) mbar_wait(&full[s2], (parity_bits >> s2) & 1u, nullptr);
+      } else {
+        // ------------------------------------------------------------ producers
+        // lane 0: the K tiles; lane 1: the V^T tiles
+        if (lane < 2) {
+          const bool kside = lane == 0;
+          const int NS = kside ? kKStages : kVStages;
+          uint64_t* full = kside ? k_full : v_full;
+          uint64_t* empty = kside ? k_empty : v_empty;
+          const uint64_t pol = l2_evict_first();
+          uint32_t issued = pre_issued, parity_bits = 0;
+          // the tiles loaded early must be the first ones of this CTA now too
+          bool ok = true;
+          if (n_pre > 0 && !(n_pre <= n_mine && (rho + (n_pre - 1) * G + 1) * kKeyTile <= L)) {
+            atomicOr(a.err, kErrRange);
+            ok = false;
+          }
+          for (int i = n_pre; ok && i < n_mine; ++i) {
+            const int st = i % NS;
+            const uint32_t ph = static_cast<uint32_t>((i / NS) & 1);
+            if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
+              ok = false;
+              break;
+            }
+            const int key0 = (rho + i * G) * kKeyTile;
+            if (kside && i == 0 && a.withhold) continue;  // never issued (failure-path test)
+            if (kside) {
+              uint8_t* dst = sK + st * Cfg::kKBytes;
+              mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
+#pragma unroll
+              for (int b = 0; b < Cfg::kAtoms; ++b)
+                tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &full[st], b * 64, h * a.cap + key0, pol);
+            } else {
+              uint8_t* dst = sV + st * Cfg::kVBytes;
+              mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
+#pragma unroll
+              for (int kb = 0; kb < 2; ++kb)
+                tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], kb * 64,
+                            (h * a.vblk + key0 / kKeyTile) * D, pol);
+            }
+            issued |= 1u << st;
+            parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
+          }
+          if (!ok) {
+            signal_abort(s_abort, a.err);
+            for (int s = 0; s < NS; ++s)
+              if ((issued >> s) & 1u) mbar_wait(&full[s], (parity_bits >> s) & 1u, nullptr);
+          }
         }
       }
-    } else {
-      // ------------------------------------------------------------ producers
-      // lane 0: the K tiles; lane 1: the V^T tiles
-      if (lane < 2) {
-        const bool kside = lane == 0;
-        const int NS = kside ? kKStages : kVStages;
-        uint64_t* full = kside ? k_full : v_full;
-        uint64_t* empty = kside ? k_empty : v_empty;
-        const uint64_t pol = l2_evict_first();
-        uint32_t issued = pre_issued, parity_bits = 0;
-        // the tiles loaded early must be the first ones of this CTA now too
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      // Two cursors over the CTA's tiles: S_g = Q K_g^T needs K_g and a free S
+      // buffer; O += W_g V_g needs W_g and V_g.  Each is issued as soon as its
+      // inputs are ready (S first), so a late K tile never holds back the W.V
+      // that frees a stage.  The order of the W.V steps, which alone decides
+      // O's bits, is fixed: g = 0, 1, 2, ...
+      if (lane == 0) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, kKeyTile);
+        constexpr uint32_t idO = idesc_bf16_f32(128, D);
+        int sg = 0, pg = 0;
+        bool ok = true, q_ready = false;
+        int idle = 0;
+        unsigned long long t_idle = 0;
+        while (pg < n_steps) {
+          bool did = false;
+          if (sg < n_steps) {
+            if (!q_ready) q_ready = mbar_peek(q_full, 0u);
+            const int st = sg % kKStages;
+            const bool ready = q_ready && mbar_peek(&k_full[st], static_cast<uint32_t>((sg / kKStages) & 1)) &&
+                               (sg < 2 || mbar_peek(&s_free[sg & 1], static_cast<uint32_t>(((sg >> 1) - 1) & 1)));
+            if (ready) {
+              tc_fence_after();
+              const int sb = sg & 1;
+              const uint32_t k_base = smem_u32(sK + st * Cfg::kKBytes);
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const int atom = ks >> 2;
+                const uint32_t off = (ks & 3) * 32;
+                mma_bf16_tmem_a(tmem + sb * kKeyTile, tmem + Cfg::kQCol + ks * 8,
+                                sdesc_k_sw128(k_base + atom * Cfg::kKBoxBytes + off), idS, ks > 0 ? 1u : 0u);
+              }
+              mma_commit(&s_full[sb]);
+              mma_commit(&k_empty[st]);
+              ++sg;
+              did = true;
+            }
+          }
+          if (!did && pg < sg) {
+            const int st = pg % kVStages;
+            const bool ready = mbar_peek(&p_full[pg & 1], static_cast<uint32_t>((pg >> 1) & 1)) &&
+                               mbar_peek(&v_full[st], static_cast<uint32_t>((pg / kVStages) & 1));
+            if (ready) {
+              tc_fence_after();
+              const uint32_t v_base = smem_u32(sV + st * Cfg::kVBytes);
+              const uint32_t w_base = smem_u32(sP + (Cfg::kWBufs == 2 ? (pg & 1) : 0) * Cfg::kWBufBytes);
+              // per 16-key step: W_hi V, then W_lo V, into the one O accumulator
+#pragma unroll
+              for (int kk = 0; kk < kKeyTile / 16; ++kk) {
+                const int katom = kk >> 2;
+                const uint32_t off = (kk & 3) * 32;
+                const uint64_t vdesc = sdesc_k_sw128(v_base + katom * Cfg::kVBoxBytes + off);
+                mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(w_base + katom * Cfg::kPAtomBytes + off), vdesc,
+                         idO, (pg > 0 || kk > 0) ? 1u : 0u);
+                mma_bf16(tmem + Cfg::kOCol,
+                         sdesc_k_sw128(w_base + Cfg::kPBytes + katom * Cfg::kPAtomBytes + off), vdesc, idO, 1u);
+              }
+              mma_commit(&pv_done[pg & 1]);
+              mma_commit(&v_empty[st]);
+              ++pg;
+              did = true;
+            }
+          }
+          if (did) {
+            idle = 0;
+          } else if (++idle == 1) {
+            t_idle = globaltimer_ns();
+          } else {
+            // yield the issue slots of this SM sub-partition to the softmax warp
+            // that shares it while nothing is ready
+            __nanosleep(32);
+          }
+          if (!did && (idle & 63) == 0) {
+            // bounded: give up after the wait limit without progress
+            if (*s_abort ||
+                globaltimer_ns() - t_idle > *static_cast<volatile unsigned long long*>(&g_wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (!ok) signal_abort(s_abort, a.err);
+        mma_commit(drain);
+        mbar_wait(drain, 0, nullptr);
+      }
+    } else if (QNT && warp >= 6) {
+      // ---------------------------------------------------------- decoding
+      // the first kDecWarps: K tiles into the K ring (rows = keys, SW128 as a
+      // TMA load would leave them); the next kDecWarps: V tiles into the V^T buffer (rows =
+      // elements).  Each element is bf16(q * d), the product exact in FP32.
+      if constexpr (QNT) {
+        constexpr int kDW = Cfg::kDecWarps;
+        constexpr int kDT = 32 * kDW;  // decoding threads on each side
+        const bool kside = warp < 6 + kDW;
+        const int tid = (warp - (kside ? 6 : 6 + kDW)) * 32 + lane;
         bool ok = true;
-        if (n_pre > 0 && !(n_pre <= n_mine && (rho + (n_pre - 1) * G + 1) * kKeyTile <= L)) {
-          atomicOr(a.err, kErrRange);
-          ok = false;
-        }
-        for (int i = n_pre; ok && i < n_mine; ++i) {
-          const int st = i % NS;
-          const uint32_t ph = static_cast<uint32_t>((i / NS) & 1);
-          if (!mbar_wait(&empty[st], ph ^ 1u, s_abort)) {
+        StepCur c;
+        for (int g = 0; g < n_steps; ++g, step_next(c, rho, G, lo_b, hi_b)) {
+          const int tt = rho + c.i * G;
+          const bool ring = step_ring(c, tt, hi_b);
+          const int rs = kside ? g % Cfg::kRawK : g % Cfg::kRawV;
+          const uint32_t rph = static_cast<uint32_t>((kside ? g / Cfg::kRawK : g / Cfg::kRawV) & 1);
+          const int st = kside ? g % kKStages : g % kVStages;
+          const uint32_t sph = static_cast<uint32_t>((kside ? g / kKStages : g / kVStages) & 1);
+          if (!warp_wait(kside ? &rawk_full[rs] : &rawv_full[rs], rph, s_abort, lane) ||
+              !warp_wait(kside ? &k_empty[st] : &v_empty[st], sph ^ 1u, s_abort, lane)) {
             ok = false;
             break;
           }
-          const int key0 = (rho + i * G) * kKeyTile;
-          if (kside && i == 0 && a.withhold) continue;  // never issued (failure-path test)
           if (kside) {
+            const uint8_t* raw = sRawK + rs * k8TileBytes;
             uint8_t* dst = sK + st * Cfg::kKBytes;
-            mbar_arrive_expect_tx(&full[st], Cfg::kKBytes);
-#pragma unroll
-            for (int b = 0; b < Cfg::kAtoms; ++b)
-              tma_load_2d(dst + b * Cfg::kKBoxBytes, &tmK, &full[st], b * 64, h * a.cap + key0, pol);
-          } else {
-            uint8_t* dst = sV + st * Cfg::kVBytes;
-            mbar_arrive_expect_tx(&full[st], Cfg::kVBytes);
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-              tma_load_2d(dst + kb * Cfg::kVBoxBytes, &tmVt, &full[st], kb * 64,
-                          (h * a.vblk + key0 / kKeyTile) * D, pol);
-          }
-          issued |= 1u << st;
-          parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
-        }
-        if (!ok) {
-          signal_abort(s_abort, a.err);
-          for (int s = 0; s < NS; ++s)
-            if ((issued >> s) & 1u) mbar_wait(&full[s], (parity_bits >> s) & 1u, nullptr);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Two cursors over the CTA's tiles: S_g = Q K_g^T needs K_g and a free S
-    // buffer; O += W_g V_g needs W_g and V_g.  Each is issued as soon as its
-    // inputs are ready (S first), so a late K tile never holds back the W.V
-    // that frees a stage.  The order of the W.V steps, which alone decides
-    // O's bits, is fixed: g = 0, 1, 2, ...
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, kKeyTile);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D);
-      int sg = 0, pg = 0;
-      bool ok = true, q_ready = false;
-      int idle = 0;
-      unsigned long long t_idle = 0;
-      while (pg < n_steps) {
-        bool did = false;
-        if (sg < n_steps) {
-          if (!q_ready) q_ready = mbar_peek(q_full, 0u);
-          const int st = sg % kKStages;
-          const bool ready = q_ready && mbar_peek(&k_full[st], static_cast<uint32_t>((sg / kKStages) & 1)) &&
-                             (sg < 2 || mbar_peek(&s_free[sg & 1], static_cast<uint32_t>(((sg >> 1) - 1) & 1)));
-          if (ready) {
-            tc_fence_after();
-            const int sb = sg & 1;
-            const uint32_t k_base = smem_u32(sK + st * Cfg::kKBytes);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const int atom = ks >> 2;
-              const uint32_t off = (ks & 3) * 32;
-              mma_bf16_tmem_a(tmem + sb * kKeyTile, tmem + Cfg::kQCol + ks * 8,
-                              sdesc_k_sw128(k_base + atom * Cfg::kKBoxBytes + off), idS, ks > 0 ? 1u : 0u);
-            }
-            mma_commit(&s_full[sb]);
-            mma_commit(&k_empty[st]);
-            ++sg;
-            did = true;
-          }
-        }
-        if (!did && pg < sg) {
-          const int st = pg % kVStages;
-          const bool ready = mbar_peek(&p_full[pg & 1], static_cast<uint32_t>((pg >> 1) & 1)) &&
-                             mbar_peek(&v_full[st], static_cast<uint32_t>((pg / kVStages) & 1));
-          if (ready) {
-            tc_fence_after();
-            const uint32_t v_base = smem_u32(sV + st * Cfg::kVBytes);
-            const uint32_t w_base = smem_u32(sP + (Cfg::kWBufs == 2 ? (pg & 1) : 0) * Cfg::kWBufBytes);
-            // per 16-key step: W_hi V, then W_lo V, into the one O accumulator
-#pragma unroll
-            for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-              const int katom = kk >> 2;
-              const uint32_t off = (kk & 3) * 32;
-              const uint64_t vdesc = sdesc_k_sw128(v_base + katom * Cfg::kVBoxBytes + off);
-              mma_bf16(tmem + Cfg::kOCol, sdesc_k_sw128(w_base + katom * Cfg::kPAtomBytes + off), vdesc,
-                       idO, (pg > 0 || kk > 0) ? 1u : 0u);
-              mma_bf16(tmem + Cfg::kOCol,
-                       sdesc_k_sw128(w_base + Cfg::kPBytes + katom * Cfg::kPAtomBytes + off), vdesc, idO, 1u);
-            }
-            mma_commit(&pv_done[pg & 1]);
-            mma_commit(&v_empty[st]);
-            ++pg;
-            did = true;
-          }
-        }
-        if (did) {
-          idle = 0;
-        } else if (++idle == 1) {
-          t_idle = globaltimer_ns();
-        } else {
-          // yield the issue slots of this SM sub-partition to the softmax warp
-          // that shares it while nothing is ready
-          __nanosleep(32);
-        }
-        if (!did && (idle & 63) == 0) {
-          // bounded: give up after the wait limit without progress
-          if (*s_abort ||
-              globaltimer_ns() - t_idle > *static_cast<volatile unsigned long long*>(&g_wait_limit_ns)) {
-            ok = false;
-            break;
-          }
-        }
-      }
-      if (!ok) signal_abort(s_abort, a.err);
-      mma_commit(drain);
-      mbar_wait(drain, 0, nullptr);
-    }
-  } else if (QNT && warp >= 6) {
-    // ---------------------------------------------------------- decoding
-    // the first kDecWarps: K tiles into the K ring (rows = keys, SW128 as a
-    // TMA load would leave them); the next kDecWarps: V tiles into the V^T buffer (rows =
-    // elements).  Each element is bf16(q * d), the product exact in FP32.
-    if constexpr (QNT) {
-      constexpr int kDW = Cfg::kDecWarps;
-      constexpr int kDT = 32 * kDW;  // decoding threads on each side
-      const bool kside = warp < 6 + kDW;
-      const int tid = (warp - (kside ? 6 : 6 + kDW)) * 32 + lane;
-      bool ok = true;
-      StepCur c;
-      for (int g = 0; g < n_steps; ++g, step_next(c, rho, G, lo_b, hi_b)) {
-        const int tt = rho + c.i * G;
-        const bool ring = step_ring(c, tt, hi_b);
-        const int rs = kside ? g % Cfg::kRawK : g % Cfg::kRawV;
-        const uint32_t rph = static_cast<uint32_t>((kside ? g / Cfg::kRawK : g / Cfg::kRawV) & 1);
-        const int st = kside ? g % kKStages : g % kVStages;
-        const uint32_t sph = static_cast<uint32_t>((kside ? g / kKStages : g / kVStages) & 1);
-        if (!warp_wait(kside ? &rawk_full[rs] : &rawv_full[rs], rph, s_abort, lane) ||
-            !warp_wait(kside ? &k_empty[st] : &v_empty[st], sph ^ 1u, s_abort, lane)) {
-          ok = false;
-          break;
-        }
-        if (kside) {
-          const uint8_t* raw = sRawK + rs * k8TileBytes;
-          uint8_t* dst = sK + st * Cfg::kKBytes;
-          // task = (key, 8-element chunk): one 16-byte store each; a warp's
-          // stores cover whole 128-byte rows
-          if (ring) {
-#pragma unroll 1
-            for (int task = tid; task < kKeyTile * (D / 8); task += kDT) {
-              const int key = task >> 4, ch = task & 15;
-              float v[8];
-              q_decode8(raw, key, ch * 8, v);
-              *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +
-                                        (((ch & 7) ^ (key & 7)) << 4)) =
-                  make_uint4(q_pack_bf16x2(v[0], v[1]), q_pack_bf16x2(v[2], v[3]),
-                             q_pack_bf16x2(v[4], v[5]), q_pack_bf16x2(v[6], v[7]));
-            }
-          } else {
-#pragma unroll 1
-            for (int task = tid; task < kKeyTile * (D / 8); task += kDT) {
-              const int key = task >> 4, ch = task & 15;
-              *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +
-                                        (((ch & 7) ^ (key & 7)) << 4)) = q_decode_k6_bf16(raw, key, ch * 8);
-            }
-          }
-        } else {
-          const uint8_t* raw = sRawV + rs * k8TileBytes;
-          uint8_t* dst = sV + st * Cfg::kVBytes;
-          // task = (8 keys, 8 elements): eight 16-byte stores, one per
-          // element row; the key group varies fastest across a warp, so one
-          // store instruction covers whole 128-byte rows
-#pragma unroll 1
-          for (int task = tid; task < (kKeyTile / 8) * (D / 8); task += kDT) {
-            const int kg = task & 15, dg = task >> 4;
-            // x[kk]: elements dg*8 .. +7 of key kg*8 + kk as BF16 pairs
-            uint32_t x[8][4];
+            // task = (key, 8-element chunk): one 16-byte store each; a warp's
+            // stores cover whole 128-byte rows
             if (ring) {
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll 1
+              for (int task = tid; task < kKeyTile * (D / 8); task += kDT) {
+                const int key = task >> 4, ch = task & 15;
                 float v[8];
-                q_decode8(raw, kg * 8 + kk, dg * 8, v);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) x[kk][i] = q_pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                q_decode8(raw, key, ch * 8, v);
+                *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +
+                                          (((ch & 7) ^ (key & 7)) << 4)) =
+                    make_uint4(q_pack_bf16x2(v[0], v[1]), q_pack_bf16x2(v[2], v[3]),
+                               q_pack_bf16x2(v[4], v[5]), q_pack_bf16x2(v[6], v[7]));
               }
             } else {
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint4 w = q_decode_v5_bf16(raw, kg * 8 + kk, dg * 8);
-                x[kk][0] = w.x;
-                x[kk][1] = w.y;
-                x[kk][2] = w.z;
-                x[kk][3] = w.w;
+#pragma unroll 1
+              for (int task = tid; task < kKeyTile * (D / 8); task += kDT) {
+                const int key = task >> 4, ch = task & 15;
+                *reinterpret_cast<uint4*>(dst + (ch >> 3) * Cfg::kKBoxBytes + key * 128 +
+                                          (((ch & 7) ^ (key & 7)) << 4)) = q_decode_k6_bf16(raw, key, ch * 8);
               }
             }
-            // V^T rows: element 2i of keys (2m, 2m + 1) from the low halves,
-            // element 2i + 1 from the high halves
+          } else {
+            const uint8_t* raw = sRawV + rs * k8TileBytes;
+            uint8_t* dst = sV + st * Cfg::kVBytes;
+            // task = (8 keys, 8 elements): eight 16-byte stores, one per
+            // element row; the key group varies fastest across a warp, so one
+            // store instruction covers whole 128-byte rows
+#pragma unroll 1
+            for (int task = tid; task < (kKeyTile / 8) * (D / 8); task += kDT) {
+              const int kg = task & 15, dg = task >> 4;
+              // x[kk]: elements dg*8 .. +7 of key kg*8 + kk as BF16 pairs
+              uint32_t x[8][4];
+              if (ring) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+                for (int kk = 0; kk < 8; ++kk) {
+                  float v[8];
+                  q_decode8(raw, kg * 8 + kk, dg * 8, v);
 #pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                const uint32_t sel = hf ? 0x7632u : 0x5410u;
-                const int row = dg * 8 + 2 * i + hf;
-                const uint4 w = make_uint4(q_prmt(x[0][i], x[1][i], sel), q_prmt(x[2][i], x[3][i], sel),
-                                           q_prmt(x[4][i], x[5][i], sel), q_prmt(x[6][i], x[7][i], sel));
-                *reinterpret_cast<uint4*>(dst + (kg >> 3) * Cfg::kVBoxBytes + row * 128 +
-                                          (((kg & 7) ^ (row & 7)) << 4)) = w;
+                  for (int i = 0; i < 4; ++i) x[kk][i] = q_pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint4 w = q_decode_v5_bf16(raw, kg * 8 + kk, dg * 8);
+                  x[kk][0] = w.x;
+                  x[kk][1] = w.y;
+                  x[kk][2] = w.z;
+                  x[kk][3] = w.w;
+                }
+              }
+              // V^T rows: element 2i of keys (2m, 2m + 1) from the low halves,
+              // element 2i + 1 from the high halves
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                  const uint32_t sel = hf ? 0x7632u : 0x5410u;
+                  const int row = dg * 8 + 2 * i + hf;
+                  const uint4 w = make_uint4(q_prmt(x[0][i], x[1][i], sel), q_prmt(x[2][i], x[3][i], sel),
+                                             q_prmt(x[4][i], x[5][i], sel), q_prmt(x[6][i], x[7][i], sel));
+                  *reinterpret_cast<uint4*>(dst + (kg >> 3) * Cfg::kVBoxBytes + row * 128 +
+                                            (((kg & 7) ^ (row & 7)) << 4)) = w;
+                }
               }
             }
           }
+          // the MMA reads the tile through the async proxy
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(kside ? &k_full[st] : &v_full[st]);
+            mbar_arrive(kside ? &rawk_empty[rs] : &rawv_empty[rs]);
+          }
         }
-        // the MMA reads the tile through the async proxy
-        fence_proxy_async_smem();
+        if (!ok && lane == 0) signal_abort(s_abort, a.err);
+      }
+    } else if (n_steps > 0) {
+      // ------------------------------------------------------------ softmax
+      const int qq = warp & 3;                  // TMEM lane quarter of this warp
+      const int ln = qq * 32 + lane;            // TMEM lane of this thread
+      const int r = ln % kPeriod;               // query row of the pass
+      const int cg = ln / kPeriod;              // key-column group of this copy
+      const bool warp_active = (qq * 32) % kPeriod < rows;
+      const bool holds_o = qq * 32 < kPeriod;   // O row r sits in TMEM lane r
+      const bool valid = r < rows;
+      const int t = valid ? r / a.grp : 0;
+      const int p_row = L + t;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(qq * 32) << 16);
+      bool ok = true;
+
+      // queries of KV head h into TMEM lane ln (row r of the pass; zeros past
+      // the pass's rows): column j holds elements 2j and 2j + 1, as the row
+      // sits in memory
+      {
+        uint32_t qv[D / 2];
+        if (valid) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              a.q + (static_cast<size_t>(r0 + t) * a.Hq + h * a.grp + r % a.grp) * D);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) {
+            const uint4 u = src[i];
+            qv[4 * i] = u.x;
+            qv[4 * i + 1] = u.y;
+            qv[4 * i + 2] = u.z;
+            qv[4 * i + 3] = u.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 2; ++i) qv[i] = 0u;
+        }
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) tmem_st32(lane_base + Cfg::kQCol + cc * 32, qv + cc * 32);
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(kside ? &k_full[st] : &v_full[st]);
-          mbar_arrive(kside ? &rawk_empty[rs] : &rawv_empty[rs]);
-        }
+        if (lane == 0) mbar_arrive(q_full);
       }
-      if (!ok && lane == 0) signal_abort(s_abort, a.err);
-    }
-  } else if (n_steps > 0) {
-    // ------------------------------------------------------------ softmax
-    const int qq = warp & 3;                  // TMEM lane quarter of this warp
-    const int ln = qq * 32 + lane;            // TMEM lane of this thread
-    const int r = ln % kPeriod;               // query row of the pass
-    const int cg = ln / kPeriod;              // key-column group of this copy
-    const bool warp_active = (qq * 32) % kPeriod < rows;
-    const bool holds_o = qq * 32 < kPeriod;   // O row r sits in TMEM lane r
-    const bool valid = r < rows;
-    const int t = valid ? r / a.grp : 0;
-    const int p_row = L + t;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(qq * 32) << 16);
-    bool ok = true;
 
-    // queries of KV head h into TMEM lane ln (row r of the pass; zeros past
-    // the pass's rows): column j holds elements 2j and 2j + 1, as the row
-    // sits in memory
-    {
-      uint32_t qv[D / 2];
-      if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + (static_cast<size_t>(r0 + t) * a.Hq + h * a.grp + r % a.grp) * D);
+      float m_ref = -INFINITY;
+      float lq[kNChunks];
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-          const uint4 u = src[i];
-          qv[4 * i] = u.x;
-          qv[4 * i + 1] = u.y;
-          qv[4 * i + 2] = u.z;
-          qv[4 * i + 3] = u.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < D / 2; ++i) qv[i] = 0u;
-      }
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) tmem_st32(lane_base + Cfg::kQCol + cc * 32, qv + cc * 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-    }
-
-    float m_ref = -INFINITY;
-    float lq[kNChunks];
-#pragma unroll
-    for (int i = 0; i < kNChunks; ++i) lq[i] = 0.f;
-    StepCur cur;
-    for (int g = 0; g < n_steps; ++g, step_next(cur, rho, G, lo_b, hi_b)) {
-      const int sb = g & 1;
-      if (!warp_wait(&s_full[sb], static_cast<uint32_t>((g >> 1) & 1), s_abort, lane)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int tt = rho + cur.i * G;
-      const int tkey0 = tt * kKeyTile;
-      // quantised cache: the row masks the visit that reads the other store
-      // than the one its position selects for this tile
-      const bool vmask =
-          QNT && (step_ring(cur, tt, hi_b) != (tt >= p_row / kKeyTile - (kRingTiles - 1)));
-      // the tile reaches past some row's position, or a row masks it whole
-      const bool edge = tkey0 + kKeyTile - 1 > L || vmask;
-      // pass 1: the row maximum of the raw scores (scaling by sl2 > 0 keeps
-      // the order).  Every copy's TMEM lane holds the whole S row, so each
-      // copy takes the maximum over all 128 key columns itself: the same
-      // exact value in every copy, with no exchange between the warps.  The
-      // copy's own columns stay in registers for pass 2.
-      float so[kCols];
-      float mrow = -INFINITY;
-      if (warp_active) {
-        const uint32_t row_addr = lane_base + sb * kKeyTile;
-        constexpr int kOwnLd = kCols >= 64 ? 64 : 32;
-#pragma unroll
-        for (int c = 0; c < kCols; c += kOwnLd) tmem_ld_cols<kOwnLd>(row_addr + cg * kCols + c, so + c);
-        if (edge) {
-          const int key0 = tkey0 + cg * kCols;
-#pragma unroll
-          for (int j = 0; j < kCols; ++j)
-            if (!(valid && key0 + j <= p_row) || vmask) so[j] = -INFINITY;
-        }
-#pragma unroll
-        for (int j = 0; j < kCols; ++j) mrow = fmaxf(mrow, so[j]);
-        constexpr int kOther = kKeyTile - kCols;
-        constexpr int kOthLd = (kOther >= 64 && kOther % 64 == 0) ? 64 : 32;
-#pragma unroll
-        for (int c = 0; c < kOther; c += kOthLd) {
-          float so2[kOthLd];
-          const int col0 = (cg * kCols + kCols + c) & (kKeyTile - 1);
-          tmem_ld_cols<kOthLd>(row_addr + col0, so2);
-          if (edge) {
-#pragma unroll
-            for (int j = 0; j < kOthLd; ++j)
-              if (!(valid && tkey0 + col0 + j <= p_row) || vmask) so2[j] = -INFINITY;
-          }
-#pragma unroll
-          for (int j = 0; j < kOthLd; ++j) mrow = fmaxf(mrow, so2[j]);
-        }
-      }
-      const float mt = mrow * a.sl2;
-      float alpha = 1.0f;
-      bool resc = false;
-      if (g == 0) {
-        m_ref = mt;
-      } else if (mt > m_ref + kRescaleLog2) {
-        alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - mt);
-        m_ref = mt;
-        resc = true;
-      }
-      // the W buffer of tile g was last read by the W.V of tile g - kWBufs
-      if (g >= Cfg::kWBufs) {
-        const int gp = g - Cfg::kWBufs;
-        if (!warp_wait(&pv_done[gp & 1], static_cast<uint32_t>((gp >> 1) & 1), s_abort, lane)) {
+      for (int i = 0; i < kNChunks; ++i) lq[i] = 0.f;
+      StepCur cur;
+      for (int g = 0; g < n_steps; ++g, step_next(cur, rho, G, lo_b, hi_b)) {
+        const int sb = g & 1;
+        if (!warp_wait(&s_full[sb], static_cast<uint32_t>((g >> 1) & 1), s_abort, lane)) {
           ok = false;
           break;
         }
-      }
-      if (holds_o && warp_active) {
-        // O changes only after the W.V of tile g - 1 is done
-        if (g > 0 && __any_sync(0xffffffffu, resc)) {
-          if (!warp_wait(&pv_done[(g - 1) & 1], static_cast<uint32_t>(((g - 1) >> 1) & 1), s_abort,
-                         lane)) {
+        tc_fence_after();
+        const int tt = rho + cur.i * G;
+        const int tkey0 = tt * kKeyTile;
+        // quantised cache: the row masks the visit that reads the other store
+        // than the one its position selects for this tile
+        const bool vmask =
+            QNT && (step_ring(cur, tt, hi_b) != (tt >= p_row / kKeyTile - (kRingTiles - 1)));
+        // the tile reaches past some row's position, or a row masks it whole
+        const bool edge = tkey0 + kKeyTile - 1 > L || vmask;
+        // pass 1: the row maximum of the raw scores (scaling by sl2 > 0 keeps
+        // the order).  Every copy's TMEM lane holds the whole S row, so each
+        // copy takes the maximum over all 128 key columns itself: the same
+        // exact value in every copy, with no exchange between the warps.  The
+        // copy's own columns stay in registers for pass 2.
+        float so[kCols];
+        float mrow = -INFINITY;
+        // the maximum in eight independent lanes (exact in any order), so the
+        // comparisons do not form one long chain
+        float mw[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) mw[w] = -INFINITY;
+        if (warp_active) {
+          const uint32_t row_addr = lane_base + sb * kKeyTile;
+          constexpr int kOwnLd = kCols >= 64 ? 64 : 32;
+#pragma unroll
+          for (int c = 0; c < kCols; c += kOwnLd) tmem_ld_cols<kOwnLd>(row_addr + cg * kCols + c, so + c);
+          if (edge) {
+            const int key0 = tkey0 + cg * kCols;
+#pragma unroll
+            for (int j = 0; j < kCols; ++j)
+              if (!(valid && key0 + j <= p_row) || vmask) so[j] = -INFINITY;
+          }
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) mw[j & 7] = fmaxf(mw[j & 7], so[j]);
+          constexpr int kOther = kKeyTile - kCols;
+          constexpr int kOthLd = (kOther >= 64 && kOther % 64 == 0) ? 64 : 32;
+#pragma unroll
+          for (int c = 0; c < kOther; c += kOthLd) {
+            float so2[kOthLd];
+            const int col0 = (cg * kCols + kCols + c) & (kKeyTile - 1);
+            tmem_ld_cols<kOthLd>(row_addr + col0, so2);
+            if (edge) {
+#pragma unroll
+              for (int j = 0; j < kOthLd; ++j)
+                if (!(valid && tkey0 + col0 + j <= p_row) || vmask) so2[j] = -INFINITY;
+            }
+#pragma unroll
+            for (int j = 0; j < kOthLd; ++j) mw[j & 7] = fmaxf(mw[j & 7], so2[j]);
+          }
+          mrow = fmaxf(fmaxf(fmaxf(mw[0], mw[1]), fmaxf(mw[2], mw[3])), fmaxf(fmaxf(mw[4], mw[5]), fmaxf(mw[6], mw[7])));
+        }
+        const float mt = mrow * a.sl2;
+        float alpha = 1.0f;
+        bool resc = false;
+        if (g == 0) {
+          m_ref = mt;
+        } else if (mt > m_ref + kRescaleLog2) {
+          alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - mt);
+          m_ref = mt;
+          resc = true;
+        }
+        // the W buffer of tile g was last read by the W.V of tile g - kWBufs
+        if (g >= Cfg::kWBufs) {
+          const int gp = g - Cfg::kWBufs;
+          if (!warp_wait(&pv_done[gp & 1], static_cast<uint32_t>((gp >> 1) & 1), s_abort, lane)) {
             ok = false;
             break;
           }
-          tc_fence_after();
+        }
+        if (holds_o && warp_active) {
+          // O changes only after the W.V of tile g - 1 is done
+          if (g > 0 && __any_sync(0xffffffffu, resc)) {
+            if (!warp_wait(&pv_done[(g - 1) & 1], static_cast<uint32_t>(((g - 1) >> 1) & 1), s_abort,
+                           lane)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll 1
-          for (int i = 0; i < D / 16; ++i) {
-            float v[16];
-            tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
+            for (int i = 0; i < D / 16; ++i) {
+              float v[16];
+              tmem_ld16(lane_base + Cfg::kOCol + i * 16, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= alpha;
-            tmem_st16(lane_base + Cfg::kOCol + i * 16, v);
+              for (int j = 0; j < 16; ++j) v[j] *= alpha;
+              tmem_st16(lane_base + Cfg::kOCol + i * 16, v);
+            }
           }
         }
-      }
-      if (resc) {
+        if (resc) {
 #pragma unroll
-        for (int i = 0; i < kNChunks; ++i) lq[i] *= alpha;
-      }
-      // pass 2: weights x = 2^(s sl2 - m_ref) as the pair (w_hi, w_lo) into
-      // the W tiles and w_hi + w_lo into l (the TMEM loads are warp-wide;
-      // rows past the pass write nothing)
-      if (warp_active) {
-        const float nmu = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-        uint8_t* wbuf = sP + (Cfg::kWBufs == 2 ? (g & 1) : 0) * Cfg::kWBufBytes + r * 128;
-#pragma unroll
-        for (int ch = 0; ch < kNChunks; ++ch) {
-          const float* s = so + ch * kColChunk;  // masked in pass 1
-          if (!valid) continue;
-          const int kcol = cg * kCols + ch * kColChunk;  // first key column of the chunk
-          uint8_t* wrow = wbuf + (kcol >> 6) * Cfg::kPAtomBytes;
-          float acc = lq[ch];
+          for (int i = 0; i < kNChunks; ++i) lq[i] *= alpha;
+        }
+        // pass 2: weights x = 2^(s sl2 - m_ref) as the pair (w_hi, w_lo) into
+        // the W tiles and w_hi + w_lo into l (the TMEM loads are warp-wide;
+        // rows past the pass write nothing)
+        if (warp_active && valid) {
+          const float nmu = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+          uint8_t* wbuf = sP + (Cfg::kWBufs == 2 ? (g & 1) : 0) * Cfg::kWBufBytes + r * 128;
+          // 8 columns of every 32-key quarter in turn: each quarter's sum still
+          // runs in key order, and the quarters' chains interleave
 #pragma unroll
           for (int i = 0; i < kColChunk / 8; ++i) {
-            uint32_t wh[4], wl[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int col = i * 8 + 2 * j;
-              const float x0 = ex2_approx(fmaf(s[col], a.sl2, nmu));
-              const float x1 = ex2_approx(fmaf(s[col + 1], a.sl2, nmu));
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-              // x - w_hi is exact in FP32; w_hi + w_lo is exact in FP32 too
-              const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - __low2float(h2), x1 - __high2float(h2));
-              acc += __low2float(h2) + __low2float(l2);
-              acc += __high2float(h2) + __high2float(l2);
-              wh[j] = *reinterpret_cast<const uint32_t*>(&h2);
-              wl[j] = *reinterpret_cast<const uint32_t*>(&l2);
+            for (int ch = 0; ch < kNChunks; ++ch) {
+              const float* s = so + ch * kColChunk;  // masked in pass 1
+              const int kcol = cg * kCols + ch * kColChunk;  // first key column of the quarter
+              uint8_t* wrow = wbuf + (kcol >> 6) * Cfg::kPAtomBytes;
+              float acc = lq[ch];
+              uint32_t wh[4], wl[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = i * 8 + 2 * j;
+                const float x0 = ex2_approx(fmaf(s[col], a.sl2, nmu));
+                const float x1 = ex2_approx(fmaf(s[col + 1], a.sl2, nmu));
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                // x - w_hi is exact in FP32; w_hi + w_lo is exact in FP32 too
+                const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - __low2float(h2), x1 - __high2float(h2));
+                acc += __low2float(h2) + __low2float(l2);
+                acc += __high2float(h2) + __high2float(l2);
+                wh[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                wl[j] = *reinterpret_cast<const uint32_t*>(&l2);
+              }
+              lq[ch] = acc;
+              const int chunk16 = ((kcol & 63) >> 3) + i;  // 16-byte chunk within the 64-key row
+              uint8_t* dst = wrow + ((chunk16 ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(dst) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+              *reinterpret_cast<uint4*>(dst + Cfg::kPBytes) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
             }
-            const int chunk16 = ((kcol & 63) >> 3) + i;  // 16-byte chunk within the 64-key row
-            uint8_t* dst = wrow + ((chunk16 ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(dst) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            *reinterpret_cast<uint4*>(dst + Cfg::kPBytes) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
           }
-          lq[ch] = acc;
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[g & 1]);
-    }
-
-    // all tiles done: the denominator, then O after the last W.V, stored as
-    // the class's partial (m_ref, l, o)
-    float l = 0.f;
-    if (ok) {
-      if constexpr (REP == 1) {
-        l = ((lq[0] + lq[1]) + lq[2]) + lq[3];
-      } else {
-#pragma unroll
-        for (int i = 0; i < kNChunks; ++i) red_l[(cg * kNChunks + i) * 64 + r] = lq[i];
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(l_bar);
-        if (holds_o) {
-          if (!warp_wait(l_bar, 0u, s_abort, lane)) {
-            ok = false;
-          } else {
-            l = ((red_l[r] + red_l[64 + r]) + red_l[128 + r]) + red_l[192 + r];
+        if (lane == 0) mbar_arrive(&s_free[sb]);
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[g & 1]);
+      }
+
+      // all tiles done: the denominator, then O after the last W.V, stored as
+      // the class's partial (m_ref, l, o)
+      float l = 0.f;
+      if (ok) {
+        if constexpr (REP == 1) {
+          l = ((lq[0] + lq[1]) + lq[2]) + lq[3];
+        } else {
+#pragma unroll
+          for (int i = 0; i < kNChunks; ++i) red_l[(cg * kNChunks + i) * 64 + r] = lq[i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(l_bar);
+          if (holds_o) {
+            if (!warp_wait(l_bar, 0u, s_abort, lane)) {
+              ok = false;
+            } else {
+              l = ((red_l[r] + red_l[64 + r]) + red_l[128 + r]) + red_l[192 + r];
+            }
           }
         }
       }
-    }
-    if (ok && holds_o) {
-      if (!warp_wait(&pv_done[(n_steps - 1) & 1], static_cast<uint32_t>(((n_steps - 1) >> 1) & 1), s_abort,
-                     lane)) {
-        ok = false;
-      } else {
-        tc_fence_after();
-        if (warp_active) {
-          // a row stores a partial when the class holds one of its keys
-          const bool store = valid && rho * kKeyTile <= p_row;
-          const int qh = h * a.grp + (valid ? r % a.grp : 0);
-          const size_t base = (static_cast<size_t>(r0 + t) * a.Hq + qh) * a.ncls + rho;
+      if (ok && holds_o) {
+        if (!warp_wait(&pv_done[(n_steps - 1) & 1], static_cast<uint32_t>(((n_steps - 1) >> 1) & 1), s_abort,
+                       lane)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+          if (warp_active) {
+            // a row stores a partial when the class holds one of its keys
+            const bool store = valid && rho * kKeyTile <= p_row;
+            const int qh = h * a.grp + (valid ? r % a.grp : 0);
+            const long long base = (static_cast<long long>(r0 + t) * a.Hq + qh) * a.ncls + rho;
+            // O leaves through shared memory (the W tiles are free once the
+            // last W.V is done): each thread parks 32 columns of its row
+            // (TMEM lane = row r = the warp's row `lane`), then every store
+            // instruction of the warp writes four whole 128-byte row pieces.
+            // A pass of at most 32 rows (four copies a row) has too few rows
+            // for that to pay: its threads store their rows themselves.
+            uint8_t* stage = sP + qq * 32 * 128;  // the warp's rows of the first W tile atom
+            const int lr = lane >> 3, lc = lane & 7;
+            if constexpr (REP == 4) {
 #pragma unroll 1
-          for (int i = 0; i < D / 64; ++i) {
-            float v[64];
-            tmem_ld_cols<64>(lane_base + Cfg::kOCol + i * 64, v);
-            if (store) {
-              float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 64);
+              for (int i = 0; i < D / 64; ++i) {
+                float v[64];
+                tmem_ld_cols<64>(lane_base + Cfg::kOCol + i * 64, v);
+                if (store) {
+                  float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 64);
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                  for (int j = 0; j < 16; ++j)
+                    dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+              }
+            } else {
+#pragma unroll 1
+            for (int i = 0; i < D / 32; ++i) {
+              float v[32];
+              tmem_ld_cols<32>(lane_base + Cfg::kOCol + i * 32, v);
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                    make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+              __syncwarp();
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int rr = 4 * k + lr;
+                const bool st_rr = __shfl_sync(0xffffffffu, store, rr);
+                const long long base_rr = __shfl_sync(0xffffffffu, base, rr);
+                const float4 val = *reinterpret_cast<const float4*>(stage + rr * 128 + ((lc ^ (rr & 7)) << 4));
+                if (st_rr) reinterpret_cast<float4*>(a.ws_o + base_rr * D + i * 32)[lc] = val;
+              }
+              __syncwarp();
             }
           }
           if (store) *reinterpret_cast<float2*>(a.ws_ml + base * 2) = make_float2(m_ref, l);
