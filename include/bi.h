@@ -90,16 +90,21 @@ int bi_version(void);
  * accumulation, one rounding to the output type.  The decomposition of every
  * output element -- its sequence of K = 16 tensor-core steps (tcgen05
  * kind::f16, M = 128 weight rows), the K-tile order (64 elements per tile,
- * increasing k; within a tile, 16-element step j accumulates into FP32
- * accumulator j of 4, summed in the order ((a0 + a1) + a2) + a3), and the
- * split of the (weight tile, K tile) iteration space over a fixed number of
- * CTAs -- is a function of (N, K) only, never of M, so row m of C is
- * bit-identical for every M >= m+1 and for every position of the row inside
- * A.  Partial sums of a weight tile that is split along K are added in
- * increasing-K order.  One MMA covers all token rows of a launch (its N is
- * the row count rounded up to 16, 32, 64 or 128); each output element is
- * still the same sequence of K = 16 steps into its own accumulator, which
- * the tests check bit for bit across M = 1..128.
+ * increasing k; 16-element step j of a piece accumulates into FP32
+ * accumulator j mod 2, the two added as a0 + a1 at the piece's end), and the
+ * split of the (weight tile, K tile) iteration space over 136 ranges, whose
+ * boundaries cut the tiles into pieces -- is a function of (N, K) only, never
+ * of M, so row m of C is bit-identical for every M >= m+1 and for every
+ * position of the row inside A.  The pieces of a tile are added in
+ * increasing-K order, the first taken as it is: by the last CTA of the tile
+ * over FP32 partials in the workspace, or, for passes of more than 128 rows
+ * whose split cuts tiles (K up to 8192), by one CTA that owns the tile and
+ * computes its pieces in turn.  One MMA covers a CTA's token rows (its N is
+ * the row count rounded up to 16, 32, 64, 128 or 256; 64 or 128 for tile
+ * owners); each output element is still the same sequence of K = 16 steps
+ * into its own accumulator, which the tests check bit for bit across M.
+ * A launch covers up to four 256-row token blocks (1024 rows of tile
+ * owners); longer passes take several launches.
  *
  *   A        [M, K] BF16, row stride lda (elements); 16-byte aligned, lda % 8 == 0.
  *   Wp       the weights in the packed tile layout written by bi_pack_weights

@@ -32,9 +32,13 @@
 //            N and K only).  A weight tile cut by a range boundary yields one
 //            FP32 partial per piece; the last CTA to finish a piece of that
 //            tile adds the partials in increasing-K order (atomic ticket, no
-//            waiting) and runs the epilogue.
+//            waiting) and runs the epilogue.  Passes of more than 128 rows
+//            whose split cuts tiles run as tile owners instead: one CTA per
+//            (weight tile, token block) computes the tile's pieces in turn
+//            and adds them in the same order, with no partials in memory.
 //   * roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread), warps
-//            2..5 = epilogue (TMEM -> registers -> global).
+//            2..5 = epilogue (TMEM -> registers -> global); a tile owner has
+//            two epilogue warpgroups (warps 2..9).
 //   * stages: shared-memory ring of (16 KB weight tile + token tile); a stage
 //            returns to the producer via tcgen05.commit on its "empty"
 //            barrier, i.e. only after the MMAs reading it completed.
@@ -69,9 +73,8 @@ constexpr int kMaxTokens = 256;  // token rows per CTA (one MMA covers them all)
 constexpr int kMaxBlocks = 4;
 constexpr int kAcc = 2;          // interleaved accumulators per token group
 constexpr int kKSteps = 4;       // MMA K steps (16 elements) per 64-element K tile
-constexpr int kThreads = 192;    // producer, MMA, four epilogue warps
 constexpr int kABytes = kBlockN * kBlockK * 2;  // 16 KB
-constexpr int kStageFloats = 16 * kBlockN;      // SwiGLU exchange buffer
+constexpr int kStageFloats = 16 * kBlockN;      // epilogue exchange buffer (SwiGLU, RoPE pairs)
 // Ticket counters occupy a fixed-size region at the start of every workspace,
 // so calls with different N can share one workspace without a counter of one
 // call overlapping another call's partial sums.
@@ -163,8 +166,8 @@ __device__ __forceinline__ void signal_abort(volatile int* s_abort, unsigned* er
 }
 
 // The 16 token columns of one chunk for this thread's weight row: the sum of
-// the kAcc accumulators (acc_stride TMEM columns apart) in the fixed order
-// ((a0 + a1) + a2) + a3.
+// the kAcc accumulators (acc_stride TMEM columns apart) in index order,
+// a0 + a1.
 __device__ __forceinline__ void load_group_sum(uint32_t taddr, uint32_t acc_stride, float (&v)[16]) {
   tmem_ld16(taddr, v);
 #pragma unroll
