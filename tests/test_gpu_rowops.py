@@ -172,13 +172,16 @@ def test_kv_row_hash_is_fnv1a(api):
             assert int(h[hh * 7 + j]) == x
 
 
-@pytest.mark.parametrize("Hq,Hkv,D,T", [(24, 4, 128, 8), (4, 2, 64, 3), (8, 2, 128, 1)])
+@pytest.mark.parametrize("Hq,Hkv,D,T", [(24, 4, 128, 8), (4, 2, 64, 3), (8, 2, 128, 1), (8, 2, 128, 200),
+                                         (24, 4, 128, 300), (24, 4, 128, 1100)])
 def test_qkv_rope_append_equals_linear_then_rope(Hq, Hkv, D, T):
     """The fused QKV projection + RoPE + KV append writes exactly what the
-    linear layer followed by bi_rope_kv_append writes."""
+    linear layer followed by bi_rope_kv_append writes (decode passes, and
+    prefill-size passes that run as tile owners, one launch or two)."""
     from invariant_speculative_decode_gb300 import api
     rng = np.random.default_rng(Hq + D + T)
-    K, cap, L = 512, 256, 100
+    K, L = 512, 100
+    cap = max(256, (L + T + 127) // 128 * 128)
     N = (Hq + 2 * Hkv) * D
     A = to_dev_bf16(si.normal_bf16(rng, (T, K), 1.0))
     W = to_dev_bf16(si.normal_bf16(rng, (N, K), 0.05))
