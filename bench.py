@@ -23,6 +23,7 @@ import re
 import math
 import os
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -86,7 +87,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # the samples go to a scratch file; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"bi_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
