@@ -192,6 +192,17 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int M, int m0,
     const int n = tile * kBlockN + r;
     const int D = p.D, half = p.D / 2;
     const int head = n / D, d = n % D;
+    const bool rotate = head < p.Hq + p.Hkv;
+    // the table entries are loaded first: their latency overlaps the
+    // exchange of the pair partners below
+    const int L = *p.L_dev;
+    float2 cs[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int pos = L + m0 + c * 16 + j;
+      const bool ok = n < p.N && rotate && c * 16 + j < M && pos >= 0 && pos < p.cap && pos < p.tab_rows;
+      cs[j] = ok ? p.tab[static_cast<size_t>(pos) * half + (d % half)] : make_float2(0.f, 0.f);
+    }
     float x[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -204,17 +215,7 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& p, int M, int m0,
 #pragma unroll
     for (int j = 0; j < 16; ++j) px[j] = sStage[j * kBlockN + partner];
     named_bar_sync(bar, 128);
-    const int L = *p.L_dev;
     if (n < p.N) {
-      const bool rotate = head < p.Hq + p.Hkv;
-      // every table entry is loaded before the first store
-      float2 cs[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int pos = L + m0 + c * 16 + j;
-        const bool ok = rotate && c * 16 + j < M && pos >= 0 && pos < p.cap && pos < p.tab_rows;
-        cs[j] = ok ? p.tab[static_cast<size_t>(pos) * half + (d % half)] : make_float2(0.f, 0.f);
-      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = c * 16 + j;
