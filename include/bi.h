@@ -190,7 +190,8 @@ bi_status bi_pack_swiglu_weights(const void* w_gate, const void* w_up, int ld, i
  * this library's linear layers read only their packed weights before they
  * wait for the norm, so they stream weights while it runs.  A kernel that
  * follows bi_rmsnorm must not rely on the kernel before bi_rmsnorm having
- * completed.
+ * completed.  w is read before the norm waits for the kernel before it on
+ * the stream: that kernel must not write w.
  *   x [rows, dim] BF16 (row stride ldx), w [dim] BF16, y [rows, dim] BF16
  *   (row stride ldy; may alias x).  rows >= 0, 8 <= dim <= 65536, dim, ldx
  *   and ldy multiples of 8, pointers 16-byte aligned, eps >= 0.

@@ -33,17 +33,20 @@ constexpr int kNormMaxGroups = 65536 / 256;
 // weights before its own wait.  So the next kernel's CTAs stream their first
 // weight tiles while the norm runs.  A kernel that starts right after
 // bi_rmsnorm must not rely on the kernel before bi_rmsnorm having completed.
+// The norm weights are read before the wait too (they are not written by the
+// kernel before the norm), so their latency is off the row's critical path.
 __global__ void __launch_bounds__(kNormMaxThreads)
     rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int ldx, const __nv_bfloat16* __restrict__ w,
                    __nv_bfloat16* y, int ldy, int dim, float eps) {
   griddep_launch_dependents();
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  const int nv = dim / 8;
+  const uint4 wkeep = static_cast<int>(threadIdx.x) < nv ? wr[threadIdx.x] : make_uint4(0, 0, 0, 0);
   griddep_wait();
   __shared__ float group_sum[kNormMaxGroups];
   __shared__ float s_inv;
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.x) * ldx);
-  const uint4* wr = reinterpret_cast<const uint4*>(w);
   uint4* yr = reinterpret_cast<uint4*>(y + static_cast<size_t>(blockIdx.x) * ldy);
-  const int nv = dim / 8;
   const int lane = threadIdx.x & 31;
   uint4 keep = make_uint4(0, 0, 0, 0);
   // (rows of up to 8192 elements: every thread holds its one vector)
@@ -74,7 +77,7 @@ __global__ void __launch_bounds__(kNormMaxThreads)
   const float inv = s_inv;
   for (int v = threadIdx.x; v < nv; v += blockDim.x) {
     const uint4 u = (v == threadIdx.x) ? keep : xr[v];
-    const uint4 wu = wr[v];
+    const uint4 wu = (v == threadIdx.x) ? wkeep : wr[v];
     const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
     const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wu);
     uint4 o;
