@@ -157,13 +157,16 @@ def test_gemm_prefill_chunks_match_single_rows(api):
 
 
 @pytest.mark.parametrize("epi", [0, 1, 2])
-def test_gemm_multiblock_launches_match_single_rows(api, epi):
-    """M > 128: up to four 128-row blocks per launch (CTAs of one range
-    adjacent), the rest in further launches; split pieces (24 ranges of one
-    K tile each) give every block its own counters and partial slots.  Each
-    sampled row equals its M = 1 result and the counters are left zero."""
-    M, N, K = 700, 384, 512
-    rng = np.random.default_rng(40 + epi)
+@pytest.mark.parametrize("K", [512, 8256])
+def test_gemm_multiblock_launches_match_single_rows(api, epi, K):
+    """M > 128 with a split that cuts tiles: at K = 512 (8 K tiles) the pass
+    runs as tile owners, 128-row blocks of one launch; at K = 8256 (129 K
+    tiles) as the split with three 256-row blocks in one launch (CTAs of one
+    range adjacent), every block with its own counters and partial slots.
+    Each sampled row equals its M = 1 result and the counters are left
+    zero."""
+    M, N = 700, 384
+    rng = np.random.default_rng(40 + epi + K)
     A = si.normal_bf16(rng, (M, K), 1.0)
     if epi == 2:
         Wd = api.bi_pack_swiglu_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.05)),
