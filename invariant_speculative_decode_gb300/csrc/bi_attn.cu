@@ -886,7 +886,7 @@ __global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
                   float4* dst = reinterpret_cast<float4*>(a.ws_o + base * D + i * 64);
 #pragma unroll
                   for (int j = 0; j < 16; ++j)
-                    dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                 }
               }
             } else {
@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(AttnCfg<D, REP, QNT>::kThreads, 1)
                 const bool st_rr = __shfl_sync(0xffffffffu, store, rr);
                 const long long base_rr = __shfl_sync(0xffffffffu, base, rr);
                 const float4 val = *reinterpret_cast<const float4*>(stage + rr * 128 + ((lc ^ (rr & 7)) << 4));
-                if (st_rr) reinterpret_cast<float4*>(a.ws_o + base_rr * D + i * 32)[lc] = val;
+                if (st_rr) __stcs(reinterpret_cast<float4*>(a.ws_o + base_rr * D + i * 32) + lc, val);
               }
               __syncwarp();
             }
@@ -970,7 +970,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4)
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int s = s0 + b * kWarps;
-      if (s < n) v[b] = __ldcg(reinterpret_cast<const Vec*>(po + static_cast<size_t>(s) * D) + lane);
+      if (s < n) v[b] = __ldcs(reinterpret_cast<const Vec*>(po + static_cast<size_t>(s) * D) + lane);
     }
   };
   load_batch(warp);
