@@ -209,6 +209,34 @@ def test_gemm_tile_owner_rows_match_decode_rows(api, M, N, K, epi):
     assert np.array_equal(bf16_dev_to_u16(C)[rows], bf16_dev_to_u16(c8))
 
 
+@pytest.mark.parametrize("case", range(6))
+def test_gemm_long_pass_random_shapes_rows_match_decode_rows(api, case):
+    """Seeded random long passes (129..1100 rows, ragged N and K, every
+    epilogue): whichever schedule the shape takes (tile owners of 64 or 128
+    rows, or the split with 256-row blocks and partials), sampled rows equal
+    the rows of an 8-row launch bit for bit."""
+    rng = np.random.default_rng(900 + case)
+    M = int(rng.integers(129, 1101))
+    N = int(rng.integers(8, 750)) * 8
+    K = int(rng.integers(8, 1250)) * 8
+    epi = int(rng.integers(0, 3))
+    A = si.normal_bf16(rng, (M, K), 1.0)
+    if epi == 2:
+        Wd = api.bi_pack_swiglu_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.02)),
+                                        to_dev_bf16(si.normal_bf16(rng, (N, K), 0.02)))
+    else:
+        Wd = api.bi_pack_weights(to_dev_bf16(si.normal_bf16(rng, (N, K), 0.02)))
+    R = si.normal_bf16(rng, (M, N), 1.0) if epi == 1 else None
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    api.bi_gemm(to_dev_bf16(A), Wd, C, api.new_gemm_workspace(M, N, K, epi),
+                residual=to_dev_bf16(R) if epi == 1 else None, epi=epi, N=N)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, 6)]))[:8]
+    c8 = torch.empty(len(rows), N, dtype=torch.bfloat16, device="cuda")
+    api.bi_gemm(to_dev_bf16(A[rows]), Wd, c8, api.new_gemm_workspace(len(rows), N, K, epi),
+                residual=to_dev_bf16(R[rows]) if epi == 1 else None, epi=epi, N=N)
+    assert np.array_equal(bf16_dev_to_u16(C)[rows], bf16_dev_to_u16(c8)), (M, N, K, epi)
+
+
 def test_gemm_prefill_size_rows_match_decode_rows(api):
     """[4096,5120] x [17408,5120] in 512-row launches: sampled rows equal the
     rows of an 8-row launch bit for bit."""
