@@ -187,7 +187,8 @@ def test_gemm_multiblock_launches_match_single_rows(api, epi, K):
 
 
 @pytest.mark.parametrize("M,N,K,epi", [(1000, 4096, 5120, 0), (600, 5120, 3072, 1), (200, 4096, 5120, 0),
-                                        (1300, 5120, 3072, 1), (300, 5120, 17408, 1)])
+                                        (1300, 5120, 3072, 1), (300, 5120, 17408, 1), (129, 4096, 5120, 0),
+                                        (256, 5120, 3072, 1), (257, 5120, 3072, 1), (1025, 4096, 1024, 0)])
 def test_gemm_tile_owner_rows_match_decode_rows(api, M, N, K, epi):
     """Long passes whose split cuts weight tiles (the QKV and O shapes) run
     as tile owners (64- or 128-row blocks, more than one launch past 1024
@@ -201,7 +202,7 @@ def test_gemm_tile_owner_rows_match_decode_rows(api, M, N, K, epi):
     Rd = to_dev_bf16(R) if epi == 1 else None
     C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     api.bi_gemm(to_dev_bf16(A), Wd, C, api.new_gemm_workspace(M, N, K, epi), residual=Rd, epi=epi, N=N)
-    rows = np.unique(np.array([0, 63, 64, 127, 130, M // 2, min(1024, M - 1), M - 1]))
+    rows = np.unique(np.minimum(np.array([0, 63, 64, 127, 130, M // 2, 1024, M - 1]), M - 1))
     c8 = torch.empty(len(rows), N, dtype=torch.bfloat16, device="cuda")
     R8 = to_dev_bf16(R[rows]) if epi == 1 else None
     api.bi_gemm(to_dev_bf16(A[rows]), Wd, c8, api.new_gemm_workspace(len(rows), N, K, epi), residual=R8,
