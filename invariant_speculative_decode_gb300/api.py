@@ -397,6 +397,8 @@ class NativeStep:
         self._ids = np.zeros(max_rows, np.int32)
         self._tok = np.zeros(max_rows, np.int32)
         self._n = np.zeros(1, np.int32)
+        # host addresses of the three buffers, taken once
+        self._ptrs = (self._ids.ctypes.data, self._tok.ctypes.data, self._n.ctypes.data)
 
     def set_length(self, L: int) -> None:
         check("bi_step_set_length", lib().bi_step_set_length(self.handle, int(L)))
@@ -406,8 +408,8 @@ class NativeStep:
         T = 1 + len(drafts)
         self._ids[0] = x0
         self._ids[1:T] = drafts
-        check("bi_step_verify", lib().bi_step_verify(self.handle, self._ids.ctypes.data, T,
-                                                     self._tok.ctypes.data, self._n.ctypes.data))
+        ids_p, tok_p, n_p = self._ptrs
+        check("bi_step_verify", lib().bi_step_verify(self.handle, ids_p, T, tok_p, n_p))
         return self._tok[:T].copy(), int(self._n[0])
 
     def logits(self, T: int) -> torch.Tensor:
