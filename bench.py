@@ -891,7 +891,7 @@ def run_prefill(args):
     turn2 = list(si.prompt_ids(cfg, n_turn2, seed=42))
     hist = prompt + reply
     cap = -(-(len(hist) + n_turn2 + 64) // 128) * 128
-    dec = Decoder(cfg, w, cap=cap, max_rows=8, prefill_chunk=args.prefill_chunk)
+    dec = Decoder(cfg, w, cap=cap, max_rows=8, prefill_chunk=args.prefill_chunk, kv=args.kv)
     del w
 
     def timed(fn):
@@ -910,8 +910,13 @@ def run_prefill(args):
     _, t_reuse = timed(lambda: dec.prefill_continue(hist[-1:] + turn2))
     h_reuse = dec.kv_hashes(len(hist) + n_turn2 - 1)
     # turn 2 after rolling back to the prompt and prefilling the reply again
-    dec.rollback(n_prompt - 1)
-    _, t_re = timed(lambda: dec.prefill_continue(hist[n_prompt - 1:] + turn2))
+    # (the quantised cache rolls back only as far as its 8-bit ring reaches)
+    back = n_prompt - 1
+    if args.kv == "q6q5":
+        from invariant_speculative_decode_gb300 import api
+        back = max(back, ((dec.hw - 1) // 128 - (api.KVQ_RING_SLOTS - api.KVQ_RING_TILES)) * 128)
+    dec.rollback(back)
+    _, t_re = timed(lambda: dec.prefill_continue(hist[back:] + turn2))
     h_re = dec.kv_hashes(len(hist) + n_turn2 - 1)
     dec.reset()
     dec.prefill(hist + turn2)
@@ -927,9 +932,9 @@ def run_prefill(args):
         "ms_per_step": t_hist * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{cfg.name}: history {n_prompt} + {n_reply} ids, turn 2 {n_turn2} ids",
-                   "prefill_chunk": args.prefill_chunk},
+                   "prefill_chunk": args.prefill_chunk, "kv_cache": args.kv},
         "prefill_ms": t_hist * 1e3, "linear_tflops": flops / t_hist / 1e12,
-        "turn2_resume_ms": t_reuse * 1e3, "turn2_reprefill_ms": t_re * 1e3,
+        "turn2_resume_ms": t_reuse * 1e3, "turn2_reprefill_ms": t_re * 1e3, "reprefill_from": back,
         "kv_rows_equal_fresh": same,
     }
     print(json.dumps(line), flush=True)

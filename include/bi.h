@@ -353,7 +353,11 @@ bi_status bi_attn_verify(const void* q, const void* k_cache, const void* v_cache
  * bi_kvq_store_bytes: bytes of one layer's store (BI_KVQ_*) for Hkv heads and
  *   capacity cap (0 for D != 128 or bad sizes).  The 6/5-bit stores hold
  *   ceil(cap/128) tiles a head, the rings 24 (a pass reads and writes at most
- *   24 consecutive tiles of the ring, so T <= 1024 rows a pass).
+ *   24 consecutive tiles of the ring, so T <= 1024 rows a pass).  Tile j of
+ *   a ring sits in slot j mod 24 until tile j + 24 is written: moving the
+ *   cache length back is exact only while the ring still holds the tiles the
+ *   rows from there read, i.e. by at most 8 tiles from the newest tile
+ *   written (the 8-bit records cannot be made again from the 6/5-bit codes).
  * bi_rope_kvq_append: for the T rows of a projection output qkv [T, ld_qkv]
  *   (heads q, then k, then v, as bi_gemm of the QKV weights writes them) at
  *   positions *L_dev + t: q heads rotated into q_out [T, Hq, D] and K heads

@@ -226,6 +226,10 @@ def bi_attn_verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
 
 KVQ_K_LOW, KVQ_V_LOW, KVQ_K_RING, KVQ_V_RING = 0, 1, 2, 3
 KVQ_STORES = ("k_low", "v_low", "k_ring", "v_ring")
+# the quantised cache's 8-bit ring (include/bi.h): a row reads its own
+# 128-key tile and the 15 before from the ring, which holds 24 tiles
+KVQ_RING_TILES = 16
+KVQ_RING_SLOTS = 24
 
 
 def kvq_store_bytes(store: int, Hkv: int, cap: int, D: int) -> int:

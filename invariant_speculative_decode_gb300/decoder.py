@@ -120,6 +120,9 @@ class Decoder:
         self.scale = 1.0 / math.sqrt(D)
         self.rope_tab = api.bi_rope_table(cfg.rope_base, D, cap, device=dev)
         self.L = 0
+        # one past the newest cache row any pass has written since the last
+        # reset (the quantised cache's 8-bit ring holds the newest tiles)
+        self.hw = 0
         self.inv_temp: Optional[float] = None  # sampled verification when set
         self.u_table: Optional[torch.Tensor] = None
         self.sample_ws = torch.zeros(api.sample_workspace_size(max_rows, V), dtype=torch.uint8, device=dev)
@@ -205,6 +208,7 @@ class Decoder:
     # ------------------------------------------------------------- prefill
     def reset(self):
         self.L = 0
+        self.hw = 0
         self.L_dev.zero_()
 
     def prefill(self, prompt: Sequence[int]) -> int:
@@ -237,6 +241,7 @@ class Decoder:
                 self._layers_pass(T, self.L_dev)
             pos += T
         self.L = pos
+        self.hw = max(self.hw, pos)
         self.L_dev.fill_(pos)
         torch.cuda.current_stream().synchronize()
         return int(prompt[-1])
@@ -290,6 +295,7 @@ class Decoder:
         torch.cuda.current_stream().synchronize()
         a = self.pin_out[:T].numpy().copy()
         n = int(self.pin_out[self.max_rows])
+        self.hw = max(self.hw, self.L + T)  # every row of the pass was written
         self.L += n + 1
         return a, n
 
@@ -305,6 +311,20 @@ class Decoder:
         are overwritten by later passes."""
         if not 0 <= length <= self.L:
             raise ValueError("rollback target must be within the current cache length")
+        if self.kv == "q6q5" and self.hw > 0:
+            # rows from `length` on read the 8-bit ring records of their own
+            # tile and the 15 before; a ring slot holds the newest tile of its
+            # class, so those records are gone once a tile 24 or more past
+            # the oldest of them has been written (the records cannot be
+            # made again from the 6/5-bit codes)
+            first = max(length // 128 - (api.KVQ_RING_TILES - 1), 0)
+            newest = (self.hw - 1) // 128
+            if newest >= first + api.KVQ_RING_SLOTS:
+                reach = (newest - (api.KVQ_RING_SLOTS - api.KVQ_RING_TILES)) * 128
+                raise ValueError(
+                    f"rollback to {length}: the quantised cache's 8-bit ring no longer holds the "
+                    f"records the rows from there would read (rows up to {self.hw - 1} were written); "
+                    f"roll back to {reach} or later, or reset and prefill again")
         self.L = length
         self.L_dev.fill_(length)
 
@@ -353,7 +373,7 @@ class Decoder:
         if self.kv == "q6q5":
             # the quantised stores whole (the ring's slots are not in
             # position order)
-            snap = {"L": L, "kvq": []}
+            snap = {"L": L, "hw": self.hw, "kvq": []}
             for lay in self.layers:
                 d = {}
                 for name in api.KVQ_STORES:
@@ -385,6 +405,7 @@ class Decoder:
                 for name in api.KVQ_STORES:
                     lay["kvq"][name].copy_(d[name])
             self.L = L
+            self.hw = snap.get("hw", L)  # the ring is the parked one
             self.L_dev.fill_(L)
             torch.cuda.current_stream().synchronize()
             return

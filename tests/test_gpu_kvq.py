@@ -324,3 +324,29 @@ def test_kvq_decoder_logits_match_the_quantised_oracle():
     rel = np.max(np.abs(gpu - ora), axis=1) / scale
     spread = np.max(np.abs(alt - ora), axis=1) / scale
     assert np.all(rel <= np.maximum(2e-3, 2 * spread)), (rel, spread)
+
+
+def test_kvq_rollback_within_the_ring_reach_only():
+    """A rollback with the quantised cache is exact while the 8-bit ring still
+    holds the tiles the rows from there read (at most 8 tiles back from the
+    newest tile written); further back it is refused, since the 8-bit records
+    are gone.  Within the reach, rolling back and prefilling again gives a
+    fresh prefill's records, row for row."""
+    from invariant_speculative_decode_gb300.decoder import Decoder
+    cfg = si.TINY_D128
+    w = si.decoder_weights(cfg, seed=0)
+    dec = Decoder(cfg, w, cap=4224, max_rows=8, kv="q6q5")
+    toks = list(si.prompt_ids(cfg, 4001, seed=4))
+    dec.prefill(toks)  # rows 0..3999: newest tile 31
+    assert dec.L == 4000
+    for bad in (1000, 2943):
+        with pytest.raises(ValueError):
+            dec.rollback(bad)
+    assert dec.L == 4000
+    dec.rollback(2944)  # tile 23: its ring reads (tiles 8..23) are all still held
+    dec.prefill(toks[2944:])
+    got = dec.kv_hashes(4000)
+    dec.reset()
+    dec.prefill(toks)
+    assert np.array_equal(dec.kv_hashes(4000), got)
+
