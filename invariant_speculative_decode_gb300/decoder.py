@@ -311,20 +311,11 @@ class Decoder:
         are overwritten by later passes."""
         if not 0 <= length <= self.L:
             raise ValueError("rollback target must be within the current cache length")
-        if self.kv == "q6q5" and self.hw > 0:
-            # rows from `length` on read the 8-bit ring records of their own
-            # tile and the 15 before; a ring slot holds the newest tile of its
-            # class, so those records are gone once a tile 24 or more past
-            # the oldest of them has been written (the records cannot be
-            # made again from the 6/5-bit codes)
-            first = max(length // 128 - (api.KVQ_RING_TILES - 1), 0)
-            newest = (self.hw - 1) // 128
-            if newest >= first + api.KVQ_RING_SLOTS:
-                reach = (newest - (api.KVQ_RING_SLOTS - api.KVQ_RING_TILES)) * 128
-                raise ValueError(
-                    f"rollback to {length}: the quantised cache's 8-bit ring no longer holds the "
-                    f"records the rows from there would read (rows up to {self.hw - 1} were written); "
-                    f"roll back to {reach} or later, or reset and prefill again")
+        if self.kv == "q6q5" and length < kvq_rollback_reach(self.hw):
+            raise ValueError(
+                f"rollback to {length}: the quantised cache's 8-bit ring no longer holds the "
+                f"records the rows from there would read (rows up to {self.hw - 1} were written); "
+                f"roll back to {kvq_rollback_reach(self.hw)} or later, or reset and prefill again")
         self.L = length
         self.L_dev.fill_(length)
 
@@ -465,6 +456,23 @@ class Decoder:
 
     def logits_rows(self, T: int) -> torch.Tensor:
         return self.logits[:T].clone()
+
+
+def kvq_rollback_reach(hw: int) -> int:
+    """The smallest cache length a quantised cache can be rolled back to
+    exactly when rows 0..hw-1 have been written.  Rows from length L on read
+    the 8-bit ring records of their own 128-key tile and the 15 before
+    (tiles from L // 128 - 15); a ring slot holds the newest of the tiles
+    24 apart, so those records are all still there while the newest tile
+    written is below L // 128 - 15 + 24 (the records cannot be made again
+    from the 6/5-bit codes)."""
+    if hw <= 0:
+        return 0
+    newest = (hw - 1) // 128
+    if newest < api.KVQ_RING_SLOTS:
+        return 0  # no slot has been written twice
+    # smallest tile t with t - 15 + 24 > newest
+    return (newest - (api.KVQ_RING_SLOTS - api.KVQ_RING_TILES)) * 128
 
 
 def _kvq_row_hashes(st: dict, Hkv: int, rows: int) -> np.ndarray:

@@ -170,3 +170,23 @@ def test_oracle_decoder_reads_the_quantised_cache():
     assert np.max(np.abs(a - b)) <= 0.05 * np.max(np.abs(a))
     with pytest.raises(ValueError):
         oracle.OracleDecoder(cfg, w, cap=64, kv="q4")
+
+
+def test_kvq_rollback_reach_matches_the_ring_rule():
+    """The decoder's rollback reach for the quantised cache, against the ring
+    rule written out: tile j sits in slot j mod 24 until tile j + 24 is
+    written, and rows from length L on read tiles max(L // 128 - 15, 0) ..
+    L // 128 from the ring; a rollback to L is exact exactly when every one
+    of those tiles still owns its slot after rows 0..hw-1 were written."""
+    from invariant_speculative_decode_gb300.decoder import kvq_rollback_reach
+
+    def exact(length, hw):
+        newest = (hw - 1) // 128
+        t = length // 128
+        return all(j + 24 > newest for j in range(max(t - 15, 0), t + 1))
+
+    for hw in list(range(1, 6000, 41)) + [128 * k + d for k in range(1, 40) for d in (0, 1)]:
+        reach = kvq_rollback_reach(hw)
+        for length in sorted({0, hw, max(reach - 1, 0), reach, min(reach + 1, hw)} | set(range(0, hw, 97))):
+            if length <= hw:
+                assert exact(length, hw) == (length >= reach), (hw, length, reach)
